@@ -1,0 +1,195 @@
+"""Seeded synthetic workloads for the sparse KV residency path.
+
+This module is the one piece shared by the CUDA path's tests/benchmark and the
+CPU oracle.  It only draws random numbers and lays out bytes; it holds none of
+the method's arithmetic (no selection, no lookup, no eviction, no dequant).
+
+Row bytes follow the Q8G64 MLA record described in "From 1M Total to 15+ x 1M
+Contexts: GLM-5.3 KV Cache Offloading", section "Separate historical capacity
+from the current working set": 512 B int8 latent, 16 B of scales (8 fp16, one
+per 64 latent bytes) and 128 B of RoPE data (64 bf16), 656 B in total, in that
+order.
+
+Recipes (every draw comes from ``numpy.random.default_rng`` keyed by a tuple
+that starts with the workload's seed and id):
+  * latent int8 uniform on [-127, 127];
+  * scales fp16(uniform[1e-3, 1e-2]);
+  * RoPE bf16 bit patterns: the upper 16 bits of float32 N(0, 1) draws;
+  * scores float32 N(0, 1), plus an optional recency term
+    ``amp * exp(-age / tau)`` (age = n - 1 - pos, computed in float64 and
+    added before the single cast to float32);
+  * carry-over: from step 1 on, ``carry`` entries of the previous step's
+    selection, drawn uniformly without replacement, get ``+carry_boost``
+    (a float32 add).  The draw is an index set into the previous selection,
+    so each side applies it to its own previous selection.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+ROW_BYTES = 656
+LATENT_BYTES = 512
+SCALE_BYTES = 16
+ROPE_BYTES = 128
+ROW_CHUNK = 1 << 16          # rows are drawn in chunks of this many positions
+
+# stream tags, so that the different draws of one workload never share a key
+_TAG_ROWS = 0x524F5753
+_TAG_SCORES = 0x53434F52
+_TAG_CARRY = 0x43415259
+_TAG_SESSION = 0x53455353
+
+
+def _rng(*key: int) -> np.random.Generator:
+    return np.random.default_rng([int(k) & 0xFFFFFFFF for k in key])
+
+
+@dataclass(frozen=True)
+class Workload:
+    """Shape of one synthetic decode workload.
+
+    ``select_every`` = 4 means only layers 0, 4, 8, ... compute a selection and
+    the next three layers reuse it (selection reuse by subsequent layers).
+    """
+    name: str
+    cfg_id: int
+    seed: int
+    layers: int
+    n0: int                  # history rows present before step 0
+    hot_rows: int
+    k: int
+    steps: int
+    appends_per_step: int
+    select_every: int = 1
+    carry: int = 0
+    carry_boost: float = 16.0
+    recency_amp: float = 0.0
+    recency_tau: float = 4096.0
+    bf16: bool = False
+    extra: dict = field(default_factory=dict, compare=False, hash=False)
+
+    @property
+    def history_cap(self) -> int:
+        return self.n0 + self.steps * self.appends_per_step
+
+    def n_at(self, step: int) -> int:
+        """History length seen by the selection of ``step`` (appends come first)."""
+        return self.n0 + (step + 1) * self.appends_per_step
+
+    def selecting_layers(self) -> list[int]:
+        return [l for l in range(self.layers) if l % self.select_every == 0]
+
+    def source_layer(self, layer: int) -> int:
+        return layer - layer % self.select_every
+
+    def scaled(self, **kw) -> "Workload":
+        d = dict(self.__dict__)
+        d.update(kw)
+        return Workload(**d)
+
+
+TINY = Workload("tiny", 0, 1, layers=1, n0=4096, hot_rows=1024, k=256, steps=16,
+                appends_per_step=0, carry=128)
+K50 = Workload("50k_single_layer", 1, 2, layers=1, n0=50_023, hot_rows=32_768, k=2048,
+               steps=1024, appends_per_step=1, carry=1229, recency_amp=2.0)
+STACK = Workload("50k_full_stack", 2, 3, layers=78, n0=50_023, hot_rows=32_768, k=2048,
+                 steps=256, appends_per_step=1, select_every=4, carry=1229, recency_amp=2.0)
+M1 = Workload("1m_cold_stress", 3, 4, layers=8, n0=1_048_576, hot_rows=32_768, k=2048,
+              steps=64, appends_per_step=0, bf16=True)
+
+WORKLOADS = {w.name: w for w in (TINY, K50, STACK, M1)}
+
+
+def rows(w: Workload, layer: int, start: int, count: int) -> np.ndarray:
+    """Rows for history positions [start, start+count) of ``layer`` (uint8 [count, 656]).
+
+    A position's bytes depend only on (workload, layer, position).
+    """
+    out = np.empty((count, ROW_BYTES), np.uint8)
+    pos = start
+    end = start + count
+    while pos < end:
+        chunk = pos // ROW_CHUNK
+        c0 = chunk * ROW_CHUNK
+        block = _row_chunk(w, layer, chunk)
+        lo = pos - c0
+        hi = min(end - c0, ROW_CHUNK)
+        out[pos - start:pos - start + (hi - lo)] = block[lo:hi]
+        pos = c0 + hi
+    return out
+
+
+def _row_chunk(w: Workload, layer: int, chunk: int) -> np.ndarray:
+    g = _rng(w.seed, w.cfg_id, layer, _TAG_ROWS, chunk)
+    m = ROW_CHUNK
+    block = np.empty((m, ROW_BYTES), np.uint8)
+    block[:, :LATENT_BYTES] = g.integers(-127, 128, size=(m, LATENT_BYTES), dtype=np.int8).view(np.uint8)
+    sc = g.uniform(1e-3, 1e-2, size=(m, 8)).astype("<f2")
+    block[:, LATENT_BYTES:LATENT_BYTES + SCALE_BYTES] = sc.view(np.uint8)
+    rope = (g.standard_normal((m, 64), dtype=np.float32).view(np.uint32) >> 16).astype("<u2")
+    block[:, LATENT_BYTES + SCALE_BYTES:] = rope.view(np.uint8)
+    return block
+
+
+def base_scores(w: Workload, layer: int, step: int, n: int | None = None) -> np.ndarray:
+    """Indexer-score stand-in for ``layer`` at ``step`` before the carry boost (float32 [n])."""
+    if n is None:
+        n = w.n_at(step)
+    g = _rng(w.seed, w.cfg_id, layer, _TAG_SCORES, step)
+    z = g.standard_normal(n, dtype=np.float64)
+    if w.recency_amp:
+        age = (n - 1 - np.arange(n, dtype=np.float64))
+        z = z + w.recency_amp * np.exp(-age / w.recency_tau)
+    return z.astype(np.float32)
+
+
+def carry_draw(w: Workload, layer: int, step: int) -> np.ndarray:
+    """Indices into the previous step's selection that get the carry boost (int64)."""
+    if step == 0 or w.carry == 0:
+        return np.zeros(0, np.int64)
+    g = _rng(w.seed, w.cfg_id, layer, _TAG_CARRY, step)
+    return np.sort(g.choice(w.k, size=w.carry, replace=False)).astype(np.int64)
+
+
+def apply_carry(scores: np.ndarray, prev_sel: np.ndarray | None, draw: np.ndarray,
+                boost: float) -> np.ndarray:
+    """scores with ``+boost`` (float32 add) at ``prev_sel[draw]``."""
+    s = np.array(scores, dtype=np.float32, copy=True)
+    if prev_sel is not None and len(draw):
+        s[np.asarray(prev_sel, np.int64)[draw]] += np.float32(boost)
+    return s
+
+
+def random_scores(seed: int, n: int, kind: str = "normal") -> np.ndarray:
+    """Small-case score vectors for edge-case tests."""
+    g = _rng(seed, n, 0x45444745)
+    if kind == "normal":
+        return g.standard_normal(n, dtype=np.float32)
+    if kind == "ties":          # few distinct values, many equal keys
+        return g.integers(-3, 4, size=n).astype(np.float32)
+    if kind == "special":       # +-0, +-inf, NaN, denormals mixed in
+        s = g.standard_normal(n, dtype=np.float32)
+        pick = g.integers(0, 7, size=n)
+        specials = np.array([0.0, -0.0, np.inf, -np.inf, np.nan, 1e-45, -1e-45], np.float32)
+        mask = g.random(n) < 0.3
+        s[mask] = specials[pick[mask]]
+        return s
+    raise ValueError(kind)
+
+
+def random_idx(seed: int, n: int, k: int, dup_frac: float = 0.0, invalid: int = 0) -> np.ndarray:
+    """Selection vectors for resolve tests: arbitrary order, optional duplicates and bad entries."""
+    g = _rng(seed, n, k, 0x49445820)
+    base = g.choice(n, size=k, replace=False) if k <= n else g.integers(0, n, size=k)
+    base = base.astype(np.int32)
+    ndup = int(round(dup_frac * k))
+    if ndup:
+        where = g.choice(k, size=ndup, replace=False)
+        base[where] = base[g.integers(0, k, size=ndup)]
+    if invalid:
+        where = g.choice(k, size=invalid, replace=False)
+        bad = np.array([-1, n, n + 7, -(2 ** 31), 2 ** 31 - 1], np.int64)
+        base[where] = bad[g.integers(0, len(bad), size=invalid)].astype(np.int32)
+    return base

@@ -1,0 +1,494 @@
+#!/usr/bin/env python
+"""Throughput of the sparse KV residency hot path on GB300.
+
+A step is one decode step of the workload: for every layer, append the new
+row to the host history, select the top-K positions from the indexer scores
+(on selecting layers), then resolve + gather the K rows (hits from the HBM
+hot cache, misses from pinned host memory, LRU fills) into the contiguous
+attention input.  Metric: selected rows resolved+gathered per second.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kvo|reference]
+                    [--workload 50k_single_layer|50k_full_stack|1m_cold_stress|tiny]
+
+Timing: inputs (history, scores, new rows) are resident before the timed
+region; a 1 GiB memset flushes L2 between steps; each step is bracketed by
+CUDA events on the launching stream and every kernel of the path by its own
+event pair.  Under torchrun each rank runs an independent replica (the path
+shards by layer/session with no exchange) and rank 0 prints one JSON line
+with the max step time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from synth import workloads as W  # noqa: E402
+
+METRIC = "selected KV rows resolved+gathered/s; GB/s vs HBM and host-link roofline"
+ROW = 656
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ----------------------------------------------------------------- helpers
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.05)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def algorithmic_bytes(w: W.Workload, n_avg: float, stats_delta: dict, resolve_launches: int,
+                      select_launches: int):
+    """Bytes the method must move per launch (reads + writes), from the
+    counters of the timed launches.
+
+    select:  4n (scores) + 4k (positions).
+    resolve: 4k (positions) + 4k (pos2slot lookups) + 4*hits (last_use stamps)
+             + 656*hits (hot rows) + R_out*k (output) + 656*fills (victim rows)
+             + 16*fills (map and stamp updates) + 4*hot_rows (LRU scan);
+             host link: 656 per miss occurrence.
+    """
+    k = w.k
+    r_out = ROW + (2 * 576 if w.bf16 else 0)
+    L = max(resolve_launches, 1)
+    hits = stats_delta["hits"] / L
+    fills = stats_delta["unique_misses"] / L
+    misses = stats_delta["misses"] / L
+    resolve_hbm = 8 * k + 4 * hits + ROW * hits + r_out * k + (ROW + 16) * fills + 4 * w.hot_rows
+    select_hbm = 4 * n_avg + 4 * k
+    return {"resolve_hbm": resolve_hbm, "resolve_host": ROW * misses, "select_hbm": select_hbm,
+            "append_host": ROW * w.appends_per_step, "hits": hits, "misses": misses, "fills": fills}
+
+
+# ------------------------------------------------------------- GPU arm
+class GpuWorkload:
+    """Device-resident inputs and a context for one replica of a workload."""
+
+    def __init__(self, w: W.Workload, layer_base: int, steps: int, host_inputs: bool = False):
+        import torch
+        from gather_radix_top_gb300 import kvo
+        self.torch, self.kvo, self.w = torch, kvo, w
+        self.steps = steps
+        self.host_inputs = host_inputs
+        self.ctx = kvo.Context(w.layers, w.history_cap, w.hot_rows)
+        self.sel = w.selecting_layers()
+        for l in range(w.layers):
+            self.ctx.append_rows(l, W.rows(w, layer_base + l, 0, w.n0))
+        dev = "cuda"
+        a = w.appends_per_step
+        if a:
+            new = np.stack([W.rows(w, layer_base + l, w.n0, steps * a) for l in range(w.layers)])
+            self.new_rows_host = torch.from_numpy(new).pin_memory() if host_inputs else None
+            self.new_rows = None if host_inputs else torch.from_numpy(new).to(dev)
+        nmax = w.n_at(steps - 1)
+        self.scores = {}
+        self.draws = {}
+        for l in self.sel:
+            base = np.zeros((steps, nmax), np.float32)
+            for s in range(steps):
+                n = w.n_at(s)
+                base[s, :n] = W.base_scores(w, layer_base + l, s, n)
+            t = torch.from_numpy(base)
+            self.scores[l] = t.pin_memory() if host_inputs else t.to(dev)
+            if w.carry:
+                d = np.stack([W.carry_draw(w, layer_base + l, s) if s else np.zeros(w.carry, np.int64)
+                              for s in range(steps)])
+                self.draws[l] = torch.from_numpy(d).to(dev)
+        self.stage = {l: torch.empty(nmax, dtype=torch.float32, device=dev) for l in self.sel}
+        self.idx = {l: [torch.zeros(w.k, dtype=torch.int32, device=dev) for _ in range(2)] for l in self.sel}
+        self.out_rows = torch.empty((w.k, ROW), dtype=torch.uint8, device=dev)
+        self.out_bf16 = torch.empty((w.k, 576), dtype=torch.bfloat16, device=dev) if w.bf16 else None
+        self.out_host = torch.empty((w.k, ROW), dtype=torch.uint8).pin_memory() if host_inputs else None
+        self.idx_hist = torch.zeros((steps, w.k), dtype=torch.int32, device=dev)
+        self.launches = 0
+
+    def scores_for(self, l, s):
+        """The step's scores on the device with the carry boost applied (not timed)."""
+        torch, w = self.torch, self.w
+        n = w.n_at(s)
+        if self.host_inputs:
+            sc = self.stage[l][:n]
+            sc.copy_(self.scores[l][s, :n], non_blocking=True)
+        else:
+            sc = self.scores[l][s, :n]
+        if w.carry and s > 0:
+            prev = self.idx[l][(s - 1) & 1]
+            pos = prev.index_select(0, self.draws[l][s]).long()
+            sc.index_add_(0, pos, torch.full((w.carry,), w.carry_boost, dtype=torch.float32, device="cuda"))
+        return sc
+
+    def step(self, s, ev=None, kev=None):
+        """One decode step over all layers.  ev: (start, end) events; kev: dict
+        kind -> list of (start, end) event pairs appended per launch."""
+        torch, w, ctx = self.torch, self.w, self.ctx
+        sc = {l: self.scores_for(l, s) for l in self.sel}
+
+        def rec(kind, fn):
+            if kev is None:
+                fn()
+            else:
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                fn()
+                b.record()
+                kev.setdefault(kind, []).append((a, b))
+            self.launches += 1
+
+        if ev:
+            ev[0].record()
+        for l in range(w.layers):
+            if w.appends_per_step:
+                src = (self.new_rows_host if self.host_inputs else self.new_rows)[l, s * w.appends_per_step:
+                                                                                  (s + 1) * w.appends_per_step]
+                rec("append", lambda: ctx.append_rows(l, src))
+            src_l = w.source_layer(l)
+            if l in self.sel:
+                rec("select", lambda: ctx.select_topk(sc[l], w.k, self.idx[l][s & 1]))
+            rec("resolve", lambda: ctx.resolve_gather(l, self.idx[src_l][s & 1], self.out_rows, self.out_bf16))
+        if self.host_inputs:
+            self.out_host.copy_(self.out_rows, non_blocking=True)
+        if ev:
+            ev[1].record()
+        self.idx_hist[s].copy_(self.idx[self.sel[0]][s & 1])
+
+    def close(self):
+        self.ctx.close()
+
+
+def measure_host_link(torch, kvo):
+    """Best of pinned H2D memcpy and zero-copy 16-byte loads over 1 GiB."""
+    nbytes = 1 << 30
+    host = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    host.fill_(1)
+    dev = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    sink = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    res = {}
+    for name, fn in (("memcpy_h2d", lambda: dev.copy_(host, non_blocking=True)),
+                     ("zero_copy_loads", lambda: kvo.kvo_probe_host_read(host, sink))):
+        best = 0.0
+        for _ in range(4):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            best = max(best, nbytes / (a.elapsed_time(b) * 1e-3) / 1e9)
+        res[name] = round(best, 1)
+    del host, dev
+    res["peak_gbs"] = max(res["memcpy_h2d"], res["zero_copy_loads"])
+    return res
+
+
+def run_gpu_arm(args, w, rank, world):
+    import torch
+    from gather_radix_top_gb300 import build, kvo
+    build.build()
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    steps = args.warmup + args.steps
+    wl = GpuWorkload(w, layer_base=rank * w.layers, steps=steps)
+    flush = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
+    dist = world > 1
+    if dist:
+        import torch.distributed as tdist
+
+    def barrier():
+        if dist:
+            tdist.barrier()
+
+    # warm-up (untimed)
+    for s in range(args.warmup):
+        flush.zero_()
+        wl.step(s)
+    torch.cuda.synchronize()
+    st0 = {l: wl.ctx.stats(l) for l in range(w.layers)}
+    clocks = ClockSampler(torch.cuda.current_device())
+    evs, kev = [], {}
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    t0 = time.perf_counter()
+    launches0 = wl.launches
+    for s in range(args.warmup, steps):
+        flush.zero_()                      # L2 flush between timed steps (not timed)
+        ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        wl.step(s, ev, kev)
+        evs.append(ev)
+    torch.cuda.synchronize()
+    barrier()
+    wall = time.perf_counter() - t0
+    clk = clocks.stop()
+    launches = wl.launches - launches0
+    st1 = {l: wl.ctx.stats(l) for l in range(w.layers)}
+    status = wl.ctx.sync()
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    total_s = sum(step_ms) * 1e-3
+    if dist:
+        t = torch.tensor([total_s], dtype=torch.float64, device="cuda")
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        total_s = float(t.item())
+    kern = {kind: [a.elapsed_time(b) for a, b in pairs] for kind, pairs in kev.items()}
+    delta = {f: sum(st1[l][f] - st0[l][f] for l in range(w.layers)) for f in st0[0]}
+    idx_hist = wl.idx_hist.cpu().numpy()
+    wl.close()
+    del flush
+    torch.cuda.empty_cache()
+    return {"total_s": total_s, "step_ms": step_ms, "kern_ms": kern, "delta": delta, "wall": wall,
+            "clocks": clk, "launches": launches, "status": status, "idx_hist": idx_hist}
+
+
+def run_e2e(args, w):
+    """Same steps through the public API with host inputs/outputs: scores and
+    new rows from pinned host memory, gathered rows back to pinned host memory,
+    copies inside each step's events."""
+    import torch
+    steps = args.warmup + args.steps
+    wl = GpuWorkload(w, layer_base=0, steps=steps, host_inputs=True)
+    flush = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
+    evs = []
+    for s in range(steps):
+        flush.zero_()
+        ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        # the H2D copy of this step's scores sits inside the events
+        ev[0].record()
+        sc = {l: wl.scores_for(l, s) for l in wl.sel}
+        wl.scores_for = (lambda cached: (lambda l, s_: cached[l]))(sc)
+        wl.step(s)
+        del wl.scores_for
+        ev[1].record()
+        if s >= args.warmup:
+            evs.append(ev)
+    torch.cuda.synchronize()
+    total = sum(a.elapsed_time(b) for a, b in evs) * 1e-3
+    nmean = float(np.mean([w.n_at(s) for s in range(args.warmup, steps)]))
+    h2d = int(len(wl.sel) * nmean * 4 + w.layers * w.appends_per_step * ROW)
+    d2h = int(w.k * ROW)
+    wl.close()
+    del flush
+    return {"value": round(args.steps * w.layers * w.k / total, 1), "unit": "rows/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ----------------------------------------------------------- oracle arm
+def run_oracle(w, max_steps, budget_s, layers=None):
+    """The oracle as it stands, on the host cores: the first steps of the
+    workload (every layer, or the first `layers`) until `budget_s` of oracle
+    time.  Returns rows/s, the steps done and the selections."""
+    from oracle import kvo_oracle as O
+    L = w.layers if layers is None else min(layers, w.layers)
+    states = []
+    extra = {}
+    for l in range(L):
+        st = O.LayerState(w.history_cap, w.hot_rows)
+        st.append(W.rows(w, l, 0, w.n0))
+        states.append(st)
+        if w.appends_per_step:
+            extra[l] = W.rows(w, l, w.n0, max_steps * w.appends_per_step)
+    prev = {}
+    sels = []
+    spent = 0.0
+    cpu0 = time.process_time()
+    done = 0
+    for s in range(max_steps):
+        scores = {l: W.apply_carry(W.base_scores(w, l, s), prev.get(l), W.carry_draw(w, l, s), w.carry_boost)
+                  for l in range(L) if l % w.select_every == 0}
+        t = time.perf_counter()
+        idx = {}
+        for l in range(L):
+            for a in range(w.appends_per_step):
+                states[l].append(extra[l][s * w.appends_per_step + a][None])
+            if l % w.select_every == 0:
+                idx[l] = O.select_topk(scores[l], w.k)
+            O.resolve_gather(states[l], idx[w.source_layer(l)], want_bf16=w.bf16)
+        spent += time.perf_counter() - t
+        prev = idx
+        sels.append(idx[0])
+        done += 1
+        if spent >= budget_s:
+            break
+    cpu = time.process_time() - cpu0
+    return {"rows_per_s": done * L * w.k / spent, "steps": done, "layers": L, "seconds": spent,
+            "cores": max(1, round(cpu / max(spent, 1e-9))), "sels": sels}
+
+
+# -------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["kvo", "reference"], default="kvo")
+    ap.add_argument("--workload", choices=sorted(W.WORKLOADS), default="50k_single_layer")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+
+    w = W.WORKLOADS[args.workload]
+    if args.steps is None:
+        args.steps = max(1, w.steps - args.warmup)
+    if args.warmup + args.steps > w.steps:
+        w = w.scaled(steps=args.warmup + args.steps)
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    config = {"workload": w.name, "layers": w.layers, "history": w.n0, "hot_rows": w.hot_rows, "k": w.k,
+              "appends_per_step": w.appends_per_step, "select_every": w.select_every,
+              "bf16_output": w.bf16, "parallelism": f"replicas{world}",
+              "l2": "flushed between steps (1 GiB memset, outside the step events)"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        o = run_oracle(w, args.warmup + args.steps, budget_s=max(30.0, 0.5 * args.cpu_seconds * 8))
+        line = {"impl": "reference", "metric": METRIC, "value": round(o["rows_per_s"], 1), "unit": "rows/s",
+                "n_gpus": world, "steps": o["steps"], "warmup": 0,
+                "ms_per_step": round(1e3 * o["seconds"] / o["steps"], 3), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic", "config": config,
+                "cpu_baseline": {"value": round(o["rows_per_s"], 1), "unit": "rows/s", "cores": o["cores"],
+                                 "kind": "oracle",
+                                 "sample": f"first {o['steps']} steps x {o['layers']} layers of {w.name}"},
+                "e2e": {"value": round(o["rows_per_s"], 1), "unit": "rows/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        tdist.init_process_group("nccl")
+
+    cpu = None
+    if rank == 0 and world == 1:
+        cpu = run_oracle(w, args.warmup + args.steps, budget_s=args.cpu_seconds)
+
+    g = run_gpu_arm(args, w, rank, world)
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as tdist
+            tdist.destroy_process_group()
+        return
+
+    import torch
+    from gather_radix_top_gb300 import kvo
+    hbm_peak, peak_src = load_peaks()
+    link = measure_host_link(torch, kvo)
+    total_rows = args.steps * w.layers * w.k * world
+    value = total_rows / g["total_s"]
+    nmean = float(np.mean([w.n_at(s) for s in range(args.warmup, args.warmup + args.steps)]))
+    nres = len(g["kern_ms"].get("resolve", [])) or 1
+    nsel = len(g["kern_ms"].get("select", [])) or 1
+    ab = algorithmic_bytes(w, nmean, g["delta"], nres, nsel)
+    kern_avg = {kind: float(np.mean(v)) for kind, v in g["kern_ms"].items()}
+    kern_tot = {kind: float(np.sum(v)) for kind, v in g["kern_ms"].items()}
+    dominant = max(kern_tot, key=kern_tot.get)
+    per_launch_bytes = {"resolve": ab["resolve_hbm"], "select": ab["select_hbm"], "append": 2 * ROW}[dominant]
+    achieved = per_launch_bytes / (kern_avg[dominant] * 1e-3) / 1e9
+    traffic = None
+    try:
+        prof = json.load(open(os.path.join(ROOT, "profiles", "dram_traffic.json")))
+        traffic = prof.get(w.name, {}).get(dominant)
+    except Exception:
+        pass
+    host_gbs = ab["resolve_host"] / (kern_avg.get("resolve", 1e9) * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "rows/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1e3 * g["total_s"] / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+        "data": "synthetic", "config": config,
+        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(achieved, 1),
+                     "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
+                     "traffic": traffic, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_src == "measured" else "fallback 6.8 TB/s",
+                     "algorithmic_bytes_per_launch": round(per_launch_bytes)},
+        "host_link": {"achieved_miss_gbs": round(host_gbs, 2), "peak_gbs": link["peak_gbs"],
+                      "frac": round(host_gbs / link["peak_gbs"], 4) if link["peak_gbs"] else None,
+                      "probe": link, "miss_bytes_per_launch": round(ab["resolve_host"])},
+        "kernels_us": {k: round(1e3 * v, 3) for k, v in kern_avg.items()},
+        "per_step": {"hits": round(ab["hits"], 1), "misses": round(ab["misses"], 1),
+                     "fills": round(ab["fills"], 1),
+                     "step_us_p50": round(1e3 * float(np.percentile(g["step_ms"], 50)), 2),
+                     "step_us_p99": round(1e3 * float(np.percentile(g["step_ms"], 99)), 2),
+                     "step_us_max": round(1e3 * float(np.max(g["step_ms"])), 2)},
+        "gpu_launches": g["launches"], "clocks": g["clocks"],
+        "wall_s": round(g["wall"], 3), "device_status": g["status"],
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = {"value": round(cpu["rows_per_s"], 1), "unit": "rows/s", "cores": cpu["cores"],
+                                "kind": "oracle",
+                                "sample": f"first {cpu['steps']} steps x {cpu['layers']} layers of {w.name} "
+                                          f"({cpu['seconds']:.1f} s of oracle time)"}
+        m = min(len(cpu["sels"]), g["idx_hist"].shape[0])
+        same = all(np.array_equal(cpu["sels"][s], g["idx_hist"][s]) for s in range(m))
+        line["parity"] = {"steps_compared": m, "selections_equal": bool(same)}
+    if not args.no_e2e and world == 1:
+        line["e2e"] = run_e2e(args, w)
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,341 @@
+// The kvo C ABI: context lifetime, argument checks and launches.
+//
+// Host memory layout: each layer's history is one pinned, device-mapped host
+// allocation of history_cap * 656 bytes ("From 1M Total to 15+ x 1M
+// Contexts: GLM-5.3 KV Cache Offloading", "Decision three": misses read the
+// registered host copy).  Device memory: per layer an exact-size hot cache
+// and tables ("Ten sessions exposed a physical-allocation problem": long-lived
+// caches get exact-capacity allocations, never pooled blocks).
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/kvo.h"
+#include "kvo_device.cuh"
+#include "kvo_internal.h"
+
+struct kvo_ctx {
+  int device = 0;
+  int32_t layers = 0;
+  int64_t history_cap = 0;
+  int32_t hot_rows = 0;
+  int max_cluster = 16;
+  std::vector<uint8_t*> hist_host;       // pinned host history per layer
+  std::vector<kvo::LayerView> views;     // device pointers per layer
+  std::vector<int64_t> length;           // host copy of each history length
+  uint32_t* counters = nullptr;          // device [layers][4]: step, length
+  unsigned long long* stats = nullptr;   // device [layers][8]
+  int32_t* evlog = nullptr;              // device [layers][1 + 3*KVO_MAX_K] when recording
+  uint32_t* status = nullptr;            // device status word
+};
+
+namespace {
+
+constexpr size_t kEvlogStride = 1 + 3 * (size_t)KVO_MAX_K;
+
+bool ok(cudaError_t e) { return e == cudaSuccess; }
+
+void free_ctx(kvo_ctx* c) {
+  if (!c) return;
+  for (auto& v : c->views) {
+    cudaFree(v.pos2slot);
+    cudaFree(v.slot2pos);
+    cudaFree(v.last_use);
+    cudaFree(v.hot);
+  }
+  for (uint8_t* h : c->hist_host) cudaFreeHost(h);
+  cudaFree(c->counters);
+  cudaFree(c->stats);
+  cudaFree(c->evlog);
+  cudaFree(c->status);
+  delete c;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool is_device_pointer(const void* p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+}
+
+// Copies device rows into the mapped host history and publishes the new
+// length (block 0) in stream order.
+__global__ void append_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, uint64_t nvec,
+                              uint32_t* counters, uint32_t new_len) {
+  const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+  for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) dst[i] = src[i];
+  if (blockIdx.x == 0 && threadIdx.x == 0) counters[1] = new_len;
+}
+
+// Reads pinned host memory with 16-byte zero-copy loads; XOR-folds into sink.
+__global__ void probe_kernel(const uint4* __restrict__ src, uint64_t nvec, uint4* sink) {
+  const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+  uint4 acc = make_uint4(0, 0, 0, 0);
+  for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
+    const uint4 v = src[i];
+    acc.x ^= v.x;
+    acc.y ^= v.y;
+    acc.z ^= v.z;
+    acc.w ^= v.w;
+  }
+  if ((acc.x | acc.y | acc.z | acc.w) == 0xdeadbeefu) sink[0] = acc;   // keeps the loads live
+}
+
+}  // namespace
+
+namespace kvo {
+
+cudaError_t launch_append(const void* src_dev, uint8_t* hist_dev_dst, uint64_t bytes,
+                          uint32_t* counters, uint32_t new_len, cudaStream_t stream) {
+  const uint64_t nvec = bytes / 16;
+  int sms = 0, dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  uint64_t blocks = (nvec + 255) / 256;
+  const uint64_t cap = (uint64_t)(sms > 0 ? sms : 1) * 4;
+  if (blocks > cap) blocks = cap;
+  if (blocks == 0) blocks = 1;
+  append_kernel<<<(unsigned)blocks, 256, 0, stream>>>(static_cast<const uint4*>(src_dev),
+                                                     reinterpret_cast<uint4*>(hist_dev_dst), nvec,
+                                                     counters, new_len);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_probe(const void* src, uint64_t bytes, void* sink, cudaStream_t stream) {
+  int sms = 0, dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  probe_kernel<<<sms * 4, 512, 0, stream>>>(static_cast<const uint4*>(src), bytes / 16,
+                                            static_cast<uint4*>(sink));
+  return cudaGetLastError();
+}
+
+}  // namespace kvo
+
+extern "C" {
+
+const char* kvo_status_string(kvo_status s) {
+  switch (s) {
+    case KVO_OK: return "ok";
+    case KVO_EINVAL: return "invalid argument";
+    case KVO_ENOMEM: return "out of memory";
+    case KVO_ECUDA: return "CUDA error";
+    case KVO_ERANGE: return "selected position outside the history";
+    case KVO_EBUSY: return "busy";
+    case KVO_ETIMEDOUT: return "device wait timed out";
+    case KVO_ECAPACITY: return "not enough blocks";
+  }
+  return "unknown status";
+}
+
+kvo_status kvo_create(int32_t layers, int64_t history_cap, int32_t hot_rows, int32_t row_bytes,
+                      kvo_ctx** out) {
+  if (!out || layers < 1 || history_cap < 1 || history_cap > INT32_MAX || hot_rows < 1 ||
+      hot_rows > KVO_MAX_HOT_ROWS || row_bytes != KVO_ROW_BYTES)
+    return KVO_EINVAL;
+  kvo_ctx* c = new (std::nothrow) kvo_ctx;
+  if (!c) return KVO_ENOMEM;
+  if (!ok(cudaGetDevice(&c->device))) {
+    delete c;
+    return KVO_ECUDA;
+  }
+  c->layers = layers;
+  c->history_cap = history_cap;
+  c->hot_rows = hot_rows;
+  c->length.assign(layers, 0);
+  bool good = ok(cudaMalloc(&c->counters, sizeof(uint32_t) * 4 * layers)) &&
+              ok(cudaMalloc(&c->stats, sizeof(unsigned long long) * 8 * layers)) &&
+              ok(cudaMalloc(&c->status, sizeof(uint32_t))) &&
+              ok(cudaMemset(c->counters, 0, sizeof(uint32_t) * 4 * layers)) &&
+              ok(cudaMemset(c->stats, 0, sizeof(unsigned long long) * 8 * layers)) &&
+              ok(cudaMemset(c->status, 0, sizeof(uint32_t)));
+  for (int32_t l = 0; good && l < layers; ++l) {
+    kvo::LayerView v = {};
+    v.hot_rows = (uint32_t)hot_rows;
+    v.history_cap = (uint32_t)history_cap;
+    v.counters = c->counters + 4 * l;
+    v.stats = c->stats + 8 * l;
+    uint8_t* h = nullptr;
+    good = ok(cudaHostAlloc((void**)&h, (size_t)history_cap * KVO_ROW_BYTES,
+                            cudaHostAllocMapped | cudaHostAllocPortable));
+    if (!good) break;
+    c->hist_host.push_back(h);
+    void* hd = nullptr;
+    good = ok(cudaHostGetDevicePointer(&hd, h, 0));
+    v.hist = static_cast<const uint8_t*>(hd);
+    good = good && ok(cudaMalloc(&v.pos2slot, sizeof(int32_t) * (size_t)history_cap)) &&
+           ok(cudaMalloc(&v.slot2pos, sizeof(int32_t) * (size_t)hot_rows)) &&
+           ok(cudaMalloc(&v.last_use, sizeof(uint32_t) * (size_t)hot_rows)) &&
+           ok(cudaMalloc(&v.hot, (size_t)hot_rows * KVO_ROW_BYTES));
+    c->views.push_back(v);
+    good = good && ok(cudaMemset(v.pos2slot, 0xff, sizeof(int32_t) * (size_t)history_cap)) &&
+           ok(cudaMemset(v.slot2pos, 0xff, sizeof(int32_t) * (size_t)hot_rows)) &&
+           ok(cudaMemset(v.last_use, 0, sizeof(uint32_t) * (size_t)hot_rows)) &&
+           ok(cudaMemset(v.hot, 0, (size_t)hot_rows * KVO_ROW_BYTES));
+  }
+  if (good) good = ok(cudaDeviceSynchronize());
+  if (!good) {
+    cudaGetLastError();
+    free_ctx(c);
+    return KVO_ENOMEM;
+  }
+  *out = c;
+  return KVO_OK;
+}
+
+kvo_status kvo_destroy(kvo_ctx* ctx) {
+  if (!ctx) return KVO_EINVAL;
+  const bool synced = ok(cudaDeviceSynchronize());
+  free_ctx(ctx);
+  return synced ? KVO_OK : KVO_ECUDA;
+}
+
+kvo_status kvo_append_rows(kvo_ctx* ctx, int32_t layer, const void* rows, int64_t r, void* stream) {
+  if (!ctx || layer < 0 || layer >= ctx->layers || r < 0) return KVO_EINVAL;
+  if (r == 0) return KVO_OK;
+  if (!rows || !aligned16(rows) || ctx->length[layer] + r > ctx->history_cap) return KVO_EINVAL;
+  const int64_t start = ctx->length[layer];
+  const uint64_t bytes = (uint64_t)r * KVO_ROW_BYTES;
+  kvo::LayerView& v = ctx->views[layer];
+  uint8_t* dst_dev = const_cast<uint8_t*>(v.hist) + (size_t)start * KVO_ROW_BYTES;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (is_device_pointer(rows)) {
+    e = kvo::launch_append(rows, dst_dev, bytes, v.counters, (uint32_t)(start + r), s);
+  } else {
+    // Host rows: copy now (the positions are beyond every enqueued read),
+    // then publish the length in stream order.
+    std::memcpy(ctx->hist_host[layer] + (size_t)start * KVO_ROW_BYTES, rows, bytes);
+    e = kvo::launch_append(nullptr, dst_dev, 0, v.counters, (uint32_t)(start + r), s);
+  }
+  if (!ok(e)) return KVO_ECUDA;
+  ctx->length[layer] = start + r;
+  return KVO_OK;
+}
+
+kvo_status kvo_select_topk(kvo_ctx* ctx, const float* scores, int64_t n, int32_t k, int32_t* idx,
+                           void* stream) {
+  if (!ctx || !scores || !idx || k < 1 || k > KVO_MAX_K || n < k || n > INT32_MAX) return KVO_EINVAL;
+  const cudaError_t e = kvo::launch_topk(scores, (uint32_t)n, (uint32_t)k, idx, ctx->max_cluster,
+                                         static_cast<cudaStream_t>(stream));
+  return ok(e) ? KVO_OK : KVO_ECUDA;
+}
+
+kvo_status kvo_resolve_gather(kvo_ctx* ctx, int32_t layer, const int32_t* idx, int32_t k,
+                              void* out_rows, uint16_t* out_bf16, void* stream) {
+  if (!ctx || layer < 0 || layer >= ctx->layers || !idx || k < 1 || k > KVO_MAX_K ||
+      k > ctx->hot_rows || (!out_rows && !out_bf16))
+    return KVO_EINVAL;
+  if ((out_rows && !aligned16(out_rows)) || (out_bf16 && !aligned16(out_bf16))) return KVO_EINVAL;
+  kvo::LayerView v = ctx->views[layer];
+  v.evlog = ctx->evlog ? ctx->evlog + kEvlogStride * layer : nullptr;
+  const cudaError_t e =
+      kvo::launch_resolve(v, idx, (uint32_t)k, static_cast<uint8_t*>(out_rows), out_bf16, ctx->status,
+                          ctx->max_cluster, static_cast<cudaStream_t>(stream));
+  return ok(e) ? KVO_OK : KVO_ECUDA;
+}
+
+kvo_status kvo_sync(kvo_ctx* ctx, void* stream) {
+  if (!ctx) return KVO_EINVAL;
+  if (!ok(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)))) return KVO_ECUDA;
+  uint32_t st = 0;
+  if (!ok(cudaMemcpy(&st, ctx->status, sizeof st, cudaMemcpyDeviceToHost))) return KVO_ECUDA;
+  if (st == 0) return KVO_OK;
+  if (!ok(cudaMemset(ctx->status, 0, sizeof st))) return KVO_ECUDA;
+  if (st & kvo::kFlagRange) return KVO_ERANGE;
+  return KVO_ECUDA;
+}
+
+kvo_status kvo_get_stats(kvo_ctx* ctx, int32_t layer, kvo_stats* out) {
+  if (!ctx || !out || layer < 0 || layer >= ctx->layers) return KVO_EINVAL;
+  unsigned long long v[8];
+  if (!ok(cudaDeviceSynchronize())) return KVO_ECUDA;
+  if (!ok(cudaMemcpy(v, ctx->stats + 8 * layer, sizeof v, cudaMemcpyDeviceToHost))) return KVO_ECUDA;
+  out->steps = v[0];
+  out->hits = v[1];
+  out->misses = v[2];
+  out->unique_misses = v[3];
+  out->evictions = v[4];
+  out->invalid = v[5];
+  out->host_bytes = v[6];
+  out->rows_out = v[7];
+  return KVO_OK;
+}
+
+kvo_status kvo_history_length(kvo_ctx* ctx, int32_t layer, int64_t* out) {
+  if (!ctx || !out || layer < 0 || layer >= ctx->layers) return KVO_EINVAL;
+  *out = ctx->length[layer];
+  return KVO_OK;
+}
+
+kvo_status kvo_debug_dump_layer(kvo_ctx* ctx, int32_t layer, int32_t* pos2slot, int32_t* slot2pos,
+                                uint32_t* last_use, void* hot, uint32_t* step) {
+  if (!ctx || layer < 0 || layer >= ctx->layers) return KVO_EINVAL;
+  const kvo::LayerView& v = ctx->views[layer];
+  if (!ok(cudaDeviceSynchronize())) return KVO_ECUDA;
+  const size_t H = (size_t)ctx->hot_rows;
+  bool good = true;
+  if (pos2slot)
+    good = good && ok(cudaMemcpy(pos2slot, v.pos2slot, sizeof(int32_t) * (size_t)ctx->history_cap,
+                                 cudaMemcpyDeviceToHost));
+  if (slot2pos) good = good && ok(cudaMemcpy(slot2pos, v.slot2pos, sizeof(int32_t) * H, cudaMemcpyDeviceToHost));
+  if (last_use) good = good && ok(cudaMemcpy(last_use, v.last_use, sizeof(uint32_t) * H, cudaMemcpyDeviceToHost));
+  if (hot) good = good && ok(cudaMemcpy(hot, v.hot, H * KVO_ROW_BYTES, cudaMemcpyDeviceToHost));
+  if (step) good = good && ok(cudaMemcpy(step, v.counters, sizeof(uint32_t), cudaMemcpyDeviceToHost));
+  return good ? KVO_OK : KVO_ECUDA;
+}
+
+kvo_status kvo_debug_record_evictions(kvo_ctx* ctx, int32_t on) {
+  if (!ctx) return KVO_EINVAL;
+  if (!ok(cudaDeviceSynchronize())) return KVO_ECUDA;
+  if (on && !ctx->evlog) {
+    const size_t bytes = sizeof(int32_t) * kEvlogStride * (size_t)ctx->layers;
+    if (!ok(cudaMalloc(&ctx->evlog, bytes))) {
+      cudaGetLastError();
+      ctx->evlog = nullptr;
+      return KVO_ENOMEM;
+    }
+    if (!ok(cudaMemset(ctx->evlog, 0, bytes))) return KVO_ECUDA;
+  } else if (!on && ctx->evlog) {
+    cudaFree(ctx->evlog);
+    ctx->evlog = nullptr;
+  }
+  return KVO_OK;
+}
+
+kvo_status kvo_debug_evictions(kvo_ctx* ctx, int32_t layer, int32_t* triples, int32_t max,
+                               int32_t* count) {
+  if (!ctx || !count || layer < 0 || layer >= ctx->layers || max < 0 || (max > 0 && !triples))
+    return KVO_EINVAL;
+  if (!ctx->evlog) {
+    *count = 0;
+    return KVO_OK;
+  }
+  if (!ok(cudaDeviceSynchronize())) return KVO_ECUDA;
+  const int32_t* base = ctx->evlog + kEvlogStride * layer;
+  int32_t n = 0;
+  if (!ok(cudaMemcpy(&n, base, sizeof n, cudaMemcpyDeviceToHost))) return KVO_ECUDA;
+  *count = n;
+  const int32_t m = n < max ? n : max;
+  if (m > 0 && !ok(cudaMemcpy(triples, base + 1, sizeof(int32_t) * 3 * (size_t)m, cudaMemcpyDeviceToHost)))
+    return KVO_ECUDA;
+  return KVO_OK;
+}
+
+kvo_status kvo_probe_host_read(const void* src, int64_t bytes, void* sink, void* stream) {
+  if (!src || !sink || bytes <= 0 || (bytes & 15) || !aligned16(src) || !aligned16(sink)) return KVO_EINVAL;
+  void* dev = nullptr;
+  if (!ok(cudaHostGetDevicePointer(&dev, const_cast<void*>(src), 0))) {
+    cudaGetLastError();
+    return KVO_EINVAL;
+  }
+  return ok(kvo::launch_probe(dev, (uint64_t)bytes, sink, static_cast<cudaStream_t>(stream))) ? KVO_OK
+                                                                                             : KVO_ECUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,47 @@
+// Host-side internals shared by the kvo translation units (not part of the
+// public C ABI).
+#pragma once
+
+#include <cstdint>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "../../include/kvo.h"
+
+namespace kvo {
+
+// Fixed per-layer device pointers (the tables never move after create).
+struct LayerView {
+  int32_t* pos2slot;              // [history_cap], -1 = not resident
+  int32_t* slot2pos;              // [hot_rows],    -1 = empty
+  uint32_t* last_use;             // [hot_rows],    0 = never
+  uint8_t* hot;                   // [hot_rows * 656]
+  const uint8_t* hist;            // device address of the mapped host history
+  uint32_t* counters;             // [0] step, [1] history length
+  unsigned long long* stats;      // kvo_stats fields, in declaration order
+  int32_t* evlog;                 // NULL, or [1 + 3 * KVO_MAX_K]: count then triples
+  uint32_t hot_rows;
+  uint32_t history_cap;
+};
+
+struct ClusterShape {
+  int cluster = 0;                // CTAs per cluster
+  size_t smem = 0;                // dynamic shared memory per CTA
+};
+
+// Launchers (return a CUDA error code; arguments are validated by the caller).
+cudaError_t launch_topk(const float* scores, uint32_t n, uint32_t k, int32_t* idx,
+                        int max_cluster, cudaStream_t stream);
+cudaError_t launch_resolve(const LayerView& L, const int32_t* idx, uint32_t k, uint8_t* out_rows,
+                           uint16_t* out_bf16, uint32_t* status, int max_cluster,
+                           cudaStream_t stream);
+cudaError_t launch_append(const void* src_dev, uint8_t* hist_dev_dst, uint64_t bytes,
+                          uint32_t* counters, uint32_t new_len, cudaStream_t stream);
+cudaError_t launch_probe(const void* src, uint64_t bytes, void* sink, cudaStream_t stream);
+
+// Largest cluster size (16 non-portable, else 8, 4, 2) that can run with the
+// given kernel's resources; 0 if none.
+int best_cluster(const void* kernel, size_t smem, int want);
+
+}  // namespace kvo

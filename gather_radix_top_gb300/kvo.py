@@ -1,0 +1,262 @@
+"""ctypes binding of libkvo (include/kvo.h): argument marshalling only.
+
+Each ``kvo_*`` function here calls the C function of the same name.  Device
+buffers are passed as torch CUDA tensors (PyTorch supplies device memory and
+streams; all the work runs in libkvo's kernels).  A missing library raises
+ImportError: there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+ROW_BYTES = 656
+DEQUANT_VALUES = 576
+MAX_K = 8192
+MAX_HOT_ROWS = 262144
+
+KVO_OK, KVO_EINVAL, KVO_ENOMEM, KVO_ECUDA, KVO_ERANGE, KVO_EBUSY, KVO_ETIMEDOUT, KVO_ECAPACITY = (
+    0, -1, -2, -3, -4, -5, -6, -7)
+
+EXPORTED = [
+    "kvo_status_string", "kvo_create", "kvo_destroy", "kvo_append_rows", "kvo_select_topk",
+    "kvo_resolve_gather", "kvo_sync", "kvo_get_stats", "kvo_history_length",
+    "kvo_debug_dump_layer", "kvo_debug_record_evictions", "kvo_debug_evictions",
+    "kvo_probe_host_read",
+]
+
+
+class KvoError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+class kvo_stats(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_uint64) for n in (
+        "steps", "hits", "misses", "unique_misses", "evictions", "invalid", "host_bytes", "rows_out")]
+
+    def as_dict(self) -> dict:
+        return {n: int(getattr(self, n)) for n, _ in self._fields_}
+
+
+_lib = None
+_vp, _i32, _i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib() -> ctypes.CDLL:
+    """Load libkvo.so (built in-tree by gather_radix_top_gb300.build)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_build.LIB):
+        raise ImportError(f"{_build.LIB} is missing: build it with gather_radix_top_gb300.build.build()")
+    L = ctypes.CDLL(_build.LIB)
+    sig = {
+        "kvo_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+        "kvo_create": (ctypes.c_int, [_i32, _i64, _i32, _i32, ctypes.POINTER(_vp)]),
+        "kvo_destroy": (ctypes.c_int, [_vp]),
+        "kvo_append_rows": (ctypes.c_int, [_vp, _i32, _vp, _i64, _vp]),
+        "kvo_select_topk": (ctypes.c_int, [_vp, _vp, _i64, _i32, _vp, _vp]),
+        "kvo_resolve_gather": (ctypes.c_int, [_vp, _i32, _vp, _i32, _vp, _vp, _vp]),
+        "kvo_sync": (ctypes.c_int, [_vp, _vp]),
+        "kvo_get_stats": (ctypes.c_int, [_vp, _i32, ctypes.POINTER(kvo_stats)]),
+        "kvo_history_length": (ctypes.c_int, [_vp, _i32, ctypes.POINTER(_i64)]),
+        "kvo_debug_dump_layer": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _vp, _vp]),
+        "kvo_debug_record_evictions": (ctypes.c_int, [_vp, _i32]),
+        "kvo_debug_evictions": (ctypes.c_int, [_vp, _i32, _vp, _i32, ctypes.POINTER(_i32)]),
+        "kvo_probe_host_read": (ctypes.c_int, [_vp, _i64, _vp, _vp]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(L, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = L
+    return L
+
+
+def status_string(status: int) -> str:
+    return lib().kvo_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str) -> int:
+    if status != KVO_OK:
+        raise KvoError(status, what)
+    return status
+
+
+def _dev_ptr(t, dtype_name: str | None = None):
+    """data_ptr of a contiguous CUDA tensor (None -> NULL)."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    if dtype_name is not None and str(t.dtype) != dtype_name:
+        raise ValueError(f"expected {dtype_name}, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+# ----------------------------------------------------------------- calls
+def kvo_create(layers: int, history_cap: int, hot_rows: int, row_bytes: int = ROW_BYTES) -> int:
+    h = _vp()
+    _check(lib().kvo_create(layers, history_cap, hot_rows, row_bytes, ctypes.byref(h)), "kvo_create")
+    return h.value
+
+
+def kvo_destroy(ctx: int) -> None:
+    _check(lib().kvo_destroy(ctx), "kvo_destroy")
+
+
+def kvo_append_rows(ctx: int, layer: int, rows, stream=None) -> None:
+    """rows: uint8 tensor [r, 656] on the GPU, or a CPU tensor / numpy array."""
+    import numpy as np
+    if hasattr(rows, "is_cuda") and rows.is_cuda:
+        ptr, r, keep = _dev_ptr(rows, "torch.uint8"), rows.numel() // ROW_BYTES, rows
+    else:
+        keep = np.ascontiguousarray(np.asarray(rows, dtype=np.uint8))
+        if keep.ctypes.data % 16:                 # the C call wants 16-byte aligned rows
+            buf = np.empty(keep.nbytes + 16, np.uint8)
+            off = (-buf.ctypes.data) % 16
+            buf[off:off + keep.nbytes] = keep.ravel()
+            keep = buf[off:off + keep.nbytes]
+        ptr, r = ctypes.c_void_p(keep.ctypes.data), keep.size // ROW_BYTES
+    _check(lib().kvo_append_rows(ctx, layer, ptr, r, _stream_ptr(stream)), "kvo_append_rows")
+    del keep
+
+
+def kvo_select_topk(ctx: int, scores, k: int, idx=None, stream=None):
+    import torch
+    if idx is None:
+        idx = torch.empty(k, dtype=torch.int32, device=scores.device)
+    _check(lib().kvo_select_topk(ctx, _dev_ptr(scores, "torch.float32"), scores.numel(), k,
+                                 _dev_ptr(idx, "torch.int32"), _stream_ptr(stream)), "kvo_select_topk")
+    return idx
+
+
+def kvo_resolve_gather(ctx: int, layer: int, idx, out_rows=None, out_bf16=None, stream=None) -> None:
+    """out_rows: uint8 [k, 656]; out_bf16: bfloat16 (or int16 bit buffer) [k, 576]."""
+    if out_bf16 is not None and str(out_bf16.dtype) not in ("torch.bfloat16", "torch.int16"):
+        raise ValueError("out_bf16 must be bfloat16 or int16")
+    _check(lib().kvo_resolve_gather(ctx, layer, _dev_ptr(idx, "torch.int32"), idx.numel(),
+                                    _dev_ptr(out_rows, "torch.uint8"), _dev_ptr(out_bf16),
+                                    _stream_ptr(stream)), "kvo_resolve_gather")
+
+
+def kvo_sync(ctx: int, stream=None) -> int:
+    """Synchronise and return the latched device status (KVO_OK, KVO_ERANGE, ...)."""
+    return lib().kvo_sync(ctx, _stream_ptr(stream))
+
+
+def kvo_get_stats(ctx: int, layer: int) -> dict:
+    s = kvo_stats()
+    _check(lib().kvo_get_stats(ctx, layer, ctypes.byref(s)), "kvo_get_stats")
+    return s.as_dict()
+
+
+def kvo_history_length(ctx: int, layer: int) -> int:
+    n = _i64()
+    _check(lib().kvo_history_length(ctx, layer, ctypes.byref(n)), "kvo_history_length")
+    return n.value
+
+
+def kvo_debug_dump_layer(ctx: int, layer: int, history_cap: int, hot_rows: int, hot: bool = True) -> dict:
+    import numpy as np
+    d = {
+        "pos2slot": np.empty(history_cap, np.int32),
+        "slot2pos": np.empty(hot_rows, np.int32),
+        "last_use": np.empty(hot_rows, np.uint32),
+        "hot": np.empty((hot_rows, ROW_BYTES), np.uint8) if hot else None,
+        "step": np.zeros(1, np.uint32),
+    }
+    p = lambda a: None if a is None else ctypes.c_void_p(a.ctypes.data)
+    _check(lib().kvo_debug_dump_layer(ctx, layer, p(d["pos2slot"]), p(d["slot2pos"]), p(d["last_use"]),
+                                      p(d["hot"]), p(d["step"])), "kvo_debug_dump_layer")
+    d["step"] = int(d["step"][0])
+    return d
+
+
+def kvo_debug_record_evictions(ctx: int, on: bool) -> None:
+    _check(lib().kvo_debug_record_evictions(ctx, 1 if on else 0), "kvo_debug_record_evictions")
+
+
+def kvo_debug_evictions(ctx: int, layer: int) -> list:
+    import numpy as np
+    buf = np.zeros(3 * MAX_K, np.int32)
+    n = _i32()
+    _check(lib().kvo_debug_evictions(ctx, layer, ctypes.c_void_p(buf.ctypes.data), MAX_K, ctypes.byref(n)),
+           "kvo_debug_evictions")
+    return [tuple(int(x) for x in buf[3 * i:3 * i + 3]) for i in range(n.value)]
+
+
+def kvo_probe_host_read(src_pinned, sink, stream=None) -> None:
+    """src_pinned: pinned CPU tensor (multiple of 16 bytes); sink: 16-byte CUDA tensor."""
+    _check(lib().kvo_probe_host_read(ctypes.c_void_p(src_pinned.data_ptr()),
+                                     src_pinned.numel() * src_pinned.element_size(),
+                                     _dev_ptr(sink), _stream_ptr(stream)), "kvo_probe_host_read")
+
+
+class Context:
+    """Owns one kvo context; methods forward to the kvo_* calls above."""
+
+    def __init__(self, layers: int, history_cap: int, hot_rows: int, row_bytes: int = ROW_BYTES):
+        self.layers, self.history_cap, self.hot_rows = layers, history_cap, hot_rows
+        self.handle = kvo_create(layers, history_cap, hot_rows, row_bytes)
+
+    def close(self):
+        if self.handle:
+            kvo_destroy(self.handle)
+            self.handle = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def append_rows(self, layer, rows, stream=None):
+        kvo_append_rows(self.handle, layer, rows, stream)
+
+    def select_topk(self, scores, k, idx=None, stream=None):
+        return kvo_select_topk(self.handle, scores, k, idx, stream)
+
+    def resolve_gather(self, layer, idx, out_rows=None, out_bf16=None, stream=None):
+        kvo_resolve_gather(self.handle, layer, idx, out_rows, out_bf16, stream)
+
+    def sync(self, stream=None) -> int:
+        return kvo_sync(self.handle, stream)
+
+    def stats(self, layer) -> dict:
+        return kvo_get_stats(self.handle, layer)
+
+    def history_length(self, layer) -> int:
+        return kvo_history_length(self.handle, layer)
+
+    def dump_layer(self, layer, hot=True) -> dict:
+        return kvo_debug_dump_layer(self.handle, layer, self.history_cap, self.hot_rows, hot)
+
+    def record_evictions(self, on=True):
+        kvo_debug_record_evictions(self.handle, on)
+
+    def evictions(self, layer) -> list:
+        return kvo_debug_evictions(self.handle, layer)

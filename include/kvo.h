@@ -1,0 +1,195 @@
+/*
+ * kvo.h - sparse KV residency for long-context MLA decode on GB300 (sm_103a).
+ *
+ * One context holds, per layer, the full MLA history in pinned host memory
+ * and a fixed-size hot cache in HBM, plus the position->slot tables that
+ * connect them.  Per decode step and layer the caller selects the top-K
+ * history positions from indexer scores (kvo_select_topk) and resolves them
+ * (kvo_resolve_gather): hits are read from the hot cache, misses from host
+ * memory, least-recently-used unpinned slots receive the misses, and the K
+ * rows are written contiguously in selection order.
+ *
+ * Sources (page title, section):
+ *   [KVO]  "From 1M Total to 15+ x 1M Contexts: GLM-5.3 KV Cache Offloading"
+ *   [CORR] "Making KV offload correct" (Running large language models on
+ *          dual GH200, post 4)
+ *
+ * Conventions for every call:
+ *   - Device pointers are CUDA device (or managed) memory of the current
+ *     device; "host" pointers are ordinary process memory.  `stream` is a
+ *     cudaStream_t passed as void* (NULL = the legacy default stream).
+ *   - Calls are asynchronous and stream-ordered unless stated otherwise.
+ *     Argument errors are detected synchronously, return KVO_EINVAL and
+ *     change no state.  Errors found by kernels (for example a selected
+ *     position outside the history) are latched in a device status word and
+ *     returned by the next kvo_sync.
+ *   - The caller owns every buffer it passes (scores, idx, outputs, rows)
+ *     and the streams; the context owns the histories, hot caches, tables
+ *     and statistics.  A context is not thread-safe; calls on one context
+ *     must come from one host thread at a time.
+ *   - A Q8G64 MLA row is 656 bytes ([KVO] "Separate historical capacity
+ *     from the current working set"): bytes [0,512) int8 latent, [512,528)
+ *     eight little-endian fp16 scales (scale g covers latent bytes
+ *     [64g, 64g+64)), [528,656) 64 little-endian bf16 RoPE values.
+ */
+#ifndef KVO_H
+#define KVO_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVO_ROW_BYTES 656
+#define KVO_LATENT_BYTES 512
+#define KVO_DEQUANT_VALUES 576      /* bf16 values per dequantised row */
+#define KVO_MAX_K 8192              /* largest selection size per call */
+#define KVO_MAX_HOT_ROWS 262144     /* largest hot cache per layer */
+
+typedef enum kvo_status {
+  KVO_OK = 0,
+  KVO_EINVAL = -1,     /* bad argument; nothing was changed or enqueued */
+  KVO_ENOMEM = -2,     /* a device or pinned-host allocation failed */
+  KVO_ECUDA = -3,      /* a CUDA runtime call failed */
+  KVO_ERANGE = -4,     /* a kernel saw a selected position outside [0, length) */
+  KVO_EBUSY = -5,      /* resource still referenced by in-flight work */
+  KVO_ETIMEDOUT = -6,  /* a bounded device-side wait gave up */
+  KVO_ECAPACITY = -7   /* not enough blocks; allocation rolled back */
+} kvo_status;
+
+typedef struct kvo_ctx kvo_ctx;
+
+/* Per-layer counters, accumulated on the device by every resolve call. */
+typedef struct kvo_stats {
+  uint64_t steps;          /* resolve calls on the layer */
+  uint64_t hits;           /* selected entries found in the hot cache */
+  uint64_t misses;         /* selected entries read from host memory (every occurrence) */
+  uint64_t unique_misses;  /* distinct missing positions (= hot-cache fills) */
+  uint64_t evictions;      /* fills that replaced a mapped position */
+  uint64_t invalid;        /* selected entries outside [0, length) */
+  uint64_t host_bytes;     /* bytes read from host memory by gathers */
+  uint64_t rows_out;       /* rows emitted */
+} kvo_stats;
+
+/* Human-readable name of a status code (static string). */
+const char* kvo_status_string(kvo_status s);
+
+/*
+ * kvo_create - allocate a context on the current device.
+ *   layers       >= 1 independent layers (each with its own history and hot
+ *                cache: [KVO] "Separate historical capacity ...": layers
+ *                that reuse a selection keep their own KV contents).
+ *   history_cap  rows of host history per layer, 1 .. 2^31-1 (pinned,
+ *                device-mapped host memory, history_cap*656 bytes per layer).
+ *   hot_rows     HBM hot-cache rows per layer, 1 .. KVO_MAX_HOT_ROWS
+ *                (hot_rows*656 bytes per layer, exact-size allocation).
+ *   row_bytes    must be KVO_ROW_BYTES.
+ *   out          receives the context; untouched on error.
+ * Every hot slot starts empty, every history length at 0.  Synchronous.
+ * Errors: KVO_EINVAL, KVO_ENOMEM (everything allocated so far is freed).
+ */
+kvo_status kvo_create(int32_t layers, int64_t history_cap, int32_t hot_rows,
+                      int32_t row_bytes, kvo_ctx** out);
+
+/* kvo_destroy - wait for all work on the device, then free the context. */
+kvo_status kvo_destroy(kvo_ctx* ctx);
+
+/*
+ * kvo_append_rows - append r rows to a layer's host history at positions
+ * [length, length + r), then length += r ([KVO] "Decision three": new KV goes
+ * to the RAM history; an appended position is a miss the first time it is
+ * selected).
+ *   rows   r*656 bytes, 16-byte aligned; device memory (copied by a kernel
+ *          in stream order) or host memory (copied before the call returns;
+ *          the new length takes effect in stream order).
+ * Errors: KVO_EINVAL if layer is out of range, r < 0, length + r exceeds
+ * history_cap or rows is NULL with r > 0.
+ */
+kvo_status kvo_append_rows(kvo_ctx* ctx, int32_t layer, const void* rows, int64_t r,
+                           void* stream);
+
+/*
+ * kvo_select_topk - the k highest of n fp32 scores ([KVO] "Separate
+ * historical capacity ...": the indexer selects the top 2,048 positions).
+ *   scores  device fp32[n].
+ *   idx     device int32[k]; receives the chosen positions in ascending
+ *           order.
+ * Order: higher score first, equal scores -> lower position first; -0.0
+ * equals +0.0; NaN ranks below every other value (NaNs tie by position).
+ * Errors: KVO_EINVAL unless 0 < k <= n, k <= KVO_MAX_K and n < 2^31.
+ */
+kvo_status kvo_select_topk(kvo_ctx* ctx, const float* scores, int64_t n, int32_t k,
+                           int32_t* idx, void* stream);
+
+/*
+ * kvo_resolve_gather - resolve k selected positions of one layer against its
+ * hot cache and emit their rows ([KVO] "Decision three: let the GPU manage
+ * the hot cache directly" and "GPU cache management has hazards too").
+ *   idx       device int32[k], any order, duplicates allowed.
+ *   out_rows  device uint8[k*656] (16-byte aligned) or NULL: row j = the
+ *             656-byte row of position idx[j].
+ *   out_bf16  device uint16[k*576] (16-byte aligned) or NULL: row j =
+ *             bf16 round-to-nearest-even of float(q)*float(scale[g]) for
+ *             the 512 latent bytes, then the 64 RoPE bf16 values copied.
+ * Per call the layer's step counter t advances by one.  Hits (positions with
+ * a hot slot) read HBM and stamp last_use = t (pinning the slot for this
+ * step).  Misses read host memory, every occurrence.  The distinct missing
+ * positions, in first-occurrence order, take the slots with the smallest
+ * (last_use, slot) among slots with last_use < t, in that order; the map is
+ * updated and each such slot receives its new row, so it becomes a hit
+ * source from the next call on.
+ * An entry outside [0, length) gets a zero row, changes no state and latches
+ * KVO_ERANGE for kvo_sync.
+ * Errors: KVO_EINVAL if layer is out of range, k < 1, k > KVO_MAX_K,
+ * k > hot_rows, both outputs are NULL or an output is misaligned.
+ */
+kvo_status kvo_resolve_gather(kvo_ctx* ctx, int32_t layer, const int32_t* idx, int32_t k,
+                              void* out_rows, uint16_t* out_bf16, void* stream);
+
+/*
+ * kvo_sync - synchronise `stream`, then return and clear the device status
+ * word: KVO_OK, or the first latched device error (KVO_ERANGE, ...).
+ */
+kvo_status kvo_sync(kvo_ctx* ctx, void* stream);
+
+/* kvo_get_stats - copy a layer's counters to *out (synchronises the device). */
+kvo_status kvo_get_stats(kvo_ctx* ctx, int32_t layer, kvo_stats* out);
+
+/* kvo_history_length - a layer's length as of all calls made so far. */
+kvo_status kvo_history_length(kvo_ctx* ctx, int32_t layer, int64_t* out);
+
+/*
+ * kvo_debug_dump_layer - copy a layer's state to host buffers (any may be
+ * NULL): pos2slot int32[history_cap] (-1 = not resident), slot2pos
+ * int32[hot_rows] (-1 = empty), last_use uint32[hot_rows] (0 = never),
+ * hot uint8[hot_rows*656], step = the layer's step counter.  Synchronises
+ * the device.  Meant for tests.
+ */
+kvo_status kvo_debug_dump_layer(kvo_ctx* ctx, int32_t layer, int32_t* pos2slot,
+                                int32_t* slot2pos, uint32_t* last_use, void* hot,
+                                uint32_t* step);
+
+/*
+ * kvo_debug_record_evictions - when enabled (on != 0), every resolve call
+ * records its fills as (slot, evicted position or -1, new position) triples,
+ * in the order the misses took them.  kvo_debug_evictions copies the last
+ * call's list for `layer` to host int32[3*max] and its length to *count
+ * (synchronises the device).
+ */
+kvo_status kvo_debug_record_evictions(kvo_ctx* ctx, int32_t on);
+kvo_status kvo_debug_evictions(kvo_ctx* ctx, int32_t layer, int32_t* triples, int32_t max,
+                               int32_t* count);
+
+/*
+ * kvo_probe_host_read - read `bytes` (multiple of 16) of pinned host memory
+ * `src` with 16-byte zero-copy loads from every SM and reduce them into
+ * device uint4 `sink`; used to measure the host link.  Stream-ordered.
+ */
+kvo_status kvo_probe_host_read(const void* src, int64_t bytes, void* sink, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVO_H */

@@ -1,0 +1,60 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds for
+sm_103a, exports every function include/kvo.h declares, and rejects bad
+arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def kvo():
+    from gather_radix_top_gb300 import build, kvo as K
+    build.build()
+    return K
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "kvo.h")).read()
+    return sorted(set(re.findall(r"\b(kvo_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for n in ("kvo_create", "kvo_destroy", "kvo_append_rows", "kvo_select_topk", "kvo_resolve_gather",
+              "kvo_sync", "kvo_get_stats", "kvo_debug_dump_layer"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(kvo):
+    L = kvo.lib()
+    for n in _declared():
+        assert hasattr(L, n), n
+    assert sorted(kvo.EXPORTED) == _declared()
+
+
+def test_bad_arguments_rejected_without_a_device(kvo):
+    L = kvo.lib()
+    h = ctypes.c_void_p()
+    assert L.kvo_create(0, 10, 4, 656, ctypes.byref(h)) == kvo.KVO_EINVAL
+    assert L.kvo_create(1, 10, 4, 640, ctypes.byref(h)) == kvo.KVO_EINVAL
+    assert L.kvo_create(1, 10, kvo.MAX_HOT_ROWS + 1, 656, ctypes.byref(h)) == kvo.KVO_EINVAL
+    assert L.kvo_create(1, 2 ** 31, 4, 656, ctypes.byref(h)) == kvo.KVO_EINVAL
+    assert h.value is None
+    assert L.kvo_sync(None, None) == kvo.KVO_EINVAL
+    assert L.kvo_select_topk(None, None, 10, 5, None, None) == kvo.KVO_EINVAL
+    assert L.kvo_resolve_gather(None, 0, None, 5, None, None, None) == kvo.KVO_EINVAL
+    assert L.kvo_append_rows(None, 0, None, 1, None) == kvo.KVO_EINVAL
+    assert L.kvo_destroy(None) == kvo.KVO_EINVAL
+    assert kvo.status_string(kvo.KVO_ERANGE) == "selected position outside the history"
+
+
+def test_binding_has_no_fallback(tmp_path, monkeypatch):
+    from gather_radix_top_gb300 import build, kvo as K
+    monkeypatch.setattr(build, "LIB", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(K, "_lib", None)
+    with pytest.raises(ImportError):
+        K.lib()

@@ -1,0 +1,242 @@
+"""CUDA path vs oracle, element by element, through the C ABI.
+
+Bar: bit-exact for positions, maps, eviction order and raw rows; 0 bf16 ULP
+for the dequant (both sides round the same exact float32 product once).
+"""
+import numpy as np
+import pytest
+
+from oracle import kvo_oracle as O
+from synth import workloads as W
+from tests.gpu_harness import GpuLayerRun, OracleLayerRun, compare_state, cuda_ok
+
+pytestmark = [pytest.mark.gpu, pytest.mark.skipif(not cuda_ok(), reason="needs a CUDA GPU")]
+
+
+@pytest.fixture(scope="module")
+def kvo():
+    from gather_radix_top_gb300 import build, kvo as K
+    build.build()
+    return K
+
+
+@pytest.fixture(scope="module")
+def ctx(kvo):
+    c = kvo.Context(1, 64, 16)
+    yield c
+    c.close()
+
+
+def _bits(x):
+    return np.asarray(x).view(np.uint16)
+
+
+def assert_bf16_equal(got, want):
+    """Bit-equal bf16, except that a NaN matches any NaN: IEEE-754 leaves the
+    sign and payload of a NaN result open, and CPUs and GPUs differ there."""
+    got, want = _bits(got), _bits(want)
+    nan_g = (got & 0x7F80) == 0x7F80
+    nan_g &= (got & 0x7F) != 0
+    nan_w = (want & 0x7F80) == 0x7F80
+    nan_w &= (want & 0x7F) != 0
+    np.testing.assert_array_equal(nan_g, nan_w)
+    np.testing.assert_array_equal(np.where(nan_g, 0, got), np.where(nan_w, 0, want))
+
+
+# ------------------------------------------------------------------ top-K
+TOPK_CASES = [
+    (1, 1, "normal"), (5, 3, "normal"), (31, 31, "normal"), (64, 32, "normal"), (100, 33, "ties"),
+    (1000, 256, "special"), (4096, 256, "normal"), (4096, 256, "ties"), (4099, 1000, "special"),
+    (50_023, 2048, "normal"), (50_023, 2048, "ties"), (51_047, 2048, "special"),
+    (65_537, 8192, "normal"), (200_000, 2048, "ties"), (1_048_576, 2048, "normal"),
+    (1_048_576, 2048, "ties"), (1_048_583, 4097, "special"),
+]
+
+
+@pytest.mark.parametrize("n,k,kind", TOPK_CASES)
+def test_topk_matches_oracle(ctx, n, k, kind):
+    import torch
+    s = W.random_scores(n * 7 + k, n, kind)
+    idx = ctx.select_topk(torch.from_numpy(s).cuda(), k)
+    np.testing.assert_array_equal(idx.cpu().numpy(), O.select_topk(s, k))
+
+
+@pytest.mark.parametrize("n,k", [(4096, 256), (50_023, 2048), (1_048_576, 2048)])
+def test_topk_degenerate_orders(ctx, n, k):
+    import torch
+    for s in (np.zeros(n, np.float32), np.arange(n, dtype=np.float32),
+              -np.arange(n, dtype=np.float32), np.full(n, np.nan, np.float32)):
+        idx = ctx.select_topk(torch.from_numpy(s).cuda(), k).cpu().numpy()
+        np.testing.assert_array_equal(idx, O.select_topk(s, k))
+
+
+def test_topk_k_equals_n_and_unaligned_scores(ctx):
+    import torch
+    s = W.random_scores(11, 3001, "special")
+    idx = ctx.select_topk(torch.from_numpy(s).cuda(), 3001).cpu().numpy()
+    np.testing.assert_array_equal(idx, np.arange(3001))
+    big = torch.from_numpy(W.random_scores(12, 9001)).cuda()
+    view = big[1:]                                   # 4-byte aligned, not 16
+    idx = ctx.select_topk(view, 777).cpu().numpy()
+    np.testing.assert_array_equal(idx, O.select_topk(big.cpu().numpy()[1:], 777))
+
+
+# ---------------------------------------------------------------- resolve
+def test_tiny_workload_full_parity(kvo):
+    w = W.TINY
+    g = GpuLayerRun(w, 0, want_bf16=True)
+    o = OracleLayerRun(w, 0, want_bf16=True)
+    g.ctx.record_evictions(True)
+    for step in range(w.steps):
+        gi = g.step(step)
+        oi = o.step(step)
+        np.testing.assert_array_equal(gi, oi)
+        np.testing.assert_array_equal(g.rows(), o.last.rows)
+        np.testing.assert_array_equal(g.bf16(), o.last.bf16)
+        assert g.ctx.evictions(0) == o.last.evictions
+        compare_state(g.ctx, 0, o.st)
+    assert g.ctx.sync() == 0
+    st = g.ctx.stats(0)
+    assert st["steps"] == w.steps and st["rows_out"] == w.steps * w.k
+    g.ctx.close()
+
+
+@pytest.mark.parametrize("seed,H,n,k,dup,bad", [
+    (1, 16, 40, 16, 0.3, 2), (2, 64, 300, 33, 0.5, 0), (3, 1024, 5000, 256, 0.2, 5),
+    (4, 1024, 5000, 1024, 0.0, 0), (5, 4096, 70_000, 2048, 0.4, 3), (6, 32_768, 60_000, 8192, 0.1, 1),
+])
+def test_resolve_random_selections(kvo, seed, H, n, k, dup, bad):
+    """Arbitrary order, duplicates and out-of-range entries; many steps so the
+    cache fills, then evicts."""
+    import torch
+    g = np.random.default_rng(seed)
+    hist = g.integers(0, 256, size=(n, O.ROW_BYTES), dtype=np.uint8)
+    ctx = kvo.Context(1, n, H)
+    ctx.append_rows(0, hist)
+    ctx.record_evictions(True)
+    st = O.LayerState(n, H)
+    st.append(hist)
+    out = torch.empty((k, O.ROW_BYTES), dtype=torch.uint8, device="cuda")
+    outb = torch.empty((k, O.DEQUANT_VALUES), dtype=torch.int16, device="cuda")
+    for step in range(12):
+        idx = W.random_idx(seed * 100 + step, n if step % 3 else min(n, 2 * H), k, dup, bad if step % 2 else 0)
+        ctx.resolve_gather(0, torch.from_numpy(idx).cuda(), out, outb)
+        res = O.resolve_gather(st, idx, want_bf16=True)
+        np.testing.assert_array_equal(out.cpu().numpy(), res.rows)
+        assert_bf16_equal(outb.cpu().numpy(), res.bf16)
+        assert ctx.evictions(0) == res.evictions
+        status = ctx.sync()
+        assert status == (kvo.KVO_ERANGE if res.invalid else 0)
+    compare_state(ctx, 0, st)
+    s = ctx.stats(0)
+    ctx.close()
+
+
+def test_hot_cache_exactly_k_rows(kvo):
+    """k = hot_rows: every slot may be needed in one step."""
+    import torch
+    n, H = 4000, 512
+    hist = np.random.default_rng(9).integers(0, 256, size=(n, O.ROW_BYTES), dtype=np.uint8)
+    ctx = kvo.Context(1, n, H)
+    ctx.append_rows(0, hist)
+    st = O.LayerState(n, H)
+    st.append(hist)
+    out = torch.empty((H, O.ROW_BYTES), dtype=torch.uint8, device="cuda")
+    for step in range(6):
+        idx = np.sort(np.random.default_rng(step).choice(n, H, replace=False)).astype(np.int32)
+        ctx.resolve_gather(0, torch.from_numpy(idx).cuda(), out)
+        res = O.resolve_gather(st, idx)
+        np.testing.assert_array_equal(out.cpu().numpy(), res.rows)
+    compare_state(ctx, 0, st)
+    ctx.close()
+
+
+def test_append_host_and_device_rows(kvo):
+    import torch
+    w = W.TINY.scaled(appends_per_step=3, steps=6)
+    g = GpuLayerRun(w, 0)
+    o = OracleLayerRun(w, 0)
+    for step in range(w.steps):
+        np.testing.assert_array_equal(g.step(step), o.step(step))
+        np.testing.assert_array_equal(g.rows(), o.last.rows)
+    assert g.ctx.history_length(0) == o.st.length
+    compare_state(g.ctx, 0, o.st)
+    g.ctx.close()
+
+
+# -------------------------------------------------- full-size workloads
+def test_50k_single_layer_all_steps(kvo):
+    """The 50K single-layer workload, all 1,024 steps, in the launch shape the
+    benchmark times: selections compared every step, rows every 64th step,
+    full state at the end."""
+    w = W.K50
+    g = GpuLayerRun(w, 0)
+    o = OracleLayerRun(w, 0)
+    for step in range(w.steps):
+        np.testing.assert_array_equal(g.step(step), o.step(step))
+        if step % 64 == 0 or step == w.steps - 1:
+            np.testing.assert_array_equal(g.rows(), o.last.rows)
+    compare_state(g.ctx, 0, o.st)
+    s = g.ctx.stats(0)
+    assert s["hits"] + s["misses"] == w.steps * w.k
+    g.ctx.close()
+
+
+def test_1m_cold_stress_sampled(kvo):
+    """1M positions, bf16 output on: one layer's first 6 steps, every output."""
+    w = W.M1.scaled(steps=6)
+    g = GpuLayerRun(w, 3)
+    o = OracleLayerRun(w, 3)
+    for step in range(w.steps):
+        np.testing.assert_array_equal(g.step(step), o.step(step))
+        np.testing.assert_array_equal(g.rows(), o.last.rows)
+        np.testing.assert_array_equal(g.bf16(), o.last.bf16)
+    compare_state(g.ctx, 0, o.st, check_hot=False)
+    g.ctx.close()
+
+
+def test_stack_layers_share_selection(kvo):
+    """Full-stack layout in one context: layers 0-3 share layer 0's selection,
+    each keeps its own history and hot cache."""
+    import torch
+    w = W.STACK.scaled(layers=4, steps=24)
+    ctx = kvo.Context(4, w.history_cap, w.hot_rows)
+    gs = [GpuLayerRun(w, l, ctx=ctx, ctx_layer=l) for l in range(4)]
+    os_ = [OracleLayerRun(w, l) for l in range(4)]
+    for step in range(w.steps):
+        idx = gs[0].step(step)                       # layer 0 selects
+        oidx = os_[0].step(step)
+        np.testing.assert_array_equal(idx, oidx)
+        idx_d = torch.from_numpy(idx).cuda()
+        for l in range(1, 4):
+            for a in range(w.appends_per_step):
+                pos = w.n0 + step
+                ctx.append_rows(l, gs[l].new_rows[pos - w.n0:pos - w.n0 + 1])
+            ctx.resolve_gather(l, idx_d, gs[l].out_rows)
+            os_[l].step(step, idx_override=oidx)
+            if step % 8 == 7:
+                np.testing.assert_array_equal(gs[l].rows(), os_[l].last.rows)
+    for l in range(4):
+        compare_state(ctx, l, os_[l].st)
+    ctx.close()
+
+
+# ------------------------------------------------------------ arguments
+def test_argument_errors_change_nothing(kvo):
+    import torch
+    ctx = kvo.Context(2, 100, 8)
+    ctx.append_rows(0, np.zeros((10, O.ROW_BYTES), np.uint8))
+    idx = torch.arange(9, dtype=torch.int32, device="cuda")
+    out = torch.empty((9, O.ROW_BYTES), dtype=torch.uint8, device="cuda")
+    with pytest.raises(kvo.KvoError):
+        ctx.resolve_gather(0, idx, out)                  # k > hot_rows
+    with pytest.raises(kvo.KvoError):
+        ctx.resolve_gather(2, idx[:4], out[:4])          # bad layer
+    with pytest.raises(kvo.KvoError):
+        ctx.select_topk(torch.zeros(5, device="cuda"), 6)
+    with pytest.raises(kvo.KvoError):
+        ctx.append_rows(1, np.zeros((101, O.ROW_BYTES), np.uint8))
+    assert ctx.history_length(1) == 0
+    d = ctx.dump_layer(0)
+    assert d["step"] == 0 and (d["slot2pos"] == -1).all()
+    ctx.close()

@@ -11,7 +11,7 @@
 #include <new>
 #include <vector>
 
-#include "../../include/kvo.h"
+#include "kvo.h"
 #include "kvo_device.cuh"
 #include "kvo_internal.h"
 

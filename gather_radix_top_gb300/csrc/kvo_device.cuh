@@ -1,7 +1,7 @@
 // Device-side building blocks shared by the kvo kernels: thread-block-cluster
 // barriers and distributed shared memory (inline PTX), block-wide scans, and
-// the cluster-wide radix select used by both the top-K selection and the LRU
-// victim choice.
+// the cluster-wide radix select + ordered compaction used by both the top-K
+// selection and the LRU victim choice.
 #pragma once
 
 #include <cstdint>
@@ -12,10 +12,11 @@ namespace kvo {
 constexpr int kThreads = 1024;          // threads per CTA of the cluster kernels
 constexpr int kWarps = kThreads / 32;
 constexpr int kRadixBins = 256;         // 8-bit digits, most significant first
+constexpr uint32_t kMaxCluster = 16;
 
 // Device status word bits (returned by kvo_sync).
 constexpr uint32_t kFlagRange = 1u;
-constexpr uint32_t kFlagInternal = 2u;      // an internal consistency check failed
+constexpr uint32_t kFlagInternal = 2u;  // an internal consistency check failed
 
 // ---------------------------------------------------------------- cluster
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -35,6 +36,17 @@ __device__ __forceinline__ uint32_t cluster_size() {
 // cluster before it is visible to every thread of the cluster after it.
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// The two halves of cluster_sync, so that a thread can work between its
+// arrival and its wait (each arrive must be followed by a wait before the
+// next arrive).
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
 }
 
 // Address of the same shared variable in CTA `rank` of this cluster.
@@ -57,6 +69,23 @@ __device__ __forceinline__ void dsmem_st_u32(uint32_t addr, uint32_t v) {
 
 __device__ __forceinline__ void dsmem_st_u64(uint32_t addr, uint64_t v) {
   asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ void dsmem_red_add_u32(uint32_t addr, uint32_t v) {
+  asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Each CTA publishes `nval` (<= 4) values; afterwards every CTA reads every
+// CTA's values from its own shared memory (table[rank][i]).  Contains one
+// cluster barrier; `table` must not be written again before the next one.
+__device__ __forceinline__ void cluster_publish(const uint32_t* vals, uint32_t nval, uint32_t (*table)[4],
+                                                uint32_t rank, uint32_t nrank) {
+  const uint32_t tid = threadIdx.x;
+  if (tid < nrank * nval) {
+    const uint32_t dst = tid / nval, i = tid % nval;
+    dsmem_st_u32(dsmem_addr(&table[rank][i], dst), vals[i]);
+  }
+  cluster_sync();
 }
 
 // ------------------------------------------------------------------ scans
@@ -88,6 +117,7 @@ __device__ __forceinline__ uint32_t block_flag_scan(bool flag, uint32_t* scratch
 }
 
 // Sum of a per-thread value over the CTA (result valid in every thread).
+// `scratch` holds kWarps + 1 words.
 __device__ __forceinline__ uint32_t block_sum(uint32_t v, uint32_t* scratch) {
   const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
@@ -106,55 +136,122 @@ __device__ __forceinline__ uint32_t block_sum(uint32_t v, uint32_t* scratch) {
   return r;
 }
 
+// Sums of two per-thread values over the CTA, returned in every thread.
+// `scratch` holds 2 * kWarps words.
+__device__ __forceinline__ void block_sum2(uint32_t a, uint32_t b, uint32_t* scratch, uint32_t* sa,
+                                           uint32_t* sb) {
+  static_assert(kWarps == 32, "one lane per warp of the CTA");
+  const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) {
+    a += __shfl_xor_sync(0xffffffffu, a, d);
+    b += __shfl_xor_sync(0xffffffffu, b, d);
+  }
+  if (lane == 0) {
+    scratch[2 * warp] = a;
+    scratch[2 * warp + 1] = b;
+  }
+  __syncthreads();
+  a = scratch[2 * lane];
+  b = scratch[2 * lane + 1];
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) {
+    a += __shfl_xor_sync(0xffffffffu, a, d);
+    b += __shfl_xor_sync(0xffffffffu, b, d);
+  }
+  __syncthreads();
+  *sa = a;
+  *sb = b;
+}
+
 // ----------------------------------------------------- cluster radix select
-// Outcome of selecting the `want` largest 32-bit keys over the cluster: the
-// selected keys are those whose top (32 - shift) bits exceed those of
-// `prefix`, plus the first `need` keys (in index order) whose top bits equal
-// them.  When the last examined bucket is taken whole, `need` equals its
-// count.
+// Outcome of selecting the `want` largest keys over the cluster: the selected
+// keys are those whose bits above `shift` exceed those of `prefix`, plus the
+// first `need` keys (in index order) whose bits above `shift` equal them.
+// When the last examined bucket is taken whole, `need` equals its count.
+// `above` / `at` count this CTA's keys above / at the cut.
 struct RadixCut {
   uint32_t prefix;
   uint32_t shift;
   uint32_t need;
+  uint32_t above;
+  uint32_t at;
 };
 
 struct RadixSmem {
-  uint32_t hist[2][kRadixBins];   // this CTA's histograms (double-buffered)
-  uint32_t total[kRadixBins];     // cluster-wide histogram of the current pass
-  uint32_t cut[4];                // bucket, count above it, bucket count
+  uint32_t hist[kRadixBins];        // this CTA's histogram of the current pass
+  uint32_t total[2][kRadixBins];    // cluster-wide histograms, added into by every CTA
+  uint32_t cut[4];                  // bucket, count above it, bucket count
+  uint32_t local[2];                // this CTA's keys above the cut, at the cut
 };
 
-// Finds the cut.  `key_at(i)` returns this CTA's i-th key for i < count.
-// Every CTA of the cluster must call it with the same `want`, and `want` must
-// not exceed the cluster's key count.  One cluster barrier per digit pass.
-template <typename KeyAt>
-__device__ RadixCut cluster_radix_select(KeyAt key_at, uint32_t count, uint32_t want,
+// Zeroes the cluster-wide histograms.  A cluster barrier must separate this
+// from the first cluster_radix_select of any CTA.
+__device__ __forceinline__ void radix_smem_init(RadixSmem* sm) {
+  for (uint32_t b = threadIdx.x; b < 2 * kRadixBins; b += kThreads) (&sm->total[0][0])[b] = 0;
+}
+
+// Adds one to bin `bin` for every lane with `valid`; lanes with the same bin
+// are combined first (one shared atomic per distinct bin per warp), because
+// the leading digits of real keys pile into a few bins.  Every lane of the
+// warp must call it.
+__device__ __forceinline__ void hist_add_warp(uint32_t* h, uint32_t bin, bool valid) {
+  const uint32_t active = __ballot_sync(0xffffffffu, valid);
+  if (valid) {
+    const uint32_t peers = __match_any_sync(active, bin);
+    if ((threadIdx.x & 31) == (uint32_t)(__ffs(peers) - 1)) atomicAdd(&h[bin], (uint32_t)__popc(peers));
+  }
+}
+
+// A CTA's keys are read four at a time: key4(g) returns keys 4g..4g+3.
+// Entries at or beyond `count` are ignored, but key4 must be safe to call for
+// every g < ceil(count / 4).
+//
+// cluster_radix_select finds the cut.  Keys are below 2^key_bits (key_bits a
+// multiple of 8, 8..32), so leading all-zero digits are skipped.  Every CTA of
+// the cluster must call it with the same `want` and `key_bits`, and `want`
+// must not exceed the cluster's key count.  Each pass: a warp-aggregated
+// shared-memory histogram, one remote add of every nonzero bin into every
+// CTA's cluster-wide histogram, one cluster barrier, then a warp scan of the
+// local copy (every CTA finds the same bucket).
+template <typename Key4>
+__device__ RadixCut cluster_radix_select(Key4 key4, uint32_t count, uint32_t want, uint32_t key_bits,
                                          RadixSmem* sm, uint32_t nrank) {
   uint32_t prefix = 0, mask = 0, remaining = want;
-  uint32_t shift = 32;
-  const uint32_t tid = threadIdx.x, lane = tid & 31;
-  for (int pass = 0; pass < 4; ++pass) {
+  uint32_t shift = key_bits;
+  const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t ngroups = (count + 3) / 4;
+  uint32_t acc_above = 0;                          // kept by warp 1
+  for (int pass = 0;; ++pass) {
     shift -= 8;
-    uint32_t* h = sm->hist[pass & 1];
-    for (uint32_t b = tid; b < kRadixBins; b += kThreads) h[b] = 0;
+    uint32_t* tot = sm->total[pass & 1];
+    for (uint32_t b = tid; b < kRadixBins; b += kThreads) {
+      sm->hist[b] = 0;
+      sm->total[(pass + 1) & 1][b] = 0;     // added into by the next pass, after the barrier below
+    }
     __syncthreads();
-    for (uint32_t i = tid; i < count; i += kThreads) {
-      const uint32_t key = key_at(i);
-      if ((key & mask) == prefix) atomicAdd(&h[(key >> shift) & 0xffu], 1u);
+    for (uint32_t g0 = 0; g0 < ngroups; g0 += kThreads) {
+      const uint32_t g = g0 + tid;
+      const uint4 kk = g < ngroups ? key4(g) : make_uint4(0, 0, 0, 0);
+      const uint32_t kv[4] = {kk.x, kk.y, kk.z, kk.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const bool valid = g < ngroups && 4 * g + e < count && (kv[e] & mask) == prefix;
+        hist_add_warp(sm->hist, (kv[e] >> shift) & 0xffu, valid);
+      }
+    }
+    __syncthreads();
+    for (uint32_t i = tid; i < kRadixBins * nrank; i += kThreads) {
+      const uint32_t v = sm->hist[i & (kRadixBins - 1)];
+      if (v) dsmem_red_add_u32(dsmem_addr(&tot[i & (kRadixBins - 1)], i / kRadixBins), v);
     }
     cluster_sync();
-    if (tid < kRadixBins) {
-      uint32_t s = 0;
-      for (uint32_t r = 0; r < nrank; ++r) s += dsmem_ld_u32(dsmem_addr(&h[tid], r));
-      sm->total[tid] = s;
-    }
-    __syncthreads();
-    if (tid < 32) {
+    if (warp == 0) {
       // lane l covers bins 255-8l down to 248-8l (largest digits first)
       uint32_t c[8], sum = 0;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        c[e] = sm->total[255 - 8 * lane - e];
+        c[e] = tot[255 - 8 * lane - e];
         sum += c[e];
       }
       uint32_t incl = sum;
@@ -180,13 +277,136 @@ __device__ RadixCut cluster_radix_select(KeyAt key_at, uint32_t count, uint32_t 
     }
     __syncthreads();
     const uint32_t bucket = sm->cut[0], above = sm->cut[1], inbucket = sm->cut[2];
-    __syncthreads();
     remaining -= above;
     prefix |= bucket << shift;
     mask |= 0xffu << shift;
-    if (remaining == inbucket) break;   // the whole bucket is selected
+    const bool done = remaining == inbucket || shift == 0;
+    if (warp == 1) {
+      // this CTA's keys that matched the prefix and fell in a higher bucket
+      uint32_t part = 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const uint32_t b = 8 * lane + e;
+        part += b > bucket ? sm->hist[b] : 0u;
+      }
+#pragma unroll
+      for (int d = 16; d > 0; d >>= 1) part += __shfl_xor_sync(0xffffffffu, part, d);
+      acc_above += part;
+      if (done && lane == 0) {
+        sm->local[0] = acc_above;
+        sm->local[1] = sm->hist[bucket];
+      }
+    }
+    __syncthreads();
+    if (done) break;
   }
-  return RadixCut{prefix, shift, remaining};
+  return RadixCut{prefix, shift, remaining, sm->local[0], sm->local[1]};
+}
+
+// Selected-before and at-cut-before counts of CTA `rank`, from every CTA's
+// published (above, at) counts in columns col, col+1 and the cut's `need`.
+__device__ __forceinline__ void cut_offsets(const uint32_t (*table)[4], uint32_t col, uint32_t rank,
+                                            uint32_t need, uint32_t* sel_before, uint32_t* at_before) {
+  uint32_t s = 0, e = 0;
+  for (uint32_t q = 0; q < rank; ++q) {
+    const uint32_t a = table[q][col], c = table[q][col + 1];
+    const uint32_t left = need > e ? need - e : 0u;
+    s += a + (c < left ? c : left);
+    e += c;
+  }
+  *sel_before = s;
+  *at_before = e;
+}
+
+// Ordered compaction after a cut: visits this CTA's keys in index order and
+// calls emit(i, out) for each selected key i, with `out` its index in the
+// cluster-wide selection.  sel_before / at_before: selected and at-cut keys
+// of lower-ranked CTAs.  Four keys per thread per tile; one block barrier per
+// tile (the two scratch buffers alternate).
+template <typename Key4, typename Emit>
+__device__ void cluster_compact(Key4 key4, uint32_t count, const RadixCut& cut, uint32_t sel_before,
+                                uint32_t at_before, uint32_t (*scratch)[2 * kWarps + 2], Emit emit) {
+  static_assert(kWarps == 32, "one lane per warp of the CTA");
+  const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t ngroups = (count + 3) / 4;
+  const uint32_t shift = cut.shift, top = cut.prefix >> shift, need = cut.need;
+  uint32_t run_sel = 0, run_at = 0, parity = 0;
+  for (uint32_t g0 = 0; g0 < ngroups; g0 += kThreads, parity ^= 1u) {
+    const uint32_t g = g0 + tid;
+    const uint4 kk = g < ngroups ? key4(g) : make_uint4(0, 0, 0, 0);
+    const uint32_t kv[4] = {kk.x, kk.y, kk.z, kk.w};
+    uint32_t amask = 0, emask = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (g < ngroups && 4 * g + e < count) {
+        const uint32_t v = kv[e] >> shift;
+        amask |= (uint32_t)(v > top) << e;
+        emask |= (uint32_t)(v == top) << e;
+      }
+    }
+    const uint32_t a = __popc(amask), e_ = __popc(emask);
+    uint32_t a_incl = a, e_incl = e_;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const uint32_t oa = __shfl_up_sync(0xffffffffu, a_incl, d);
+      const uint32_t oe = __shfl_up_sync(0xffffffffu, e_incl, d);
+      if (lane >= (uint32_t)d) {
+        a_incl += oa;
+        e_incl += oe;
+      }
+    }
+    uint32_t* sc = scratch[parity];
+    if (lane == 31) {
+      sc[2 * warp] = a_incl;
+      sc[2 * warp + 1] = e_incl;
+    }
+    __syncthreads();
+    const uint32_t used = at_before + run_at;
+    const uint32_t left = need > used ? need - used : 0u;   // at-cut keys still to take
+    // lane l works on warp l's totals
+    const uint32_t A_l = sc[2 * lane], E_l = sc[2 * lane + 1];
+    uint32_t E_incl = E_l;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const uint32_t o = __shfl_up_sync(0xffffffffu, E_incl, d);
+      if (lane >= (uint32_t)d) E_incl += o;
+    }
+    const uint32_t E_excl = E_incl - E_l;
+    const uint32_t left_l = left > E_excl ? left - E_excl : 0u;
+    const uint32_t S_l = A_l + (E_l < left_l ? E_l : left_l);
+    uint32_t S_incl = S_l;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const uint32_t o = __shfl_up_sync(0xffffffffu, S_incl, d);
+      if (lane >= (uint32_t)d) S_incl += o;
+    }
+    const uint32_t Eoff = __shfl_sync(0xffffffffu, E_excl, warp);
+    const uint32_t Soff = __shfl_sync(0xffffffffu, S_incl - S_l, warp);
+    const uint32_t tile_at = __shfl_sync(0xffffffffu, E_incl, 31);
+    const uint32_t tile_sel = __shfl_sync(0xffffffffu, S_incl, 31);
+    const uint32_t e_before = Eoff + e_incl - e_;
+    uint32_t take_at = left > e_before ? left - e_before : 0u;
+    take_at = take_at < e_ ? take_at : e_;
+    const uint32_t s = a + take_at;
+    uint32_t s_incl = s;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const uint32_t o = __shfl_up_sync(0xffffffffu, s_incl, d);
+      if (lane >= (uint32_t)d) s_incl += o;
+    }
+    uint32_t out = sel_before + run_sel + Soff + s_incl - s;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if ((amask >> e) & 1u) {
+        emit(4 * g + e, out++);
+      } else if (((emask >> e) & 1u) && take_at) {
+        emit(4 * g + e, out++);
+        --take_at;
+      }
+    }
+    run_sel += tile_sel;
+    run_at += tile_at;
+  }
 }
 
 // ------------------------------------------------------------------ keys

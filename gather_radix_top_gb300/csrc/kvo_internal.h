@@ -7,7 +7,7 @@
 
 #include <cuda_runtime.h>
 
-#include "../../include/kvo.h"
+#include "kvo.h"
 
 namespace kvo {
 

@@ -8,12 +8,14 @@
 // One thread-block cluster does the whole selection in a single launch:
 //   1. each CTA owns a contiguous range of positions and keeps its keys in
 //      shared memory when they fit (else re-reads the scores each pass);
-//   2. an MSB-first 8-bit radix select finds the cut; each pass builds
-//      per-CTA histograms, and every CTA sums all of them over distributed
-//      shared memory (one cluster barrier per pass);
+//   2. an MSB-first 8-bit radix select finds the cut; each pass builds a
+//      warp-aggregated per-CTA histogram and adds its nonzero bins into every
+//      CTA's cluster-wide histogram over distributed shared memory (one
+//      cluster barrier per pass);
 //   3. an ordered compaction writes the chosen positions in ascending order:
-//      per-CTA counts are exchanged over DSMEM, then each CTA scans its range
-//      tile by tile with warp ballots.
+//      per-CTA counts (taken from the radix histograms) are published over
+//      DSMEM, then each CTA walks its range four keys per thread, one block
+//      barrier per 4,096 keys.
 // Ties at the cut go to the lowest positions because the compaction takes
 // equal keys in position order.
 #include <cstdint>
@@ -25,16 +27,11 @@ namespace kvo {
 
 namespace {
 
-constexpr uint32_t kTopkStaticSmem = 4096;                 // headroom for static smem
+constexpr uint32_t kTopkStaticSmem = 6144;                 // headroom for static smem
 constexpr uint32_t kTopkMaxDynSmem = 227 * 1024 - kTopkStaticSmem;
 
-__device__ __forceinline__ void range_of(uint32_t n, uint32_t r, uint32_t C, uint32_t* lo,
-                                         uint32_t* hi) {
-  // chunk boundaries on multiples of 4 positions (16-byte aligned scores)
-  const uint32_t chunk = ((n + C - 1) / C + 3u) & ~3u;
-  const uint64_t a = (uint64_t)chunk * r;
-  *lo = a < n ? (uint32_t)a : n;
-  *hi = (a + chunk) < n ? (uint32_t)(a + chunk) : n;
+__host__ __device__ __forceinline__ uint32_t topk_chunk(uint32_t n, uint32_t C) {
+  return ((n + C - 1) / C + 3u) & ~3u;   // multiples of 4 positions: 16-byte aligned slices
 }
 
 template <bool kResident>
@@ -42,84 +39,52 @@ __global__ void __launch_bounds__(kThreads, 1)
     topk_kernel(const float* __restrict__ scores, uint32_t n, uint32_t k, int32_t* __restrict__ idx) {
   extern __shared__ __align__(16) uint8_t dyn_smem[];
   __shared__ RadixSmem rsm;
-  __shared__ uint32_t scratch[kWarps + 1];
-  __shared__ uint32_t counts[2];          // this CTA's (above-cut, at-cut) counts, read remotely
-  __shared__ uint32_t offsets[2];         // (selected before this CTA, at-cut before this CTA)
+  __shared__ uint32_t scratch[2][2 * kWarps + 2];
+  __shared__ uint32_t table[kMaxCluster][4];
 
   const uint32_t tid = threadIdx.x;
   const uint32_t r = cluster_rank(), C = cluster_size();
-  uint32_t lo, hi;
-  range_of(n, r, C, &lo, &hi);
+  const uint32_t chunk = topk_chunk(n, C);
+  const uint64_t lo64 = (uint64_t)chunk * r;
+  const uint32_t lo = lo64 < n ? (uint32_t)lo64 : n;
+  const uint32_t hi = (lo64 + chunk) < n ? (uint32_t)(lo64 + chunk) : n;
   const uint32_t cnt = hi - lo;
   uint32_t* keys = reinterpret_cast<uint32_t*>(dyn_smem);
   const float* src = scores + lo;
+  const bool vec = ((reinterpret_cast<uintptr_t>(src) & 15u) == 0);
 
-  if (kResident) {
-    const bool vec = ((reinterpret_cast<uintptr_t>(src) & 15u) == 0);
-    const uint32_t nvec = vec ? cnt / 4 : 0;
-    const float4* src4 = reinterpret_cast<const float4*>(src);
-    for (uint32_t i = tid; i < nvec; i += kThreads) {
-      const float4 f = __ldg(src4 + i);
-      reinterpret_cast<uint4*>(keys)[i] =
-          make_uint4(score_key(f.x), score_key(f.y), score_key(f.z), score_key(f.w));
+  // keys 4g..4g+3 of this CTA's slice, straight from the scores
+  auto load4 = [&](uint32_t g) -> uint4 {
+    const uint32_t i = 4 * g;
+    if (vec && i + 3 < cnt) {
+      const float4 f = __ldg(reinterpret_cast<const float4*>(src) + g);
+      return make_uint4(score_key(f.x), score_key(f.y), score_key(f.z), score_key(f.w));
     }
-    for (uint32_t i = nvec * 4 + tid; i < cnt; i += kThreads) keys[i] = score_key(__ldg(src + i));
-    __syncthreads();
-  }
-  auto key_at = [&](uint32_t i) -> uint32_t {
-    if (kResident) return keys[i];
-    return score_key(__ldg(src + i));
+    uint32_t v[4] = {0, 0, 0, 0};
+    for (uint32_t e = 0; e < 4; ++e)
+      if (i + e < cnt) v[e] = score_key(__ldg(src + i + e));
+    return make_uint4(v[0], v[1], v[2], v[3]);
   };
 
-  const RadixCut cut = cluster_radix_select(key_at, cnt, k, &rsm, C);
-  const uint32_t shift = cut.shift, top = cut.prefix >> shift, need = cut.need;
+  radix_smem_init(&rsm);
+  if (kResident) {
+    for (uint32_t g = tid; g < (cnt + 3) / 4; g += kThreads) reinterpret_cast<uint4*>(keys)[g] = load4(g);
+  }
+  cluster_sync();                                  // histograms zeroed everywhere, keys in place
+  auto key4 = [&](uint32_t g) -> uint4 {
+    if (kResident) return reinterpret_cast<const uint4*>(keys)[g];
+    return load4(g);
+  };
 
-  uint32_t above = 0, at = 0;
-  for (uint32_t i = tid; i < cnt; i += kThreads) {
-    const uint32_t t = key_at(i) >> shift;
-    above += t > top;
-    at += t == top;
-  }
-  above = block_sum(above, scratch);
-  at = block_sum(at, scratch);
-  if (tid == 0) {
-    counts[0] = above;
-    counts[1] = at;
-  }
-  cluster_sync();
-  if (tid == 0) {
-    uint32_t sel_before = 0, at_before = 0;
-    for (uint32_t q = 0; q < r; ++q) {
-      const uint32_t a = dsmem_ld_u32(dsmem_addr(&counts[0], q));
-      const uint32_t e = dsmem_ld_u32(dsmem_addr(&counts[1], q));
-      const uint32_t left = need > at_before ? need - at_before : 0u;
-      sel_before += a + (e < left ? e : left);
-      at_before += e;
-    }
-    offsets[0] = sel_before;
-    offsets[1] = at_before;
-  }
-  __syncthreads();
-  const uint32_t sel_before = offsets[0], at_before = offsets[1];
-
-  uint32_t run_sel = 0, run_at = 0;
-  for (uint32_t base = 0; base < cnt; base += kThreads) {
-    const uint32_t i = base + tid;
-    const bool valid = i < cnt;
-    const uint32_t t = valid ? key_at(i) >> shift : 0u;
-    const bool is_at = valid && t == top;
-    const bool is_above = valid && t > top;
-    uint32_t tile_at, tile_sel;
-    const uint32_t at_rank = block_flag_scan(is_at, scratch, &tile_at);
-    const bool sel = is_above || (is_at && at_before + run_at + at_rank < need);
-    const uint32_t sel_rank = block_flag_scan(sel, scratch, &tile_sel);
-    const uint32_t out = sel_before + run_sel + sel_rank;
-    if (sel && out < k) idx[out] = (int32_t)(lo + i);
-    run_at += tile_at;
-    run_sel += tile_sel;
-  }
-  // Keep this CTA's shared memory alive until every remote read is done.
-  cluster_sync();
+  const RadixCut cut = cluster_radix_select(key4, cnt, k, 32, &rsm, C);
+  const uint32_t mine[2] = {cut.above, cut.at};
+  cluster_publish(mine, 2, table, r, C);
+  uint32_t sel_before, at_before;
+  cut_offsets(table, 0, r, cut.need, &sel_before, &at_before);
+  cluster_compact(key4, cnt, cut, sel_before, at_before, scratch, [&](uint32_t i, uint32_t out) {
+    if (out < k) idx[out] = (int32_t)(lo + i);
+  });
+  // Every remote access happened before the publish barrier: CTAs may exit.
 }
 
 struct TopkConfig {
@@ -140,16 +105,19 @@ cudaError_t launch_topk(const float* scores, uint32_t n, uint32_t k, int32_t* id
     e = cudaFuncSetAttribute(topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kTopkMaxDynSmem);
     if (e != cudaSuccess) return e;
-    cfg.cluster_res = best_cluster((const void*)topk_kernel<true>, kTopkMaxDynSmem, 16);
-    cfg.cluster_stream = best_cluster((const void*)topk_kernel<false>, 0, 16);
+    cfg.cluster_res = best_cluster((const void*)topk_kernel<true>, kTopkMaxDynSmem, (int)kMaxCluster);
+    cfg.cluster_stream = best_cluster((const void*)topk_kernel<false>, 0, (int)kMaxCluster);
     if (cfg.cluster_res == 0 || cfg.cluster_stream == 0) return cudaErrorInvalidConfiguration;
     cfg.init = true;
   }
   // Resident when one CTA's share of the keys fits in shared memory.
   int C = cfg.cluster_res < max_cluster ? cfg.cluster_res : max_cluster;
-  uint32_t chunk = ((n + C - 1) / C + 3u) & ~3u;
-  bool resident = (uint64_t)chunk * 4u <= kTopkMaxDynSmem;
-  if (!resident) C = cfg.cluster_stream < max_cluster ? cfg.cluster_stream : max_cluster;
+  uint32_t chunk = topk_chunk(n, (uint32_t)C);
+  const bool resident = (uint64_t)chunk * 4u <= kTopkMaxDynSmem;
+  if (!resident) {
+    C = cfg.cluster_stream < max_cluster ? cfg.cluster_stream : max_cluster;
+    chunk = topk_chunk(n, (uint32_t)C);
+  }
 
   cudaLaunchConfig_t lc = {};
   cudaLaunchAttribute attr[1];

@@ -126,6 +126,22 @@ def algorithmic_bytes(w: W.Workload, n_avg: float, stats_delta: dict, resolve_la
             "append_host": ROW * w.appends_per_step, "hits": hits, "misses": misses, "fills": fills}
 
 
+def dram_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch from the committed ncu capture, or None when the
+    kernel's source has changed since the counters were taken."""
+    import hashlib
+    try:
+        prof = json.load(open(os.path.join(ROOT, "profiles", "dram_traffic.json")))
+        ent = prof[workload][kernel]
+        for name, want in ent["source_sha256_16"].items():
+            path = os.path.join(ROOT, "gather_radix_top_gb300", "csrc", name)
+            if hashlib.sha256(open(path, "rb").read()).hexdigest()[:16] != want:
+                return None
+        return ent["bytes"]
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 # ------------------------------------------------------------- GPU arm
 class GpuWorkload:
     """Device-resident inputs and a context for one replica of a workload."""
@@ -448,12 +464,7 @@ def main():
     dominant = max(kern_tot, key=kern_tot.get)
     per_launch_bytes = {"resolve": ab["resolve_hbm"], "select": ab["select_hbm"], "append": 2 * ROW}[dominant]
     achieved = per_launch_bytes / (kern_avg[dominant] * 1e-3) / 1e9
-    traffic = None
-    try:
-        prof = json.load(open(os.path.join(ROOT, "profiles", "dram_traffic.json")))
-        traffic = prof.get(w.name, {}).get(dominant)
-    except Exception:
-        pass
+    traffic = dram_traffic(w.name, dominant)
     host_gbs = ab["resolve_host"] / (kern_avg.get("resolve", 1e9) * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "rows/s", "n_gpus": world, "steps": args.steps,

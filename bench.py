@@ -146,7 +146,8 @@ def dram_traffic(workload: str, kernel: str):
 class GpuWorkload:
     """Device-resident inputs and a context for one replica of a workload."""
 
-    def __init__(self, w: W.Workload, layer_base: int, steps: int, host_inputs: bool = False):
+    def __init__(self, w: W.Workload, layer_base: int, steps: int, host_inputs: bool = False,
+                 fused: bool = True):
         import torch
         from gather_radix_top_gb300 import kvo
         self.torch, self.kvo, self.w = torch, kvo, w
@@ -183,6 +184,10 @@ class GpuWorkload:
         self.out_host = torch.empty((w.k, ROW), dtype=torch.uint8).pin_memory() if host_inputs else None
         self.idx_hist = torch.zeros((steps, w.k), dtype=torch.int32, device=dev)
         self.launches = 0
+        self.fused = fused
+        # host-input runs stage each step's new rows on the device (H2D inside the step)
+        self.new_stage = (torch.empty((w.layers, max(a, 1), ROW), dtype=torch.uint8, device=dev)
+                          if host_inputs and a else None)
 
     def scores_for(self, l, s):
         """The step's scores on the device with the carry boost applied (not timed)."""
@@ -218,12 +223,22 @@ class GpuWorkload:
 
         if ev:
             ev[0].record()
+        a = w.appends_per_step
         for l in range(w.layers):
-            if w.appends_per_step:
-                src = (self.new_rows_host if self.host_inputs else self.new_rows)[l, s * w.appends_per_step:
-                                                                                  (s + 1) * w.appends_per_step]
-                rec("append", lambda: ctx.append_rows(l, src))
+            src = None
+            if a:
+                if self.host_inputs:
+                    src = self.new_stage[l, :a]
+                    src.copy_(self.new_rows_host[l, s * a:(s + 1) * a], non_blocking=True)
+                else:
+                    src = self.new_rows[l, s * a:(s + 1) * a]
             src_l = w.source_layer(l)
+            if self.fused and l in self.sel:
+                rec("step", lambda: ctx.decode_step(l, src, sc[l], w.k, self.idx[l][s & 1], self.out_rows,
+                                                    self.out_bf16))
+                continue
+            if a:
+                rec("append", lambda: ctx.append_rows(l, src))
             if l in self.sel:
                 rec("select", lambda: ctx.select_topk(sc[l], w.k, self.idx[l][s & 1]))
             rec("resolve", lambda: ctx.resolve_gather(l, self.idx[src_l][s & 1], self.out_rows, self.out_bf16))
@@ -267,7 +282,7 @@ def run_gpu_arm(args, w, rank, world):
     build.build()
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
     steps = args.warmup + args.steps
-    wl = GpuWorkload(w, layer_base=rank * w.layers, steps=steps)
+    wl = GpuWorkload(w, layer_base=rank * w.layers, steps=steps, fused=not args.separate)
     flush = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
     dist = world > 1
     if dist:
@@ -324,7 +339,7 @@ def run_e2e(args, w):
     copies inside each step's events."""
     import torch
     steps = args.warmup + args.steps
-    wl = GpuWorkload(w, layer_base=0, steps=steps, host_inputs=True)
+    wl = GpuWorkload(w, layer_base=0, steps=steps, host_inputs=True, fused=not args.separate)
     flush = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
     evs = []
     for s in range(steps):
@@ -402,6 +417,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(W.WORKLOADS), default="50k_single_layer")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--separate", action="store_true",
+                    help="time kvo_append_rows + kvo_select_topk + kvo_resolve_gather instead of kvo_decode_step")
     args = ap.parse_args()
 
     w = W.WORKLOADS[args.workload]
@@ -414,6 +431,7 @@ def main():
     config = {"workload": w.name, "layers": w.layers, "history": w.n0, "hot_rows": w.hot_rows, "k": w.k,
               "appends_per_step": w.appends_per_step, "select_every": w.select_every,
               "bf16_output": w.bf16, "parallelism": f"replicas{world}",
+              "calls": "kvo_append_rows+kvo_select_topk+kvo_resolve_gather" if args.separate else "kvo_decode_step",
               "l2": "flushed between steps (1 GiB memset, outside the step events)"}
 
     if args.impl == "reference":
@@ -456,16 +474,18 @@ def main():
     total_rows = args.steps * w.layers * w.k * world
     value = total_rows / g["total_s"]
     nmean = float(np.mean([w.n_at(s) for s in range(args.warmup, args.warmup + args.steps)]))
-    nres = len(g["kern_ms"].get("resolve", [])) or 1
+    nres = (len(g["kern_ms"].get("resolve", [])) + len(g["kern_ms"].get("step", []))) or 1
     nsel = len(g["kern_ms"].get("select", [])) or 1
     ab = algorithmic_bytes(w, nmean, g["delta"], nres, nsel)
     kern_avg = {kind: float(np.mean(v)) for kind, v in g["kern_ms"].items()}
     kern_tot = {kind: float(np.sum(v)) for kind, v in g["kern_ms"].items()}
     dominant = max(kern_tot, key=kern_tot.get)
-    per_launch_bytes = {"resolve": ab["resolve_hbm"], "select": ab["select_hbm"], "append": 2 * ROW}[dominant]
+    per_launch_bytes = {"resolve": ab["resolve_hbm"], "select": ab["select_hbm"], "append": 2 * ROW * w.appends_per_step,
+                        "step": ab["resolve_hbm"] + ab["select_hbm"] + ROW * w.appends_per_step}[dominant]
     achieved = per_launch_bytes / (kern_avg[dominant] * 1e-3) / 1e9
     traffic = dram_traffic(w.name, dominant)
-    host_gbs = ab["resolve_host"] / (kern_avg.get("resolve", 1e9) * 1e-3) / 1e9
+    t_resolve = kern_avg.get("resolve", kern_avg.get("step", 1e9))
+    host_gbs = ab["resolve_host"] / (t_resolve * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "rows/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(1e3 * g["total_s"] / args.steps, 4),

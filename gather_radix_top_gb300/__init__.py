@@ -4,7 +4,7 @@ The hot path (top-K selection, hot-cache resolve, LRU victims, gather and
 bf16 dequant) runs in the CUDA kernels of ``libkvo.so`` behind the C ABI in
 ``include/kvo.h``; ``gather_radix_top_gb300.kvo`` is its Python binding.
 """
-from .kvo import (Context, KvoError, kvo_append_rows, kvo_create, kvo_debug_dump_layer,  # noqa: F401
+from .kvo import (Context, KvoError, kvo_append_rows, kvo_create, kvo_debug_dump_layer, kvo_decode_step,  # noqa: F401
                   kvo_debug_evictions, kvo_debug_record_evictions, kvo_destroy, kvo_get_stats,
                   kvo_history_length, kvo_probe_host_read, kvo_resolve_gather, kvo_select_topk,
                   kvo_sync, lib, library_path)

@@ -240,6 +240,27 @@ kvo_status kvo_resolve_gather(kvo_ctx* ctx, int32_t layer, const int32_t* idx, i
   return ok(e) ? KVO_OK : KVO_ECUDA;
 }
 
+kvo_status kvo_decode_step(kvo_ctx* ctx, int32_t layer, const void* new_rows, int64_t r,
+                           const float* scores, int64_t n, int32_t k, int32_t* idx,
+                           void* out_rows, uint16_t* out_bf16, void* stream) {
+  if (!ctx || layer < 0 || layer >= ctx->layers || r < 0 || !scores || !idx || k < 1 || k > KVO_MAX_K ||
+      n < k || n > INT32_MAX || k > ctx->hot_rows || (!out_rows && !out_bf16))
+    return KVO_EINVAL;
+  if ((out_rows && !aligned16(out_rows)) || (out_bf16 && !aligned16(out_bf16))) return KVO_EINVAL;
+  if (r > 0 && (!new_rows || !aligned16(new_rows) || !is_device_pointer(new_rows))) return KVO_EINVAL;
+  const int64_t start = ctx->length[layer];
+  if (start + r > ctx->history_cap) return KVO_EINVAL;
+  kvo::LayerView v = ctx->views[layer];
+  v.evlog = ctx->evlog ? ctx->evlog + kEvlogStride * layer : nullptr;
+  const cudaError_t e = kvo::launch_decode_step(v, r ? new_rows : nullptr, (uint32_t)r, (uint32_t)start, scores,
+                                                (uint32_t)n, (uint32_t)k, idx, static_cast<uint8_t*>(out_rows),
+                                                out_bf16, ctx->status, ctx->max_cluster,
+                                                static_cast<cudaStream_t>(stream));
+  if (!ok(e)) return KVO_ECUDA;
+  ctx->length[layer] = start + r;
+  return KVO_OK;
+}
+
 kvo_status kvo_sync(kvo_ctx* ctx, void* stream) {
   if (!ctx) return KVO_EINVAL;
   if (!ok(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)))) return KVO_ECUDA;

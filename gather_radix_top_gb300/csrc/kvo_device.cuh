@@ -178,7 +178,7 @@ struct RadixCut {
   uint32_t at;
 };
 
-struct RadixSmem {
+struct __align__(16) RadixSmem {
   uint32_t hist[kRadixBins];        // this CTA's histogram of the current pass
   uint32_t total[2][kRadixBins];    // cluster-wide histograms, added into by every CTA
   uint32_t cut[4];                  // bucket, count above it, bucket count
@@ -247,13 +247,14 @@ __device__ RadixCut cluster_radix_select(Key4 key4, uint32_t count, uint32_t wan
     }
     cluster_sync();
     if (warp == 0) {
-      // lane l covers bins 255-8l down to 248-8l (largest digits first)
-      uint32_t c[8], sum = 0;
+      // lane l covers bins 255-8l down to 248-8l (largest digits first):
+      // eight contiguous words, read as two 16-byte loads
+      const uint4 lo = reinterpret_cast<const uint4*>(tot)[(248 - 8 * lane) / 4];
+      const uint4 hi = reinterpret_cast<const uint4*>(tot)[(248 - 8 * lane) / 4 + 1];
+      const uint32_t c[8] = {hi.w, hi.z, hi.y, hi.x, lo.w, lo.z, lo.y, lo.x};
+      uint32_t sum = 0;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        c[e] = tot[255 - 8 * lane - e];
-        sum += c[e];
-      }
+      for (int e = 0; e < 8; ++e) sum += c[e];
       uint32_t incl = sum;
 #pragma unroll
       for (int d = 1; d < 32; d <<= 1) {
@@ -283,12 +284,12 @@ __device__ RadixCut cluster_radix_select(Key4 key4, uint32_t count, uint32_t wan
     const bool done = remaining == inbucket || shift == 0;
     if (warp == 1) {
       // this CTA's keys that matched the prefix and fell in a higher bucket
+      const uint4 h0 = reinterpret_cast<const uint4*>(sm->hist)[2 * lane];
+      const uint4 h1 = reinterpret_cast<const uint4*>(sm->hist)[2 * lane + 1];
+      const uint32_t hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
       uint32_t part = 0;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const uint32_t b = 8 * lane + e;
-        part += b > bucket ? sm->hist[b] : 0u;
-      }
+      for (int e = 0; e < 8; ++e) part += (8 * lane + e) > bucket ? hv[e] : 0u;
 #pragma unroll
       for (int d = 16; d > 0; d >>= 1) part += __shfl_xor_sync(0xffffffffu, part, d);
       acc_above += part;

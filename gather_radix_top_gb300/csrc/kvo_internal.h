@@ -36,6 +36,9 @@ cudaError_t launch_topk(const float* scores, uint32_t n, uint32_t k, int32_t* id
 cudaError_t launch_resolve(const LayerView& L, const int32_t* idx, uint32_t k, uint8_t* out_rows,
                            uint16_t* out_bf16, uint32_t* status, int max_cluster,
                            cudaStream_t stream);
+cudaError_t launch_decode_step(const LayerView& L, const void* new_rows, uint32_t r, uint32_t old_len,
+                               const float* scores, uint32_t n, uint32_t k, int32_t* idx, uint8_t* out_rows,
+                               uint16_t* out_bf16, uint32_t* status, int max_cluster, cudaStream_t stream);
 cudaError_t launch_append(const void* src_dev, uint8_t* hist_dev_dst, uint64_t bytes,
                           uint32_t* counters, uint32_t new_len, cudaStream_t stream);
 cudaError_t launch_probe(const void* src, uint64_t bytes, void* sink, cudaStream_t stream);

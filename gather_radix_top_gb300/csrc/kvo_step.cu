@@ -1,0 +1,138 @@
+// Fused decode step of one layer (kvo_decode_step): append the new rows,
+// select the top-K positions and resolve + gather them, in one cluster
+// launch.
+//
+// "From 1M Total to 15+ x 1M Contexts: GLM-5.3 KV Cache Offloading",
+// "Decision three: let the GPU manage the hot cache directly": the CPU stays
+// out of the per-selection loop; selection, lookup and gather run on the GPU
+// back to back.  Fusing them also removes two kernel launches and the trip of
+// the selection through global memory: the top-K compaction hands each
+// selected position straight to the CTA that resolves it, over distributed
+// shared memory.
+#include <cstdint>
+
+#include "kvo_internal.h"
+#include "kvo_resolve_body.cuh"
+#include "kvo_topk_body.cuh"
+
+namespace kvo {
+
+namespace {
+
+using namespace resolve_detail;
+using namespace topk_detail;
+
+struct StepArgs {
+  ResolveArgs R;              // fused = 1; R.len = history length after the append
+  const float* scores;
+  uint32_t n;
+  int32_t* idx;               // the selection, also returned to the caller
+  const uint4* new_rows;      // r rows appended in this step (device memory)
+  uint4* hist_dst;            // device address of history row `old length`
+  uint32_t r;
+  uint32_t topk_bytes;        // dynamic shared memory used by the top-K phase
+};
+
+template <bool kResident>
+__global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const StepArgs s) {
+  extern __shared__ __align__(16) uint8_t dyn_smem[];
+  const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t rank = cluster_rank(), C = cluster_size();
+  constexpr uint32_t kVec = KVO_ROW_BYTES / 16;
+
+  // append: one warp per new row, spread over the cluster
+  for (uint32_t i = rank * kWarps + warp; i < s.r; i += C * kWarps) {
+    s.hist_dst[(size_t)i * kVec + lane] = s.new_rows[(size_t)i * kVec + lane];
+    if (lane < kVec - 32) s.hist_dst[(size_t)i * kVec + 32 + lane] = s.new_rows[(size_t)i * kVec + 32 + lane];
+  }
+
+  uint8_t* rdyn = dyn_smem + s.topk_bytes;
+  const SmemLayout lay = smem_layout(s.R.k, s.R.kchunk, s.R.hchunk, s.R.sort_len);
+  int32_t* sel = reinterpret_cast<int32_t*>(rdyn + lay.sel);
+  const uint32_t kchunk = s.R.kchunk;
+  topk_body<kResident>(s.scores, s.n, s.R.k, dyn_smem, [&](uint32_t pos, uint32_t out) {
+    s.idx[out] = (int32_t)pos;
+    const uint32_t owner = out / kchunk;
+    dsmem_st_u32(dsmem_addr(&sel[out - owner * kchunk], owner), pos);
+  });
+  cluster_sync();                                  // every selected position delivered
+  resolve_body(s.R, rdyn);
+  if (rank == 0 && tid == 0) s.R.L.counters[1] = s.R.len;
+}
+
+struct StepConfig {
+  bool init = false;
+  int cluster = 0;
+};
+StepConfig g_step[64];
+
+constexpr size_t kStepMaxDynSmem = 216 * 1024;
+
+}  // namespace
+
+cudaError_t launch_decode_step(const LayerView& L, const void* new_rows, uint32_t r, uint32_t old_len,
+                               const float* scores, uint32_t n, uint32_t k, int32_t* idx, uint8_t* out_rows,
+                               uint16_t* out_bf16, uint32_t* status, int max_cluster, cudaStream_t stream) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  StepConfig& cfg = g_step[dev & 63];
+  if (!cfg.init) {
+    e = cudaFuncSetAttribute(decode_step_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kStepMaxDynSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(decode_step_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kStepMaxDynSmem);
+    if (e != cudaSuccess) return e;
+    const int c1 = best_cluster((const void*)decode_step_kernel<true>, kStepMaxDynSmem, (int)kMaxCluster);
+    const int c2 = best_cluster((const void*)decode_step_kernel<false>, kStepMaxDynSmem, (int)kMaxCluster);
+    cfg.cluster = c1 < c2 ? c1 : c2;
+    if (cfg.cluster == 0) return cudaErrorInvalidConfiguration;
+    cfg.init = true;
+  }
+  const uint32_t C = (uint32_t)(cfg.cluster < max_cluster ? cfg.cluster : max_cluster);
+  StepArgs s;
+  ResolveArgs& a = s.R;
+  a.L = L;
+  a.idx = idx;
+  a.out_rows = out_rows;
+  a.out_bf16 = out_bf16;
+  a.status = status;
+  a.k = k;
+  a.kchunk = (k + C - 1) / C;
+  a.hchunk = ((L.hot_rows + C - 1) / C + 3u) & ~3u;
+  a.sort_len = 1;
+  while (a.sort_len < k) a.sort_len <<= 1;
+  a.fused = 1;
+  a.len = old_len + r;
+  a.fresh = r ? static_cast<const uint8_t*>(new_rows) : nullptr;
+  a.fresh_from = old_len;
+  s.scores = scores;
+  s.n = n;
+  s.idx = idx;
+  s.new_rows = static_cast<const uint4*>(new_rows);
+  s.hist_dst = reinterpret_cast<uint4*>(const_cast<uint8_t*>(L.hist) + (size_t)old_len * KVO_ROW_BYTES);
+  s.r = r;
+  const SmemLayout lay = smem_layout(k, a.kchunk, a.hchunk, a.sort_len);
+  const size_t topk_res = ((size_t)topk_chunk(n, C) * 4u + 15u) & ~(size_t)15u;
+  if (lay.total > kStepMaxDynSmem) return cudaErrorInvalidValue;
+  const bool resident = topk_res + lay.total <= kStepMaxDynSmem;
+  s.topk_bytes = resident ? (uint32_t)topk_res : 0u;
+
+  cudaLaunchConfig_t lc = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  lc.gridDim = dim3(C, 1, 1);
+  lc.blockDim = dim3(kThreads, 1, 1);
+  lc.dynamicSmemBytes = s.topk_bytes + lay.total;
+  lc.stream = stream;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  if (resident) return cudaLaunchKernelEx(&lc, decode_step_kernel<true>, s);
+  return cudaLaunchKernelEx(&lc, decode_step_kernel<false>, s);
+}
+
+}  // namespace kvo

@@ -22,7 +22,7 @@ KVO_OK, KVO_EINVAL, KVO_ENOMEM, KVO_ECUDA, KVO_ERANGE, KVO_EBUSY, KVO_ETIMEDOUT,
 
 EXPORTED = [
     "kvo_status_string", "kvo_create", "kvo_destroy", "kvo_append_rows", "kvo_select_topk",
-    "kvo_resolve_gather", "kvo_sync", "kvo_get_stats", "kvo_history_length",
+    "kvo_resolve_gather", "kvo_decode_step", "kvo_sync", "kvo_get_stats", "kvo_history_length",
     "kvo_debug_dump_layer", "kvo_debug_record_evictions", "kvo_debug_evictions",
     "kvo_probe_host_read",
 ]
@@ -65,6 +65,7 @@ def lib() -> ctypes.CDLL:
         "kvo_append_rows": (ctypes.c_int, [_vp, _i32, _vp, _i64, _vp]),
         "kvo_select_topk": (ctypes.c_int, [_vp, _vp, _i64, _i32, _vp, _vp]),
         "kvo_resolve_gather": (ctypes.c_int, [_vp, _i32, _vp, _i32, _vp, _vp, _vp]),
+        "kvo_decode_step": (ctypes.c_int, [_vp, _i32, _vp, _i64, _vp, _i64, _i32, _vp, _vp, _vp, _vp]),
         "kvo_sync": (ctypes.c_int, [_vp, _vp]),
         "kvo_get_stats": (ctypes.c_int, [_vp, _i32, ctypes.POINTER(kvo_stats)]),
         "kvo_history_length": (ctypes.c_int, [_vp, _i32, ctypes.POINTER(_i64)]),
@@ -157,6 +158,23 @@ def kvo_resolve_gather(ctx: int, layer: int, idx, out_rows=None, out_bf16=None, 
                                     _stream_ptr(stream)), "kvo_resolve_gather")
 
 
+def kvo_decode_step(ctx: int, layer: int, new_rows, scores, k: int, idx=None, out_rows=None, out_bf16=None,
+                    stream=None):
+    """Append (new_rows: uint8 CUDA tensor [r, 656] or None), select and
+    resolve one layer's decode step in one launch; returns idx."""
+    import torch
+    if idx is None:
+        idx = torch.empty(k, dtype=torch.int32, device=scores.device)
+    if out_bf16 is not None and str(out_bf16.dtype) not in ("torch.bfloat16", "torch.int16"):
+        raise ValueError("out_bf16 must be bfloat16 or int16")
+    r = 0 if new_rows is None else new_rows.numel() // ROW_BYTES
+    _check(lib().kvo_decode_step(ctx, layer, _dev_ptr(new_rows, "torch.uint8"), r,
+                                 _dev_ptr(scores, "torch.float32"), scores.numel(), k,
+                                 _dev_ptr(idx, "torch.int32"), _dev_ptr(out_rows, "torch.uint8"),
+                                 _dev_ptr(out_bf16), _stream_ptr(stream)), "kvo_decode_step")
+    return idx
+
+
 def kvo_sync(ctx: int, stream=None) -> int:
     """Synchronise and return the latched device status (KVO_OK, KVO_ERANGE, ...)."""
     return lib().kvo_sync(ctx, _stream_ptr(stream))
@@ -242,6 +260,9 @@ class Context:
 
     def resolve_gather(self, layer, idx, out_rows=None, out_bf16=None, stream=None):
         kvo_resolve_gather(self.handle, layer, idx, out_rows, out_bf16, stream)
+
+    def decode_step(self, layer, new_rows, scores, k, idx=None, out_rows=None, out_bf16=None, stream=None):
+        return kvo_decode_step(self.handle, layer, new_rows, scores, k, idx, out_rows, out_bf16, stream)
 
     def sync(self, stream=None) -> int:
         return kvo_sync(self.handle, stream)

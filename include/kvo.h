@@ -148,6 +148,23 @@ kvo_status kvo_resolve_gather(kvo_ctx* ctx, int32_t layer, const int32_t* idx, i
                               void* out_rows, uint16_t* out_bf16, void* stream);
 
 /*
+ * kvo_decode_step - one decode step of one layer in a single launch: the
+ * same results as kvo_append_rows(layer, new_rows, r), then
+ * kvo_select_topk(scores, n, k, idx), then kvo_resolve_gather(layer, idx, k,
+ * out_rows, out_bf16), in that stream order ([KVO] "Decision three": the
+ * GPU selects, looks up and gathers with no host round trip).
+ *   new_rows  device uint8[r*656] (16-byte aligned), or NULL with r = 0.
+ *             Host rows are refused: append them with kvo_append_rows.
+ *   scores    device fp32[n]; idx device int32[k] receives the selection
+ *             (ascending positions); outputs as for kvo_resolve_gather.
+ * Errors: KVO_EINVAL for any argument the three calls would refuse, or for
+ * host-memory new_rows.  Nothing is changed or enqueued on an error.
+ */
+kvo_status kvo_decode_step(kvo_ctx* ctx, int32_t layer, const void* new_rows, int64_t r,
+                           const float* scores, int64_t n, int32_t k, int32_t* idx,
+                           void* out_rows, uint16_t* out_bf16, void* stream);
+
+/*
  * kvo_sync - synchronise `stream`, then return and clear the device status
  * word: KVO_OK, or the first latched device error (KVO_ERANGE, ...).
  */

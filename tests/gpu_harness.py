@@ -22,7 +22,7 @@ class GpuLayerRun:
     """One layer of a workload on the GPU, driven step by step."""
 
     def __init__(self, w: W.Workload, layer: int, ctx=None, ctx_layer: int = 0, want_rows=True,
-                 want_bf16=None):
+                 want_bf16=None, fused: bool = False):
         import torch
         from gather_radix_top_gb300 import kvo
         self.torch = torch
@@ -38,18 +38,24 @@ class GpuLayerRun:
         self.out_rows = torch.empty((w.k, O.ROW_BYTES), dtype=torch.uint8, device="cuda") if want_rows else None
         self.out_bf16 = torch.empty((w.k, O.DEQUANT_VALUES), dtype=torch.bfloat16, device="cuda") if bf else None
         self.prev = None
+        self.fused = fused
 
     def step(self, step: int):
         torch = self.torch
         w = self.w
-        for a in range(w.appends_per_step):
-            pos = w.n0 + step * w.appends_per_step + a
-            self.ctx.append_rows(self.cl, self.new_rows[pos - w.n0:pos - w.n0 + 1])   # device rows
+        a = w.appends_per_step
         s = W.apply_carry(W.base_scores(w, self.layer, step), self.prev,
                           W.carry_draw(w, self.layer, step), w.carry_boost)
         scores = torch.from_numpy(s).cuda()
-        idx = self.ctx.select_topk(scores, w.k)
-        self.ctx.resolve_gather(self.cl, idx, self.out_rows, self.out_bf16)
+        if self.fused:
+            new = self.new_rows[step * a:(step + 1) * a] if a else None
+            idx = self.ctx.decode_step(self.cl, new, scores, w.k, out_rows=self.out_rows, out_bf16=self.out_bf16)
+        else:
+            for i in range(a):
+                pos = w.n0 + step * a + i
+                self.ctx.append_rows(self.cl, self.new_rows[pos - w.n0:pos - w.n0 + 1])   # device rows
+            idx = self.ctx.select_topk(scores, w.k)
+            self.ctx.resolve_gather(self.cl, idx, self.out_rows, self.out_bf16)
         idx_h = idx.cpu().numpy()
         self.prev = idx_h
         return idx_h

@@ -240,3 +240,93 @@ def test_argument_errors_change_nothing(kvo):
     d = ctx.dump_layer(0)
     assert d["step"] == 0 and (d["slot2pos"] == -1).all()
     ctx.close()
+
+
+# ------------------------------------------------ fused decode step
+@pytest.mark.parametrize("appends", [0, 2])
+def test_decode_step_tiny_full_parity(kvo, appends):
+    """One launch per step (append + select + resolve) equals the oracle
+    step by step: selections, rows, bf16, eviction order, maps."""
+    w = W.TINY.scaled(appends_per_step=appends)
+    g = GpuLayerRun(w, 0, want_bf16=True, fused=True)
+    o = OracleLayerRun(w, 0, want_bf16=True)
+    g.ctx.record_evictions(True)
+    for step in range(w.steps):
+        np.testing.assert_array_equal(g.step(step), o.step(step))
+        np.testing.assert_array_equal(g.rows(), o.last.rows)
+        np.testing.assert_array_equal(g.bf16(), o.last.bf16)
+        assert g.ctx.evictions(0) == o.last.evictions
+        compare_state(g.ctx, 0, o.st)
+    assert g.ctx.history_length(0) == o.st.length
+    assert g.ctx.sync() == 0
+    g.ctx.close()
+
+
+def test_decode_step_50k_all_steps(kvo):
+    """The benchmark's configuration: 50K single layer, 1,024 fused steps."""
+    w = W.K50
+    g = GpuLayerRun(w, 0, fused=True)
+    o = OracleLayerRun(w, 0)
+    for step in range(w.steps):
+        np.testing.assert_array_equal(g.step(step), o.step(step))
+        if step % 64 == 0 or step == w.steps - 1:
+            np.testing.assert_array_equal(g.rows(), o.last.rows)
+    compare_state(g.ctx, 0, o.st)
+    g.ctx.close()
+
+
+def test_decode_step_1m_sampled(kvo):
+    """1M positions (scores streamed, not resident), bf16 on, fused steps."""
+    w = W.M1.scaled(steps=4)
+    g = GpuLayerRun(w, 5, fused=True)
+    o = OracleLayerRun(w, 5)
+    for step in range(w.steps):
+        np.testing.assert_array_equal(g.step(step), o.step(step))
+        np.testing.assert_array_equal(g.rows(), o.last.rows)
+        np.testing.assert_array_equal(g.bf16(), o.last.bf16)
+    compare_state(g.ctx, 0, o.st, check_hot=False)
+    g.ctx.close()
+
+
+def test_decode_step_selects_rows_appended_in_the_same_step(kvo):
+    """Increasing scores put the rows appended by this very call into the
+    selection: they are misses read from the device copy, and equal the
+    oracle's history rows."""
+    import torch
+    n0, r, k, H = 3000, 40, 64, 128
+    hist = np.random.default_rng(3).integers(0, 256, size=(n0 + 5 * r, O.ROW_BYTES), dtype=np.uint8)
+    ctx = kvo.Context(1, n0 + 5 * r, H)
+    ctx.append_rows(0, hist[:n0])
+    st = O.LayerState(n0 + 5 * r, H)
+    st.append(hist[:n0])
+    out = torch.empty((k, O.ROW_BYTES), dtype=torch.uint8, device="cuda")
+    for step in range(5):
+        lo = n0 + step * r
+        new = torch.from_numpy(hist[lo:lo + r]).cuda()
+        scores = np.arange(lo + r, dtype=np.float32)
+        idx = ctx.decode_step(0, new, torch.from_numpy(scores).cuda(), k, out_rows=out).cpu().numpy()
+        st.append(hist[lo:lo + r])
+        oidx = O.select_topk(scores, k)
+        res = O.resolve_gather(st, oidx)
+        np.testing.assert_array_equal(idx, oidx)
+        np.testing.assert_array_equal(out.cpu().numpy(), res.rows)
+    compare_state(ctx, 0, st)
+    ctx.close()
+
+
+def test_decode_step_rejects_host_rows_and_bad_sizes(kvo):
+    import torch
+    ctx = kvo.Context(1, 100, 16)
+    ctx.append_rows(0, np.zeros((50, O.ROW_BYTES), np.uint8))
+    scores = torch.zeros(50, device="cuda")
+    out = torch.empty((8, O.ROW_BYTES), dtype=torch.uint8, device="cuda")
+    host_rows = torch.zeros((1, O.ROW_BYTES), dtype=torch.uint8)
+    with pytest.raises(ValueError):
+        ctx.decode_step(0, host_rows, scores, 8, out_rows=out)      # binding refuses CPU tensors
+    with pytest.raises(kvo.KvoError):
+        ctx.decode_step(0, None, scores, 17, out_rows=out)          # k > hot_rows
+    with pytest.raises(kvo.KvoError):
+        ctx.decode_step(0, torch.zeros((51, O.ROW_BYTES), dtype=torch.uint8, device="cuda"), scores, 8,
+                        out_rows=out)                               # past history_cap
+    assert ctx.history_length(0) == 50
+    ctx.close()

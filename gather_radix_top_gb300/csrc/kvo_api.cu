@@ -43,6 +43,7 @@ void free_ctx(kvo_ctx* c) {
     cudaFree(v.slot2pos);
     cudaFree(v.last_use);
     cudaFree(v.hot);
+    cudaFree(v.order);
   }
   for (uint8_t* h : c->hist_host) cudaFreeHost(h);
   cudaFree(c->counters);
@@ -154,6 +155,11 @@ kvo_status kvo_create(int32_t layers, int64_t history_cap, int32_t hot_rows, int
               ok(cudaMemset(c->counters, 0, sizeof(uint32_t) * 4 * layers)) &&
               ok(cudaMemset(c->stats, 0, sizeof(unsigned long long) * 8 * layers)) &&
               ok(cudaMemset(c->status, 0, sizeof(uint32_t)));
+  // slot tables padded to whole 16-byte pieces: kernels copy them in 16-byte units
+  const size_t padded_rows = ((size_t)hot_rows + 3) & ~(size_t)3;
+  // every slot starts empty (last_use 0): the LRU order is slot order
+  std::vector<int32_t> iota(padded_rows);
+  for (size_t i = 0; i < padded_rows; ++i) iota[i] = (int32_t)i;
   for (int32_t l = 0; good && l < layers; ++l) {
     kvo::LayerView v = {};
     v.hot_rows = (uint32_t)hot_rows;
@@ -169,14 +175,16 @@ kvo_status kvo_create(int32_t layers, int64_t history_cap, int32_t hot_rows, int
     good = ok(cudaHostGetDevicePointer(&hd, h, 0));
     v.hist = static_cast<const uint8_t*>(hd);
     good = good && ok(cudaMalloc(&v.pos2slot, sizeof(int32_t) * (size_t)history_cap)) &&
-           ok(cudaMalloc(&v.slot2pos, sizeof(int32_t) * (size_t)hot_rows)) &&
-           ok(cudaMalloc(&v.last_use, sizeof(uint32_t) * (size_t)hot_rows)) &&
-           ok(cudaMalloc(&v.hot, (size_t)hot_rows * KVO_ROW_BYTES));
+           ok(cudaMalloc(&v.slot2pos, sizeof(int32_t) * padded_rows)) &&
+           ok(cudaMalloc(&v.last_use, sizeof(uint32_t) * padded_rows)) &&
+           ok(cudaMalloc(&v.hot, (size_t)hot_rows * KVO_ROW_BYTES)) &&
+           ok(cudaMalloc(&v.order, sizeof(int32_t) * 2 * padded_rows));
     c->views.push_back(v);
     good = good && ok(cudaMemset(v.pos2slot, 0xff, sizeof(int32_t) * (size_t)history_cap)) &&
-           ok(cudaMemset(v.slot2pos, 0xff, sizeof(int32_t) * (size_t)hot_rows)) &&
-           ok(cudaMemset(v.last_use, 0, sizeof(uint32_t) * (size_t)hot_rows)) &&
-           ok(cudaMemset(v.hot, 0, (size_t)hot_rows * KVO_ROW_BYTES));
+           ok(cudaMemset(v.slot2pos, 0xff, sizeof(int32_t) * padded_rows)) &&
+           ok(cudaMemset(v.last_use, 0, sizeof(uint32_t) * padded_rows)) &&
+           ok(cudaMemset(v.hot, 0, (size_t)hot_rows * KVO_ROW_BYTES)) &&
+           ok(cudaMemcpy(v.order, iota.data(), sizeof(int32_t) * padded_rows, cudaMemcpyHostToDevice));
   }
   if (good) good = ok(cudaDeviceSynchronize());
   if (!good) {

@@ -11,7 +11,6 @@ namespace kvo {
 
 constexpr int kThreads = 1024;          // threads per CTA of the cluster kernels
 constexpr int kWarps = kThreads / 32;
-constexpr int kRadixBins = 256;         // 8-bit digits, most significant first
 constexpr uint32_t kMaxCluster = 16;
 
 // Device status word bits (returned by kvo_sync).
@@ -74,6 +73,18 @@ __device__ __forceinline__ void dsmem_st_u64(uint32_t addr, uint64_t v) {
 __device__ __forceinline__ void dsmem_red_add_u32(uint32_t addr, uint32_t v) {
   asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
+
+__device__ __forceinline__ void dsmem_red_or_u32(uint32_t addr, uint32_t v) {
+  asm volatile("red.shared::cluster.or.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Asynchronous 16-byte global -> shared copy (completes at cp_async_wait_all).
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gmem_src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // Each CTA publishes `nval` (<= 4) values; afterwards every CTA reads every
 // CTA's values from its own shared memory (table[rank][i]).  Contains one
@@ -169,26 +180,30 @@ __device__ __forceinline__ void block_sum2(uint32_t a, uint32_t b, uint32_t* scr
 // keys are those whose bits above `shift` exceed those of `prefix`, plus the
 // first `need` keys (in index order) whose bits above `shift` equal them.
 // When the last examined bucket is taken whole, `need` equals its count.
-// `above` / `at` count this CTA's keys above / at the cut.
 struct RadixCut {
   uint32_t prefix;
   uint32_t shift;
   uint32_t need;
-  uint32_t above;
-  uint32_t at;
 };
 
+constexpr int kDigitBits = 8;                    // 256-bin digits (wider ones cost more in DSMEM traffic)
+constexpr uint32_t kBins = 1u << kDigitBits;
+constexpr uint32_t kBinsPerThread = kBins >= (uint32_t)kThreads ? kBins / kThreads : 1u;
+constexpr uint32_t kScanThreads = kBins / kBinsPerThread;   // threads taking part in the bin scan
+static_assert(kScanThreads % 32 == 0 && kScanThreads <= (uint32_t)kThreads, "whole warps scan the bins");
+
 struct __align__(16) RadixSmem {
-  uint32_t hist[kRadixBins];        // this CTA's histogram of the current pass
-  uint32_t total[2][kRadixBins];    // cluster-wide histograms, added into by every CTA
+  uint32_t whist[kWarps][kBins];    // per-warp histograms: warps never contend on a bin
+  uint32_t hist[kBins];             // this CTA's histogram of the current pass
+  uint32_t total[2][kBins];         // cluster-wide histograms, added into by every CTA
+  uint32_t warp_sum[kWarps];        // block scan of the cluster-wide histogram
   uint32_t cut[4];                  // bucket, count above it, bucket count
-  uint32_t local[2];                // this CTA's keys above the cut, at the cut
 };
 
 // Zeroes the cluster-wide histograms.  A cluster barrier must separate this
 // from the first cluster_radix_select of any CTA.
 __device__ __forceinline__ void radix_smem_init(RadixSmem* sm) {
-  for (uint32_t b = threadIdx.x; b < 2 * kRadixBins; b += kThreads) (&sm->total[0][0])[b] = 0;
+  for (uint32_t b = threadIdx.x; b < 2 * kBins; b += kThreads) (&sm->total[0][0])[b] = 0;
 }
 
 // Adds one to bin `bin` for every lane with `valid`; lanes with the same bin
@@ -207,13 +222,14 @@ __device__ __forceinline__ void hist_add_warp(uint32_t* h, uint32_t bin, bool va
 // Entries at or beyond `count` are ignored, but key4 must be safe to call for
 // every g < ceil(count / 4).
 //
-// cluster_radix_select finds the cut.  Keys are below 2^key_bits (key_bits a
-// multiple of 8, 8..32), so leading all-zero digits are skipped.  Every CTA of
-// the cluster must call it with the same `want` and `key_bits`, and `want`
-// must not exceed the cluster's key count.  Each pass: a warp-aggregated
-// shared-memory histogram, one remote add of every nonzero bin into every
-// CTA's cluster-wide histogram, one cluster barrier, then a warp scan of the
-// local copy (every CTA finds the same bucket).
+// cluster_radix_select finds the cut.  Keys are below 2^key_bits (1..32), so
+// only significant digits are examined: digits of up to 11 bits, most
+// significant first.  Every CTA of the cluster must call it with the same
+// `want` and `key_bits`, and `want` must not exceed the cluster's key count.
+// Each pass: a warp-aggregated shared-memory histogram, one remote add of
+// every nonzero bin into every CTA's cluster-wide histogram, one cluster
+// barrier, then a block scan of the local copy from the largest digit down
+// (every CTA finds the same bucket with no further exchange).
 template <typename Key4>
 __device__ RadixCut cluster_radix_select(Key4 key4, uint32_t count, uint32_t want, uint32_t key_bits,
                                          RadixSmem* sm, uint32_t nrank) {
@@ -221,14 +237,16 @@ __device__ RadixCut cluster_radix_select(Key4 key4, uint32_t count, uint32_t wan
   uint32_t shift = key_bits;
   const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t ngroups = (count + 3) / 4;
-  uint32_t acc_above = 0;                          // kept by warp 1
   for (int pass = 0;; ++pass) {
-    shift -= 8;
+    const uint32_t d = shift < (uint32_t)kDigitBits ? shift : (uint32_t)kDigitBits;
+    shift -= d;
+    const uint32_t dmask = (1u << d) - 1u;
     uint32_t* tot = sm->total[pass & 1];
-    for (uint32_t b = tid; b < kRadixBins; b += kThreads) {
+    for (uint32_t b = tid; b < kBins; b += kThreads) {
       sm->hist[b] = 0;
       sm->total[(pass + 1) & 1][b] = 0;     // added into by the next pass, after the barrier below
     }
+    for (uint32_t b = tid; b < kWarps * kBins; b += kThreads) (&sm->whist[0][0])[b] = 0;
     __syncthreads();
     for (uint32_t g0 = 0; g0 < ngroups; g0 += kThreads) {
       const uint32_t g = g0 + tid;
@@ -237,71 +255,92 @@ __device__ RadixCut cluster_radix_select(Key4 key4, uint32_t count, uint32_t wan
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const bool valid = g < ngroups && 4 * g + e < count && (kv[e] & mask) == prefix;
-        hist_add_warp(sm->hist, (kv[e] >> shift) & 0xffu, valid);
+        hist_add_warp(sm->whist[warp], (kv[e] >> shift) & dmask, valid);
       }
     }
     __syncthreads();
-    for (uint32_t i = tid; i < kRadixBins * nrank; i += kThreads) {
-      const uint32_t v = sm->hist[i & (kRadixBins - 1)];
-      if (v) dsmem_red_add_u32(dsmem_addr(&tot[i & (kRadixBins - 1)], i / kRadixBins), v);
+    {
+      // merge the per-warp histograms: thread (b, q) sums warps q*G .. q*G+G-1
+      constexpr uint32_t kParts = kThreads / kBins > 0 ? kThreads / kBins : 1;
+      constexpr uint32_t kG = kWarps / kParts;
+      for (uint32_t i = tid; i < kBins * kParts; i += kThreads) {
+        const uint32_t b = i % kBins, q = i / kBins;
+        uint32_t v = 0;
+#pragma unroll
+        for (uint32_t w = 0; w < kG; ++w) v += sm->whist[q * kG + w][b];
+        if (v) atomicAdd(&sm->hist[b], v);
+      }
+    }
+    __syncthreads();
+    for (uint32_t i = tid; i < (dmask + 1u) * nrank; i += kThreads) {
+      const uint32_t b = i & dmask;
+      const uint32_t v = sm->hist[b];
+      if (v) dsmem_red_add_u32(dsmem_addr(&tot[b], i >> d), v);
     }
     cluster_sync();
-    if (warp == 0) {
-      // lane l covers bins 255-8l down to 248-8l (largest digits first):
-      // eight contiguous words, read as two 16-byte loads
-      const uint4 lo = reinterpret_cast<const uint4*>(tot)[(248 - 8 * lane) / 4];
-      const uint4 hi = reinterpret_cast<const uint4*>(tot)[(248 - 8 * lane) / 4 + 1];
-      const uint32_t c[8] = {hi.w, hi.z, hi.y, hi.x, lo.w, lo.z, lo.y, lo.x};
-      uint32_t sum = 0;
+    // block scan from the largest digit down: thread t holds bins
+    // kBins-1-2t and kBins-2-2t (bins above dmask are zero)
+    const bool scans = tid < kScanThreads;
+    uint32_t c[kBinsPerThread], sum = 0;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) sum += c[e];
-      uint32_t incl = sum;
+    for (uint32_t e = 0; e < kBinsPerThread; ++e) {
+      c[e] = scans ? tot[kBins - 1 - kBinsPerThread * tid - e] : 0u;
+      sum += c[e];
+    }
+    uint32_t incl = sum;
 #pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        uint32_t o = __shfl_up_sync(0xffffffffu, incl, d);
-        if (lane >= (uint32_t)d) incl += o;
-      }
-      const uint32_t excl = incl - sum;
-      if (excl < remaining && remaining <= incl) {
-        uint32_t above = excl;
+    for (int dd = 1; dd < 32; dd <<= 1) {
+      const uint32_t o = __shfl_up_sync(0xffffffffu, incl, dd);
+      if (lane >= (uint32_t)dd) incl += o;
+    }
+    if (lane == 31) sm->warp_sum[warp] = incl;
+    __syncthreads();
+    uint32_t before = lane < warp ? sm->warp_sum[lane] : 0u;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          if (above + c[e] >= remaining) {
-            sm->cut[0] = 255 - 8 * lane - e;
-            sm->cut[1] = above;
-            sm->cut[2] = c[e];
-            break;
-          }
-          above += c[e];
+    for (int dd = 16; dd > 0; dd >>= 1) before += __shfl_xor_sync(0xffffffffu, before, dd);
+    const uint32_t excl = before + incl - sum;
+    if (scans && excl < remaining && remaining <= excl + sum) {
+      uint32_t above = excl;
+#pragma unroll
+      for (uint32_t e = 0; e < kBinsPerThread; ++e) {
+        if (above + c[e] >= remaining) {
+          sm->cut[0] = kBins - 1 - kBinsPerThread * tid - e;
+          sm->cut[1] = above;
+          sm->cut[2] = c[e];
+          break;
         }
+        above += c[e];
       }
     }
     __syncthreads();
     const uint32_t bucket = sm->cut[0], above = sm->cut[1], inbucket = sm->cut[2];
     remaining -= above;
     prefix |= bucket << shift;
-    mask |= 0xffu << shift;
-    const bool done = remaining == inbucket || shift == 0;
-    if (warp == 1) {
-      // this CTA's keys that matched the prefix and fell in a higher bucket
-      const uint4 h0 = reinterpret_cast<const uint4*>(sm->hist)[2 * lane];
-      const uint4 h1 = reinterpret_cast<const uint4*>(sm->hist)[2 * lane + 1];
-      const uint32_t hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-      uint32_t part = 0;
+    mask |= dmask << shift;
+    if (remaining == inbucket || shift == 0) break;   // the whole bucket is selected, or keys are exhausted
+  }
+  return RadixCut{prefix, shift, remaining};
+}
+
+// This CTA's keys above and at the cut (one pass over the keys).
+template <typename Key4>
+__device__ void cut_counts(Key4 key4, uint32_t count, const RadixCut& cut, uint32_t* scratch, uint32_t* above,
+                           uint32_t* at) {
+  const uint32_t top = cut.prefix >> cut.shift;
+  uint32_t a = 0, e = 0;
+  for (uint32_t g = threadIdx.x; g < (count + 3) / 4; g += kThreads) {
+    const uint4 kk = key4(g);
+    const uint32_t kv[4] = {kk.x, kk.y, kk.z, kk.w};
 #pragma unroll
-      for (int e = 0; e < 8; ++e) part += (8 * lane + e) > bucket ? hv[e] : 0u;
-#pragma unroll
-      for (int d = 16; d > 0; d >>= 1) part += __shfl_xor_sync(0xffffffffu, part, d);
-      acc_above += part;
-      if (done && lane == 0) {
-        sm->local[0] = acc_above;
-        sm->local[1] = sm->hist[bucket];
+    for (uint32_t q = 0; q < 4; ++q) {
+      if (4 * g + q < count) {
+        const uint32_t v = kv[q] >> cut.shift;
+        a += v > top;
+        e += v == top;
       }
     }
-    __syncthreads();
-    if (done) break;
   }
-  return RadixCut{prefix, shift, remaining, sm->local[0], sm->local[1]};
+  block_sum2(a, e, scratch, above, at);
 }
 
 // Selected-before and at-cut-before counts of CTA `rank`, from every CTA's

@@ -21,6 +21,7 @@ struct LayerView {
   uint32_t* counters;             // [0] step, [1] history length
   unsigned long long* stats;      // kvo_stats fields, in declaration order
   int32_t* evlog;                 // NULL, or [1 + 3 * KVO_MAX_K]: count then triples
+  int32_t* order;                 // [2][hot_rows]: slots by (last_use, slot), double-buffered
   uint32_t hot_rows;
   uint32_t history_cap;
 };

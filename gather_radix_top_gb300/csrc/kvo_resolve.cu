@@ -49,14 +49,12 @@ cudaError_t launch_resolve(const LayerView& L, const int32_t* idx, uint32_t k, u
   a.status = status;
   a.k = k;
   a.kchunk = (k + C - 1) / C;
-  a.hchunk = ((L.hot_rows + C - 1) / C + 3u) & ~3u;
-  a.sort_len = 1;
-  while (a.sort_len < k) a.sort_len <<= 1;
+  a.hchunk = ((L.hot_rows + C - 1) / C + 31u) & ~31u;
   a.fused = 0;
   a.len = 0;
   a.fresh = nullptr;
   a.fresh_from = 0;
-  const SmemLayout lay = smem_layout(k, a.kchunk, a.hchunk, a.sort_len);
+  const SmemLayout lay = smem_layout(k, a.kchunk, a.hchunk, L.hot_rows);
   if (lay.total > kResolveMaxDynSmem) return cudaErrorInvalidValue;
 
   cudaLaunchConfig_t lc = {};

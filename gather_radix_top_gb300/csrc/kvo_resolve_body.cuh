@@ -1,8 +1,6 @@
 // Device body of the resolve + gather call, shared by the standalone kernel
 // and the fused decode-step kernel.
 //
-// Resolve + gather of one layer's selection against its HBM hot cache.
-//
 // "From 1M Total to 15+ x 1M Contexts: GLM-5.3 KV Cache Offloading":
 //   section "Decision three: let the GPU manage the hot cache directly" -
 //     selection stays on the GPU, which checks hot slots directly; hits read
@@ -14,8 +12,12 @@
 // Victims are the least recently used unpinned slots, keyed (last_use, slot).
 //
 // One thread-block cluster runs the whole call; CTA r owns a contiguous range
-// of selection entries j and a contiguous range of hot slots.
-//   P1 classify: hit = pos2slot[p] >= 0 (stamp last_use = t); a miss does an
+// of selection entries j, a contiguous range of hot slots and the same range
+// of positions of the layer's LRU order (slots sorted by (last_use, slot)).
+//   P0 the CTA's range of the LRU order starts copying to shared memory
+//      (cp.async) while the rest of the call proceeds.
+//   P1 classify: hit = pos2slot[p] >= 0 (stamp last_use = t and set the
+//      slot's bit in its owner's pin bitmap over DSMEM); a miss does an
 //      atomicMin of a negative first-occurrence code into pos2slot[p], so the
 //      smallest j of each missing position wins (dedupe without a table).
 //      Then, while the cluster barrier completes, every row is gathered:
@@ -25,15 +27,16 @@
 //      shared memory.  When idx is strictly increasing (always true for
 //      kvo_select_topk output) every miss is unique: the counts published at
 //      the first barrier already give every rank.
-//   P3 victims: a cluster radix select of the M oldest unpinned slots on the
-//      key t - last_use (0 for pinned slots; only its significant digits are
-//      examined), ties to the lower slot.  Winners go to CTA 0 as 64-bit
-//      (last_use, slot) keys together with the position each slot holds.
-//   P4 rank (CTA 0): the i-th oldest winner is the victim of the i-th
-//      unique miss.
-//   P5 fill + map update, spread over the cluster: unmap the evicted
-//      position, map the new one, stamp last_use = t, copy the row (from the
-//      output just written) into the victim slot.
+//   P3 victims: the i-th unpinned entry of the LRU order, for i < M, is the
+//      victim of the i-th unique miss: one ordered count over the order (each
+//      CTA pulls the whole pin bitmap, counts its unpinned entries and
+//      publishes the count), no selection and no sort.
+//   P4 the CTA holding a victim unmaps the evicted position, maps the new
+//      one, stamps last_use = t and copies the row (from the output just
+//      written) into the victim slot.
+//   P5 the next LRU order: unpinned non-victim entries keep their order
+//      (they shift down by M), then every slot used in this call (hits and
+//      fills, all now last used at t) in slot order.
 #pragma once
 
 #include <cstdint>
@@ -50,7 +53,6 @@ namespace resolve_detail {
 constexpr int32_t kSlotMiss = -1;
 constexpr int32_t kSlotInvalid = -2;
 constexpr uint32_t kRowVec = KVO_ROW_BYTES / 16;   // 41 16-byte pieces per row
-constexpr uint32_t kRankMax = 512;                  // rank winners by counting up to here, else sort
 constexpr uint32_t kRowsInFlight = 4;               // rows a warp loads before it stores
 
 struct ResolveArgs {
@@ -61,8 +63,7 @@ struct ResolveArgs {
   uint32_t* status;
   uint32_t k;
   uint32_t kchunk;        // selection entries per CTA
-  uint32_t hchunk;        // hot slots per CTA (multiple of 4)
-  uint32_t sort_len;      // power of two >= k
+  uint32_t hchunk;        // hot slots (and LRU order positions) per CTA, a multiple of 32
   // fused decode step only: the selection is in shared memory, the history
   // length is `len`, and positions >= fresh_from were appended by this very
   // launch and are read from `fresh` (device memory) rather than host memory
@@ -76,32 +77,38 @@ struct ResolveArgs {
 // same fused launch, their device copy (same bytes, no host round trip).
 __device__ __forceinline__ const uint4* miss_row(const ResolveArgs& a, const uint4* hist4, int32_t p) {
   if (a.fresh && (uint32_t)p >= a.fresh_from)
-    return reinterpret_cast<const uint4*>(a.fresh) + (size_t)((uint32_t)p - a.fresh_from) * (KVO_ROW_BYTES / 16);
-  return hist4 + (size_t)p * (KVO_ROW_BYTES / 16);
+    return reinterpret_cast<const uint4*>(a.fresh) + (size_t)((uint32_t)p - a.fresh_from) * kRowVec;
+  return hist4 + (size_t)p * kRowVec;
 }
 
 struct SmemLayout {
-  uint32_t sortkeys, lukeys, meta_slot, meta_pos, uniq, miss_pos, miss_j, win_old, vic_slot, vic_old, share, sel,
-      total;
+  uint32_t miss_pos, miss_j, ord, pinbits, fullbits, meta_slot, meta_pos, uniq, sel, vic_rank, vic_slot, vic_pos,
+      vic_j, total;
 };
 
-__host__ __device__ inline SmemLayout smem_layout(uint32_t k, uint32_t kchunk, uint32_t hchunk,
-                                                  uint32_t sort_len) {
+__host__ __device__ inline uint32_t round16(uint32_t x) { return (x + 15u) & ~15u; }
+
+// hchunk: slots (and order positions) per CTA, a multiple of 32 so that the
+// pin bitmap of a CTA is whole words of the layer's bitmap.
+__host__ __device__ inline SmemLayout smem_layout(uint32_t k, uint32_t kchunk, uint32_t hchunk, uint32_t hot_rows) {
   SmemLayout s;
+  const uint32_t vcap = k < hchunk ? k : hchunk;   // victims one CTA can hold
   uint32_t o = 0;
-  s.sortkeys = o;  o += sort_len * 8u;          // CTA 0: winners' (last_use, slot)
-  s.lukeys = o;    o += hchunk * 4u;            // this CTA's LRU keys
+  s.miss_pos = o;  o += k * 4u;                 // CTA 0: unique misses in j order
+  s.miss_j = o;    o += k * 4u;
+  o = round16(o);
+  s.ord = o;       o += hchunk * 4u;            // this CTA's range of the LRU order
+  s.pinbits = o;   o += round16(hchunk / 8u);   // this CTA's slots used in this call
+  s.fullbits = o;  o += round16((hot_rows + 31u) / 32u * 4u);   // every slot pinned in this call
   s.meta_slot = o; o += kchunk * 4u;            // per entry: hot slot, or miss / invalid
   s.meta_pos = o;  o += kchunk * 4u;            // per entry: position
   s.uniq = o;      o += kchunk * 4u;            // per entry: 1 = unique miss
-  s.miss_pos = o;  o += k * 4u;                 // CTA 0: unique misses in j order
-  s.miss_j = o;    o += k * 4u;
-  s.win_old = o;   o += k * 4u;                 // CTA 0: position each winner holds (winner order)
-  s.vic_slot = o;  o += k * 4u;                 // CTA 0: victims in rank order, and what they held
-  s.vic_old = o;   o += k * 4u;
-  s.share = o;     o += 4u * kchunk * 4u;       // this CTA's share of the fills (slot, old, pos, j)
   s.sel = o;       o += kchunk * 4u;            // fused step: this CTA's selected positions
-  s.total = (o + 15u) & ~15u;
+  s.vic_rank = o;  o += vcap * 4u;              // victims found in this CTA's order range
+  s.vic_slot = o;  o += vcap * 4u;
+  s.vic_pos = o;   o += vcap * 4u;
+  s.vic_j = o;     o += vcap * 4u;
+  s.total = round16(o);
   return s;
 }
 
@@ -146,37 +153,82 @@ __device__ __forceinline__ void dequant_row(const uint4& va, const uint4& vb, ui
   if (lane >= 1 && lane < kRowVec - 32) d[64 + (lane - 1)] = vb;   // RoPE, copied
 }
 
+// Copies one 656-byte row with a warp (L2 reads: the source may have been
+// written by another CTA of this launch).
+__device__ __forceinline__ void copy_row(const uint4* src, uint4* dst, uint32_t lane) {
+  const uint4 x = __ldcg(src + lane);
+  uint4 y = make_uint4(0, 0, 0, 0);
+  if (lane < kRowVec - 32) y = __ldcg(src + 32 + lane);
+  dst[lane] = x;
+  if (lane < kRowVec - 32) dst[32 + lane] = y;
+}
+
+// One map update: slot v receives position p, evicting `old` (or -1).
+// Returns 1 when a mapped position was evicted.
+__device__ __forceinline__ uint32_t map_update(const ResolveArgs& a, uint32_t v, int32_t old, int32_t p,
+                                               uint32_t t, uint32_t e) {
+  const LayerView& L = a.L;
+  if (v >= L.hot_rows || p < 0 || (uint32_t)p >= L.history_cap) {
+    atomicOr(a.status, kFlagInternal);              // cannot happen; never write out of bounds
+    return 0;
+  }
+  if (old >= 0) L.pos2slot[old] = -1;
+  L.pos2slot[p] = (int32_t)v;
+  L.slot2pos[v] = p;
+  L.last_use[v] = t;
+  if (L.evlog) {
+    L.evlog[1 + 3 * e] = (int32_t)v;
+    L.evlog[2 + 3 * e] = old;
+    L.evlog[3 + 3 * e] = p;
+  }
+  return old >= 0 ? 1u : 0u;
+}
+
 __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_smem) {
-  __shared__ RadixSmem rsm;
   __shared__ uint32_t scratch[2][2 * kWarps + 2];
   __shared__ uint32_t table[kMaxCluster][4];
   __shared__ uint32_t table2[kMaxCluster][4];
+  __shared__ uint32_t table3[kMaxCluster][4];
+  __shared__ uint32_t tcount[kMaxCluster];         // victims per slot-owner CTA
+  __shared__ uint32_t nvic;
 
   const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t r = cluster_rank(), C = cluster_size();
   const LayerView& L = a.L;
   const uint32_t k = a.k;
+  const uint32_t H = L.hot_rows;
 
-  const SmemLayout lay = smem_layout(k, a.kchunk, a.hchunk, a.sort_len);
-  uint64_t* sortkeys = reinterpret_cast<uint64_t*>(dyn_smem + lay.sortkeys);
-  uint32_t* lukeys = reinterpret_cast<uint32_t*>(dyn_smem + lay.lukeys);
+  const SmemLayout lay = smem_layout(k, a.kchunk, a.hchunk, H);
+  int32_t* miss_pos = reinterpret_cast<int32_t*>(dyn_smem + lay.miss_pos);
+  int32_t* miss_j = reinterpret_cast<int32_t*>(dyn_smem + lay.miss_j);
+  int32_t* ord = reinterpret_cast<int32_t*>(dyn_smem + lay.ord);
+  uint32_t* pinbits = reinterpret_cast<uint32_t*>(dyn_smem + lay.pinbits);
+  uint32_t* fullbits = reinterpret_cast<uint32_t*>(dyn_smem + lay.fullbits);
   int32_t* meta_slot = reinterpret_cast<int32_t*>(dyn_smem + lay.meta_slot);
   int32_t* meta_pos = reinterpret_cast<int32_t*>(dyn_smem + lay.meta_pos);
   uint32_t* uniq = reinterpret_cast<uint32_t*>(dyn_smem + lay.uniq);
-  int32_t* miss_pos = reinterpret_cast<int32_t*>(dyn_smem + lay.miss_pos);
-  int32_t* miss_j = reinterpret_cast<int32_t*>(dyn_smem + lay.miss_j);
-  int32_t* win_old = reinterpret_cast<int32_t*>(dyn_smem + lay.win_old);
-  int32_t* vic_slot = reinterpret_cast<int32_t*>(dyn_smem + lay.vic_slot);
-  int32_t* vic_old = reinterpret_cast<int32_t*>(dyn_smem + lay.vic_old);
-  int32_t* share = reinterpret_cast<int32_t*>(dyn_smem + lay.share);
   const int32_t* sel = reinterpret_cast<const int32_t*>(dyn_smem + lay.sel);
+  uint32_t* vic_rank = reinterpret_cast<uint32_t*>(dyn_smem + lay.vic_rank);
+  uint32_t* vic_slot = reinterpret_cast<uint32_t*>(dyn_smem + lay.vic_slot);
+  int32_t* vic_pos = reinterpret_cast<int32_t*>(dyn_smem + lay.vic_pos);
+  uint32_t* vic_j = reinterpret_cast<uint32_t*>(dyn_smem + lay.vic_j);
 
   const uint32_t t = L.counters[0] + 1u;        // this call's step
   const uint32_t len = a.fused ? a.len : L.counters[1];
   const uint32_t jlo = min(k, r * a.kchunk), jhi = min(k, jlo + a.kchunk), jcnt = jhi - jlo;
-  radix_smem_init(&rsm);
-  // B0: every CTA of the cluster is running before any DSMEM access (its
-  // wait is just before the first remote store, so classification overlaps).
+  const uint32_t slo = min(H, r * a.hchunk), shi = min(H, slo + a.hchunk), hcnt = shi - slo;
+  const uint32_t words = a.hchunk / 32u;         // pin-bitmap words per CTA
+  const uint32_t Hp = (H + 3u) & ~3u;            // order buffers are padded to whole 16-byte pieces
+  const int32_t* ord_in = L.order + (size_t)((t + 1u) & 1u) * Hp;   // written by the previous call
+  int32_t* ord_out = L.order + (size_t)(t & 1u) * Hp;
+
+  // ---------------------------------------------------------------- P0
+  for (uint32_t i = tid; i < words; i += kThreads) pinbits[i] = 0;
+  for (uint32_t i = tid; i < (hcnt + 3) / 4; i += kThreads) cp_async16(ord + 4 * i, ord_in + slo + 4 * i);
+  if (tid < kMaxCluster) tcount[tid] = 0;
+  if (tid == 0) nvic = 0;
+  // B0: every CTA of the cluster is running (and has zeroed what others add
+  // into) before any DSMEM access; classification overlaps the barrier.
   cluster_arrive();
 
   // ---------------------------------------------------------------- P1
@@ -209,12 +261,19 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
   block_sum2(unordered, nmiss, scratch[0], &cta_unordered, &cta_miss);
   cluster_wait();                                   // B0
   if (tid < 2 * C) dsmem_st_u32(dsmem_addr(&table[r][tid & 1], tid >> 1), (tid & 1) ? cta_miss : cta_unordered);
-  cluster_arrive();                                 // B1: stamps, claims, counts
+  for (uint32_t jj = tid; jj < jcnt; jj += kThreads) {
+    const int32_t s = meta_slot[jj];
+    if (s >= 0) {                                   // pin: the slot's bit in its owner CTA
+      const uint32_t owner = (uint32_t)s / a.hchunk, b = (uint32_t)s - owner * a.hchunk;
+      dsmem_red_or_u32(dsmem_addr(&pinbits[b >> 5], owner), 1u << (b & 31));
+    }
+  }
+  cluster_arrive();                                 // B1: stamps, claims, counts, pins
 
-  const uint4* hot4 = reinterpret_cast<const uint4*>(L.hot);
-  const uint4* hist4 = reinterpret_cast<const uint4*>(L.hist);
   // Each warp loads up to kRowsInFlight rows before storing any, so that all
   // of this CTA's rows are in flight at once.
+  const uint4* hot4 = reinterpret_cast<const uint4*>(L.hot);
+  const uint4* hist4 = reinterpret_cast<const uint4*>(L.hist);
   for (uint32_t jj0 = warp; jj0 < jcnt; jj0 += kWarps * kRowsInFlight) {
     uint4 va[kRowsInFlight], vb[kRowsInFlight];
 #pragma unroll
@@ -247,6 +306,7 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
         dequant_row(va[u], vb[u], lane, reinterpret_cast<uint4*>(a.out_bf16 + (size_t)j * KVO_DEQUANT_VALUES));
     }
   }
+  cp_async_wait_all();
   cluster_wait();                                   // B1
 
   // ---------------------------------------------------------------- P2
@@ -282,160 +342,125 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
     }
   }
   if (r == 0 && tid == 0) L.counters[0] = t;       // every CTA read the old step before B1
-
-  uint32_t nevict = 0;
   if (M > 0) {
-    {
-      const uint32_t mp0 = dsmem_addr(miss_pos, 0), mj0 = dsmem_addr(miss_j, 0);
-      uint32_t run = 0;
-      for (uint32_t base = 0; base < jcnt; base += kThreads) {
-        const uint32_t jj = base + tid;
-        const bool f = jj < jcnt && uniq[jj];
-        uint32_t tile;
-        const uint32_t rank = block_flag_scan(f, scratch[0], &tile);
-        const uint32_t i = uniq_before + run + rank;
-        if (f && i < k) {
-          dsmem_st_u32(mp0 + 4u * i, (uint32_t)meta_pos[jj]);
-          dsmem_st_u32(mj0 + 4u * i, jlo + jj);
-        }
-        run += tile;
+    const uint32_t mp0 = dsmem_addr(miss_pos, 0), mj0 = dsmem_addr(miss_j, 0);
+    uint32_t run = 0;
+    for (uint32_t base = 0; base < jcnt; base += kThreads) {
+      const uint32_t jj = base + tid;
+      const bool f = jj < jcnt && uniq[jj];
+      uint32_t tile;
+      const uint32_t rank = block_flag_scan(f, scratch[0], &tile);
+      const uint32_t i = uniq_before + run + rank;
+      if (f && i < k) {
+        dsmem_st_u32(mp0 + 4u * i, (uint32_t)meta_pos[jj]);
+        dsmem_st_u32(mj0 + 4u * i, jlo + jj);
       }
+      run += tile;
     }
-    // -------------------------------------------------------------- P3
-    const uint32_t H = L.hot_rows;
-    const uint32_t slo = min(H, r * a.hchunk), shi = min(H, slo + a.hchunk), hcnt = shi - slo;
-    for (uint32_t i = tid; i < hcnt; i += kThreads) {
-      const uint32_t lu = __ldcg(&L.last_use[slo + i]);   // stamps came from other CTAs
-      lukeys[i] = lu < t ? t - lu : 0u;                   // larger = older; pinned slots 0
+  }
+
+  // ---------------------------------------------------------------- P3
+  // the whole layer's pin bitmap: every CTA's words, pulled over DSMEM
+  for (uint32_t w = tid; w < (H + 31u) / 32u; w += kThreads) {
+    const uint32_t q = w / words;
+    fullbits[w] = dsmem_ld_u32(dsmem_addr(&pinbits[w - q * words], q));
+  }
+  uint32_t mypins = 0;
+  for (uint32_t w = tid; w < words; w += kThreads) mypins += __popc(pinbits[w]);
+  __syncthreads();
+  uint32_t unpinned = 0;
+  for (uint32_t i = tid; i < hcnt; i += kThreads) {
+    const uint32_t s = (uint32_t)ord[i];
+    unpinned += ((fullbits[s >> 5] >> (s & 31)) & 1u) ^ 1u;
+  }
+  uint32_t cta_unpinned, cta_pins;
+  block_sum2(unpinned, mypins, scratch[1], &cta_unpinned, &cta_pins);
+  const uint32_t mine3[2] = {cta_unpinned, cta_pins};
+  cluster_publish(mine3, 2, table3, r, C);         // B3: also fences the pin-bitmap pulls
+  uint32_t u_before = 0;
+  for (uint32_t q = 0; q < r; ++q) u_before += table3[q][0];
+  // Ordered pass over this CTA's order range: unpinned entry of rank u is the
+  // victim of unique miss u when u < M, else it survives at position u - M.
+  {
+    uint32_t run = 0;
+    for (uint32_t base = 0; base < hcnt; base += kThreads) {
+      const uint32_t i = base + tid;
+      uint32_t s = 0;
+      bool f = false;
+      if (i < hcnt) {
+        s = (uint32_t)ord[i];
+        f = !((fullbits[s >> 5] >> (s & 31)) & 1u);
+      }
+      uint32_t tile;
+      const uint32_t rank = block_flag_scan(f, scratch[0], &tile);
+      const uint32_t u = u_before + run + rank;
+      if (f) {
+        if (u < M) {
+          const uint32_t c = atomicAdd(&nvic, 1u);
+          vic_rank[c] = u;
+          vic_slot[c] = s;
+        } else if (u - M < H) {
+          ord_out[u - M] = (int32_t)s;
+        }
+      }
+      run += tile;
+    }
+  }
+  __syncthreads();
+
+  // ---------------------------------------------------------------- P4
+  uint32_t nevict = 0;
+  const uint32_t nv = nvic;
+  if (M > 0) {
+    for (uint32_t c = tid; c < nv; c += kThreads) {
+      const uint32_t i = vic_rank[c] < M ? vic_rank[c] : 0u;
+      vic_pos[c] = (int32_t)dsmem_ld_u32(dsmem_addr(&miss_pos[i], 0));
+      vic_j[c] = dsmem_ld_u32(dsmem_addr(&miss_j[i], 0));
     }
     __syncthreads();
-    const uint32_t key_bits = ((32u - (uint32_t)__clz((int)t)) + 7u) & ~7u;
-    auto key4 = [&](uint32_t g) -> uint4 { return reinterpret_cast<const uint4*>(lukeys)[g]; };
-    const RadixCut cut = cluster_radix_select(key4, hcnt, M, key_bits, &rsm, C);
-    const uint32_t mine2[2] = {cut.above, cut.at};
-    cluster_publish(mine2, 2, table, r, C);        // B3
-    uint32_t sel_before, at_before;
-    cut_offsets(table, 0, r, cut.need, &sel_before, &at_before);
-    const uint32_t sk0 = dsmem_addr(sortkeys, 0), old0 = dsmem_addr(win_old, 0);
-    cluster_compact(key4, hcnt, cut, sel_before, at_before, scratch, [&](uint32_t i, uint32_t out) {
-      if (out < M) {
-        const uint32_t slot = slo + i;
-        const uint64_t lu = (uint64_t)(t - lukeys[i]);
-        dsmem_st_u64(sk0 + 8u * out, (lu << 32) | slot);
-        dsmem_st_u32(old0 + 4u * out, (uint32_t)L.slot2pos[slot]);
-      }
-    });
-    cluster_sync();                                 // B4: miss list and winners in CTA 0
-
-    // -------------------------------------------------------------- P4
-    if (r == 0) {
-      if (M <= kRankMax) {
-        // rank of winner c among all winners (the keys are distinct); S
-        // threads share each winner's count
-        uint32_t S = 32;
-        while (S > 1 && S * M > kThreads) S >>= 1;
-        const uint32_t c = tid / S, part = tid % S;
-        uint32_t rank = 0;
-        uint64_t key = 0;
-        if (c < M) {
-          key = sortkeys[c];
-          for (uint32_t o = part; o < M; o += S) rank += sortkeys[o] < key;
-        }
-        for (uint32_t d = 1; d < S; d <<= 1) rank += __shfl_xor_sync(0xffffffffu, rank, d);
-        if (c < M && part == 0) {
-          vic_slot[rank] = (int32_t)(key & 0xffffffffu);
-          vic_old[rank] = win_old[c];
-        }
-      } else {
-        // bitonic sort of (last_use:32, slot:18, winner index:13) keys
-        const uint32_t P = a.sort_len;
-        for (uint32_t i = tid; i < P; i += kThreads) {
-          uint64_t v = ~0ull;
-          if (i < M) {
-            const uint64_t key = sortkeys[i];
-            v = ((key >> 32) << 31) | ((key & 0x3ffffu) << 13) | i;
-          }
-          sortkeys[i] = v;
-        }
-        __syncthreads();
-        uint32_t Pn = 1;
-        while (Pn < M && Pn < P) Pn <<= 1;
-        for (uint32_t size = 2; size <= Pn; size <<= 1) {
-          for (uint32_t stride = size >> 1; stride > 0; stride >>= 1) {
-            for (uint32_t i = tid; i < Pn / 2; i += kThreads) {
-              const uint32_t lo = 2 * i - (i & (stride - 1)), hi = lo + stride;
-              const bool ascending = (lo & size) == 0;
-              const uint64_t x = sortkeys[lo], y = sortkeys[hi];
-              if ((x > y) == ascending) {
-                sortkeys[lo] = y;
-                sortkeys[hi] = x;
-              }
-            }
-            __syncthreads();
-          }
-        }
-        for (uint32_t i = tid; i < M; i += kThreads) {
-          const uint64_t v = sortkeys[i];
-          vic_slot[i] = (int32_t)((v >> 13) & 0x3ffffu);
-          vic_old[i] = win_old[v & 0x1fffu];
-        }
-      }
+    for (uint32_t c = tid; c < nv; c += kThreads) {
+      const uint32_t v = vic_slot[c];
+      nevict += map_update(a, v, L.slot2pos[v], vic_pos[c], t, vic_rank[c]);
+      const uint32_t owner = v / a.hchunk, b = v - owner * a.hchunk;
+      dsmem_red_or_u32(dsmem_addr(&pinbits[b >> 5], owner), 1u << (b & 31));   // used in this call
     }
-    cluster_sync();                                 // B5: victims ranked
-
-    // -------------------------------------------------------------- P5
-    // This CTA's share of the fills: entries [f0, f1) of the rank order.
-    const uint32_t per = (M + C - 1) / C;
-    const uint32_t f0 = min(M, r * per), f1 = min(M, f0 + per), fn = f1 - f0;
-    int32_t* sh_slot = share;
-    int32_t* sh_old = share + a.kchunk;
-    int32_t* sh_pos = share + 2 * a.kchunk;
-    int32_t* sh_j = share + 3 * a.kchunk;
-    for (uint32_t i = tid; i < fn; i += kThreads) {
-      sh_slot[i] = (int32_t)dsmem_ld_u32(dsmem_addr(&vic_slot[f0 + i], 0));
-      sh_old[i] = (int32_t)dsmem_ld_u32(dsmem_addr(&vic_old[f0 + i], 0));
-      sh_pos[i] = (int32_t)dsmem_ld_u32(dsmem_addr(&miss_pos[f0 + i], 0));
-      sh_j[i] = (int32_t)dsmem_ld_u32(dsmem_addr(&miss_j[f0 + i], 0));
+    // every CTA learns how many fills landed in each owner's slot range
+    for (uint32_t i = tid; i < nv * C; i += kThreads) {
+      const uint32_t c = i / C, q = i - c * C;
+      dsmem_red_add_u32(dsmem_addr(&tcount[vic_slot[c] / a.hchunk], q), 1u);
     }
-    __syncthreads();
-    cluster_arrive();                               // B6: this CTA is done reading CTA 0
-    for (uint32_t i = tid; i < fn; i += kThreads) {
-      const uint32_t v = (uint32_t)sh_slot[i];
-      const int32_t old = sh_old[i], p = sh_pos[i];
-      if (v >= L.hot_rows || p < 0 || (uint32_t)p >= L.history_cap) {
-        atomicOr(a.status, kFlagInternal);          // cannot happen; never write out of bounds
-        continue;
-      }
-      if (old >= 0) {
-        L.pos2slot[old] = -1;
-        ++nevict;
-      }
-      L.pos2slot[p] = (int32_t)v;
-      L.slot2pos[v] = p;
-      L.last_use[v] = t;
-      if (L.evlog) {
-        const uint32_t e = f0 + i;
-        L.evlog[1 + 3 * e] = (int32_t)v;
-        L.evlog[2 + 3 * e] = old;
-        L.evlog[3 + 3 * e] = p;
-      }
-    }
-    for (uint32_t i = warp; i < fn; i += kWarps) {
-      const uint32_t v = (uint32_t)sh_slot[i];
-      const int32_t p = sh_pos[i];
-      const uint32_t j = (uint32_t)sh_j[i];
-      if (v >= L.hot_rows || p < 0 || (uint32_t)p >= L.history_cap || j >= k) continue;
+    cluster_arrive();                               // B4: fill bits and counts (CTA 0's list read)
+    for (uint32_t c = warp; c < nv; c += kWarps) {
+      const uint32_t v = vic_slot[c], j = vic_j[c];
+      const int32_t p = vic_pos[c];
+      if (v >= H || j >= k || p < 0 || (uint32_t)p >= L.history_cap) continue;
       // the output row written in P1 (by any CTA), else the host row
       const uint4* src = a.out_rows ? reinterpret_cast<const uint4*>(a.out_rows) + (size_t)j * kRowVec
                                     : miss_row(a, hist4, p);
-      uint4* d = reinterpret_cast<uint4*>(L.hot) + (size_t)v * kRowVec;
-      const uint4 x = __ldcg(src + lane);
-      uint4 y = make_uint4(0, 0, 0, 0);
-      if (lane < kRowVec - 32) y = __ldcg(src + 32 + lane);
-      d[lane] = x;
-      if (lane < kRowVec - 32) d[32 + lane] = y;
+      copy_row(src, reinterpret_cast<uint4*>(L.hot) + (size_t)v * kRowVec, lane);
     }
-    cluster_wait();                                 // B6
+    cluster_wait();                                 // B4
+  }
+
+  // ---------------------------------------------------------------- P5
+  // The used slots, in slot order, fill the end of the next order.
+  {
+    uint32_t used_before = 0, used = 0;
+    for (uint32_t q = 0; q < C; ++q) {
+      const uint32_t n_q = table3[q][1] + tcount[q];
+      used_before += q < r ? n_q : 0u;
+      used += n_q;
+    }
+    const uint32_t tail0 = H - used + used_before;
+    uint32_t run = 0;
+    for (uint32_t base = 0; base < hcnt; base += kThreads) {
+      const uint32_t i = base + tid;
+      const bool f = i < hcnt && ((pinbits[i >> 5] >> (i & 31)) & 1u);
+      uint32_t tile;
+      const uint32_t rank = block_flag_scan(f, scratch[0], &tile);
+      if (f && tail0 + run + rank < H) ord_out[tail0 + run + rank] = (int32_t)(slo + i);
+      run += tile;
+    }
   }
   if (L.evlog && r == 0 && tid == 0) L.evlog[0] = (int32_t)M;
 

@@ -36,6 +36,7 @@ struct StepArgs {
 template <bool kResident>
 __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const StepArgs s) {
   extern __shared__ __align__(16) uint8_t dyn_smem[];
+  __shared__ RadixSmem rsm;                        // the top-K phase's radix histograms
   const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t rank = cluster_rank(), C = cluster_size();
   constexpr uint32_t kVec = KVO_ROW_BYTES / 16;
@@ -47,10 +48,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const StepArgs
   }
 
   uint8_t* rdyn = dyn_smem + s.topk_bytes;
-  const SmemLayout lay = smem_layout(s.R.k, s.R.kchunk, s.R.hchunk, s.R.sort_len);
+  const SmemLayout lay = smem_layout(s.R.k, s.R.kchunk, s.R.hchunk, s.R.L.hot_rows);
   int32_t* sel = reinterpret_cast<int32_t*>(rdyn + lay.sel);
   const uint32_t kchunk = s.R.kchunk;
-  topk_body<kResident>(s.scores, s.n, s.R.k, dyn_smem, [&](uint32_t pos, uint32_t out) {
+  topk_body<kResident>(s.scores, s.n, s.R.k, dyn_smem, &rsm, [&](uint32_t pos, uint32_t out) {
     s.idx[out] = (int32_t)pos;
     const uint32_t owner = out / kchunk;
     dsmem_st_u32(dsmem_addr(&sel[out - owner * kchunk], owner), pos);
@@ -66,7 +67,7 @@ struct StepConfig {
 };
 StepConfig g_step[64];
 
-constexpr size_t kStepMaxDynSmem = 216 * 1024;
+constexpr size_t kStepMaxDynSmem = 187 * 1024;     // 227 KB less the static radix histograms
 
 }  // namespace
 
@@ -100,9 +101,7 @@ cudaError_t launch_decode_step(const LayerView& L, const void* new_rows, uint32_
   a.status = status;
   a.k = k;
   a.kchunk = (k + C - 1) / C;
-  a.hchunk = ((L.hot_rows + C - 1) / C + 3u) & ~3u;
-  a.sort_len = 1;
-  while (a.sort_len < k) a.sort_len <<= 1;
+  a.hchunk = ((L.hot_rows + C - 1) / C + 31u) & ~31u;
   a.fused = 1;
   a.len = old_len + r;
   a.fresh = r ? static_cast<const uint8_t*>(new_rows) : nullptr;
@@ -113,7 +112,7 @@ cudaError_t launch_decode_step(const LayerView& L, const void* new_rows, uint32_
   s.new_rows = static_cast<const uint4*>(new_rows);
   s.hist_dst = reinterpret_cast<uint4*>(const_cast<uint8_t*>(L.hist) + (size_t)old_len * KVO_ROW_BYTES);
   s.r = r;
-  const SmemLayout lay = smem_layout(k, a.kchunk, a.hchunk, a.sort_len);
+  const SmemLayout lay = smem_layout(k, a.kchunk, a.hchunk, L.hot_rows);
   const size_t topk_res = ((size_t)topk_chunk(n, C) * 4u + 15u) & ~(size_t)15u;
   if (lay.total > kStepMaxDynSmem) return cudaErrorInvalidValue;
   const bool resident = topk_res + lay.total <= kStepMaxDynSmem;

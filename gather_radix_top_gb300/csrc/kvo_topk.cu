@@ -15,7 +15,8 @@ template <bool kResident>
 __global__ void __launch_bounds__(kThreads, 1)
     topk_kernel(const float* __restrict__ scores, uint32_t n, uint32_t k, int32_t* __restrict__ idx) {
   extern __shared__ __align__(16) uint8_t dyn_smem[];
-  topk_body<kResident>(scores, n, k, dyn_smem, [&](uint32_t pos, uint32_t out) { idx[out] = (int32_t)pos; });
+  __shared__ RadixSmem rsm;
+  topk_body<kResident>(scores, n, k, dyn_smem, &rsm, [&](uint32_t pos, uint32_t out) { idx[out] = (int32_t)pos; });
 }
 
 struct TopkConfig {

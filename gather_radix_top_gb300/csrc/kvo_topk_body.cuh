@@ -29,7 +29,7 @@ namespace kvo {
 
 namespace topk_detail {
 
-constexpr uint32_t kTopkStaticSmem = 6144;                 // headroom for static smem
+constexpr uint32_t kTopkStaticSmem = 40 * 1024;            // headroom for static smem (radix histograms)
 constexpr uint32_t kTopkMaxDynSmem = 227 * 1024 - kTopkStaticSmem;
 
 __host__ __device__ __forceinline__ uint32_t topk_chunk(uint32_t n, uint32_t C) {
@@ -44,8 +44,7 @@ __host__ __device__ __forceinline__ uint32_t topk_chunk(uint32_t n, uint32_t C) 
 // a cluster barrier.
 template <bool kResident, typename Emit>
 __device__ __forceinline__ void topk_body(const float* __restrict__ scores, uint32_t n, uint32_t k,
-                                          uint8_t* dyn_smem, Emit emit) {
-  __shared__ RadixSmem rsm;
+                                          uint8_t* dyn_smem, RadixSmem* rsm, Emit emit) {
   __shared__ uint32_t scratch[2][2 * kWarps + 2];
   __shared__ uint32_t table[kMaxCluster][4];
 
@@ -73,7 +72,7 @@ __device__ __forceinline__ void topk_body(const float* __restrict__ scores, uint
     return make_uint4(v[0], v[1], v[2], v[3]);
   };
 
-  radix_smem_init(&rsm);
+  radix_smem_init(rsm);
   if (kResident) {
     for (uint32_t g = tid; g < (cnt + 3) / 4; g += kThreads) reinterpret_cast<uint4*>(keys)[g] = load4(g);
   }
@@ -83,8 +82,10 @@ __device__ __forceinline__ void topk_body(const float* __restrict__ scores, uint
     return load4(g);
   };
 
-  const RadixCut cut = cluster_radix_select(key4, cnt, k, 32, &rsm, C);
-  const uint32_t mine[2] = {cut.above, cut.at};
+  const RadixCut cut = cluster_radix_select(key4, cnt, k, 32, rsm, C);
+  uint32_t above, at;
+  cut_counts(key4, cnt, cut, scratch[1], &above, &at);
+  const uint32_t mine[2] = {above, at};
   cluster_publish(mine, 2, table, r, C);
   uint32_t sel_before, at_before;
   cut_offsets(table, 0, r, cut.need, &sel_before, &at_before);

@@ -15,7 +15,7 @@ from . import build as _build
 ROW_BYTES = 656
 DEQUANT_VALUES = 576
 MAX_K = 4096
-MAX_HOT_ROWS = 262144
+MAX_HOT_ROWS = 131072
 
 KVO_OK, KVO_EINVAL, KVO_ENOMEM, KVO_ECUDA, KVO_ERANGE, KVO_EBUSY, KVO_ETIMEDOUT, KVO_ECAPACITY = (
     0, -1, -2, -3, -4, -5, -6, -7)

@@ -45,7 +45,7 @@ extern "C" {
 #define KVO_LATENT_BYTES 512
 #define KVO_DEQUANT_VALUES 576      /* bf16 values per dequantised row */
 #define KVO_MAX_K 4096              /* largest selection size per call */
-#define KVO_MAX_HOT_ROWS 262144     /* largest hot cache per layer */
+#define KVO_MAX_HOT_ROWS 131072     /* largest hot cache per layer */
 
 typedef enum kvo_status {
   KVO_OK = 0,

@@ -103,7 +103,7 @@ def test_tiny_workload_full_parity(kvo):
 
 @pytest.mark.parametrize("seed,H,n,k,dup,bad", [
     (1, 16, 40, 16, 0.3, 2), (2, 64, 300, 33, 0.5, 0), (3, 1024, 5000, 256, 0.2, 5),
-    (4, 1024, 5000, 1024, 0.0, 0), (5, 4096, 70_000, 2048, 0.4, 3), (6, 32_768, 60_000, 4096, 0.1, 1), (7, 262_144, 300_000, 4096, 0.0, 0),
+    (4, 1024, 5000, 1024, 0.0, 0), (5, 4096, 70_000, 2048, 0.4, 3), (6, 32_768, 60_000, 4096, 0.1, 1), (7, 131_072, 300_000, 4096, 0.0, 0),
 ])
 def test_resolve_random_selections(kvo, seed, H, n, k, dup, bad):
     """Arbitrary order, duplicates and out-of-range entries; many steps so the

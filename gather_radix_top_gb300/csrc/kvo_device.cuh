@@ -62,6 +62,21 @@ __device__ __forceinline__ uint32_t dsmem_ld_u32(uint32_t addr) {
   return v;
 }
 
+__device__ __forceinline__ uint4 dsmem_ld_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void dsmem_st_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
 __device__ __forceinline__ void dsmem_st_u32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
@@ -125,6 +140,31 @@ __device__ __forceinline__ uint32_t block_flag_scan(bool flag, uint32_t* scratch
   *total = scratch[kWarps];
   __syncthreads();
   return r;
+}
+
+// Exclusive prefix sum of a per-thread value over the CTA in thread order;
+// *total gets the CTA's sum.  `scratch` holds kWarps + 1 words.  Two
+// __syncthreads; scratch is reusable afterwards.
+__device__ __forceinline__ uint32_t block_excl_sum(uint32_t v, uint32_t* scratch, uint32_t* total) {
+  const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t incl = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint32_t o = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= (uint32_t)d) incl += o;
+  }
+  if (lane == 31) scratch[warp] = incl;
+  __syncthreads();
+  uint32_t before = lane < warp ? scratch[lane] : 0u;
+  uint32_t all = scratch[lane];
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) {
+    before += __shfl_xor_sync(0xffffffffu, before, d);
+    all += __shfl_xor_sync(0xffffffffu, all, d);
+  }
+  __syncthreads();
+  *total = all;
+  return before + incl - v;
 }
 
 // Sum of a per-thread value over the CTA (result valid in every thread).
@@ -193,7 +233,6 @@ constexpr uint32_t kScanThreads = kBins / kBinsPerThread;   // threads taking pa
 static_assert(kScanThreads % 32 == 0 && kScanThreads <= (uint32_t)kThreads, "whole warps scan the bins");
 
 struct __align__(16) RadixSmem {
-  uint32_t whist[kWarps][kBins];    // per-warp histograms: warps never contend on a bin
   uint32_t hist[kBins];             // this CTA's histogram of the current pass
   uint32_t total[2][kBins];         // cluster-wide histograms, added into by every CTA
   uint32_t warp_sum[kWarps];        // block scan of the cluster-wide histogram
@@ -246,7 +285,6 @@ __device__ RadixCut cluster_radix_select(Key4 key4, uint32_t count, uint32_t wan
       sm->hist[b] = 0;
       sm->total[(pass + 1) & 1][b] = 0;     // added into by the next pass, after the barrier below
     }
-    for (uint32_t b = tid; b < kWarps * kBins; b += kThreads) (&sm->whist[0][0])[b] = 0;
     __syncthreads();
     for (uint32_t g0 = 0; g0 < ngroups; g0 += kThreads) {
       const uint32_t g = g0 + tid;
@@ -255,20 +293,7 @@ __device__ RadixCut cluster_radix_select(Key4 key4, uint32_t count, uint32_t wan
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const bool valid = g < ngroups && 4 * g + e < count && (kv[e] & mask) == prefix;
-        hist_add_warp(sm->whist[warp], (kv[e] >> shift) & dmask, valid);
-      }
-    }
-    __syncthreads();
-    {
-      // merge the per-warp histograms: thread (b, q) sums warps q*G .. q*G+G-1
-      constexpr uint32_t kParts = kThreads / kBins > 0 ? kThreads / kBins : 1;
-      constexpr uint32_t kG = kWarps / kParts;
-      for (uint32_t i = tid; i < kBins * kParts; i += kThreads) {
-        const uint32_t b = i % kBins, q = i / kBins;
-        uint32_t v = 0;
-#pragma unroll
-        for (uint32_t w = 0; w < kG; ++w) v += sm->whist[q * kG + w][b];
-        if (v) atomicAdd(&sm->hist[b], v);
+        hist_add_warp(sm->hist, (kv[e] >> shift) & dmask, valid);
       }
     }
     __syncthreads();

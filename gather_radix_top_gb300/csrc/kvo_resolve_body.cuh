@@ -54,6 +54,7 @@ constexpr int32_t kSlotMiss = -1;
 constexpr int32_t kSlotInvalid = -2;
 constexpr uint32_t kRowVec = KVO_ROW_BYTES / 16;   // 41 16-byte pieces per row
 constexpr uint32_t kRowsInFlight = 4;               // rows a warp loads before it stores
+constexpr uint32_t kTiles = 2;                      // order range per CTA <= kTiles * 4 * kThreads
 
 struct ResolveArgs {
   LayerView L;
@@ -63,7 +64,7 @@ struct ResolveArgs {
   uint32_t* status;
   uint32_t k;
   uint32_t kchunk;        // selection entries per CTA
-  uint32_t hchunk;        // hot slots (and LRU order positions) per CTA, a multiple of 32
+  uint32_t hchunk;        // hot slots (and LRU order positions) per CTA, a multiple of 128
   // fused decode step only: the selection is in shared memory, the history
   // length is `len`, and positions >= fresh_from were appended by this very
   // launch and are read from `fresh` (device memory) rather than host memory
@@ -82,14 +83,14 @@ __device__ __forceinline__ const uint4* miss_row(const ResolveArgs& a, const uin
 }
 
 struct SmemLayout {
-  uint32_t miss_pos, miss_j, ord, pinbits, fullbits, meta_slot, meta_pos, uniq, sel, vic_rank, vic_slot, vic_pos,
-      vic_j, total;
+  uint32_t miss_pos, miss_j, ord, pinbits, fullbits, meta_slot, meta_pos, uniq, sel, vic_rank, vic_slot, rec,
+      total;
 };
 
 __host__ __device__ inline uint32_t round16(uint32_t x) { return (x + 15u) & ~15u; }
 
-// hchunk: slots (and order positions) per CTA, a multiple of 32 so that the
-// pin bitmap of a CTA is whole words of the layer's bitmap.
+// hchunk: slots (and order positions) per CTA, a multiple of 128 so that the
+// pin bitmap of a CTA is whole 16-byte pieces of the layer's bitmap.
 __host__ __device__ inline SmemLayout smem_layout(uint32_t k, uint32_t kchunk, uint32_t hchunk, uint32_t hot_rows) {
   SmemLayout s;
   const uint32_t vcap = k < hchunk ? k : hchunk;   // victims one CTA can hold
@@ -106,8 +107,8 @@ __host__ __device__ inline SmemLayout smem_layout(uint32_t k, uint32_t kchunk, u
   s.sel = o;       o += kchunk * 4u;            // fused step: this CTA's selected positions
   s.vic_rank = o;  o += vcap * 4u;              // victims found in this CTA's order range
   s.vic_slot = o;  o += vcap * 4u;
-  s.vic_pos = o;   o += vcap * 4u;
-  s.vic_j = o;     o += vcap * 4u;
+  o = round16(o);
+  s.rec = o;       o += kchunk * 16u;           // victims this CTA maps and fills: (slot, pos, j, rank)
   s.total = round16(o);
   return s;
 }
@@ -189,7 +190,8 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
   __shared__ uint32_t table[kMaxCluster][4];
   __shared__ uint32_t table2[kMaxCluster][4];
   __shared__ uint32_t table3[kMaxCluster][4];
-  __shared__ uint32_t tcount[kMaxCluster];         // victims per slot-owner CTA
+  __shared__ uint32_t tcount[kMaxCluster];         // victims per slot-owner CTA, over the cluster
+  __shared__ uint32_t ocount[kMaxCluster];         // victims per slot-owner CTA found here
   __shared__ uint32_t nvic;
 
   const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -210,8 +212,7 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
   const int32_t* sel = reinterpret_cast<const int32_t*>(dyn_smem + lay.sel);
   uint32_t* vic_rank = reinterpret_cast<uint32_t*>(dyn_smem + lay.vic_rank);
   uint32_t* vic_slot = reinterpret_cast<uint32_t*>(dyn_smem + lay.vic_slot);
-  int32_t* vic_pos = reinterpret_cast<int32_t*>(dyn_smem + lay.vic_pos);
-  uint32_t* vic_j = reinterpret_cast<uint32_t*>(dyn_smem + lay.vic_j);
+  uint4* rec = reinterpret_cast<uint4*>(dyn_smem + lay.rec);
 
   const uint32_t t = L.counters[0] + 1u;        // this call's step
   const uint32_t len = a.fused ? a.len : L.counters[1];
@@ -225,7 +226,10 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
   // ---------------------------------------------------------------- P0
   for (uint32_t i = tid; i < words; i += kThreads) pinbits[i] = 0;
   for (uint32_t i = tid; i < (hcnt + 3) / 4; i += kThreads) cp_async16(ord + 4 * i, ord_in + slo + 4 * i);
-  if (tid < kMaxCluster) tcount[tid] = 0;
+  if (tid < kMaxCluster) {
+    tcount[tid] = 0;
+    ocount[tid] = 0;
+  }
   if (tid == 0) nvic = 0;
   // B0: every CTA of the cluster is running (and has zeroed what others add
   // into) before any DSMEM access; classification overlaps the barrier.
@@ -360,90 +364,108 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
   }
 
   // ---------------------------------------------------------------- P3
-  // the whole layer's pin bitmap: every CTA's words, pulled over DSMEM
-  for (uint32_t w = tid; w < (H + 31u) / 32u; w += kThreads) {
+  // the whole layer's pin bitmap: every CTA's words, pulled over DSMEM in
+  // 16-byte pieces (a CTA's words are a multiple of 4)
+  for (uint32_t w = 4 * tid; w < (H + 31u) / 32u; w += 4 * kThreads) {
     const uint32_t q = w / words;
-    fullbits[w] = dsmem_ld_u32(dsmem_addr(&pinbits[w - q * words], q));
+    *reinterpret_cast<uint4*>(&fullbits[w]) = dsmem_ld_v4(dsmem_addr(&pinbits[w - q * words], q));
   }
   uint32_t mypins = 0;
   for (uint32_t w = tid; w < words; w += kThreads) mypins += __popc(pinbits[w]);
   __syncthreads();
-  uint32_t unpinned = 0;
-  for (uint32_t i = tid; i < hcnt; i += kThreads) {
-    const uint32_t s = (uint32_t)ord[i];
-    unpinned += ((fullbits[s >> 5] >> (s & 31)) & 1u) ^ 1u;
+  // Ordered pass over this CTA's order range, four entries per thread: the
+  // unpinned entry of rank u is the victim of unique miss u when u < M, else
+  // it survives at position u - M of the next order.
+  uint32_t cnt4[kTiles], total4[kTiles], unpinned = 0;
+#pragma unroll
+  for (uint32_t tile = 0; tile < kTiles; ++tile) {
+    const uint32_t i0 = 4 * (tile * kThreads + tid);
+    uint32_t c = 0;
+#pragma unroll
+    for (uint32_t e = 0; e < 4; ++e) {
+      if (i0 + e < hcnt) {
+        const uint32_t sl = (uint32_t)ord[i0 + e];
+        c += ((fullbits[sl >> 5] >> (sl & 31)) & 1u) ^ 1u;
+      }
+    }
+    cnt4[tile] = c;
+    unpinned += c;
   }
   uint32_t cta_unpinned, cta_pins;
   block_sum2(unpinned, mypins, scratch[1], &cta_unpinned, &cta_pins);
   const uint32_t mine3[2] = {cta_unpinned, cta_pins};
   cluster_publish(mine3, 2, table3, r, C);         // B3: also fences the pin-bitmap pulls
-  uint32_t u_before = 0;
-  for (uint32_t q = 0; q < r; ++q) u_before += table3[q][0];
-  // Ordered pass over this CTA's order range: unpinned entry of rank u is the
-  // victim of unique miss u when u < M, else it survives at position u - M.
-  {
-    uint32_t run = 0;
-    for (uint32_t base = 0; base < hcnt; base += kThreads) {
-      const uint32_t i = base + tid;
-      uint32_t s = 0;
-      bool f = false;
-      if (i < hcnt) {
-        s = (uint32_t)ord[i];
-        f = !((fullbits[s >> 5] >> (s & 31)) & 1u);
-      }
-      uint32_t tile;
-      const uint32_t rank = block_flag_scan(f, scratch[0], &tile);
-      const uint32_t u = u_before + run + rank;
-      if (f) {
-        if (u < M) {
-          const uint32_t c = atomicAdd(&nvic, 1u);
-          vic_rank[c] = u;
-          vic_slot[c] = s;
-        } else if (u - M < H) {
-          ord_out[u - M] = (int32_t)s;
+  uint32_t u_run = 0;
+  for (uint32_t q = 0; q < r; ++q) u_run += table3[q][0];
+#pragma unroll
+  for (uint32_t tile = 0; tile < kTiles; ++tile) {
+    const uint32_t i0 = 4 * (tile * kThreads + tid);
+    uint32_t u = u_run + block_excl_sum(cnt4[tile], scratch[tile & 1], &total4[tile]);
+#pragma unroll
+    for (uint32_t e = 0; e < 4; ++e) {
+      if (i0 + e < hcnt) {
+        const uint32_t sl = (uint32_t)ord[i0 + e];
+        if (!((fullbits[sl >> 5] >> (sl & 31)) & 1u)) {
+          if (u < M) {
+            const uint32_t c = atomicAdd(&nvic, 1u);
+            vic_rank[c] = u;
+            vic_slot[c] = sl;
+          } else if (u - M < H) {
+            ord_out[u - M] = (int32_t)sl;
+          }
+          ++u;
         }
       }
-      run += tile;
     }
+    u_run += total4[tile];
   }
   __syncthreads();
 
   // ---------------------------------------------------------------- P4
+  // The CTA holding a victim marks it used (its owner's bit), counts it for
+  // its owner and sends (slot, position, entry, rank) to the handler CTA
+  // rank % C, which then maps it and copies its row.
   uint32_t nevict = 0;
   const uint32_t nv = nvic;
   if (M > 0) {
     for (uint32_t c = tid; c < nv; c += kThreads) {
-      const uint32_t i = vic_rank[c] < M ? vic_rank[c] : 0u;
-      vic_pos[c] = (int32_t)dsmem_ld_u32(dsmem_addr(&miss_pos[i], 0));
-      vic_j[c] = dsmem_ld_u32(dsmem_addr(&miss_j[i], 0));
-    }
-    __syncthreads();
-    for (uint32_t c = tid; c < nv; c += kThreads) {
-      const uint32_t v = vic_slot[c];
-      nevict += map_update(a, v, L.slot2pos[v], vic_pos[c], t, vic_rank[c]);
+      const uint32_t u = vic_rank[c] < M ? vic_rank[c] : 0u, v = vic_slot[c];
+      const uint32_t p = dsmem_ld_u32(dsmem_addr(&miss_pos[u], 0));
+      const uint32_t j = dsmem_ld_u32(dsmem_addr(&miss_j[u], 0));
+      const uint32_t h = u % C;
+      dsmem_st_v4(dsmem_addr(&rec[u / C], h), make_uint4(v, p, j, u));
       const uint32_t owner = v / a.hchunk, b = v - owner * a.hchunk;
       dsmem_red_or_u32(dsmem_addr(&pinbits[b >> 5], owner), 1u << (b & 31));   // used in this call
+      atomicAdd(&ocount[owner], 1u);
     }
+    __syncthreads();
     // every CTA learns how many fills landed in each owner's slot range
-    for (uint32_t i = tid; i < nv * C; i += kThreads) {
-      const uint32_t c = i / C, q = i - c * C;
-      dsmem_red_add_u32(dsmem_addr(&tcount[vic_slot[c] / a.hchunk], q), 1u);
+    for (uint32_t i = tid; i < C * C; i += kThreads) {
+      const uint32_t o = i / C, q = i - o * C;
+      const uint32_t n = ocount[o];
+      if (n) dsmem_red_add_u32(dsmem_addr(&tcount[o], q), n);
     }
-    cluster_arrive();                               // B4: fill bits and counts (CTA 0's list read)
-    for (uint32_t c = warp; c < nv; c += kWarps) {
-      const uint32_t v = vic_slot[c], j = vic_j[c];
-      const int32_t p = vic_pos[c];
+    cluster_sync();                                 // B4: records, bits and counts delivered
+    const uint32_t nrec = r < M ? (M - r + C - 1) / C : 0u;
+    for (uint32_t c = tid; c < nrec; c += kThreads) {
+      const uint4 rc = rec[c];
+      nevict += map_update(a, rc.x, L.slot2pos[rc.x], (int32_t)rc.y, t, rc.w);
+    }
+    for (uint32_t c = warp; c < nrec; c += kWarps) {
+      const uint4 rc = rec[c];
+      const uint32_t v = rc.x, j = rc.z;
+      const int32_t p = (int32_t)rc.y;
       if (v >= H || j >= k || p < 0 || (uint32_t)p >= L.history_cap) continue;
       // the output row written in P1 (by any CTA), else the host row
       const uint4* src = a.out_rows ? reinterpret_cast<const uint4*>(a.out_rows) + (size_t)j * kRowVec
                                     : miss_row(a, hist4, p);
       copy_row(src, reinterpret_cast<uint4*>(L.hot) + (size_t)v * kRowVec, lane);
     }
-    cluster_wait();                                 // B4
   }
 
   // ---------------------------------------------------------------- P5
-  // The used slots, in slot order, fill the end of the next order.
+  // The used slots, in slot order, fill the end of the next order: one
+  // 32-bit word of this CTA's used-slot bitmap per thread.
   {
     uint32_t used_before = 0, used = 0;
     for (uint32_t q = 0; q < C; ++q) {
@@ -453,13 +475,19 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
     }
     const uint32_t tail0 = H - used + used_before;
     uint32_t run = 0;
-    for (uint32_t base = 0; base < hcnt; base += kThreads) {
-      const uint32_t i = base + tid;
-      const bool f = i < hcnt && ((pinbits[i >> 5] >> (i & 31)) & 1u);
-      uint32_t tile;
-      const uint32_t rank = block_flag_scan(f, scratch[0], &tile);
-      if (f && tail0 + run + rank < H) ord_out[tail0 + run + rank] = (int32_t)(slo + i);
-      run += tile;
+    for (uint32_t w0 = 0; w0 < words; w0 += kThreads) {
+      const uint32_t w = w0 + tid;
+      uint32_t bits = w < words ? pinbits[w] : 0u;
+      uint32_t tot;
+      uint32_t pos = tail0 + run + block_excl_sum(__popc(bits), scratch[0], &tot);
+      while (bits) {
+        const uint32_t b = __ffs(bits) - 1;
+        bits &= bits - 1;
+        const uint32_t i = 32 * w + b;
+        if (i < hcnt && pos < H) ord_out[pos] = (int32_t)(slo + i);
+        ++pos;
+      }
+      run += tot;
     }
   }
   if (L.evlog && r == 0 && tid == 0) L.evlog[0] = (int32_t)M;

@@ -101,7 +101,8 @@ cudaError_t launch_decode_step(const LayerView& L, const void* new_rows, uint32_
   a.status = status;
   a.k = k;
   a.kchunk = (k + C - 1) / C;
-  a.hchunk = ((L.hot_rows + C - 1) / C + 31u) & ~31u;
+  a.hchunk = ((L.hot_rows + C - 1) / C + 127u) & ~127u;
+  if (a.hchunk > kTiles * 4u * kThreads) return cudaErrorInvalidValue;   // order range per CTA too long
   a.fused = 1;
   a.len = old_len + r;
   a.fresh = r ? static_cast<const uint8_t*>(new_rows) : nullptr;

@@ -7,6 +7,7 @@
 // and tables ("Ten sessions exposed a physical-allocation problem": long-lived
 // caches get exact-capacity allocations, never pooled blocks).
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 #include <vector>
@@ -144,6 +145,11 @@ kvo_status kvo_create(int32_t layers, int64_t history_cap, int32_t hot_rows, int
   if (!ok(cudaGetDevice(&c->device))) {
     delete c;
     return KVO_ECUDA;
+  }
+  // KVO_MAX_CLUSTER (2, 4, 8 or 16) caps the CTAs per cluster: a tuning knob
+  if (const char* env = std::getenv("KVO_MAX_CLUSTER")) {
+    const int m = std::atoi(env);
+    if (m == 2 || m == 4 || m == 8 || m == 16) c->max_cluster = m;
   }
   c->layers = layers;
   c->history_cap = history_cap;

@@ -156,7 +156,7 @@ __device__ __forceinline__ uint32_t block_excl_sum(uint32_t v, uint32_t* scratch
   if (lane == 31) scratch[warp] = incl;
   __syncthreads();
   uint32_t before = lane < warp ? scratch[lane] : 0u;
-  uint32_t all = scratch[lane];
+  uint32_t all = lane < (uint32_t)kWarps ? scratch[lane] : 0u;
 #pragma unroll
   for (int d = 16; d > 0; d >>= 1) {
     before += __shfl_xor_sync(0xffffffffu, before, d);
@@ -191,7 +191,7 @@ __device__ __forceinline__ uint32_t block_sum(uint32_t v, uint32_t* scratch) {
 // `scratch` holds 2 * kWarps words.
 __device__ __forceinline__ void block_sum2(uint32_t a, uint32_t b, uint32_t* scratch, uint32_t* sa,
                                            uint32_t* sb) {
-  static_assert(kWarps == 32, "one lane per warp of the CTA");
+  static_assert(kWarps <= 32, "one lane per warp of the CTA");
   const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int d = 16; d > 0; d >>= 1) {
@@ -203,8 +203,8 @@ __device__ __forceinline__ void block_sum2(uint32_t a, uint32_t b, uint32_t* scr
     scratch[2 * warp + 1] = b;
   }
   __syncthreads();
-  a = scratch[2 * lane];
-  b = scratch[2 * lane + 1];
+  a = lane < (uint32_t)kWarps ? scratch[2 * lane] : 0u;
+  b = lane < (uint32_t)kWarps ? scratch[2 * lane + 1] : 0u;
 #pragma unroll
   for (int d = 16; d > 0; d >>= 1) {
     a += __shfl_xor_sync(0xffffffffu, a, d);
@@ -391,7 +391,7 @@ __device__ __forceinline__ void cut_offsets(const uint32_t (*table)[4], uint32_t
 template <typename Key4, typename Emit>
 __device__ void cluster_compact(Key4 key4, uint32_t count, const RadixCut& cut, uint32_t sel_before,
                                 uint32_t at_before, uint32_t (*scratch)[2 * kWarps + 2], Emit emit) {
-  static_assert(kWarps == 32, "one lane per warp of the CTA");
+  static_assert(kWarps <= 32, "one lane per warp of the CTA");
   const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t ngroups = (count + 3) / 4;
   const uint32_t shift = cut.shift, top = cut.prefix >> shift, need = cut.need;
@@ -429,7 +429,8 @@ __device__ void cluster_compact(Key4 key4, uint32_t count, const RadixCut& cut, 
     const uint32_t used = at_before + run_at;
     const uint32_t left = need > used ? need - used : 0u;   // at-cut keys still to take
     // lane l works on warp l's totals
-    const uint32_t A_l = sc[2 * lane], E_l = sc[2 * lane + 1];
+    const uint32_t A_l = lane < (uint32_t)kWarps ? sc[2 * lane] : 0u;
+    const uint32_t E_l = lane < (uint32_t)kWarps ? sc[2 * lane + 1] : 0u;
     uint32_t E_incl = E_l;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {

@@ -193,6 +193,8 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
   __shared__ uint32_t tcount[kMaxCluster];         // victims per slot-owner CTA, over the cluster
   __shared__ uint32_t ocount[kMaxCluster];         // victims per slot-owner CTA found here
   __shared__ uint32_t nvic;
+  __shared__ uint32_t nevict_cta;
+  __shared__ uint32_t cta_hits, cta_inv;
 
   const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t r = cluster_rank(), C = cluster_size();
@@ -225,12 +227,16 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
 
   // ---------------------------------------------------------------- P0
   for (uint32_t i = tid; i < words; i += kThreads) pinbits[i] = 0;
+  for (uint32_t i = tid; i < (H + 31u) / 32u; i += kThreads) fullbits[i] = 0;
   for (uint32_t i = tid; i < (hcnt + 3) / 4; i += kThreads) cp_async16(ord + 4 * i, ord_in + slo + 4 * i);
   if (tid < kMaxCluster) {
     tcount[tid] = 0;
     ocount[tid] = 0;
   }
-  if (tid == 0) nvic = 0;
+  if (tid == 0) {
+    nvic = 0;
+    nevict_cta = 0;
+  }
   // B0: every CTA of the cluster is running (and has zeroed what others add
   // into) before any DSMEM access; classification overlaps the barrier.
   cluster_arrive();
@@ -261,16 +267,30 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
     meta_slot[jj] = slot;
     meta_pos[jj] = p;
   }
-  uint32_t cta_unordered, cta_miss;
-  block_sum2(unordered, nmiss, scratch[0], &cta_unordered, &cta_miss);
+  // local rank of each miss in j order (the global rank once the counts of
+  // lower CTAs are known); every miss is unique when idx is increasing
+  uint32_t cta_miss = 0;
+  for (uint32_t base = 0; base < jcnt; base += kThreads) {
+    const uint32_t jj = base + tid;
+    const bool f = jj < jcnt && meta_slot[jj] == kSlotMiss;
+    uint32_t tile;
+    const uint32_t rank = block_flag_scan(f, scratch[0], &tile);
+    if (f) uniq[jj] = cta_miss + rank;
+    cta_miss += tile;
+  }
+  uint32_t cta_unordered, cta_hit_inv;
+  block_sum2(unordered, nhit | (ninv << 16), scratch[1], &cta_unordered, &cta_hit_inv);
+  if (tid == 0) {
+    cta_hits = cta_hit_inv & 0xffffu;
+    cta_inv = cta_hit_inv >> 16;
+  }
   cluster_wait();                                   // B0
   if (tid < 2 * C) dsmem_st_u32(dsmem_addr(&table[r][tid & 1], tid >> 1), (tid & 1) ? cta_miss : cta_unordered);
-  for (uint32_t jj = tid; jj < jcnt; jj += kThreads) {
-    const int32_t s = meta_slot[jj];
-    if (s >= 0) {                                   // pin: the slot's bit in its owner CTA
-      const uint32_t owner = (uint32_t)s / a.hchunk, b = (uint32_t)s - owner * a.hchunk;
-      dsmem_red_or_u32(dsmem_addr(&pinbits[b >> 5], owner), 1u << (b & 31));
-    }
+  // pin: every CTA gets every hit slot's bit
+  for (uint32_t i = tid; i < jcnt * C; i += kThreads) {
+    const uint32_t jj = i / C, q = i - jj * C;
+    const int32_t sl = meta_slot[jj];
+    if (sl >= 0) dsmem_red_or_u32(dsmem_addr(&fullbits[(uint32_t)sl >> 5], q), 1u << ((uint32_t)sl & 31));
   }
   cluster_arrive();                                 // B1: stamps, claims, counts, pins
 
@@ -322,9 +342,17 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
     M += table[q][1];
   }
   if (!any_unordered) {
-    // strictly increasing idx: every miss is a distinct position
-    for (uint32_t jj = tid; jj < jcnt; jj += kThreads) uniq[jj] = meta_slot[jj] == kSlotMiss;
-    __syncthreads();
+    // strictly increasing idx: every miss is a distinct position, ranked in P1
+    if (M > 0) {
+      const uint32_t mp0 = dsmem_addr(miss_pos, 0), mj0 = dsmem_addr(miss_j, 0);
+      for (uint32_t jj = tid; jj < jcnt; jj += kThreads) {
+        const uint32_t i = uniq_before + uniq[jj];
+        if (meta_slot[jj] == kSlotMiss && i < k) {
+          dsmem_st_u32(mp0 + 4u * i, (uint32_t)meta_pos[jj]);
+          dsmem_st_u32(mj0 + 4u * i, jlo + jj);
+        }
+      }
+    }
   } else {
     // The smallest claiming j owns each missing position; the claims came
     // from other CTAs, so read them from L2.
@@ -346,7 +374,7 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
     }
   }
   if (r == 0 && tid == 0) L.counters[0] = t;       // every CTA read the old step before B1
-  if (M > 0) {
+  if (M > 0 && any_unordered) {
     const uint32_t mp0 = dsmem_addr(miss_pos, 0), mj0 = dsmem_addr(miss_j, 0);
     uint32_t run = 0;
     for (uint32_t base = 0; base < jcnt; base += kThreads) {
@@ -364,15 +392,11 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
   }
 
   // ---------------------------------------------------------------- P3
-  // the whole layer's pin bitmap: every CTA's words, pulled over DSMEM in
-  // 16-byte pieces (a CTA's words are a multiple of 4)
-  for (uint32_t w = 4 * tid; w < (H + 31u) / 32u; w += 4 * kThreads) {
-    const uint32_t q = w / words;
-    *reinterpret_cast<uint4*>(&fullbits[w]) = dsmem_ld_v4(dsmem_addr(&pinbits[w - q * words], q));
-  }
+  // the layer's pin bitmap arrived before B1; this CTA's own slots are
+  // words [slo / 32, slo / 32 + words) of it
+  const uint32_t hwords = (hcnt + 31u) / 32u;     // words of this CTA's own slots (none if it has none)
   uint32_t mypins = 0;
-  for (uint32_t w = tid; w < words; w += kThreads) mypins += __popc(pinbits[w]);
-  __syncthreads();
+  for (uint32_t w = tid; w < hwords; w += kThreads) mypins += __popc(fullbits[slo / 32u + w]);
   // Ordered pass over this CTA's order range, four entries per thread: the
   // unpinned entry of rank u is the victim of unique miss u when u < M, else
   // it survives at position u - M of the next order.
@@ -399,6 +423,7 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
   for (uint32_t q = 0; q < r; ++q) u_run += table3[q][0];
 #pragma unroll
   for (uint32_t tile = 0; tile < kTiles; ++tile) {
+    if (tile * 4u * kThreads >= hcnt) break;       // uniform over the CTA
     const uint32_t i0 = 4 * (tile * kThreads + tid);
     uint32_t u = u_run + block_excl_sum(cnt4[tile], scratch[tile & 1], &total4[tile]);
 #pragma unroll
@@ -425,7 +450,6 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
   // The CTA holding a victim marks it used (its owner's bit), counts it for
   // its owner and sends (slot, position, entry, rank) to the handler CTA
   // rank % C, which then maps it and copies its row.
-  uint32_t nevict = 0;
   const uint32_t nv = nvic;
   if (M > 0) {
     for (uint32_t c = tid; c < nv; c += kThreads) {
@@ -449,7 +473,7 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
     const uint32_t nrec = r < M ? (M - r + C - 1) / C : 0u;
     for (uint32_t c = tid; c < nrec; c += kThreads) {
       const uint4 rc = rec[c];
-      nevict += map_update(a, rc.x, L.slot2pos[rc.x], (int32_t)rc.y, t, rc.w);
+      if (map_update(a, rc.x, L.slot2pos[rc.x], (int32_t)rc.y, t, rc.w)) atomicAdd(&nevict_cta, 1u);
     }
     for (uint32_t c = warp; c < nrec; c += kWarps) {
       const uint4 rc = rec[c];
@@ -475,9 +499,9 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
     }
     const uint32_t tail0 = H - used + used_before;
     uint32_t run = 0;
-    for (uint32_t w0 = 0; w0 < words; w0 += kThreads) {
+    for (uint32_t w0 = 0; w0 < hwords; w0 += kThreads) {
       const uint32_t w = w0 + tid;
-      uint32_t bits = w < words ? pinbits[w] : 0u;
+      uint32_t bits = w < hwords ? pinbits[w] | fullbits[slo / 32u + w] : 0u;
       uint32_t tot;
       uint32_t pos = tail0 + run + block_excl_sum(__popc(bits), scratch[0], &tot);
       while (bits) {
@@ -493,19 +517,17 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
   if (L.evlog && r == 0 && tid == 0) L.evlog[0] = (int32_t)M;
 
   // ------------------------------------------------------------- stats
-  uint32_t s_hit, s_miss, s_inv, s_evict;
-  block_sum2(nhit, nmiss, scratch[0], &s_hit, &s_miss);
-  block_sum2(ninv, nevict, scratch[1], &s_inv, &s_evict);
+  __syncthreads();
   if (tid == 0) {
     unsigned long long* st = L.stats;
-    if (s_hit) atomicAdd(st + 1, (unsigned long long)s_hit);
-    if (s_miss) {
-      atomicAdd(st + 2, (unsigned long long)s_miss);
-      atomicAdd(st + 6, (unsigned long long)s_miss * KVO_ROW_BYTES);
+    if (cta_hits) atomicAdd(st + 1, (unsigned long long)cta_hits);
+    if (cta_miss) {
+      atomicAdd(st + 2, (unsigned long long)cta_miss);
+      atomicAdd(st + 6, (unsigned long long)cta_miss * KVO_ROW_BYTES);
     }
-    if (s_evict) atomicAdd(st + 4, (unsigned long long)s_evict);
-    if (s_inv) {
-      atomicAdd(st + 5, (unsigned long long)s_inv);
+    if (nevict_cta) atomicAdd(st + 4, (unsigned long long)nevict_cta);
+    if (cta_inv) {
+      atomicAdd(st + 5, (unsigned long long)cta_inv);
       atomicOr(a.status, kFlagRange);
     }
     if (r == 0) {

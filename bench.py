@@ -8,7 +8,13 @@ hot cache, misses from pinned host memory, LRU fills) into the contiguous
 attention input.  Metric: selected rows resolved+gathered per second.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kvo|reference]
-                    [--workload 50k_single_layer|50k_full_stack|1m_cold_stress|tiny]
+                    [--workload 50k_single_layer|50k_full_stack|1m_cold_stress|tiny|
+                                session_evict_restore]
+
+With --workload session_evict_restore a step is one evict/restore cycle of
+the secondary path instead: store every session's blocks from the HBM pool
+to the pinned host tier, release them, overwrite the pool with filler, and
+restore all sessions in one admission.
 
 Timing: inputs (history, scores, new rows) are resident before the timed
 region; a 1 GiB memset flushes L2 between steps; each step is bracketed by
@@ -261,6 +267,7 @@ def measure_host_link(torch, kvo):
     sink = torch.zeros(16, dtype=torch.uint8, device="cuda")
     res = {}
     for name, fn in (("memcpy_h2d", lambda: dev.copy_(host, non_blocking=True)),
+                     ("memcpy_d2h", lambda: host.copy_(dev, non_blocking=True)),
                      ("zero_copy_loads", lambda: kvo.kvo_probe_host_read(host, sink))):
         best = 0.0
         for _ in range(4):
@@ -273,6 +280,7 @@ def measure_host_link(torch, kvo):
         res[name] = round(best, 1)
     del host, dev
     res["peak_gbs"] = max(res["memcpy_h2d"], res["zero_copy_loads"])
+    res["peak_d2h_gbs"] = res["memcpy_d2h"]
     return res
 
 
@@ -407,6 +415,184 @@ def run_oracle(w, max_steps, budget_s, layers=None):
             "cores": max(1, round(cpu / max(spent, 1e-9))), "sels": sels}
 
 
+# ------------------------------------------------- session evict/restore
+SESSION_METRIC = ("session KV rows stored+restored/s (HBM block pool <-> pinned host tier); "
+                  "GB/s vs host-link roofline")
+
+
+def session_config(sw, world):
+    return {"workload": sw.name, "sessions": sw.sessions, "tokens": sw.tokens, "layers": sw.layers,
+            "block_tokens": sw.block_tokens, "block_bytes": sw.block_bytes, "parallelism": f"replicas{world}",
+            "calls": "kvo_store_blocks x sessions, kvo_pool_release, kvo_pool_fill, kvo_restore_blocks(all)",
+            "l2": "inputs (%.1f GB per direction) far larger than L2" % (
+                sw.sessions * sw.blocks_per_session * sw.block_bytes / 1e9)}
+
+
+def run_sessions_oracle(sw, budget_s):
+    """The pool oracle as it stands: one session of the workload's length on
+    the first 8 layers, store -> complete -> release -> fill -> restore ->
+    complete, repeated until `budget_s` of oracle time."""
+    from oracle import kvo_pool_oracle as PO
+    L = min(8, sw.layers)
+    nb = sw.blocks_per_layer * L
+    o = PO.PoolOracle(L, nb, sw.block_tokens, ROW, nb)
+    assert o.alloc(0, sw.tokens) == PO.KVO_OK
+    cpu0, spent, cycles = time.process_time(), 0.0, 0
+    while spent < budget_s or cycles == 0:
+        t = time.perf_counter()
+        assert o.store(0) == PO.KVO_OK
+        o.complete_copies()
+        assert o.release(0) == PO.KVO_OK
+        o.fill(0xA5)
+        assert o.restore([0]) == PO.KVO_OK
+        o.complete_copies()
+        spent += time.perf_counter() - t
+        cycles += 1
+    cpu = time.process_time() - cpu0
+    rows = 2 * cycles * L * sw.tokens
+    return {"rows_per_s": rows / spent, "cycles": cycles, "layers": L, "seconds": spent,
+            "cores": max(1, round(cpu / max(spent, 1e-9)))}
+
+
+def run_sessions(args, rank, world):
+    import torch
+    from gather_radix_top_gb300 import build, kvo
+    build.build()
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    sw = W.SESSIONS
+    S, per = sw.sessions, sw.blocks_per_session
+    nb = S * per
+    pool = kvo.Pool(sw.layers, nb, sw.block_tokens, nb)
+    dev = torch.device("cuda")
+    for s in range(S):
+        assert pool.alloc(s, sw.tokens) == kvo.KVO_OK
+        for layer in range(sw.layers):
+            pool.write(s, layer, 0, W.session_rows_device(sw, s, layer, dev))
+    torch.cuda.synchronize()
+    order = list(range(S))
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    def cycle(timed):
+        e = [ev() for _ in range(4)]
+        w0 = time.perf_counter()
+        e[0].record()
+        for s in order:
+            assert pool.store(s) == kvo.KVO_OK
+        e[1].record()
+        pool.sync()
+        w1 = time.perf_counter()
+        for s in order:
+            assert pool.release(s) == kvo.KVO_OK
+        pool.fill(0xA5)                              # filler overwrites the whole pool
+        torch.cuda.synchronize()
+        w2 = time.perf_counter()
+        e[2].record()
+        assert pool.restore(order) == kvo.KVO_OK
+        e[3].record()
+        pool.sync()
+        w3 = time.perf_counter()
+        return e, (w1 - w0) + (w3 - w2)
+
+    for _ in range(args.warmup):
+        cycle(False)
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    evs, walls = [], []
+    for _ in range(args.steps):
+        e, wall = cycle(True)
+        evs.append(e)
+        walls.append(wall)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    store_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    restore_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    # bytewise check of a sample of groups after the last restore
+    out = torch.empty((sw.tokens, ROW), dtype=torch.uint8, device=dev)
+    checked = 0
+    for s in range(S):
+        for layer in (0, sw.layers // 2, sw.layers - 1):
+            pool.read(s, layer, 0, out)
+            assert torch.equal(out, W.session_rows_device(sw, s, layer, dev)), (s, layer)
+            checked += 1
+    st = pool.stats()
+    pool.close()
+    return {"store_ms": store_ms, "restore_ms": restore_ms, "walls": walls, "clocks": clk, "stats": st,
+            "checked_groups": checked, "launches_per_cycle": S + 1}
+
+
+def sessions_main(args, rank, world):
+    sw = W.SESSIONS
+    config = session_config(sw, world)
+    rows_cycle = 2 * sw.sessions * sw.tokens * sw.layers
+    bytes_dir = sw.sessions * sw.blocks_per_session * sw.block_bytes
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        o = run_sessions_oracle(sw, max(10.0, args.cpu_seconds))
+        line = {"impl": "reference", "metric": SESSION_METRIC, "value": round(o["rows_per_s"], 1),
+                "unit": "rows/s", "n_gpus": world, "steps": o["cycles"], "warmup": 0,
+                "ms_per_step": round(1e3 * o["seconds"] / o["cycles"], 3), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic", "config": config,
+                "cpu_baseline": {"value": round(o["rows_per_s"], 1), "unit": "rows/s", "cores": o["cores"],
+                                 "kind": "oracle",
+                                 "sample": f"1 session x {o['layers']} layers x {sw.tokens} tokens, "
+                                           f"{o['cycles']} store/restore cycles"},
+                "e2e": {"value": round(o["rows_per_s"], 1), "unit": "rows/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        tdist.init_process_group("nccl")
+    cpu = run_sessions_oracle(sw, args.cpu_seconds) if rank == 0 and world == 1 else None
+    g = run_sessions(args, rank, world)
+    total_s = (sum(g["store_ms"]) + sum(g["restore_ms"])) * 1e-3
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        t = torch.tensor([total_s], dtype=torch.float64, device="cuda")
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        total_s = float(t.item())
+        if rank != 0:
+            tdist.destroy_process_group()
+            return
+    import torch
+    from gather_radix_top_gb300 import kvo
+    link = measure_host_link(torch, kvo)
+    st_avg, rs_avg = float(np.mean(g["store_ms"])), float(np.mean(g["restore_ms"]))
+    store_gbs = bytes_dir / (st_avg * 1e-3) / 1e9
+    restore_gbs = bytes_dir / (rs_avg * 1e-3) / 1e9
+    value = args.steps * rows_cycle * world / total_s
+    line = {
+        "metric": SESSION_METRIC, "value": round(value, 1), "unit": "rows/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total_s / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "config": config,
+        "roofline": {"bound": "host_link", "kernel": "restore", "achieved": round(restore_gbs, 1),
+                     "peak": link["peak_gbs"], "unit": "GB/s", "frac": round(restore_gbs / link["peak_gbs"], 4),
+                     "traffic": None, "peak_source": "measured in this run: best of pinned H2D memcpy and "
+                                                     "zero-copy loads over 1 GiB",
+                     "algorithmic_bytes_per_launch": bytes_dir},
+        "store": {"ms": round(st_avg, 3), "gbs": round(store_gbs, 1), "peak_d2h_gbs": link["peak_d2h_gbs"],
+                  "frac": round(store_gbs / link["peak_d2h_gbs"], 4)},
+        "restore": {"ms": round(rs_avg, 3), "gbs": round(restore_gbs, 1)},
+        "host_link": link, "pool_stats": g["stats"], "checked_groups": g["checked_groups"],
+        "gpu_launches": args.steps * g["launches_per_cycle"], "clocks": g["clocks"],
+        "e2e": {"value": round(args.steps * rows_cycle / sum(g["walls"]), 1), "unit": "rows/s",
+                "h2d_bytes_per_step": bytes_dir, "d2h_bytes_per_step": bytes_dir,
+                "note": "host wall clock from the first kvo_store_blocks call to kvo_pool_sync, plus from "
+                        "kvo_restore_blocks to kvo_pool_sync (release and filler excluded)"},
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = {"value": round(cpu["rows_per_s"], 1), "unit": "rows/s", "cores": cpu["cores"],
+                                "kind": "oracle",
+                                "sample": f"1 session x {cpu['layers']} layers x {sw.tokens} tokens, "
+                                          f"{cpu['cycles']} store/restore cycles ({cpu['seconds']:.1f} s)"}
+    print(json.dumps(line))
+
+
 # -------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -414,13 +600,18 @@ def main():
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["kvo", "reference"], default="kvo")
-    ap.add_argument("--workload", choices=sorted(W.WORKLOADS), default="50k_single_layer")
+    ap.add_argument("--workload", choices=sorted(W.WORKLOADS) + [W.SESSIONS.name], default="50k_single_layer")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--separate", action="store_true",
                     help="time kvo_append_rows + kvo_select_topk + kvo_resolve_gather instead of kvo_decode_step")
     args = ap.parse_args()
 
+    if args.workload == W.SESSIONS.name:
+        if args.steps is None:
+            args.steps = 5
+        sessions_main(args, int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")))
+        return
     w = W.WORKLOADS[args.workload]
     if args.steps is None:
         args.steps = max(1, w.steps - args.warmup)

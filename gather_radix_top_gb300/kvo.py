@@ -25,6 +25,10 @@ EXPORTED = [
     "kvo_resolve_gather", "kvo_decode_step", "kvo_sync", "kvo_get_stats", "kvo_history_length",
     "kvo_debug_dump_layer", "kvo_debug_record_evictions", "kvo_debug_evictions",
     "kvo_probe_host_read",
+    "kvo_tier_blocks", "kvo_pool_create", "kvo_pool_destroy", "kvo_pool_alloc", "kvo_pool_write",
+    "kvo_pool_read", "kvo_pool_fill", "kvo_store_blocks", "kvo_pool_release", "kvo_restore_blocks",
+    "kvo_pool_sync", "kvo_pool_block_table", "kvo_pool_get_stats", "kvo_pool_debug_fail_after",
+    "kvo_pool_debug_free_queue",
 ]
 
 
@@ -37,6 +41,15 @@ class KvoError(RuntimeError):
 class kvo_stats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in (
         "steps", "hits", "misses", "unique_misses", "evictions", "invalid", "host_bytes", "rows_out")]
+
+    def as_dict(self) -> dict:
+        return {n: int(getattr(self, n)) for n, _ in self._fields_}
+
+
+class kvo_pool_stats(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_uint64) for n in (
+        "stores", "restores", "rollbacks", "bytes_stored", "bytes_restored", "free_blocks",
+        "tier_free_blocks", "pending_copies")]
 
     def as_dict(self) -> dict:
         return {n: int(getattr(self, n)) for n, _ in self._fields_}
@@ -73,6 +86,21 @@ def lib() -> ctypes.CDLL:
         "kvo_debug_record_evictions": (ctypes.c_int, [_vp, _i32]),
         "kvo_debug_evictions": (ctypes.c_int, [_vp, _i32, _vp, _i32, ctypes.POINTER(_i32)]),
         "kvo_probe_host_read": (ctypes.c_int, [_vp, _i64, _vp, _vp]),
+        "kvo_tier_blocks": (_i64, [_i64, _i64]),
+        "kvo_pool_create": (ctypes.c_int, [_i32, _i64, _i32, _i32, _i64, ctypes.POINTER(_vp)]),
+        "kvo_pool_destroy": (ctypes.c_int, [_vp]),
+        "kvo_pool_alloc": (ctypes.c_int, [_vp, _i32, _i64]),
+        "kvo_pool_write": (ctypes.c_int, [_vp, _i32, _i32, _i64, _vp, _i64, _vp]),
+        "kvo_pool_read": (ctypes.c_int, [_vp, _i32, _i32, _i64, _i64, _vp, _vp]),
+        "kvo_pool_fill": (ctypes.c_int, [_vp, ctypes.c_uint8, _vp]),
+        "kvo_store_blocks": (ctypes.c_int, [_vp, _i32, _vp]),
+        "kvo_pool_release": (ctypes.c_int, [_vp, _i32]),
+        "kvo_restore_blocks": (ctypes.c_int, [_vp, _vp, _i32, _vp]),
+        "kvo_pool_sync": (ctypes.c_int, [_vp, _vp]),
+        "kvo_pool_block_table": (ctypes.c_int, [_vp, _i32, _i32, _i32, _vp, _i64, ctypes.POINTER(_i64)]),
+        "kvo_pool_get_stats": (ctypes.c_int, [_vp, ctypes.POINTER(kvo_pool_stats)]),
+        "kvo_pool_debug_fail_after": (ctypes.c_int, [_vp, _i32, _i64]),
+        "kvo_pool_debug_free_queue": (ctypes.c_int, [_vp, _i32, _vp, _i64, ctypes.POINTER(_i64)]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -281,3 +309,167 @@ class Context:
 
     def evictions(self, layer) -> list:
         return kvo_debug_evictions(self.handle, layer)
+
+
+# ------------------------------------------------------ session block pool
+def kvo_tier_blocks(tier_bytes: int, block_bytes: int) -> int:
+    return int(lib().kvo_tier_blocks(tier_bytes, block_bytes))
+
+
+def kvo_pool_create(layers: int, pool_blocks: int, block_tokens: int, tier_blocks: int,
+                    row_bytes: int = ROW_BYTES) -> int:
+    h = _vp()
+    _check(lib().kvo_pool_create(layers, pool_blocks, block_tokens, row_bytes, tier_blocks, ctypes.byref(h)),
+           "kvo_pool_create")
+    return h.value
+
+
+def kvo_pool_destroy(pool: int) -> None:
+    _check(lib().kvo_pool_destroy(pool), "kvo_pool_destroy")
+
+
+def kvo_pool_alloc(pool: int, session: int, tokens: int) -> int:
+    """Returns KVO_OK or KVO_ECAPACITY (a refused, rolled-back allocation);
+    raises on other errors."""
+    st = lib().kvo_pool_alloc(pool, session, tokens)
+    if st not in (KVO_OK, KVO_ECAPACITY):
+        raise KvoError(st, "kvo_pool_alloc")
+    return st
+
+
+def kvo_pool_write(pool: int, session: int, layer: int, first_token: int, rows, stream=None) -> None:
+    """rows: uint8 CUDA tensor [n, 656]."""
+    _check(lib().kvo_pool_write(pool, session, layer, first_token, _dev_ptr(rows, "torch.uint8"),
+                                rows.numel() // ROW_BYTES, _stream_ptr(stream)), "kvo_pool_write")
+
+
+def kvo_pool_read(pool: int, session: int, layer: int, first_token: int, out, stream=None) -> None:
+    """out: uint8 CUDA tensor [n, 656]."""
+    _check(lib().kvo_pool_read(pool, session, layer, first_token, out.numel() // ROW_BYTES,
+                               _dev_ptr(out, "torch.uint8"), _stream_ptr(stream)), "kvo_pool_read")
+
+
+def kvo_pool_fill(pool: int, byte: int, stream=None) -> None:
+    _check(lib().kvo_pool_fill(pool, byte, _stream_ptr(stream)), "kvo_pool_fill")
+
+
+def kvo_store_blocks(pool: int, session: int, stream=None) -> int:
+    st = lib().kvo_store_blocks(pool, session, _stream_ptr(stream))
+    if st not in (KVO_OK, KVO_ECAPACITY):
+        raise KvoError(st, "kvo_store_blocks")
+    return st
+
+
+def kvo_pool_release(pool: int, session: int) -> int:
+    """Returns KVO_OK or KVO_EBUSY (a copy that depends on the blocks is pending)."""
+    st = lib().kvo_pool_release(pool, session)
+    if st not in (KVO_OK, KVO_EBUSY):
+        raise KvoError(st, "kvo_pool_release")
+    return st
+
+
+def kvo_restore_blocks(pool: int, sessions, stream=None) -> int:
+    ids = (_i32 * len(sessions))(*sessions)
+    st = lib().kvo_restore_blocks(pool, ids, len(sessions), _stream_ptr(stream))
+    if st not in (KVO_OK, KVO_ECAPACITY):
+        raise KvoError(st, "kvo_restore_blocks")
+    return st
+
+
+def kvo_pool_sync(pool: int, stream=None) -> None:
+    _check(lib().kvo_pool_sync(pool, _stream_ptr(stream)), "kvo_pool_sync")
+
+
+def kvo_pool_block_table(pool: int, session: int, layer: int, which: int = 0):
+    """Block ids of the session's layer group (which 0: pool, 1: tier), or None."""
+    n = _i64()
+    _check(lib().kvo_pool_block_table(pool, session, layer, which, None, 0, ctypes.byref(n)),
+           "kvo_pool_block_table")
+    if n.value == 0:
+        return None
+    buf = (_i32 * n.value)()
+    _check(lib().kvo_pool_block_table(pool, session, layer, which, buf, n.value, ctypes.byref(n)),
+           "kvo_pool_block_table")
+    return list(buf)
+
+
+def kvo_pool_get_stats(pool: int) -> dict:
+    s = kvo_pool_stats()
+    _check(lib().kvo_pool_get_stats(pool, ctypes.byref(s)), "kvo_pool_get_stats")
+    return s.as_dict()
+
+
+def kvo_pool_debug_fail_after(pool: int, which: int, n: int) -> None:
+    _check(lib().kvo_pool_debug_fail_after(pool, which, n), "kvo_pool_debug_fail_after")
+
+
+def kvo_pool_debug_free_queue(pool: int, which: int) -> list:
+    n = _i64()
+    _check(lib().kvo_pool_debug_free_queue(pool, which, None, 0, ctypes.byref(n)), "kvo_pool_debug_free_queue")
+    buf = (_i32 * max(n.value, 1))()
+    _check(lib().kvo_pool_debug_free_queue(pool, which, buf, n.value, ctypes.byref(n)),
+           "kvo_pool_debug_free_queue")
+    return list(buf)[:n.value]
+
+
+class Pool:
+    """Owns one session block pool; methods forward to the kvo_pool_* calls."""
+
+    def __init__(self, layers: int, pool_blocks: int, block_tokens: int, tier_blocks: int,
+                 row_bytes: int = ROW_BYTES):
+        self.layers, self.pool_blocks, self.block_tokens, self.tier_blocks = (
+            layers, pool_blocks, block_tokens, tier_blocks)
+        self.handle = kvo_pool_create(layers, pool_blocks, block_tokens, tier_blocks, row_bytes)
+
+    def close(self):
+        if self.handle:
+            kvo_pool_destroy(self.handle)
+            self.handle = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def alloc(self, session, tokens):
+        return kvo_pool_alloc(self.handle, session, tokens)
+
+    def write(self, session, layer, first_token, rows, stream=None):
+        kvo_pool_write(self.handle, session, layer, first_token, rows, stream)
+
+    def read(self, session, layer, first_token, out, stream=None):
+        kvo_pool_read(self.handle, session, layer, first_token, out, stream)
+
+    def fill(self, byte, stream=None):
+        kvo_pool_fill(self.handle, byte, stream)
+
+    def store(self, session, stream=None):
+        return kvo_store_blocks(self.handle, session, stream)
+
+    def release(self, session):
+        return kvo_pool_release(self.handle, session)
+
+    def restore(self, sessions, stream=None):
+        return kvo_restore_blocks(self.handle, list(sessions), stream)
+
+    def sync(self, stream=None):
+        kvo_pool_sync(self.handle, stream)
+
+    def block_table(self, session, layer, which=0):
+        return kvo_pool_block_table(self.handle, session, layer, which)
+
+    def stats(self) -> dict:
+        return kvo_pool_get_stats(self.handle)
+
+    def fail_after(self, which, n):
+        kvo_pool_debug_fail_after(self.handle, which, n)
+
+    def free_queue(self, which=0) -> list:
+        return kvo_pool_debug_free_queue(self.handle, which)

@@ -205,6 +205,142 @@ kvo_status kvo_debug_evictions(kvo_ctx* ctx, int32_t layer, int32_t* triples, in
  */
 kvo_status kvo_probe_host_read(const void* src, int64_t bytes, void* sink, void* stream);
 
+/* ------------------------------------------------------------------------
+ * Session block store/restore.
+ *
+ * Sources (page title, section):
+ *   [TIER] "A 60k-token context comes back off disk in 17 seconds instead of
+ *          65 seconds of prefill" (vllm-bounded-fs-kv-tier README): KV of a
+ *          session lives in fixed-size blocks of a GPU pool; whole sessions
+ *          are stored to a lower tier and restored from it; a restore is
+ *          admitted only when every group's blocks can be placed; the tier
+ *          holds tier_bytes / block_bytes blocks (floor); the pool's free
+ *          queue hands out blocks from its front and takes freed blocks at
+ *          its back.
+ *   [CORR] "Making KV offload correct", section "A grouped allocation is a
+ *          transaction": a multi-group allocation either gives every group
+ *          its blocks or leaves the allocator exactly as it was (free-queue
+ *          order, tables, counters); section "Response completion is not
+ *          copy completion": blocks are released only after the copies that
+ *          depend on them have finished.
+ *
+ * A pool holds `pool_blocks` HBM blocks and `tier_blocks` pinned host blocks,
+ * each of block_tokens rows of 656 bytes (row t of a block at byte
+ * t * 656).  A session owns ceil(tokens / block_tokens) blocks in every one
+ * of `layers` groups; the group of layer l maps session token t to block
+ * table[l][t / block_tokens], row t % block_tokens.  The allocators and the
+ * session tables live on the host: block ids returned by the calls below are
+ * final when the call returns, while the bytes move stream-ordered.  A pool
+ * is not thread-safe.
+ * ---------------------------------------------------------------------- */
+
+typedef struct kvo_pool kvo_pool;
+
+typedef struct kvo_pool_stats {
+  uint64_t stores;            /* successful kvo_store_blocks calls */
+  uint64_t restores;          /* successful kvo_restore_blocks calls */
+  uint64_t rollbacks;         /* grouped allocations refused and undone */
+  uint64_t bytes_stored;      /* pool -> tier bytes enqueued */
+  uint64_t bytes_restored;    /* tier -> pool bytes enqueued */
+  uint64_t free_blocks;       /* pool blocks in the free queue */
+  uint64_t tier_free_blocks;  /* tier blocks in the free queue */
+  uint64_t pending_copies;    /* store/restore calls whose copies are not known complete */
+} kvo_pool_stats;
+
+/* [TIER] tier capacity in blocks: tier_bytes / block_bytes, rounded down;
+ * -1 if tier_bytes < 0 or block_bytes <= 0.  Host only. */
+int64_t kvo_tier_blocks(int64_t tier_bytes, int64_t block_bytes);
+
+/*
+ * kvo_pool_create - allocate a pool on the current device (synchronous).
+ *   layers >= 1, 1 <= pool_blocks <= INT32_MAX, block_tokens >= 1,
+ *   row_bytes must be KVO_ROW_BYTES, 0 <= tier_blocks <= INT32_MAX.
+ * The HBM pool starts zeroed; both free queues start 0, 1, 2, ...
+ * Returns KVO_EINVAL on bad arguments, KVO_ENOMEM if an allocation fails
+ * (nothing is leaked).
+ */
+kvo_status kvo_pool_create(int32_t layers, int64_t pool_blocks, int32_t block_tokens, int32_t row_bytes,
+                           int64_t tier_blocks, kvo_pool** out);
+
+/* Waits for the device, frees everything (KVO_ECUDA if the wait failed). */
+kvo_status kvo_pool_destroy(kvo_pool* pool);
+
+/*
+ * kvo_pool_alloc - [CORR] transactional: give new session `session` (an id
+ * not in use) ceil(tokens / block_tokens) pool blocks in each layer group,
+ * taken from the front of the free queue group after group.  If any block
+ * cannot be had, every block taken is put back where it was and
+ * KVO_ECAPACITY is returned (stats.rollbacks counts it).  Host only.
+ */
+kvo_status kvo_pool_alloc(kvo_pool* pool, int32_t session, int64_t tokens);
+
+/*
+ * kvo_pool_write / kvo_pool_read - copy `ntokens` rows between a contiguous
+ * row buffer (656-byte rows, 16-byte aligned, device memory or mapped pinned
+ * host memory) and tokens [first_token, first_token + ntokens) of the
+ * session's layer group in the pool.  The session must be resident in the
+ * pool and the range inside its tokens, else KVO_EINVAL.  Stream-ordered.
+ */
+kvo_status kvo_pool_write(kvo_pool* pool, int32_t session, int32_t layer, int64_t first_token,
+                          const void* rows, int64_t ntokens, void* stream);
+kvo_status kvo_pool_read(kvo_pool* pool, int32_t session, int32_t layer, int64_t first_token,
+                         int64_t ntokens, void* out, void* stream);
+
+/* Sets every byte of the HBM pool to `byte` (stream-ordered). */
+kvo_status kvo_pool_fill(kvo_pool* pool, uint8_t byte, void* stream);
+
+/*
+ * kvo_store_blocks - [TIER] store: take tier blocks for every group of the
+ * session (transactional as kvo_pool_alloc, KVO_ECAPACITY on a shortfall)
+ * and enqueue one copy of every pool block to its tier block.  The session
+ * must be resident in the pool and not already stored.  Until the copy has
+ * completed the session counts as busy: kvo_pool_release returns
+ * KVO_EBUSY ([CORR] "Response completion is not copy completion").
+ */
+kvo_status kvo_store_blocks(kvo_pool* pool, int32_t session, void* stream);
+
+/*
+ * kvo_pool_release - give the session's pool blocks back to the end of the
+ * free queue (layer group by group, block-table order).  KVO_EBUSY while a
+ * store or restore of the session has not completed (nothing changes).  A
+ * stored session keeps its tier blocks and can be restored; a session with
+ * no stored copy is forgotten.  Host only.
+ */
+kvo_status kvo_pool_release(kvo_pool* pool, int32_t session);
+
+/*
+ * kvo_restore_blocks - [TIER] restore `ns` distinct stored, non-resident
+ * sessions as one admission: pool blocks for every group of every listed
+ * session (in list order, layer order) or none (KVO_ECAPACITY, state
+ * unchanged).  Enqueues the tier -> pool copies; the sessions' tier blocks
+ * return to the tier free queue once those copies have completed, and the
+ * sessions are busy until then.
+ */
+kvo_status kvo_restore_blocks(kvo_pool* pool, const int32_t* sessions, int32_t ns, void* stream);
+
+/* Waits for `stream`, then retires every completed copy (busy counts drop,
+ * tier blocks of finished restores are freed). */
+kvo_status kvo_pool_sync(kvo_pool* pool, void* stream);
+
+/*
+ * kvo_pool_block_table - copy the block ids of the session's layer group,
+ * which = 0 for its pool blocks, 1 for its tier blocks, into out[0..max);
+ * *count = the group's length (0 when the session has no such copy or does
+ * not exist).  Host only.
+ */
+kvo_status kvo_pool_block_table(kvo_pool* pool, int32_t session, int32_t layer, int32_t which, int32_t* out,
+                                int64_t max, int64_t* count);
+
+kvo_status kvo_pool_get_stats(kvo_pool* pool, kvo_pool_stats* out);
+
+/* Test hook: the n-th next single-block allocation (0 = the next one) from
+ * the pool (which = 0) or tier (which = 1) queue fails; n < 0 disarms. */
+kvo_status kvo_pool_debug_fail_after(kvo_pool* pool, int32_t which, int64_t n);
+
+/* Copies the pool (which = 0) or tier (which = 1) free queue, front first,
+ * into out[0..max); *count = its length.  Host only. */
+kvo_status kvo_pool_debug_free_queue(kvo_pool* pool, int32_t which, int32_t* out, int64_t max, int64_t* count);
+
 #ifdef __cplusplus
 }
 #endif

@@ -193,3 +193,65 @@ def random_idx(seed: int, n: int, k: int, dup_frac: float = 0.0, invalid: int = 
         bad = np.array([-1, n, n + 7, -(2 ** 31), 2 ** 31 - 1], np.int64)
         base[where] = bad[g.integers(0, len(bad), size=invalid)].astype(np.int32)
     return base
+
+
+# ------------------------------------------------------- session store/restore
+@dataclass(frozen=True)
+class SessionWorkload:
+    """Sessions whose KV lives in fixed-size blocks of an HBM pool and is
+    stored to / restored from a pinned host tier (the bounded-FS tier page's
+    evict/restore cycle: ~60k-token sessions, 16-token blocks)."""
+    name: str
+    cfg_id: int
+    seed: int
+    sessions: int
+    tokens: int
+    layers: int
+    block_tokens: int = 16
+
+    @property
+    def blocks_per_layer(self) -> int:
+        return -(-self.tokens // self.block_tokens)
+
+    @property
+    def blocks_per_session(self) -> int:
+        return self.blocks_per_layer * self.layers
+
+    @property
+    def block_bytes(self) -> int:
+        return self.block_tokens * ROW_BYTES
+
+    def scaled(self, **kw) -> "SessionWorkload":
+        d = dict(self.__dict__)
+        d.update(kw)
+        return SessionWorkload(**d)
+
+
+SESSIONS = SessionWorkload("session_evict_restore", 4, 5, sessions=8, tokens=60_000, layers=78)
+
+
+def session_rows(sw: SessionWorkload, session: int, layer: int, start: int, count: int) -> np.ndarray:
+    """Uniform random bytes for tokens [start, start+count) of one (session,
+    layer) group, uint8 [count, 656]; a token's bytes depend only on
+    (workload, session, layer, token)."""
+    out = np.empty((count, ROW_BYTES), np.uint8)
+    t = start
+    while t < start + count:
+        c = t // ROW_CHUNK
+        lo, hi = c * ROW_CHUNK, (c + 1) * ROW_CHUNK
+        g = _rng(sw.seed, sw.cfg_id, _TAG_SESSION, session, layer, c)
+        block = g.integers(0, 256, size=(min(hi, sw.tokens) - lo, ROW_BYTES), dtype=np.uint8)
+        e = min(hi, start + count)
+        out[t - start:e - start] = block[t - lo:e - lo]
+        t = e
+    return out
+
+
+def session_rows_device(sw: SessionWorkload, session: int, layer: int, device):
+    """All of one group's rows drawn on the GPU (torch, seeded by (workload,
+    session, layer)): uint8 [tokens, 656].  For sizes where a CPU draw is too
+    slow; not bytewise equal to ``session_rows``."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed((sw.seed * 1_000_003 + sw.cfg_id * 10_007 + session * 101 + layer) & 0x7FFFFFFFFFFFFFFF)
+    return torch.randint(0, 256, (sw.tokens, ROW_BYTES), dtype=torch.uint8, device=device, generator=g)

@@ -52,6 +52,31 @@ def test_bad_arguments_rejected_without_a_device(kvo):
     assert kvo.status_string(kvo.KVO_ERANGE) == "selected position outside the history"
 
 
+def test_pool_bad_arguments_rejected_without_a_device(kvo):
+    L = kvo.lib()
+    h = ctypes.c_void_p()
+    assert L.kvo_pool_create(0, 8, 16, 656, 8, ctypes.byref(h)) == kvo.KVO_EINVAL
+    assert L.kvo_pool_create(1, 0, 16, 656, 8, ctypes.byref(h)) == kvo.KVO_EINVAL
+    assert L.kvo_pool_create(1, 8, 0, 656, 8, ctypes.byref(h)) == kvo.KVO_EINVAL
+    assert L.kvo_pool_create(1, 8, 16, 640, 8, ctypes.byref(h)) == kvo.KVO_EINVAL
+    assert L.kvo_pool_create(1, 8, 16, 656, -1, ctypes.byref(h)) == kvo.KVO_EINVAL
+    assert L.kvo_pool_create(1, 2 ** 31, 16, 656, 8, ctypes.byref(h)) == kvo.KVO_EINVAL
+    assert h.value is None
+    assert L.kvo_pool_alloc(None, 0, 10) == kvo.KVO_EINVAL
+    assert L.kvo_store_blocks(None, 0, None) == kvo.KVO_EINVAL
+    assert L.kvo_restore_blocks(None, None, 1, None) == kvo.KVO_EINVAL
+    assert L.kvo_pool_release(None, 0) == kvo.KVO_EINVAL
+    assert L.kvo_pool_destroy(None) == kvo.KVO_EINVAL
+
+
+def test_tier_blocks_matches_the_printed_sizes(kvo):
+    # "A 60k-token context comes back off disk ..." README: 32 GiB -> 632 and
+    # 260 GB -> 4785 blocks of 54,329,344 bytes
+    assert kvo.kvo_tier_blocks(32 * 2 ** 30, 54_329_344) == 632
+    assert kvo.kvo_tier_blocks(260_000_000_000, 54_329_344) == 4785
+    assert kvo.kvo_tier_blocks(-1, 10) == -1 and kvo.kvo_tier_blocks(10, 0) == -1
+
+
 def test_binding_has_no_fallback(tmp_path, monkeypatch):
     from gather_radix_top_gb300 import build, kvo as K
     monkeypatch.setattr(build, "LIB", str(tmp_path / "missing.so"))

@@ -487,3 +487,49 @@ kvo_status kvo_pool_debug_free_queue(kvo_pool* p, int32_t which, int32_t* out, i
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// kvo_copy_blocks_noalloc: the block-copy kernel above, driven from a fixed
+// static device array instead of a pool's plan buffer, for callers that own
+// their block arrays and may not allocate (see include/kvo.h).
+namespace {
+
+// Scratch for the (source, destination) pairs of one call.  Nothing in it has
+// to start at zero: every call writes entries [0, n) before its kernel reads
+// them and no entry at or past n is ever read.
+static __device__ __align__(256) int2 g_noalloc_pairs[KVO_NOALLOC_MAX_PAIRS];
+
+int2* g_noalloc_addr[64] = {};   // per device, looked up by the first call on it
+
+}  // namespace
+
+extern "C" kvo_status kvo_copy_blocks_noalloc(const void* src, void* dst, int64_t block_bytes,
+                                              const int32_t* pairs, int64_t n, void* stream) {
+  if (n < 0 || n > KVO_NOALLOC_MAX_PAIRS || block_bytes <= 0 || (block_bytes & 15) ||
+      (n > 0 && (!src || !dst || !pairs || (reinterpret_cast<uintptr_t>(src) & 15u) ||
+                 (reinterpret_cast<uintptr_t>(dst) & 15u))))
+    return KVO_EINVAL;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KVO_ECUDA;
+  if (!g_noalloc_addr[dev]) {
+    void* a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_noalloc_pairs) != cudaSuccess) {
+      cudaGetLastError();
+      return KVO_ECUDA;
+    }
+    g_noalloc_addr[dev] = static_cast<int2*>(a);
+  }
+  if (n == 0) return KVO_OK;
+  if (!device_accessible(src) || !device_accessible(dst)) return KVO_EINVAL;
+  for (int64_t i = 0; i < 2 * n; ++i)
+    if (pairs[i] < 0) return KVO_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(g_noalloc_addr[dev], pairs, (size_t)n * sizeof(int2), cudaMemcpyHostToDevice, s) !=
+      cudaSuccess)
+    return KVO_ECUDA;
+  const int64_t cap = (int64_t)sm_count() * 8;
+  block_copy_kernel<<<(unsigned)(n < cap ? n : cap), 256, 0, s>>>(
+      static_cast<const uint4*>(src), static_cast<uint4*>(dst), g_noalloc_addr[dev], n,
+      (uint32_t)(block_bytes / 16));
+  return cudaGetLastError() == cudaSuccess ? KVO_OK : KVO_ECUDA;
+}

@@ -16,6 +16,7 @@ ROW_BYTES = 656
 DEQUANT_VALUES = 576
 MAX_K = 4096
 MAX_HOT_ROWS = 131072
+NOALLOC_MAX_PAIRS = 65536
 
 KVO_OK, KVO_EINVAL, KVO_ENOMEM, KVO_ECUDA, KVO_ERANGE, KVO_EBUSY, KVO_ETIMEDOUT, KVO_ECAPACITY = (
     0, -1, -2, -3, -4, -5, -6, -7)
@@ -28,7 +29,7 @@ EXPORTED = [
     "kvo_tier_blocks", "kvo_pool_create", "kvo_pool_destroy", "kvo_pool_alloc", "kvo_pool_write",
     "kvo_pool_read", "kvo_pool_fill", "kvo_store_blocks", "kvo_pool_release", "kvo_restore_blocks",
     "kvo_pool_sync", "kvo_pool_block_table", "kvo_pool_get_stats", "kvo_pool_debug_fail_after",
-    "kvo_pool_debug_free_queue",
+    "kvo_pool_debug_free_queue", "kvo_copy_blocks_noalloc",
 ]
 
 
@@ -101,6 +102,7 @@ def lib() -> ctypes.CDLL:
         "kvo_pool_get_stats": (ctypes.c_int, [_vp, ctypes.POINTER(kvo_pool_stats)]),
         "kvo_pool_debug_fail_after": (ctypes.c_int, [_vp, _i32, _i64]),
         "kvo_pool_debug_free_queue": (ctypes.c_int, [_vp, _i32, _vp, _i64, ctypes.POINTER(_i64)]),
+        "kvo_copy_blocks_noalloc": (ctypes.c_int, [_vp, _vp, _i64, _vp, _i64, _vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -410,6 +412,25 @@ def kvo_pool_debug_free_queue(pool: int, which: int) -> list:
     _check(lib().kvo_pool_debug_free_queue(pool, which, buf, n.value, ctypes.byref(n)),
            "kvo_pool_debug_free_queue")
     return list(buf)[:n.value]
+
+
+def kvo_copy_blocks_noalloc(src, dst, block_bytes: int, pairs, stream=None) -> None:
+    """Copy blocks pairs[i, 0] of `src` to blocks pairs[i, 1] of `dst`
+    without allocating (the pair list goes through the library's fixed
+    static device array).  src, dst: CUDA tensors or pinned CPU tensors;
+    pairs: int32 array-like of shape [n, 2] (host)."""
+    import numpy as np
+    pr = np.ascontiguousarray(np.asarray(pairs, dtype=np.int32).reshape(-1, 2))
+
+    def ptr(t):
+        if not t.is_contiguous():
+            raise ValueError("expected a contiguous tensor")
+        if not t.is_cuda and not t.is_pinned():
+            raise ValueError("expected a CUDA tensor or pinned host memory")
+        return ctypes.c_void_p(t.data_ptr())
+
+    _check(lib().kvo_copy_blocks_noalloc(ptr(src), ptr(dst), block_bytes, ctypes.c_void_p(pr.ctypes.data),
+                                         pr.shape[0], _stream_ptr(stream)), "kvo_copy_blocks_noalloc")
 
 
 class Pool:

@@ -341,6 +341,45 @@ kvo_status kvo_pool_debug_fail_after(kvo_pool* pool, int32_t which, int64_t n);
  * into out[0..max); *count = its length.  Host only. */
 kvo_status kvo_pool_debug_free_queue(kvo_pool* pool, int32_t which, int32_t* out, int64_t max, int64_t* count);
 
+/*
+ * kvo_copy_blocks_noalloc - copy n whole blocks of block_bytes bytes:
+ * block pairs[2i] of `src` to block pairs[2i+1] of `dst`, for i < n, with
+ * the block-copy kernel of kvo_store_blocks / kvo_restore_blocks.
+ *
+ * The sources above have no counterpart to this call.  It is for callers
+ * that keep their own block arrays (their own pool, their own pinned tier)
+ * and must not allocate while it runs: an engine whose allocator already
+ * owns the device memory budget, or a path where the device-wide
+ * synchronisation of cudaMalloc/cudaFree is not allowed.  It needs no
+ * kvo_pool and allocates nothing: the pair list is staged in a fixed static
+ * device array of KVO_NOALLOC_MAX_PAIRS pairs (512 KiB) inside the library.
+ *
+ *   src, dst     device memory or mapped pinned host memory, 16-byte
+ *                aligned, holding at least (largest id + 1) blocks each;
+ *                owned by the caller.  Source and destination blocks must
+ *                not overlap.
+ *   block_bytes  > 0, a multiple of 16.
+ *   pairs        host array of 2n non-negative block ids.  It is copied with
+ *                cudaMemcpyAsync on `stream`: pageable memory may be reused
+ *                when the call returns, pinned memory only once the stream
+ *                has passed the call.
+ *   n            0 <= n <= KVO_NOALLOC_MAX_PAIRS; a larger n is refused with
+ *                KVO_EINVAL before anything is enqueued (split the list).
+ * Returns KVO_EINVAL on bad arguments, KVO_ECUDA if a CUDA call fails.
+ * Stream-ordered.
+ *
+ * The first call on each device looks up the scratch array's address
+ * (cudaGetSymbolAddress, with that device current) and keeps it; n = 0 does
+ * only this.  Make that first call before any stream capture begins.
+ * Every call on a device shares the one scratch array: calls whose copies
+ * may overlap in time (different streams, or host threads, without an
+ * ordering between them) race on it and may copy the wrong blocks.  Issue
+ * them on one stream, or order them explicitly.
+ */
+#define KVO_NOALLOC_MAX_PAIRS 65536
+kvo_status kvo_copy_blocks_noalloc(const void* src, void* dst, int64_t block_bytes, const int32_t* pairs,
+                                   int64_t n, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -459,7 +459,7 @@ def run_sessions(args, rank, world):
     from gather_radix_top_gb300 import build, kvo
     build.build()
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
-    sw = W.SESSIONS
+    sw = session_workload(args)
     S, per = sw.sessions, sw.blocks_per_session
     nb = S * per
     pool = kvo.Pool(sw.layers, nb, sw.block_tokens, nb)
@@ -520,8 +520,17 @@ def run_sessions(args, rank, world):
             "checked_groups": checked, "launches_per_cycle": S + 1}
 
 
-def sessions_main(args, rank, world):
+def session_workload(args):
     sw = W.SESSIONS
+    if args.sessions:
+        sw = sw.scaled(sessions=args.sessions)
+    if args.session_tokens:
+        sw = sw.scaled(tokens=args.session_tokens)
+    return sw
+
+
+def sessions_main(args, rank, world):
+    sw = session_workload(args)
     config = session_config(sw, world)
     rows_cycle = 2 * sw.sessions * sw.tokens * sw.layers
     bytes_dir = sw.sessions * sw.blocks_per_session * sw.block_bytes
@@ -603,6 +612,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(W.WORKLOADS) + [W.SESSIONS.name], default="50k_single_layer")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--sessions", type=int, default=None, help="session_evict_restore: number of sessions")
+    ap.add_argument("--session-tokens", type=int, default=None, help="session_evict_restore: tokens per session")
     ap.add_argument("--separate", action="store_true",
                     help="time kvo_append_rows + kvo_select_topk + kvo_resolve_gather instead of kvo_decode_step")
     args = ap.parse_args()

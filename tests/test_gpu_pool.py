@@ -253,6 +253,14 @@ def test_eight_sessions_store_fill_restore(kvo):
     assert pool.restore(list(range(sw.sessions))) == PO.KVO_ECAPACITY
     assert pool.release(100) == PO.KVO_OK
     order = [3, 0, 7, 1, 6, 2, 5, 4]
+    # a forced failure 60% of the way through the admission leaves everything as it was
+    before = (pool.free_queue(0), pool.free_queue(1),
+              [pool.block_table(s, l, w) for s in order for l in (0, sw.layers - 1) for w in (0, 1)])
+    pool.fail_after(0, int(0.6 * sw.sessions * per))
+    assert pool.restore(order) == PO.KVO_ECAPACITY
+    after = (pool.free_queue(0), pool.free_queue(1),
+             [pool.block_table(s, l, w) for s in order for l in (0, sw.layers - 1) for w in (0, 1)])
+    assert after == before
     assert pool.restore(order) == PO.KVO_OK
     pool.sync()
     for s in range(sw.sessions):
@@ -260,7 +268,7 @@ def test_eight_sessions_store_fill_restore(kvo):
             pool.read(s, layer, 0, out)
             assert torch.equal(out, W.session_rows_device(sw, s, layer, dev)), (s, layer)
     st = pool.stats()
-    assert st["stores"] == 8 and st["restores"] == 1 and st["rollbacks"] == 1
+    assert st["stores"] == 8 and st["restores"] == 1 and st["rollbacks"] == 2
     assert st["bytes_stored"] == st["bytes_restored"] == sw.sessions * per * sw.block_bytes
     assert st["tier_free_blocks"] == sw.sessions * per and st["free_blocks"] == 0
     pool.close()

@@ -25,7 +25,7 @@ struct kvo_ctx {
   std::vector<uint8_t*> hist_host;       // pinned host history per layer
   std::vector<kvo::LayerView> views;     // device pointers per layer
   std::vector<int64_t> length;           // host copy of each history length
-  uint32_t* counters = nullptr;          // device [layers][4]: step, length
+  uint32_t* counters = nullptr;          // device [layers][8]: step, length, queue head, tail, buffer
   unsigned long long* stats = nullptr;   // device [layers][8]
   int32_t* evlog = nullptr;              // device [layers][1 + 3*KVO_MAX_K] when recording
   uint32_t* status = nullptr;            // device status word
@@ -44,7 +44,7 @@ void free_ctx(kvo_ctx* c) {
     cudaFree(v.slot2pos);
     cudaFree(v.last_use);
     cudaFree(v.hot);
-    cudaFree(v.order);
+    cudaFree(v.ring);
   }
   for (uint8_t* h : c->hist_host) cudaFreeHost(h);
   cudaFree(c->counters);
@@ -155,22 +155,27 @@ kvo_status kvo_create(int32_t layers, int64_t history_cap, int32_t hot_rows, int
   c->history_cap = history_cap;
   c->hot_rows = hot_rows;
   c->length.assign(layers, 0);
-  bool good = ok(cudaMalloc(&c->counters, sizeof(uint32_t) * 4 * layers)) &&
+  bool good = ok(cudaMalloc(&c->counters, sizeof(uint32_t) * 8 * layers)) &&
               ok(cudaMalloc(&c->stats, sizeof(unsigned long long) * 8 * layers)) &&
               ok(cudaMalloc(&c->status, sizeof(uint32_t))) &&
-              ok(cudaMemset(c->counters, 0, sizeof(uint32_t) * 4 * layers)) &&
+              ok(cudaMemset(c->counters, 0, sizeof(uint32_t) * 8 * layers)) &&
               ok(cudaMemset(c->stats, 0, sizeof(unsigned long long) * 8 * layers)) &&
               ok(cudaMemset(c->status, 0, sizeof(uint32_t)));
   // slot tables padded to whole 16-byte pieces: kernels copy them in 16-byte units
   const size_t padded_rows = ((size_t)hot_rows + 3) & ~(size_t)3;
-  // every slot starts empty (last_use 0): the LRU order is slot order
-  std::vector<int32_t> iota(padded_rows);
-  for (size_t i = 0; i < padded_rows; ++i) iota[i] = (int32_t)i;
+  // every slot starts empty (last_use 0): the LRU queue starts as one entry
+  // per slot, stamped 0, in slot order; head 0, tail hot_rows
+  uint32_t ring_cap = 1;
+  while (ring_cap < 8u * (uint32_t)hot_rows) ring_cap <<= 1;
+  std::vector<uint64_t> first(hot_rows);
+  for (int32_t i = 0; i < hot_rows; ++i) first[i] = (uint64_t)(uint32_t)i;
+  const uint32_t init_counters[8] = {0, 0, 0, (uint32_t)hot_rows, 0, 0, 0, 0};
   for (int32_t l = 0; good && l < layers; ++l) {
     kvo::LayerView v = {};
     v.hot_rows = (uint32_t)hot_rows;
     v.history_cap = (uint32_t)history_cap;
-    v.counters = c->counters + 4 * l;
+    v.counters = c->counters + 8 * l;
+    v.ring_cap = ring_cap;
     v.stats = c->stats + 8 * l;
     uint8_t* h = nullptr;
     good = ok(cudaHostAlloc((void**)&h, (size_t)history_cap * KVO_ROW_BYTES,
@@ -184,13 +189,14 @@ kvo_status kvo_create(int32_t layers, int64_t history_cap, int32_t hot_rows, int
            ok(cudaMalloc(&v.slot2pos, sizeof(int32_t) * padded_rows)) &&
            ok(cudaMalloc(&v.last_use, sizeof(uint32_t) * padded_rows)) &&
            ok(cudaMalloc(&v.hot, (size_t)hot_rows * KVO_ROW_BYTES)) &&
-           ok(cudaMalloc(&v.order, sizeof(int32_t) * 2 * padded_rows));
+           ok(cudaMalloc(&v.ring, sizeof(uint64_t) * 2 * (size_t)ring_cap));
     c->views.push_back(v);
     good = good && ok(cudaMemset(v.pos2slot, 0xff, sizeof(int32_t) * (size_t)history_cap)) &&
            ok(cudaMemset(v.slot2pos, 0xff, sizeof(int32_t) * padded_rows)) &&
            ok(cudaMemset(v.last_use, 0, sizeof(uint32_t) * padded_rows)) &&
            ok(cudaMemset(v.hot, 0, (size_t)hot_rows * KVO_ROW_BYTES)) &&
-           ok(cudaMemcpy(v.order, iota.data(), sizeof(int32_t) * padded_rows, cudaMemcpyHostToDevice));
+           ok(cudaMemcpy(v.ring, first.data(), sizeof(uint64_t) * (size_t)hot_rows, cudaMemcpyHostToDevice)) &&
+           ok(cudaMemcpy(v.counters, init_counters, sizeof(init_counters), cudaMemcpyHostToDevice));
   }
   if (good) good = ok(cudaDeviceSynchronize());
   if (!good) {

@@ -50,7 +50,6 @@ cudaError_t launch_resolve(const LayerView& L, const int32_t* idx, uint32_t k, u
   a.k = k;
   a.kchunk = (k + C - 1) / C;
   a.hchunk = ((L.hot_rows + C - 1) / C + 127u) & ~127u;
-  if (a.hchunk > kTiles * 4u * kThreads) return cudaErrorInvalidValue;   // order range per CTA too long
   a.fused = 0;
   a.len = 0;
   a.fresh = nullptr;

@@ -12,31 +12,37 @@
 // Victims are the least recently used unpinned slots, keyed (last_use, slot).
 //
 // One thread-block cluster runs the whole call; CTA r owns a contiguous range
-// of selection entries j, a contiguous range of hot slots and the same range
-// of positions of the layer's LRU order (slots sorted by (last_use, slot)).
-//   P0 the CTA's range of the LRU order starts copying to shared memory
-//      (cp.async) while the rest of the call proceeds.
-//   P1 classify: hit = pos2slot[p] >= 0 (stamp last_use = t and set the
-//      slot's bit in its owner's pin bitmap over DSMEM); a miss does an
-//      atomicMin of a negative first-occurrence code into pos2slot[p], so the
-//      smallest j of each missing position wins (dedupe without a table).
-//      Then, while the cluster barrier completes, every row is gathered:
-//      hits from the hot slot (HBM), misses from host memory (zero-copy),
-//      16-byte pieces, one warp per 656-byte row, plus the bf16 dequant.
-//   P2 compact: unique misses are ranked in j order and listed in CTA 0's
-//      shared memory.  When idx is strictly increasing (always true for
-//      kvo_select_topk output) every miss is unique: the counts published at
-//      the first barrier already give every rank.
-//   P3 victims: the i-th unpinned entry of the LRU order, for i < M, is the
-//      victim of the i-th unique miss: one ordered count over the order (each
-//      CTA pulls the whole pin bitmap, counts its unpinned entries and
-//      publishes the count), no selection and no sort.
-//   P4 the CTA holding a victim unmaps the evicted position, maps the new
-//      one, stamps last_use = t and copies the row (from the output just
-//      written) into the victim slot.
-//   P5 the next LRU order: unpinned non-victim entries keep their order
-//      (they shift down by M), then every slot used in this call (hits and
-//      fills, all now last used at t) in slot order.
+// of selection entries j and a contiguous range of hot slots.  The LRU order
+// is a per-layer queue of (stamp, slot) entries in HBM: every call appends
+// one entry, stamped with its step, for every slot it used (hits and fills),
+// in slot order, so the queue runs in (last_use, slot) order; an entry is
+// current while last_use[slot] still equals its stamp, and older entries of
+// a slot are stale and skipped.
+//   P1 classify: hit = pos2slot[p] >= 0 (stamp last_use = t, set the slot's
+//      bit in its owner's used-slot bitmap over DSMEM and count it for the
+//      owner's range); a miss does an atomicMin of a negative
+//      first-occurrence code into pos2slot[p], so the smallest j of each
+//      missing position wins (dedupe without a table).  Then, while the
+//      cluster barrier completes, every row is gathered: hits from the hot
+//      slot (HBM), misses from host memory (zero-copy), 16-byte pieces, one
+//      warp per 656-byte row, plus the bf16 dequant.
+//   P2 unique misses are ranked in j order.  When idx is strictly increasing
+//      (always true for kvo_select_topk output) every miss is unique and the
+//      counts published at the first barrier give every rank; otherwise the
+//      claims are re-read and the counts published once more.
+//   P3 victims: CTA 0 walks the queue from its head.  The current entries,
+//      in order, are the unpinned slots by (last_use, slot) (a slot used in
+//      this call was stamped with t, so its entry is stale); the i-th one
+//      is the victim of the i-th unique miss and goes to the CTA holding
+//      that miss.  CTA 0 also hands every CTA the queue position of its
+//      range's used slots.
+//   P4 the CTA holding a miss unmaps the evicted position, maps the new one,
+//      stamps last_use = t and copies the row (from the output just written)
+//      into the victim slot.
+//   P5 every CTA appends its range's used slots, in slot order, stamped t.
+// When the queue nears its capacity, its current entries are first copied,
+// in order, to the other of its two buffers (a compaction, once every many
+// calls).
 #pragma once
 
 #include <cstdint>
@@ -54,7 +60,7 @@ constexpr int32_t kSlotMiss = -1;
 constexpr int32_t kSlotInvalid = -2;
 constexpr uint32_t kRowVec = KVO_ROW_BYTES / 16;   // 41 16-byte pieces per row
 constexpr uint32_t kRowsInFlight = 4;               // rows a warp loads before it stores
-constexpr uint32_t kTiles = 2;                      // order range per CTA <= kTiles * 4 * kThreads
+constexpr uint32_t kNoRank = 0xffffffffu;
 
 struct ResolveArgs {
   LayerView L;
@@ -64,7 +70,7 @@ struct ResolveArgs {
   uint32_t* status;
   uint32_t k;
   uint32_t kchunk;        // selection entries per CTA
-  uint32_t hchunk;        // hot slots (and LRU order positions) per CTA, a multiple of 128
+  uint32_t hchunk;        // hot slots per CTA, a multiple of 128
   // fused decode step only: the selection is in shared memory, the history
   // length is `len`, and positions >= fresh_from were appended by this very
   // launch and are read from `fresh` (device memory) rather than host memory
@@ -83,32 +89,23 @@ __device__ __forceinline__ const uint4* miss_row(const ResolveArgs& a, const uin
 }
 
 struct SmemLayout {
-  uint32_t miss_pos, miss_j, ord, pinbits, fullbits, meta_slot, meta_pos, uniq, sel, vic_rank, vic_slot, rec,
-      total;
+  uint32_t pinbits, meta_slot, meta_pos, uniq, sel, vslot, total;
 };
 
 __host__ __device__ inline uint32_t round16(uint32_t x) { return (x + 15u) & ~15u; }
 
-// hchunk: slots (and order positions) per CTA, a multiple of 128 so that the
-// pin bitmap of a CTA is whole 16-byte pieces of the layer's bitmap.
+// hchunk: slots per CTA, a multiple of 128 (whole 16-byte pieces of bitmap).
 __host__ __device__ inline SmemLayout smem_layout(uint32_t k, uint32_t kchunk, uint32_t hchunk, uint32_t hot_rows) {
+  (void)k;
+  (void)hot_rows;
   SmemLayout s;
-  const uint32_t vcap = k < hchunk ? k : hchunk;   // victims one CTA can hold
   uint32_t o = 0;
-  s.miss_pos = o;  o += k * 4u;                 // CTA 0: unique misses in j order
-  s.miss_j = o;    o += k * 4u;
-  o = round16(o);
-  s.ord = o;       o += hchunk * 4u;            // this CTA's range of the LRU order
   s.pinbits = o;   o += round16(hchunk / 8u);   // this CTA's slots used in this call
-  s.fullbits = o;  o += round16((hot_rows + 31u) / 32u * 4u);   // every slot pinned in this call
   s.meta_slot = o; o += kchunk * 4u;            // per entry: hot slot, or miss / invalid
   s.meta_pos = o;  o += kchunk * 4u;            // per entry: position
-  s.uniq = o;      o += kchunk * 4u;            // per entry: 1 = unique miss
+  s.uniq = o;      o += kchunk * 4u;            // per entry: rank among this CTA's unique misses, or kNoRank
   s.sel = o;       o += kchunk * 4u;            // fused step: this CTA's selected positions
-  s.vic_rank = o;  o += vcap * 4u;              // victims found in this CTA's order range
-  s.vic_slot = o;  o += vcap * 4u;
-  o = round16(o);
-  s.rec = o;       o += kchunk * 16u;           // victims this CTA maps and fills: (slot, pos, j, rank)
+  s.vslot = o;     o += kchunk * 4u;            // per unique miss (local rank): its victim slot
   s.total = round16(o);
   return s;
 }
@@ -155,7 +152,7 @@ __device__ __forceinline__ void dequant_row(const uint4& va, const uint4& vb, ui
 }
 
 // Copies one 656-byte row with a warp (L2 reads: the source may have been
-// written by another CTA of this launch).
+// written by another warp of this launch).
 __device__ __forceinline__ void copy_row(const uint4* src, uint4* dst, uint32_t lane) {
   const uint4 x = __ldcg(src + lane);
   uint4 y = make_uint4(0, 0, 0, 0);
@@ -185,14 +182,61 @@ __device__ __forceinline__ uint32_t map_update(const ResolveArgs& a, uint32_t v,
   return old >= 0 ? 1u : 0u;
 }
 
+// A queue entry: stamp in the upper 32 bits, slot in the lower.
+__device__ __forceinline__ bool entry_current(const LayerView& L, uint64_t e) {
+  const uint32_t sl = (uint32_t)e;
+  return sl < L.hot_rows && __ldcg(&L.last_use[sl]) == (uint32_t)(e >> 32);
+}
+
+// Copies the current entries of [head, tail) of ring buffer `buf`, in order,
+// to the front of the other buffer.  Every CTA of the cluster calls it; it
+// returns the number of entries kept (the number of slots).
+static __device__ __noinline__ uint32_t compact_queue(const LayerView& L, uint32_t head, uint32_t tail, uint32_t buf,
+                                  uint32_t (*scratch)[2 * kWarps + 2], uint32_t (*table)[4]) {
+  const uint32_t tid = threadIdx.x, r = cluster_rank(), C = cluster_size();
+  const uint32_t Q = L.ring_cap, qmask = Q - 1u;
+  const uint64_t* src = L.ring + (size_t)buf * Q;
+  uint64_t* dst = L.ring + (size_t)(buf ^ 1u) * Q;
+  const uint32_t span = tail - head;
+  const uint32_t chunk = (span + C - 1u) / C;
+  const uint32_t lo = min(span, r * chunk), hi = min(span, lo + chunk);
+  cluster_sync();                                   // every CTA is running before the publish below
+  uint32_t c = 0;
+  for (uint32_t i = lo + tid; i < hi; i += kThreads) c += entry_current(L, src[(head + i) & qmask]);
+  const uint32_t mine[1] = {block_sum(c, scratch[1])};
+  cluster_publish(mine, 1, table, r, C);
+  uint32_t before = 0, total = 0;
+  for (uint32_t q = 0; q < C; ++q) {
+    before += q < r ? table[q][0] : 0u;
+    total += table[q][0];
+  }
+  uint32_t run = 0;
+  for (uint32_t base = lo; base < hi; base += kThreads) {
+    const uint32_t i = base + tid;
+    uint64_t e = 0;
+    bool keep = false;
+    if (i < hi) {
+      e = src[(head + i) & qmask];
+      keep = entry_current(L, e);
+    }
+    uint32_t tile;
+    const uint32_t rank = block_flag_scan(keep, scratch[0], &tile);
+    if (keep && before + run + rank < Q) dst[before + run + rank] = e;
+    run += tile;
+  }
+  return total;
+}
+
 __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_smem) {
   __shared__ uint32_t scratch[2][2 * kWarps + 2];
-  __shared__ uint32_t table[kMaxCluster][4];
-  __shared__ uint32_t table2[kMaxCluster][4];
-  __shared__ uint32_t table3[kMaxCluster][4];
-  __shared__ uint32_t tcount[kMaxCluster];         // victims per slot-owner CTA, over the cluster
-  __shared__ uint32_t ocount[kMaxCluster];         // victims per slot-owner CTA found here
-  __shared__ uint32_t nvic;
+  __shared__ uint32_t table[kMaxCluster][4];       // per CTA: (idx not increasing, misses)
+  __shared__ uint32_t table2[kMaxCluster][4];      // idx not increasing: (unique misses, used hit slots)
+  __shared__ uint32_t hitcnt[kMaxCluster];         // CTA 0: hit slots per owner range
+  __shared__ uint32_t fillcnt[kMaxCluster];        // CTA 0: victims per owner range
+  __shared__ uint32_t own_hits[kMaxCluster];       // this CTA's hits per owner range
+  __shared__ uint32_t mbefore[kMaxCluster + 1];    // CTA 0: unique misses of lower CTAs
+  __shared__ uint32_t ring_off;                    // queue position of this range's used slots
+  __shared__ uint32_t head_hit;                    // CTA 0: offset of the first current entry left
   __shared__ uint32_t nevict_cta;
   __shared__ uint32_t cta_hits, cta_inv;
 
@@ -203,39 +247,45 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
   const uint32_t H = L.hot_rows;
 
   const SmemLayout lay = smem_layout(k, a.kchunk, a.hchunk, H);
-  int32_t* miss_pos = reinterpret_cast<int32_t*>(dyn_smem + lay.miss_pos);
-  int32_t* miss_j = reinterpret_cast<int32_t*>(dyn_smem + lay.miss_j);
-  int32_t* ord = reinterpret_cast<int32_t*>(dyn_smem + lay.ord);
   uint32_t* pinbits = reinterpret_cast<uint32_t*>(dyn_smem + lay.pinbits);
-  uint32_t* fullbits = reinterpret_cast<uint32_t*>(dyn_smem + lay.fullbits);
   int32_t* meta_slot = reinterpret_cast<int32_t*>(dyn_smem + lay.meta_slot);
   int32_t* meta_pos = reinterpret_cast<int32_t*>(dyn_smem + lay.meta_pos);
   uint32_t* uniq = reinterpret_cast<uint32_t*>(dyn_smem + lay.uniq);
   const int32_t* sel = reinterpret_cast<const int32_t*>(dyn_smem + lay.sel);
-  uint32_t* vic_rank = reinterpret_cast<uint32_t*>(dyn_smem + lay.vic_rank);
-  uint32_t* vic_slot = reinterpret_cast<uint32_t*>(dyn_smem + lay.vic_slot);
-  uint4* rec = reinterpret_cast<uint4*>(dyn_smem + lay.rec);
+  uint32_t* vslot = reinterpret_cast<uint32_t*>(dyn_smem + lay.vslot);
 
   const uint32_t t = L.counters[0] + 1u;        // this call's step
   const uint32_t len = a.fused ? a.len : L.counters[1];
+  uint32_t head = L.counters[2], tail = L.counters[3], buf = L.counters[4] & 1u;
+  const uint32_t Q = L.ring_cap, qmask = Q - 1u;
   const uint32_t jlo = min(k, r * a.kchunk), jhi = min(k, jlo + a.kchunk), jcnt = jhi - jlo;
   const uint32_t slo = min(H, r * a.hchunk), shi = min(H, slo + a.hchunk), hcnt = shi - slo;
-  const uint32_t words = a.hchunk / 32u;         // pin-bitmap words per CTA
-  const uint32_t Hp = (H + 3u) & ~3u;            // order buffers are padded to whole 16-byte pieces
-  const int32_t* ord_in = L.order + (size_t)((t + 1u) & 1u) * Hp;   // written by the previous call
-  int32_t* ord_out = L.order + (size_t)(t & 1u) * Hp;
+  const uint32_t words = a.hchunk / 32u;         // used-slot bitmap words per CTA
+
+  // ------------------------------------------------- queue compaction
+  // This call appends at most k entries; make room first when needed (every
+  // CTA read the same counters, so every CTA takes the same branch).
+  if (tail - head > Q - k) {
+    tail = compact_queue(L, head, tail, buf, scratch, table2);
+    head = 0;
+    buf ^= 1u;
+    if (r == 0 && tid == 0 && tail != H) atomicOr(a.status, kFlagInternal);
+  }
+  const uint64_t* ring_in = L.ring + (size_t)buf * Q;
+  uint64_t* ring_out = L.ring + (size_t)buf * Q;
 
   // ---------------------------------------------------------------- P0
   for (uint32_t i = tid; i < words; i += kThreads) pinbits[i] = 0;
-  for (uint32_t i = tid; i < (H + 31u) / 32u; i += kThreads) fullbits[i] = 0;
-  for (uint32_t i = tid; i < (hcnt + 3) / 4; i += kThreads) cp_async16(ord + 4 * i, ord_in + slo + 4 * i);
+  for (uint32_t i = tid; i < jcnt; i += kThreads) vslot[i] = kNoRank;
   if (tid < kMaxCluster) {
-    tcount[tid] = 0;
-    ocount[tid] = 0;
+    hitcnt[tid] = 0;
+    fillcnt[tid] = 0;
+    own_hits[tid] = 0;
   }
   if (tid == 0) {
-    nvic = 0;
     nevict_cta = 0;
+    ring_off = 0;
+    head_hit = kNoRank;
   }
   // B0: every CTA of the cluster is running (and has zeroed what others add
   // into) before any DSMEM access; classification overlaps the barrier.
@@ -253,10 +303,15 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
       slot = kSlotInvalid;
       ++ninv;
     } else {
-      const int32_t s = L.pos2slot[p];
+      int32_t s = L.pos2slot[p];
+      if (s >= (int32_t)H) {
+        atomicOr(a.status, kFlagInternal);          // cannot happen; keep every index in bounds
+        s = -1;
+      }
       if (s >= 0) {
         slot = s;
         L.last_use[s] = t;
+        atomicAdd(&own_hits[(uint32_t)s / a.hchunk], 1u);
         ++nhit;
       } else {
         slot = kSlotMiss;
@@ -275,7 +330,7 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
     const bool f = jj < jcnt && meta_slot[jj] == kSlotMiss;
     uint32_t tile;
     const uint32_t rank = block_flag_scan(f, scratch[0], &tile);
-    if (f) uniq[jj] = cta_miss + rank;
+    if (jj < jcnt) uniq[jj] = f ? cta_miss + rank : kNoRank;
     cta_miss += tile;
   }
   uint32_t cta_unordered, cta_hit_inv;
@@ -286,12 +341,16 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
   }
   cluster_wait();                                   // B0
   if (tid < 2 * C) dsmem_st_u32(dsmem_addr(&table[r][tid & 1], tid >> 1), (tid & 1) ? cta_miss : cta_unordered);
-  // pin: every CTA gets every hit slot's bit
-  for (uint32_t i = tid; i < jcnt * C; i += kThreads) {
-    const uint32_t jj = i / C, q = i - jj * C;
+  // pin: every hit slot's bit goes to the CTA that owns the slot
+  for (uint32_t jj = tid; jj < jcnt; jj += kThreads) {
     const int32_t sl = meta_slot[jj];
-    if (sl >= 0) dsmem_red_or_u32(dsmem_addr(&fullbits[(uint32_t)sl >> 5], q), 1u << ((uint32_t)sl & 31));
+    if (sl >= 0) {
+      const uint32_t owner = (uint32_t)sl / a.hchunk, b = (uint32_t)sl - owner * a.hchunk;
+      dsmem_red_or_u32(dsmem_addr(&pinbits[b >> 5], owner), 1u << (b & 31));
+    }
   }
+  // hit counts per owner range (exact when idx does not repeat a position)
+  if (tid < C && own_hits[tid]) dsmem_red_add_u32(dsmem_addr(&hitcnt[tid], 0), own_hits[tid]);
   cluster_arrive();                                 // B1: stamps, claims, counts, pins
 
   // Each warp loads up to kRowsInFlight rows before storing any, so that all
@@ -330,7 +389,6 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
         dequant_row(va[u], vb[u], lane, reinterpret_cast<uint4*>(a.out_bf16 + (size_t)j * KVO_DEQUANT_VALUES));
     }
   }
-  cp_async_wait_all();
   cluster_wait();                                   // B1
 
   // ---------------------------------------------------------------- P2
@@ -341,174 +399,136 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
     uniq_before += q < r ? table[q][1] : 0u;
     M += table[q][1];
   }
-  if (!any_unordered) {
-    // strictly increasing idx: every miss is a distinct position, ranked in P1
-    if (M > 0) {
-      const uint32_t mp0 = dsmem_addr(miss_pos, 0), mj0 = dsmem_addr(miss_j, 0);
-      for (uint32_t jj = tid; jj < jcnt; jj += kThreads) {
-        const uint32_t i = uniq_before + uniq[jj];
-        if (meta_slot[jj] == kSlotMiss && i < k) {
-          dsmem_st_u32(mp0 + 4u * i, (uint32_t)meta_pos[jj]);
-          dsmem_st_u32(mj0 + 4u * i, jlo + jj);
-        }
-      }
-    }
-  } else {
-    // The smallest claiming j owns each missing position; the claims came
-    // from other CTAs, so read them from L2.
+  const uint32_t (*mtab)[4] = table;               // column 1: unique misses per CTA
+  uint32_t mcol = 1;
+  if (any_unordered) {
+    // The smallest claiming j owns each missing position (claims came from
+    // other CTAs: read them from L2); unique hit slots are counted from the
+    // owners' bitmaps, so that a repeated position counts once.
     uint32_t nuniq = 0;
-    for (uint32_t jj = tid; jj < jcnt; jj += kThreads) {
-      const bool u = meta_slot[jj] == kSlotMiss &&
+    for (uint32_t base = 0; base < jcnt; base += kThreads) {
+      const uint32_t jj = base + tid;
+      const bool f = jj < jcnt && meta_slot[jj] == kSlotMiss &&
                      __ldcg(&L.pos2slot[meta_pos[jj]]) == (int32_t)(jlo + jj) - (int32_t)k - 1;
-      uniq[jj] = u;
-      nuniq += u;
+      uint32_t tile;
+      const uint32_t rank = block_flag_scan(f, scratch[0], &tile);
+      if (jj < jcnt) uniq[jj] = f ? nuniq + rank : kNoRank;
+      nuniq += tile;
     }
-    nuniq = block_sum(nuniq, scratch[1]);
-    const uint32_t mine1[1] = {nuniq};
-    cluster_publish(mine1, 1, table2, r, C);       // B2 (only for an unordered idx)
+    uint32_t used = 0;
+    for (uint32_t w = tid; w < words; w += kThreads) used += __popc(pinbits[w]);
+    const uint32_t mine2[2] = {nuniq, block_sum(used, scratch[1])};
+    cluster_publish(mine2, 2, table2, r, C);       // B2 (only for an idx that is not increasing)
     uniq_before = 0;
     M = 0;
     for (uint32_t q = 0; q < C; ++q) {
       uniq_before += q < r ? table2[q][0] : 0u;
       M += table2[q][0];
     }
+    mtab = table2;
+    mcol = 0;
   }
   if (r == 0 && tid == 0) L.counters[0] = t;       // every CTA read the old step before B1
-  if (M > 0 && any_unordered) {
-    const uint32_t mp0 = dsmem_addr(miss_pos, 0), mj0 = dsmem_addr(miss_j, 0);
-    uint32_t run = 0;
-    for (uint32_t base = 0; base < jcnt; base += kThreads) {
-      const uint32_t jj = base + tid;
-      const bool f = jj < jcnt && uniq[jj];
-      uint32_t tile;
-      const uint32_t rank = block_flag_scan(f, scratch[0], &tile);
-      const uint32_t i = uniq_before + run + rank;
-      if (f && i < k) {
-        dsmem_st_u32(mp0 + 4u * i, (uint32_t)meta_pos[jj]);
-        dsmem_st_u32(mj0 + 4u * i, jlo + jj);
-      }
-      run += tile;
-    }
-  }
 
   // ---------------------------------------------------------------- P3
-  // the layer's pin bitmap arrived before B1; this CTA's own slots are
-  // words [slo / 32, slo / 32 + words) of it
-  const uint32_t hwords = (hcnt + 31u) / 32u;     // words of this CTA's own slots (none if it has none)
-  uint32_t mypins = 0;
-  for (uint32_t w = tid; w < hwords; w += kThreads) mypins += __popc(fullbits[slo / 32u + w]);
-  // Ordered pass over this CTA's order range, four entries per thread: the
-  // unpinned entry of rank u is the victim of unique miss u when u < M, else
-  // it survives at position u - M of the next order.
-  uint32_t cnt4[kTiles], total4[kTiles], unpinned = 0;
-#pragma unroll
-  for (uint32_t tile = 0; tile < kTiles; ++tile) {
-    const uint32_t i0 = 4 * (tile * kThreads + tid);
-    uint32_t c = 0;
-#pragma unroll
-    for (uint32_t e = 0; e < 4; ++e) {
-      if (i0 + e < hcnt) {
-        const uint32_t sl = (uint32_t)ord[i0 + e];
-        c += ((fullbits[sl >> 5] >> (sl & 31)) & 1u) ^ 1u;
-      }
-    }
-    cnt4[tile] = c;
-    unpinned += c;
-  }
-  uint32_t cta_unpinned, cta_pins;
-  block_sum2(unpinned, mypins, scratch[1], &cta_unpinned, &cta_pins);
-  const uint32_t mine3[2] = {cta_unpinned, cta_pins};
-  cluster_publish(mine3, 2, table3, r, C);         // B3: also fences the pin-bitmap pulls
-  uint32_t u_run = 0;
-  for (uint32_t q = 0; q < r; ++q) u_run += table3[q][0];
-#pragma unroll
-  for (uint32_t tile = 0; tile < kTiles; ++tile) {
-    if (tile * 4u * kThreads >= hcnt) break;       // uniform over the CTA
-    const uint32_t i0 = 4 * (tile * kThreads + tid);
-    uint32_t u = u_run + block_excl_sum(cnt4[tile], scratch[tile & 1], &total4[tile]);
-#pragma unroll
-    for (uint32_t e = 0; e < 4; ++e) {
-      if (i0 + e < hcnt) {
-        const uint32_t sl = (uint32_t)ord[i0 + e];
-        if (!((fullbits[sl >> 5] >> (sl & 31)) & 1u)) {
-          if (u < M) {
-            const uint32_t c = atomicAdd(&nvic, 1u);
-            vic_rank[c] = u;
-            vic_slot[c] = sl;
-          } else if (u - M < H) {
-            ord_out[u - M] = (int32_t)sl;
-          }
-          ++u;
-        }
-      }
-    }
-    u_run += total4[tile];
-  }
-  __syncthreads();
-
-  // ---------------------------------------------------------------- P4
-  // The CTA holding a victim marks it used (its owner's bit), counts it for
-  // its owner and sends (slot, position, entry, rank) to the handler CTA
-  // rank % C, which then maps it and copies its row.
-  const uint32_t nv = nvic;
-  if (M > 0) {
-    for (uint32_t c = tid; c < nv; c += kThreads) {
-      const uint32_t u = vic_rank[c] < M ? vic_rank[c] : 0u, v = vic_slot[c];
-      const uint32_t p = dsmem_ld_u32(dsmem_addr(&miss_pos[u], 0));
-      const uint32_t j = dsmem_ld_u32(dsmem_addr(&miss_j[u], 0));
-      const uint32_t h = u % C;
-      dsmem_st_v4(dsmem_addr(&rec[u / C], h), make_uint4(v, p, j, u));
-      const uint32_t owner = v / a.hchunk, b = v - owner * a.hchunk;
-      dsmem_red_or_u32(dsmem_addr(&pinbits[b >> 5], owner), 1u << (b & 31));   // used in this call
-      atomicAdd(&ocount[owner], 1u);
+  // CTA 0 walks the queue from its head: the current entries are the
+  // unpinned slots in (last_use, slot) order; the u-th is the victim of
+  // unique miss u, sent to the CTA holding that miss.
+  if (r == 0) {
+    if (tid <= C) {
+      uint32_t b = 0;
+      for (uint32_t q = 0; q < tid; ++q) b += mtab[q][mcol];
+      mbefore[tid] = b;
     }
     __syncthreads();
-    // every CTA learns how many fills landed in each owner's slot range
-    for (uint32_t i = tid; i < C * C; i += kThreads) {
-      const uint32_t o = i / C, q = i - o * C;
-      const uint32_t n = ocount[o];
-      if (n) dsmem_red_add_u32(dsmem_addr(&tcount[o], q), n);
+    const uint32_t span = tail - head;
+    uint32_t found = 0, off = 0;
+    while (found < M && off < span) {              // uniform over the CTA
+      uint64_t e[4];                               // ~0 marks an entry that is not current
+      uint32_t ncur = 0;
+#pragma unroll
+      for (uint32_t q = 0; q < 4; ++q) {
+        const uint32_t o = off + 4 * tid + q;
+        e[q] = o < span ? __ldcg(&ring_in[(head + o) & qmask]) : ~0ull;
+        if (e[q] != ~0ull && entry_current(L, e[q])) ++ncur;
+        else e[q] = ~0ull;
+      }
+      uint32_t tot;
+      uint32_t u = found + block_excl_sum(ncur, scratch[0], &tot);
+#pragma unroll
+      for (uint32_t q = 0; q < 4; ++q) {
+        if (e[q] == ~0ull) continue;
+        const uint32_t sl = (uint32_t)e[q];
+        if (u < M) {
+          uint32_t h = 0;
+          while (h + 1 < C && mbefore[h + 1] <= u) ++h;
+          dsmem_st_u32(dsmem_addr(&vslot[u - mbefore[h]], h), sl);
+          const uint32_t owner = sl / a.hchunk, b = sl - owner * a.hchunk;
+          dsmem_red_or_u32(dsmem_addr(&pinbits[b >> 5], owner), 1u << (b & 31));   // used in this call
+          atomicAdd(&fillcnt[owner], 1u);
+        } else if (u == M) {
+          head_hit = off + 4 * tid + q;            // the first current entry that stays
+        }
+        ++u;
+      }
+      found += tot;
+      off += 4 * kThreads;
     }
-    cluster_sync();                                 // B4: records, bits and counts delivered
-    const uint32_t nrec = r < M ? (M - r + C - 1) / C : 0u;
-    for (uint32_t c = tid; c < nrec; c += kThreads) {
-      const uint4 rc = rec[c];
-      if (map_update(a, rc.x, L.slot2pos[rc.x], (int32_t)rc.y, t, rc.w)) atomicAdd(&nevict_cta, 1u);
+    __syncthreads();
+    if (tid == 0) {
+      // every range's used slots go to the tail, ranges in slot order
+      uint32_t pos = tail;
+      for (uint32_t q = 0; q < C; ++q) {
+        const uint32_t hq = any_unordered ? table2[q][1] : hitcnt[q];
+        dsmem_st_u32(dsmem_addr(&ring_off, q), pos);
+        pos += hq + fillcnt[q];
+      }
+      uint32_t nh = head;
+      if (M > 0) nh = head + (head_hit != kNoRank ? head_hit : min(off, span));
+      L.counters[2] = nh;
+      L.counters[3] = pos;
+      L.counters[4] = buf;
     }
-    for (uint32_t c = warp; c < nrec; c += kWarps) {
-      const uint4 rc = rec[c];
-      const uint32_t v = rc.x, j = rc.z;
-      const int32_t p = (int32_t)rc.y;
-      if (v >= H || j >= k || p < 0 || (uint32_t)p >= L.history_cap) continue;
-      // the output row written in P1 (by any CTA), else the host row
-      const uint4* src = a.out_rows ? reinterpret_cast<const uint4*>(a.out_rows) + (size_t)j * kRowVec
-                                    : miss_row(a, hist4, p);
-      copy_row(src, reinterpret_cast<uint4*>(L.hot) + (size_t)v * kRowVec, lane);
-    }
+  }
+  cluster_sync();                                   // B3: victims, bits and queue positions delivered
+
+  // ---------------------------------------------------------------- P4
+  for (uint32_t jj = tid; jj < jcnt; jj += kThreads) {
+    const uint32_t lr = uniq[jj];
+    if (lr == kNoRank) continue;
+    const uint32_t v = vslot[lr < jcnt ? lr : 0];
+    const int32_t old = v < H ? __ldcg(&L.slot2pos[v]) : -1;
+    if (map_update(a, v, old, meta_pos[jj], t, uniq_before + lr)) atomicAdd(&nevict_cta, 1u);
+  }
+  for (uint32_t jj = warp; jj < jcnt; jj += kWarps) {
+    const uint32_t lr = uniq[jj];
+    if (lr == kNoRank) continue;
+    const uint32_t v = vslot[lr < jcnt ? lr : 0];
+    const int32_t p = meta_pos[jj];
+    if (v >= H || p < 0 || (uint32_t)p >= L.history_cap) continue;
+    // the output row this CTA wrote in P1, else the host row
+    const uint4* src = a.out_rows ? reinterpret_cast<const uint4*>(a.out_rows) + (size_t)(jlo + jj) * kRowVec
+                                  : miss_row(a, hist4, p);
+    copy_row(src, reinterpret_cast<uint4*>(L.hot) + (size_t)v * kRowVec, lane);
   }
 
   // ---------------------------------------------------------------- P5
-  // The used slots, in slot order, fill the end of the next order: one
-  // 32-bit word of this CTA's used-slot bitmap per thread.
+  // The used slots of this CTA's range, in slot order, stamped t, at the
+  // queue position CTA 0 assigned: one 32-bit bitmap word per thread.
   {
-    uint32_t used_before = 0, used = 0;
-    for (uint32_t q = 0; q < C; ++q) {
-      const uint32_t n_q = table3[q][1] + tcount[q];
-      used_before += q < r ? n_q : 0u;
-      used += n_q;
-    }
-    const uint32_t tail0 = H - used + used_before;
+    const uint32_t hwords = (hcnt + 31u) / 32u;
+    const uint64_t stamp = (uint64_t)t << 32;
     uint32_t run = 0;
     for (uint32_t w0 = 0; w0 < hwords; w0 += kThreads) {
       const uint32_t w = w0 + tid;
-      uint32_t bits = w < hwords ? pinbits[w] | fullbits[slo / 32u + w] : 0u;
+      uint32_t bits = w < hwords ? pinbits[w] : 0u;
       uint32_t tot;
-      uint32_t pos = tail0 + run + block_excl_sum(__popc(bits), scratch[0], &tot);
+      uint32_t pos = ring_off + run + block_excl_sum(__popc(bits), scratch[0], &tot);
       while (bits) {
         const uint32_t b = __ffs(bits) - 1;
         bits &= bits - 1;
         const uint32_t i = 32 * w + b;
-        if (i < hcnt && pos < H) ord_out[pos] = (int32_t)(slo + i);
+        if (i < hcnt) ring_out[pos & qmask] = stamp | (uint64_t)(slo + i);
         ++pos;
       }
       run += tot;

@@ -102,7 +102,6 @@ cudaError_t launch_decode_step(const LayerView& L, const void* new_rows, uint32_
   a.k = k;
   a.kchunk = (k + C - 1) / C;
   a.hchunk = ((L.hot_rows + C - 1) / C + 127u) & ~127u;
-  if (a.hchunk > kTiles * 4u * kThreads) return cudaErrorInvalidValue;   // order range per CTA too long
   a.fused = 1;
   a.len = old_len + r;
   a.fresh = r ? static_cast<const uint8_t*>(new_rows) : nullptr;

@@ -132,6 +132,33 @@ def test_resolve_random_selections(kvo, seed, H, n, k, dup, bad):
     ctx.close()
 
 
+@pytest.mark.parametrize("H,k,sub,dup", [(64, 64, 100, 0.0), (64, 40, 90, 0.0), (64, 8, 70, 0.0), (64, 40, 90, 0.3)])
+def test_lru_queue_compaction_over_many_steps(kvo, H, k, sub, dup):
+    """Selections drawn from a small range of positions, so most entries hit
+    and few slots are evicted: the LRU queue fills with stale entries and is
+    compacted many times over 120 steps.  Evictions compared every step."""
+    import torch
+    n = 400
+    hist = np.random.default_rng(H + k).integers(0, 256, size=(n, O.ROW_BYTES), dtype=np.uint8)
+    ctx = kvo.Context(1, n, H)
+    ctx.append_rows(0, hist)
+    ctx.record_evictions(True)
+    st = O.LayerState(n, H)
+    st.append(hist)
+    out = torch.empty((k, O.ROW_BYTES), dtype=torch.uint8, device="cuda")
+    for step in range(120):
+        idx = W.random_idx(7000 + step, sub if step % 10 else n, k, dup, 0)
+        if dup == 0.0:
+            idx = np.sort(idx)
+        ctx.resolve_gather(0, torch.from_numpy(idx).cuda(), out)
+        res = O.resolve_gather(st, idx)
+        np.testing.assert_array_equal(out.cpu().numpy(), res.rows)
+        assert ctx.evictions(0) == res.evictions, step
+    assert ctx.sync() == 0
+    compare_state(ctx, 0, st)
+    ctx.close()
+
+
 def test_hot_cache_exactly_k_rows(kvo):
     """k = hot_rows: every slot may be needed in one step."""
     import torch

@@ -288,6 +288,7 @@ kvo_status kvo_sync(kvo_ctx* ctx, void* stream) {
   if (!ok(cudaMemcpy(&st, ctx->status, sizeof st, cudaMemcpyDeviceToHost))) return KVO_ECUDA;
   if (st == 0) return KVO_OK;
   if (!ok(cudaMemset(ctx->status, 0, sizeof st))) return KVO_ECUDA;
+  if (st & kvo::kFlagTimeout) return KVO_ETIMEDOUT;
   if (st & kvo::kFlagRange) return KVO_ERANGE;
   return KVO_ECUDA;
 }

@@ -48,7 +48,7 @@ cudaError_t launch_resolve(const LayerView& L, const int32_t* idx, uint32_t k, u
   a.out_bf16 = out_bf16;
   a.status = status;
   a.k = k;
-  a.kchunk = (k + C - 1) / C;
+  a.kchunk = (k + C - 2) / (C - 1);                 // CTA 0 keeps the LRU order, CTAs 1..C-1 the entries
   a.hchunk = ((L.hot_rows + C - 1) / C + 127u) & ~127u;
   a.fused = 0;
   a.len = 0;

@@ -11,8 +11,9 @@
 //     read host memory directly, and slots used by this round are pinned.
 // Victims are the least recently used unpinned slots, keyed (last_use, slot).
 //
-// One thread-block cluster runs the whole call; CTA r owns a contiguous range
-// of selection entries j and a contiguous range of hot slots.  The LRU order
+// One thread-block cluster runs the whole call.  CTA 0 keeps the LRU order;
+// every other CTA owns a contiguous range of selection entries j; every CTA
+// owns a contiguous range of hot slots.  The LRU order
 // is a per-layer queue of (stamp, slot) entries in HBM: every call appends
 // one entry, stamped with its step, for every slot it used (hits and fills),
 // in slot order, so the queue runs in (last_use, slot) order; an entry is
@@ -30,7 +31,10 @@
 //      (always true for kvo_select_topk output) every miss is unique and the
 //      counts published at the first barrier give every rank; otherwise the
 //      claims are re-read and the counts published once more.
-//   P3 victims: CTA 0 walks the queue from its head.  The current entries,
+//   P3 victims: CTA 0 copies the head of the queue (TMA bulk copy) and reads
+//      its entries' last_use while the other CTAs classify and gather; after
+//      the barrier it only has to drop the slots pinned in this call.  It
+//      walks the queue from its head.  The current entries,
 //      in order, are the unpinned slots by (last_use, slot) (a slot used in
 //      this call was stamped with t, so its entry is stale); the i-th one
 //      is the victim of the i-th unique miss and goes to the CTA holding
@@ -61,6 +65,8 @@ constexpr int32_t kSlotInvalid = -2;
 constexpr uint32_t kRowVec = KVO_ROW_BYTES / 16;   // 41 16-byte pieces per row
 constexpr uint32_t kRowsInFlight = 4;               // rows a warp loads before it stores
 constexpr uint32_t kNoRank = 0xffffffffu;
+constexpr uint32_t kWindow = 4 * kThreads;          // LRU queue entries CTA 0 examines per round
+constexpr uint32_t kWindowPolls = 1u << 18;         // bound on the wait for the window copy (~20 ms)
 
 struct ResolveArgs {
   LayerView L;
@@ -69,7 +75,7 @@ struct ResolveArgs {
   uint16_t* out_bf16;
   uint32_t* status;
   uint32_t k;
-  uint32_t kchunk;        // selection entries per CTA
+  uint32_t kchunk;        // selection entries per CTA (CTAs 1..C-1; CTA 0 has none)
   uint32_t hchunk;        // hot slots per CTA, a multiple of 128
   // fused decode step only: the selection is in shared memory, the history
   // length is `len`, and positions >= fresh_from were appended by this very
@@ -89,7 +95,7 @@ __device__ __forceinline__ const uint4* miss_row(const ResolveArgs& a, const uin
 }
 
 struct SmemLayout {
-  uint32_t pinbits, meta_slot, meta_pos, uniq, sel, vslot, total;
+  uint32_t pinbits, meta_slot, meta_pos, uniq, sel, vslot, mlist, window, fullpin, total;
 };
 
 __host__ __device__ inline uint32_t round16(uint32_t x) { return (x + 15u) & ~15u; }
@@ -97,7 +103,6 @@ __host__ __device__ inline uint32_t round16(uint32_t x) { return (x + 15u) & ~15
 // hchunk: slots per CTA, a multiple of 128 (whole 16-byte pieces of bitmap).
 __host__ __device__ inline SmemLayout smem_layout(uint32_t k, uint32_t kchunk, uint32_t hchunk, uint32_t hot_rows) {
   (void)k;
-  (void)hot_rows;
   SmemLayout s;
   uint32_t o = 0;
   s.pinbits = o;   o += round16(hchunk / 8u);   // this CTA's slots used in this call
@@ -106,6 +111,10 @@ __host__ __device__ inline SmemLayout smem_layout(uint32_t k, uint32_t kchunk, u
   s.uniq = o;      o += kchunk * 4u;            // per entry: rank among this CTA's unique misses, or kNoRank
   s.sel = o;       o += kchunk * 4u;            // fused step: this CTA's selected positions
   s.vslot = o;     o += kchunk * 4u;            // per unique miss (local rank): its victim slot
+  s.mlist = o;     o += kchunk * 4u;            // per unique miss (local rank): its entry
+  o = round16(o);
+  s.window = o;    o += kWindow * 8u;           // CTA 0: the first queue entries, copied early
+  s.fullpin = o;   o += round16((hot_rows + 31u) / 32u * 4u);   // CTA 0: every slot hit in this call
   s.total = round16(o);
   return s;
 }
@@ -149,16 +158,6 @@ __device__ __forceinline__ void dequant_row(const uint4& va, const uint4& vb, ui
   d[2 * lane] = make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
   d[2 * lane + 1] = make_uint4(pack2(f[8], f[9]), pack2(f[10], f[11]), pack2(f[12], f[13]), pack2(f[14], f[15]));
   if (lane >= 1 && lane < kRowVec - 32) d[64 + (lane - 1)] = vb;   // RoPE, copied
-}
-
-// Copies one 656-byte row with a warp (L2 reads: the source may have been
-// written by another warp of this launch).
-__device__ __forceinline__ void copy_row(const uint4* src, uint4* dst, uint32_t lane) {
-  const uint4 x = __ldcg(src + lane);
-  uint4 y = make_uint4(0, 0, 0, 0);
-  if (lane < kRowVec - 32) y = __ldcg(src + 32 + lane);
-  dst[lane] = x;
-  if (lane < kRowVec - 32) dst[32 + lane] = y;
 }
 
 // One map update: slot v receives position p, evicting `old` (or -1).
@@ -239,6 +238,7 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
   __shared__ uint32_t head_hit;                    // CTA 0: offset of the first current entry left
   __shared__ uint32_t nevict_cta;
   __shared__ uint32_t cta_hits, cta_inv;
+  __shared__ __align__(8) uint64_t wbar;           // CTA 0: completion of the window copy
 
   const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t r = cluster_rank(), C = cluster_size();
@@ -253,12 +253,16 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
   uint32_t* uniq = reinterpret_cast<uint32_t*>(dyn_smem + lay.uniq);
   const int32_t* sel = reinterpret_cast<const int32_t*>(dyn_smem + lay.sel);
   uint32_t* vslot = reinterpret_cast<uint32_t*>(dyn_smem + lay.vslot);
+  uint32_t* mlist = reinterpret_cast<uint32_t*>(dyn_smem + lay.mlist);
+  uint64_t* window = reinterpret_cast<uint64_t*>(dyn_smem + lay.window);
+  uint32_t* fullpin = reinterpret_cast<uint32_t*>(dyn_smem + lay.fullpin);
 
   const uint32_t t = L.counters[0] + 1u;        // this call's step
   const uint32_t len = a.fused ? a.len : L.counters[1];
   uint32_t head = L.counters[2], tail = L.counters[3], buf = L.counters[4] & 1u;
   const uint32_t Q = L.ring_cap, qmask = Q - 1u;
-  const uint32_t jlo = min(k, r * a.kchunk), jhi = min(k, jlo + a.kchunk), jcnt = jhi - jlo;
+  const uint32_t jlo = r == 0 ? 0u : min(k, (r - 1u) * a.kchunk);
+  const uint32_t jcnt = r == 0 ? 0u : min(k, jlo + a.kchunk) - jlo;
   const uint32_t slo = min(H, r * a.hchunk), shi = min(H, slo + a.hchunk), hcnt = shi - slo;
   const uint32_t words = a.hchunk / 32u;         // used-slot bitmap words per CTA
 
@@ -270,6 +274,7 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
     head = 0;
     buf ^= 1u;
     if (r == 0 && tid == 0 && tail != H) atomicOr(a.status, kFlagInternal);
+    cluster_sync();                                 // the compacted queue is complete before CTA 0 reads it
   }
   const uint64_t* ring_in = L.ring + (size_t)buf * Q;
   uint64_t* ring_out = L.ring + (size_t)buf * Q;
@@ -277,6 +282,8 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
   // ---------------------------------------------------------------- P0
   for (uint32_t i = tid; i < words; i += kThreads) pinbits[i] = 0;
   for (uint32_t i = tid; i < jcnt; i += kThreads) vslot[i] = kNoRank;
+  if (r == 0)
+    for (uint32_t i = tid; i < (H + 31u) / 32u; i += kThreads) fullpin[i] = 0;
   if (tid < kMaxCluster) {
     hitcnt[tid] = 0;
     fillcnt[tid] = 0;
@@ -286,6 +293,22 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
     nevict_cta = 0;
     ring_off = 0;
     head_hit = kNoRank;
+  }
+  // CTA 0 copies the head of the queue now (one or two bulk copies from a
+  // 16-byte boundary: window[sh + o] is the entry o places after the head);
+  // the victims come from it later.
+  const uint32_t span = tail - head;
+  const uint32_t sh = head & 1u;
+  const uint32_t wcopy = (min(span + sh, kWindow) + 1u) & ~1u;   // entries copied, even
+  uint32_t wlen = wcopy - sh < span ? wcopy - sh : span;         // entries usable from the window
+  if (r == 0 && tid == 0) {
+    asm volatile("fence.proxy.async.global;" ::: "memory");   // a compaction above wrote the queue
+    mbar_init(&wbar, 1);
+    const uint32_t a0 = (head - sh) & qmask;
+    const uint32_t first = min(wcopy, Q - a0);
+    mbar_arrive_expect_tx(&wbar, wcopy * 8u);
+    bulk_copy_g2s(window, ring_in + a0, first * 8u, &wbar);
+    if (wcopy > first) bulk_copy_g2s(window + first, ring_in, (wcopy - first) * 8u, &wbar);
   }
   // B0: every CTA of the cluster is running (and has zeroed what others add
   // into) before any DSMEM access; classification overlaps the barrier.
@@ -331,6 +354,7 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
     uint32_t tile;
     const uint32_t rank = block_flag_scan(f, scratch[0], &tile);
     if (jj < jcnt) uniq[jj] = f ? cta_miss + rank : kNoRank;
+    if (f) mlist[cta_miss + rank] = jj;
     cta_miss += tile;
   }
   uint32_t cta_unordered, cta_hit_inv;
@@ -347,6 +371,7 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
     if (sl >= 0) {
       const uint32_t owner = (uint32_t)sl / a.hchunk, b = (uint32_t)sl - owner * a.hchunk;
       dsmem_red_or_u32(dsmem_addr(&pinbits[b >> 5], owner), 1u << (b & 31));
+      dsmem_red_or_u32(dsmem_addr(&fullpin[(uint32_t)sl >> 5], 0), 1u << ((uint32_t)sl & 31));
     }
   }
   // hit counts per owner range (exact when idx does not repeat a position)
@@ -389,18 +414,41 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
         dequant_row(va[u], vb[u], lane, reinterpret_cast<uint4*>(a.out_bf16 + (size_t)j * KVO_DEQUANT_VALUES));
     }
   }
+  // CTA 0 (no entries to gather): wait for the window and read its slots'
+  // last_use now.  A stamp of this call may or may not be seen yet; either
+  // way the entry's slot is pinned, and the pin bitmap drops it after B1.
+  bool win_ok = true;
+  uint32_t pre4 = 0;                                // bit q: entry 4 * tid + q of the window was current
+  if (r == 0) {
+    win_ok = __syncthreads_and(mbar_wait_bounded(&wbar, 0, kWindowPolls));
+    if (!win_ok) {
+      wlen = 0;                                     // read the queue from global memory instead
+      if (tid == 0) atomicOr(a.status, kFlagTimeout);
+    }
+    uint64_t e[4];
+    uint32_t lu[4];
+#pragma unroll
+    for (uint32_t q = 0; q < 4; ++q) e[q] = 4 * tid + q < wlen ? window[sh + 4 * tid + q] : ~0ull;
+#pragma unroll
+    for (uint32_t q = 0; q < 4; ++q) {
+      const uint32_t sl = (uint32_t)e[q];
+      lu[q] = __ldcg(&L.last_use[sl < H ? sl : 0u]);
+      prefetch_l2(&L.slot2pos[sl < H ? sl : 0u]);
+    }
+#pragma unroll
+    for (uint32_t q = 0; q < 4; ++q)
+      if (e[q] != ~0ull && (uint32_t)e[q] < H && lu[q] == (uint32_t)(e[q] >> 32)) pre4 |= 1u << q;
+  }
   cluster_wait();                                   // B1
 
   // ---------------------------------------------------------------- P2
-  bool any_unordered = false;
-  uint32_t uniq_before = 0, M = 0;
-  for (uint32_t q = 0; q < C; ++q) {
-    any_unordered |= table[q][0] != 0;
-    uniq_before += q < r ? table[q][1] : 0u;
-    M += table[q][1];
-  }
-  const uint32_t (*mtab)[4] = table;               // column 1: unique misses per CTA
-  uint32_t mcol = 1;
+  // per-CTA counts, one CTA per lane (every warp computes the same sums)
+  const uint32_t t0 = lane < C ? table[lane][0] : 0u, t1 = lane < C ? table[lane][1] : 0u;
+  const bool any_unordered = __any_sync(0xffffffffu, t0 != 0);
+  uint32_t M = __reduce_add_sync(0xffffffffu, t1);
+  uint32_t uniq_before = __reduce_add_sync(0xffffffffu, lane < r ? t1 : 0u);
+  uint32_t nuniq_cta = cta_miss;                   // unique misses held by this CTA
+  uint32_t mcount = t1;                            // lane q: unique misses of CTA q
   if (any_unordered) {
     // The smallest claiming j owns each missing position (claims came from
     // other CTAs: read them from L2); unique hit slots are counted from the
@@ -413,20 +461,17 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
       uint32_t tile;
       const uint32_t rank = block_flag_scan(f, scratch[0], &tile);
       if (jj < jcnt) uniq[jj] = f ? nuniq + rank : kNoRank;
+      if (f) mlist[nuniq + rank] = jj;
       nuniq += tile;
     }
     uint32_t used = 0;
     for (uint32_t w = tid; w < words; w += kThreads) used += __popc(pinbits[w]);
     const uint32_t mine2[2] = {nuniq, block_sum(used, scratch[1])};
     cluster_publish(mine2, 2, table2, r, C);       // B2 (only for an idx that is not increasing)
-    uniq_before = 0;
-    M = 0;
-    for (uint32_t q = 0; q < C; ++q) {
-      uniq_before += q < r ? table2[q][0] : 0u;
-      M += table2[q][0];
-    }
-    mtab = table2;
-    mcol = 0;
+    mcount = lane < C ? table2[lane][0] : 0u;
+    M = __reduce_add_sync(0xffffffffu, mcount);
+    uniq_before = __reduce_add_sync(0xffffffffu, lane < r ? mcount : 0u);
+    nuniq_cta = nuniq;
   }
   if (r == 0 && tid == 0) L.counters[0] = t;       // every CTA read the old step before B1
 
@@ -435,32 +480,57 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
   // unpinned slots in (last_use, slot) order; the u-th is the victim of
   // unique miss u, sent to the CTA holding that miss.
   if (r == 0) {
-    if (tid <= C) {
-      uint32_t b = 0;
-      for (uint32_t q = 0; q < tid; ++q) b += mtab[q][mcol];
-      mbefore[tid] = b;
+    if (warp == 0) {                               // mbefore[q]: unique misses of CTAs below q
+      uint32_t incl = mcount;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t o = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= (uint32_t)d) incl += o;
+      }
+      if (lane <= C) mbefore[lane] = incl - mcount;
     }
-    __syncthreads();
-    const uint32_t span = tail - head;
+    __syncthreads();                               // mbefore, and the window copied by other threads
     uint32_t found = 0, off = 0;
     while (found < M && off < span) {              // uniform over the CTA
       uint64_t e[4];                               // ~0 marks an entry that is not current
-      uint32_t ncur = 0;
+      uint32_t lu[4], ncur = 0;
 #pragma unroll
       for (uint32_t q = 0; q < 4; ++q) {
         const uint32_t o = off + 4 * tid + q;
-        e[q] = o < span ? __ldcg(&ring_in[(head + o) & qmask]) : ~0ull;
-        if (e[q] != ~0ull && entry_current(L, e[q])) ++ncur;
+        e[q] = o >= span ? ~0ull : o < wlen ? window[sh + o] : __ldcg(&ring_in[(head + o) & qmask]);
+      }
+#pragma unroll
+      for (uint32_t q = 0; q < 4; ++q) {           // four independent loads in flight
+        const uint32_t o = off + 4 * tid + q, sl = (uint32_t)e[q];
+        lu[q] = o < wlen ? 0u : __ldcg(&L.last_use[sl < H ? sl : 0u]);
+      }
+#pragma unroll
+      for (uint32_t q = 0; q < 4; ++q) {
+        const uint32_t o = off + 4 * tid + q, sl = (uint32_t)e[q];
+        // in the window: current before this call and not pinned by it
+        const bool cur = e[q] != ~0ull && sl < H &&
+                         (o < wlen ? ((pre4 >> q) & 1u) && !((fullpin[sl >> 5] >> (sl & 31)) & 1u)
+                                   : lu[q] == (uint32_t)(e[q] >> 32));
+        if (cur) ++ncur;
         else e[q] = ~0ull;
       }
       uint32_t tot;
       uint32_t u = found + block_excl_sum(ncur, scratch[0], &tot);
+      // the CTA holding unique miss u (this thread's victims are consecutive)
+      uint32_t h = 0;
+      if (ncur && u < M) {
+        uint32_t hi = C;
+        while (hi - h > 1) {
+          const uint32_t mid = (h + hi) >> 1;
+          if (mbefore[mid] <= u) h = mid;
+          else hi = mid;
+        }
+      }
 #pragma unroll
       for (uint32_t q = 0; q < 4; ++q) {
         if (e[q] == ~0ull) continue;
         const uint32_t sl = (uint32_t)e[q];
         if (u < M) {
-          uint32_t h = 0;
           while (h + 1 < C && mbefore[h + 1] <= u) ++h;
           dsmem_st_u32(dsmem_addr(&vslot[u - mbefore[h]], h), sl);
           const uint32_t owner = sl / a.hchunk, b = sl - owner * a.hchunk;
@@ -475,41 +545,46 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
       off += 4 * kThreads;
     }
     __syncthreads();
-    if (tid == 0) {
+    if (warp == 0) {
       // every range's used slots go to the tail, ranges in slot order
-      uint32_t pos = tail;
-      for (uint32_t q = 0; q < C; ++q) {
-        const uint32_t hq = any_unordered ? table2[q][1] : hitcnt[q];
-        dsmem_st_u32(dsmem_addr(&ring_off, q), pos);
-        pos += hq + fillcnt[q];
+      const uint32_t used = lane < C ? (any_unordered ? table2[lane][1] : hitcnt[lane]) + fillcnt[lane] : 0u;
+      uint32_t incl = used;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t o = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= (uint32_t)d) incl += o;
       }
-      uint32_t nh = head;
-      if (M > 0) nh = head + (head_hit != kNoRank ? head_hit : min(off, span));
-      L.counters[2] = nh;
-      L.counters[3] = pos;
-      L.counters[4] = buf;
+      if (lane < C) dsmem_st_u32(dsmem_addr(&ring_off, lane), tail + incl - used);
+      if (lane == 31) {
+        L.counters[2] = M > 0 ? head + (head_hit != kNoRank ? head_hit : min(off, span)) : head;
+        L.counters[3] = tail + incl;
+        L.counters[4] = buf;
+      }
     }
   }
   cluster_sync();                                   // B3: victims, bits and queue positions delivered
 
   // ---------------------------------------------------------------- P4
-  for (uint32_t jj = tid; jj < jcnt; jj += kThreads) {
-    const uint32_t lr = uniq[jj];
-    if (lr == kNoRank) continue;
-    const uint32_t v = vslot[lr < jcnt ? lr : 0];
-    const int32_t old = v < H ? __ldcg(&L.slot2pos[v]) : -1;
-    if (map_update(a, v, old, meta_pos[jj], t, uniq_before + lr)) atomicAdd(&nevict_cta, 1u);
-  }
-  for (uint32_t jj = warp; jj < jcnt; jj += kWarps) {
-    const uint32_t lr = uniq[jj];
-    if (lr == kNoRank) continue;
-    const uint32_t v = vslot[lr < jcnt ? lr : 0];
+  // One warp per unique miss: the row is read first (the output row this
+  // CTA wrote in P1, else the host row), then the maps are updated and the
+  // row lands in the victim slot.
+  for (uint32_t lr = warp; lr < nuniq_cta; lr += kWarps) {
+    const uint32_t jj = mlist[lr];
+    const uint32_t v = vslot[lr];
     const int32_t p = meta_pos[jj];
-    if (v >= H || p < 0 || (uint32_t)p >= L.history_cap) continue;
-    // the output row this CTA wrote in P1, else the host row
+    if (v >= H || p < 0 || (uint32_t)p >= L.history_cap) {
+      if (lane == 0) atomicOr(a.status, kFlagInternal);   // cannot happen; never write out of bounds
+      continue;
+    }
     const uint4* src = a.out_rows ? reinterpret_cast<const uint4*>(a.out_rows) + (size_t)(jlo + jj) * kRowVec
                                   : miss_row(a, hist4, p);
-    copy_row(src, reinterpret_cast<uint4*>(L.hot) + (size_t)v * kRowVec, lane);
+    const uint4 x = __ldcg(src + lane);
+    uint4 y = make_uint4(0, 0, 0, 0);
+    if (lane < kRowVec - 32) y = __ldcg(src + 32 + lane);
+    if (lane == 0 && map_update(a, v, __ldcg(&L.slot2pos[v]), p, t, uniq_before + lr)) atomicAdd(&nevict_cta, 1u);
+    uint4* dst = reinterpret_cast<uint4*>(L.hot) + (size_t)v * kRowVec;
+    dst[lane] = x;
+    if (lane < kRowVec - 32) dst[32 + lane] = y;
   }
 
   // ---------------------------------------------------------------- P5
@@ -535,6 +610,8 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
     }
   }
   if (L.evlog && r == 0 && tid == 0) L.evlog[0] = (int32_t)M;
+  // a window copy that never completed must not land after this CTA exits
+  if (r == 0 && !win_ok) mbar_wait_bounded(&wbar, 0, kWindowPolls);
 
   // ------------------------------------------------------------- stats
   __syncthreads();

@@ -53,8 +53,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const StepArgs
   const uint32_t kchunk = s.R.kchunk;
   topk_body<kResident>(s.scores, s.n, s.R.k, dyn_smem, &rsm, [&](uint32_t pos, uint32_t out) {
     s.idx[out] = (int32_t)pos;
-    const uint32_t owner = out / kchunk;
-    dsmem_st_u32(dsmem_addr(&sel[out - owner * kchunk], owner), pos);
+    const uint32_t q = out / kchunk;                 // CTA q + 1 resolves entries [q * kchunk, ...)
+    dsmem_st_u32(dsmem_addr(&sel[out - q * kchunk], q + 1), pos);
   });
   cluster_sync();                                  // every selected position delivered
   resolve_body(s.R, rdyn);
@@ -100,7 +100,7 @@ cudaError_t launch_decode_step(const LayerView& L, const void* new_rows, uint32_
   a.out_bf16 = out_bf16;
   a.status = status;
   a.k = k;
-  a.kchunk = (k + C - 1) / C;
+  a.kchunk = (k + C - 2) / (C - 1);                 // CTA 0 keeps the LRU order, CTAs 1..C-1 the entries
   a.hchunk = ((L.hot_rows + C - 1) / C + 127u) & ~127u;
   a.fused = 1;
   a.len = old_len + r;

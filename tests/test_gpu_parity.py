@@ -289,6 +289,26 @@ def test_decode_step_tiny_full_parity(kvo, appends):
     g.ctx.close()
 
 
+@pytest.mark.parametrize("cluster", [2, 4, 8])
+@pytest.mark.parametrize("fused", [False, True])
+def test_smaller_clusters_full_parity(kvo, monkeypatch, cluster, fused):
+    """Every cluster size the launcher may pick (KVO_MAX_CLUSTER caps it):
+    one CTA keeps the LRU order, the others split the selection."""
+    monkeypatch.setenv("KVO_MAX_CLUSTER", str(cluster))
+    w = W.TINY.scaled(appends_per_step=1, steps=12)
+    g = GpuLayerRun(w, 0, want_bf16=True, fused=fused)
+    o = OracleLayerRun(w, 0, want_bf16=True)
+    g.ctx.record_evictions(True)
+    for step in range(w.steps):
+        np.testing.assert_array_equal(g.step(step), o.step(step))
+        np.testing.assert_array_equal(g.rows(), o.last.rows)
+        np.testing.assert_array_equal(g.bf16(), o.last.bf16)
+        assert g.ctx.evictions(0) == o.last.evictions
+        compare_state(g.ctx, 0, o.st)
+    assert g.ctx.sync() == 0
+    g.ctx.close()
+
+
 def test_decode_step_50k_all_steps(kvo):
     """The benchmark's configuration: 50K single layer, 1,024 fused steps."""
     w = W.K50

@@ -115,18 +115,21 @@ def algorithmic_bytes(w: W.Workload, n_avg: float, stats_delta: dict, resolve_la
     counters of the timed launches.
 
     select:  4n (scores) + 4k (positions).
-    resolve: 4k (positions) + 4k (pos2slot lookups) + 4*hits (last_use stamps)
-             + 656*hits (hot rows) + R_out*k (output) + 656*fills (victim rows)
-             + 16*fills (map and stamp updates) + 4*hot_rows (LRU scan);
-             host link: 656 per miss occurrence.
+    resolve: 4K (positions) + 4K (pos2slot lookups) + 4*hits (last_use stamps)
+             + 656*hits (hot rows) + R_out*K (output) + 656*fills (victim rows)
+             + 16*fills (map and stamp updates) + 12*4096 (the LRU-queue window
+             and its slots' last_use) + 8*(hits + fills) (queue appends);
+             host link: 656 per miss occurrence.  K = k x query rows.
     """
-    k = w.k
+    k = w.k * w.queries
     r_out = ROW + (2 * 576 if w.bf16 else 0)
     L = max(resolve_launches, 1)
     hits = stats_delta["hits"] / L
     fills = stats_delta["unique_misses"] / L
     misses = stats_delta["misses"] / L
-    resolve_hbm = 8 * k + 4 * hits + ROW * hits + r_out * k + (ROW + 16) * fills + 4 * w.hot_rows
+    window = min(4096, 8 * w.hot_rows)
+    resolve_hbm = (8 * k + 4 * hits + ROW * hits + r_out * k + (ROW + 16) * fills + 12 * window
+                   + 8 * (hits + fills))
     select_hbm = 4 * n_avg + 4 * k
     return {"resolve_hbm": resolve_hbm, "resolve_host": ROW * misses, "select_hbm": select_hbm,
             "append_host": ROW * w.appends_per_step, "hits": hits, "misses": misses, "fills": fills}
@@ -183,11 +186,27 @@ class GpuWorkload:
                 d = np.stack([W.carry_draw(w, layer_base + l, s) if s else np.zeros(w.carry, np.int64)
                               for s in range(steps)])
                 self.draws[l] = torch.from_numpy(d).to(dev)
+        # query rows 1.. of an MTP round: row 0 plus float32 noise, added in float64
+        self.nq = w.queries
+        self.noise = {}
+        if self.nq > 1:
+            for l in self.sel:
+                z = np.zeros((steps, self.nq - 1, nmax), np.float32)
+                for s in range(steps):
+                    for q in range(1, self.nq):
+                        z[s, q - 1, :w.n_at(s)] = W.query_noise32(w, layer_base + l, s, q, w.n_at(s))
+                t = torch.from_numpy(z)
+                self.noise[l] = t.pin_memory() if host_inputs else t.to(dev)
+        self.noise_stage = {l: torch.empty((self.nq - 1, nmax), dtype=torch.float32, device=dev)
+                            for l in self.sel} if self.nq > 1 and host_inputs else None
+        self.qrows = {l: torch.empty((max(self.nq - 1, 1), nmax), dtype=torch.float32, device=dev) for l in self.sel}
         self.stage = {l: torch.empty(nmax, dtype=torch.float32, device=dev) for l in self.sel}
-        self.idx = {l: [torch.zeros(w.k, dtype=torch.int32, device=dev) for _ in range(2)] for l in self.sel}
-        self.out_rows = torch.empty((w.k, ROW), dtype=torch.uint8, device=dev)
-        self.out_bf16 = torch.empty((w.k, 576), dtype=torch.bfloat16, device=dev) if w.bf16 else None
-        self.out_host = torch.empty((w.k, ROW), dtype=torch.uint8).pin_memory() if host_inputs else None
+        self.idx = {l: [torch.zeros((self.nq, w.k), dtype=torch.int32, device=dev) for _ in range(2)]
+                    for l in self.sel}
+        kq = self.nq * w.k
+        self.out_rows = torch.empty((kq, ROW), dtype=torch.uint8, device=dev)
+        self.out_bf16 = torch.empty((kq, 576), dtype=torch.bfloat16, device=dev) if w.bf16 else None
+        self.out_host = torch.empty((kq, ROW), dtype=torch.uint8).pin_memory() if host_inputs else None
         self.idx_hist = torch.zeros((steps, w.k), dtype=torch.int32, device=dev)
         self.launches = 0
         self.fused = fused
@@ -205,16 +224,29 @@ class GpuWorkload:
         else:
             sc = self.scores[l][s, :n]
         if w.carry and s > 0:
-            prev = self.idx[l][(s - 1) & 1]
+            prev = self.idx[l][(s - 1) & 1][0]
             pos = prev.index_select(0, self.draws[l][s]).long()
             sc.index_add_(0, pos, torch.full((w.carry,), w.carry_boost, dtype=torch.float32, device="cuda"))
         return sc
+
+    def query_rows(self, l, s, row0):
+        """Rows 1.. of an MTP round (row 0 + noise in float64, cast once)."""
+        n = row0.shape[0]
+        if self.host_inputs:
+            z = self.noise_stage[l][:, :n]
+            z.copy_(self.noise[l][s, :, :n], non_blocking=True)
+        else:
+            z = self.noise[l][s, :, :n]
+        out = self.qrows[l][:, :n]
+        out.copy_((row0.double().unsqueeze(0) + z.double()).float())
+        return [row0] + [out[q] for q in range(self.nq - 1)]
 
     def step(self, s, ev=None, kev=None):
         """One decode step over all layers.  ev: (start, end) events; kev: dict
         kind -> list of (start, end) event pairs appended per launch."""
         torch, w, ctx = self.torch, self.w, self.ctx
         sc = {l: self.scores_for(l, s) for l in self.sel}
+        qr = {l: self.query_rows(l, s, sc[l]) for l in self.sel} if self.nq > 1 and not self.host_inputs else None
 
         def rec(kind, fn):
             if kev is None:
@@ -229,6 +261,8 @@ class GpuWorkload:
 
         if ev:
             ev[0].record()
+        if self.nq > 1 and self.host_inputs:                # the rows' noise is a step input too
+            qr = {l: self.query_rows(l, s, sc[l]) for l in self.sel}
         a = w.appends_per_step
         for l in range(w.layers):
             src = None
@@ -239,20 +273,28 @@ class GpuWorkload:
                 else:
                     src = self.new_rows[l, s * a:(s + 1) * a]
             src_l = w.source_layer(l)
-            if self.fused and l in self.sel:
-                rec("step", lambda: ctx.decode_step(l, src, sc[l], w.k, self.idx[l][s & 1], self.out_rows,
+            if self.fused and self.nq == 1 and l in self.sel:
+                rec("step", lambda: ctx.decode_step(l, src, sc[l], w.k, self.idx[l][s & 1][0], self.out_rows,
                                                     self.out_bf16))
                 continue
             if a:
                 rec("append", lambda: ctx.append_rows(l, src))
+            if self.nq > 1:
+                if l in self.sel:
+                    for q, row in enumerate(qr[l]):
+                        rec("select", lambda: ctx.select_topk(row, w.k, self.idx[l][s & 1][q]))
+                rec("resolve", lambda: ctx.resolve_gather_multi(l, self.idx[src_l][s & 1], self.out_rows,
+                                                                 self.out_bf16))
+                continue
             if l in self.sel:
-                rec("select", lambda: ctx.select_topk(sc[l], w.k, self.idx[l][s & 1]))
-            rec("resolve", lambda: ctx.resolve_gather(l, self.idx[src_l][s & 1], self.out_rows, self.out_bf16))
+                rec("select", lambda: ctx.select_topk(sc[l], w.k, self.idx[l][s & 1][0]))
+            rec("resolve", lambda: ctx.resolve_gather(l, self.idx[src_l][s & 1][0], self.out_rows,
+                                                      self.out_bf16))
         if self.host_inputs:
             self.out_host.copy_(self.out_rows, non_blocking=True)
         if ev:
             ev[1].record()
-        self.idx_hist[s].copy_(self.idx[self.sel[0]][s & 1])
+        self.idx_hist[s].copy_(self.idx[self.sel[0]][s & 1][0])
 
     def close(self):
         self.ctx.close()
@@ -365,11 +407,11 @@ def run_e2e(args, w):
     torch.cuda.synchronize()
     total = sum(a.elapsed_time(b) for a, b in evs) * 1e-3
     nmean = float(np.mean([w.n_at(s) for s in range(args.warmup, steps)]))
-    h2d = int(len(wl.sel) * nmean * 4 + w.layers * w.appends_per_step * ROW)
-    d2h = int(w.k * ROW)
+    h2d = int(len(wl.sel) * nmean * 4 * w.queries + w.layers * w.appends_per_step * ROW)
+    d2h = int(w.queries * w.k * ROW)
     wl.close()
     del flush
-    return {"value": round(args.steps * w.layers * w.k / total, 1), "unit": "rows/s",
+    return {"value": round(args.steps * w.layers * w.k * w.queries / total, 1), "unit": "rows/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 
@@ -402,16 +444,17 @@ def run_oracle(w, max_steps, budget_s, layers=None):
             for a in range(w.appends_per_step):
                 states[l].append(extra[l][s * w.appends_per_step + a][None])
             if l % w.select_every == 0:
-                idx[l] = O.select_topk(scores[l], w.k)
-            O.resolve_gather(states[l], idx[w.source_layer(l)], want_bf16=w.bf16)
+                rows = [scores[l]] + [W.query_scores(w, l, s, q, scores[l]) for q in range(1, w.queries)]
+                idx[l] = np.stack([O.select_topk(row, w.k) for row in rows])
+            O.resolve_gather_multi(states[l], idx[w.source_layer(l)], want_bf16=w.bf16)
         spent += time.perf_counter() - t
-        prev = idx
-        sels.append(idx[0])
+        prev = {l: v[0] for l, v in idx.items()}
+        sels.append(idx[0][0])
         done += 1
         if spent >= budget_s:
             break
     cpu = time.process_time() - cpu0
-    return {"rows_per_s": done * L * w.k / spent, "steps": done, "layers": L, "seconds": spent,
+    return {"rows_per_s": done * L * w.k * w.queries / spent, "steps": done, "layers": L, "seconds": spent,
             "cores": max(1, round(cpu / max(spent, 1e-9))), "sels": sels}
 
 
@@ -632,8 +675,10 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     config = {"workload": w.name, "layers": w.layers, "history": w.n0, "hot_rows": w.hot_rows, "k": w.k,
               "appends_per_step": w.appends_per_step, "select_every": w.select_every,
-              "bf16_output": w.bf16, "parallelism": f"replicas{world}",
-              "calls": "kvo_append_rows+kvo_select_topk+kvo_resolve_gather" if args.separate else "kvo_decode_step",
+              "bf16_output": w.bf16, "queries": w.queries, "parallelism": f"replicas{world}",
+              "calls": ("kvo_append_rows+kvo_select_topk x%d+kvo_resolve_gather_multi" % w.queries if w.queries > 1
+                        else "kvo_append_rows+kvo_select_topk+kvo_resolve_gather" if args.separate
+                        else "kvo_decode_step"),
               "l2": "flushed between steps (1 GiB memset, outside the step events)"}
 
     if args.impl == "reference":
@@ -673,7 +718,7 @@ def main():
     from gather_radix_top_gb300 import kvo
     hbm_peak, peak_src = load_peaks()
     link = measure_host_link(torch, kvo)
-    total_rows = args.steps * w.layers * w.k * world
+    total_rows = args.steps * w.layers * w.k * w.queries * world
     value = total_rows / g["total_s"]
     nmean = float(np.mean([w.n_at(s) for s in range(args.warmup, args.warmup + args.steps)]))
     nres = (len(g["kern_ms"].get("resolve", [])) + len(g["kern_ms"].get("step", []))) or 1

@@ -27,13 +27,13 @@ struct kvo_ctx {
   std::vector<int64_t> length;           // host copy of each history length
   uint32_t* counters = nullptr;          // device [layers][8]: step, length, queue head, tail, buffer
   unsigned long long* stats = nullptr;   // device [layers][8]
-  int32_t* evlog = nullptr;              // device [layers][1 + 3*KVO_MAX_K] when recording
+  int32_t* evlog = nullptr;              // device [layers][1 + 3*KVO_MAX_ROUND] when recording
   uint32_t* status = nullptr;            // device status word
 };
 
 namespace {
 
-constexpr size_t kEvlogStride = 1 + 3 * (size_t)KVO_MAX_K;
+constexpr size_t kEvlogStride = 1 + 3 * (size_t)KVO_MAX_ROUND;
 
 bool ok(cudaError_t e) { return e == cudaSuccess; }
 
@@ -257,6 +257,21 @@ kvo_status kvo_resolve_gather(kvo_ctx* ctx, int32_t layer, const int32_t* idx, i
   const cudaError_t e =
       kvo::launch_resolve(v, idx, (uint32_t)k, static_cast<uint8_t*>(out_rows), out_bf16, ctx->status,
                           ctx->max_cluster, static_cast<cudaStream_t>(stream));
+  return ok(e) ? KVO_OK : KVO_ECUDA;
+}
+
+kvo_status kvo_resolve_gather_multi(kvo_ctx* ctx, int32_t layer, const int32_t* idx, int32_t nq, int32_t k,
+                                    void* out_rows, uint16_t* out_bf16, void* stream) {
+  if (!ctx || layer < 0 || layer >= ctx->layers || !idx || nq < 1 || k < 1 || k > KVO_MAX_K ||
+      (int64_t)nq * k > KVO_MAX_ROUND || (int64_t)nq * k > ctx->hot_rows || (!out_rows && !out_bf16))
+    return KVO_EINVAL;
+  if ((out_rows && !aligned16(out_rows)) || (out_bf16 && !aligned16(out_bf16))) return KVO_EINVAL;
+  kvo::LayerView v = ctx->views[layer];
+  v.evlog = ctx->evlog ? ctx->evlog + kEvlogStride * layer : nullptr;
+  const cudaError_t e =
+      kvo::launch_resolve(v, idx, (uint32_t)(nq * k), static_cast<uint8_t*>(out_rows), out_bf16, ctx->status,
+                          ctx->max_cluster, static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorInvalidValue) return KVO_EINVAL;   // the round does not fit this cluster's shared memory
   return ok(e) ? KVO_OK : KVO_ECUDA;
 }
 

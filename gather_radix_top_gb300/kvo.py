@@ -15,6 +15,7 @@ from . import build as _build
 ROW_BYTES = 656
 DEQUANT_VALUES = 576
 MAX_K = 4096
+MAX_ROUND = 8192
 MAX_HOT_ROWS = 131072
 NOALLOC_MAX_PAIRS = 65536
 
@@ -23,7 +24,7 @@ KVO_OK, KVO_EINVAL, KVO_ENOMEM, KVO_ECUDA, KVO_ERANGE, KVO_EBUSY, KVO_ETIMEDOUT,
 
 EXPORTED = [
     "kvo_status_string", "kvo_create", "kvo_destroy", "kvo_append_rows", "kvo_select_topk",
-    "kvo_resolve_gather", "kvo_decode_step", "kvo_sync", "kvo_get_stats", "kvo_history_length",
+    "kvo_resolve_gather", "kvo_resolve_gather_multi", "kvo_decode_step", "kvo_sync", "kvo_get_stats", "kvo_history_length",
     "kvo_debug_dump_layer", "kvo_debug_record_evictions", "kvo_debug_evictions",
     "kvo_probe_host_read",
     "kvo_tier_blocks", "kvo_pool_create", "kvo_pool_destroy", "kvo_pool_alloc", "kvo_pool_write",
@@ -79,6 +80,7 @@ def lib() -> ctypes.CDLL:
         "kvo_append_rows": (ctypes.c_int, [_vp, _i32, _vp, _i64, _vp]),
         "kvo_select_topk": (ctypes.c_int, [_vp, _vp, _i64, _i32, _vp, _vp]),
         "kvo_resolve_gather": (ctypes.c_int, [_vp, _i32, _vp, _i32, _vp, _vp, _vp]),
+        "kvo_resolve_gather_multi": (ctypes.c_int, [_vp, _i32, _vp, _i32, _i32, _vp, _vp, _vp]),
         "kvo_decode_step": (ctypes.c_int, [_vp, _i32, _vp, _i64, _vp, _i64, _i32, _vp, _vp, _vp, _vp]),
         "kvo_sync": (ctypes.c_int, [_vp, _vp]),
         "kvo_get_stats": (ctypes.c_int, [_vp, _i32, ctypes.POINTER(kvo_stats)]),
@@ -188,6 +190,18 @@ def kvo_resolve_gather(ctx: int, layer: int, idx, out_rows=None, out_bf16=None, 
                                     _stream_ptr(stream)), "kvo_resolve_gather")
 
 
+def kvo_resolve_gather_multi(ctx: int, layer: int, idx, out_rows=None, out_bf16=None, stream=None) -> None:
+    """idx: int32 CUDA tensor [nq, k] (one query row's selection per row);
+    out_rows: uint8 [nq*k, 656]; out_bf16: bfloat16 (or int16) [nq*k, 576]."""
+    if idx.dim() != 2:
+        raise ValueError("idx must be [nq, k]")
+    if out_bf16 is not None and str(out_bf16.dtype) not in ("torch.bfloat16", "torch.int16"):
+        raise ValueError("out_bf16 must be bfloat16 or int16")
+    _check(lib().kvo_resolve_gather_multi(ctx, layer, _dev_ptr(idx, "torch.int32"), idx.shape[0], idx.shape[1],
+                                          _dev_ptr(out_rows, "torch.uint8"), _dev_ptr(out_bf16),
+                                          _stream_ptr(stream)), "kvo_resolve_gather_multi")
+
+
 def kvo_decode_step(ctx: int, layer: int, new_rows, scores, k: int, idx=None, out_rows=None, out_bf16=None,
                     stream=None):
     """Append (new_rows: uint8 CUDA tensor [r, 656] or None), select and
@@ -244,9 +258,9 @@ def kvo_debug_record_evictions(ctx: int, on: bool) -> None:
 
 def kvo_debug_evictions(ctx: int, layer: int) -> list:
     import numpy as np
-    buf = np.zeros(3 * MAX_K, np.int32)
+    buf = np.zeros(3 * MAX_ROUND, np.int32)
     n = _i32()
-    _check(lib().kvo_debug_evictions(ctx, layer, ctypes.c_void_p(buf.ctypes.data), MAX_K, ctypes.byref(n)),
+    _check(lib().kvo_debug_evictions(ctx, layer, ctypes.c_void_p(buf.ctypes.data), MAX_ROUND, ctypes.byref(n)),
            "kvo_debug_evictions")
     return [tuple(int(x) for x in buf[3 * i:3 * i + 3]) for i in range(n.value)]
 
@@ -290,6 +304,9 @@ class Context:
 
     def resolve_gather(self, layer, idx, out_rows=None, out_bf16=None, stream=None):
         kvo_resolve_gather(self.handle, layer, idx, out_rows, out_bf16, stream)
+
+    def resolve_gather_multi(self, layer, idx, out_rows=None, out_bf16=None, stream=None):
+        kvo_resolve_gather_multi(self.handle, layer, idx, out_rows, out_bf16, stream)
 
     def decode_step(self, layer, new_rows, scores, k, idx=None, out_rows=None, out_bf16=None, stream=None):
         return kvo_decode_step(self.handle, layer, new_rows, scores, k, idx, out_rows, out_bf16, stream)

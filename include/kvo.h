@@ -45,6 +45,7 @@ extern "C" {
 #define KVO_LATENT_BYTES 512
 #define KVO_DEQUANT_VALUES 576      /* bf16 values per dequantised row */
 #define KVO_MAX_K 4096              /* largest selection size per call */
+#define KVO_MAX_ROUND 8192          /* most entries in one multi-query round */
 #define KVO_MAX_HOT_ROWS 131072     /* largest hot cache per layer */
 
 typedef enum kvo_status {
@@ -146,6 +147,26 @@ kvo_status kvo_select_topk(kvo_ctx* ctx, const float* scores, int64_t n, int32_t
  */
 kvo_status kvo_resolve_gather(kvo_ctx* ctx, int32_t layer, const int32_t* idx, int32_t k,
                               void* out_rows, uint16_t* out_bf16, void* stream);
+
+/*
+ * kvo_resolve_gather_multi - one round of several query rows ([KVO] "GPU
+ * cache management has hazards too": verification with MTP processes
+ * several rows, and several queries can select the same missing position).
+ *   idx       device int32[nq*k]: row q's selection is idx[q*k .. q*k+k),
+ *             rows one after another.
+ *   out_rows  device uint8[nq*k*656] or NULL, out_bf16 device
+ *             uint16[nq*k*576] or NULL: entry q*k+j in the same order.
+ * The round is exactly kvo_resolve_gather over the nq*k entries in that
+ * order: the layer's step advances once; the first occurrence of a missing
+ * position takes the slot, every later occurrence (in this or another row)
+ * reads host memory, and a slot filled in this round is a hit source only
+ * from the next round on; every slot the round uses is pinned.
+ * Requires 1 <= nq, 1 <= k <= KVO_MAX_K, nq*k <= KVO_MAX_ROUND and
+ * nq*k <= hot_rows, else KVO_EINVAL (also when the round does not fit the
+ * shared memory of the cluster size in use).
+ */
+kvo_status kvo_resolve_gather_multi(kvo_ctx* ctx, int32_t layer, const int32_t* idx, int32_t nq, int32_t k,
+                                    void* out_rows, uint16_t* out_bf16, void* stream);
 
 /*
  * kvo_decode_step - one decode step of one layer in a single launch: the

@@ -238,6 +238,21 @@ def resolve_gather(state: LayerState, idx, want_bf16: bool = False) -> ResolveRe
 # Dequantisation to bf16: bf16 = RNE(float32(q) * float32(scale[g])), RoPE
 # copied bit for bit.
 # ---------------------------------------------------------------------------
+def resolve_gather_multi(state: LayerState, idx_rows, want_bf16: bool = False) -> ResolveResult:
+    """One round of several query rows ("GPU cache management has hazards
+    too": MTP verification processes several rows, and several queries can
+    select the same missing position).  The round is one resolve over the
+    rows' selections taken one row after another: the step advances once,
+    the first occurrence of a missing position takes the slot, every later
+    occurrence (in any row) reads host memory, a slot filled in the round is
+    a hit source only from the next round, and every slot the round uses is
+    pinned.  Output entry q * k + j belongs to row q, entry j."""
+    rows = np.asarray(idx_rows, np.int64)
+    if rows.ndim != 2 or rows.shape[0] < 1:
+        raise ValueError("idx_rows must be [nq, k]")
+    return resolve_gather(state, rows.reshape(-1), want_bf16)
+
+
 def bf16_round_nearest_even(x: np.ndarray) -> np.ndarray:
     """IEEE-754 round-to-nearest, ties-to-even, of float32 values to bf16 bits.
 

@@ -40,6 +40,7 @@ _TAG_ROWS = 0x524F5753
 _TAG_SCORES = 0x53434F52
 _TAG_CARRY = 0x43415259
 _TAG_SESSION = 0x53455353
+_TAG_QUERY = 0x51524F57
 
 
 def _rng(*key: int) -> np.random.Generator:
@@ -68,6 +69,8 @@ class Workload:
     recency_amp: float = 0.0
     recency_tau: float = 4096.0
     bf16: bool = False
+    queries: int = 1                     # query rows per step (MTP verification rounds)
+    query_noise: float = 0.25            # rows 1.. = row 0's scores + N(0, query_noise)
     extra: dict = field(default_factory=dict, compare=False, hash=False)
 
     @property
@@ -99,7 +102,11 @@ STACK = Workload("50k_full_stack", 2, 3, layers=78, n0=50_023, hot_rows=32_768, 
 M1 = Workload("1m_cold_stress", 3, 4, layers=8, n0=1_048_576, hot_rows=32_768, k=2048,
               steps=64, appends_per_step=0, bf16=True)
 
-WORKLOADS = {w.name: w for w in (TINY, K50, STACK, M1)}
+# MTP verification: four query rows per step (the token and three drafts),
+# row 0 exactly the 50K single-layer scores, rows 1-3 close to it
+K50_MTP = K50.scaled(name="50k_mtp4", queries=4)
+
+WORKLOADS = {w.name: w for w in (TINY, K50, STACK, M1, K50_MTP)}
 
 
 def rows(w: Workload, layer: int, start: int, count: int) -> np.ndarray:
@@ -160,6 +167,20 @@ def apply_carry(scores: np.ndarray, prev_sel: np.ndarray | None, draw: np.ndarra
     if prev_sel is not None and len(draw):
         s[np.asarray(prev_sel, np.int64)[draw]] += np.float32(boost)
     return s
+
+
+def query_noise32(w: Workload, layer: int, step: int, q: int, n: int) -> np.ndarray:
+    """The float32 noise of query row q (q >= 1) of a step: N(0, query_noise)."""
+    g = _rng(w.seed, w.cfg_id, layer, step, q, _TAG_QUERY)
+    return (g.standard_normal(n) * w.query_noise).astype(np.float32)
+
+
+def query_scores(w: Workload, layer: int, step: int, q: int, row0: np.ndarray) -> np.ndarray:
+    """Scores of query row q (q >= 1) of a step: row 0's scores (after the
+    carry-over) plus the row's float32 noise, added in float64 and cast once
+    to float32 (exact on any IEEE device)."""
+    noise = query_noise32(w, layer, step, q, row0.shape[0])
+    return (row0.astype(np.float64) + noise.astype(np.float64)).astype(np.float32)
 
 
 def random_scores(seed: int, n: int, kind: str = "normal") -> np.ndarray:

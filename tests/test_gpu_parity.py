@@ -377,3 +377,75 @@ def test_decode_step_rejects_host_rows_and_bad_sizes(kvo):
                         out_rows=out)                               # past history_cap
     assert ctx.history_length(0) == 50
     ctx.close()
+
+
+# ------------------------------------------------ multi-query rounds (MTP)
+def _mtp_run(kvo, w, steps, check_every=1, want_bf16=False):
+    """Each step: append, nq top-K selections (row 0 from the score model,
+    rows 1.. = row 0 + noise), one multi-query round; GPU vs oracle."""
+    import torch
+    nq, k = w.queries, w.k
+    ctx = kvo.Context(1, w.history_cap, w.hot_rows)
+    ctx.append_rows(0, W.rows(w, 0, 0, w.n0))
+    ctx.record_evictions(True)
+    st = O.LayerState(w.history_cap, w.hot_rows)
+    st.append(W.rows(w, 0, 0, w.n0))
+    extra = W.rows(w, 0, w.n0, w.history_cap - w.n0) if w.history_cap > w.n0 else None
+    out = torch.empty((nq * k, O.ROW_BYTES), dtype=torch.uint8, device="cuda")
+    outb = torch.empty((nq * k, O.DEQUANT_VALUES), dtype=torch.int16, device="cuda") if want_bf16 else None
+    idx = torch.empty((nq, k), dtype=torch.int32, device="cuda")
+    prev = None
+    for step in range(steps):
+        for a in range(w.appends_per_step):
+            pos = w.n0 + step * w.appends_per_step + a
+            row = extra[pos - w.n0:pos - w.n0 + 1]
+            ctx.append_rows(0, torch.from_numpy(row).cuda())
+            st.append(row)
+        row0 = W.apply_carry(W.base_scores(w, 0, step), prev, W.carry_draw(w, 0, step), w.carry_boost)
+        rows = [row0] + [W.query_scores(w, 0, step, q, row0) for q in range(1, nq)]
+        for q, r in enumerate(rows):
+            ctx.select_topk(torch.from_numpy(r).cuda(), k, idx[q])
+        ctx.resolve_gather_multi(0, idx, out, outb)
+        want = np.stack([O.select_topk(r, k) for r in rows])
+        res = O.resolve_gather_multi(st, want, want_bf16=want_bf16)
+        np.testing.assert_array_equal(idx.cpu().numpy(), want)
+        assert ctx.evictions(0) == res.evictions, step
+        if step % check_every == 0 or step == steps - 1:
+            np.testing.assert_array_equal(out.cpu().numpy(), res.rows)
+            if want_bf16:
+                assert_bf16_equal(outb.cpu().numpy(), res.bf16)
+        prev = want[0]
+    assert ctx.sync() == 0
+    compare_state(ctx, 0, st)
+    s = ctx.stats(0)
+    assert s["rows_out"] == steps * nq * k and s["misses"] >= s["unique_misses"]
+    ctx.close()
+
+
+def test_multi_query_rounds_tiny(kvo):
+    _mtp_run(kvo, W.TINY.scaled(queries=4, appends_per_step=1), 16, want_bf16=True)
+
+
+def test_multi_query_rounds_50k(kvo):
+    """The MTP bench workload: 4 query rows of 2,048 per round, 120 rounds."""
+    _mtp_run(kvo, W.K50_MTP.scaled(steps=120), 120, check_every=10)
+
+
+def test_multi_query_argument_errors(kvo):
+    import torch
+    ctx = kvo.Context(1, 20_000, 8192)
+    ctx.append_rows(0, np.zeros((20_000, O.ROW_BYTES), np.uint8))
+    out = torch.empty((8193, O.ROW_BYTES), dtype=torch.uint8, device="cuda")
+    with pytest.raises(kvo.KvoError):                  # nq * k > KVO_MAX_ROUND
+        ctx.resolve_gather_multi(0, torch.zeros((3, 2731), dtype=torch.int32, device="cuda"), out)
+    with pytest.raises(kvo.KvoError):                  # k > KVO_MAX_K
+        ctx.resolve_gather_multi(0, torch.zeros((1, 4097), dtype=torch.int32, device="cuda"), out)
+    ctx.resolve_gather_multi(0, torch.arange(8192, dtype=torch.int32, device="cuda").view(4, 2048), out[:8192])
+    assert ctx.sync() == 0
+    assert ctx.stats(0)["unique_misses"] == 8192
+    small = kvo.Context(1, 100, 16)
+    small.append_rows(0, np.zeros((100, O.ROW_BYTES), np.uint8))
+    with pytest.raises(kvo.KvoError):                  # nq * k > hot_rows
+        small.resolve_gather_multi(0, torch.zeros((2, 9), dtype=torch.int32, device="cuda"), out[:18])
+    ctx.close()
+    small.close()

@@ -242,6 +242,48 @@ def test_empty_slots_fill_in_slot_order_then_lru():
     assert r.evictions == [(1, 11, 14), (0, 10, 15)]
 
 
+# ------------------------------------------------- multi-query rounds
+def test_multi_query_round_worked_example():
+    """Two query rows select the same missing position in one round: only
+    its first occurrence takes a slot, the second reads host memory, and the
+    slot becomes a hit source in the next round."""
+    st = O.LayerState(100, 4)
+    st.append(np.arange(100 * O.ROW_BYTES, dtype=np.uint64).astype(np.uint8).reshape(100, -1))
+    r = O.resolve_gather_multi(st, [[10, 20], [20, 30]])
+    assert (r.hits, r.misses, r.unique_misses) == (0, 4, 3)
+    assert r.evictions == [(0, -1, 10), (1, -1, 20), (2, -1, 30)]
+    assert list(r.slot_of) == [-1, -1, -1, -1]       # the repeat of 20 is not served from slot 1
+    np.testing.assert_array_equal(r.rows[2], st.history[20])
+    r = O.resolve_gather_multi(st, [[20, 40], [40, 10]])
+    assert (r.hits, r.misses, r.unique_misses) == (2, 2, 1)
+    assert r.evictions == [(3, -1, 40)]
+    # rows taken as separate rounds would differ: row 1 would hit the slot row 0 filled
+    st2 = O.LayerState(100, 4)
+    st2.append(st.history[:100])
+    O.resolve_gather(st2, [10, 20])
+    assert O.resolve_gather(st2, [20, 30]).hits == 1
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_multi_query_round_equals_brute_force(seed):
+    """Rows of overlapping selections (as MTP draft rows are) resolved as one
+    round equal the sequential-LRU definition applied to the whole round."""
+    g = np.random.default_rng(100 + seed)
+    H, n, nq, k = 48, 160, 4, 10
+    st = O.LayerState(n, H)
+    hist = g.integers(0, 256, size=(n, O.ROW_BYTES), dtype=np.uint8)
+    st.append(hist)
+    pairs, slot2pos, last_use = [], [-1] * H, [0] * H
+    for t in range(1, 25):
+        base = g.choice(n, size=k, replace=False)
+        rows = np.stack([np.where(g.random(k) < 0.3, g.integers(0, n, size=k), base) for _ in range(nq)])
+        res = O.resolve_gather_multi(st, rows)
+        out, ev = _brute_step(hist, n, H, pairs, slot2pos, last_use, t, rows.reshape(-1))
+        assert res.evictions == ev
+        assert [bytes(x) for x in res.rows] == out
+        assert st.pos2slot == {p: s for p, s in pairs}
+
+
 # ------------------------------------------------------------------ dequant
 def _all_finite_fp16():
     bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)

@@ -199,7 +199,7 @@ class GpuWorkload:
                 self.noise[l] = t.pin_memory() if host_inputs else t.to(dev)
         self.noise_stage = {l: torch.empty((self.nq - 1, nmax), dtype=torch.float32, device=dev)
                             for l in self.sel} if self.nq > 1 and host_inputs else None
-        self.qrows = {l: torch.empty((max(self.nq - 1, 1), nmax), dtype=torch.float32, device=dev) for l in self.sel}
+        self.qrows = {l: torch.empty((self.nq, nmax), dtype=torch.float32, device=dev) for l in self.sel}
         self.stage = {l: torch.empty(nmax, dtype=torch.float32, device=dev) for l in self.sel}
         self.idx = {l: [torch.zeros((self.nq, w.k), dtype=torch.int32, device=dev) for _ in range(2)]
                     for l in self.sel}
@@ -237,9 +237,10 @@ class GpuWorkload:
             z.copy_(self.noise[l][s, :, :n], non_blocking=True)
         else:
             z = self.noise[l][s, :, :n]
-        out = self.qrows[l][:, :n]
-        out.copy_((row0.double().unsqueeze(0) + z.double()).float())
-        return [row0] + [out[q] for q in range(self.nq - 1)]
+        out = self.qrows[l]
+        out[0, :n].copy_(row0)
+        out[1:, :n].copy_((row0.double().unsqueeze(0) + z.double()).float())
+        return out, n
 
     def step(self, s, ev=None, kev=None):
         """One decode step over all layers.  ev: (start, end) events; kev: dict
@@ -281,8 +282,8 @@ class GpuWorkload:
                 rec("append", lambda: ctx.append_rows(l, src))
             if self.nq > 1:
                 if l in self.sel:
-                    for q, row in enumerate(qr[l]):
-                        rec("select", lambda: ctx.select_topk(row, w.k, self.idx[l][s & 1][q]))
+                    rows, n = qr[l]
+                    rec("select", lambda: ctx.select_topk_batch(rows, w.k, n, self.idx[l][s & 1]))
                 rec("resolve", lambda: ctx.resolve_gather_multi(l, self.idx[src_l][s & 1], self.out_rows,
                                                                  self.out_bf16))
                 continue
@@ -676,7 +677,7 @@ def main():
     config = {"workload": w.name, "layers": w.layers, "history": w.n0, "hot_rows": w.hot_rows, "k": w.k,
               "appends_per_step": w.appends_per_step, "select_every": w.select_every,
               "bf16_output": w.bf16, "queries": w.queries, "parallelism": f"replicas{world}",
-              "calls": ("kvo_append_rows+kvo_select_topk x%d+kvo_resolve_gather_multi" % w.queries if w.queries > 1
+              "calls": ("kvo_append_rows+kvo_select_topk_batch(%d rows)+kvo_resolve_gather_multi" % w.queries if w.queries > 1
                         else "kvo_append_rows+kvo_select_topk+kvo_resolve_gather" if args.separate
                         else "kvo_decode_step"),
               "l2": "flushed between steps (1 GiB memset, outside the step events)"}

@@ -246,6 +246,16 @@ kvo_status kvo_select_topk(kvo_ctx* ctx, const float* scores, int64_t n, int32_t
   return ok(e) ? KVO_OK : KVO_ECUDA;
 }
 
+kvo_status kvo_select_topk_batch(kvo_ctx* ctx, const float* scores, int64_t n, int64_t ld, int32_t nq, int32_t k,
+                                 int32_t* idx, void* stream) {
+  if (!ctx || !scores || !idx || nq < 1 || nq > 65535 || k < 1 || k > KVO_MAX_K || n < k || n > INT32_MAX ||
+      ld < n)
+    return KVO_EINVAL;
+  const cudaError_t e = kvo::launch_topk(scores, (uint32_t)n, (uint32_t)k, idx, ctx->max_cluster,
+                                         static_cast<cudaStream_t>(stream), (uint32_t)nq, (uint64_t)ld);
+  return ok(e) ? KVO_OK : KVO_ECUDA;
+}
+
 kvo_status kvo_resolve_gather(kvo_ctx* ctx, int32_t layer, const int32_t* idx, int32_t k,
                               void* out_rows, uint16_t* out_bf16, void* stream) {
   if (!ctx || layer < 0 || layer >= ctx->layers || !idx || k < 1 || k > KVO_MAX_K ||

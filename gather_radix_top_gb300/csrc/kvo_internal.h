@@ -35,7 +35,7 @@ struct ClusterShape {
 
 // Launchers (return a CUDA error code; arguments are validated by the caller).
 cudaError_t launch_topk(const float* scores, uint32_t n, uint32_t k, int32_t* idx,
-                        int max_cluster, cudaStream_t stream);
+                        int max_cluster, cudaStream_t stream, uint32_t nq = 1, uint64_t ld = 0);
 cudaError_t launch_resolve(const LayerView& L, const int32_t* idx, uint32_t k, uint8_t* out_rows,
                            uint16_t* out_bf16, uint32_t* status, int max_cluster,
                            cudaStream_t stream);

@@ -11,12 +11,17 @@ namespace {
 
 using namespace topk_detail;
 
+// One cluster per row of scores: cluster blockIdx.x / clusterDim.x selects
+// from row scores + row * ld into idx + row * k.
 template <bool kResident>
 __global__ void __launch_bounds__(kThreads, 1)
-    topk_kernel(const float* __restrict__ scores, uint32_t n, uint32_t k, int32_t* __restrict__ idx) {
+    topk_kernel(const float* __restrict__ scores, uint32_t n, uint64_t ld, uint32_t k, int32_t* __restrict__ idx) {
   extern __shared__ __align__(16) uint8_t dyn_smem[];
   __shared__ RadixSmem rsm;
-  topk_body<kResident>(scores, n, k, dyn_smem, &rsm, [&](uint32_t pos, uint32_t out) { idx[out] = (int32_t)pos; });
+  const uint32_t row = blockIdx.x / cluster_size();
+  const float* s = scores + row * ld;
+  int32_t* out_idx = idx + (size_t)row * k;
+  topk_body<kResident>(s, n, k, dyn_smem, &rsm, [&](uint32_t pos, uint32_t out) { out_idx[out] = (int32_t)pos; });
 }
 
 struct TopkConfig {
@@ -28,7 +33,7 @@ TopkConfig g_topk[64];
 }  // namespace
 
 cudaError_t launch_topk(const float* scores, uint32_t n, uint32_t k, int32_t* idx,
-                        int max_cluster, cudaStream_t stream) {
+                        int max_cluster, cudaStream_t stream, uint32_t nq, uint64_t ld) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -57,14 +62,14 @@ cudaError_t launch_topk(const float* scores, uint32_t n, uint32_t k, int32_t* id
   attr[0].val.clusterDim.x = C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  lc.gridDim = dim3(C, 1, 1);
+  lc.gridDim = dim3((unsigned)C * nq, 1, 1);
   lc.blockDim = dim3(kThreads, 1, 1);
   lc.dynamicSmemBytes = resident ? (size_t)chunk * 4u : 0;
   lc.stream = stream;
   lc.attrs = attr;
   lc.numAttrs = 1;
-  if (resident) return cudaLaunchKernelEx(&lc, topk_kernel<true>, scores, n, k, idx);
-  return cudaLaunchKernelEx(&lc, topk_kernel<false>, scores, n, k, idx);
+  if (resident) return cudaLaunchKernelEx(&lc, topk_kernel<true>, scores, n, ld, k, idx);
+  return cudaLaunchKernelEx(&lc, topk_kernel<false>, scores, n, ld, k, idx);
 }
 
 int best_cluster(const void* kernel, size_t smem, int want) {

@@ -24,6 +24,7 @@ KVO_OK, KVO_EINVAL, KVO_ENOMEM, KVO_ECUDA, KVO_ERANGE, KVO_EBUSY, KVO_ETIMEDOUT,
 
 EXPORTED = [
     "kvo_status_string", "kvo_create", "kvo_destroy", "kvo_append_rows", "kvo_select_topk",
+    "kvo_select_topk_batch",
     "kvo_resolve_gather", "kvo_resolve_gather_multi", "kvo_decode_step", "kvo_sync", "kvo_get_stats", "kvo_history_length",
     "kvo_debug_dump_layer", "kvo_debug_record_evictions", "kvo_debug_evictions",
     "kvo_probe_host_read",
@@ -79,6 +80,7 @@ def lib() -> ctypes.CDLL:
         "kvo_destroy": (ctypes.c_int, [_vp]),
         "kvo_append_rows": (ctypes.c_int, [_vp, _i32, _vp, _i64, _vp]),
         "kvo_select_topk": (ctypes.c_int, [_vp, _vp, _i64, _i32, _vp, _vp]),
+        "kvo_select_topk_batch": (ctypes.c_int, [_vp, _vp, _i64, _i64, _i32, _i32, _vp, _vp]),
         "kvo_resolve_gather": (ctypes.c_int, [_vp, _i32, _vp, _i32, _vp, _vp, _vp]),
         "kvo_resolve_gather_multi": (ctypes.c_int, [_vp, _i32, _vp, _i32, _i32, _vp, _vp, _vp]),
         "kvo_decode_step": (ctypes.c_int, [_vp, _i32, _vp, _i64, _vp, _i64, _i32, _vp, _vp, _vp, _vp]),
@@ -178,6 +180,21 @@ def kvo_select_topk(ctx: int, scores, k: int, idx=None, stream=None):
         idx = torch.empty(k, dtype=torch.int32, device=scores.device)
     _check(lib().kvo_select_topk(ctx, _dev_ptr(scores, "torch.float32"), scores.numel(), k,
                                  _dev_ptr(idx, "torch.int32"), _stream_ptr(stream)), "kvo_select_topk")
+    return idx
+
+
+def kvo_select_topk_batch(ctx: int, scores, k: int, n: int | None = None, idx=None, stream=None):
+    """scores: float32 CUDA tensor [nq, ld] (row-contiguous); the first n
+    (default ld) of each row are selected from.  Returns idx int32 [nq, k]."""
+    import torch
+    if scores.dim() != 2 or scores.stride(1) != 1:
+        raise ValueError("scores must be [nq, ld] with contiguous rows")
+    nq, ld = scores.shape[0], scores.stride(0)
+    n = scores.shape[1] if n is None else n
+    if idx is None:
+        idx = torch.empty((nq, k), dtype=torch.int32, device=scores.device)
+    _check(lib().kvo_select_topk_batch(ctx, ctypes.c_void_p(scores.data_ptr()), n, ld, nq, k,
+                                       _dev_ptr(idx, "torch.int32"), _stream_ptr(stream)), "kvo_select_topk_batch")
     return idx
 
 
@@ -301,6 +318,9 @@ class Context:
 
     def select_topk(self, scores, k, idx=None, stream=None):
         return kvo_select_topk(self.handle, scores, k, idx, stream)
+
+    def select_topk_batch(self, scores, k, n=None, idx=None, stream=None):
+        return kvo_select_topk_batch(self.handle, scores, k, n, idx, stream)
 
     def resolve_gather(self, layer, idx, out_rows=None, out_bf16=None, stream=None):
         kvo_resolve_gather(self.handle, layer, idx, out_rows, out_bf16, stream)

@@ -124,6 +124,19 @@ kvo_status kvo_select_topk(kvo_ctx* ctx, const float* scores, int64_t n, int32_t
                            int32_t* idx, void* stream);
 
 /*
+ * kvo_select_topk_batch - kvo_select_topk for nq rows of scores in one
+ * launch (one thread-block cluster per row): the rows of a multi-query
+ * round ([KVO] "GPU cache management has hazards too": MTP verification
+ * selects for several query rows).
+ *   scores  device fp32; row q starts at scores + q*ld (ld >= n).
+ *   idx     device int32[nq*k]; row q's positions, ascending, at idx + q*k.
+ * Errors: KVO_EINVAL unless nq >= 1, ld >= n and kvo_select_topk's limits
+ * hold.
+ */
+kvo_status kvo_select_topk_batch(kvo_ctx* ctx, const float* scores, int64_t n, int64_t ld, int32_t nq, int32_t k,
+                                 int32_t* idx, void* stream);
+
+/*
  * kvo_resolve_gather - resolve k selected positions of one layer against its
  * hot cache and emit their rows ([KVO] "Decision three: let the GPU manage
  * the hot cache directly" and "GPU cache management has hazards too").

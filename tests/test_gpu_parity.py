@@ -70,6 +70,21 @@ def test_topk_degenerate_orders(ctx, n, k):
         np.testing.assert_array_equal(idx, O.select_topk(s, k))
 
 
+@pytest.mark.parametrize("nq,n,ld,k", [(1, 1000, 1000, 100), (4, 50_024, 51_200, 2048), (3, 4099, 4101, 1000),
+                                        (5, 1_048_576, 1_048_576, 2048), (2, 200_000, 200_003, 4093)])
+def test_topk_batch_matches_oracle_per_row(ctx, nq, n, ld, k):
+    """One launch, one cluster per row; rows at any stride (unaligned too)."""
+    import torch
+    rows = np.zeros((nq, ld), np.float32)
+    for q in range(nq):
+        rows[q, :n] = W.random_scores(nq * 1000 + q + n, n, ["normal", "ties", "special"][q % 3])
+        rows[q, n:] = np.inf                          # beyond n: must never be selected
+    idx = ctx.select_topk_batch(torch.from_numpy(rows).cuda(), k, n)
+    got = idx.cpu().numpy()
+    for q in range(nq):
+        np.testing.assert_array_equal(got[q], O.select_topk(rows[q, :n], k))
+
+
 def test_topk_k_equals_n_and_unaligned_scores(ctx):
     import torch
     s = W.random_scores(11, 3001, "special")
@@ -403,8 +418,7 @@ def _mtp_run(kvo, w, steps, check_every=1, want_bf16=False):
             st.append(row)
         row0 = W.apply_carry(W.base_scores(w, 0, step), prev, W.carry_draw(w, 0, step), w.carry_boost)
         rows = [row0] + [W.query_scores(w, 0, step, q, row0) for q in range(1, nq)]
-        for q, r in enumerate(rows):
-            ctx.select_topk(torch.from_numpy(r).cuda(), k, idx[q])
+        ctx.select_topk_batch(torch.from_numpy(np.stack(rows)).cuda(), k, idx=idx)
         ctx.resolve_gather_multi(0, idx, out, outb)
         want = np.stack([O.select_topk(r, k) for r in rows])
         res = O.resolve_gather_multi(st, want, want_bf16=want_bf16)

@@ -110,9 +110,19 @@ class LayerState:
     pos2slot is a plain dict (position -> slot); slot2pos uses -1 for an
     empty slot; last_use uses 0 for "never referenced"; ``step`` counts this
     layer's resolve calls (the first call runs at step 1).
+
+    ``policy`` picks the replacement rule: "lru" (least recently used
+    unpinned slot first, keyed (last_use, slot)) or "circular" (the pages'
+    final rule, "GPU cache management has hazards too": a hand walks the
+    slots in circular order and the next unpinned slot is evicted; ``hand``
+    is where the next walk starts).
     """
 
-    def __init__(self, history_cap: int, hot_rows: int):
+    def __init__(self, history_cap: int, hot_rows: int, policy: str = "lru"):
+        if policy not in ("lru", "circular"):
+            raise ValueError("policy must be 'lru' or 'circular'")
+        self.policy = policy
+        self.hand = 0
         self.history_cap = int(history_cap)
         self.hot_rows = int(hot_rows)
         self.history = np.zeros((self.history_cap, ROW_BYTES), np.uint8)
@@ -206,9 +216,18 @@ def resolve_gather(state: LayerState, idx, want_bf16: bool = False) -> ResolveRe
                 unique.append(p)
     res.unique_misses = len(unique)
 
-    free = np.nonzero(state.last_use < t)[0]
-    order = np.lexsort((free, state.last_use[free]))    # by last_use, then slot
-    victims = free[order][:len(unique)]
+    if state.policy == "lru":
+        free = np.nonzero(state.last_use < t)[0]
+        order = np.lexsort((free, state.last_use[free]))    # by last_use, then slot
+        victims = free[order][:len(unique)]
+    else:
+        # circular: the unpinned slots in the order hand, hand+1, ... (mod H);
+        # the hand moves past the last victim
+        H = state.hot_rows
+        walk = (state.hand + np.arange(H)) % H
+        victims = walk[state.last_use[walk] < t][:len(unique)]
+        if len(victims):
+            state.hand = (int(victims[-1]) + 1) % H
     assert len(victims) == len(unique)
 
     for p, v in zip(unique, victims):

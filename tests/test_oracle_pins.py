@@ -242,6 +242,79 @@ def test_empty_slots_fill_in_slot_order_then_lru():
     assert r.evictions == [(1, 11, 14), (0, 10, 15)]
 
 
+# ------------------------------------------------- circular replacement
+def _brute_step_circular(H, pairs, slot2pos, last_use, hand, t, idx, length):
+    """The circular rule one miss at a time: from the hand, step over every
+    slot referenced in this step (hits and slots already filled in it) and
+    evict the first other one; the hand then points past it."""
+    touched = set()
+    unique = []
+    for p in idx:
+        p = int(p)
+        if p < 0 or p >= length:
+            continue
+        s = next((sl for (q, sl) in pairs if q == p), None)
+        if s is not None:
+            touched.add(s)
+        elif p not in unique:
+            unique.append(p)
+    ev = []
+    for p in unique:
+        while hand in touched:
+            hand = (hand + 1) % H
+        v = hand
+        hand = (hand + 1) % H
+        touched.add(v)
+        old = slot2pos[v]
+        if old >= 0:
+            pairs[:] = [pr for pr in pairs if pr[0] != old]
+        pairs.append([p, v])
+        slot2pos[v] = p
+        ev.append((v, old, p))
+    for s in touched:
+        last_use[s] = t
+    return ev, hand
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_circular_equals_sequential_definition(seed):
+    g = np.random.default_rng(500 + seed)
+    H = int(g.integers(4, 40))
+    n = int(g.integers(H, 4 * H + 8))
+    st = O.LayerState(n, H, policy="circular")
+    st.append(g.integers(0, 256, size=(n, O.ROW_BYTES), dtype=np.uint8))
+    pairs, slot2pos, last_use, hand = [], [-1] * H, [0] * H, 0
+    for t in range(1, 40):
+        k = int(g.integers(1, min(12, H) + 1))
+        idx = g.integers(0, n, size=k)
+        if g.random() < 0.5:
+            idx[g.integers(0, k)] = idx[0]
+        res = O.resolve_gather(st, idx)
+        ev, hand = _brute_step_circular(H, pairs, slot2pos, last_use, hand, t, idx, n)
+        assert res.evictions == ev
+        assert st.hand == hand
+        assert np.array_equal(st.slot2pos, slot2pos)
+        assert np.array_equal(st.last_use, last_use)
+
+
+def test_circular_worked_example():
+    st = O.LayerState(100, 4, policy="circular")
+    st.append(np.zeros((100, O.ROW_BYTES), np.uint8))
+    assert O.resolve_gather(st, [10, 11, 12]).evictions == [(0, -1, 10), (1, -1, 11), (2, -1, 12)]
+    assert st.hand == 3
+    # 10 and 12 pinned by hits; the hand takes 3, wraps, skips 0 (pinned), takes 1
+    assert O.resolve_gather(st, [10, 12, 13, 14]).evictions == [(3, -1, 13), (1, 11, 14)]
+    assert st.hand == 2
+    # LRU takes the same two here: slot 3 (never used) before slot 1 (used at t=1)
+    lru = O.LayerState(100, 4)
+    lru.append(np.zeros((100, O.ROW_BYTES), np.uint8))
+    O.resolve_gather(lru, [10, 11, 12])
+    assert O.resolve_gather(lru, [10, 12, 13, 14]).evictions == [(3, -1, 13), (1, 11, 14)]
+    # the policies part ways when a recently used slot lies under the hand
+    assert O.resolve_gather(st, [15]).evictions == [(2, 12, 15)]      # circular: next after the hand
+    assert O.resolve_gather(lru, [15]).evictions == [(0, 10, 15)]     # LRU: the oldest (slot 0, t=2)
+
+
 # ------------------------------------------------- multi-query rounds
 def test_multi_query_round_worked_example():
     """Two query rows select the same missing position in one round: only

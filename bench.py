@@ -156,13 +156,15 @@ class GpuWorkload:
     """Device-resident inputs and a context for one replica of a workload."""
 
     def __init__(self, w: W.Workload, layer_base: int, steps: int, host_inputs: bool = False,
-                 fused: bool = True):
+                 fused: bool = True, policy: str = "lru"):
         import torch
         from gather_radix_top_gb300 import kvo
         self.torch, self.kvo, self.w = torch, kvo, w
         self.steps = steps
         self.host_inputs = host_inputs
         self.ctx = kvo.Context(w.layers, w.history_cap, w.hot_rows)
+        if policy == "circular":
+            self.ctx.set_policy(kvo.POLICY_CIRCULAR)
         self.sel = w.selecting_layers()
         for l in range(w.layers):
             self.ctx.append_rows(l, W.rows(w, layer_base + l, 0, w.n0))
@@ -333,7 +335,7 @@ def run_gpu_arm(args, w, rank, world):
     build.build()
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
     steps = args.warmup + args.steps
-    wl = GpuWorkload(w, layer_base=rank * w.layers, steps=steps, fused=not args.separate)
+    wl = GpuWorkload(w, layer_base=rank * w.layers, steps=steps, fused=not args.separate, policy=args.policy)
     flush = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
     dist = world > 1
     if dist:
@@ -390,7 +392,7 @@ def run_e2e(args, w):
     copies inside each step's events."""
     import torch
     steps = args.warmup + args.steps
-    wl = GpuWorkload(w, layer_base=0, steps=steps, host_inputs=True, fused=not args.separate)
+    wl = GpuWorkload(w, layer_base=0, steps=steps, host_inputs=True, fused=not args.separate, policy=args.policy)
     flush = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
     evs = []
     for s in range(steps):
@@ -417,7 +419,7 @@ def run_e2e(args, w):
 
 
 # ----------------------------------------------------------- oracle arm
-def run_oracle(w, max_steps, budget_s, layers=None):
+def run_oracle(w, max_steps, budget_s, layers=None, policy="lru"):
     """The oracle as it stands, on the host cores: the first steps of the
     workload (every layer, or the first `layers`) until `budget_s` of oracle
     time.  Returns rows/s, the steps done and the selections."""
@@ -426,7 +428,7 @@ def run_oracle(w, max_steps, budget_s, layers=None):
     states = []
     extra = {}
     for l in range(L):
-        st = O.LayerState(w.history_cap, w.hot_rows)
+        st = O.LayerState(w.history_cap, w.hot_rows, policy=policy)
         st.append(W.rows(w, l, 0, w.n0))
         states.append(st)
         if w.appends_per_step:
@@ -646,6 +648,128 @@ def sessions_main(args, rank, world):
     print(json.dumps(line))
 
 
+# ----------------------------------------------- replacement-policy probe
+def probe_rounds(w, steps):
+    idxs, prev = [], None
+    for s in range(steps):
+        prev = W.probe_idx(w, s, prev)
+        idxs.append(prev)
+    return np.stack(idxs)
+
+
+def run_probe_oracle(w, idxs, first, budget_s, policy):
+    """The oracle on the probe's rounds; rounds before `first` are the untimed fill."""
+    from oracle import kvo_oracle as O
+    st = O.LayerState(w.n0, w.hot_rows, policy=policy)
+    st.append(W.rows(w, 0, 0, w.n0))
+    spent, done, cpu = 0.0, 0, 0.0
+    for s in range(idxs.shape[0]):
+        t, c = time.perf_counter(), time.process_time()
+        O.resolve_gather(st, idxs[s])
+        if s >= first:
+            spent += time.perf_counter() - t
+            cpu += time.process_time() - c
+            done += 1
+            if spent >= budget_s:
+                break
+    return {"rows_per_s": done * w.k / max(spent, 1e-9), "rounds": done, "seconds": spent,
+            "cores": max(1, round(cpu / max(spent, 1e-9)))}
+
+
+def probe_main(args, rank, world):
+    """Per-gather latency of the resolve on a full hot cache with 1% misses,
+    for the chosen replacement policy (the pages' clock pathology probe)."""
+    w = W.PROBE
+    warm = w.extra["warm_rounds"]
+    if args.steps is None:
+        args.steps = 512
+    steps = warm + args.warmup + args.steps
+    idxs = probe_rounds(w, steps)
+    config = {"workload": w.name, "policy": args.policy, "hot_rows": w.hot_rows, "k": w.k,
+              "misses_per_round": w.extra["fresh"], "history": w.n0, "fill_rounds": warm,
+              "calls": "kvo_resolve_gather", "parallelism": f"replicas{world}",
+              "l2": "flushed between rounds (1 GiB memset, outside the events)"}
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        o = run_probe_oracle(w, idxs, warm + args.warmup, max(10.0, args.cpu_seconds), args.policy)
+        print(json.dumps({"impl": "reference", "metric": METRIC, "value": round(o["rows_per_s"], 1),
+                          "unit": "rows/s", "n_gpus": world, "steps": o["rounds"], "warmup": 0,
+                          "ms_per_step": round(1e3 * o["seconds"] / max(o["rounds"], 1), 3),
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+                          "data": "synthetic", "config": config,
+                          "cpu_baseline": {"value": round(o["rows_per_s"], 1), "unit": "rows/s",
+                                           "cores": o["cores"], "kind": "oracle",
+                                           "sample": f"{o['rounds']} probe rounds"},
+                          "e2e": {"value": round(o["rows_per_s"], 1), "unit": "rows/s", "h2d_bytes_per_step": 0,
+                                  "d2h_bytes_per_step": 0}}))
+        return
+    import torch
+    from gather_radix_top_gb300 import build, kvo
+    build.build()
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    cpu = (run_probe_oracle(w, idxs, warm + args.warmup, args.cpu_seconds, args.policy)
+           if rank == 0 and world == 1 else None)
+    ctx = kvo.Context(1, w.n0, w.hot_rows)
+    if args.policy == "circular":
+        ctx.set_policy(kvo.POLICY_CIRCULAR)
+    ctx.append_rows(0, W.rows(w, 0, 0, w.n0))
+    idx_dev = torch.from_numpy(idxs).cuda()
+    out = torch.empty((w.k, ROW), dtype=torch.uint8, device="cuda")
+    flush = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
+    for s in range(warm + args.warmup):
+        flush.zero_()
+        ctx.resolve_gather(0, idx_dev[s], out)
+    torch.cuda.synchronize()
+    st0 = ctx.stats(0)
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    evs = []
+    for s in range(warm + args.warmup, steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        ctx.resolve_gather(0, idx_dev[s], out)
+        b.record()
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    status = ctx.sync()
+    st1 = ctx.stats(0)
+    ms = [a.elapsed_time(b) for a, b in evs]
+    total_s = sum(ms) * 1e-3
+    delta = {f: st1[f] - st0[f] for f in st0}
+    ctx.close()
+    if world > 1:
+        import torch.distributed as tdist
+        t = torch.tensor([total_s], dtype=torch.float64, device="cuda")
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        total_s = float(t.item())
+        if rank != 0:
+            return
+    hbm_peak, peak_src = load_peaks()
+    ab = algorithmic_bytes(w, 0.0, delta, args.steps, 1)
+    us = float(np.mean(ms)) * 1e3
+    achieved = ab["resolve_hbm"] / (us * 1e-6) / 1e9
+    line = {"metric": METRIC, "value": round(args.steps * w.k * world / total_s, 1), "unit": "rows/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * total_s / args.steps, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "u8", "data": "synthetic", "config": config,
+            "roofline": {"bound": "hbm", "kernel": "resolve", "achieved": round(achieved, 1), "peak": hbm_peak,
+                         "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "traffic": None,
+                         "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
+                         "algorithmic_bytes_per_launch": round(ab["resolve_hbm"])},
+            "per_call": {"us_p50": round(1e3 * float(np.percentile(ms, 50)), 2),
+                         "us_p99": round(1e3 * float(np.percentile(ms, 99)), 2),
+                         "us_max": round(1e3 * float(np.max(ms)), 2),
+                         "hits": round(ab["hits"], 1), "misses": round(ab["misses"], 1)},
+            "gpu_launches": args.steps, "clocks": clk, "device_status": status}
+    if cpu is not None:
+        line["cpu_baseline"] = {"value": round(cpu["rows_per_s"], 1), "unit": "rows/s", "cores": cpu["cores"],
+                                "kind": "oracle", "sample": f"{cpu['rounds']} probe rounds ({cpu['seconds']:.1f} s)"}
+    print(json.dumps(line))
+
+
 # -------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -656,12 +780,16 @@ def main():
     ap.add_argument("--workload", choices=sorted(W.WORKLOADS) + [W.SESSIONS.name], default="50k_single_layer")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--policy", choices=["lru", "circular"], default="lru", help="hot-cache replacement policy")
     ap.add_argument("--sessions", type=int, default=None, help="session_evict_restore: number of sessions")
     ap.add_argument("--session-tokens", type=int, default=None, help="session_evict_restore: tokens per session")
     ap.add_argument("--separate", action="store_true",
                     help="time kvo_append_rows + kvo_select_topk + kvo_resolve_gather instead of kvo_decode_step")
     args = ap.parse_args()
 
+    if args.workload == W.PROBE.name:
+        probe_main(args, int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")))
+        return
     if args.workload == W.SESSIONS.name:
         if args.steps is None:
             args.steps = 5
@@ -676,7 +804,7 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     config = {"workload": w.name, "layers": w.layers, "history": w.n0, "hot_rows": w.hot_rows, "k": w.k,
               "appends_per_step": w.appends_per_step, "select_every": w.select_every,
-              "bf16_output": w.bf16, "queries": w.queries, "parallelism": f"replicas{world}",
+              "bf16_output": w.bf16, "queries": w.queries, "policy": args.policy, "parallelism": f"replicas{world}",
               "calls": ("kvo_append_rows+kvo_select_topk_batch(%d rows)+kvo_resolve_gather_multi" % w.queries if w.queries > 1
                         else "kvo_append_rows+kvo_select_topk+kvo_resolve_gather" if args.separate
                         else "kvo_decode_step"),
@@ -685,7 +813,7 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        o = run_oracle(w, args.warmup + args.steps, budget_s=max(30.0, 0.5 * args.cpu_seconds * 8))
+        o = run_oracle(w, args.warmup + args.steps, budget_s=max(30.0, 0.5 * args.cpu_seconds * 8), policy=args.policy)
         line = {"impl": "reference", "metric": METRIC, "value": round(o["rows_per_s"], 1), "unit": "rows/s",
                 "n_gpus": world, "steps": o["steps"], "warmup": 0,
                 "ms_per_step": round(1e3 * o["seconds"] / o["steps"], 3), "higher_is_better": True,
@@ -706,7 +834,7 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1:
-        cpu = run_oracle(w, args.warmup + args.steps, budget_s=args.cpu_seconds)
+        cpu = run_oracle(w, args.warmup + args.steps, budget_s=args.cpu_seconds, policy=args.policy)
 
     g = run_gpu_arm(args, w, rank, world)
     if rank != 0:

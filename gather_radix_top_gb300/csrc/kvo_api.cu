@@ -25,10 +25,11 @@ struct kvo_ctx {
   std::vector<uint8_t*> hist_host;       // pinned host history per layer
   std::vector<kvo::LayerView> views;     // device pointers per layer
   std::vector<int64_t> length;           // host copy of each history length
-  uint32_t* counters = nullptr;          // device [layers][8]: step, length, queue head, tail, buffer
+  uint32_t* counters = nullptr;          // device [layers][8]: step, length, queue head, tail, buffer, hand
   unsigned long long* stats = nullptr;   // device [layers][8]
   int32_t* evlog = nullptr;              // device [layers][1 + 3*KVO_MAX_ROUND] when recording
   uint32_t* status = nullptr;            // device status word
+  bool resolved = false;                 // a resolve has been enqueued (the policy is fixed from then on)
 };
 
 namespace {
@@ -234,6 +235,7 @@ kvo_status kvo_append_rows(kvo_ctx* ctx, int32_t layer, const void* rows, int64_
     e = kvo::launch_append(nullptr, dst_dev, 0, v.counters, (uint32_t)(start + r), s);
   }
   if (!ok(e)) return KVO_ECUDA;
+  ctx->resolved = true;
   ctx->length[layer] = start + r;
   return KVO_OK;
 }
@@ -244,6 +246,20 @@ kvo_status kvo_select_topk(kvo_ctx* ctx, const float* scores, int64_t n, int32_t
   const cudaError_t e = kvo::launch_topk(scores, (uint32_t)n, (uint32_t)k, idx, ctx->max_cluster,
                                          static_cast<cudaStream_t>(stream));
   return ok(e) ? KVO_OK : KVO_ECUDA;
+}
+
+kvo_status kvo_set_policy(kvo_ctx* ctx, int32_t policy) {
+  if (!ctx || (policy != KVO_POLICY_LRU && policy != KVO_POLICY_CIRCULAR)) return KVO_EINVAL;
+  if (ctx->resolved) return KVO_EBUSY;
+  for (kvo::LayerView& v : ctx->views) v.policy = (uint32_t)policy;
+  return KVO_OK;
+}
+
+kvo_status kvo_debug_layer_counters(kvo_ctx* ctx, int32_t layer, uint32_t* out) {
+  if (!ctx || !out || layer < 0 || layer >= ctx->layers) return KVO_EINVAL;
+  if (!ok(cudaDeviceSynchronize())) return KVO_ECUDA;
+  return ok(cudaMemcpy(out, ctx->views[layer].counters, 8 * sizeof(uint32_t), cudaMemcpyDeviceToHost)) ? KVO_OK
+                                                                                                  : KVO_ECUDA;
 }
 
 kvo_status kvo_select_topk_batch(kvo_ctx* ctx, const float* scores, int64_t n, int64_t ld, int32_t nq, int32_t k,
@@ -267,6 +283,7 @@ kvo_status kvo_resolve_gather(kvo_ctx* ctx, int32_t layer, const int32_t* idx, i
   const cudaError_t e =
       kvo::launch_resolve(v, idx, (uint32_t)k, static_cast<uint8_t*>(out_rows), out_bf16, ctx->status,
                           ctx->max_cluster, static_cast<cudaStream_t>(stream));
+  ctx->resolved = true;
   return ok(e) ? KVO_OK : KVO_ECUDA;
 }
 
@@ -281,6 +298,7 @@ kvo_status kvo_resolve_gather_multi(kvo_ctx* ctx, int32_t layer, const int32_t* 
   const cudaError_t e =
       kvo::launch_resolve(v, idx, (uint32_t)(nq * k), static_cast<uint8_t*>(out_rows), out_bf16, ctx->status,
                           ctx->max_cluster, static_cast<cudaStream_t>(stream));
+  ctx->resolved = true;
   if (e == cudaErrorInvalidValue) return KVO_EINVAL;   // the round does not fit this cluster's shared memory
   return ok(e) ? KVO_OK : KVO_ECUDA;
 }

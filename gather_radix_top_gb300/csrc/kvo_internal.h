@@ -19,13 +19,14 @@ struct LayerView {
   uint8_t* hot;                   // [hot_rows * 656]
   const uint8_t* hist;            // device address of the mapped host history
   uint32_t* counters;             // [0] step, [1] history length, [2] queue head, [3] queue tail,
-                                  // [4] queue buffer in use
+                                  // [4] queue buffer in use, [5] circular hand
   unsigned long long* stats;      // kvo_stats fields, in declaration order
   int32_t* evlog;                 // NULL, or [1 + 3 * KVO_MAX_K]: count then triples
   uint64_t* ring;                 // [2][ring_cap]: LRU queue entries (stamp << 32 | slot), two buffers
   uint32_t hot_rows;
   uint32_t history_cap;
   uint32_t ring_cap;              // entries per queue buffer, a power of two >= 8 * hot_rows
+  uint32_t policy;                // KVO_POLICY_LRU or KVO_POLICY_CIRCULAR
 };
 
 struct ClusterShape {

@@ -47,6 +47,8 @@
 // When the queue nears its capacity, its current entries are first copied,
 // in order, to the other of its two buffers (a compaction, once every many
 // calls).
+// With the circular policy there is no queue: CTA 0 walks the slots from the
+// layer's hand instead, skipping the pinned ones, and P5 has nothing to do.
 #pragma once
 
 #include <cstdint>
@@ -236,6 +238,7 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
   __shared__ uint32_t mbefore[kMaxCluster + 1];    // CTA 0: unique misses of lower CTAs
   __shared__ uint32_t ring_off;                    // queue position of this range's used slots
   __shared__ uint32_t head_hit;                    // CTA 0: offset of the first current entry left
+  __shared__ uint32_t last_vic;                    // CTA 0: the last victim (circular policy)
   __shared__ uint32_t nevict_cta;
   __shared__ uint32_t cta_hits, cta_inv;
   __shared__ __align__(8) uint64_t wbar;           // CTA 0: completion of the window copy
@@ -260,6 +263,8 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
   const uint32_t t = L.counters[0] + 1u;        // this call's step
   const uint32_t len = a.fused ? a.len : L.counters[1];
   uint32_t head = L.counters[2], tail = L.counters[3], buf = L.counters[4] & 1u;
+  const uint32_t hand = L.counters[5];
+  const bool lru = L.policy == KVO_POLICY_LRU;     // uniform: one policy per layer
   const uint32_t Q = L.ring_cap, qmask = Q - 1u;
   const uint32_t jlo = r == 0 ? 0u : min(k, (r - 1u) * a.kchunk);
   const uint32_t jcnt = r == 0 ? 0u : min(k, jlo + a.kchunk) - jlo;
@@ -269,7 +274,7 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
   // ------------------------------------------------- queue compaction
   // This call appends at most k entries; make room first when needed (every
   // CTA read the same counters, so every CTA takes the same branch).
-  if (tail - head > Q - k) {
+  if (lru && tail - head > Q - k) {
     tail = compact_queue(L, head, tail, buf, scratch, table2);
     head = 0;
     buf ^= 1u;
@@ -300,8 +305,8 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
   const uint32_t span = tail - head;
   const uint32_t sh = head & 1u;
   const uint32_t wcopy = (min(span + sh, kWindow) + 1u) & ~1u;   // entries copied, even
-  uint32_t wlen = wcopy - sh < span ? wcopy - sh : span;         // entries usable from the window
-  if (r == 0 && tid == 0) {
+  uint32_t wlen = !lru ? 0u : wcopy - sh < span ? wcopy - sh : span;   // entries usable from the window
+  if (lru && r == 0 && tid == 0) {
     asm volatile("fence.proxy.async.global;" ::: "memory");   // a compaction above wrote the queue
     mbar_init(&wbar, 1);
     const uint32_t a0 = (head - sh) & qmask;
@@ -419,7 +424,7 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
   // way the entry's slot is pinned, and the pin bitmap drops it after B1.
   bool win_ok = true;
   uint32_t pre4 = 0;                                // bit q: entry 4 * tid + q of the window was current
-  if (r == 0) {
+  if (lru && r == 0) {
     win_ok = __syncthreads_and(mbar_wait_bounded(&wbar, 0, kWindowPolls));
     if (!win_ok) {
       wlen = 0;                                     // read the queue from global memory instead
@@ -490,27 +495,34 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
       if (lane <= C) mbefore[lane] = incl - mcount;
     }
     __syncthreads();                               // mbefore, and the window copied by other threads
+    // LRU: the queue from its head.  Circular: the slots from the hand.
+    const uint32_t limit = lru ? span : H;
     uint32_t found = 0, off = 0;
-    while (found < M && off < span) {              // uniform over the CTA
+    while (found < M && off < limit) {             // uniform over the CTA
       uint64_t e[4];                               // ~0 marks an entry that is not current
       uint32_t lu[4], ncur = 0;
 #pragma unroll
       for (uint32_t q = 0; q < 4; ++q) {
         const uint32_t o = off + 4 * tid + q;
-        e[q] = o >= span ? ~0ull : o < wlen ? window[sh + o] : __ldcg(&ring_in[(head + o) & qmask]);
+        if (!lru) {
+          const uint32_t sl = hand + o < H ? hand + o : hand + o - H;
+          e[q] = o < H && !((fullpin[sl >> 5] >> (sl & 31)) & 1u) ? (uint64_t)sl : ~0ull;
+        } else {
+          e[q] = o >= span ? ~0ull : o < wlen ? window[sh + o] : __ldcg(&ring_in[(head + o) & qmask]);
+        }
       }
 #pragma unroll
       for (uint32_t q = 0; q < 4; ++q) {           // four independent loads in flight
         const uint32_t o = off + 4 * tid + q, sl = (uint32_t)e[q];
-        lu[q] = o < wlen ? 0u : __ldcg(&L.last_use[sl < H ? sl : 0u]);
+        lu[q] = !lru || o < wlen ? 0u : __ldcg(&L.last_use[sl < H ? sl : 0u]);
       }
 #pragma unroll
       for (uint32_t q = 0; q < 4; ++q) {
         const uint32_t o = off + 4 * tid + q, sl = (uint32_t)e[q];
         // in the window: current before this call and not pinned by it
         const bool cur = e[q] != ~0ull && sl < H &&
-                         (o < wlen ? ((pre4 >> q) & 1u) && !((fullpin[sl >> 5] >> (sl & 31)) & 1u)
-                                   : lu[q] == (uint32_t)(e[q] >> 32));
+                         (!lru || (o < wlen ? ((pre4 >> q) & 1u) && !((fullpin[sl >> 5] >> (sl & 31)) & 1u)
+                                            : lu[q] == (uint32_t)(e[q] >> 32)));
         if (cur) ++ncur;
         else e[q] = ~0ull;
       }
@@ -536,6 +548,7 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
           const uint32_t owner = sl / a.hchunk, b = sl - owner * a.hchunk;
           dsmem_red_or_u32(dsmem_addr(&pinbits[b >> 5], owner), 1u << (b & 31));   // used in this call
           atomicAdd(&fillcnt[owner], 1u);
+          if (u == M - 1) last_vic = sl;
         } else if (u == M) {
           head_hit = off + 4 * tid + q;            // the first current entry that stays
         }
@@ -554,8 +567,9 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
         const uint32_t o = __shfl_up_sync(0xffffffffu, incl, d);
         if (lane >= (uint32_t)d) incl += o;
       }
-      if (lane < C) dsmem_st_u32(dsmem_addr(&ring_off, lane), tail + incl - used);
-      if (lane == 31) {
+      if (lru && lane < C) dsmem_st_u32(dsmem_addr(&ring_off, lane), tail + incl - used);
+      if (!lru && lane == 31) L.counters[5] = M > 0 ? (last_vic + 1u == H ? 0u : last_vic + 1u) : hand;
+      if (lru && lane == 31) {
         L.counters[2] = M > 0 ? head + (head_hit != kNoRank ? head_hit : min(off, span)) : head;
         L.counters[3] = tail + incl;
         L.counters[4] = buf;
@@ -590,7 +604,7 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
   // ---------------------------------------------------------------- P5
   // The used slots of this CTA's range, in slot order, stamped t, at the
   // queue position CTA 0 assigned: one 32-bit bitmap word per thread.
-  {
+  if (lru) {
     const uint32_t hwords = (hcnt + 31u) / 32u;
     const uint64_t stamp = (uint64_t)t << 32;
     uint32_t run = 0;

@@ -16,6 +16,7 @@ ROW_BYTES = 656
 DEQUANT_VALUES = 576
 MAX_K = 4096
 MAX_ROUND = 8192
+POLICY_LRU, POLICY_CIRCULAR = 0, 1
 MAX_HOT_ROWS = 131072
 NOALLOC_MAX_PAIRS = 65536
 
@@ -26,7 +27,8 @@ EXPORTED = [
     "kvo_status_string", "kvo_create", "kvo_destroy", "kvo_append_rows", "kvo_select_topk",
     "kvo_select_topk_batch",
     "kvo_resolve_gather", "kvo_resolve_gather_multi", "kvo_decode_step", "kvo_sync", "kvo_get_stats", "kvo_history_length",
-    "kvo_debug_dump_layer", "kvo_debug_record_evictions", "kvo_debug_evictions",
+    "kvo_debug_dump_layer", "kvo_debug_record_evictions", "kvo_debug_evictions", "kvo_set_policy",
+    "kvo_debug_layer_counters",
     "kvo_probe_host_read",
     "kvo_tier_blocks", "kvo_pool_create", "kvo_pool_destroy", "kvo_pool_alloc", "kvo_pool_write",
     "kvo_pool_read", "kvo_pool_fill", "kvo_store_blocks", "kvo_pool_release", "kvo_restore_blocks",
@@ -91,6 +93,8 @@ def lib() -> ctypes.CDLL:
         "kvo_debug_record_evictions": (ctypes.c_int, [_vp, _i32]),
         "kvo_debug_evictions": (ctypes.c_int, [_vp, _i32, _vp, _i32, ctypes.POINTER(_i32)]),
         "kvo_probe_host_read": (ctypes.c_int, [_vp, _i64, _vp, _vp]),
+        "kvo_set_policy": (ctypes.c_int, [_vp, _i32]),
+        "kvo_debug_layer_counters": (ctypes.c_int, [_vp, _i32, _vp]),
         "kvo_tier_blocks": (_i64, [_i64, _i64]),
         "kvo_pool_create": (ctypes.c_int, [_i32, _i64, _i32, _i32, _i64, ctypes.POINTER(_vp)]),
         "kvo_pool_destroy": (ctypes.c_int, [_vp]),
@@ -269,6 +273,19 @@ def kvo_debug_dump_layer(ctx: int, layer: int, history_cap: int, hot_rows: int, 
     return d
 
 
+def kvo_set_policy(ctx: int, policy: int) -> None:
+    """POLICY_LRU or POLICY_CIRCULAR; only before the context's first resolve."""
+    _check(lib().kvo_set_policy(ctx, policy), "kvo_set_policy")
+
+
+def kvo_debug_layer_counters(ctx: int, layer: int) -> dict:
+    import numpy as np
+    c = np.zeros(8, np.uint32)
+    _check(lib().kvo_debug_layer_counters(ctx, layer, ctypes.c_void_p(c.ctypes.data)), "kvo_debug_layer_counters")
+    return {"step": int(c[0]), "length": int(c[1]), "queue_head": int(c[2]), "queue_tail": int(c[3]),
+            "queue_buffer": int(c[4]), "hand": int(c[5])}
+
+
 def kvo_debug_record_evictions(ctx: int, on: bool) -> None:
     _check(lib().kvo_debug_record_evictions(ctx, 1 if on else 0), "kvo_debug_record_evictions")
 
@@ -342,6 +359,12 @@ class Context:
 
     def dump_layer(self, layer, hot=True) -> dict:
         return kvo_debug_dump_layer(self.handle, layer, self.history_cap, self.hot_rows, hot)
+
+    def set_policy(self, policy):
+        kvo_set_policy(self.handle, policy)
+
+    def counters(self, layer) -> dict:
+        return kvo_debug_layer_counters(self.handle, layer)
 
     def record_evictions(self, on=True):
         kvo_debug_record_evictions(self.handle, on)

@@ -111,6 +111,24 @@ kvo_status kvo_append_rows(kvo_ctx* ctx, int32_t layer, const void* rows, int64_
                            void* stream);
 
 /*
+ * Replacement policies ([KVO] "GPU cache management has hazards too").  In
+ * both, the slots used by a round (its hits, and the slots it fills) are
+ * pinned, and the round's distinct missing positions, in first-occurrence
+ * order, take the victims in the policy's order:
+ *   KVO_POLICY_LRU       the unpinned slots by (last_use, slot) ascending
+ *                        (the default);
+ *   KVO_POLICY_CIRCULAR  the unpinned slots in circular slot order starting
+ *                        at the layer's hand; the hand then moves past the
+ *                        last victim (the pages' final rule).
+ * kvo_set_policy applies to every layer of the context and is accepted only
+ * before the context's first resolve (else KVO_EBUSY); KVO_EINVAL for an
+ * unknown policy.  Host only.
+ */
+#define KVO_POLICY_LRU 0
+#define KVO_POLICY_CIRCULAR 1
+kvo_status kvo_set_policy(kvo_ctx* ctx, int32_t policy);
+
+/*
  * kvo_select_topk - the k highest of n fp32 scores ([KVO] "Separate
  * historical capacity ...": the indexer selects the top 2,048 positions).
  *   scores  device fp32[n].
@@ -220,6 +238,13 @@ kvo_status kvo_history_length(kvo_ctx* ctx, int32_t layer, int64_t* out);
 kvo_status kvo_debug_dump_layer(kvo_ctx* ctx, int32_t layer, int32_t* pos2slot,
                                 int32_t* slot2pos, uint32_t* last_use, void* hot,
                                 uint32_t* step);
+
+/*
+ * kvo_debug_layer_counters - copy the layer's eight device counters to host
+ * uint32[8]: step, history length, LRU-queue head, tail and buffer, the
+ * circular hand, two unused (synchronises the device).
+ */
+kvo_status kvo_debug_layer_counters(kvo_ctx* ctx, int32_t layer, uint32_t* out);
 
 /*
  * kvo_debug_record_evictions - when enabled (on != 0), every resolve call

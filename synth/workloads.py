@@ -41,6 +41,7 @@ _TAG_SCORES = 0x53434F52
 _TAG_CARRY = 0x43415259
 _TAG_SESSION = 0x53455353
 _TAG_QUERY = 0x51524F57
+_TAG_PROBE = 0x50524F42
 
 
 def _rng(*key: int) -> np.random.Generator:
@@ -106,7 +107,15 @@ M1 = Workload("1m_cold_stress", 3, 4, layers=8, n0=1_048_576, hot_rows=32_768, k
 # row 0 exactly the 50K single-layer scores, rows 1-3 close to it
 K50_MTP = K50.scaled(name="50k_mtp4", queries=4)
 
-WORKLOADS = {w.name: w for w in (TINY, K50, STACK, M1, K50_MTP)}
+# Replacement-policy probe ("GPU cache management has hazards too": a full
+# hot cache, every slot recently used, 1% misses per 2,048-row gather).
+# Rounds 0..15 fill the 32,768 slots with positions 0..32,767; from then on
+# every round keeps 2,028 positions of the previous round (all hits) and
+# adds 20 never-seen positions (the misses).
+PROBE = Workload("eviction_probe_1pct", 6, 7, layers=1, n0=32_768 + 20 * 1024, hot_rows=32_768, k=2048,
+                 steps=1024, appends_per_step=0, extra={"warm_rounds": 16, "fresh": 20})
+
+WORKLOADS = {w.name: w for w in (TINY, K50, STACK, M1, K50_MTP, PROBE)}
 
 
 def rows(w: Workload, layer: int, start: int, count: int) -> np.ndarray:
@@ -181,6 +190,19 @@ def query_scores(w: Workload, layer: int, step: int, q: int, row0: np.ndarray) -
     to float32 (exact on any IEEE device)."""
     noise = query_noise32(w, layer, step, q, row0.shape[0])
     return (row0.astype(np.float64) + noise.astype(np.float64)).astype(np.float32)
+
+
+def probe_idx(w: Workload, step: int, prev) -> np.ndarray:
+    """The probe's selection for round `step` (ascending), given the previous
+    round's selection `prev` (None for round 0)."""
+    warm, fresh = w.extra["warm_rounds"], w.extra["fresh"]
+    if step < warm:
+        return np.arange(step * w.k, (step + 1) * w.k, dtype=np.int32)
+    g = _rng(w.seed, w.cfg_id, step, _TAG_PROBE)
+    keep = g.choice(np.asarray(prev), size=w.k - fresh, replace=False)
+    base = warm * w.k + (step - warm) * fresh
+    new = np.arange(base, base + fresh)
+    return np.sort(np.concatenate([keep, new])).astype(np.int32)
 
 
 def random_scores(seed: int, n: int, kind: str = "normal") -> np.ndarray:

@@ -22,13 +22,15 @@ class GpuLayerRun:
     """One layer of a workload on the GPU, driven step by step."""
 
     def __init__(self, w: W.Workload, layer: int, ctx=None, ctx_layer: int = 0, want_rows=True,
-                 want_bf16=None, fused: bool = False):
+                 want_bf16=None, fused: bool = False, policy: int = 0):
         import torch
         from gather_radix_top_gb300 import kvo
         self.torch = torch
         self.w, self.layer = w, layer
         self.own = ctx is None
         self.ctx = ctx or kvo.Context(1, w.history_cap, w.hot_rows)
+        if policy:
+            self.ctx.set_policy(policy)
         self.cl = ctx_layer
         self.ctx.append_rows(self.cl, W.rows(w, layer, 0, w.n0))          # host rows
         extra = w.history_cap - w.n0
@@ -70,9 +72,9 @@ class GpuLayerRun:
 
 
 class OracleLayerRun:
-    def __init__(self, w: W.Workload, layer: int, want_bf16=None):
+    def __init__(self, w: W.Workload, layer: int, want_bf16=None, policy: str = "lru"):
         self.w, self.layer = w, layer
-        self.st = O.LayerState(w.history_cap, w.hot_rows)
+        self.st = O.LayerState(w.history_cap, w.hot_rows, policy=policy)
         self.st.append(W.rows(w, layer, 0, w.n0))
         self.extra = W.rows(w, layer, w.n0, w.history_cap - w.n0) if w.history_cap > w.n0 else None
         self.bf = w.bf16 if want_bf16 is None else want_bf16

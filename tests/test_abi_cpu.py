@@ -49,6 +49,7 @@ def test_bad_arguments_rejected_without_a_device(kvo):
     assert L.kvo_resolve_gather(None, 0, None, 5, None, None, None) == kvo.KVO_EINVAL
     assert L.kvo_append_rows(None, 0, None, 1, None) == kvo.KVO_EINVAL
     assert L.kvo_destroy(None) == kvo.KVO_EINVAL
+    assert L.kvo_set_policy(None, 0) == kvo.KVO_EINVAL
     assert kvo.status_string(kvo.KVO_ERANGE) == "selected position outside the history"
 
 

@@ -463,3 +463,62 @@ def test_multi_query_argument_errors(kvo):
         small.resolve_gather_multi(0, torch.zeros((2, 9), dtype=torch.int32, device="cuda"), out[:18])
     ctx.close()
     small.close()
+
+
+# ------------------------------------------------ circular replacement
+@pytest.mark.parametrize("fused", [False, True])
+def test_circular_policy_tiny_full_parity(kvo, fused):
+    w = W.TINY.scaled(appends_per_step=1)
+    g = GpuLayerRun(w, 0, want_bf16=True, fused=fused, policy=kvo.POLICY_CIRCULAR)
+    o = OracleLayerRun(w, 0, want_bf16=True, policy="circular")
+    g.ctx.record_evictions(True)
+    for step in range(w.steps):
+        np.testing.assert_array_equal(g.step(step), o.step(step))
+        np.testing.assert_array_equal(g.rows(), o.last.rows)
+        np.testing.assert_array_equal(g.bf16(), o.last.bf16)
+        assert g.ctx.evictions(0) == o.last.evictions
+        compare_state(g.ctx, 0, o.st)
+        assert g.ctx.counters(0)["hand"] == o.st.hand
+    assert g.ctx.sync() == 0
+    g.ctx.close()
+
+
+@pytest.mark.parametrize("seed,H,n,k,dup", [(1, 16, 40, 16, 0.3), (3, 1024, 5000, 256, 0.2),
+                                           (6, 32_768, 60_000, 4096, 0.1), (8, 4096, 9000, 3000, 0.0)])
+def test_circular_policy_random_selections(kvo, seed, H, n, k, dup):
+    """The hand wraps many times; duplicates and arbitrary order."""
+    import torch
+    g = np.random.default_rng(seed)
+    hist = g.integers(0, 256, size=(n, O.ROW_BYTES), dtype=np.uint8)
+    ctx = kvo.Context(1, n, H)
+    ctx.set_policy(kvo.POLICY_CIRCULAR)
+    ctx.append_rows(0, hist)
+    ctx.record_evictions(True)
+    st = O.LayerState(n, H, policy="circular")
+    st.append(hist)
+    out = torch.empty((k, O.ROW_BYTES), dtype=torch.uint8, device="cuda")
+    for step in range(20):
+        idx = W.random_idx(seed * 100 + step, n if step % 3 else min(n, 2 * H), k, dup, 0)
+        ctx.resolve_gather(0, torch.from_numpy(idx).cuda(), out)
+        res = O.resolve_gather(st, idx)
+        np.testing.assert_array_equal(out.cpu().numpy(), res.rows)
+        assert ctx.evictions(0) == res.evictions, step
+        assert ctx.counters(0)["hand"] == st.hand
+    assert ctx.sync() == 0
+    compare_state(ctx, 0, st)
+    with pytest.raises(kvo.KvoError):                  # the policy is fixed once resolves ran
+        ctx.set_policy(kvo.POLICY_LRU)
+    ctx.close()
+
+
+def test_circular_policy_50k_all_steps(kvo):
+    w = W.K50
+    g = GpuLayerRun(w, 0, fused=True, policy=kvo.POLICY_CIRCULAR)
+    o = OracleLayerRun(w, 0, policy="circular")
+    for step in range(w.steps):
+        np.testing.assert_array_equal(g.step(step), o.step(step))
+        if step % 64 == 0 or step == w.steps - 1:
+            np.testing.assert_array_equal(g.rows(), o.last.rows)
+    compare_state(g.ctx, 0, o.st)
+    assert g.ctx.counters(0)["hand"] == o.st.hand
+    g.ctx.close()

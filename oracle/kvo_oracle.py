@@ -48,6 +48,7 @@ GROUP = 64                    # "G64": one scale per 64 latent bytes
 N_GROUPS = LATENT_BYTES // GROUP
 ROPE_VALUES = ROPE_BYTES // 2
 DEQUANT_VALUES = LATENT_BYTES + ROPE_VALUES   # 576 bf16 per dequantised row
+COPYBACK_BATCH = 64       # rows per recent-ring copyback
 
 MiB = 1 << 20
 GiB = 1 << 30
@@ -111,6 +112,15 @@ class LayerState:
     empty slot; last_use uses 0 for "never referenced"; ``step`` counts this
     layer's resolve calls (the first call runs at step 1).
 
+    ``ring_rows`` > 0 turns on the recent ring ("From 1M Total to 15+ x 1M
+    Contexts", pipeline "New KV -> GPU recent ring -> batched copyback -> RAM
+    history"; "GPU cache management has hazards too": the ring protects new
+    tokens that have not yet reached RAM): rows appended from device memory
+    wait in the ring and reach RAM in batches of COPYBACK_BATCH rows;
+    ``ram_len`` is how many rows RAM holds (a miss below it reads RAM, at or
+    above it the ring).  Rows appended from host memory go straight to RAM
+    after the pending ring rows.  Without the ring, ram_len == length.
+
     ``policy`` picks the replacement rule: "lru" (least recently used
     unpinned slot first, keyed (last_use, slot)) or "circular" (the pages'
     final rule, "GPU cache management has hazards too": a hand walks the
@@ -118,11 +128,13 @@ class LayerState:
     is where the next walk starts).
     """
 
-    def __init__(self, history_cap: int, hot_rows: int, policy: str = "lru"):
+    def __init__(self, history_cap: int, hot_rows: int, policy: str = "lru", ring_rows: int = 0):
         if policy not in ("lru", "circular"):
             raise ValueError("policy must be 'lru' or 'circular'")
         self.policy = policy
         self.hand = 0
+        self.ring_rows = int(ring_rows)
+        self.ram_len = 0
         self.history_cap = int(history_cap)
         self.hot_rows = int(hot_rows)
         self.history = np.zeros((self.history_cap, ROW_BYTES), np.uint8)
@@ -133,11 +145,13 @@ class LayerState:
         self.last_use = np.zeros(self.hot_rows, np.int64)
         self.step = 0
 
-    def append(self, new_rows: np.ndarray) -> None:
-        """Copy rows to history positions [length, length + r) and grow length.
+    def append(self, new_rows: np.ndarray, from_device: bool = False) -> None:
+        """Rows for history positions [length, length + r); length grows.
 
-        Reading: append touches host history only; an appended row becomes a
-        miss the first time it is selected.
+        Reading: append never touches the hot cache; an appended row becomes
+        a miss the first time it is selected.  With the ring, device rows
+        wait in it until COPYBACK_BATCH of them have gathered (then whole
+        batches move to RAM); host rows first flush the ring, then go to RAM.
         """
         new_rows = np.asarray(new_rows, np.uint8).reshape(-1, ROW_BYTES)
         r = new_rows.shape[0]
@@ -145,6 +159,15 @@ class LayerState:
             raise ValueError("history capacity exceeded")
         self.history[self.length:self.length + r] = new_rows
         self.length += r
+        if self.ring_rows and from_device:
+            pending = self.length - self.ram_len
+            self.ram_len += pending // COPYBACK_BATCH * COPYBACK_BATCH
+        else:
+            self.ram_len = self.length
+
+    def flush_ring(self) -> None:
+        """Every pending ring row to RAM (the export consistency boundary)."""
+        self.ram_len = self.length
 
     def pos2slot_array(self) -> np.ndarray:
         """pos2slot as a dense int32 array over [0, history_cap) (-1 = absent)."""
@@ -162,6 +185,7 @@ class ResolveResult:
         self.misses = 0             # occurrences read from host memory
         self.unique_misses = 0
         self.invalid = 0            # entries outside [0, length)
+        self.host_reads = 0         # miss occurrences served from RAM (position < ram_len)
         self.evictions = []         # (victim slot, evicted position or -1, new position)
         self.slot_of = None         # int32 [k]: hot slot read for a hit, -1 miss, -2 invalid
 
@@ -211,6 +235,7 @@ def resolve_gather(state: LayerState, idx, want_bf16: bool = False) -> ResolveRe
             res.hits += 1
         else:
             res.misses += 1
+            res.host_reads += p < state.ram_len
             if p not in seen_missing:
                 seen_missing.add(p)
                 unique.append(p)

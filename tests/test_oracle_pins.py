@@ -242,6 +242,54 @@ def test_empty_slots_fill_in_slot_order_then_lru():
     assert r.evictions == [(1, 11, 14), (0, 10, 15)]
 
 
+# ------------------------------------------------------- recent ring
+def test_ring_copyback_schedule_closed_form():
+    """Device rows wait in the ring; whole 64-row batches reach RAM."""
+    st = O.LayerState(1000, 16, ring_rows=256)
+    st.append(np.zeros((300, O.ROW_BYTES), np.uint8))          # host rows: straight to RAM
+    assert st.ram_len == 300
+    for i in range(1, 200):
+        st.append(np.full((1, O.ROW_BYTES), i % 251, np.uint8), from_device=True)
+        assert st.ram_len == 300 + 64 * (i // 64)
+        assert 0 <= st.length - st.ram_len < 64
+    st.append(np.zeros((7, O.ROW_BYTES), np.uint8), from_device=True)
+    assert st.ram_len == 300 + 64 * ((199 + 7) // 64)
+    st.append(np.zeros((5, O.ROW_BYTES), np.uint8))            # host rows flush the ring first
+    assert st.ram_len == st.length == 511
+    st.append(np.zeros((3, O.ROW_BYTES), np.uint8), from_device=True)
+    st.flush_ring()
+    assert st.ram_len == st.length == 514
+
+
+def test_ring_changes_no_output_only_where_rows_come_from():
+    """The same run with and without the ring: identical rows, evictions and
+    maps; host reads are the misses below ram_len (all misses without ring)."""
+    w = W.TINY.scaled(appends_per_step=3, steps=16)
+    runs = {}
+    for ring in (0, 256):
+        st = O.LayerState(w.history_cap, w.hot_rows, ring_rows=ring)
+        st.append(W.rows(w, 0, 0, w.n0))
+        extra = W.rows(w, 0, w.n0, w.history_cap - w.n0)
+        prev, log = None, []
+        for step in range(w.steps):
+            st.append(extra[step * 3:step * 3 + 3], from_device=True)
+            ram = st.ram_len
+            s = W.apply_carry(W.base_scores(w, 0, step), prev, W.carry_draw(w, 0, step), w.carry_boost)
+            idx = O.select_topk(s, w.k)
+            res = O.resolve_gather(st, idx)
+            missed = [int(p) for p, sl in zip(idx, res.slot_of) if sl == -1]
+            assert res.host_reads == sum(p < ram for p in missed)
+            log.append((idx.tobytes(), res.rows.tobytes(), tuple(res.evictions), res.host_reads, res.misses))
+            prev = idx
+        runs[ring] = (log, st)
+    for a, b in zip(runs[0][0], runs[256][0]):
+        assert a[:3] == b[:3]
+        assert a[3] == a[4]                       # without the ring every miss reads RAM
+        assert b[3] <= b[4]
+    assert any(b[3] < b[4] for b in runs[256][0])   # recent rows were selected and read from the ring
+    assert runs[0][1].pos2slot == runs[256][1].pos2slot
+
+
 # ------------------------------------------------- circular replacement
 def _brute_step_circular(H, pairs, slot2pos, last_use, hand, t, idx, length):
     """The circular rule one miss at a time: from the hand, step over every

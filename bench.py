@@ -131,7 +131,8 @@ def algorithmic_bytes(w: W.Workload, n_avg: float, stats_delta: dict, resolve_la
     resolve_hbm = (8 * k + 4 * hits + ROW * hits + r_out * k + (ROW + 16) * fills + 12 * window
                    + 8 * (hits + fills))
     select_hbm = 4 * n_avg + 4 * k
-    return {"resolve_hbm": resolve_hbm, "resolve_host": ROW * misses, "select_hbm": select_hbm,
+    host = stats_delta.get("host_bytes", ROW * stats_delta["misses"]) / L   # misses served from the ring excluded
+    return {"resolve_hbm": resolve_hbm, "resolve_host": host, "select_hbm": select_hbm,
             "append_host": ROW * w.appends_per_step, "hits": hits, "misses": misses, "fills": fills}
 
 
@@ -156,7 +157,7 @@ class GpuWorkload:
     """Device-resident inputs and a context for one replica of a workload."""
 
     def __init__(self, w: W.Workload, layer_base: int, steps: int, host_inputs: bool = False,
-                 fused: bool = True, policy: str = "lru"):
+                 fused: bool = True, policy: str = "lru", ring: int = 0):
         import torch
         from gather_radix_top_gb300 import kvo
         self.torch, self.kvo, self.w = torch, kvo, w
@@ -165,6 +166,8 @@ class GpuWorkload:
         self.ctx = kvo.Context(w.layers, w.history_cap, w.hot_rows)
         if policy == "circular":
             self.ctx.set_policy(kvo.POLICY_CIRCULAR)
+        if ring:
+            self.ctx.set_recent_ring(ring)
         self.sel = w.selecting_layers()
         for l in range(w.layers):
             self.ctx.append_rows(l, W.rows(w, layer_base + l, 0, w.n0))
@@ -335,7 +338,8 @@ def run_gpu_arm(args, w, rank, world):
     build.build()
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
     steps = args.warmup + args.steps
-    wl = GpuWorkload(w, layer_base=rank * w.layers, steps=steps, fused=not args.separate, policy=args.policy)
+    wl = GpuWorkload(w, layer_base=rank * w.layers, steps=steps, fused=not args.separate, policy=args.policy,
+                     ring=args.ring)
     flush = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
     dist = world > 1
     if dist:
@@ -392,7 +396,8 @@ def run_e2e(args, w):
     copies inside each step's events."""
     import torch
     steps = args.warmup + args.steps
-    wl = GpuWorkload(w, layer_base=0, steps=steps, host_inputs=True, fused=not args.separate, policy=args.policy)
+    wl = GpuWorkload(w, layer_base=0, steps=steps, host_inputs=True, fused=not args.separate, policy=args.policy,
+                     ring=args.ring)
     flush = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
     evs = []
     for s in range(steps):
@@ -419,7 +424,7 @@ def run_e2e(args, w):
 
 
 # ----------------------------------------------------------- oracle arm
-def run_oracle(w, max_steps, budget_s, layers=None, policy="lru"):
+def run_oracle(w, max_steps, budget_s, layers=None, policy="lru", ring=0):
     """The oracle as it stands, on the host cores: the first steps of the
     workload (every layer, or the first `layers`) until `budget_s` of oracle
     time.  Returns rows/s, the steps done and the selections."""
@@ -428,7 +433,7 @@ def run_oracle(w, max_steps, budget_s, layers=None, policy="lru"):
     states = []
     extra = {}
     for l in range(L):
-        st = O.LayerState(w.history_cap, w.hot_rows, policy=policy)
+        st = O.LayerState(w.history_cap, w.hot_rows, policy=policy, ring_rows=ring)
         st.append(W.rows(w, l, 0, w.n0))
         states.append(st)
         if w.appends_per_step:
@@ -445,7 +450,7 @@ def run_oracle(w, max_steps, budget_s, layers=None, policy="lru"):
         idx = {}
         for l in range(L):
             for a in range(w.appends_per_step):
-                states[l].append(extra[l][s * w.appends_per_step + a][None])
+                states[l].append(extra[l][s * w.appends_per_step + a][None], from_device=True)
             if l % w.select_every == 0:
                 rows = [scores[l]] + [W.query_scores(w, l, s, q, scores[l]) for q in range(1, w.queries)]
                 idx[l] = np.stack([O.select_topk(row, w.k) for row in rows])
@@ -781,6 +786,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--policy", choices=["lru", "circular"], default="lru", help="hot-cache replacement policy")
+    ap.add_argument("--ring", type=int, default=0, help="recent-ring rows per layer (0: appends go straight to RAM)")
     ap.add_argument("--sessions", type=int, default=None, help="session_evict_restore: number of sessions")
     ap.add_argument("--session-tokens", type=int, default=None, help="session_evict_restore: tokens per session")
     ap.add_argument("--separate", action="store_true",
@@ -804,7 +810,7 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     config = {"workload": w.name, "layers": w.layers, "history": w.n0, "hot_rows": w.hot_rows, "k": w.k,
               "appends_per_step": w.appends_per_step, "select_every": w.select_every,
-              "bf16_output": w.bf16, "queries": w.queries, "policy": args.policy, "parallelism": f"replicas{world}",
+              "bf16_output": w.bf16, "queries": w.queries, "policy": args.policy, "recent_ring": args.ring, "parallelism": f"replicas{world}",
               "calls": ("kvo_append_rows+kvo_select_topk_batch(%d rows)+kvo_resolve_gather_multi" % w.queries if w.queries > 1
                         else "kvo_append_rows+kvo_select_topk+kvo_resolve_gather" if args.separate
                         else "kvo_decode_step"),
@@ -813,7 +819,8 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        o = run_oracle(w, args.warmup + args.steps, budget_s=max(30.0, 0.5 * args.cpu_seconds * 8), policy=args.policy)
+        o = run_oracle(w, args.warmup + args.steps, budget_s=max(30.0, 0.5 * args.cpu_seconds * 8), policy=args.policy,
+                       ring=args.ring)
         line = {"impl": "reference", "metric": METRIC, "value": round(o["rows_per_s"], 1), "unit": "rows/s",
                 "n_gpus": world, "steps": o["steps"], "warmup": 0,
                 "ms_per_step": round(1e3 * o["seconds"] / o["steps"], 3), "higher_is_better": True,
@@ -834,7 +841,7 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1:
-        cpu = run_oracle(w, args.warmup + args.steps, budget_s=args.cpu_seconds, policy=args.policy)
+        cpu = run_oracle(w, args.warmup + args.steps, budget_s=args.cpu_seconds, policy=args.policy, ring=args.ring)
 
     g = run_gpu_arm(args, w, rank, world)
     if rank != 0:

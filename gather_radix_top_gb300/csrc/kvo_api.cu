@@ -8,6 +8,7 @@
 // caches get exact-capacity allocations, never pooled blocks).
 #include <cstdint>
 #include <cstdlib>
+#include <algorithm>
 #include <cstring>
 #include <new>
 #include <vector>
@@ -30,6 +31,8 @@ struct kvo_ctx {
   int32_t* evlog = nullptr;              // device [layers][1 + 3*KVO_MAX_ROUND] when recording
   uint32_t* status = nullptr;            // device status word
   bool resolved = false;                 // a resolve has been enqueued (the policy is fixed from then on)
+  uint32_t ring_rows = 0;                // recent ring rows per layer (0: appends go straight to RAM)
+  std::vector<int64_t> ram_len;          // per layer: rows the host history (RAM) holds
 };
 
 namespace {
@@ -46,6 +49,7 @@ void free_ctx(kvo_ctx* c) {
     cudaFree(v.last_use);
     cudaFree(v.hot);
     cudaFree(v.ring);
+    cudaFree(v.recent);
   }
   for (uint8_t* h : c->hist_host) cudaFreeHost(h);
   cudaFree(c->counters);
@@ -72,6 +76,20 @@ __global__ void append_kernel(const uint4* __restrict__ src, uint4* __restrict__
                               uint32_t* counters, uint32_t new_len) {
   const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
   for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) dst[i] = src[i];
+  if (blockIdx.x == 0 && threadIdx.x == 0) counters[1] = new_len;
+}
+
+// Copies device rows into the recent ring (row i to slot (start + i) mod
+// ring rows) and publishes the new length (block 0) in stream order.
+__global__ void ring_append_kernel(const uint4* __restrict__ src, uint4* __restrict__ ring, uint32_t r,
+                                   uint32_t start, uint32_t ring_mask, uint32_t* counters, uint32_t new_len) {
+  constexpr uint32_t kVec = KVO_ROW_BYTES / 16;
+  const uint64_t total = (uint64_t)r * kVec;
+  const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+  for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+    const uint32_t row = (uint32_t)(i / kVec), v = (uint32_t)(i - (uint64_t)row * kVec);
+    ring[(size_t)((start + row) & ring_mask) * kVec + v] = src[i];
+  }
   if (blockIdx.x == 0 && threadIdx.x == 0) counters[1] = new_len;
 }
 
@@ -109,6 +127,18 @@ cudaError_t launch_append(const void* src_dev, uint8_t* hist_dev_dst, uint64_t b
   return cudaGetLastError();
 }
 
+cudaError_t launch_ring_append(const void* src_dev, uint8_t* ring, uint32_t r, uint32_t start, uint32_t ring_mask,
+                               uint32_t* counters, uint32_t new_len, cudaStream_t stream) {
+  const uint64_t nvec = (uint64_t)r * (KVO_ROW_BYTES / 16);
+  uint64_t blocks = (nvec + 255) / 256;
+  if (blocks > 1024) blocks = 1024;
+  if (blocks == 0) blocks = 1;
+  ring_append_kernel<<<(unsigned)blocks, 256, 0, stream>>>(static_cast<const uint4*>(src_dev),
+                                                          reinterpret_cast<uint4*>(ring), r, start, ring_mask,
+                                                          counters, new_len);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_probe(const void* src, uint64_t bytes, void* sink, cudaStream_t stream) {
   int sms = 0, dev = 0;
   cudaGetDevice(&dev);
@@ -119,6 +149,39 @@ cudaError_t launch_probe(const void* src, uint64_t bytes, void* sink, cudaStream
 }
 
 }  // namespace kvo
+
+namespace {
+
+// Moves the layer's ring rows [ram_len, upto) to the host history (one or
+// two copies; the ring wraps) and advances ram_len, in stream order.
+cudaError_t ring_copyback(kvo_ctx* ctx, int32_t layer, int64_t upto, cudaStream_t s) {
+  const int64_t from = ctx->ram_len[layer];
+  if (!ctx->ring_rows || upto <= from) return cudaSuccess;
+  const kvo::LayerView& v = ctx->views[layer];
+  const int64_t R = ctx->ring_rows;
+  int64_t pos = from;
+  while (pos < upto) {
+    const int64_t slot = pos & (R - 1);
+    const int64_t n = std::min(upto - pos, R - slot);
+    const cudaError_t e = cudaMemcpyAsync(ctx->hist_host[layer] + (size_t)pos * KVO_ROW_BYTES,
+                                          v.recent + (size_t)slot * KVO_ROW_BYTES, (size_t)n * KVO_ROW_BYTES,
+                                          cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return e;
+    pos += n;
+  }
+  ctx->ram_len[layer] = upto;
+  return cudaSuccess;
+}
+
+// After device rows were appended: whole batches of KVO_COPYBACK_BATCH rows
+// move to RAM.
+cudaError_t ring_after_append(kvo_ctx* ctx, int32_t layer, cudaStream_t s) {
+  if (!ctx->ring_rows) return cudaSuccess;
+  const int64_t pending = ctx->length[layer] - ctx->ram_len[layer];
+  return ring_copyback(ctx, layer, ctx->ram_len[layer] + pending / KVO_COPYBACK_BATCH * KVO_COPYBACK_BATCH, s);
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -156,6 +219,7 @@ kvo_status kvo_create(int32_t layers, int64_t history_cap, int32_t hot_rows, int
   c->history_cap = history_cap;
   c->hot_rows = hot_rows;
   c->length.assign(layers, 0);
+  c->ram_len.assign(layers, 0);
   bool good = ok(cudaMalloc(&c->counters, sizeof(uint32_t) * 8 * layers)) &&
               ok(cudaMalloc(&c->stats, sizeof(unsigned long long) * 8 * layers)) &&
               ok(cudaMalloc(&c->status, sizeof(uint32_t))) &&
@@ -220,23 +284,34 @@ kvo_status kvo_append_rows(kvo_ctx* ctx, int32_t layer, const void* rows, int64_
   if (!ctx || layer < 0 || layer >= ctx->layers || r < 0) return KVO_EINVAL;
   if (r == 0) return KVO_OK;
   if (!rows || !aligned16(rows) || ctx->length[layer] + r > ctx->history_cap) return KVO_EINVAL;
+  const bool dev_rows = is_device_pointer(rows);
+  if (dev_rows && ctx->ring_rows && r > (int64_t)ctx->ring_rows - KVO_COPYBACK_BATCH) return KVO_EINVAL;
   const int64_t start = ctx->length[layer];
   const uint64_t bytes = (uint64_t)r * KVO_ROW_BYTES;
   kvo::LayerView& v = ctx->views[layer];
   uint8_t* dst_dev = const_cast<uint8_t*>(v.hist) + (size_t)start * KVO_ROW_BYTES;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (is_device_pointer(rows)) {
+  if (dev_rows && ctx->ring_rows) {
+    e = kvo::launch_ring_append(rows, v.recent, (uint32_t)r, (uint32_t)start, ctx->ring_rows - 1, v.counters,
+                                (uint32_t)(start + r), s);
+    if (!ok(e)) return KVO_ECUDA;
+    ctx->length[layer] = start + r;
+    return ok(ring_after_append(ctx, layer, s)) ? KVO_OK : KVO_ECUDA;
+  }
+  if (dev_rows) {
     e = kvo::launch_append(rows, dst_dev, bytes, v.counters, (uint32_t)(start + r), s);
   } else {
-    // Host rows: copy now (the positions are beyond every enqueued read),
-    // then publish the length in stream order.
+    // Host rows: the ring's pending rows go first (they precede these
+    // positions), then the rows are copied now (the positions are beyond
+    // every enqueued read) and the length is published in stream order.
+    if (!ok(ring_copyback(ctx, layer, start, s))) return KVO_ECUDA;
     std::memcpy(ctx->hist_host[layer] + (size_t)start * KVO_ROW_BYTES, rows, bytes);
     e = kvo::launch_append(nullptr, dst_dev, 0, v.counters, (uint32_t)(start + r), s);
   }
   if (!ok(e)) return KVO_ECUDA;
-  ctx->resolved = true;
   ctx->length[layer] = start + r;
+  ctx->ram_len[layer] = start + r;
   return KVO_OK;
 }
 
@@ -246,6 +321,55 @@ kvo_status kvo_select_topk(kvo_ctx* ctx, const float* scores, int64_t n, int32_t
   const cudaError_t e = kvo::launch_topk(scores, (uint32_t)n, (uint32_t)k, idx, ctx->max_cluster,
                                          static_cast<cudaStream_t>(stream));
   return ok(e) ? KVO_OK : KVO_ECUDA;
+}
+
+kvo_status kvo_set_recent_ring(kvo_ctx* ctx, int32_t rows) {
+  if (!ctx || rows < 0 || (rows && (rows < 128 || rows > 65536 || (rows & (rows - 1))))) return KVO_EINVAL;
+  for (int64_t n : ctx->length)
+    if (n) return KVO_EBUSY;
+  if (!ok(cudaDeviceSynchronize())) return KVO_ECUDA;
+  for (kvo::LayerView& v : ctx->views) {
+    cudaFree(v.recent);
+    v.recent = nullptr;
+    v.ring_rows = 0;
+  }
+  ctx->ring_rows = 0;
+  if (!rows) return KVO_OK;
+  for (kvo::LayerView& v : ctx->views) {
+    if (!ok(cudaMalloc(&v.recent, (size_t)rows * KVO_ROW_BYTES))) {
+      cudaGetLastError();
+      for (kvo::LayerView& w : ctx->views) {
+        cudaFree(w.recent);
+        w.recent = nullptr;
+        w.ring_rows = 0;
+      }
+      return KVO_ENOMEM;
+    }
+    v.ring_rows = (uint32_t)rows;
+  }
+  ctx->ring_rows = (uint32_t)rows;
+  return KVO_OK;
+}
+
+kvo_status kvo_flush_ring(kvo_ctx* ctx, int32_t layer, void* stream) {
+  if (!ctx || layer < 0 || layer >= ctx->layers) return KVO_EINVAL;
+  return ok(ring_copyback(ctx, layer, ctx->length[layer], static_cast<cudaStream_t>(stream))) ? KVO_OK
+                                                                                                : KVO_ECUDA;
+}
+
+kvo_status kvo_ram_length(kvo_ctx* ctx, int32_t layer, int64_t* out) {
+  if (!ctx || !out || layer < 0 || layer >= ctx->layers) return KVO_EINVAL;
+  *out = ctx->ram_len[layer];
+  return KVO_OK;
+}
+
+kvo_status kvo_debug_read_history(kvo_ctx* ctx, int32_t layer, int64_t start, int64_t count, void* out) {
+  if (!ctx || !out || layer < 0 || layer >= ctx->layers || start < 0 || count < 0 ||
+      start + count > ctx->history_cap)
+    return KVO_EINVAL;
+  if (!ok(cudaDeviceSynchronize())) return KVO_ECUDA;
+  std::memcpy(out, ctx->hist_host[layer] + (size_t)start * KVO_ROW_BYTES, (size_t)count * KVO_ROW_BYTES);
+  return KVO_OK;
 }
 
 kvo_status kvo_set_policy(kvo_ctx* ctx, int32_t policy) {
@@ -280,6 +404,7 @@ kvo_status kvo_resolve_gather(kvo_ctx* ctx, int32_t layer, const int32_t* idx, i
   if ((out_rows && !aligned16(out_rows)) || (out_bf16 && !aligned16(out_bf16))) return KVO_EINVAL;
   kvo::LayerView v = ctx->views[layer];
   v.evlog = ctx->evlog ? ctx->evlog + kEvlogStride * layer : nullptr;
+  v.ram_len = (uint32_t)ctx->ram_len[layer];
   const cudaError_t e =
       kvo::launch_resolve(v, idx, (uint32_t)k, static_cast<uint8_t*>(out_rows), out_bf16, ctx->status,
                           ctx->max_cluster, static_cast<cudaStream_t>(stream));
@@ -295,6 +420,7 @@ kvo_status kvo_resolve_gather_multi(kvo_ctx* ctx, int32_t layer, const int32_t* 
   if ((out_rows && !aligned16(out_rows)) || (out_bf16 && !aligned16(out_bf16))) return KVO_EINVAL;
   kvo::LayerView v = ctx->views[layer];
   v.evlog = ctx->evlog ? ctx->evlog + kEvlogStride * layer : nullptr;
+  v.ram_len = (uint32_t)ctx->ram_len[layer];
   const cudaError_t e =
       kvo::launch_resolve(v, idx, (uint32_t)(nq * k), static_cast<uint8_t*>(out_rows), out_bf16, ctx->status,
                           ctx->max_cluster, static_cast<cudaStream_t>(stream));
@@ -311,17 +437,21 @@ kvo_status kvo_decode_step(kvo_ctx* ctx, int32_t layer, const void* new_rows, in
     return KVO_EINVAL;
   if ((out_rows && !aligned16(out_rows)) || (out_bf16 && !aligned16(out_bf16))) return KVO_EINVAL;
   if (r > 0 && (!new_rows || !aligned16(new_rows) || !is_device_pointer(new_rows))) return KVO_EINVAL;
+  if (ctx->ring_rows && r > (int64_t)ctx->ring_rows - KVO_COPYBACK_BATCH) return KVO_EINVAL;
   const int64_t start = ctx->length[layer];
   if (start + r > ctx->history_cap) return KVO_EINVAL;
   kvo::LayerView v = ctx->views[layer];
   v.evlog = ctx->evlog ? ctx->evlog + kEvlogStride * layer : nullptr;
+  v.ram_len = (uint32_t)ctx->ram_len[layer];
   const cudaError_t e = kvo::launch_decode_step(v, r ? new_rows : nullptr, (uint32_t)r, (uint32_t)start, scores,
                                                 (uint32_t)n, (uint32_t)k, idx, static_cast<uint8_t*>(out_rows),
                                                 out_bf16, ctx->status, ctx->max_cluster,
                                                 static_cast<cudaStream_t>(stream));
   if (!ok(e)) return KVO_ECUDA;
+  ctx->resolved = true;
   ctx->length[layer] = start + r;
-  return KVO_OK;
+  if (!ctx->ring_rows) ctx->ram_len[layer] = start + r;
+  return ok(ring_after_append(ctx, layer, static_cast<cudaStream_t>(stream))) ? KVO_OK : KVO_ECUDA;
 }
 
 kvo_status kvo_sync(kvo_ctx* ctx, void* stream) {

@@ -27,6 +27,9 @@ struct LayerView {
   uint32_t history_cap;
   uint32_t ring_cap;              // entries per queue buffer, a power of two >= 8 * hot_rows
   uint32_t policy;                // KVO_POLICY_LRU or KVO_POLICY_CIRCULAR
+  uint8_t* recent;                // NULL, or the recent ring: [ring_rows * 656] in HBM
+  uint32_t ring_rows;             // 0, or a power of two: position p waits in slot p mod ring_rows
+  uint32_t ram_len;               // per launch: positions below it are in the host history
 };
 
 struct ClusterShape {
@@ -45,6 +48,8 @@ cudaError_t launch_decode_step(const LayerView& L, const void* new_rows, uint32_
                                uint16_t* out_bf16, uint32_t* status, int max_cluster, cudaStream_t stream);
 cudaError_t launch_append(const void* src_dev, uint8_t* hist_dev_dst, uint64_t bytes,
                           uint32_t* counters, uint32_t new_len, cudaStream_t stream);
+cudaError_t launch_ring_append(const void* src_dev, uint8_t* ring, uint32_t r, uint32_t start, uint32_t ring_mask,
+                               uint32_t* counters, uint32_t new_len, cudaStream_t stream);
 cudaError_t launch_probe(const void* src, uint64_t bytes, void* sink, cudaStream_t stream);
 
 // Largest cluster size (16 non-portable, else 8, 4, 2) that can run with the

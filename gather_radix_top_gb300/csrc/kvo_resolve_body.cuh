@@ -88,12 +88,21 @@ struct ResolveArgs {
   uint32_t fresh_from;
 };
 
-// The row of a missing position: host history, or, for rows appended in the
-// same fused launch, their device copy (same bytes, no host round trip).
+// The row of a missing position: for rows appended in the same fused launch
+// their device copy; for rows still waiting in the recent ring (at or above
+// the host history's length) the ring; else the host history.
 __device__ __forceinline__ const uint4* miss_row(const ResolveArgs& a, const uint4* hist4, int32_t p) {
   if (a.fresh && (uint32_t)p >= a.fresh_from)
     return reinterpret_cast<const uint4*>(a.fresh) + (size_t)((uint32_t)p - a.fresh_from) * kRowVec;
+  if (a.L.ring_rows && (uint32_t)p >= a.L.ram_len)
+    return reinterpret_cast<const uint4*>(a.L.recent) + (size_t)((uint32_t)p & (a.L.ring_rows - 1u)) * kRowVec;
   return hist4 + (size_t)p * kRowVec;
+}
+
+// Whether a missing position is read from the host history.
+__device__ __forceinline__ bool miss_from_host(const ResolveArgs& a, int32_t p) {
+  if (a.fresh && (uint32_t)p >= a.fresh_from) return false;
+  return !(a.L.ring_rows && (uint32_t)p >= a.L.ram_len);
 }
 
 struct SmemLayout {
@@ -240,7 +249,7 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
   __shared__ uint32_t head_hit;                    // CTA 0: offset of the first current entry left
   __shared__ uint32_t last_vic;                    // CTA 0: the last victim (circular policy)
   __shared__ uint32_t nevict_cta;
-  __shared__ uint32_t cta_hits, cta_inv;
+  __shared__ uint32_t cta_hits, cta_inv, cta_host;
   __shared__ __align__(8) uint64_t wbar;           // CTA 0: completion of the window copy
 
   const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -320,7 +329,7 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
   cluster_arrive();
 
   // ---------------------------------------------------------------- P1
-  uint32_t nhit = 0, nmiss = 0, ninv = 0, unordered = 0;   // per thread
+  uint32_t nhit = 0, nmiss = 0, nhost = 0, ninv = 0, unordered = 0;   // per thread
   for (uint32_t jj = tid; jj < jcnt; jj += kThreads) {
     const uint32_t j = jlo + jj;
     // fused calls take the selection from shared memory, already ascending
@@ -345,6 +354,7 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
         slot = kSlotMiss;
         atomicMin(&L.pos2slot[p], (int32_t)j - (int32_t)k - 1);
         ++nmiss;
+        nhost += miss_from_host(a, p);
       }
     }
     meta_slot[jj] = slot;
@@ -362,10 +372,14 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
     if (f) mlist[cta_miss + rank] = jj;
     cta_miss += tile;
   }
-  uint32_t cta_unordered, cta_hit_inv;
-  block_sum2(unordered, nhit | (ninv << 16), scratch[1], &cta_unordered, &cta_hit_inv);
+  uint32_t cta_hit_inv;
+  // per-thread counts are at most the CTA's entries (< 2^16): two per word
+  uint32_t cta_unord_host;
+  block_sum2(unordered | (nhost << 16), nhit | (ninv << 16), scratch[1], &cta_unord_host, &cta_hit_inv);
+  const uint32_t cta_unordered = cta_unord_host & 0xffffu;
   if (tid == 0) {
     cta_hits = cta_hit_inv & 0xffffu;
+    cta_host = cta_unord_host >> 16;
     cta_inv = cta_hit_inv >> 16;
   }
   cluster_wait();                                   // B0
@@ -634,7 +648,7 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
     if (cta_hits) atomicAdd(st + 1, (unsigned long long)cta_hits);
     if (cta_miss) {
       atomicAdd(st + 2, (unsigned long long)cta_miss);
-      atomicAdd(st + 6, (unsigned long long)cta_miss * KVO_ROW_BYTES);
+      if (cta_host) atomicAdd(st + 6, (unsigned long long)cta_host * KVO_ROW_BYTES);
     }
     if (nevict_cta) atomicAdd(st + 4, (unsigned long long)nevict_cta);
     if (cta_inv) {

@@ -28,7 +28,8 @@ struct StepArgs {
   uint32_t n;
   int32_t* idx;               // the selection, also returned to the caller
   const uint4* new_rows;      // r rows appended in this step (device memory)
-  uint4* hist_dst;            // device address of history row `old length`
+  uint4* hist_dst;            // device address of history row `old length` (no recent ring)
+  uint32_t old_len;
   uint32_t r;
   uint32_t topk_bytes;        // dynamic shared memory used by the top-K phase
 };
@@ -41,10 +42,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const StepArgs
   const uint32_t rank = cluster_rank(), C = cluster_size();
   constexpr uint32_t kVec = KVO_ROW_BYTES / 16;
 
-  // append: one warp per new row, spread over the cluster
+  // append: one warp per new row, spread over the cluster; to the recent
+  // ring when there is one, else to the host history
+  const LayerView& L = s.R.L;
   for (uint32_t i = rank * kWarps + warp; i < s.r; i += C * kWarps) {
-    s.hist_dst[(size_t)i * kVec + lane] = s.new_rows[(size_t)i * kVec + lane];
-    if (lane < kVec - 32) s.hist_dst[(size_t)i * kVec + 32 + lane] = s.new_rows[(size_t)i * kVec + 32 + lane];
+    uint4* dst = L.ring_rows ? reinterpret_cast<uint4*>(L.recent) + (size_t)((s.old_len + i) & (L.ring_rows - 1u)) * kVec
+                             : s.hist_dst + (size_t)i * kVec;
+    dst[lane] = s.new_rows[(size_t)i * kVec + lane];
+    if (lane < kVec - 32) dst[32 + lane] = s.new_rows[(size_t)i * kVec + 32 + lane];
   }
 
   uint8_t* rdyn = dyn_smem + s.topk_bytes;
@@ -111,6 +116,7 @@ cudaError_t launch_decode_step(const LayerView& L, const void* new_rows, uint32_
   s.idx = idx;
   s.new_rows = static_cast<const uint4*>(new_rows);
   s.hist_dst = reinterpret_cast<uint4*>(const_cast<uint8_t*>(L.hist) + (size_t)old_len * KVO_ROW_BYTES);
+  s.old_len = old_len;
   s.r = r;
   const SmemLayout lay = smem_layout(k, a.kchunk, a.hchunk, L.hot_rows);
   const size_t topk_res = ((size_t)topk_chunk(n, C) * 4u + 15u) & ~(size_t)15u;

@@ -17,6 +17,7 @@ DEQUANT_VALUES = 576
 MAX_K = 4096
 MAX_ROUND = 8192
 POLICY_LRU, POLICY_CIRCULAR = 0, 1
+COPYBACK_BATCH = 64
 MAX_HOT_ROWS = 131072
 NOALLOC_MAX_PAIRS = 65536
 
@@ -28,7 +29,8 @@ EXPORTED = [
     "kvo_select_topk_batch",
     "kvo_resolve_gather", "kvo_resolve_gather_multi", "kvo_decode_step", "kvo_sync", "kvo_get_stats", "kvo_history_length",
     "kvo_debug_dump_layer", "kvo_debug_record_evictions", "kvo_debug_evictions", "kvo_set_policy",
-    "kvo_debug_layer_counters",
+    "kvo_debug_layer_counters", "kvo_set_recent_ring", "kvo_flush_ring", "kvo_ram_length",
+    "kvo_debug_read_history",
     "kvo_probe_host_read",
     "kvo_tier_blocks", "kvo_pool_create", "kvo_pool_destroy", "kvo_pool_alloc", "kvo_pool_write",
     "kvo_pool_read", "kvo_pool_fill", "kvo_store_blocks", "kvo_pool_release", "kvo_restore_blocks",
@@ -94,6 +96,10 @@ def lib() -> ctypes.CDLL:
         "kvo_debug_evictions": (ctypes.c_int, [_vp, _i32, _vp, _i32, ctypes.POINTER(_i32)]),
         "kvo_probe_host_read": (ctypes.c_int, [_vp, _i64, _vp, _vp]),
         "kvo_set_policy": (ctypes.c_int, [_vp, _i32]),
+        "kvo_set_recent_ring": (ctypes.c_int, [_vp, _i32]),
+        "kvo_flush_ring": (ctypes.c_int, [_vp, _i32, _vp]),
+        "kvo_ram_length": (ctypes.c_int, [_vp, _i32, ctypes.POINTER(_i64)]),
+        "kvo_debug_read_history": (ctypes.c_int, [_vp, _i32, _i64, _i64, _vp]),
         "kvo_debug_layer_counters": (ctypes.c_int, [_vp, _i32, _vp]),
         "kvo_tier_blocks": (_i64, [_i64, _i64]),
         "kvo_pool_create": (ctypes.c_int, [_i32, _i64, _i32, _i32, _i64, ctypes.POINTER(_vp)]),
@@ -278,6 +284,29 @@ def kvo_set_policy(ctx: int, policy: int) -> None:
     _check(lib().kvo_set_policy(ctx, policy), "kvo_set_policy")
 
 
+def kvo_set_recent_ring(ctx: int, rows: int) -> None:
+    """0 (no ring) or a power of two in [128, 65536]; before the first append."""
+    _check(lib().kvo_set_recent_ring(ctx, rows), "kvo_set_recent_ring")
+
+
+def kvo_flush_ring(ctx: int, layer: int, stream=None) -> None:
+    _check(lib().kvo_flush_ring(ctx, layer, _stream_ptr(stream)), "kvo_flush_ring")
+
+
+def kvo_ram_length(ctx: int, layer: int) -> int:
+    n = _i64()
+    _check(lib().kvo_ram_length(ctx, layer, ctypes.byref(n)), "kvo_ram_length")
+    return n.value
+
+
+def kvo_debug_read_history(ctx: int, layer: int, start: int, count: int):
+    import numpy as np
+    out = np.empty((count, ROW_BYTES), np.uint8)
+    _check(lib().kvo_debug_read_history(ctx, layer, start, count, ctypes.c_void_p(out.ctypes.data)),
+           "kvo_debug_read_history")
+    return out
+
+
 def kvo_debug_layer_counters(ctx: int, layer: int) -> dict:
     import numpy as np
     c = np.zeros(8, np.uint32)
@@ -362,6 +391,18 @@ class Context:
 
     def set_policy(self, policy):
         kvo_set_policy(self.handle, policy)
+
+    def set_recent_ring(self, rows):
+        kvo_set_recent_ring(self.handle, rows)
+
+    def flush_ring(self, layer, stream=None):
+        kvo_flush_ring(self.handle, layer, stream)
+
+    def ram_length(self, layer) -> int:
+        return kvo_ram_length(self.handle, layer)
+
+    def read_history(self, layer, start, count):
+        return kvo_debug_read_history(self.handle, layer, start, count)
 
     def counters(self, layer) -> dict:
         return kvo_debug_layer_counters(self.handle, layer)

@@ -46,6 +46,7 @@ extern "C" {
 #define KVO_DEQUANT_VALUES 576      /* bf16 values per dequantised row */
 #define KVO_MAX_K 4096              /* largest selection size per call */
 #define KVO_MAX_ROUND 8192          /* most entries in one multi-query round */
+#define KVO_COPYBACK_BATCH 64       /* rows per recent-ring copyback */
 #define KVO_MAX_HOT_ROWS 131072     /* largest hot cache per layer */
 
 typedef enum kvo_status {
@@ -109,6 +110,40 @@ kvo_status kvo_destroy(kvo_ctx* ctx);
  */
 kvo_status kvo_append_rows(kvo_ctx* ctx, int32_t layer, const void* rows, int64_t r,
                            void* stream);
+
+/*
+ * Recent ring ([KVO] pipeline "New KV -> GPU recent ring -> batched
+ * copyback -> RAM history"; "GPU cache management has hazards too": the ring
+ * protects new tokens that have not yet reached RAM).
+ * kvo_set_recent_ring(ctx, rows) with rows a power of two in [128, 65536]
+ * gives every layer a ring of `rows` HBM rows; 0 removes it (the default:
+ * device rows go straight to the host history).  Accepted only before the
+ * first append to any layer (else KVO_EBUSY); KVO_ENOMEM if the rings cannot
+ * be allocated.  With a ring:
+ *   - rows appended from device memory (kvo_append_rows, kvo_decode_step)
+ *     wait in the ring, position p in row p mod rows; as soon as
+ *     KVO_COPYBACK_BATCH or more are pending, whole batches of them move to
+ *     the host history with one or two asynchronous copies on the call's
+ *     stream.  At most rows - KVO_COPYBACK_BATCH rows per call.
+ *   - rows appended from host memory first move every pending ring row to
+ *     the host history, then go there themselves.
+ *   - a selected position that misses the hot cache and is not yet in the
+ *     host history is read from the ring; kvo_stats.host_bytes counts only
+ *     the reads from the host history.
+ *   - kvo_decode_step reads the rows it appends from its own input rows and
+ *     moves full batches to the host history after its resolve.
+ * kvo_flush_ring moves every pending row to the host history (stream-
+ * ordered): the point up to which an export of the host history is
+ * complete.  kvo_ram_length gives the number of positions the host history
+ * holds once the work enqueued so far has run (host only).
+ */
+kvo_status kvo_set_recent_ring(kvo_ctx* ctx, int32_t rows);
+kvo_status kvo_flush_ring(kvo_ctx* ctx, int32_t layer, void* stream);
+kvo_status kvo_ram_length(kvo_ctx* ctx, int32_t layer, int64_t* out);
+
+/* Test hook: copies positions [start, start + count) of the layer's host
+ * history (RAM) to host memory `out` (synchronises the device first). */
+kvo_status kvo_debug_read_history(kvo_ctx* ctx, int32_t layer, int64_t start, int64_t count, void* out);
 
 /*
  * Replacement policies ([KVO] "GPU cache management has hazards too").  In

@@ -145,7 +145,7 @@ class LayerState:
         self.last_use = np.zeros(self.hot_rows, np.int64)
         self.step = 0
 
-    def append(self, new_rows: np.ndarray, from_device: bool = False) -> None:
+    def append(self, new_rows: np.ndarray, from_device: bool = False, copyback: bool = True) -> None:
         """Rows for history positions [length, length + r); length grows.
 
         Reading: append never touches the hot cache; an appended row becomes
@@ -160,10 +160,16 @@ class LayerState:
         self.history[self.length:self.length + r] = new_rows
         self.length += r
         if self.ring_rows and from_device:
-            pending = self.length - self.ram_len
-            self.ram_len += pending // COPYBACK_BATCH * COPYBACK_BATCH
+            if copyback:
+                self.ring_copyback()
         else:
             self.ram_len = self.length
+
+    def ring_copyback(self) -> None:
+        """Whole batches of COPYBACK_BATCH pending ring rows move to RAM."""
+        if self.ring_rows:
+            pending = self.length - self.ram_len
+            self.ram_len += pending // COPYBACK_BATCH * COPYBACK_BATCH
 
     def flush_ring(self) -> None:
         """Every pending ring row to RAM (the export consistency boundary)."""

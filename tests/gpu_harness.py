@@ -22,7 +22,7 @@ class GpuLayerRun:
     """One layer of a workload on the GPU, driven step by step."""
 
     def __init__(self, w: W.Workload, layer: int, ctx=None, ctx_layer: int = 0, want_rows=True,
-                 want_bf16=None, fused: bool = False, policy: int = 0):
+                 want_bf16=None, fused: bool = False, policy: int = 0, ring: int = 0):
         import torch
         from gather_radix_top_gb300 import kvo
         self.torch = torch
@@ -31,6 +31,8 @@ class GpuLayerRun:
         self.ctx = ctx or kvo.Context(1, w.history_cap, w.hot_rows)
         if policy:
             self.ctx.set_policy(policy)
+        if ring:
+            self.ctx.set_recent_ring(ring)
         self.cl = ctx_layer
         self.ctx.append_rows(self.cl, W.rows(w, layer, 0, w.n0))          # host rows
         extra = w.history_cap - w.n0
@@ -72,20 +74,24 @@ class GpuLayerRun:
 
 
 class OracleLayerRun:
-    def __init__(self, w: W.Workload, layer: int, want_bf16=None, policy: str = "lru"):
+    def __init__(self, w: W.Workload, layer: int, want_bf16=None, policy: str = "lru", ring: int = 0,
+                 fused: bool = False):
         self.w, self.layer = w, layer
-        self.st = O.LayerState(w.history_cap, w.hot_rows, policy=policy)
+        self.st = O.LayerState(w.history_cap, w.hot_rows, policy=policy, ring_rows=ring)
         self.st.append(W.rows(w, layer, 0, w.n0))
         self.extra = W.rows(w, layer, w.n0, w.history_cap - w.n0) if w.history_cap > w.n0 else None
         self.bf = w.bf16 if want_bf16 is None else want_bf16
         self.prev = None
         self.last = None
+        # the fused decode step copies full ring batches back after its own
+        # resolve (its appended rows are read from its input rows)
+        self.fused = fused
 
     def step(self, step: int, idx_override=None):
         w = self.w
         for a in range(w.appends_per_step):
             pos = w.n0 + step * w.appends_per_step + a
-            self.st.append(self.extra[pos - w.n0:pos - w.n0 + 1])
+            self.st.append(self.extra[pos - w.n0:pos - w.n0 + 1], from_device=True, copyback=not self.fused)
         if idx_override is None:
             s = W.apply_carry(W.base_scores(w, self.layer, step), self.prev,
                               W.carry_draw(w, self.layer, step), w.carry_boost)
@@ -93,6 +99,8 @@ class OracleLayerRun:
         else:
             idx = idx_override
         self.last = O.resolve_gather(self.st, idx, want_bf16=self.bf)
+        if self.fused:
+            self.st.ring_copyback()
         self.prev = idx
         return idx
 

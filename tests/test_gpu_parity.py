@@ -522,3 +522,81 @@ def test_circular_policy_50k_all_steps(kvo):
     compare_state(g.ctx, 0, o.st)
     assert g.ctx.counters(0)["hand"] == o.st.hand
     g.ctx.close()
+
+
+# ------------------------------------------------------- recent ring
+@pytest.mark.parametrize("fused", [False, True])
+@pytest.mark.parametrize("appends", [1, 5])
+def test_recent_ring_parity(kvo, fused, appends):
+    """Device appends wait in a 128-row ring; 64-row batches reach RAM.
+    Rows, evictions and maps equal the oracle's; RAM holds exactly the
+    oracle's first ram_len rows; host_bytes counts only RAM reads."""
+    w = W.TINY.scaled(appends_per_step=appends, steps=40)
+    g = GpuLayerRun(w, 0, want_bf16=True, fused=fused, ring=128)
+    o = OracleLayerRun(w, 0, want_bf16=True, ring=128, fused=fused)
+    g.ctx.record_evictions(True)
+    host_reads = 0
+    for step in range(w.steps):
+        np.testing.assert_array_equal(g.step(step), o.step(step))
+        np.testing.assert_array_equal(g.rows(), o.last.rows)
+        np.testing.assert_array_equal(g.bf16(), o.last.bf16)
+        assert g.ctx.evictions(0) == o.last.evictions
+        assert g.ctx.ram_length(0) == o.st.ram_len
+        host_reads += o.last.host_reads
+        if step % 8 == 7:
+            compare_state(g.ctx, 0, o.st)
+            ram = o.st.ram_len
+            np.testing.assert_array_equal(g.ctx.read_history(0, 0, ram), o.st.history[:ram])
+    assert g.ctx.stats(0)["host_bytes"] == host_reads * O.ROW_BYTES
+    assert host_reads < g.ctx.stats(0)["misses"]     # recent rows came from the ring
+    g.ctx.flush_ring(0)
+    n = o.st.length
+    assert g.ctx.ram_length(0) == n
+    np.testing.assert_array_equal(g.ctx.read_history(0, 0, n), o.st.history[:n])
+    assert g.ctx.sync() == 0
+    g.ctx.close()
+
+
+def test_recent_ring_host_rows_flush_first(kvo):
+    import torch
+    ctx = kvo.Context(1, 2000, 64)
+    ctx.set_recent_ring(128)
+    st = O.LayerState(2000, 64, ring_rows=128)
+    rng = np.random.default_rng(3)
+    base = rng.integers(0, 256, size=(500, O.ROW_BYTES), dtype=np.uint8)
+    ctx.append_rows(0, base)
+    st.append(base)
+    for chunk in (10, 30, 50, 7):                       # device rows
+        rows = rng.integers(0, 256, size=(chunk, O.ROW_BYTES), dtype=np.uint8)
+        ctx.append_rows(0, torch.from_numpy(rows).cuda())
+        st.append(rows, from_device=True)
+        assert ctx.ram_length(0) == st.ram_len
+    host = rng.integers(0, 256, size=(5, O.ROW_BYTES), dtype=np.uint8)
+    ctx.append_rows(0, host)                            # host rows: the ring goes first
+    st.append(host)
+    assert ctx.ram_length(0) == st.ram_len == st.length
+    np.testing.assert_array_equal(ctx.read_history(0, 0, st.length), st.history[:st.length])
+    idx = torch.arange(st.length - 64, st.length, dtype=torch.int32, device="cuda")
+    out = torch.empty((64, O.ROW_BYTES), dtype=torch.uint8, device="cuda")
+    ctx.resolve_gather(0, idx, out)
+    np.testing.assert_array_equal(out.cpu().numpy(), st.history[st.length - 64:st.length])
+    with pytest.raises(kvo.KvoError):                   # more than ring - batch rows in one call
+        ctx.append_rows(0, torch.zeros((65, O.ROW_BYTES), dtype=torch.uint8, device="cuda"))
+    with pytest.raises(kvo.KvoError):                   # the ring is fixed once rows exist
+        ctx.set_recent_ring(256)
+    assert ctx.sync() == 0
+    ctx.close()
+
+
+def test_recent_ring_50k_fused(kvo):
+    """The benchmark's fused path with a 1,024-row ring, 300 steps."""
+    w = W.K50.scaled(steps=300)
+    g = GpuLayerRun(w, 0, fused=True, ring=1024)
+    o = OracleLayerRun(w, 0, ring=1024, fused=True)
+    for step in range(w.steps):
+        np.testing.assert_array_equal(g.step(step), o.step(step))
+        assert g.ctx.ram_length(0) == o.st.ram_len
+        if step % 50 == 0 or step == w.steps - 1:
+            np.testing.assert_array_equal(g.rows(), o.last.rows)
+    compare_state(g.ctx, 0, o.st)
+    g.ctx.close()

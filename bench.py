@@ -157,7 +157,8 @@ class GpuWorkload:
     """Device-resident inputs and a context for one replica of a workload."""
 
     def __init__(self, w: W.Workload, layer_base: int, steps: int, host_inputs: bool = False,
-                 fused: bool = True, policy: str = "lru", ring: int = 0):
+                 fused: bool = True, policy: str = "lru", ring: int = 0, gather: str = "loads",
+                 auto_miss_pct: int = 10):
         import torch
         from gather_radix_top_gb300 import kvo
         self.torch, self.kvo, self.w = torch, kvo, w
@@ -168,6 +169,8 @@ class GpuWorkload:
             self.ctx.set_policy(kvo.POLICY_CIRCULAR)
         if ring:
             self.ctx.set_recent_ring(ring)
+        if gather != "loads":
+            self.ctx.set_gather_mode({"staged": kvo.GATHER_STAGED, "auto": kvo.GATHER_AUTO}[gather], auto_miss_pct)
         self.sel = w.selecting_layers()
         for l in range(w.layers):
             self.ctx.append_rows(l, W.rows(w, layer_base + l, 0, w.n0))
@@ -339,7 +342,7 @@ def run_gpu_arm(args, w, rank, world):
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
     steps = args.warmup + args.steps
     wl = GpuWorkload(w, layer_base=rank * w.layers, steps=steps, fused=not args.separate, policy=args.policy,
-                     ring=args.ring)
+                     ring=args.ring, gather=args.gather, auto_miss_pct=args.auto_miss_pct)
     flush = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
     dist = world > 1
     if dist:
@@ -397,7 +400,7 @@ def run_e2e(args, w):
     import torch
     steps = args.warmup + args.steps
     wl = GpuWorkload(w, layer_base=0, steps=steps, host_inputs=True, fused=not args.separate, policy=args.policy,
-                     ring=args.ring)
+                     ring=args.ring, gather=args.gather, auto_miss_pct=args.auto_miss_pct)
     flush = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
     evs = []
     for s in range(steps):
@@ -775,6 +778,62 @@ def probe_main(args, rank, world):
     print(json.dumps(line))
 
 
+# ------------------------------------------------------- miss-rate sweep
+SWEEP_PCTS = [0, 1, 5, 10, 25, 50, 75, 100]
+
+
+def sweep_main(args):
+    """Resolve time per 2,048-row call against the miss rate, for both
+    gather modes (register loads and TMA-staged), on a full 32,768-row hot
+    cache: every round keeps k - m positions of the previous round (hits)
+    and adds m never-seen ones (misses, read from host memory)."""
+    import torch
+    from gather_radix_top_gb300 import build, kvo
+    build.build()
+    rounds = args.steps or 32
+    rows = []
+    for pct in SWEEP_PCTS:
+        m = 2048 * pct // 100
+        w = W.PROBE.scaled(name="miss_rate_sweep", n0=32_768 + max(m, 1) * (rounds + args.warmup + 1),
+                           extra={"warm_rounds": 16, "fresh": m})
+        steps = 16 + args.warmup + rounds
+        idxs = torch.from_numpy(probe_rounds(w, steps)).cuda()
+        hist = W.rows(w, 0, 0, w.n0)
+        res = {"miss_pct": pct, "misses_per_call": m}
+        for mode, code in (("loads", kvo.GATHER_LOADS), ("staged", kvo.GATHER_STAGED)):
+            ctx = kvo.Context(1, w.n0, w.hot_rows)
+            ctx.set_gather_mode(code, 0)
+            ctx.append_rows(0, hist)
+            out = torch.empty((w.k, ROW), dtype=torch.uint8, device="cuda")
+            flush = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
+            ms = []
+            for s in range(steps):
+                flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                ctx.resolve_gather(0, idxs[s], out)
+                b.record()
+                if s >= 16 + args.warmup:
+                    ms.append((a, b))
+            torch.cuda.synchronize()
+            t = [x.elapsed_time(y) * 1e3 for x, y in ms]
+            assert ctx.sync() == 0
+            res[mode + "_us_p50"] = round(float(np.percentile(t, 50)), 2)
+            ctx.close()
+            del flush
+        res["faster"] = "staged" if res["staged_us_p50"] < res["loads_us_p50"] else "loads"
+        rows.append(res)
+    staged_up_to = max([r["miss_pct"] for r in rows if r["faster"] == "staged"], default=None)
+    best = min(min(r["loads_us_p50"], r["staged_us_p50"]) for r in rows)
+    line = {"metric": METRIC, "value": round(2048 / (best * 1e-6), 1), "unit": "rows/s", "n_gpus": 1,
+            "steps": rounds, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+            "config": {"workload": "miss_rate_sweep", "hot_rows": 32_768, "k": 2048,
+                       "calls": "kvo_resolve_gather", "l2": "flushed between calls"},
+            "sweep": rows, "staged_faster_up_to_miss_pct": staged_up_to}
+    print(json.dumps(line))
+
+
 # -------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -782,17 +841,23 @@ def main():
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["kvo", "reference"], default="kvo")
-    ap.add_argument("--workload", choices=sorted(W.WORKLOADS) + [W.SESSIONS.name], default="50k_single_layer")
+    ap.add_argument("--workload", choices=sorted(W.WORKLOADS) + [W.SESSIONS.name, "miss_rate_sweep"],
+                    default="50k_single_layer")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--policy", choices=["lru", "circular"], default="lru", help="hot-cache replacement policy")
     ap.add_argument("--ring", type=int, default=0, help="recent-ring rows per layer (0: appends go straight to RAM)")
+    ap.add_argument("--gather", choices=["loads", "staged", "auto"], default="loads", help="row gather mode")
+    ap.add_argument("--auto-miss-pct", type=int, default=10, help="--gather auto: staged up to this miss share")
     ap.add_argument("--sessions", type=int, default=None, help="session_evict_restore: number of sessions")
     ap.add_argument("--session-tokens", type=int, default=None, help="session_evict_restore: tokens per session")
     ap.add_argument("--separate", action="store_true",
                     help="time kvo_append_rows + kvo_select_topk + kvo_resolve_gather instead of kvo_decode_step")
     args = ap.parse_args()
 
+    if args.workload == "miss_rate_sweep":
+        sweep_main(args)
+        return
     if args.workload == W.PROBE.name:
         probe_main(args, int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")))
         return
@@ -810,7 +875,8 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     config = {"workload": w.name, "layers": w.layers, "history": w.n0, "hot_rows": w.hot_rows, "k": w.k,
               "appends_per_step": w.appends_per_step, "select_every": w.select_every,
-              "bf16_output": w.bf16, "queries": w.queries, "policy": args.policy, "recent_ring": args.ring, "parallelism": f"replicas{world}",
+              "bf16_output": w.bf16, "queries": w.queries, "policy": args.policy, "recent_ring": args.ring,
+              "gather": args.gather if args.gather != "auto" else f"auto<={args.auto_miss_pct}%", "parallelism": f"replicas{world}",
               "calls": ("kvo_append_rows+kvo_select_topk_batch(%d rows)+kvo_resolve_gather_multi" % w.queries if w.queries > 1
                         else "kvo_append_rows+kvo_select_topk+kvo_resolve_gather" if args.separate
                         else "kvo_decode_step"),

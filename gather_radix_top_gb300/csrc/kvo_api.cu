@@ -372,6 +372,16 @@ kvo_status kvo_debug_read_history(kvo_ctx* ctx, int32_t layer, int64_t start, in
   return KVO_OK;
 }
 
+kvo_status kvo_set_gather_mode(kvo_ctx* ctx, int32_t mode, int32_t auto_miss_pct) {
+  if (!ctx || mode < KVO_GATHER_LOADS || mode > KVO_GATHER_AUTO || auto_miss_pct < 0 || auto_miss_pct > 100)
+    return KVO_EINVAL;
+  for (kvo::LayerView& v : ctx->views) {
+    v.gather_mode = (uint32_t)mode;
+    v.auto_miss_pct = (uint32_t)auto_miss_pct;
+  }
+  return KVO_OK;
+}
+
 kvo_status kvo_set_policy(kvo_ctx* ctx, int32_t policy) {
   if (!ctx || (policy != KVO_POLICY_LRU && policy != KVO_POLICY_CIRCULAR)) return KVO_EINVAL;
   if (ctx->resolved) return KVO_EBUSY;

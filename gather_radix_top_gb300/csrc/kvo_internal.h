@@ -30,6 +30,8 @@ struct LayerView {
   uint8_t* recent;                // NULL, or the recent ring: [ring_rows * 656] in HBM
   uint32_t ring_rows;             // 0, or a power of two: position p waits in slot p mod ring_rows
   uint32_t ram_len;               // per launch: positions below it are in the host history
+  uint32_t gather_mode;           // KVO_GATHER_LOADS, KVO_GATHER_STAGED or KVO_GATHER_AUTO
+  uint32_t auto_miss_pct;         // KVO_GATHER_AUTO: staged when a CTA's misses are at most this share
 };
 
 struct ClusterShape {

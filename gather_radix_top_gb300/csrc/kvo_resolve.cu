@@ -54,7 +54,13 @@ cudaError_t launch_resolve(const LayerView& L, const int32_t* idx, uint32_t k, u
   a.len = 0;
   a.fresh = nullptr;
   a.fresh_from = 0;
-  const SmemLayout lay = smem_layout(k, a.kchunk, a.hchunk, L.hot_rows);
+  a.stage_rows = L.gather_mode != KVO_GATHER_LOADS ? (a.kchunk < kStageMax ? a.kchunk : kStageMax) : 0u;
+  a.stage_max_miss_pct = L.gather_mode == KVO_GATHER_STAGED ? 100u : L.auto_miss_pct;
+  SmemLayout lay = smem_layout(k, a.kchunk, a.hchunk, L.hot_rows, a.stage_rows);
+  if (a.stage_rows && lay.total > kResolveMaxDynSmem) {
+    a.stage_rows = 0;
+    lay = smem_layout(k, a.kchunk, a.hchunk, L.hot_rows, 0);
+  }
   if (lay.total > kResolveMaxDynSmem) return cudaErrorInvalidValue;
 
   cudaLaunchConfig_t lc = {};

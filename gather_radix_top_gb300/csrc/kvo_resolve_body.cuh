@@ -69,6 +69,7 @@ constexpr uint32_t kRowsInFlight = 4;               // rows a warp loads before 
 constexpr uint32_t kNoRank = 0xffffffffu;
 constexpr uint32_t kWindow = 4 * kThreads;          // LRU queue entries CTA 0 examines per round
 constexpr uint32_t kWindowPolls = 1u << 18;         // bound on the wait for the window copy (~20 ms)
+constexpr uint32_t kStageMax = 160;                 // rows one CTA stages at most (105 KB of shared memory)
 
 struct ResolveArgs {
   LayerView L;
@@ -79,6 +80,12 @@ struct ResolveArgs {
   uint32_t k;
   uint32_t kchunk;        // selection entries per CTA (CTAs 1..C-1; CTA 0 has none)
   uint32_t hchunk;        // hot slots per CTA, a multiple of 128
+  // Staged gather (rows pulled into shared memory by TMA bulk copies, the
+  // CTA's output slice written back with one bulk store) when the CTA's
+  // entries fit `stage_rows` rows and its share of misses is at most
+  // stage_max_miss_pct percent; else rows pass through registers.
+  uint32_t stage_rows;
+  uint32_t stage_max_miss_pct;
   // fused decode step only: the selection is in shared memory, the history
   // length is `len`, and positions >= fresh_from were appended by this very
   // launch and are read from `fresh` (device memory) rather than host memory
@@ -112,7 +119,8 @@ struct SmemLayout {
 __host__ __device__ inline uint32_t round16(uint32_t x) { return (x + 15u) & ~15u; }
 
 // hchunk: slots per CTA, a multiple of 128 (whole 16-byte pieces of bitmap).
-__host__ __device__ inline SmemLayout smem_layout(uint32_t k, uint32_t kchunk, uint32_t hchunk, uint32_t hot_rows) {
+__host__ __device__ inline SmemLayout smem_layout(uint32_t k, uint32_t kchunk, uint32_t hchunk, uint32_t hot_rows,
+                                                  uint32_t stage_rows = 0) {
   (void)k;
   SmemLayout s;
   uint32_t o = 0;
@@ -124,7 +132,10 @@ __host__ __device__ inline SmemLayout smem_layout(uint32_t k, uint32_t kchunk, u
   s.vslot = o;     o += kchunk * 4u;            // per unique miss (local rank): its victim slot
   s.mlist = o;     o += kchunk * 4u;            // per unique miss (local rank): its entry
   o = round16(o);
-  s.window = o;    o += kWindow * 8u;           // CTA 0: the first queue entries, copied early
+  s.window = o;                                 // CTA 0: the first queue entries, copied early;
+  o += kWindow * 8u > stage_rows * (uint32_t)KVO_ROW_BYTES     // other CTAs: their staged rows
+           ? kWindow * 8u
+           : stage_rows * (uint32_t)KVO_ROW_BYTES;
   s.fullpin = o;   o += round16((hot_rows + 31u) / 32u * 4u);   // CTA 0: every slot hit in this call
   s.total = round16(o);
   return s;
@@ -251,6 +262,7 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
   __shared__ uint32_t nevict_cta;
   __shared__ uint32_t cta_hits, cta_inv, cta_host;
   __shared__ __align__(8) uint64_t wbar;           // CTA 0: completion of the window copy
+  __shared__ __align__(8) uint64_t gbar;           // other CTAs: completion of the staged rows
 
   const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t r = cluster_rank(), C = cluster_size();
@@ -258,7 +270,7 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
   const uint32_t k = a.k;
   const uint32_t H = L.hot_rows;
 
-  const SmemLayout lay = smem_layout(k, a.kchunk, a.hchunk, H);
+  const SmemLayout lay = smem_layout(k, a.kchunk, a.hchunk, H, a.stage_rows);
   uint32_t* pinbits = reinterpret_cast<uint32_t*>(dyn_smem + lay.pinbits);
   int32_t* meta_slot = reinterpret_cast<int32_t*>(dyn_smem + lay.meta_slot);
   int32_t* meta_pos = reinterpret_cast<int32_t*>(dyn_smem + lay.meta_pos);
@@ -397,40 +409,81 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
   if (tid < C && own_hits[tid]) dsmem_red_add_u32(dsmem_addr(&hitcnt[tid], 0), own_hits[tid]);
   cluster_arrive();                                 // B1: stamps, claims, counts, pins
 
-  // Each warp loads up to kRowsInFlight rows before storing any, so that all
-  // of this CTA's rows are in flight at once.
   const uint4* hot4 = reinterpret_cast<const uint4*>(L.hot);
   const uint4* hist4 = reinterpret_cast<const uint4*>(L.hist);
-  for (uint32_t jj0 = warp; jj0 < jcnt; jj0 += kWarps * kRowsInFlight) {
-    uint4 va[kRowsInFlight], vb[kRowsInFlight];
-#pragma unroll
-    for (uint32_t u = 0; u < kRowsInFlight; ++u) {
-      const uint32_t jj = jj0 + u * kWarps;
-      va[u] = make_uint4(0, 0, 0, 0);
-      vb[u] = make_uint4(0, 0, 0, 0);
-      if (jj < jcnt) {
-        const int32_t slot = meta_slot[jj];
-        const uint4* src = nullptr;
-        if (slot >= 0) src = hot4 + (size_t)slot * kRowVec;
-        else if (slot == kSlotMiss) src = miss_row(a, hist4, meta_pos[jj]);
-        if (src) {
-          va[u] = src[lane];
-          if (lane < kRowVec - 32) vb[u] = src[32 + lane];
-        }
+  uint4* stage4 = reinterpret_cast<uint4*>(dyn_smem + lay.window);
+  const bool staged = a.stage_rows && jcnt && jcnt <= a.stage_rows &&
+                      cta_miss * 100u <= a.stage_max_miss_pct * jcnt;   // uniform over the CTA
+  bool gather_ok = true;
+  if (staged) {
+    // One bulk copy per row into shared memory, all in flight at once;
+    // invalid entries get a zero row.
+    if (tid == 0) {
+      mbar_init(&gbar, 1);
+      mbar_arrive_expect_tx(&gbar, (jcnt - cta_inv) * (uint32_t)KVO_ROW_BYTES);
+    }
+    __syncthreads();
+    for (uint32_t jj = tid; jj < jcnt; jj += kThreads) {
+      const int32_t slot = meta_slot[jj];
+      const uint4* src = slot >= 0 ? hot4 + (size_t)slot * kRowVec
+                         : slot == kSlotMiss ? miss_row(a, hist4, meta_pos[jj])
+                                             : nullptr;
+      if (src) {
+        bulk_copy_g2s(stage4 + (size_t)jj * kRowVec, src, KVO_ROW_BYTES, &gbar);
+      } else {
+        for (uint32_t v = 0; v < kRowVec; ++v) stage4[(size_t)jj * kRowVec + v] = make_uint4(0, 0, 0, 0);
       }
     }
-#pragma unroll
-    for (uint32_t u = 0; u < kRowsInFlight; ++u) {
-      const uint32_t jj = jj0 + u * kWarps;
-      if (jj >= jcnt) break;
-      const uint32_t j = jlo + jj;
-      if (a.out_rows) {
-        uint4* d = reinterpret_cast<uint4*>(a.out_rows) + (size_t)j * kRowVec;
-        d[lane] = va[u];
-        if (lane < kRowVec - 32) d[32 + lane] = vb[u];
+    fence_proxy_async_smem();                       // the zero rows, before the bulk store reads them
+    gather_ok = __syncthreads_and(mbar_wait_bounded(&gbar, 0, kWindowPolls));
+    if (!gather_ok) {
+      if (tid == 0) atomicOr(a.status, kFlagTimeout);
+    } else {
+      if (a.out_rows && tid == 0) {                // this CTA's slice of the output is contiguous
+        bulk_copy_s2g(a.out_rows + (size_t)jlo * KVO_ROW_BYTES, stage4, jcnt * (uint32_t)KVO_ROW_BYTES);
+        bulk_commit();
       }
       if (a.out_bf16)
-        dequant_row(va[u], vb[u], lane, reinterpret_cast<uint4*>(a.out_bf16 + (size_t)j * KVO_DEQUANT_VALUES));
+        for (uint32_t jj = warp; jj < jcnt; jj += kWarps) {
+          const uint4 va = stage4[(size_t)jj * kRowVec + lane];
+          const uint4 vb = lane < kRowVec - 32 ? stage4[(size_t)jj * kRowVec + 32 + lane] : make_uint4(0, 0, 0, 0);
+          dequant_row(va, vb, lane, reinterpret_cast<uint4*>(a.out_bf16 + (size_t)(jlo + jj) * KVO_DEQUANT_VALUES));
+        }
+    }
+  } else {
+    // Each warp loads up to kRowsInFlight rows before storing any, so that
+    // all of this CTA's rows are in flight at once.
+    for (uint32_t jj0 = warp; jj0 < jcnt; jj0 += kWarps * kRowsInFlight) {
+      uint4 va[kRowsInFlight], vb[kRowsInFlight];
+#pragma unroll
+      for (uint32_t u = 0; u < kRowsInFlight; ++u) {
+        const uint32_t jj = jj0 + u * kWarps;
+        va[u] = make_uint4(0, 0, 0, 0);
+        vb[u] = make_uint4(0, 0, 0, 0);
+        if (jj < jcnt) {
+          const int32_t slot = meta_slot[jj];
+          const uint4* src = nullptr;
+          if (slot >= 0) src = hot4 + (size_t)slot * kRowVec;
+          else if (slot == kSlotMiss) src = miss_row(a, hist4, meta_pos[jj]);
+          if (src) {
+            va[u] = src[lane];
+            if (lane < kRowVec - 32) vb[u] = src[32 + lane];
+          }
+        }
+      }
+#pragma unroll
+      for (uint32_t u = 0; u < kRowsInFlight; ++u) {
+        const uint32_t jj = jj0 + u * kWarps;
+        if (jj >= jcnt) break;
+        const uint32_t j = jlo + jj;
+        if (a.out_rows) {
+          uint4* d = reinterpret_cast<uint4*>(a.out_rows) + (size_t)j * kRowVec;
+          d[lane] = va[u];
+          if (lane < kRowVec - 32) d[32 + lane] = vb[u];
+        }
+        if (a.out_bf16)
+          dequant_row(va[u], vb[u], lane, reinterpret_cast<uint4*>(a.out_bf16 + (size_t)j * KVO_DEQUANT_VALUES));
+      }
     }
   }
   // CTA 0 (no entries to gather): wait for the window and read its slots'
@@ -604,16 +657,27 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
       if (lane == 0) atomicOr(a.status, kFlagInternal);   // cannot happen; never write out of bounds
       continue;
     }
+    uint4* dst = reinterpret_cast<uint4*>(L.hot) + (size_t)v * kRowVec;
+    if (staged && gather_ok) {
+      // the row is still in shared memory: one bulk store into the slot
+      if (lane == 0) {
+        if (map_update(a, v, __ldcg(&L.slot2pos[v]), p, t, uniq_before + lr)) atomicAdd(&nevict_cta, 1u);
+        bulk_copy_s2g(dst, stage4 + (size_t)jj * kRowVec, KVO_ROW_BYTES);
+        bulk_commit();
+      }
+      continue;
+    }
     const uint4* src = a.out_rows ? reinterpret_cast<const uint4*>(a.out_rows) + (size_t)(jlo + jj) * kRowVec
                                   : miss_row(a, hist4, p);
     const uint4 x = __ldcg(src + lane);
     uint4 y = make_uint4(0, 0, 0, 0);
     if (lane < kRowVec - 32) y = __ldcg(src + 32 + lane);
     if (lane == 0 && map_update(a, v, __ldcg(&L.slot2pos[v]), p, t, uniq_before + lr)) atomicAdd(&nevict_cta, 1u);
-    uint4* dst = reinterpret_cast<uint4*>(L.hot) + (size_t)v * kRowVec;
     dst[lane] = x;
     if (lane < kRowVec - 32) dst[32 + lane] = y;
   }
+  if (staged) bulk_wait_all();                      // the output slice and the fills have left shared memory
+  if (staged && !gather_ok) mbar_wait_bounded(&gbar, 0, kWindowPolls);   // nothing may land after the exit
 
   // ---------------------------------------------------------------- P5
   // The used slots of this CTA's range, in slot order, stamped t, at the

@@ -53,7 +53,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const StepArgs
   }
 
   uint8_t* rdyn = dyn_smem + s.topk_bytes;
-  const SmemLayout lay = smem_layout(s.R.k, s.R.kchunk, s.R.hchunk, s.R.L.hot_rows);
+  const SmemLayout lay = smem_layout(s.R.k, s.R.kchunk, s.R.hchunk, s.R.L.hot_rows, s.R.stage_rows);
   int32_t* sel = reinterpret_cast<int32_t*>(rdyn + lay.sel);
   const uint32_t kchunk = s.R.kchunk;
   topk_body<kResident>(s.scores, s.n, s.R.k, dyn_smem, &rsm, [&](uint32_t pos, uint32_t out) {
@@ -118,8 +118,16 @@ cudaError_t launch_decode_step(const LayerView& L, const void* new_rows, uint32_
   s.hist_dst = reinterpret_cast<uint4*>(const_cast<uint8_t*>(L.hist) + (size_t)old_len * KVO_ROW_BYTES);
   s.old_len = old_len;
   s.r = r;
-  const SmemLayout lay = smem_layout(k, a.kchunk, a.hchunk, L.hot_rows);
   const size_t topk_res = ((size_t)topk_chunk(n, C) * 4u + 15u) & ~(size_t)15u;
+  // staged gather when the rows fit next to the resident keys (else next to
+  // streamed keys), else rows through registers
+  a.stage_rows = L.gather_mode != KVO_GATHER_LOADS ? (a.kchunk < kStageMax ? a.kchunk : kStageMax) : 0u;
+  a.stage_max_miss_pct = L.gather_mode == KVO_GATHER_STAGED ? 100u : L.auto_miss_pct;
+  SmemLayout lay = smem_layout(k, a.kchunk, a.hchunk, L.hot_rows, a.stage_rows);
+  if (a.stage_rows && lay.total > kStepMaxDynSmem) {
+    a.stage_rows = 0;
+    lay = smem_layout(k, a.kchunk, a.hchunk, L.hot_rows, 0);
+  }
   if (lay.total > kStepMaxDynSmem) return cudaErrorInvalidValue;
   const bool resident = topk_res + lay.total <= kStepMaxDynSmem;
   s.topk_bytes = resident ? (uint32_t)topk_res : 0u;

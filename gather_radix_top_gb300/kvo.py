@@ -18,6 +18,7 @@ MAX_K = 4096
 MAX_ROUND = 8192
 POLICY_LRU, POLICY_CIRCULAR = 0, 1
 COPYBACK_BATCH = 64
+GATHER_LOADS, GATHER_STAGED, GATHER_AUTO = 0, 1, 2
 MAX_HOT_ROWS = 131072
 NOALLOC_MAX_PAIRS = 65536
 
@@ -30,7 +31,7 @@ EXPORTED = [
     "kvo_resolve_gather", "kvo_resolve_gather_multi", "kvo_decode_step", "kvo_sync", "kvo_get_stats", "kvo_history_length",
     "kvo_debug_dump_layer", "kvo_debug_record_evictions", "kvo_debug_evictions", "kvo_set_policy",
     "kvo_debug_layer_counters", "kvo_set_recent_ring", "kvo_flush_ring", "kvo_ram_length",
-    "kvo_debug_read_history",
+    "kvo_debug_read_history", "kvo_set_gather_mode",
     "kvo_probe_host_read",
     "kvo_tier_blocks", "kvo_pool_create", "kvo_pool_destroy", "kvo_pool_alloc", "kvo_pool_write",
     "kvo_pool_read", "kvo_pool_fill", "kvo_store_blocks", "kvo_pool_release", "kvo_restore_blocks",
@@ -97,6 +98,7 @@ def lib() -> ctypes.CDLL:
         "kvo_probe_host_read": (ctypes.c_int, [_vp, _i64, _vp, _vp]),
         "kvo_set_policy": (ctypes.c_int, [_vp, _i32]),
         "kvo_set_recent_ring": (ctypes.c_int, [_vp, _i32]),
+        "kvo_set_gather_mode": (ctypes.c_int, [_vp, _i32, _i32]),
         "kvo_flush_ring": (ctypes.c_int, [_vp, _i32, _vp]),
         "kvo_ram_length": (ctypes.c_int, [_vp, _i32, ctypes.POINTER(_i64)]),
         "kvo_debug_read_history": (ctypes.c_int, [_vp, _i32, _i64, _i64, _vp]),
@@ -284,6 +286,12 @@ def kvo_set_policy(ctx: int, policy: int) -> None:
     _check(lib().kvo_set_policy(ctx, policy), "kvo_set_policy")
 
 
+def kvo_set_gather_mode(ctx: int, mode: int, auto_miss_pct: int = 0) -> None:
+    """GATHER_LOADS, GATHER_STAGED or GATHER_AUTO (staged for CTAs whose
+    misses are at most auto_miss_pct percent of their entries)."""
+    _check(lib().kvo_set_gather_mode(ctx, mode, auto_miss_pct), "kvo_set_gather_mode")
+
+
 def kvo_set_recent_ring(ctx: int, rows: int) -> None:
     """0 (no ring) or a power of two in [128, 65536]; before the first append."""
     _check(lib().kvo_set_recent_ring(ctx, rows), "kvo_set_recent_ring")
@@ -391,6 +399,9 @@ class Context:
 
     def set_policy(self, policy):
         kvo_set_policy(self.handle, policy)
+
+    def set_gather_mode(self, mode, auto_miss_pct=0):
+        kvo_set_gather_mode(self.handle, mode, auto_miss_pct)
 
     def set_recent_ring(self, rows):
         kvo_set_recent_ring(self.handle, rows)

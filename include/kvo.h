@@ -146,6 +146,23 @@ kvo_status kvo_ram_length(kvo_ctx* ctx, int32_t layer, int64_t* out);
 kvo_status kvo_debug_read_history(kvo_ctx* ctx, int32_t layer, int64_t start, int64_t count, void* out);
 
 /*
+ * Gather modes: how the selected rows reach the output (and the fills their
+ * slots).  KVO_GATHER_LOADS: 16-byte loads into registers (zero-copy loads
+ * for rows in host memory).  KVO_GATHER_STAGED: every row of a CTA's share
+ * is pulled into shared memory by a TMA bulk copy (all in flight at once,
+ * host rows included) and the share written back with one bulk store; used
+ * where a CTA's share fits its shared memory, else loads.  KVO_GATHER_AUTO:
+ * staged for a CTA whose misses are at most auto_miss_pct percent of its
+ * entries, loads otherwise (decided per CTA and call, after classification).
+ * Outputs are identical in every mode.  Default: KVO_GATHER_LOADS.  Host
+ * only; takes effect from the next call.
+ */
+#define KVO_GATHER_LOADS 0
+#define KVO_GATHER_STAGED 1
+#define KVO_GATHER_AUTO 2
+kvo_status kvo_set_gather_mode(kvo_ctx* ctx, int32_t mode, int32_t auto_miss_pct);
+
+/*
  * Replacement policies ([KVO] "GPU cache management has hazards too").  In
  * both, the slots used by a round (its hits, and the slots it fills) are
  * pinned, and the round's distinct missing positions, in first-occurrence

@@ -22,7 +22,7 @@ class GpuLayerRun:
     """One layer of a workload on the GPU, driven step by step."""
 
     def __init__(self, w: W.Workload, layer: int, ctx=None, ctx_layer: int = 0, want_rows=True,
-                 want_bf16=None, fused: bool = False, policy: int = 0, ring: int = 0):
+                 want_bf16=None, fused: bool = False, policy: int = 0, ring: int = 0, gather=None):
         import torch
         from gather_radix_top_gb300 import kvo
         self.torch = torch
@@ -33,6 +33,8 @@ class GpuLayerRun:
             self.ctx.set_policy(policy)
         if ring:
             self.ctx.set_recent_ring(ring)
+        if gather is not None:
+            self.ctx.set_gather_mode(*gather)
         self.cl = ctx_layer
         self.ctx.append_rows(self.cl, W.rows(w, layer, 0, w.n0))          # host rows
         extra = w.history_cap - w.n0

@@ -600,3 +600,69 @@ def test_recent_ring_50k_fused(kvo):
             np.testing.assert_array_equal(g.rows(), o.last.rows)
     compare_state(g.ctx, 0, o.st)
     g.ctx.close()
+
+
+# ------------------------------------------------ staged (TMA) gather
+GATHERS = [(1, 0), (2, 10)]     # staged always; staged for CTAs with at most 10 % misses
+
+
+@pytest.mark.parametrize("gather", GATHERS)
+@pytest.mark.parametrize("fused", [False, True])
+def test_staged_gather_tiny_full_parity(kvo, gather, fused):
+    w = W.TINY.scaled(appends_per_step=2)
+    g = GpuLayerRun(w, 0, want_bf16=True, fused=fused, gather=gather)
+    o = OracleLayerRun(w, 0, want_bf16=True)
+    g.ctx.record_evictions(True)
+    for step in range(w.steps):
+        np.testing.assert_array_equal(g.step(step), o.step(step))
+        np.testing.assert_array_equal(g.rows(), o.last.rows)
+        np.testing.assert_array_equal(g.bf16(), o.last.bf16)
+        assert g.ctx.evictions(0) == o.last.evictions
+        compare_state(g.ctx, 0, o.st)
+    assert g.ctx.sync() == 0
+    g.ctx.close()
+
+
+@pytest.mark.parametrize("gather", GATHERS)
+@pytest.mark.parametrize("seed,H,n,k,dup,bad", [(1, 16, 40, 16, 0.3, 2), (3, 1024, 5000, 256, 0.2, 5),
+                                               (5, 4096, 70_000, 2048, 0.4, 3), (6, 32_768, 60_000, 4096, 0.1, 1)])
+def test_staged_gather_random_selections(kvo, gather, seed, H, n, k, dup, bad):
+    """Duplicates, invalid entries (zero rows), host misses by TMA; bf16 only
+    on odd steps (the fills then come from shared memory, not the output)."""
+    import torch
+    g = np.random.default_rng(seed)
+    hist = g.integers(0, 256, size=(n, O.ROW_BYTES), dtype=np.uint8)
+    ctx = kvo.Context(1, n, H)
+    ctx.set_gather_mode(*gather)
+    ctx.append_rows(0, hist)
+    ctx.record_evictions(True)
+    st = O.LayerState(n, H)
+    st.append(hist)
+    out = torch.empty((k, O.ROW_BYTES), dtype=torch.uint8, device="cuda")
+    outb = torch.empty((k, O.DEQUANT_VALUES), dtype=torch.int16, device="cuda")
+    for step in range(10):
+        idx = W.random_idx(seed * 100 + step, n if step % 3 else min(n, 2 * H), k, dup, bad if step % 2 else 0)
+        rows_out = None if step % 2 else out
+        ctx.resolve_gather(0, torch.from_numpy(idx).cuda(), rows_out, outb)
+        res = O.resolve_gather(st, idx, want_bf16=True)
+        if rows_out is not None:
+            np.testing.assert_array_equal(out.cpu().numpy(), res.rows)
+        assert_bf16_equal(outb.cpu().numpy(), res.bf16)
+        assert ctx.evictions(0) == res.evictions
+        assert ctx.sync() == (kvo.KVO_ERANGE if res.invalid else 0)
+    compare_state(ctx, 0, st)
+    ctx.close()
+
+
+@pytest.mark.parametrize("gather", GATHERS)
+def test_staged_gather_50k_fused_with_ring(kvo, gather):
+    w = W.K50.scaled(steps=200)
+    g = GpuLayerRun(w, 0, fused=True, ring=1024, gather=gather)
+    o = OracleLayerRun(w, 0, ring=1024, fused=True)
+    for step in range(w.steps):
+        np.testing.assert_array_equal(g.step(step), o.step(step))
+        if step % 25 == 0 or step == w.steps - 1:
+            np.testing.assert_array_equal(g.rows(), o.last.rows)
+    compare_state(g.ctx, 0, o.st)
+    assert g.ctx.sync() == 0
+    g.ctx.close()

@@ -241,6 +241,8 @@ kvo_status kvo_create(int32_t layers, int64_t history_cap, int32_t hot_rows, int
     v.history_cap = (uint32_t)history_cap;
     v.counters = c->counters + 8 * l;
     v.ring_cap = ring_cap;
+    v.gather_mode = KVO_GATHER_AUTO;              // staged from 5 % misses on: the measured crossover
+    v.auto_miss_pct = 5;
     v.stats = c->stats + 8 * l;
     uint8_t* h = nullptr;
     good = ok(cudaHostAlloc((void**)&h, (size_t)history_cap * KVO_ROW_BYTES,

@@ -31,7 +31,7 @@ struct LayerView {
   uint32_t ring_rows;             // 0, or a power of two: position p waits in slot p mod ring_rows
   uint32_t ram_len;               // per launch: positions below it are in the host history
   uint32_t gather_mode;           // KVO_GATHER_LOADS, KVO_GATHER_STAGED or KVO_GATHER_AUTO
-  uint32_t auto_miss_pct;         // KVO_GATHER_AUTO: staged when a CTA's misses are at most this share
+  uint32_t auto_miss_pct;         // KVO_GATHER_AUTO: staged when a CTA's misses are at least this share
 };
 
 struct ClusterShape {

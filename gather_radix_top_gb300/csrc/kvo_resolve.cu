@@ -10,9 +10,10 @@ namespace {
 
 using namespace resolve_detail;
 
+template <bool kLru>
 __global__ void __launch_bounds__(kThreads, 1) resolve_gather_kernel(const ResolveArgs a) {
   extern __shared__ __align__(16) uint8_t dyn_smem[];
-  resolve_body(a, dyn_smem);
+  resolve_body<kLru>(a, dyn_smem);
 }
 
 struct ResolveConfig {
@@ -33,10 +34,15 @@ cudaError_t launch_resolve(const LayerView& L, const int32_t* idx, uint32_t k, u
   if (e != cudaSuccess) return e;
   ResolveConfig& cfg = g_resolve[dev & 63];
   if (!cfg.init) {
-    e = cudaFuncSetAttribute(resolve_gather_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(resolve_gather_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kResolveMaxDynSmem);
     if (e != cudaSuccess) return e;
-    cfg.cluster = best_cluster((const void*)resolve_gather_kernel, kResolveMaxDynSmem, (int)kMaxCluster);
+    e = cudaFuncSetAttribute(resolve_gather_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kResolveMaxDynSmem);
+    if (e != cudaSuccess) return e;
+    const int c1 = best_cluster((const void*)resolve_gather_kernel<true>, kResolveMaxDynSmem, (int)kMaxCluster);
+    const int c2 = best_cluster((const void*)resolve_gather_kernel<false>, kResolveMaxDynSmem, (int)kMaxCluster);
+    cfg.cluster = c1 < c2 ? c1 : c2;
     if (cfg.cluster == 0) return cudaErrorInvalidConfiguration;
     cfg.init = true;
   }
@@ -55,7 +61,7 @@ cudaError_t launch_resolve(const LayerView& L, const int32_t* idx, uint32_t k, u
   a.fresh = nullptr;
   a.fresh_from = 0;
   a.stage_rows = L.gather_mode != KVO_GATHER_LOADS ? (a.kchunk < kStageMax ? a.kchunk : kStageMax) : 0u;
-  a.stage_max_miss_pct = L.gather_mode == KVO_GATHER_STAGED ? 100u : L.auto_miss_pct;
+  a.stage_min_miss_pct = L.gather_mode == KVO_GATHER_STAGED ? 0u : L.auto_miss_pct;
   SmemLayout lay = smem_layout(k, a.kchunk, a.hchunk, L.hot_rows, a.stage_rows);
   if (a.stage_rows && lay.total > kResolveMaxDynSmem) {
     a.stage_rows = 0;
@@ -75,7 +81,8 @@ cudaError_t launch_resolve(const LayerView& L, const int32_t* idx, uint32_t k, u
   lc.stream = stream;
   lc.attrs = attr;
   lc.numAttrs = 1;
-  return cudaLaunchKernelEx(&lc, resolve_gather_kernel, a);
+  if (L.policy == KVO_POLICY_LRU) return cudaLaunchKernelEx(&lc, resolve_gather_kernel<true>, a);
+  return cudaLaunchKernelEx(&lc, resolve_gather_kernel<false>, a);
 }
 
 }  // namespace kvo

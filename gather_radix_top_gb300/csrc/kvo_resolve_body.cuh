@@ -82,10 +82,10 @@ struct ResolveArgs {
   uint32_t hchunk;        // hot slots per CTA, a multiple of 128
   // Staged gather (rows pulled into shared memory by TMA bulk copies, the
   // CTA's output slice written back with one bulk store) when the CTA's
-  // entries fit `stage_rows` rows and its share of misses is at most
-  // stage_max_miss_pct percent; else rows pass through registers.
+  // entries fit `stage_rows` rows and its share of misses is at least
+  // stage_min_miss_pct percent; else rows pass through registers.
   uint32_t stage_rows;
-  uint32_t stage_max_miss_pct;
+  uint32_t stage_min_miss_pct;
   // fused decode step only: the selection is in shared memory, the history
   // length is `len`, and positions >= fresh_from were appended by this very
   // launch and are read from `fresh` (device memory) rather than host memory
@@ -248,6 +248,9 @@ static __device__ __noinline__ uint32_t compact_queue(const LayerView& L, uint32
   return total;
 }
 
+// kLru: the layer's policy (KVO_POLICY_LRU, else KVO_POLICY_CIRCULAR); each
+// policy gets its own kernel so that neither carries the other's code.
+template <bool kLru>
 __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_smem) {
   __shared__ uint32_t scratch[2][2 * kWarps + 2];
   __shared__ uint32_t table[kMaxCluster][4];       // per CTA: (idx not increasing, misses)
@@ -285,7 +288,7 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
   const uint32_t len = a.fused ? a.len : L.counters[1];
   uint32_t head = L.counters[2], tail = L.counters[3], buf = L.counters[4] & 1u;
   const uint32_t hand = L.counters[5];
-  const bool lru = L.policy == KVO_POLICY_LRU;     // uniform: one policy per layer
+  constexpr bool lru = kLru;
   const uint32_t Q = L.ring_cap, qmask = Q - 1u;
   const uint32_t jlo = r == 0 ? 0u : min(k, (r - 1u) * a.kchunk);
   const uint32_t jcnt = r == 0 ? 0u : min(k, jlo + a.kchunk) - jlo;
@@ -413,7 +416,7 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
   const uint4* hist4 = reinterpret_cast<const uint4*>(L.hist);
   uint4* stage4 = reinterpret_cast<uint4*>(dyn_smem + lay.window);
   const bool staged = a.stage_rows && jcnt && jcnt <= a.stage_rows &&
-                      cta_miss * 100u <= a.stage_max_miss_pct * jcnt;   // uniform over the CTA
+                      cta_miss * 100u >= a.stage_min_miss_pct * jcnt;   // uniform over the CTA
   bool gather_ok = true;
   if (staged) {
     // One bulk copy per row into shared memory, all in flight at once;

@@ -34,7 +34,7 @@ struct StepArgs {
   uint32_t topk_bytes;        // dynamic shared memory used by the top-K phase
 };
 
-template <bool kResident>
+template <bool kResident, bool kLru>
 __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const StepArgs s) {
   extern __shared__ __align__(16) uint8_t dyn_smem[];
   __shared__ RadixSmem rsm;                        // the top-K phase's radix histograms
@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const StepArgs
     dsmem_st_u32(dsmem_addr(&sel[out - q * kchunk], q + 1), pos);
   });
   cluster_sync();                                  // every selected position delivered
-  resolve_body(s.R, rdyn);
+  resolve_body<kLru>(s.R, rdyn);
   if (rank == 0 && tid == 0) s.R.L.counters[1] = s.R.len;
 }
 
@@ -84,15 +84,16 @@ cudaError_t launch_decode_step(const LayerView& L, const void* new_rows, uint32_
   if (e != cudaSuccess) return e;
   StepConfig& cfg = g_step[dev & 63];
   if (!cfg.init) {
-    e = cudaFuncSetAttribute(decode_step_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kStepMaxDynSmem);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(decode_step_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kStepMaxDynSmem);
-    if (e != cudaSuccess) return e;
-    const int c1 = best_cluster((const void*)decode_step_kernel<true>, kStepMaxDynSmem, (int)kMaxCluster);
-    const int c2 = best_cluster((const void*)decode_step_kernel<false>, kStepMaxDynSmem, (int)kMaxCluster);
-    cfg.cluster = c1 < c2 ? c1 : c2;
+    const void* kernels[4] = {(const void*)decode_step_kernel<true, true>, (const void*)decode_step_kernel<false, true>,
+                              (const void*)decode_step_kernel<true, false>, (const void*)decode_step_kernel<false, false>};
+    int c1 = (int)kMaxCluster;
+    for (const void* kern : kernels) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStepMaxDynSmem);
+      if (e != cudaSuccess) return e;
+      const int c = best_cluster(kern, kStepMaxDynSmem, (int)kMaxCluster);
+      c1 = c < c1 ? c : c1;
+    }
+    cfg.cluster = c1;
     if (cfg.cluster == 0) return cudaErrorInvalidConfiguration;
     cfg.init = true;
   }
@@ -122,7 +123,7 @@ cudaError_t launch_decode_step(const LayerView& L, const void* new_rows, uint32_
   // staged gather when the rows fit next to the resident keys (else next to
   // streamed keys), else rows through registers
   a.stage_rows = L.gather_mode != KVO_GATHER_LOADS ? (a.kchunk < kStageMax ? a.kchunk : kStageMax) : 0u;
-  a.stage_max_miss_pct = L.gather_mode == KVO_GATHER_STAGED ? 100u : L.auto_miss_pct;
+  a.stage_min_miss_pct = L.gather_mode == KVO_GATHER_STAGED ? 0u : L.auto_miss_pct;
   SmemLayout lay = smem_layout(k, a.kchunk, a.hchunk, L.hot_rows, a.stage_rows);
   if (a.stage_rows && lay.total > kStepMaxDynSmem) {
     a.stage_rows = 0;
@@ -144,8 +145,11 @@ cudaError_t launch_decode_step(const LayerView& L, const void* new_rows, uint32_
   lc.stream = stream;
   lc.attrs = attr;
   lc.numAttrs = 1;
-  if (resident) return cudaLaunchKernelEx(&lc, decode_step_kernel<true>, s);
-  return cudaLaunchKernelEx(&lc, decode_step_kernel<false>, s);
+  const bool lru = L.policy == KVO_POLICY_LRU;
+  if (resident) return lru ? cudaLaunchKernelEx(&lc, decode_step_kernel<true, true>, s)
+                           : cudaLaunchKernelEx(&lc, decode_step_kernel<true, false>, s);
+  return lru ? cudaLaunchKernelEx(&lc, decode_step_kernel<false, true>, s)
+             : cudaLaunchKernelEx(&lc, decode_step_kernel<false, false>, s);
 }
 
 }  // namespace kvo

@@ -441,6 +441,45 @@ kvo_status kvo_resolve_gather_multi(kvo_ctx* ctx, int32_t layer, const int32_t* 
   return ok(e) ? KVO_OK : KVO_ECUDA;
 }
 
+kvo_status kvo_decode_layers(kvo_ctx* ctx, const kvo_layer_task* tasks, int32_t ntasks, int32_t k, void* stream) {
+  if (!ctx || !tasks || ntasks < 0 || ntasks > ctx->layers || k < 1 || k > KVO_MAX_K || k > ctx->hot_rows)
+    return KVO_EINVAL;
+  if (ntasks == 0) return KVO_OK;
+  std::vector<kvo::StepTask> st(ntasks);
+  std::vector<bool> seen(ctx->layers, false);
+  for (int32_t i = 0; i < ntasks; ++i) {
+    const kvo_layer_task& t = tasks[i];
+    if (t.layer < 0 || t.layer >= ctx->layers || seen[t.layer] || t.r < 0 || !t.idx ||
+        (!t.out_rows && !t.out_bf16) || (t.out_rows && !aligned16(t.out_rows)) ||
+        (t.out_bf16 && !aligned16(t.out_bf16)))
+      return KVO_EINVAL;
+    seen[t.layer] = true;
+    if (t.r > 0 && (!t.new_rows || !aligned16(t.new_rows) || !is_device_pointer(t.new_rows))) return KVO_EINVAL;
+    if (ctx->ring_rows && t.r > (int64_t)ctx->ring_rows - KVO_COPYBACK_BATCH) return KVO_EINVAL;
+    const int64_t start = ctx->length[t.layer];
+    if (start + t.r > ctx->history_cap) return KVO_EINVAL;
+    if (t.scores && (t.n < k || t.n > start + t.r)) return KVO_EINVAL;
+    kvo::LayerView v = ctx->views[t.layer];
+    v.evlog = ctx->evlog ? ctx->evlog + kEvlogStride * t.layer : nullptr;
+    v.ram_len = (uint32_t)ctx->ram_len[t.layer];
+    st[i] = kvo::StepTask{v, t.r ? t.new_rows : nullptr, (uint32_t)t.r, (uint32_t)start, t.scores,
+                          (uint32_t)(t.scores ? t.n : 0), t.idx, static_cast<uint8_t*>(t.out_rows), t.out_bf16};
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cudaError_t e =
+      kvo::launch_decode_layers(st.data(), (uint32_t)ntasks, (uint32_t)k, ctx->status, ctx->max_cluster, s);
+  if (e == cudaErrorInvalidValue) return KVO_EINVAL;
+  if (!ok(e)) return KVO_ECUDA;
+  ctx->resolved = true;
+  for (int32_t i = 0; i < ntasks; ++i) {
+    const int32_t l = tasks[i].layer;
+    ctx->length[l] += tasks[i].r;
+    if (!ctx->ring_rows) ctx->ram_len[l] = ctx->length[l];
+    else if (!ok(ring_after_append(ctx, l, s))) return KVO_ECUDA;
+  }
+  return KVO_OK;
+}
+
 kvo_status kvo_decode_step(kvo_ctx* ctx, int32_t layer, const void* new_rows, int64_t r,
                            const float* scores, int64_t n, int32_t k, int32_t* idx,
                            void* out_rows, uint16_t* out_bf16, void* stream) {

@@ -45,6 +45,20 @@ cudaError_t launch_topk(const float* scores, uint32_t n, uint32_t k, int32_t* id
 cudaError_t launch_resolve(const LayerView& L, const int32_t* idx, uint32_t k, uint8_t* out_rows,
                            uint16_t* out_bf16, uint32_t* status, int max_cluster,
                            cudaStream_t stream);
+// One layer of a batched decode step (kvo_decode_layers).
+struct StepTask {
+  LayerView L;
+  const void* new_rows;           // device rows to append, or NULL
+  uint32_t r;
+  uint32_t old_len;               // the layer's history length before the append
+  const float* scores;            // device scores to select from, or NULL: resolve idx as given
+  uint32_t n;
+  int32_t* idx;                   // device int32[k]: written with scores, read without
+  uint8_t* out_rows;
+  uint16_t* out_bf16;
+};
+cudaError_t launch_decode_layers(const StepTask* tasks, uint32_t ntasks, uint32_t k, uint32_t* status,
+                                 int max_cluster, cudaStream_t stream);
 cudaError_t launch_decode_step(const LayerView& L, const void* new_rows, uint32_t r, uint32_t old_len,
                                const float* scores, uint32_t n, uint32_t k, int32_t* idx, uint8_t* out_rows,
                                uint16_t* out_bf16, uint32_t* status, int max_cluster, cudaStream_t stream);

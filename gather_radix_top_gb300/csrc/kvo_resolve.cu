@@ -57,6 +57,7 @@ cudaError_t launch_resolve(const LayerView& L, const int32_t* idx, uint32_t k, u
   a.kchunk = (k + C - 2) / (C - 1);                 // CTA 0 keeps the LRU order, CTAs 1..C-1 the entries
   a.hchunk = ((L.hot_rows + C - 1) / C + 127u) & ~127u;
   a.fused = 0;
+  a.sel_in_smem = 0;
   a.len = 0;
   a.fresh = nullptr;
   a.fresh_from = 0;

@@ -86,10 +86,13 @@ struct ResolveArgs {
   // stage_min_miss_pct percent; else rows pass through registers.
   uint32_t stage_rows;
   uint32_t stage_min_miss_pct;
-  // fused decode step only: the selection is in shared memory, the history
-  // length is `len`, and positions >= fresh_from were appended by this very
-  // launch and are read from `fresh` (device memory) rather than host memory
+  // decode-step launches: the history length is `len`, and positions >=
+  // fresh_from were appended by this very launch and are read from `fresh`
+  // (device memory) rather than from host memory
   uint32_t fused;
+  // the selection was handed over in shared memory (`sel`, ascending) by the
+  // top-K phase of the same launch, rather than read from `idx`
+  uint32_t sel_in_smem;
   uint32_t len;
   const uint8_t* fresh;
   uint32_t fresh_from;
@@ -347,9 +350,9 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
   uint32_t nhit = 0, nmiss = 0, nhost = 0, ninv = 0, unordered = 0;   // per thread
   for (uint32_t jj = tid; jj < jcnt; jj += kThreads) {
     const uint32_t j = jlo + jj;
-    // fused calls take the selection from shared memory, already ascending
-    const int32_t p = a.fused ? sel[jj] : a.idx[j];
-    if (!a.fused && j > 0 && a.idx[j - 1] >= p) ++unordered;
+    // a selection made in the same launch comes from shared memory, ascending
+    const int32_t p = a.sel_in_smem ? sel[jj] : a.idx[j];
+    if (!a.sel_in_smem && j > 0 && a.idx[j - 1] >= p) ++unordered;
     int32_t slot;
     if (p < 0 || (uint32_t)p >= len) {
       slot = kSlotInvalid;

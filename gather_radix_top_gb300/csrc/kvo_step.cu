@@ -1,6 +1,7 @@
 // Fused decode step of one layer (kvo_decode_step): append the new rows,
 // select the top-K positions and resolve + gather them, in one cluster
-// launch.
+// launch; and the same for many layers at once (kvo_decode_layers), one
+// cluster per layer in one launch.
 //
 // "From 1M Total to 15+ x 1M Contexts: GLM-5.3 KV Cache Offloading",
 // "Decision three: let the GPU manage the hot cache directly": the CPU stays
@@ -8,8 +9,11 @@
 // back to back.  Fusing them also removes two kernel launches and the trip of
 // the selection through global memory: the top-K compaction hands each
 // selected position straight to the CTA that resolves it, over distributed
-// shared memory.
+// shared memory.  Section "Separate historical capacity from the current
+// working set": later layers reuse a selection and keep their own KV, so a
+// layer's task may also bring its selection instead of scores.
 #include <cstdint>
+#include <cstring>
 
 #include "kvo_internal.h"
 #include "kvo_resolve_body.cuh"
@@ -24,7 +28,7 @@ using namespace topk_detail;
 
 struct StepArgs {
   ResolveArgs R;              // fused = 1; R.len = history length after the append
-  const float* scores;
+  const float* scores;        // NULL: resolve the selection in R.idx as given
   uint32_t n;
   int32_t* idx;               // the selection, also returned to the caller
   const uint4* new_rows;      // r rows appended in this step (device memory)
@@ -34,10 +38,9 @@ struct StepArgs {
   uint32_t topk_bytes;        // dynamic shared memory used by the top-K phase
 };
 
+// One layer's step, run by one cluster: append, select (with scores), resolve.
 template <bool kResident, bool kLru>
-__global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const StepArgs s) {
-  extern __shared__ __align__(16) uint8_t dyn_smem[];
-  __shared__ RadixSmem rsm;                        // the top-K phase's radix histograms
+__device__ __forceinline__ void decode_body(const StepArgs& s, uint8_t* dyn_smem, RadixSmem* rsm) {
   const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t rank = cluster_rank(), C = cluster_size();
   constexpr uint32_t kVec = KVO_ROW_BYTES / 16;
@@ -53,17 +56,41 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const StepArgs
   }
 
   uint8_t* rdyn = dyn_smem + s.topk_bytes;
-  const SmemLayout lay = smem_layout(s.R.k, s.R.kchunk, s.R.hchunk, s.R.L.hot_rows, s.R.stage_rows);
-  int32_t* sel = reinterpret_cast<int32_t*>(rdyn + lay.sel);
-  const uint32_t kchunk = s.R.kchunk;
-  topk_body<kResident>(s.scores, s.n, s.R.k, dyn_smem, &rsm, [&](uint32_t pos, uint32_t out) {
-    s.idx[out] = (int32_t)pos;
-    const uint32_t q = out / kchunk;                 // CTA q + 1 resolves entries [q * kchunk, ...)
-    dsmem_st_u32(dsmem_addr(&sel[out - q * kchunk], q + 1), pos);
-  });
-  cluster_sync();                                  // every selected position delivered
+  if (s.scores) {
+    const SmemLayout lay = smem_layout(s.R.k, s.R.kchunk, s.R.hchunk, s.R.L.hot_rows, s.R.stage_rows);
+    int32_t* sel = reinterpret_cast<int32_t*>(rdyn + lay.sel);
+    const uint32_t kchunk = s.R.kchunk;
+    topk_body<kResident>(s.scores, s.n, s.R.k, dyn_smem, rsm, [&](uint32_t pos, uint32_t out) {
+      s.idx[out] = (int32_t)pos;
+      const uint32_t q = out / kchunk;               // CTA q + 1 resolves entries [q * kchunk, ...)
+      dsmem_st_u32(dsmem_addr(&sel[out - q * kchunk], q + 1), pos);
+    });
+    cluster_sync();                                // every selected position delivered
+  }
   resolve_body<kLru>(s.R, rdyn);
   if (rank == 0 && tid == 0) s.R.L.counters[1] = s.R.len;
+}
+
+template <bool kResident, bool kLru>
+__global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const StepArgs s) {
+  extern __shared__ __align__(16) uint8_t dyn_smem[];
+  __shared__ RadixSmem rsm;                        // the top-K phase's radix histograms
+  decode_body<kResident, kLru>(s, dyn_smem, &rsm);
+}
+
+// The tasks of one launch travel as its parameter (no staging buffer, no
+// upload): as many as fit the 32 KB parameter space.
+constexpr uint32_t kParamTasks = 30000u / sizeof(StepArgs);
+struct TaskBatch {
+  StepArgs t[kParamTasks];
+};
+
+// Cluster blockIdx.x / clusterDim.x runs task b.t[that index].
+template <bool kResident, bool kLru>
+__global__ void __launch_bounds__(kThreads, 1) decode_layers_kernel(const __grid_constant__ TaskBatch b) {
+  extern __shared__ __align__(16) uint8_t dyn_smem[];
+  __shared__ RadixSmem rsm;
+  decode_body<kResident, kLru>(b.t[blockIdx.x / cluster_size()], dyn_smem, &rsm);
 }
 
 struct StepConfig {
@@ -74,18 +101,17 @@ StepConfig g_step[64];
 
 constexpr size_t kStepMaxDynSmem = 187 * 1024;     // 227 KB less the static radix histograms
 
-}  // namespace
-
-cudaError_t launch_decode_step(const LayerView& L, const void* new_rows, uint32_t r, uint32_t old_len,
-                               const float* scores, uint32_t n, uint32_t k, int32_t* idx, uint8_t* out_rows,
-                               uint16_t* out_bf16, uint32_t* status, int max_cluster, cudaStream_t stream) {
+cudaError_t step_init(int* cluster) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   StepConfig& cfg = g_step[dev & 63];
   if (!cfg.init) {
-    const void* kernels[4] = {(const void*)decode_step_kernel<true, true>, (const void*)decode_step_kernel<false, true>,
-                              (const void*)decode_step_kernel<true, false>, (const void*)decode_step_kernel<false, false>};
+    const void* kernels[8] = {
+        (const void*)decode_step_kernel<true, true>,   (const void*)decode_step_kernel<false, true>,
+        (const void*)decode_step_kernel<true, false>,  (const void*)decode_step_kernel<false, false>,
+        (const void*)decode_layers_kernel<true, true>, (const void*)decode_layers_kernel<false, true>,
+        (const void*)decode_layers_kernel<true, false>, (const void*)decode_layers_kernel<false, false>};
     int c1 = (int)kMaxCluster;
     for (const void* kern : kernels) {
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStepMaxDynSmem);
@@ -97,31 +123,39 @@ cudaError_t launch_decode_step(const LayerView& L, const void* new_rows, uint32_
     if (cfg.cluster == 0) return cudaErrorInvalidConfiguration;
     cfg.init = true;
   }
-  const uint32_t C = (uint32_t)(cfg.cluster < max_cluster ? cfg.cluster : max_cluster);
-  StepArgs s;
-  ResolveArgs& a = s.R;
+  *cluster = cfg.cluster;
+  return cudaSuccess;
+}
+
+// Fills one layer's StepArgs for a cluster of C CTAs.  *need_res / *need_stream:
+// dynamic shared memory with the keys resident / streamed (0 when it does not
+// fit).
+void build_step(const StepTask& t, uint32_t k, uint32_t* status, uint32_t C, StepArgs* s, size_t* need_res,
+                size_t* need_stream) {
+  const LayerView& L = t.L;
+  ResolveArgs& a = s->R;
+  std::memset(static_cast<void*>(s), 0, sizeof *s);
   a.L = L;
-  a.idx = idx;
-  a.out_rows = out_rows;
-  a.out_bf16 = out_bf16;
+  a.idx = t.idx;
+  a.out_rows = t.out_rows;
+  a.out_bf16 = t.out_bf16;
   a.status = status;
   a.k = k;
   a.kchunk = (k + C - 2) / (C - 1);                 // CTA 0 keeps the LRU order, CTAs 1..C-1 the entries
   a.hchunk = ((L.hot_rows + C - 1) / C + 127u) & ~127u;
   a.fused = 1;
-  a.len = old_len + r;
-  a.fresh = r ? static_cast<const uint8_t*>(new_rows) : nullptr;
-  a.fresh_from = old_len;
-  s.scores = scores;
-  s.n = n;
-  s.idx = idx;
-  s.new_rows = static_cast<const uint4*>(new_rows);
-  s.hist_dst = reinterpret_cast<uint4*>(const_cast<uint8_t*>(L.hist) + (size_t)old_len * KVO_ROW_BYTES);
-  s.old_len = old_len;
-  s.r = r;
-  const size_t topk_res = ((size_t)topk_chunk(n, C) * 4u + 15u) & ~(size_t)15u;
-  // staged gather when the rows fit next to the resident keys (else next to
-  // streamed keys), else rows through registers
+  a.sel_in_smem = t.scores ? 1u : 0u;
+  a.len = t.old_len + t.r;
+  a.fresh = t.r ? static_cast<const uint8_t*>(t.new_rows) : nullptr;
+  a.fresh_from = t.old_len;
+  s->scores = t.scores;
+  s->n = t.n;
+  s->idx = t.idx;
+  s->new_rows = static_cast<const uint4*>(t.new_rows);
+  s->hist_dst = reinterpret_cast<uint4*>(const_cast<uint8_t*>(L.hist) + (size_t)t.old_len * KVO_ROW_BYTES);
+  s->old_len = t.old_len;
+  s->r = t.r;
+  // staged gather when the rows fit, else rows through registers
   a.stage_rows = L.gather_mode != KVO_GATHER_LOADS ? (a.kchunk < kStageMax ? a.kchunk : kStageMax) : 0u;
   a.stage_min_miss_pct = L.gather_mode == KVO_GATHER_STAGED ? 0u : L.auto_miss_pct;
   SmemLayout lay = smem_layout(k, a.kchunk, a.hchunk, L.hot_rows, a.stage_rows);
@@ -129,27 +163,83 @@ cudaError_t launch_decode_step(const LayerView& L, const void* new_rows, uint32_
     a.stage_rows = 0;
     lay = smem_layout(k, a.kchunk, a.hchunk, L.hot_rows, 0);
   }
-  if (lay.total > kStepMaxDynSmem) return cudaErrorInvalidValue;
-  const bool resident = topk_res + lay.total <= kStepMaxDynSmem;
-  s.topk_bytes = resident ? (uint32_t)topk_res : 0u;
+  const size_t topk_res = t.scores ? ((size_t)topk_chunk(t.n, C) * 4u + 15u) & ~(size_t)15u : 0u;
+  *need_stream = lay.total <= kStepMaxDynSmem ? lay.total : 0u;
+  *need_res = topk_res + lay.total <= kStepMaxDynSmem ? topk_res + lay.total : 0u;
+  s->topk_bytes = (uint32_t)topk_res;               // set to 0 by the caller when keys are streamed
+}
 
+cudaError_t launch(uint32_t C, uint32_t nclusters, size_t smem, cudaStream_t stream, bool resident, bool lru,
+                   const StepArgs* one, const TaskBatch* many) {
   cudaLaunchConfig_t lc = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  lc.gridDim = dim3(C, 1, 1);
+  lc.gridDim = dim3(C * nclusters, 1, 1);
   lc.blockDim = dim3(kThreads, 1, 1);
-  lc.dynamicSmemBytes = s.topk_bytes + lay.total;
+  lc.dynamicSmemBytes = smem;
   lc.stream = stream;
   lc.attrs = attr;
   lc.numAttrs = 1;
-  const bool lru = L.policy == KVO_POLICY_LRU;
-  if (resident) return lru ? cudaLaunchKernelEx(&lc, decode_step_kernel<true, true>, s)
-                           : cudaLaunchKernelEx(&lc, decode_step_kernel<true, false>, s);
-  return lru ? cudaLaunchKernelEx(&lc, decode_step_kernel<false, true>, s)
-             : cudaLaunchKernelEx(&lc, decode_step_kernel<false, false>, s);
+  if (one) {
+    if (resident) return lru ? cudaLaunchKernelEx(&lc, decode_step_kernel<true, true>, *one)
+                             : cudaLaunchKernelEx(&lc, decode_step_kernel<true, false>, *one);
+    return lru ? cudaLaunchKernelEx(&lc, decode_step_kernel<false, true>, *one)
+               : cudaLaunchKernelEx(&lc, decode_step_kernel<false, false>, *one);
+  }
+  if (resident) return lru ? cudaLaunchKernelEx(&lc, decode_layers_kernel<true, true>, *many)
+                           : cudaLaunchKernelEx(&lc, decode_layers_kernel<true, false>, *many);
+  return lru ? cudaLaunchKernelEx(&lc, decode_layers_kernel<false, true>, *many)
+             : cudaLaunchKernelEx(&lc, decode_layers_kernel<false, false>, *many);
+}
+
+}  // namespace
+
+cudaError_t launch_decode_step(const LayerView& L, const void* new_rows, uint32_t r, uint32_t old_len,
+                               const float* scores, uint32_t n, uint32_t k, int32_t* idx, uint8_t* out_rows,
+                               uint16_t* out_bf16, uint32_t* status, int max_cluster, cudaStream_t stream) {
+  int cl = 0;
+  cudaError_t e = step_init(&cl);
+  if (e != cudaSuccess) return e;
+  const uint32_t C = (uint32_t)(cl < max_cluster ? cl : max_cluster);
+  const StepTask t = {L, new_rows, r, old_len, scores, n, idx, out_rows, out_bf16};
+  StepArgs s;
+  size_t need_res = 0, need_stream = 0;
+  build_step(t, k, status, C, &s, &need_res, &need_stream);
+  if (!need_stream) return cudaErrorInvalidValue;
+  const bool resident = need_res != 0;
+  if (!resident) s.topk_bytes = 0;
+  return launch(C, 1, resident ? need_res : need_stream, stream, resident, L.policy == KVO_POLICY_LRU, &s, nullptr);
+}
+
+cudaError_t launch_decode_layers(const StepTask* tasks, uint32_t ntasks, uint32_t k, uint32_t* status,
+                                 int max_cluster, cudaStream_t stream) {
+  int cl = 0;
+  cudaError_t e = step_init(&cl);
+  if (e != cudaSuccess) return e;
+  const uint32_t C = (uint32_t)(cl < max_cluster ? cl : max_cluster);
+  static thread_local TaskBatch b;                  // 30 KB: kept off the stack
+  for (uint32_t first = 0; first < ntasks; first += kParamTasks) {
+    const uint32_t nb = ntasks - first < kParamTasks ? ntasks - first : kParamTasks;
+    size_t res_max = 0, stream_max = 0;
+    bool resident = true;
+    for (uint32_t i = 0; i < nb; ++i) {
+      size_t need_res = 0, need_stream = 0;
+      build_step(tasks[first + i], k, status, C, &b.t[i], &need_res, &need_stream);
+      if (!need_stream) return cudaErrorInvalidValue;
+      resident = resident && need_res != 0;
+      res_max = need_res > res_max ? need_res : res_max;
+      stream_max = need_stream > stream_max ? need_stream : stream_max;
+    }
+    if (!resident)
+      for (uint32_t i = 0; i < nb; ++i) b.t[i].topk_bytes = 0;
+    e = launch(C, nb, resident ? res_max : stream_max, stream, resident, tasks[first].L.policy == KVO_POLICY_LRU,
+               nullptr, &b);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace kvo

@@ -28,7 +28,7 @@ KVO_OK, KVO_EINVAL, KVO_ENOMEM, KVO_ECUDA, KVO_ERANGE, KVO_EBUSY, KVO_ETIMEDOUT,
 EXPORTED = [
     "kvo_status_string", "kvo_create", "kvo_destroy", "kvo_append_rows", "kvo_select_topk",
     "kvo_select_topk_batch",
-    "kvo_resolve_gather", "kvo_resolve_gather_multi", "kvo_decode_step", "kvo_sync", "kvo_get_stats", "kvo_history_length",
+    "kvo_resolve_gather", "kvo_resolve_gather_multi", "kvo_decode_step", "kvo_decode_layers", "kvo_sync", "kvo_get_stats", "kvo_history_length",
     "kvo_debug_dump_layer", "kvo_debug_record_evictions", "kvo_debug_evictions", "kvo_set_policy",
     "kvo_debug_layer_counters", "kvo_set_recent_ring", "kvo_flush_ring", "kvo_ram_length",
     "kvo_debug_read_history", "kvo_set_gather_mode",
@@ -52,6 +52,12 @@ class kvo_stats(ctypes.Structure):
 
     def as_dict(self) -> dict:
         return {n: int(getattr(self, n)) for n, _ in self._fields_}
+
+
+class kvo_layer_task(ctypes.Structure):
+    _fields_ = [("layer", ctypes.c_int32), ("reserved", ctypes.c_int32), ("new_rows", ctypes.c_void_p),
+                ("r", ctypes.c_int64), ("scores", ctypes.c_void_p), ("n", ctypes.c_int64),
+                ("idx", ctypes.c_void_p), ("out_rows", ctypes.c_void_p), ("out_bf16", ctypes.c_void_p)]
 
 
 class kvo_pool_stats(ctypes.Structure):
@@ -89,6 +95,7 @@ def lib() -> ctypes.CDLL:
         "kvo_resolve_gather": (ctypes.c_int, [_vp, _i32, _vp, _i32, _vp, _vp, _vp]),
         "kvo_resolve_gather_multi": (ctypes.c_int, [_vp, _i32, _vp, _i32, _i32, _vp, _vp, _vp]),
         "kvo_decode_step": (ctypes.c_int, [_vp, _i32, _vp, _i64, _vp, _i64, _i32, _vp, _vp, _vp, _vp]),
+        "kvo_decode_layers": (ctypes.c_int, [_vp, ctypes.POINTER(kvo_layer_task), _i32, _i32, _vp]),
         "kvo_sync": (ctypes.c_int, [_vp, _vp]),
         "kvo_get_stats": (ctypes.c_int, [_vp, _i32, ctypes.POINTER(kvo_stats)]),
         "kvo_history_length": (ctypes.c_int, [_vp, _i32, ctypes.POINTER(_i64)]),
@@ -248,6 +255,39 @@ def kvo_decode_step(ctx: int, layer: int, new_rows, scores, k: int, idx=None, ou
     return idx
 
 
+def make_layer_tasks(tasks):
+    """A kvo_layer_task array from dicts with layer, idx (int32 CUDA [k]) and
+    out_rows and/or out_bf16, optionally new_rows (uint8 CUDA [r, 656]) and
+    scores (float32 CUDA [n]; without scores idx is resolved as given).  The
+    array holds raw device addresses: it stays valid while the tensors do."""
+    arr = (kvo_layer_task * len(tasks))()
+    for i, t in enumerate(tasks):
+        nr = t.get("new_rows")
+        sc = t.get("scores")
+        ob = t.get("out_bf16")
+        if ob is not None and str(ob.dtype) not in ("torch.bfloat16", "torch.int16"):
+            raise ValueError("out_bf16 must be bfloat16 or int16")
+        arr[i].layer = t["layer"]
+        arr[i].new_rows = None if nr is None else _dev_ptr(nr, "torch.uint8")
+        arr[i].r = 0 if nr is None else nr.numel() // ROW_BYTES
+        arr[i].scores = None if sc is None else _dev_ptr(sc, "torch.float32")
+        arr[i].n = 0 if sc is None else sc.numel()
+        arr[i].idx = _dev_ptr(t["idx"], "torch.int32")
+        arr[i].out_rows = _dev_ptr(t.get("out_rows"), "torch.uint8")
+        arr[i].out_bf16 = _dev_ptr(ob)
+    return arr
+
+
+def kvo_decode_layers_prepared(ctx: int, arr, k: int, stream=None) -> None:
+    """kvo_decode_layers with an array from make_layer_tasks (no marshalling)."""
+    _check(lib().kvo_decode_layers(ctx, arr, len(arr), k, _stream_ptr(stream)), "kvo_decode_layers")
+
+
+def kvo_decode_layers(ctx: int, tasks, k: int, stream=None) -> None:
+    """One decode step of several layers in one launch; tasks as in make_layer_tasks."""
+    kvo_decode_layers_prepared(ctx, make_layer_tasks(tasks), k, stream)
+
+
 def kvo_sync(ctx: int, stream=None) -> int:
     """Synchronise and return the latched device status (KVO_OK, KVO_ERANGE, ...)."""
     return lib().kvo_sync(ctx, _stream_ptr(stream))
@@ -288,7 +328,7 @@ def kvo_set_policy(ctx: int, policy: int) -> None:
 
 def kvo_set_gather_mode(ctx: int, mode: int, auto_miss_pct: int = 0) -> None:
     """GATHER_LOADS, GATHER_STAGED or GATHER_AUTO (staged for CTAs whose
-    misses are at most auto_miss_pct percent of their entries)."""
+    misses are at least auto_miss_pct percent of their entries)."""
     _check(lib().kvo_set_gather_mode(ctx, mode, auto_miss_pct), "kvo_set_gather_mode")
 
 
@@ -384,6 +424,12 @@ class Context:
 
     def decode_step(self, layer, new_rows, scores, k, idx=None, out_rows=None, out_bf16=None, stream=None):
         return kvo_decode_step(self.handle, layer, new_rows, scores, k, idx, out_rows, out_bf16, stream)
+
+    def decode_layers(self, tasks, k, stream=None):
+        kvo_decode_layers(self.handle, tasks, k, stream)
+
+    def decode_layers_prepared(self, arr, k, stream=None):
+        kvo_decode_layers_prepared(self.handle, arr, k, stream)
 
     def sync(self, stream=None) -> int:
         return kvo_sync(self.handle, stream)

@@ -152,10 +152,12 @@ kvo_status kvo_debug_read_history(kvo_ctx* ctx, int32_t layer, int64_t start, in
  * is pulled into shared memory by a TMA bulk copy (all in flight at once,
  * host rows included) and the share written back with one bulk store; used
  * where a CTA's share fits its shared memory, else loads.  KVO_GATHER_AUTO:
- * staged for a CTA whose misses are at most auto_miss_pct percent of its
+ * staged for a CTA whose misses are at least auto_miss_pct percent of its
  * entries, loads otherwise (decided per CTA and call, after classification).
- * Outputs are identical in every mode.  Default: KVO_GATHER_LOADS.  Host
- * only; takes effect from the next call.
+ * Outputs are identical in every mode.  Default: KVO_GATHER_AUTO with 5 %
+ * (per 2,048-row call on a full cache the staged gather is as fast below
+ * 5 % misses and 0.4-1.4 us faster from 5 % up).  Host only; takes effect
+ * from the next call.
  */
 #define KVO_GATHER_LOADS 0
 #define KVO_GATHER_STAGED 1
@@ -250,6 +252,38 @@ kvo_status kvo_resolve_gather(kvo_ctx* ctx, int32_t layer, const int32_t* idx, i
  */
 kvo_status kvo_resolve_gather_multi(kvo_ctx* ctx, int32_t layer, const int32_t* idx, int32_t nq, int32_t k,
                                     void* out_rows, uint16_t* out_bf16, void* stream);
+
+/*
+ * kvo_decode_layers - one decode step of several layers in one launch (one
+ * thread-block cluster per task); each task is what kvo_decode_step does for
+ * its layer, except that a task without scores resolves the selection its
+ * idx already holds ([KVO] "Separate historical capacity from the current
+ * working set": later layers reuse a layer's selection and keep their own
+ * KV).  Per task:
+ *   layer     a layer of the context; at most one task per layer per call.
+ *   new_rows  device rows to append first (16-byte aligned), r of them, or
+ *             NULL with r = 0.
+ *   scores    device fp32[n]: select the top k of them into idx; or NULL:
+ *             idx is an input (any order, duplicates allowed, as in
+ *             kvo_resolve_gather), and n is ignored.
+ *   idx       device int32[k].
+ *   out_rows / out_bf16  as in kvo_resolve_gather (at least one).
+ * The tasks of one call run concurrently: a task must not read an idx that
+ * another task of the same call writes (select in one call, reuse in the
+ * next).  KVO_EINVAL on a bad task (nothing enqueued).
+ */
+typedef struct kvo_layer_task {
+  int32_t layer;
+  int32_t reserved;
+  const void* new_rows;
+  int64_t r;
+  const float* scores;
+  int64_t n;
+  int32_t* idx;
+  void* out_rows;
+  uint16_t* out_bf16;
+} kvo_layer_task;
+kvo_status kvo_decode_layers(kvo_ctx* ctx, const kvo_layer_task* tasks, int32_t ntasks, int32_t k, void* stream);
 
 /*
  * kvo_decode_step - one decode step of one layer in a single launch: the

@@ -603,7 +603,7 @@ def test_recent_ring_50k_fused(kvo):
 
 
 # ------------------------------------------------ staged (TMA) gather
-GATHERS = [(1, 0), (2, 10)]     # staged always; staged for CTAs with at most 10 % misses
+GATHERS = [(0, 0), (1, 0), (2, 10)]   # loads; staged always; staged for CTAs with at least 10 % misses
 
 
 @pytest.mark.parametrize("gather", GATHERS)
@@ -666,3 +666,80 @@ def test_staged_gather_50k_fused_with_ring(kvo, gather):
     compare_state(g.ctx, 0, o.st)
     assert g.ctx.sync() == 0
     g.ctx.close()
+
+
+# ------------------------------------------------ batched layers (one launch)
+@pytest.mark.parametrize("policy,ring,gather", [(0, 0, None), (1, 128, (1, 0))])
+def test_decode_layers_stack_parity(kvo, policy, ring, gather):
+    """Eight layers, selection on layers 0 and 4 (one launch), reused by the
+    others (a second launch); appends every step.  Every layer equals its
+    own oracle: selections, rows, evictions, maps."""
+    import torch
+    w = W.STACK.scaled(layers=8, n0=6000, hot_rows=1024, k=256, steps=24, carry=150)
+    L = w.layers
+    ctx = kvo.Context(L, w.history_cap, w.hot_rows)
+    if policy:
+        ctx.set_policy(policy)
+    if ring:
+        ctx.set_recent_ring(ring)
+    if gather:
+        ctx.set_gather_mode(*gather)
+    ctx.record_evictions(True)
+    pol = "circular" if policy else "lru"
+    orc = [OracleLayerRun(w, l, policy=pol, ring=ring, fused=True) for l in range(L)]
+    new = [torch.from_numpy(W.rows(w, l, w.n0, w.history_cap - w.n0)).cuda() for l in range(L)]
+    for l in range(L):
+        ctx.append_rows(l, W.rows(w, l, 0, w.n0))
+    idx = [torch.empty(w.k, dtype=torch.int32, device="cuda") for _ in range(L)]
+    out = [torch.empty((w.k, O.ROW_BYTES), dtype=torch.uint8, device="cuda") for _ in range(L)]
+    prev = {}
+    for step in range(w.steps):
+        sel_tasks, reuse_tasks = [], []
+        for l in range(L):
+            t = {"layer": l, "idx": idx[l], "out_rows": out[l], "new_rows": new[l][step:step + 1]}
+            if l in w.selecting_layers():
+                s = W.apply_carry(W.base_scores(w, l, step), prev.get(l), W.carry_draw(w, l, step), w.carry_boost)
+                t["scores"] = torch.from_numpy(s).cuda()
+                sel_tasks.append(t)
+            else:
+                reuse_tasks.append(t)
+        ctx.decode_layers(sel_tasks, w.k)
+        for t in reuse_tasks:                           # the source layer's selection, copied in stream order
+            t["idx"].copy_(idx[w.source_layer(t["layer"])])
+        ctx.decode_layers(reuse_tasks, w.k)
+        for l in range(L):
+            src = w.source_layer(l)
+            if l == src:
+                want = orc[l].step(step)
+                np.testing.assert_array_equal(idx[l].cpu().numpy(), want)
+                prev[l] = want
+            else:
+                orc[l].step(step, idx_override=prev[src])
+            np.testing.assert_array_equal(out[l].cpu().numpy(), orc[l].last.rows)
+            assert ctx.evictions(l) == orc[l].last.evictions, (step, l)
+    for l in range(L):
+        compare_state(ctx, l, orc[l].st)
+        assert ctx.history_length(l) == orc[l].st.length
+    assert ctx.sync() == 0
+    ctx.close()
+
+
+def test_decode_layers_argument_errors(kvo):
+    import torch
+    ctx = kvo.Context(2, 1000, 64)
+    for l in range(2):
+        ctx.append_rows(l, np.zeros((500, O.ROW_BYTES), np.uint8))
+    i0, i1 = (torch.zeros(16, dtype=torch.int32, device="cuda") for _ in range(2))
+    o = torch.empty((16, O.ROW_BYTES), dtype=torch.uint8, device="cuda")
+    sc = torch.zeros(500, device="cuda")
+    with pytest.raises(kvo.KvoError):                   # the same layer twice
+        ctx.decode_layers([{"layer": 0, "idx": i0, "out_rows": o}, {"layer": 0, "idx": i1, "out_rows": o}], 16)
+    with pytest.raises(kvo.KvoError):                   # n beyond the history
+        ctx.decode_layers([{"layer": 1, "idx": i0, "out_rows": o, "scores": torch.zeros(600, device="cuda")}], 16)
+    with pytest.raises(kvo.KvoError):                   # no output
+        ctx.decode_layers([{"layer": 1, "idx": i0}], 16)
+    ctx.decode_layers([{"layer": 0, "idx": i0, "out_rows": o, "scores": sc},
+                       {"layer": 1, "idx": i1, "out_rows": torch.empty_like(o)}], 16)
+    assert ctx.sync() == 0
+    assert ctx.stats(0)["steps"] == 1 and ctx.stats(1)["steps"] == 1
+    ctx.close()

@@ -219,7 +219,14 @@ cudaError_t launch_decode_layers(const StepTask* tasks, uint32_t ntasks, uint32_
   int cl = 0;
   cudaError_t e = step_init(&cl);
   if (e != cudaSuccess) return e;
-  const uint32_t C = (uint32_t)(cl < max_cluster ? cl : max_cluster);
+  // 16-CTA clusters while the tasks fit one wave of the SMs, else 8 (twice
+  // as many layers at a time: 0.57 vs 0.47 G rows/s on the 78-layer stack)
+  int sms = 0, dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int want = cl < max_cluster ? cl : max_cluster;
+  if (want > 8 && (uint32_t)(sms / want) < ntasks) want = 8;
+  const uint32_t C = (uint32_t)want;
   static thread_local TaskBatch b;                  // 30 KB: kept off the stack
   for (uint32_t first = 0; first < ntasks; first += kParamTasks) {
     const uint32_t nb = ntasks - first < kParamTasks ? ntasks - first : kParamTasks;

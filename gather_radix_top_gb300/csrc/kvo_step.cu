@@ -35,7 +35,7 @@ struct StepArgs {
   uint4* hist_dst;            // device address of history row `old length` (no recent ring)
   uint32_t old_len;
   uint32_t r;
-  uint32_t topk_bytes;        // dynamic shared memory used by the top-K phase
+  uint32_t topk_bytes;        // dynamic shared memory of the top-K phase (resident keys or candidates)
 };
 
 // One layer's step, run by one cluster: append, select (with scores), resolve.
@@ -60,7 +60,7 @@ __device__ __forceinline__ void decode_body(const StepArgs& s, uint8_t* dyn_smem
     const SmemLayout lay = smem_layout(s.R.k, s.R.kchunk, s.R.hchunk, s.R.L.hot_rows, s.R.stage_rows);
     int32_t* sel = reinterpret_cast<int32_t*>(rdyn + lay.sel);
     const uint32_t kchunk = s.R.kchunk;
-    topk_body<kResident>(s.scores, s.n, s.R.k, dyn_smem, rsm, [&](uint32_t pos, uint32_t out) {
+    topk_body<kResident>(s.scores, s.n, s.R.k, dyn_smem, s.topk_bytes, rsm, [&](uint32_t pos, uint32_t out) {
       s.idx[out] = (int32_t)pos;
       const uint32_t q = out / kchunk;               // CTA q + 1 resolves entries [q * kchunk, ...)
       dsmem_st_u32(dsmem_addr(&sel[out - q * kchunk], q + 1), pos);
@@ -96,12 +96,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layers_kernel(const __grid
 struct StepConfig {
   bool init = false;
   int cluster = 0;
+  int active16 = 0;          // 16-CTA clusters of the batched kernel that fit at once
 };
 StepConfig g_step[64];
 
 constexpr size_t kStepMaxDynSmem = 187 * 1024;     // 227 KB less the static radix histograms
 
-cudaError_t step_init(int* cluster) {
+cudaError_t step_init(int* cluster, int* active16 = nullptr) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -121,17 +122,37 @@ cudaError_t step_init(int* cluster) {
     }
     cfg.cluster = c1;
     if (cfg.cluster == 0) return cudaErrorInvalidConfiguration;
+    if (cfg.cluster >= 16) {
+      cudaLaunchConfig_t lc = {};
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 16;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      lc.gridDim = dim3(16, 1, 1);
+      lc.blockDim = dim3(kThreads, 1, 1);
+      lc.dynamicSmemBytes = kStepMaxDynSmem;
+      lc.attrs = attr;
+      lc.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&cfg.active16, (const void*)decode_layers_kernel<false, true>, &lc) !=
+          cudaSuccess) {
+        cudaGetLastError();
+        cfg.active16 = 0;
+      }
+    }
     cfg.init = true;
   }
   *cluster = cfg.cluster;
+  if (active16) *active16 = cfg.active16;
   return cudaSuccess;
 }
 
 // Fills one layer's StepArgs for a cluster of C CTAs.  *need_res / *need_stream:
 // dynamic shared memory with the keys resident / streamed (0 when it does not
-// fit).
+// fit); *stream_topk: the top-K phase's share when streamed (what the resolve
+// phase leaves, for the filtered route's candidates).
 void build_step(const StepTask& t, uint32_t k, uint32_t* status, uint32_t C, StepArgs* s, size_t* need_res,
-                size_t* need_stream) {
+                size_t* need_stream, uint32_t* stream_topk) {
   const LayerView& L = t.L;
   ResolveArgs& a = s->R;
   std::memset(static_cast<void*>(s), 0, sizeof *s);
@@ -164,9 +185,11 @@ void build_step(const StepTask& t, uint32_t k, uint32_t* status, uint32_t C, Ste
     lay = smem_layout(k, a.kchunk, a.hchunk, L.hot_rows, 0);
   }
   const size_t topk_res = t.scores ? ((size_t)topk_chunk(t.n, C) * 4u + 15u) & ~(size_t)15u : 0u;
-  *need_stream = lay.total <= kStepMaxDynSmem ? lay.total : 0u;
+  const size_t cand = t.scores && lay.total <= kStepMaxDynSmem ? (kStepMaxDynSmem - lay.total) & ~(size_t)15u : 0u;
+  *stream_topk = (uint32_t)cand;
+  *need_stream = lay.total <= kStepMaxDynSmem ? cand + lay.total : 0u;
   *need_res = topk_res + lay.total <= kStepMaxDynSmem ? topk_res + lay.total : 0u;
-  s->topk_bytes = (uint32_t)topk_res;               // set to 0 by the caller when keys are streamed
+  s->topk_bytes = (uint32_t)topk_res;               // replaced by *stream_topk when keys are streamed
 }
 
 cudaError_t launch(uint32_t C, uint32_t nclusters, size_t smem, cudaStream_t stream, bool resident, bool lru,
@@ -207,41 +230,41 @@ cudaError_t launch_decode_step(const LayerView& L, const void* new_rows, uint32_
   const StepTask t = {L, new_rows, r, old_len, scores, n, idx, out_rows, out_bf16};
   StepArgs s;
   size_t need_res = 0, need_stream = 0;
-  build_step(t, k, status, C, &s, &need_res, &need_stream);
+  uint32_t stream_topk = 0;
+  build_step(t, k, status, C, &s, &need_res, &need_stream, &stream_topk);
   if (!need_stream) return cudaErrorInvalidValue;
   const bool resident = need_res != 0;
-  if (!resident) s.topk_bytes = 0;
+  if (!resident) s.topk_bytes = stream_topk;
   return launch(C, 1, resident ? need_res : need_stream, stream, resident, L.policy == KVO_POLICY_LRU, &s, nullptr);
 }
 
 cudaError_t launch_decode_layers(const StepTask* tasks, uint32_t ntasks, uint32_t k, uint32_t* status,
                                  int max_cluster, cudaStream_t stream) {
-  int cl = 0;
-  cudaError_t e = step_init(&cl);
+  int cl = 0, active16 = 0;
+  cudaError_t e = step_init(&cl, &active16);
   if (e != cudaSuccess) return e;
-  // 16-CTA clusters while the tasks fit one wave of the SMs, else 8 (twice
-  // as many layers at a time: 0.57 vs 0.47 G rows/s on the 78-layer stack)
-  int sms = 0, dev = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // 16-CTA clusters while the tasks fit one wave of them (a cluster stays
+  // inside one GPC: 7 at a time on a 152-SM GB300), else 8 (15 at a time:
+  // 0.60 vs 0.47 G rows/s on the 78-layer stack)
   int want = cl < max_cluster ? cl : max_cluster;
-  if (want > 8 && (uint32_t)(sms / want) < ntasks) want = 8;
+  if (want > 8 && (uint32_t)active16 < ntasks) want = 8;
   const uint32_t C = (uint32_t)want;
   static thread_local TaskBatch b;                  // 30 KB: kept off the stack
   for (uint32_t first = 0; first < ntasks; first += kParamTasks) {
     const uint32_t nb = ntasks - first < kParamTasks ? ntasks - first : kParamTasks;
     size_t res_max = 0, stream_max = 0;
     bool resident = true;
+    static thread_local uint32_t stream_topk[kParamTasks];
     for (uint32_t i = 0; i < nb; ++i) {
       size_t need_res = 0, need_stream = 0;
-      build_step(tasks[first + i], k, status, C, &b.t[i], &need_res, &need_stream);
+      build_step(tasks[first + i], k, status, C, &b.t[i], &need_res, &need_stream, &stream_topk[i]);
       if (!need_stream) return cudaErrorInvalidValue;
       resident = resident && need_res != 0;
       res_max = need_res > res_max ? need_res : res_max;
       stream_max = need_stream > stream_max ? need_stream : stream_max;
     }
     if (!resident)
-      for (uint32_t i = 0; i < nb; ++i) b.t[i].topk_bytes = 0;
+      for (uint32_t i = 0; i < nb; ++i) b.t[i].topk_bytes = stream_topk[i];
     e = launch(C, nb, resident ? res_max : stream_max, stream, resident, tasks[first].L.policy == KVO_POLICY_LRU,
                nullptr, &b);
     if (e != cudaSuccess) return e;

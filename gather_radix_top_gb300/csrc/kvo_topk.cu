@@ -21,7 +21,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t row = blockIdx.x / cluster_size();
   const float* s = scores + row * ld;
   int32_t* out_idx = idx + (size_t)row * k;
-  topk_body<kResident>(s, n, k, dyn_smem, &rsm, [&](uint32_t pos, uint32_t out) { out_idx[out] = (int32_t)pos; });
+  topk_body<kResident>(s, n, k, dyn_smem, kTopkMaxDynSmem, &rsm,
+                       [&](uint32_t pos, uint32_t out) { out_idx[out] = (int32_t)pos; });
 }
 
 struct TopkConfig {
@@ -39,15 +40,17 @@ cudaError_t launch_topk(const float* scores, uint32_t n, uint32_t k, int32_t* id
   if (e != cudaSuccess) return e;
   TopkConfig& cfg = g_topk[dev & 63];
   if (!cfg.init) {
-    e = cudaFuncSetAttribute(topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kTopkMaxDynSmem);
-    if (e != cudaSuccess) return e;
+    for (const void* kern : {(const void*)topk_kernel<true>, (const void*)topk_kernel<false>}) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTopkMaxDynSmem);
+      if (e != cudaSuccess) return e;
+    }
     cfg.cluster_res = best_cluster((const void*)topk_kernel<true>, kTopkMaxDynSmem, (int)kMaxCluster);
-    cfg.cluster_stream = best_cluster((const void*)topk_kernel<false>, 0, (int)kMaxCluster);
+    cfg.cluster_stream = best_cluster((const void*)topk_kernel<false>, kTopkMaxDynSmem, (int)kMaxCluster);
     if (cfg.cluster_res == 0 || cfg.cluster_stream == 0) return cudaErrorInvalidConfiguration;
     cfg.init = true;
   }
-  // Resident when one CTA's share of the keys fits in shared memory.
+  // Resident when one CTA's share of the keys fits in shared memory, else
+  // the filtered route with all of it for candidates.
   int C = cfg.cluster_res < max_cluster ? cfg.cluster_res : max_cluster;
   uint32_t chunk = topk_chunk(n, (uint32_t)C);
   const bool resident = (uint64_t)chunk * 4u <= kTopkMaxDynSmem;
@@ -64,7 +67,7 @@ cudaError_t launch_topk(const float* scores, uint32_t n, uint32_t k, int32_t* id
   attr[0].val.clusterDim.z = 1;
   lc.gridDim = dim3((unsigned)C * nq, 1, 1);
   lc.blockDim = dim3(kThreads, 1, 1);
-  lc.dynamicSmemBytes = resident ? (size_t)chunk * 4u : 0;
+  lc.dynamicSmemBytes = resident ? (size_t)chunk * 4u : kTopkMaxDynSmem;   // streamed: room for candidates
   lc.stream = stream;
   lc.attrs = attr;
   lc.numAttrs = 1;

@@ -219,6 +219,33 @@ def random_scores(seed: int, n: int, kind: str = "normal") -> np.ndarray:
         mask = g.random(n) < 0.3
         s[mask] = specials[pick[mask]]
         return s
+    if kind == "coarse":        # N(0, 1) on a 1/64 grid: dozens of equal keys at any cut
+        return (np.round(g.standard_normal(n) * 64.0) / 64.0).astype(np.float32)
+    if kind == "recent":        # N(0, 1) with the last 4,096 positions raised by 6
+        s = g.standard_normal(n, dtype=np.float32)
+        s[max(0, n - 4096):] += np.float32(6.0)
+        return s
+    if kind == "lognormal":     # exp(N(0, 2)): positive, spread over many binades
+        return np.exp(2.0 * g.standard_normal(n)).astype(np.float32)
+    if kind == "sprinkled":     # N(0, 1) with 1% specials (+-0, +-inf, NaN, denormals)
+        s = g.standard_normal(n, dtype=np.float32)
+        specials = np.array([0.0, -0.0, np.inf, -np.inf, np.nan, 1e-45, -1e-45], np.float32)
+        where = g.choice(n, size=n // 100, replace=False)
+        s[where] = specials[g.integers(0, 7, size=where.size)]
+        return s
+    if kind == "negative":      # every score negative: -(|N(0, 1)| + 1e-3)
+        return (-(np.abs(g.standard_normal(n)) + 1e-3)).astype(np.float32)
+    if kind == "negzero":       # "negative" with 0.25% -0.0 and 0.25% -1e-45 (above every other score)
+        s = (-(np.abs(g.standard_normal(n)) + 1e-3)).astype(np.float32)
+        where = g.choice(n, size=n // 200, replace=False)
+        s[where] = np.array([-0.0, -1e-45], np.float32)[g.integers(0, 2, size=where.size)]
+        return s
+    if kind == "nan_inf":       # NaN everywhere but 3,000 -inf and 1,000 -1e30
+        s = np.full(n, np.nan, np.float32)
+        where = g.choice(n, size=4000, replace=False)
+        s[where[:3000]] = -np.inf
+        s[where[3000:]] = np.float32(-1e30)
+        return s
     raise ValueError(kind)
 
 

@@ -50,6 +50,13 @@ TOPK_CASES = [
     (50_023, 2048, "normal"), (50_023, 2048, "ties"), (51_047, 2048, "special"),
     (65_537, 4096, "normal"), (200_000, 2048, "ties"), (1_048_576, 2048, "normal"),
     (1_048_576, 2048, "ties"), (1_048_583, 4093, "special"),
+    # beyond the shared-memory-resident size: the filtered route and its fallback
+    (786_433, 2048, "normal"), (1_048_576, 1, "normal"), (1_048_576, 2048, "coarse"),
+    (1_048_576, 4096, "coarse"), (1_048_576, 2048, "recent"), (1_048_577, 4096, "recent"),
+    (2_000_003, 2048, "lognormal"), (3_000_017, 4096, "coarse"), (1_048_576, 2048, "sprinkled"),
+    (1_048_576, 2048, "negative"), (1_048_576, 2048, "negzero"), (1_048_576, 4096, "negzero"),
+    (1_048_576, 2048, "nan_inf"),
+    (1_048_579, 1000, "nan_inf"),
 ]
 
 
@@ -71,13 +78,15 @@ def test_topk_degenerate_orders(ctx, n, k):
 
 
 @pytest.mark.parametrize("nq,n,ld,k", [(1, 1000, 1000, 100), (4, 50_024, 51_200, 2048), (3, 4099, 4101, 1000),
-                                        (5, 1_048_576, 1_048_576, 2048), (2, 200_000, 200_003, 4093)])
+                                        (5, 1_048_576, 1_048_576, 2048), (2, 200_000, 200_003, 4093),
+                                        (3, 1_048_583, 1_048_591, 2048)])
 def test_topk_batch_matches_oracle_per_row(ctx, nq, n, ld, k):
     """One launch, one cluster per row; rows at any stride (unaligned too)."""
     import torch
     rows = np.zeros((nq, ld), np.float32)
     for q in range(nq):
-        rows[q, :n] = W.random_scores(nq * 1000 + q + n, n, ["normal", "ties", "special"][q % 3])
+        kinds = ["normal", "ties", "special"] if n < 1_048_583 else ["normal", "coarse", "recent"]
+        rows[q, :n] = W.random_scores(nq * 1000 + q + n, n, kinds[q % 3])
         rows[q, n:] = np.inf                          # beyond n: must never be selected
     idx = ctx.select_topk_batch(torch.from_numpy(rows).cuda(), k, n)
     got = idx.cpu().numpy()

@@ -909,6 +909,8 @@ def main():
         sessions_main(args, int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")))
         return
     w = W.WORKLOADS[args.workload]
+    settle = int(w.extra.get("settle", 0))
+    args.warmup += settle                  # untimed steps: the workload's settle phase, then the warm-up
     if args.steps is None:
         args.steps = max(1, w.steps - args.warmup)
     if args.warmup + args.steps > w.steps:
@@ -924,6 +926,8 @@ def main():
                         else "kvo_decode_layers x2 (selecting layers, then reusing layers)" if w.layers > 1
                         else "kvo_decode_step"),
               "l2": "flushed between steps (1 GiB memset, outside the step events)"}
+    if settle:
+        config["settle_steps"] = settle
 
     if args.impl == "reference":
         if rank != 0:

@@ -100,8 +100,11 @@ K50 = Workload("50k_single_layer", 1, 2, layers=1, n0=50_023, hot_rows=32_768, k
                steps=1024, appends_per_step=1, carry=1229, recency_amp=2.0)
 STACK = Workload("50k_full_stack", 2, 3, layers=78, n0=50_023, hot_rows=32_768, k=2048,
                  steps=256, appends_per_step=1, select_every=4, carry=1229, recency_amp=2.0)
+# "settle": untimed steps before a timed run's warm-up (the 32,768-slot hot
+# cache fills in 16 steps of 2,048 misses; the GPU's view of the 5.5 GB host
+# history settles in about as many more)
 M1 = Workload("1m_cold_stress", 3, 4, layers=8, n0=1_048_576, hot_rows=32_768, k=2048,
-              steps=64, appends_per_step=0, bf16=True)
+              steps=80, appends_per_step=0, bf16=True, extra={"settle": 24})
 
 # MTP verification: four query rows per step (the token and three drafts),
 # row 0 exactly the 50K single-layer scores, rows 1-3 close to it

@@ -251,10 +251,18 @@ static __device__ __noinline__ uint32_t compact_queue(const LayerView& L, uint32
   return total;
 }
 
+// No work for the CTAs that wait while CTA 0 picks the victims.
+struct NoIdleWork {
+  __device__ void operator()(uint32_t, uint32_t) const {}
+};
+
 // kLru: the layer's policy (KVO_POLICY_LRU, else KVO_POLICY_CIRCULAR); each
 // policy gets its own kernel so that neither carries the other's code.
-template <bool kLru>
-__device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_smem) {
+// idle(w, nw): called by every CTA but CTA 0 while CTA 0 picks the victims
+// (w = this CTA's first warp among nw warps of those CTAs, all of them
+// calling with the same nw); it must not touch the resolve's state.
+template <bool kLru, typename IdleWork = NoIdleWork>
+__device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_smem, IdleWork idle = IdleWork()) {
   __shared__ uint32_t scratch[2][2 * kWarps + 2];
   __shared__ uint32_t table[kMaxCluster][4];       // per CTA: (idx not increasing, misses)
   __shared__ uint32_t table2[kMaxCluster][4];      // idx not increasing: (unique misses, used hit slots)
@@ -649,6 +657,7 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
       }
     }
   }
+  if (r != 0) idle((r - 1u) * kWarps + warp, (C - 1u) * kWarps);
   cluster_sync();                                   // B3: victims, bits and queue positions delivered
 
   // ---------------------------------------------------------------- P4

@@ -38,22 +38,12 @@ struct StepArgs {
   uint32_t topk_bytes;        // dynamic shared memory of the top-K phase (resident keys or candidates)
 };
 
-// One layer's step, run by one cluster: append, select (with scores), resolve.
+// One layer's step, run by one cluster: select (with scores), resolve, append.
 template <bool kResident, bool kLru>
 __device__ __forceinline__ void decode_body(const StepArgs& s, uint8_t* dyn_smem, RadixSmem* rsm) {
-  const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const uint32_t rank = cluster_rank(), C = cluster_size();
+  const uint32_t tid = threadIdx.x, lane = tid & 31;
+  const uint32_t rank = cluster_rank();
   constexpr uint32_t kVec = KVO_ROW_BYTES / 16;
-
-  // append: one warp per new row, spread over the cluster; to the recent
-  // ring when there is one, else to the host history
-  const LayerView& L = s.R.L;
-  for (uint32_t i = rank * kWarps + warp; i < s.r; i += C * kWarps) {
-    uint4* dst = L.ring_rows ? reinterpret_cast<uint4*>(L.recent) + (size_t)((s.old_len + i) & (L.ring_rows - 1u)) * kVec
-                             : s.hist_dst + (size_t)i * kVec;
-    dst[lane] = s.new_rows[(size_t)i * kVec + lane];
-    if (lane < kVec - 32) dst[32 + lane] = s.new_rows[(size_t)i * kVec + 32 + lane];
-  }
 
   uint8_t* rdyn = dyn_smem + s.topk_bytes;
   if (s.scores) {
@@ -62,12 +52,25 @@ __device__ __forceinline__ void decode_body(const StepArgs& s, uint8_t* dyn_smem
     const uint32_t kchunk = s.R.kchunk;
     topk_body<kResident>(s.scores, s.n, s.R.k, dyn_smem, s.topk_bytes, rsm, [&](uint32_t pos, uint32_t out) {
       s.idx[out] = (int32_t)pos;
+      prefetch_l2(&s.R.L.pos2slot[pos]);           // the resolve looks it up next
       const uint32_t q = out / kchunk;               // CTA q + 1 resolves entries [q * kchunk, ...)
       dsmem_st_u32(dsmem_addr(&sel[out - q * kchunk], q + 1), pos);
     });
     cluster_sync();                                // every selected position delivered
   }
-  resolve_body<kLru>(s.R, rdyn);
+  // The append: one warp per new row, to the recent ring when there is one,
+  // else to the host history.  This call reads these rows from their device
+  // copy (the resolve's fresh rows), so they are written while CTAs 1..C-1
+  // wait for CTA 0's victims rather than by CTA 0 ahead of the top-K.
+  const LayerView& L = s.R.L;
+  resolve_body<kLru>(s.R, rdyn, [&](uint32_t w, uint32_t nw) {
+    for (uint32_t i = w; i < s.r; i += nw) {
+      uint4* dst = L.ring_rows ? reinterpret_cast<uint4*>(L.recent) + (size_t)((s.old_len + i) & (L.ring_rows - 1u)) * kVec
+                               : s.hist_dst + (size_t)i * kVec;
+      dst[lane] = s.new_rows[(size_t)i * kVec + lane];
+      if (lane < kVec - 32) dst[32 + lane] = s.new_rows[(size_t)i * kVec + 32 + lane];
+    }
+  });
   if (rank == 0 && tid == 0) s.R.L.counters[1] = s.R.len;
 }
 

@@ -434,12 +434,63 @@ def run_gpu_arm(args, w, rank, world):
             "clocks": clk, "launches": launches, "status": status, "idx_hist": idx_hist}
 
 
+def run_e2e_host_step(args, w, steps):
+    """One layer, one query row: every step is one kvo_decode_step_host call
+    on pinned host buffers (scores and the new row in; idx and the gathered
+    rows out), the copies inside the step's events.  The indexer stand-in
+    (the carry boost from the previous step's selection) builds the step's
+    scores in pinned memory before the events, as an indexer would hand them
+    over; its arithmetic is the float32 add of the device path."""
+    import torch
+    from gather_radix_top_gb300 import kvo
+    ctx = kvo.Context(1, w.history_cap, w.hot_rows)
+    if args.policy == "circular":
+        ctx.set_policy(kvo.POLICY_CIRCULAR)
+    if args.ring:
+        ctx.set_recent_ring(args.ring)
+    ctx.set_gather_mode({"loads": kvo.GATHER_LOADS, "staged": kvo.GATHER_STAGED,
+                         "auto": kvo.GATHER_AUTO}[args.gather], args.auto_miss_pct)
+    ctx.append_rows(0, W.rows(w, 0, 0, w.n0))
+    a = w.appends_per_step
+    new = torch.from_numpy(W.rows(w, 0, w.n0, steps * a)).pin_memory() if a else None
+    nmax = w.n_at(steps - 1)
+    sc_host = torch.empty(nmax, dtype=torch.float32).pin_memory()
+    idx_h = torch.empty(w.k, dtype=torch.int32).pin_memory()
+    out_h = torch.empty((w.k, ROW), dtype=torch.uint8).pin_memory()
+    bf_h = torch.empty((w.k, 576), dtype=torch.int16).pin_memory() if w.bf16 else None
+    flush = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
+    prev, evs = None, []
+    for s in range(steps):
+        n = w.n_at(s)
+        sc_host[:n].numpy()[:] = W.apply_carry(W.base_scores(w, 0, s, n), prev, W.carry_draw(w, 0, s),
+                                               w.carry_boost)
+        flush.zero_()
+        ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        ev[0].record()
+        ctx.decode_step_host(0, new[s * a:(s + 1) * a] if a else None, sc_host[:n], w.k, idx_h, out_h, bf_h)
+        ev[1].record()
+        torch.cuda.synchronize()                       # the host reads idx and rewrites the scores next
+        prev = idx_h.numpy().copy()
+        if s >= args.warmup:
+            evs.append(ev)
+    total = sum(x.elapsed_time(y) for x, y in evs) * 1e-3
+    nmean = float(np.mean([w.n_at(s) for s in range(args.warmup, steps)]))
+    ctx.close()
+    del flush
+    return {"value": round(args.steps * w.k / total, 1), "unit": "rows/s",
+            "h2d_bytes_per_step": int(nmean * 4 + a * ROW),
+            "d2h_bytes_per_step": int(w.k * 4 + w.k * ROW + (w.k * 576 * 2 if w.bf16 else 0)),
+            "call": "kvo_decode_step_host"}
+
+
 def run_e2e(args, w):
     """Same steps through the public API with host inputs/outputs: scores and
     new rows from pinned host memory, gathered rows back to pinned host memory,
     copies inside each step's events."""
     import torch
     steps = args.warmup + args.steps
+    if w.layers == 1 and w.queries == 1 and not args.separate:
+        return run_e2e_host_step(args, w, steps)
     wl = GpuWorkload(w, layer_base=0, steps=steps, host_inputs=True, fused=not args.separate, policy=args.policy,
                      ring=args.ring, gather=args.gather, auto_miss_pct=args.auto_miss_pct)
     flush = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")

@@ -33,6 +33,14 @@ struct kvo_ctx {
   bool resolved = false;                 // a resolve has been enqueued (the policy is fixed from then on)
   uint32_t ring_rows = 0;                // recent ring rows per layer (0: appends go straight to RAM)
   std::vector<int64_t> ram_len;          // per layer: rows the host history (RAM) holds
+  struct {                               // kvo_decode_step_host's device staging
+    float* scores = nullptr;             // history_cap fp32
+    int32_t* idx = nullptr;              // KVO_MAX_K
+    uint8_t* out = nullptr;              // KVO_MAX_K rows
+    uint16_t* bf16 = nullptr;            // KVO_MAX_K dequantised rows (allocated on first use)
+    uint8_t* rows = nullptr;             // rows_cap new rows (grows)
+    int64_t rows_cap = 0;
+  } stage;
 };
 
 namespace {
@@ -54,6 +62,11 @@ void free_ctx(kvo_ctx* c) {
   for (uint8_t* h : c->hist_host) cudaFreeHost(h);
   cudaFree(c->counters);
   cudaFree(c->stats);
+  cudaFree(c->stage.scores);
+  cudaFree(c->stage.idx);
+  cudaFree(c->stage.out);
+  cudaFree(c->stage.bf16);
+  cudaFree(c->stage.rows);
   cudaFree(c->evlog);
   cudaFree(c->status);
   delete c;
@@ -480,29 +493,93 @@ kvo_status kvo_decode_layers(kvo_ctx* ctx, const kvo_layer_task* tasks, int32_t 
   return KVO_OK;
 }
 
-kvo_status kvo_decode_step(kvo_ctx* ctx, int32_t layer, const void* new_rows, int64_t r,
-                           const float* scores, int64_t n, int32_t k, int32_t* idx,
-                           void* out_rows, uint16_t* out_bf16, void* stream) {
+// Argument checks shared by kvo_decode_step and kvo_decode_step_host (the
+// buffers' memory kind is each caller's own check).
+static bool decode_step_args_ok(const kvo_ctx* ctx, int32_t layer, const void* new_rows, int64_t r,
+                                const float* scores, int64_t n, int32_t k, const int32_t* idx, const void* out_rows,
+                                const uint16_t* out_bf16) {
   if (!ctx || layer < 0 || layer >= ctx->layers || r < 0 || !scores || !idx || k < 1 || k > KVO_MAX_K ||
       n < k || n > INT32_MAX || k > ctx->hot_rows || (!out_rows && !out_bf16))
-    return KVO_EINVAL;
-  if ((out_rows && !aligned16(out_rows)) || (out_bf16 && !aligned16(out_bf16))) return KVO_EINVAL;
-  if (r > 0 && (!new_rows || !aligned16(new_rows) || !is_device_pointer(new_rows))) return KVO_EINVAL;
-  if (ctx->ring_rows && r > (int64_t)ctx->ring_rows - KVO_COPYBACK_BATCH) return KVO_EINVAL;
+    return false;
+  if (r > 0 && !new_rows) return false;
+  if (ctx->ring_rows && r > (int64_t)ctx->ring_rows - KVO_COPYBACK_BATCH) return false;
+  return ctx->length[layer] + r <= ctx->history_cap;
+}
+
+// The step on device buffers (arguments already checked).
+static kvo_status decode_step_enqueue(kvo_ctx* ctx, int32_t layer, const void* new_rows, int64_t r,
+                                      const float* scores, int64_t n, int32_t k, int32_t* idx, void* out_rows,
+                                      uint16_t* out_bf16, cudaStream_t stream) {
   const int64_t start = ctx->length[layer];
-  if (start + r > ctx->history_cap) return KVO_EINVAL;
   kvo::LayerView v = ctx->views[layer];
   v.evlog = ctx->evlog ? ctx->evlog + kEvlogStride * layer : nullptr;
   v.ram_len = (uint32_t)ctx->ram_len[layer];
   const cudaError_t e = kvo::launch_decode_step(v, r ? new_rows : nullptr, (uint32_t)r, (uint32_t)start, scores,
                                                 (uint32_t)n, (uint32_t)k, idx, static_cast<uint8_t*>(out_rows),
-                                                out_bf16, ctx->status, ctx->max_cluster,
-                                                static_cast<cudaStream_t>(stream));
+                                                out_bf16, ctx->status, ctx->max_cluster, stream);
   if (!ok(e)) return KVO_ECUDA;
   ctx->resolved = true;
   ctx->length[layer] = start + r;
   if (!ctx->ring_rows) ctx->ram_len[layer] = start + r;
-  return ok(ring_after_append(ctx, layer, static_cast<cudaStream_t>(stream))) ? KVO_OK : KVO_ECUDA;
+  return ok(ring_after_append(ctx, layer, stream)) ? KVO_OK : KVO_ECUDA;
+}
+
+kvo_status kvo_decode_step(kvo_ctx* ctx, int32_t layer, const void* new_rows, int64_t r,
+                           const float* scores, int64_t n, int32_t k, int32_t* idx,
+                           void* out_rows, uint16_t* out_bf16, void* stream) {
+  if (!decode_step_args_ok(ctx, layer, new_rows, r, scores, n, k, idx, out_rows, out_bf16)) return KVO_EINVAL;
+  if ((out_rows && !aligned16(out_rows)) || (out_bf16 && !aligned16(out_bf16))) return KVO_EINVAL;
+  if (r > 0 && (!aligned16(new_rows) || !is_device_pointer(new_rows))) return KVO_EINVAL;
+  return decode_step_enqueue(ctx, layer, new_rows, r, scores, n, k, idx, out_rows, out_bf16,
+                             static_cast<cudaStream_t>(stream));
+}
+
+kvo_status kvo_decode_step_host(kvo_ctx* ctx, int32_t layer, const void* new_rows, int64_t r,
+                                const float* scores, int64_t n, int32_t k, int32_t* idx,
+                                void* out_rows, uint16_t* out_bf16, void* stream) {
+  if (!decode_step_args_ok(ctx, layer, new_rows, r, scores, n, k, idx, out_rows, out_bf16)) return KVO_EINVAL;
+  if (is_device_pointer(scores) || is_device_pointer(idx) || (r > 0 && is_device_pointer(new_rows)) ||
+      (out_rows && is_device_pointer(out_rows)) || (out_bf16 && is_device_pointer(out_bf16)))
+    return KVO_EINVAL;
+  auto& st = ctx->stage;
+  // staging first (sized for the largest call), so that a failure enqueues nothing
+  bool good = true;
+  if (!st.scores) good = ok(cudaMalloc(&st.scores, sizeof(float) * (size_t)ctx->history_cap));
+  if (good && !st.idx) good = ok(cudaMalloc(&st.idx, sizeof(int32_t) * KVO_MAX_K));
+  if (good && !st.out) good = ok(cudaMalloc(&st.out, (size_t)KVO_MAX_K * KVO_ROW_BYTES));
+  if (good && out_bf16 && !st.bf16)
+    good = ok(cudaMalloc(&st.bf16, sizeof(uint16_t) * (size_t)KVO_MAX_K * KVO_DEQUANT_VALUES));
+  if (good && r > st.rows_cap) {
+    const int64_t cap = r > 2 * st.rows_cap ? r : 2 * st.rows_cap;
+    good = ok(cudaDeviceSynchronize());            // earlier steps may still read the old rows
+    if (good) {
+      cudaFree(st.rows);
+      st.rows = nullptr;
+      st.rows_cap = 0;
+      good = ok(cudaMalloc(&st.rows, (size_t)cap * KVO_ROW_BYTES));
+      if (good) st.rows_cap = cap;
+    }
+  }
+  if (!good) {
+    cudaGetLastError();
+    return KVO_ENOMEM;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (!ok(cudaMemcpyAsync(st.scores, scores, sizeof(float) * (size_t)n, cudaMemcpyHostToDevice, s)))
+    return KVO_ECUDA;
+  if (r > 0 && !ok(cudaMemcpyAsync(st.rows, new_rows, (size_t)r * KVO_ROW_BYTES, cudaMemcpyHostToDevice, s)))
+    return KVO_ECUDA;
+  const kvo_status rc = decode_step_enqueue(ctx, layer, st.rows, r, st.scores, n, k, st.idx,
+                                            out_rows ? st.out : nullptr, out_bf16 ? st.bf16 : nullptr, s);
+  if (rc != KVO_OK) return rc;
+  if (!ok(cudaMemcpyAsync(idx, st.idx, sizeof(int32_t) * (size_t)k, cudaMemcpyDeviceToHost, s))) return KVO_ECUDA;
+  if (out_rows &&
+      !ok(cudaMemcpyAsync(out_rows, st.out, (size_t)k * KVO_ROW_BYTES, cudaMemcpyDeviceToHost, s)))
+    return KVO_ECUDA;
+  if (out_bf16 && !ok(cudaMemcpyAsync(out_bf16, st.bf16, sizeof(uint16_t) * (size_t)k * KVO_DEQUANT_VALUES,
+                                      cudaMemcpyDeviceToHost, s)))
+    return KVO_ECUDA;
+  return KVO_OK;
 }
 
 kvo_status kvo_sync(kvo_ctx* ctx, void* stream) {

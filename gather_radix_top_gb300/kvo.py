@@ -28,7 +28,7 @@ KVO_OK, KVO_EINVAL, KVO_ENOMEM, KVO_ECUDA, KVO_ERANGE, KVO_EBUSY, KVO_ETIMEDOUT,
 EXPORTED = [
     "kvo_status_string", "kvo_create", "kvo_destroy", "kvo_append_rows", "kvo_select_topk",
     "kvo_select_topk_batch",
-    "kvo_resolve_gather", "kvo_resolve_gather_multi", "kvo_decode_step", "kvo_decode_layers", "kvo_sync", "kvo_get_stats", "kvo_history_length",
+    "kvo_resolve_gather", "kvo_resolve_gather_multi", "kvo_decode_step", "kvo_decode_step_host", "kvo_decode_layers", "kvo_sync", "kvo_get_stats", "kvo_history_length",
     "kvo_debug_dump_layer", "kvo_debug_record_evictions", "kvo_debug_evictions", "kvo_set_policy",
     "kvo_debug_layer_counters", "kvo_set_recent_ring", "kvo_flush_ring", "kvo_ram_length",
     "kvo_debug_read_history", "kvo_set_gather_mode",
@@ -95,6 +95,7 @@ def lib() -> ctypes.CDLL:
         "kvo_resolve_gather": (ctypes.c_int, [_vp, _i32, _vp, _i32, _vp, _vp, _vp]),
         "kvo_resolve_gather_multi": (ctypes.c_int, [_vp, _i32, _vp, _i32, _i32, _vp, _vp, _vp]),
         "kvo_decode_step": (ctypes.c_int, [_vp, _i32, _vp, _i64, _vp, _i64, _i32, _vp, _vp, _vp, _vp]),
+        "kvo_decode_step_host": (ctypes.c_int, [_vp, _i32, _vp, _i64, _vp, _i64, _i32, _vp, _vp, _vp, _vp]),
         "kvo_decode_layers": (ctypes.c_int, [_vp, ctypes.POINTER(kvo_layer_task), _i32, _i32, _vp]),
         "kvo_sync": (ctypes.c_int, [_vp, _vp]),
         "kvo_get_stats": (ctypes.c_int, [_vp, _i32, ctypes.POINTER(kvo_stats)]),
@@ -143,6 +144,20 @@ def _check(status: int, what: str) -> int:
     if status != KVO_OK:
         raise KvoError(status, what)
     return status
+
+
+def _host_ptr(t, dtype_name: str | None = None):
+    """data_ptr of a contiguous CPU tensor (None -> NULL); pinned memory gives
+    the host link's full rate."""
+    if t is None:
+        return None
+    if t.is_cuda:
+        raise ValueError("expected a CPU tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    if dtype_name is not None and str(t.dtype) != dtype_name:
+        raise ValueError(f"expected {dtype_name}, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
 
 
 def _dev_ptr(t, dtype_name: str | None = None):
@@ -236,6 +251,22 @@ def kvo_resolve_gather_multi(ctx: int, layer: int, idx, out_rows=None, out_bf16=
     _check(lib().kvo_resolve_gather_multi(ctx, layer, _dev_ptr(idx, "torch.int32"), idx.shape[0], idx.shape[1],
                                           _dev_ptr(out_rows, "torch.uint8"), _dev_ptr(out_bf16),
                                           _stream_ptr(stream)), "kvo_resolve_gather_multi")
+
+
+def kvo_decode_step_host(ctx: int, layer: int, new_rows, scores, k: int, idx, out_rows=None, out_bf16=None,
+                         stream=None):
+    """kvo_decode_step on CPU tensors (pinned for full speed): new_rows uint8
+    [r, 656] or None, scores fp32[n], idx int32[k] (output), out_rows uint8
+    [k, 656] and/or out_bf16 [k, 576].  Enqueued on `stream`: synchronise
+    before reading the outputs."""
+    if out_bf16 is not None and str(out_bf16.dtype) not in ("torch.bfloat16", "torch.int16"):
+        raise ValueError("out_bf16 must be bfloat16 or int16")
+    r = 0 if new_rows is None else new_rows.numel() // ROW_BYTES
+    _check(lib().kvo_decode_step_host(ctx, layer, _host_ptr(new_rows, "torch.uint8"), r,
+                                      _host_ptr(scores, "torch.float32"), scores.numel(), k,
+                                      _host_ptr(idx, "torch.int32"), _host_ptr(out_rows, "torch.uint8"),
+                                      _host_ptr(out_bf16), _stream_ptr(stream)), "kvo_decode_step_host")
+    return idx
 
 
 def kvo_decode_step(ctx: int, layer: int, new_rows, scores, k: int, idx=None, out_rows=None, out_bf16=None,
@@ -424,6 +455,9 @@ class Context:
 
     def decode_step(self, layer, new_rows, scores, k, idx=None, out_rows=None, out_bf16=None, stream=None):
         return kvo_decode_step(self.handle, layer, new_rows, scores, k, idx, out_rows, out_bf16, stream)
+
+    def decode_step_host(self, layer, new_rows, scores, k, idx, out_rows=None, out_bf16=None, stream=None):
+        return kvo_decode_step_host(self.handle, layer, new_rows, scores, k, idx, out_rows, out_bf16, stream)
 
     def decode_layers(self, tasks, k, stream=None):
         kvo_decode_layers(self.handle, tasks, k, stream)

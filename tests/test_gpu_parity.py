@@ -403,6 +403,73 @@ def test_decode_step_rejects_host_rows_and_bad_sizes(kvo):
     ctx.close()
 
 
+def test_decode_step_host_matches_device_buffers(kvo):
+    """kvo_decode_step_host (pinned CPU tensors, staged by the library) gives
+    the same selections, rows, bf16 rows and layer state as kvo_decode_step on
+    device tensors, step for step (appends, carry-over, bf16 on)."""
+    import torch
+    w = W.K50.scaled(steps=12)
+    ctxs = [kvo.Context(1, w.history_cap, w.hot_rows) for _ in range(2)]
+    for c in ctxs:
+        c.append_rows(0, W.rows(w, 0, 0, w.n0))
+    extra = W.rows(w, 0, w.n0, w.history_cap - w.n0)
+    k = w.k
+    d_idx = torch.empty(k, dtype=torch.int32, device="cuda")
+    d_out = torch.empty((k, O.ROW_BYTES), dtype=torch.uint8, device="cuda")
+    d_bf = torch.empty((k, O.DEQUANT_VALUES), dtype=torch.int16, device="cuda")
+    h_idx = torch.empty(k, dtype=torch.int32).pin_memory()
+    h_out = torch.empty((k, O.ROW_BYTES), dtype=torch.uint8).pin_memory()
+    h_bf = torch.empty((k, O.DEQUANT_VALUES), dtype=torch.int16).pin_memory()
+    prev = None
+    for step in range(w.steps):
+        n = w.n_at(step)
+        sc = W.apply_carry(W.base_scores(w, 0, step, n), prev, W.carry_draw(w, 0, step), w.carry_boost)
+        row = extra[step:step + 1]
+        ctxs[0].decode_step(0, torch.from_numpy(row).cuda(), torch.from_numpy(sc).cuda(), k, d_idx, d_out, d_bf)
+        ctxs[1].decode_step_host(0, torch.from_numpy(row).pin_memory(), torch.from_numpy(sc).pin_memory(), k,
+                                 h_idx, h_out, h_bf)
+        assert ctxs[0].sync() == kvo.KVO_OK and ctxs[1].sync() == kvo.KVO_OK
+        np.testing.assert_array_equal(h_idx.numpy(), d_idx.cpu().numpy())
+        np.testing.assert_array_equal(h_out.numpy(), d_out.cpu().numpy())
+        np.testing.assert_array_equal(h_bf.numpy(), d_bf.cpu().numpy())
+        np.testing.assert_array_equal(h_idx.numpy(), O.select_topk(sc, k))
+        prev = h_idx.numpy().copy()
+    a, b = (c.dump_layer(0) for c in ctxs)
+    for key in ("pos2slot", "slot2pos", "last_use", "hot"):
+        np.testing.assert_array_equal(a[key], b[key])
+    assert ctxs[0].stats(0) == ctxs[1].stats(0)
+    assert ctxs[1].history_length(0) == w.n0 + w.steps
+    np.testing.assert_array_equal(ctxs[1].read_history(0, w.n0, w.steps), extra[:w.steps])
+    for c in ctxs:
+        c.close()
+
+
+def test_decode_step_host_rejects_device_buffers_and_bad_sizes(kvo):
+    import ctypes
+    import torch
+    ctx = kvo.Context(1, 100, 16)
+    ctx.append_rows(0, np.zeros((50, O.ROW_BYTES), np.uint8))
+    sc = torch.zeros(50).pin_memory()
+    idx = torch.empty(8, dtype=torch.int32).pin_memory()
+    out = torch.empty((8, O.ROW_BYTES), dtype=torch.uint8).pin_memory()
+    with pytest.raises(ValueError):
+        ctx.decode_step_host(0, None, sc.cuda(), 8, idx, out)       # binding refuses CUDA tensors
+    lib = kvo.lib()
+    d_sc = sc.cuda()
+    rc = lib.kvo_decode_step_host(ctypes.c_void_p(ctx.handle), 0, None, 0, ctypes.c_void_p(d_sc.data_ptr()), 50, 8,
+                                  ctypes.c_void_p(idx.data_ptr()), ctypes.c_void_p(out.data_ptr()), None, None)
+    assert rc == kvo.KVO_EINVAL                                       # device scores refused by the library too
+    with pytest.raises(kvo.KvoError):
+        ctx.decode_step_host(0, None, sc, 17, torch.empty(17, dtype=torch.int32), out)   # k > hot_rows
+    with pytest.raises(kvo.KvoError):
+        ctx.decode_step_host(0, torch.zeros((51, O.ROW_BYTES), dtype=torch.uint8), sc, 8, idx, out)  # past cap
+    with pytest.raises(kvo.KvoError):
+        ctx.decode_step_host(0, None, sc, 8, idx, None, None)        # no output
+    assert ctx.history_length(0) == 50
+    assert ctx.stats(0)["steps"] == 0
+    ctx.close()
+
+
 # ------------------------------------------------ multi-query rounds (MTP)
 def _mtp_run(kvo, w, steps, check_every=1, want_bf16=False):
     """Each step: append, nq top-K selections (row 0 from the score model,

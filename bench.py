@@ -437,7 +437,8 @@ def run_gpu_arm(args, w, rank, world):
 def run_e2e_host_step(args, w, steps):
     """One layer, one query row: every step is one kvo_decode_step_host call
     on pinned host buffers (scores and the new row in; idx and the gathered
-    rows out), the copies inside the step's events.  The indexer stand-in
+    rows out), which the step kernel reads and writes in place: every byte
+    crosses the host link inside the step's events.  The indexer stand-in
     (the carry boost from the previous step's selection) builds the step's
     scores in pinned memory before the events, as an indexer would hand them
     over; its arithmetic is the float32 add of the device path."""
@@ -480,7 +481,8 @@ def run_e2e_host_step(args, w, steps):
     return {"value": round(args.steps * w.k / total, 1), "unit": "rows/s",
             "h2d_bytes_per_step": int(nmean * 4 + a * ROW),
             "d2h_bytes_per_step": int(w.k * 4 + w.k * ROW + (w.k * 576 * 2 if w.bf16 else 0)),
-            "call": "kvo_decode_step_host"}
+            "call": "kvo_decode_step_host",
+            "transfer": "pinned host buffers read and written in place by the step kernel over the host link"}
 
 
 def run_e2e(args, w):

@@ -509,14 +509,14 @@ static bool decode_step_args_ok(const kvo_ctx* ctx, int32_t layer, const void* n
 // The step on device buffers (arguments already checked).
 static kvo_status decode_step_enqueue(kvo_ctx* ctx, int32_t layer, const void* new_rows, int64_t r,
                                       const float* scores, int64_t n, int32_t k, int32_t* idx, void* out_rows,
-                                      uint16_t* out_bf16, cudaStream_t stream) {
+                                      uint16_t* out_bf16, cudaStream_t stream, bool out_host = false) {
   const int64_t start = ctx->length[layer];
   kvo::LayerView v = ctx->views[layer];
   v.evlog = ctx->evlog ? ctx->evlog + kEvlogStride * layer : nullptr;
   v.ram_len = (uint32_t)ctx->ram_len[layer];
   const cudaError_t e = kvo::launch_decode_step(v, r ? new_rows : nullptr, (uint32_t)r, (uint32_t)start, scores,
                                                 (uint32_t)n, (uint32_t)k, idx, static_cast<uint8_t*>(out_rows),
-                                                out_bf16, ctx->status, ctx->max_cluster, stream);
+                                                out_bf16, ctx->status, ctx->max_cluster, stream, out_host);
   if (!ok(e)) return KVO_ECUDA;
   ctx->resolved = true;
   ctx->length[layer] = start + r;
@@ -534,6 +534,17 @@ kvo_status kvo_decode_step(kvo_ctx* ctx, int32_t layer, const void* new_rows, in
                              static_cast<cudaStream_t>(stream));
 }
 
+// The device address of page-locked host memory (the kernels read and write
+// it directly over the host link), or NULL for pageable memory.
+static void* mapped_host(const void* p) {
+  cudaPointerAttributes at;
+  if (!p || cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
+
 kvo_status kvo_decode_step_host(kvo_ctx* ctx, int32_t layer, const void* new_rows, int64_t r,
                                 const float* scores, int64_t n, int32_t k, int32_t* idx,
                                 void* out_rows, uint16_t* out_bf16, void* stream) {
@@ -541,15 +552,27 @@ kvo_status kvo_decode_step_host(kvo_ctx* ctx, int32_t layer, const void* new_row
   if (is_device_pointer(scores) || is_device_pointer(idx) || (r > 0 && is_device_pointer(new_rows)) ||
       (out_rows && is_device_pointer(out_rows)) || (out_bf16 && is_device_pointer(out_bf16)))
     return KVO_EINVAL;
+  // Page-locked buffers are used in place: the step reads the scores and the
+  // new rows and writes idx and the outputs over the host link itself, with
+  // no copy before or after.  Pageable (or, for rows, unaligned) buffers go
+  // through the context's device staging.
+  const float* d_scores = static_cast<const float*>(mapped_host(scores));
+  const void* d_rows = r > 0 ? mapped_host(new_rows) : nullptr;
+  if (d_rows && !aligned16(d_rows)) d_rows = nullptr;
+  int32_t* d_idx = static_cast<int32_t*>(mapped_host(idx));
+  void* d_out = out_rows ? mapped_host(out_rows) : nullptr;
+  if (d_out && !aligned16(d_out)) d_out = nullptr;
+  uint16_t* d_bf16 = out_bf16 ? static_cast<uint16_t*>(mapped_host(out_bf16)) : nullptr;
+  if (d_bf16 && !aligned16(d_bf16)) d_bf16 = nullptr;
   auto& st = ctx->stage;
   // staging first (sized for the largest call), so that a failure enqueues nothing
   bool good = true;
-  if (!st.scores) good = ok(cudaMalloc(&st.scores, sizeof(float) * (size_t)ctx->history_cap));
-  if (good && !st.idx) good = ok(cudaMalloc(&st.idx, sizeof(int32_t) * KVO_MAX_K));
-  if (good && !st.out) good = ok(cudaMalloc(&st.out, (size_t)KVO_MAX_K * KVO_ROW_BYTES));
-  if (good && out_bf16 && !st.bf16)
+  if (!d_scores && !st.scores) good = ok(cudaMalloc(&st.scores, sizeof(float) * (size_t)ctx->history_cap));
+  if (good && !d_idx && !st.idx) good = ok(cudaMalloc(&st.idx, sizeof(int32_t) * KVO_MAX_K));
+  if (good && out_rows && !d_out && !st.out) good = ok(cudaMalloc(&st.out, (size_t)KVO_MAX_K * KVO_ROW_BYTES));
+  if (good && out_bf16 && !d_bf16 && !st.bf16)
     good = ok(cudaMalloc(&st.bf16, sizeof(uint16_t) * (size_t)KVO_MAX_K * KVO_DEQUANT_VALUES));
-  if (good && r > st.rows_cap) {
+  if (good && r > 0 && !d_rows && r > st.rows_cap) {
     const int64_t cap = r > 2 * st.rows_cap ? r : 2 * st.rows_cap;
     good = ok(cudaDeviceSynchronize());            // earlier steps may still read the old rows
     if (good) {
@@ -565,19 +588,28 @@ kvo_status kvo_decode_step_host(kvo_ctx* ctx, int32_t layer, const void* new_row
     return KVO_ENOMEM;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (!ok(cudaMemcpyAsync(st.scores, scores, sizeof(float) * (size_t)n, cudaMemcpyHostToDevice, s)))
-    return KVO_ECUDA;
-  if (r > 0 && !ok(cudaMemcpyAsync(st.rows, new_rows, (size_t)r * KVO_ROW_BYTES, cudaMemcpyHostToDevice, s)))
-    return KVO_ECUDA;
-  const kvo_status rc = decode_step_enqueue(ctx, layer, st.rows, r, st.scores, n, k, st.idx,
-                                            out_rows ? st.out : nullptr, out_bf16 ? st.bf16 : nullptr, s);
+  if (!d_scores) {
+    if (!ok(cudaMemcpyAsync(st.scores, scores, sizeof(float) * (size_t)n, cudaMemcpyHostToDevice, s)))
+      return KVO_ECUDA;
+    d_scores = st.scores;
+  }
+  if (r > 0 && !d_rows) {
+    if (!ok(cudaMemcpyAsync(st.rows, new_rows, (size_t)r * KVO_ROW_BYTES, cudaMemcpyHostToDevice, s)))
+      return KVO_ECUDA;
+    d_rows = st.rows;
+  }
+  const bool out_mapped = d_out != nullptr;
+  const kvo_status rc = decode_step_enqueue(ctx, layer, d_rows, r, d_scores, n, k, d_idx ? d_idx : st.idx,
+                                            out_rows ? (out_mapped ? d_out : st.out) : nullptr,
+                                            out_bf16 ? (d_bf16 ? d_bf16 : st.bf16) : nullptr, s, out_mapped);
   if (rc != KVO_OK) return rc;
-  if (!ok(cudaMemcpyAsync(idx, st.idx, sizeof(int32_t) * (size_t)k, cudaMemcpyDeviceToHost, s))) return KVO_ECUDA;
-  if (out_rows &&
+  if (!d_idx && !ok(cudaMemcpyAsync(idx, st.idx, sizeof(int32_t) * (size_t)k, cudaMemcpyDeviceToHost, s)))
+    return KVO_ECUDA;
+  if (out_rows && !out_mapped &&
       !ok(cudaMemcpyAsync(out_rows, st.out, (size_t)k * KVO_ROW_BYTES, cudaMemcpyDeviceToHost, s)))
     return KVO_ECUDA;
-  if (out_bf16 && !ok(cudaMemcpyAsync(out_bf16, st.bf16, sizeof(uint16_t) * (size_t)k * KVO_DEQUANT_VALUES,
-                                      cudaMemcpyDeviceToHost, s)))
+  if (out_bf16 && !d_bf16 && !ok(cudaMemcpyAsync(out_bf16, st.bf16, sizeof(uint16_t) * (size_t)k * KVO_DEQUANT_VALUES,
+                                                 cudaMemcpyDeviceToHost, s)))
     return KVO_ECUDA;
   return KVO_OK;
 }

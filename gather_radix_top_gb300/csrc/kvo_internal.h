@@ -56,12 +56,14 @@ struct StepTask {
   int32_t* idx;                   // device int32[k]: written with scores, read without
   uint8_t* out_rows;
   uint16_t* out_bf16;
+  uint32_t out_host;              // out_rows is mapped host memory (plain stores, never read back)
 };
 cudaError_t launch_decode_layers(const StepTask* tasks, uint32_t ntasks, uint32_t k, uint32_t* status,
                                  int max_cluster, cudaStream_t stream);
 cudaError_t launch_decode_step(const LayerView& L, const void* new_rows, uint32_t r, uint32_t old_len,
                                const float* scores, uint32_t n, uint32_t k, int32_t* idx, uint8_t* out_rows,
-                               uint16_t* out_bf16, uint32_t* status, int max_cluster, cudaStream_t stream);
+                               uint16_t* out_bf16, uint32_t* status, int max_cluster, cudaStream_t stream,
+                               bool out_host = false);
 cudaError_t launch_append(const void* src_dev, uint8_t* hist_dev_dst, uint64_t bytes,
                           uint32_t* counters, uint32_t new_len, cudaStream_t stream);
 cudaError_t launch_ring_append(const void* src_dev, uint8_t* ring, uint32_t r, uint32_t start, uint32_t ring_mask,

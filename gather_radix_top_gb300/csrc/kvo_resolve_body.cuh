@@ -96,6 +96,9 @@ struct ResolveArgs {
   uint32_t len;
   const uint8_t* fresh;
   uint32_t fresh_from;
+  // out_rows is (mapped) host memory: written with plain stores only, and
+  // never read back (the fills take their rows from the rows' sources)
+  uint32_t out_host;
 };
 
 // The row of a missing position: for rows appended in the same fused launch
@@ -453,7 +456,10 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
     if (!gather_ok) {
       if (tid == 0) atomicOr(a.status, kFlagTimeout);
     } else {
-      if (a.out_rows && tid == 0) {                // this CTA's slice of the output is contiguous
+      if (a.out_rows && a.out_host) {              // host memory: plain 16-byte stores
+        uint4* o4 = reinterpret_cast<uint4*>(a.out_rows) + (size_t)jlo * kRowVec;
+        for (uint32_t i = tid; i < jcnt * kRowVec; i += kThreads) o4[i] = stage4[i];
+      } else if (a.out_rows && tid == 0) {         // this CTA's slice of the output is contiguous
         bulk_copy_s2g(a.out_rows + (size_t)jlo * KVO_ROW_BYTES, stage4, jcnt * (uint32_t)KVO_ROW_BYTES);
         bulk_commit();
       }
@@ -682,8 +688,9 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
       }
       continue;
     }
-    const uint4* src = a.out_rows ? reinterpret_cast<const uint4*>(a.out_rows) + (size_t)(jlo + jj) * kRowVec
-                                  : miss_row(a, hist4, p);
+    const uint4* src = a.out_rows && !a.out_host
+                           ? reinterpret_cast<const uint4*>(a.out_rows) + (size_t)(jlo + jj) * kRowVec
+                           : miss_row(a, hist4, p);
     const uint4 x = __ldcg(src + lane);
     uint4 y = make_uint4(0, 0, 0, 0);
     if (lane < kRowVec - 32) y = __ldcg(src + 32 + lane);

@@ -163,6 +163,7 @@ void build_step(const StepTask& t, uint32_t k, uint32_t* status, uint32_t C, Ste
   a.idx = t.idx;
   a.out_rows = t.out_rows;
   a.out_bf16 = t.out_bf16;
+  a.out_host = t.out_host;
   a.status = status;
   a.k = k;
   a.kchunk = (k + C - 2) / (C - 1);                 // CTA 0 keeps the LRU order, CTAs 1..C-1 the entries
@@ -225,12 +226,13 @@ cudaError_t launch(uint32_t C, uint32_t nclusters, size_t smem, cudaStream_t str
 
 cudaError_t launch_decode_step(const LayerView& L, const void* new_rows, uint32_t r, uint32_t old_len,
                                const float* scores, uint32_t n, uint32_t k, int32_t* idx, uint8_t* out_rows,
-                               uint16_t* out_bf16, uint32_t* status, int max_cluster, cudaStream_t stream) {
+                               uint16_t* out_bf16, uint32_t* status, int max_cluster, cudaStream_t stream,
+                               bool out_host) {
   int cl = 0;
   cudaError_t e = step_init(&cl);
   if (e != cudaSuccess) return e;
   const uint32_t C = (uint32_t)(cl < max_cluster ? cl : max_cluster);
-  const StepTask t = {L, new_rows, r, old_len, scores, n, idx, out_rows, out_bf16};
+  const StepTask t = {L, new_rows, r, old_len, scores, n, idx, out_rows, out_bf16, out_host ? 1u : 0u};
   StepArgs s;
   size_t need_res = 0, need_stream = 0;
   uint32_t stream_topk = 0;

@@ -304,19 +304,21 @@ kvo_status kvo_decode_step(kvo_ctx* ctx, int32_t layer, const void* new_rows, in
 
 /*
  * kvo_decode_step_host - kvo_decode_step with host buffers, for a caller
- * whose inputs and outputs live in host memory: the call copies new_rows
- * and scores into the context's device staging, runs the step there, and
- * copies idx, out_rows and out_bf16 back, all in order on `stream`.  It
- * returns once the work is enqueued: synchronise the stream (kvo_sync)
- * before reading the outputs or rewriting the inputs.  Pinned host memory
- * gives the host link's full rate; pageable memory works, more slowly.
+ * whose inputs and outputs live in host memory.  Page-locked (pinned)
+ * buffers are used in place: the step reads the scores and the new rows and
+ * writes idx and the outputs over the host link itself, with no copy before
+ * or after.  Pageable buffers (and row buffers not 16-byte aligned) go
+ * through device staging owned by the context: copied in before the step,
+ * out after it.  Everything is in order on `stream`, and the call returns
+ * once the work is enqueued: synchronise the stream (kvo_sync) before
+ * reading the outputs or rewriting the inputs.
  *   new_rows  host uint8[r*656], or NULL with r = 0.
  *   scores    host fp32[n].
  *   idx       host int32[k] receives the selection (ascending positions).
  *   out_rows  host uint8[k*656] or NULL; out_bf16 host uint16[k*576] or
  *             NULL; at least one.
- * The staging (scores, rows, idx and outputs) is allocated on first use and
- * grows with n, r and k: KVO_ENOMEM if it cannot be.  One staging set per
+ * The staging a call needs (scores, rows, idx and outputs) is allocated on
+ * first use and grows with r: KVO_ENOMEM if it cannot be.  One staging set per
  * context: calls on different streams must not overlap.  Errors as for
  * kvo_decode_step; nothing is changed or enqueued on an error.
  */

@@ -403,11 +403,14 @@ def test_decode_step_rejects_host_rows_and_bad_sizes(kvo):
     ctx.close()
 
 
-def test_decode_step_host_matches_device_buffers(kvo):
-    """kvo_decode_step_host (pinned CPU tensors, staged by the library) gives
-    the same selections, rows, bf16 rows and layer state as kvo_decode_step on
-    device tensors, step for step (appends, carry-over, bf16 on)."""
+@pytest.mark.parametrize("pinned", [True, False])
+def test_decode_step_host_matches_device_buffers(kvo, pinned):
+    """kvo_decode_step_host gives the same selections, rows, bf16 rows and
+    layer state as kvo_decode_step on device tensors, step for step (appends,
+    carry-over, bf16 on): pinned CPU tensors are read and written in place by
+    the kernel, pageable ones go through the context's staging."""
     import torch
+    pin = (lambda t: t.pin_memory()) if pinned else (lambda t: t)
     w = W.K50.scaled(steps=12)
     ctxs = [kvo.Context(1, w.history_cap, w.hot_rows) for _ in range(2)]
     for c in ctxs:
@@ -417,17 +420,16 @@ def test_decode_step_host_matches_device_buffers(kvo):
     d_idx = torch.empty(k, dtype=torch.int32, device="cuda")
     d_out = torch.empty((k, O.ROW_BYTES), dtype=torch.uint8, device="cuda")
     d_bf = torch.empty((k, O.DEQUANT_VALUES), dtype=torch.int16, device="cuda")
-    h_idx = torch.empty(k, dtype=torch.int32).pin_memory()
-    h_out = torch.empty((k, O.ROW_BYTES), dtype=torch.uint8).pin_memory()
-    h_bf = torch.empty((k, O.DEQUANT_VALUES), dtype=torch.int16).pin_memory()
+    h_idx = pin(torch.empty(k, dtype=torch.int32))
+    h_out = pin(torch.empty((k, O.ROW_BYTES), dtype=torch.uint8))
+    h_bf = pin(torch.empty((k, O.DEQUANT_VALUES), dtype=torch.int16))
     prev = None
     for step in range(w.steps):
         n = w.n_at(step)
         sc = W.apply_carry(W.base_scores(w, 0, step, n), prev, W.carry_draw(w, 0, step), w.carry_boost)
         row = extra[step:step + 1]
         ctxs[0].decode_step(0, torch.from_numpy(row).cuda(), torch.from_numpy(sc).cuda(), k, d_idx, d_out, d_bf)
-        ctxs[1].decode_step_host(0, torch.from_numpy(row).pin_memory(), torch.from_numpy(sc).pin_memory(), k,
-                                 h_idx, h_out, h_bf)
+        ctxs[1].decode_step_host(0, pin(torch.from_numpy(row)), pin(torch.from_numpy(sc)), k, h_idx, h_out, h_bf)
         assert ctxs[0].sync() == kvo.KVO_OK and ctxs[1].sync() == kvo.KVO_OK
         np.testing.assert_array_equal(h_idx.numpy(), d_idx.cpu().numpy())
         np.testing.assert_array_equal(h_out.numpy(), d_out.cpu().numpy())

@@ -98,8 +98,11 @@ TINY = Workload("tiny", 0, 1, layers=1, n0=4096, hot_rows=1024, k=256, steps=16,
                 appends_per_step=0, carry=128)
 K50 = Workload("50k_single_layer", 1, 2, layers=1, n0=50_023, hot_rows=32_768, k=2048,
                steps=1024, appends_per_step=1, carry=1229, recency_amp=2.0)
+# the 78 layers' first steps after loading 2.5 GB of host history are slow
+# (18.7 ms, 16.7 ms, then ~8 steps down to the steady ~0.25 ms): "settle"
 STACK = Workload("50k_full_stack", 2, 3, layers=78, n0=50_023, hot_rows=32_768, k=2048,
-                 steps=256, appends_per_step=1, select_every=4, carry=1229, recency_amp=2.0)
+                 steps=256, appends_per_step=1, select_every=4, carry=1229, recency_amp=2.0,
+                 extra={"settle": 16})
 # "settle": untimed steps before a timed run's warm-up (the 32,768-slot hot
 # cache fills in 16 steps of 2,048 misses; the GPU's view of the 5.5 GB host
 # history settles in about as many more)

@@ -485,6 +485,88 @@ def run_e2e_host_step(args, w, steps):
             "transfer": "pinned host buffers read and written in place by the step kernel over the host link"}
 
 
+def run_e2e_layers(args, w, steps):
+    """Several layers, one query row: every step is the two kvo_decode_layers
+    calls of the device path (the selecting layers, then the layers reusing
+    their selection) on device buffers; inside the step's events the scores
+    of all selecting layers and every layer's new rows come in from pinned
+    host memory (one contiguous copy each) and every selecting layer's idx and
+    the last layer's rows go back.  The indexer stand-in builds the scores in
+    pinned memory before the events, from the selections the previous step
+    returned, and the task arrays are built there too."""
+    import torch
+    from gather_radix_top_gb300 import kvo
+    ctx = kvo.Context(w.layers, w.history_cap, w.hot_rows)
+    if args.policy == "circular":
+        ctx.set_policy(kvo.POLICY_CIRCULAR)
+    if args.ring:
+        ctx.set_recent_ring(args.ring)
+    ctx.set_gather_mode({"loads": kvo.GATHER_LOADS, "staged": kvo.GATHER_STAGED,
+                         "auto": kvo.GATHER_AUTO}[args.gather], args.auto_miss_pct)
+    for l in range(w.layers):
+        ctx.append_rows(l, W.rows(w, l, 0, w.n0))
+    sel = w.selecting_layers()
+    nsel, a, k = len(sel), w.appends_per_step, w.k
+    nmax = w.n_at(steps - 1)
+    sc_host = torch.empty(nsel * nmax, dtype=torch.float32).pin_memory()
+    sc_dev = torch.empty(nsel * nmax, dtype=torch.float32, device="cuda")
+    new_host = new_dev = None
+    if a:                                             # [step, layer, row]: one contiguous block per step
+        rows = np.stack([W.rows(w, l, w.n0, steps * a) for l in range(w.layers)])   # [layer, step*a + j]
+        new_host = torch.from_numpy(np.ascontiguousarray(
+            rows.reshape(w.layers, steps, a, ROW).transpose(1, 0, 2, 3)).reshape(steps, w.layers * a, ROW)).pin_memory()
+        new_dev = torch.empty((w.layers * a, ROW), dtype=torch.uint8, device="cuda")
+    idx_dev = torch.empty((2, nsel, k), dtype=torch.int32, device="cuda")
+    idx_host = torch.empty((nsel, k), dtype=torch.int32).pin_memory()
+    out_dev = torch.empty((w.layers, k, ROW), dtype=torch.uint8, device="cuda")
+    bf_dev = torch.empty((w.layers, k, 576), dtype=torch.int16, device="cuda") if w.bf16 else None
+    out_host = torch.empty((k, ROW), dtype=torch.uint8).pin_memory()
+    flush = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
+    prev, evs = [None] * nsel, []
+    for s in range(steps):
+        n, par = w.n_at(s), s & 1
+        sch = sc_host[:nsel * n].view(nsel, n).numpy()
+        for i, l in enumerate(sel):
+            sch[i] = W.apply_carry(W.base_scores(w, l, s, n), prev[i], W.carry_draw(w, l, s), w.carry_boost)
+        groups = {True: [], False: []}
+        for l in range(w.layers):
+            i = sel.index(w.source_layer(l))
+            t = {"layer": l, "idx": idx_dev[par, i], "out_rows": out_dev[l]}
+            if bf_dev is not None:
+                t["out_bf16"] = bf_dev[l]
+            if a:
+                t["new_rows"] = new_dev[l * a:(l + 1) * a]
+            if l in sel:
+                t["scores"] = sc_dev[i * n:(i + 1) * n]
+            groups[l in sel].append(t)
+        arr_sel = kvo.make_layer_tasks(groups[True])
+        arr_reuse = kvo.make_layer_tasks(groups[False]) if groups[False] else None
+        flush.zero_()
+        ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        ev[0].record()
+        sc_dev[:nsel * n].copy_(sc_host[:nsel * n], non_blocking=True)
+        if a:
+            new_dev.copy_(new_host[s], non_blocking=True)
+        ctx.decode_layers_prepared(arr_sel, k)
+        if arr_reuse is not None:
+            ctx.decode_layers_prepared(arr_reuse, k)
+        idx_host.copy_(idx_dev[par], non_blocking=True)
+        out_host.copy_(out_dev[w.layers - 1], non_blocking=True)
+        ev[1].record()
+        torch.cuda.synchronize()                       # the host reads idx and rewrites the scores next
+        prev = [idx_host[i].numpy().copy() for i in range(nsel)]
+        if s >= args.warmup:
+            evs.append(ev)
+    total = sum(x.elapsed_time(y) for x, y in evs) * 1e-3
+    nmean = float(np.mean([w.n_at(s) for s in range(args.warmup, steps)]))
+    ctx.close()
+    del flush
+    return {"value": round(args.steps * w.layers * k / total, 1), "unit": "rows/s",
+            "h2d_bytes_per_step": int(nsel * nmean * 4 + w.layers * a * ROW),
+            "d2h_bytes_per_step": int(nsel * k * 4 + k * ROW),
+            "call": "kvo_decode_layers x2, contiguous host copies in and out"}
+
+
 def run_e2e(args, w):
     """Same steps through the public API with host inputs/outputs: scores and
     new rows from pinned host memory, gathered rows back to pinned host memory,
@@ -493,6 +575,8 @@ def run_e2e(args, w):
     steps = args.warmup + args.steps
     if w.layers == 1 and w.queries == 1 and not args.separate:
         return run_e2e_host_step(args, w, steps)
+    if w.layers > 1 and w.queries == 1 and not args.separate:
+        return run_e2e_layers(args, w, steps)
     wl = GpuWorkload(w, layer_base=0, steps=steps, host_inputs=True, fused=not args.separate, policy=args.policy,
                      ring=args.ring, gather=args.gather, auto_miss_pct=args.auto_miss_pct)
     flush = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")

@@ -567,6 +567,73 @@ def run_e2e_layers(args, w, steps):
             "call": "kvo_decode_layers x2, contiguous host copies in and out"}
 
 
+def run_e2e_mtp(args, w, steps):
+    """One layer, several query rows (MTP verification rounds): per round the
+    device path's append, batched top-K of every row and multi-query resolve;
+    inside the round's events the new row and all query rows come in from
+    pinned host memory (one contiguous copy each) and every row's selection
+    and the round's rows go back.  The rows are built on the host before the
+    events: row 0 by the indexer stand-in (the carry boost from the previous
+    round's row-0 selection), rows 1.. as row 0 plus their float32 noise
+    added in float64 (the device path's arithmetic)."""
+    import torch
+    from gather_radix_top_gb300 import kvo
+    ctx = kvo.Context(1, w.history_cap, w.hot_rows)
+    if args.policy == "circular":
+        ctx.set_policy(kvo.POLICY_CIRCULAR)
+    if args.ring:
+        ctx.set_recent_ring(args.ring)
+    ctx.set_gather_mode({"loads": kvo.GATHER_LOADS, "staged": kvo.GATHER_STAGED,
+                         "auto": kvo.GATHER_AUTO}[args.gather], args.auto_miss_pct)
+    ctx.append_rows(0, W.rows(w, 0, 0, w.n0))
+    a, k, nq = w.appends_per_step, w.k, w.queries
+    nmax = w.n_at(steps - 1)
+    new_host = torch.from_numpy(W.rows(w, 0, w.n0, steps * a)).pin_memory() if a else None
+    new_dev = torch.empty((max(a, 1), ROW), dtype=torch.uint8, device="cuda")
+    q_host = torch.empty(nq * nmax, dtype=torch.float32).pin_memory()
+    q_dev = torch.empty(nq * nmax, dtype=torch.float32, device="cuda")
+    idx_dev = torch.empty((nq, k), dtype=torch.int32, device="cuda")
+    idx_host = torch.empty((nq, k), dtype=torch.int32).pin_memory()
+    out_dev = torch.empty((nq * k, ROW), dtype=torch.uint8, device="cuda")
+    out_host = torch.empty((nq * k, ROW), dtype=torch.uint8).pin_memory()
+    bf_dev = torch.empty((nq * k, 576), dtype=torch.int16, device="cuda") if w.bf16 else None
+    bf_host = torch.empty((nq * k, 576), dtype=torch.int16).pin_memory() if w.bf16 else None
+    flush = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
+    prev, evs = None, []
+    for s in range(steps):
+        n = w.n_at(s)
+        qh = q_host[:nq * n].view(nq, n).numpy()
+        qh[0] = W.apply_carry(W.base_scores(w, 0, s, n), prev, W.carry_draw(w, 0, s), w.carry_boost)
+        for q in range(1, nq):
+            qh[q] = W.query_scores(w, 0, s, q, qh[0])
+        flush.zero_()
+        ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        ev[0].record()
+        q_dev[:nq * n].copy_(q_host[:nq * n], non_blocking=True)
+        if a:
+            new_dev[:a].copy_(new_host[s * a:(s + 1) * a], non_blocking=True)
+            ctx.append_rows(0, new_dev[:a])
+        ctx.select_topk_batch(q_dev[:nq * n].view(nq, n), k, n, idx_dev)
+        ctx.resolve_gather_multi(0, idx_dev, out_dev, bf_dev)
+        idx_host.copy_(idx_dev, non_blocking=True)
+        out_host.copy_(out_dev, non_blocking=True)
+        if bf_dev is not None:
+            bf_host.copy_(bf_dev, non_blocking=True)
+        ev[1].record()
+        torch.cuda.synchronize()                       # the host reads idx and rewrites the rows next
+        prev = idx_host[0].numpy().copy()
+        if s >= args.warmup:
+            evs.append(ev)
+    total = sum(x.elapsed_time(y) for x, y in evs) * 1e-3
+    nmean = float(np.mean([w.n_at(s) for s in range(args.warmup, steps)]))
+    ctx.close()
+    del flush
+    return {"value": round(args.steps * nq * k / total, 1), "unit": "rows/s",
+            "h2d_bytes_per_step": int(nq * nmean * 4 + a * ROW),
+            "d2h_bytes_per_step": int(nq * k * 4 + nq * k * ROW + (nq * k * 576 * 2 if w.bf16 else 0)),
+            "call": "kvo_append_rows + kvo_select_topk_batch + kvo_resolve_gather_multi, contiguous host copies"}
+
+
 def run_e2e(args, w):
     """Same steps through the public API with host inputs/outputs: scores and
     new rows from pinned host memory, gathered rows back to pinned host memory,
@@ -577,6 +644,8 @@ def run_e2e(args, w):
         return run_e2e_host_step(args, w, steps)
     if w.layers > 1 and w.queries == 1 and not args.separate:
         return run_e2e_layers(args, w, steps)
+    if w.layers == 1 and w.queries > 1 and not args.separate:
+        return run_e2e_mtp(args, w, steps)
     wl = GpuWorkload(w, layer_base=0, steps=steps, host_inputs=True, fused=not args.separate, policy=args.policy,
                      ring=args.ring, gather=args.gather, auto_miss_pct=args.auto_miss_pct)
     flush = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")

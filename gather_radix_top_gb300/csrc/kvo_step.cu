@@ -12,6 +12,11 @@
 // shared memory.  Section "Separate historical capacity from the current
 // working set": later layers reuse a selection and keep their own KV, so a
 // layer's task may also bring its selection instead of scores.
+//
+// The step's results are those of append, then select, then resolve: the
+// selection sees the new rows, and the resolve reads them from their device
+// copy; their copy in the host history (or the recent ring) is written while
+// the resolve waits for CTA 0's victims.
 #include <cstdint>
 #include <cstring>
 

@@ -50,7 +50,8 @@ constexpr uint32_t kFirstBits = 11;                        // digit of the filte
 constexpr uint32_t kFirstBins = 1u << kFirstBits;
 constexpr uint32_t kLowBits = 32 - kFirstBits;             // key bits below that digit
 constexpr uint32_t kLowMask = (1u << kLowBits) - 1u;
-constexpr uint32_t kFilterMinBytes = 2 * kFirstBins * 4;   // the filtering pass's two histograms
+constexpr uint32_t kHistCopies = 4;                        // filtering histogram copies (warp mod 4)
+constexpr uint32_t kFilterMinBytes = (kHistCopies + 1) * kFirstBins * 4;   // the copies and the totals
 constexpr int kUnroll = 4;                                 // 4-key groups in flight per thread
 static_assert(kFirstBins % kThreads == 0, "whole bins per thread in the cut scan");
 
@@ -160,10 +161,12 @@ __device__ __forceinline__ void select_and_emit(Key4 key4, uint32_t count, uint3
   });
 }
 
-// Filtering pass (a): h, tot = two kFirstBins-word arrays in shared memory,
-// zeroed before a cluster barrier that precedes this call.  Adds this CTA's
-// histogram of the top kFirstBits key bits into every CTA's tot, then finds
-// the cut bucket of the `want` largest keys (out[0..2] as in find_cut).
+// Filtering pass (a): h = kHistCopies kFirstBins-word histograms, tot one
+// more, in shared memory, zeroed before a cluster barrier that precedes this
+// call.  Each warp adds into copy (warp mod kHistCopies), so that the few
+// bins that most keys fall into are not all contended by every warp; the
+// copies are summed, added into every CTA's tot, and the cut bucket of the
+// `want` largest keys found (out[0..2] as in find_cut).
 template <typename Load4>
 __device__ __forceinline__ void first_digit_cut(Load4 load4, uint32_t count, uint32_t want, uint32_t* h,
                                                 uint32_t* tot, uint32_t* warp_sum, uint32_t* out) {
@@ -174,8 +177,15 @@ __device__ __forceinline__ void first_digit_cut(Load4 load4, uint32_t count, uin
     uint32_t vm = 0;
 #pragma unroll
     for (int e = 0; e < 4; ++e) vm |= (uint32_t)(g < ngroups && 4 * g + e < count) << e;
-    hist_add_warp4(h, bins, vm);
+    hist_add_warp4(h + ((threadIdx.x >> 5) % kHistCopies) * kFirstBins, bins, vm);
   });
+  __syncthreads();
+  for (uint32_t b = threadIdx.x; b < kFirstBins; b += kThreads) {
+    uint32_t v = h[b];
+#pragma unroll
+    for (uint32_t c = 1; c < kHistCopies; ++c) v += h[c * kFirstBins + b];
+    h[b] = v;
+  }
   __syncthreads();
   for (uint32_t i = threadIdx.x; i < kFirstBins * C; i += kThreads) {
     const uint32_t v = h[i & (kFirstBins - 1u)];
@@ -326,7 +336,7 @@ __device__ __forceinline__ void topk_body(const float* __restrict__ scores, uint
   if (kResident) {
     for (uint32_t g = tid; g < (cnt + 3) / 4; g += kThreads) reinterpret_cast<uint4*>(keys)[g] = load4(g);
   } else if (cap) {
-    for (uint32_t b = tid; b < 2 * kFirstBins; b += kThreads) keys[b] = 0;   // the filtering histograms
+    for (uint32_t b = tid; b < (kHistCopies + 1) * kFirstBins; b += kThreads) keys[b] = 0;   // the filtering histograms
   }
   cluster_sync();                                  // histograms zeroed everywhere, keys in place
 
@@ -339,7 +349,7 @@ __device__ __forceinline__ void topk_body(const float* __restrict__ scores, uint
     select_and_emit(load4, cnt, k, 32, rsm, scratch, table, emit_at);
     return;
   }
-  first_digit_cut(load4, cnt, k, keys, keys + kFirstBins, &scratch[0][0], cutw);
+  first_digit_cut(load4, cnt, k, keys, keys + kHistCopies * kFirstBins, &scratch[0][0], cutw);
   const uint32_t bucket = cutw[0];
   const uint32_t total = cutw[1] + cutw[2];        // keys in or above the bucket, cluster-wide
   if (total <= cap) {

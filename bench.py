@@ -136,6 +136,18 @@ def algorithmic_bytes(w: W.Workload, n_avg: float, stats_delta: dict, resolve_la
             "append_host": ROW * w.appends_per_step, "hits": hits, "misses": misses, "fills": fills}
 
 
+def max_over_ranks(x: float, device: str = "cuda") -> float:
+    """The largest x over the ranks of the default process group (x itself
+    without one): a multi-GPU run reports the slowest replica's time."""
+    import torch
+    import torch.distributed as tdist
+    if not (tdist.is_available() and tdist.is_initialized()) or tdist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def dram_traffic(workload: str, kernel: str):
     """DRAM bytes per launch from the committed ncu capture, or None when the
     kernel's source has changed since the counters were taken."""
@@ -420,10 +432,7 @@ def run_gpu_arm(args, w, rank, world):
     status = wl.ctx.sync()
     step_ms = [a.elapsed_time(b) for a, b in evs]
     total_s = sum(step_ms) * 1e-3
-    if dist:
-        t = torch.tensor([total_s], dtype=torch.float64, device="cuda")
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        total_s = float(t.item())
+    total_s = max_over_ranks(total_s)
     kern = {kind: [a.elapsed_time(b) for a, b in pairs] for kind, pairs in kev.items()}
     delta = {f: sum(st1[l][f] - st0[l][f] for l in range(w.layers)) for f in st0[0]}
     idx_hist = wl.idx_hist.cpu().numpy()
@@ -859,12 +868,9 @@ def sessions_main(args, rank, world):
     cpu = run_sessions_oracle(sw, args.cpu_seconds) if rank == 0 and world == 1 else None
     g = run_sessions(args, rank, world)
     total_s = (sum(g["store_ms"]) + sum(g["restore_ms"])) * 1e-3
+    total_s = max_over_ranks(total_s)
     if world > 1:
-        import torch
         import torch.distributed as tdist
-        t = torch.tensor([total_s], dtype=torch.float64, device="cuda")
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        total_s = float(t.item())
         if rank != 0:
             tdist.destroy_process_group()
             return
@@ -995,13 +1001,9 @@ def probe_main(args, rank, world):
     total_s = sum(ms) * 1e-3
     delta = {f: st1[f] - st0[f] for f in st0}
     ctx.close()
-    if world > 1:
-        import torch.distributed as tdist
-        t = torch.tensor([total_s], dtype=torch.float64, device="cuda")
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        total_s = float(t.item())
-        if rank != 0:
-            return
+    total_s = max_over_ranks(total_s)
+    if world > 1 and rank != 0:
+        return
     hbm_peak, peak_src = load_peaks()
     ab = algorithmic_bytes(w, 0.0, delta, args.steps, 1)
     us = float(np.mean(ms)) * 1e3

@@ -66,3 +66,36 @@ def test_host_carry_boost_equals_the_device_path_ops(step):
     sc.index_add_(0, pos, torch.full((w.carry,), w.carry_boost, dtype=torch.float32))
     np.testing.assert_array_equal(host.view(np.uint32), sc.numpy().view(np.uint32))
     assert (host != base).sum() == w.carry
+
+
+def _report_max(rank, world, port, q):
+    import torch.distributed as tdist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    tdist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    q.put((rank, bench.max_over_ranks(10.0 + 3.5 * rank, device="cpu")))
+    tdist.barrier()
+    tdist.destroy_process_group()
+
+
+def test_max_over_ranks_two_gloo_ranks():
+    """A multi-GPU run reports the slowest replica's time: every rank gets the
+    maximum over the group (here two gloo ranks on the CPU)."""
+    import socket
+    import torch.multiprocessing as mp
+    sys.path.insert(0, str(ROOT))
+    import bench
+    assert bench.max_over_ranks(7.0, device="cpu") == 7.0            # no process group: the value itself
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_report_max, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert got == {0: 13.5, 1: 13.5}

@@ -433,25 +433,56 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
                       cta_miss * 100u >= a.stage_min_miss_pct * jcnt;   // uniform over the CTA
   bool gather_ok = true;
   if (staged) {
-    // One bulk copy per row into shared memory, all in flight at once;
-    // invalid entries get a zero row.
+    // One bulk copy per row in device memory (hot slots, this launch's new
+    // rows, the recent ring) into shared memory, all in flight at once.
+    // Rows of the host history come in through plain 16-byte loads, one warp
+    // per row: a bulk copy's first touch of a host page can take longer than
+    // the bounded wait (one took over 20 ms on a 50K-token layer), loads do
+    // not.  Invalid entries get a zero row.
+    const uint32_t host_rows = cta_unord_host >> 16;   // this CTA's entries served from the host history
     if (tid == 0) {
       mbar_init(&gbar, 1);
-      mbar_arrive_expect_tx(&gbar, (jcnt - cta_inv) * (uint32_t)KVO_ROW_BYTES);
+      mbar_arrive_expect_tx(&gbar, (jcnt - cta_inv - host_rows) * (uint32_t)KVO_ROW_BYTES);
     }
     __syncthreads();
     for (uint32_t jj = tid; jj < jcnt; jj += kThreads) {
       const int32_t slot = meta_slot[jj];
+      const bool from_host = slot == kSlotMiss && miss_from_host(a, meta_pos[jj]);
       const uint4* src = slot >= 0 ? hot4 + (size_t)slot * kRowVec
-                         : slot == kSlotMiss ? miss_row(a, hist4, meta_pos[jj])
-                                             : nullptr;
+                         : slot == kSlotMiss && !from_host ? miss_row(a, hist4, meta_pos[jj])
+                                                           : nullptr;
       if (src) {
         bulk_copy_g2s(stage4 + (size_t)jj * kRowVec, src, KVO_ROW_BYTES, &gbar);
-      } else {
+      } else if (!from_host) {
         for (uint32_t v = 0; v < kRowVec; ++v) stage4[(size_t)jj * kRowVec + v] = make_uint4(0, 0, 0, 0);
       }
     }
-    fence_proxy_async_smem();                       // the zero rows, before the bulk store reads them
+    if (host_rows) {                                // up to kRowsInFlight host rows per warp in flight
+      for (uint32_t jj0 = warp; jj0 < jcnt; jj0 += kWarps * kRowsInFlight) {
+        uint4 va[kRowsInFlight], vb[kRowsInFlight];
+        uint32_t hm = 0;                            // bit u: entry jj0 + u * kWarps is a host row (warp-uniform)
+#pragma unroll
+        for (uint32_t u = 0; u < kRowsInFlight; ++u) {
+          const uint32_t jj = jj0 + u * kWarps;
+          va[u] = make_uint4(0, 0, 0, 0);
+          vb[u] = make_uint4(0, 0, 0, 0);
+          if (jj < jcnt && meta_slot[jj] == kSlotMiss && miss_from_host(a, meta_pos[jj])) {
+            const uint4* src = miss_row(a, hist4, meta_pos[jj]);
+            va[u] = src[lane];
+            if (lane < kRowVec - 32) vb[u] = src[32 + lane];
+            hm |= 1u << u;
+          }
+        }
+#pragma unroll
+        for (uint32_t u = 0; u < kRowsInFlight; ++u) {
+          if (!((hm >> u) & 1u)) continue;
+          uint4* dst = stage4 + (size_t)(jj0 + u * kWarps) * kRowVec;
+          dst[lane] = va[u];
+          if (lane < kRowVec - 32) dst[32 + lane] = vb[u];
+        }
+      }
+    }
+    fence_proxy_async_smem();                       // the zero and host rows, before the bulk store reads them
     gather_ok = __syncthreads_and(mbar_wait_bounded(&gbar, 0, kWindowPolls));
     if (!gather_ok) {
       if (tid == 0) atomicOr(a.status, kFlagTimeout);

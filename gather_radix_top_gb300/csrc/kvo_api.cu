@@ -73,6 +73,8 @@ void free_ctx(kvo_ctx* c) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// fp32 scores and int32 positions are read and written as whole words
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 bool is_device_pointer(const void* p) {
   cudaPointerAttributes at;
@@ -333,6 +335,7 @@ kvo_status kvo_append_rows(kvo_ctx* ctx, int32_t layer, const void* rows, int64_
 kvo_status kvo_select_topk(kvo_ctx* ctx, const float* scores, int64_t n, int32_t k, int32_t* idx,
                            void* stream) {
   if (!ctx || !scores || !idx || k < 1 || k > KVO_MAX_K || n < k || n > INT32_MAX) return KVO_EINVAL;
+  if (!aligned4(scores) || !aligned4(idx)) return KVO_EINVAL;
   const cudaError_t e = kvo::launch_topk(scores, (uint32_t)n, (uint32_t)k, idx, ctx->max_cluster,
                                          static_cast<cudaStream_t>(stream));
   return ok(e) ? KVO_OK : KVO_ECUDA;
@@ -414,7 +417,7 @@ kvo_status kvo_debug_layer_counters(kvo_ctx* ctx, int32_t layer, uint32_t* out) 
 kvo_status kvo_select_topk_batch(kvo_ctx* ctx, const float* scores, int64_t n, int64_t ld, int32_t nq, int32_t k,
                                  int32_t* idx, void* stream) {
   if (!ctx || !scores || !idx || nq < 1 || nq > 65535 || k < 1 || k > KVO_MAX_K || n < k || n > INT32_MAX ||
-      ld < n)
+      ld < n || !aligned4(scores) || !aligned4(idx))
     return KVO_EINVAL;
   const cudaError_t e = kvo::launch_topk(scores, (uint32_t)n, (uint32_t)k, idx, ctx->max_cluster,
                                          static_cast<cudaStream_t>(stream), (uint32_t)nq, (uint64_t)ld);
@@ -423,7 +426,7 @@ kvo_status kvo_select_topk_batch(kvo_ctx* ctx, const float* scores, int64_t n, i
 
 kvo_status kvo_resolve_gather(kvo_ctx* ctx, int32_t layer, const int32_t* idx, int32_t k,
                               void* out_rows, uint16_t* out_bf16, void* stream) {
-  if (!ctx || layer < 0 || layer >= ctx->layers || !idx || k < 1 || k > KVO_MAX_K ||
+  if (!ctx || layer < 0 || layer >= ctx->layers || !idx || !aligned4(idx) || k < 1 || k > KVO_MAX_K ||
       k > ctx->hot_rows || (!out_rows && !out_bf16))
     return KVO_EINVAL;
   if ((out_rows && !aligned16(out_rows)) || (out_bf16 && !aligned16(out_bf16))) return KVO_EINVAL;
@@ -439,7 +442,7 @@ kvo_status kvo_resolve_gather(kvo_ctx* ctx, int32_t layer, const int32_t* idx, i
 
 kvo_status kvo_resolve_gather_multi(kvo_ctx* ctx, int32_t layer, const int32_t* idx, int32_t nq, int32_t k,
                                     void* out_rows, uint16_t* out_bf16, void* stream) {
-  if (!ctx || layer < 0 || layer >= ctx->layers || !idx || nq < 1 || k < 1 || k > KVO_MAX_K ||
+  if (!ctx || layer < 0 || layer >= ctx->layers || !idx || !aligned4(idx) || nq < 1 || k < 1 || k > KVO_MAX_K ||
       (int64_t)nq * k > KVO_MAX_ROUND || (int64_t)nq * k > ctx->hot_rows || (!out_rows && !out_bf16))
     return KVO_EINVAL;
   if ((out_rows && !aligned16(out_rows)) || (out_bf16 && !aligned16(out_bf16))) return KVO_EINVAL;
@@ -462,8 +465,8 @@ kvo_status kvo_decode_layers(kvo_ctx* ctx, const kvo_layer_task* tasks, int32_t 
   std::vector<bool> seen(ctx->layers, false);
   for (int32_t i = 0; i < ntasks; ++i) {
     const kvo_layer_task& t = tasks[i];
-    if (t.layer < 0 || t.layer >= ctx->layers || seen[t.layer] || t.r < 0 || !t.idx ||
-        (!t.out_rows && !t.out_bf16) || (t.out_rows && !aligned16(t.out_rows)) ||
+    if (t.layer < 0 || t.layer >= ctx->layers || seen[t.layer] || t.r < 0 || !t.idx || !aligned4(t.idx) ||
+        (t.scores && !aligned4(t.scores)) || (!t.out_rows && !t.out_bf16) || (t.out_rows && !aligned16(t.out_rows)) ||
         (t.out_bf16 && !aligned16(t.out_bf16)))
       return KVO_EINVAL;
     seen[t.layer] = true;
@@ -501,6 +504,7 @@ static bool decode_step_args_ok(const kvo_ctx* ctx, int32_t layer, const void* n
   if (!ctx || layer < 0 || layer >= ctx->layers || r < 0 || !scores || !idx || k < 1 || k > KVO_MAX_K ||
       n < k || n > INT32_MAX || k > ctx->hot_rows || (!out_rows && !out_bf16))
     return false;
+  if (!aligned4(scores) || !aligned4(idx)) return false;
   if (r > 0 && !new_rows) return false;
   if (ctx->ring_rows && r > (int64_t)ctx->ring_rows - KVO_COPYBACK_BATCH) return false;
   return ctx->length[layer] + r <= ctx->history_cap;

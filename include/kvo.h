@@ -190,7 +190,8 @@ kvo_status kvo_set_policy(kvo_ctx* ctx, int32_t policy);
  *           order.
  * Order: higher score first, equal scores -> lower position first; -0.0
  * equals +0.0; NaN ranks below every other value (NaNs tie by position).
- * Errors: KVO_EINVAL unless 0 < k <= n, k <= KVO_MAX_K and n < 2^31.
+ * Errors: KVO_EINVAL unless 0 < k <= n, k <= KVO_MAX_K and n < 2^31, or if
+ * scores or idx is not 4-byte aligned.
  */
 kvo_status kvo_select_topk(kvo_ctx* ctx, const float* scores, int64_t n, int32_t k,
                            int32_t* idx, void* stream);
@@ -203,7 +204,7 @@ kvo_status kvo_select_topk(kvo_ctx* ctx, const float* scores, int64_t n, int32_t
  *   scores  device fp32; row q starts at scores + q*ld (ld >= n).
  *   idx     device int32[nq*k]; row q's positions, ascending, at idx + q*k.
  * Errors: KVO_EINVAL unless nq >= 1, ld >= n and kvo_select_topk's limits
- * hold.
+ * hold (4-byte aligned scores and idx included).
  */
 kvo_status kvo_select_topk_batch(kvo_ctx* ctx, const float* scores, int64_t n, int64_t ld, int32_t nq, int32_t k,
                                  int32_t* idx, void* stream);
@@ -228,7 +229,8 @@ kvo_status kvo_select_topk_batch(kvo_ctx* ctx, const float* scores, int64_t n, i
  * An entry outside [0, length) gets a zero row, changes no state and latches
  * KVO_ERANGE for kvo_sync.
  * Errors: KVO_EINVAL if layer is out of range, k < 1, k > KVO_MAX_K,
- * k > hot_rows, both outputs are NULL or an output is misaligned.
+ * k > hot_rows, both outputs are NULL, an output is not 16-byte aligned or
+ * idx is not 4-byte aligned.
  */
 kvo_status kvo_resolve_gather(kvo_ctx* ctx, int32_t layer, const int32_t* idx, int32_t k,
                               void* out_rows, uint16_t* out_bf16, void* stream);
@@ -247,8 +249,8 @@ kvo_status kvo_resolve_gather(kvo_ctx* ctx, int32_t layer, const int32_t* idx, i
  * reads host memory, and a slot filled in this round is a hit source only
  * from the next round on; every slot the round uses is pinned.
  * Requires 1 <= nq, 1 <= k <= KVO_MAX_K, nq*k <= KVO_MAX_ROUND and
- * nq*k <= hot_rows, else KVO_EINVAL (also when the round does not fit the
- * shared memory of the cluster size in use).
+ * nq*k <= hot_rows and a 4-byte aligned idx, else KVO_EINVAL (also when the
+ * round does not fit the shared memory of the cluster size in use).
  */
 kvo_status kvo_resolve_gather_multi(kvo_ctx* ctx, int32_t layer, const int32_t* idx, int32_t nq, int32_t k,
                                     void* out_rows, uint16_t* out_bf16, void* stream);
@@ -270,7 +272,8 @@ kvo_status kvo_resolve_gather_multi(kvo_ctx* ctx, int32_t layer, const int32_t* 
  *   out_rows / out_bf16  as in kvo_resolve_gather (at least one).
  * The tasks of one call run concurrently: a task must not read an idx that
  * another task of the same call writes (select in one call, reuse in the
- * next).  KVO_EINVAL on a bad task (nothing enqueued).
+ * next).  KVO_EINVAL on a bad task (nothing enqueued), misaligned scores or
+ * idx (4 bytes) included.
  */
 typedef struct kvo_layer_task {
   int32_t layer;

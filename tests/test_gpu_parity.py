@@ -472,6 +472,41 @@ def test_decode_step_host_rejects_device_buffers_and_bad_sizes(kvo):
     ctx.close()
 
 
+def test_misaligned_scores_and_idx_are_refused(kvo):
+    """fp32 scores and int32 positions must be 4-byte aligned: every call
+    that takes them returns KVO_EINVAL for a misaligned pointer and changes
+    nothing."""
+    import ctypes
+    import torch
+    ctx = kvo.Context(1, 100, 16)
+    ctx.append_rows(0, np.zeros((50, O.ROW_BYTES), np.uint8))
+    buf = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+    base = buf.data_ptr()                              # 256-byte aligned
+    out = torch.empty((8, O.ROW_BYTES), dtype=torch.uint8, device="cuda")
+    lib = kvo.lib()
+    h = ctypes.c_void_p(ctx.handle)
+    vp = lambda a: ctypes.c_void_p(a)
+    scores_ok, scores_bad = vp(base), vp(base + 2)
+    idx_ok, idx_bad = vp(base + 2048), vp(base + 2048 + 1)
+    assert lib.kvo_select_topk(h, scores_bad, 50, 8, idx_ok, None) == kvo.KVO_EINVAL
+    assert lib.kvo_select_topk(h, scores_ok, 50, 8, idx_bad, None) == kvo.KVO_EINVAL
+    assert lib.kvo_select_topk_batch(h, scores_bad, 50, 50, 1, 8, idx_ok, None) == kvo.KVO_EINVAL
+    assert lib.kvo_resolve_gather(h, 0, idx_bad, 8, vp(out.data_ptr()), None, None) == kvo.KVO_EINVAL
+    assert lib.kvo_resolve_gather_multi(h, 0, idx_bad, 1, 8, vp(out.data_ptr()), None, None) == kvo.KVO_EINVAL
+    assert lib.kvo_decode_step(h, 0, None, 0, scores_bad, 50, 8, idx_ok, vp(out.data_ptr()), None,
+                               None) == kvo.KVO_EINVAL
+    assert lib.kvo_decode_step(h, 0, None, 0, scores_ok, 50, 8, idx_bad, vp(out.data_ptr()), None,
+                               None) == kvo.KVO_EINVAL
+    bad = kvo.make_layer_tasks([{"layer": 0, "idx": torch.empty(8, dtype=torch.int32, device="cuda"),
+                                 "out_rows": out}])
+    bad[0].idx = idx_bad
+    with pytest.raises(kvo.KvoError):
+        ctx.decode_layers_prepared(bad, 8)
+    assert ctx.sync() == kvo.KVO_OK
+    assert ctx.history_length(0) == 50 and ctx.stats(0)["steps"] == 0
+    ctx.close()
+
+
 # ------------------------------------------------ multi-query rounds (MTP)
 def _mtp_run(kvo, w, steps, check_every=1, want_bf16=False):
     """Each step: append, nq top-K selections (row 0 from the score model,

@@ -26,7 +26,11 @@
 //      missing position wins (dedupe without a table).  Then, while the
 //      cluster barrier completes, every row is gathered: hits from the hot
 //      slot (HBM), misses from host memory (zero-copy), 16-byte pieces, one
-//      warp per 656-byte row, plus the bf16 dequant.
+//      warp per 656-byte row, plus the bf16 dequant.  A CTA whose misses are
+//      a large enough share of its entries stages instead: its device-memory
+//      rows arrive by TMA bulk copies and its host rows by the same 16-byte
+//      loads, into shared memory, and its output slice leaves in one bulk
+//      store.
 //   P2 unique misses are ranked in j order.  When idx is strictly increasing
 //      (always true for kvo_select_topk output) every miss is unique and the
 //      counts published at the first barrier give every rank; otherwise the
@@ -41,8 +45,8 @@
 //      that miss.  CTA 0 also hands every CTA the queue position of its
 //      range's used slots.
 //   P4 the CTA holding a miss unmaps the evicted position, maps the new one,
-//      stamps last_use = t and copies the row (from the output just written)
-//      into the victim slot.
+//      stamps last_use = t and copies the row (its staged copy, the output
+//      just written, or its source) into the victim slot.
 //   P5 every CTA appends its range's used slots, in slot order, stamped t.
 // When the queue nears its capacity, its current entries are first copied,
 // in order, to the other of its two buffers (a compaction, once every many

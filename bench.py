@@ -26,6 +26,7 @@ with the max step time over ranks.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import json
 import os
 import statistics
@@ -136,6 +137,29 @@ def algorithmic_bytes(w: W.Workload, n_avg: float, stats_delta: dict, resolve_la
             "append_host": ROW * w.appends_per_step, "hits": hits, "misses": misses, "fills": fills}
 
 
+def gather_bytes(w: W.Workload, ab: dict) -> float:
+    """HBM bytes of one layer in the gather launch of kvo_decode_layers: its
+    positions and their pos2slot entries (4k + 4k), the hit slots' stamps and
+    rows (4 + 656 per hit), the output (R_out per entry) and this step's new
+    rows read from their device copy; misses cross the host link instead."""
+    k = w.k * w.queries
+    r_out = ROW + (2 * 576 if w.bf16 else 0)
+    return 8 * k + (4 + ROW) * ab["hits"] + r_out * k
+
+
+def finish_bytes(w: W.Workload, ab: dict) -> float:
+    """HBM bytes of one layer in the finish launch: the positions and their
+    claims again (8k), the LRU queue window and its slots' last_use (12 per
+    entry; up to 4,096), the map updates (16 per fill), the fills (656 read
+    from the output, 656 written to the slot), the scan of last_use for the
+    used slots (4 per slot) and their queue entries (8 per used slot), and
+    the new rows' copy to the host history (656 read per row)."""
+    k = w.k * w.queries
+    window = min(4096, 8 * w.hot_rows)
+    return (8 * k + 12 * window + (16 + 2 * ROW) * ab["fills"] + 4 * w.hot_rows
+            + 8 * (ab["hits"] + ab["fills"]) + ROW * w.appends_per_step)
+
+
 def max_over_ranks(x: float, device: str = "cuda") -> float:
     """The largest x over the ranks of the default process group (x itself
     without one): a multi-GPU run reports the slowest replica's time."""
@@ -170,11 +194,12 @@ class GpuWorkload:
 
     def __init__(self, w: W.Workload, layer_base: int, steps: int, host_inputs: bool = False,
                  fused: bool = True, policy: str = "lru", ring: int = 0, gather: str = "auto",
-                 auto_miss_pct: int = 5):
+                 auto_miss_pct: int = 5, layer_calls: int = 1):
         import torch
         from gather_radix_top_gb300 import kvo
         self.torch, self.kvo, self.w = torch, kvo, w
         self.steps = steps
+        self.layer_calls = layer_calls
         self.host_inputs = host_inputs
         self.ctx = kvo.Context(w.layers, w.history_cap, w.hot_rows)
         if policy == "circular":
@@ -235,6 +260,7 @@ class GpuWorkload:
         self.out_host = torch.empty((kq, ROW), dtype=torch.uint8).pin_memory() if host_inputs else None
         self.idx_hist = torch.zeros((steps, w.k), dtype=torch.int32, device=dev)
         self.launches = 0
+        self.api_host_s = 0.0                 # host time spent inside the kvo_decode_layers calls
         self.fused = fused
         # host-input runs stage each step's new rows on the device (H2D inside the step)
         self.new_stage = (torch.empty((w.layers, max(a, 1), ROW), dtype=torch.uint8, device=dev)
@@ -269,7 +295,10 @@ class GpuWorkload:
         return out, n
 
     def prepare_layers(self, s, sc):
-        """The two kvo_layer_task arrays of step s (device addresses only)."""
+        """The kvo_layer_task arrays of step s (device addresses only): one
+        array with every layer (a reusing layer names its source layer's
+        idx, which the call's selections fill first), or with
+        layer_calls = 2 the selecting layers and then the reusing ones."""
         w = self.w
         a = w.appends_per_step
         groups = {True: [], False: []}
@@ -282,6 +311,8 @@ class GpuWorkload:
             if l in self.sel:
                 t["scores"] = sc[l]
             groups[l in self.sel].append(t)
+        if self.layer_calls == 1:
+            return (self.kvo.make_layer_tasks(groups[True] + groups[False]), None)
         return (self.kvo.make_layer_tasks(groups[True]),
                 self.kvo.make_layer_tasks(groups[False]) if groups[False] else None)
 
@@ -317,9 +348,11 @@ class GpuWorkload:
             if a and self.host_inputs:
                 for l in range(w.layers):
                     self.new_stage[l, :a].copy_(self.new_rows_host[l, s * a:(s + 1) * a], non_blocking=True)
+            h0 = time.perf_counter()
             rec("layers", lambda: ctx.decode_layers_prepared(sel_arr, w.k))
             if reuse_arr is not None:
                 rec("layers", lambda: ctx.decode_layers_prepared(reuse_arr, w.k))
+            self.api_host_s += time.perf_counter() - h0
             if self.host_inputs:
                 self.out_host.copy_(self.out_layers[w.layers - 1], non_blocking=True)
             if ev:
@@ -394,8 +427,11 @@ def run_gpu_arm(args, w, rank, world):
     build.build()
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
     steps = args.warmup + args.steps
-    wl = GpuWorkload(w, layer_base=rank * w.layers, steps=steps, fused=not args.separate, policy=args.policy,
-                     ring=args.ring, gather=args.gather, auto_miss_pct=args.auto_miss_pct)
+    batched = not args.separate and w.queries == 1 and w.layers > 1
+    phase_steps = args.phase_steps if batched else 0
+    wl = GpuWorkload(w, layer_base=rank * w.layers, steps=steps + phase_steps, fused=not args.separate,
+                     policy=args.policy, ring=args.ring, gather=args.gather, auto_miss_pct=args.auto_miss_pct,
+                     layer_calls=args.layer_calls)
     flush = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
     dist = world > 1
     if dist:
@@ -405,11 +441,16 @@ def run_gpu_arm(args, w, rank, world):
         if dist:
             tdist.barrier()
 
-    # warm-up (untimed)
+    # settle phase and warm-up (not part of the timed region; each step's
+    # own events are kept, so that the cold start can be reported)
+    settle_ev = []
     for s in range(args.warmup):
         flush.zero_()
-        wl.step(s)
+        ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        wl.step(s, ev)
+        settle_ev.append(ev)
     torch.cuda.synchronize()
+    settle_ms = [a.elapsed_time(b) for a, b in settle_ev]
     st0 = {l: wl.ctx.stats(l) for l in range(w.layers)}
     clocks = ClockSampler(torch.cuda.current_device())
     evs, kev = [], {}
@@ -418,6 +459,8 @@ def run_gpu_arm(args, w, rank, world):
     clocks.start()
     t0 = time.perf_counter()
     launches0 = wl.launches
+    klaunch0 = wl.ctx.layers_launch_count() if wl.batched else 0
+    wl.api_host_s = 0.0
     for s in range(args.warmup, steps):
         flush.zero_()                      # L2 flush between timed steps (not timed)
         ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -428,8 +471,32 @@ def run_gpu_arm(args, w, rank, world):
     wall = time.perf_counter() - t0
     clk = clocks.stop()
     launches = wl.launches - launches0
+    if wl.batched:                         # the kernels kvo_decode_layers launched in the timed steps
+        launches = wl.ctx.layers_launch_count() - klaunch0
+    api_host_us = 1e6 * wl.api_host_s / max(1, steps - args.warmup)
     st1 = {l: wl.ctx.stats(l) for l in range(w.layers)}
     status = wl.ctx.sync()
+    phases = None
+    if phase_steps:
+        # A pass after the timed region, for the kernels' own durations:
+        # events between the three launches of every kvo_decode_layers call,
+        # which then run in order on one stream (no overlap of the call's
+        # parts, no early scheduling).
+        wl.ctx.set_phase_timing(True)
+        pst0 = {l: wl.ctx.stats(l) for l in range(w.layers)}
+        pev = []
+        for s in range(steps, steps + phase_steps):
+            flush.zero_()
+            ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            wl.step(s, ev)
+            pev.append(ev)
+        torch.cuda.synchronize()
+        (t_sel, t_gat, t_fin), calls = wl.ctx.layers_phase_times()
+        wl.ctx.set_phase_timing(False)
+        pst1 = {l: wl.ctx.stats(l) for l in range(w.layers)}
+        phases = {"calls": calls, "steps": phase_steps, "layers_select": t_sel, "layers_gather": t_gat,
+                  "layers_finish": t_fin, "step_ms": [a.elapsed_time(b) for a, b in pev],
+                  "delta": {f: sum(pst1[l][f] - pst0[l][f] for l in range(w.layers)) for f in pst0[0]}}
     step_ms = [a.elapsed_time(b) for a, b in evs]
     total_s = sum(step_ms) * 1e-3
     total_s = max_over_ranks(total_s)
@@ -440,7 +507,8 @@ def run_gpu_arm(args, w, rank, world):
     del flush
     torch.cuda.empty_cache()
     return {"total_s": total_s, "step_ms": step_ms, "kern_ms": kern, "delta": delta, "wall": wall,
-            "clocks": clk, "launches": launches, "status": status, "idx_hist": idx_hist}
+            "clocks": clk, "launches": launches, "status": status, "idx_hist": idx_hist, "settle_ms": settle_ms,
+            "phases": phases, "api_host_us": api_host_us}
 
 
 def run_e2e_host_step(args, w, steps):
@@ -495,9 +563,8 @@ def run_e2e_host_step(args, w, steps):
 
 
 def run_e2e_layers(args, w, steps):
-    """Several layers, one query row: every step is the two kvo_decode_layers
-    calls of the device path (the selecting layers, then the layers reusing
-    their selection) on device buffers; inside the step's events the scores
+    """Several layers, one query row: every step is the kvo_decode_layers
+    call(s) of the device path on device buffers; inside the step's events the scores
     of all selecting layers and every layer's new rows come in from pinned
     host memory (one contiguous copy each) and every selecting layer's idx and
     the last layer's rows go back.  The indexer stand-in builds the scores in
@@ -548,8 +615,11 @@ def run_e2e_layers(args, w, steps):
             if l in sel:
                 t["scores"] = sc_dev[i * n:(i + 1) * n]
             groups[l in sel].append(t)
-        arr_sel = kvo.make_layer_tasks(groups[True])
-        arr_reuse = kvo.make_layer_tasks(groups[False]) if groups[False] else None
+        if args.layer_calls == 1:                      # every layer in one call
+            arr_sel, arr_reuse = kvo.make_layer_tasks(groups[True] + groups[False]), None
+        else:
+            arr_sel = kvo.make_layer_tasks(groups[True])
+            arr_reuse = kvo.make_layer_tasks(groups[False]) if groups[False] else None
         flush.zero_()
         ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
         ev[0].record()
@@ -573,7 +643,10 @@ def run_e2e_layers(args, w, steps):
     return {"value": round(args.steps * w.layers * k / total, 1), "unit": "rows/s",
             "h2d_bytes_per_step": int(nsel * nmean * 4 + w.layers * a * ROW),
             "d2h_bytes_per_step": int(nsel * k * 4 + k * ROW),
-            "call": "kvo_decode_layers x2, contiguous host copies in and out"}
+            "call": "kvo_decode_layers x%d, contiguous host copies in and out" % args.layer_calls,
+            "to_host": "every selecting layer's idx (the indexer stand-in's next input) and the last layer's "
+                       "rows; the other layers' rows stay in HBM, where attention reads them",
+            "from_host": "the selecting layers' scores and every layer's new rows"}
 
 
 def run_e2e_mtp(args, w, steps):
@@ -1084,6 +1157,106 @@ def sweep_main(args):
     print(json.dumps(line))
 
 
+# -------------------------------------------------------------- cold start
+def _read_text(path):
+    try:
+        return open(path).read().strip()
+    except OSError:
+        return None
+
+
+def cold_start_main(args):
+    """The first decode steps of a fresh stack after its host history was
+    written, under several conditions, each on a fresh context: nothing
+    before step 0; every byte of the history read once from the GPU; one
+    16-byte GPU load per 4 KiB and per 64 KiB page; every byte read once by
+    the CPU.  Then step 0 alone with the selection confined to few or to many
+    distinct host pages (every layer resolving one given selection).  The
+    host's memory settings are recorded beside the numbers.  Nothing here is
+    timed for the headline: this locates where a cold start goes."""
+    import torch
+    from gather_radix_top_gb300 import build, kvo
+    build.build()
+    w = W.STACK.scaled(layers=args.layers or W.STACK.layers, steps=8)
+    L, k = w.layers, w.k
+    nsteps = 4
+    rows = [W.rows(w, l, 0, w.n0) for l in range(L)]
+    new = torch.from_numpy(np.stack([W.rows(w, l, w.n0, nsteps) for l in range(L)])).cuda()
+    sel = w.selecting_layers()
+    sink = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    hist_bytes = w.history_cap * ROW
+
+    def fresh():
+        ctx = kvo.Context(L, w.history_cap, w.hot_rows)
+        for l in range(L):
+            ctx.append_rows(l, rows[l])
+        torch.cuda.synchronize()
+        return ctx
+
+    def run_steps(ctx):
+        idx = {l: torch.empty(k, dtype=torch.int32, device="cuda") for l in sel}
+        out = torch.empty((L, k, ROW), dtype=torch.uint8, device="cuda")
+        prev, times = {}, []
+        for s in range(nsteps):
+            n = w.n_at(s)
+            sc = {l: torch.from_numpy(W.apply_carry(W.base_scores(w, l, s, n), prev.get(l), W.carry_draw(w, l, s),
+                                                    w.carry_boost)).cuda() for l in sel}
+            tasks = [{"layer": l, "idx": idx[w.source_layer(l)], "out_rows": out[l], "new_rows": new[l, s:s + 1],
+                      **({"scores": sc[l]} if l in sel else {})} for l in range(L)]
+            arr = kvo.make_layer_tasks(tasks)
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            ctx.decode_layers_prepared(arr, k)
+            b.record()
+            b.synchronize()
+            times.append(round(a.elapsed_time(b), 3))
+            prev = {l: idx[l].cpu().numpy() for l in sel}
+        assert ctx.sync() == 0
+        return times
+
+    res = {}
+    for name, pre in (("plain", None), ("gpu_read_every_byte", 16), ("gpu_touch_4k", 4096),
+                      ("gpu_touch_64k", 65536), ("cpu_read_every_byte", "cpu")):
+        ctx = fresh()
+        t0 = time.perf_counter()
+        if pre == "cpu":
+            acc = 0
+            for l in range(L):
+                buf = (ctypes.c_uint8 * hist_bytes).from_address(ctx.history_host(l))
+                acc ^= int(np.frombuffer(buf, dtype=np.uint64).sum() & 0xffff)
+        elif pre:
+            for l in range(L):
+                kvo.kvo_probe_host_touch(ctx.history_host(l), hist_bytes, pre, sink)
+            torch.cuda.synchronize()
+        pre_ms = round(1e3 * (time.perf_counter() - t0), 1)
+        res[name] = {"pass_ms": pre_ms if pre else 0.0, "step_ms": run_steps(ctx)}
+        ctx.close()
+    # step 0 with one given selection on every layer: contiguous rows (few
+    # pages) against rows one every 24 positions (a different 4 KiB page each)
+    for name, pos in (("pages_contiguous", np.arange(k)), ("pages_spread", np.arange(k) * 24)):
+        ctx = fresh()
+        idx = torch.from_numpy(pos.astype(np.int32)).cuda()
+        out = torch.empty((L, k, ROW), dtype=torch.uint8, device="cuda")
+        arr = kvo.make_layer_tasks([{"layer": l, "idx": idx, "out_rows": out[l]} for l in range(L)])
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        ctx.decode_layers_prepared(arr, k)
+        b.record()
+        b.synchronize()
+        assert ctx.sync() == 0
+        span = int(pos[-1]) * ROW + ROW
+        res[name] = {"step0_ms": round(a.elapsed_time(b), 3), "pages_4k_per_layer": len({int(p) * ROW // 4096 for p in pos}),
+                     "span_bytes_per_layer": span}
+        ctx.close()
+    line = {"workload": "cold_start", "layers": L, "history_bytes_per_layer": hist_bytes,
+            "page_size": os.sysconf("SC_PAGE_SIZE"),
+            "numa_balancing": _read_text("/proc/sys/kernel/numa_balancing"),
+            "compaction_proactiveness": _read_text("/proc/sys/vm/compaction_proactiveness"),
+            "thp": _read_text("/sys/kernel/mm/transparent_hugepage/enabled"), "results": res}
+    print(json.dumps(line))
+
+
 # -------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -1091,8 +1264,8 @@ def main():
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["kvo", "reference"], default="kvo")
-    ap.add_argument("--workload", choices=sorted(W.WORKLOADS) + [W.SESSIONS.name, "miss_rate_sweep"],
-                    default="50k_single_layer")
+    ap.add_argument("--workload", choices=sorted(W.WORKLOADS) + [W.SESSIONS.name, "miss_rate_sweep", "cold_start"],
+                    default="50k_full_stack")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--policy", choices=["lru", "circular"], default="lru", help="hot-cache replacement policy")
@@ -1101,12 +1274,24 @@ def main():
     ap.add_argument("--auto-miss-pct", type=int, default=5, help="--gather auto: staged from this miss share on")
     ap.add_argument("--sessions", type=int, default=None, help="session_evict_restore: number of sessions")
     ap.add_argument("--session-tokens", type=int, default=None, help="session_evict_restore: tokens per session")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="run the workload with this many layers (a smaller case of the same shape, for profiling)")
+    ap.add_argument("--settle", type=int, default=None, help="untimed settle steps (default: the workload's own)")
+    ap.add_argument("--phase-steps", type=int, default=30,
+                    help="multi-layer workloads: steps after the timed region run with CUDA events between the "
+                         "launches of every kvo_decode_layers call, for the kernels' own durations (roofline)")
+    ap.add_argument("--layer-calls", type=int, choices=[1, 2], default=1,
+                    help="multi-layer workloads: kvo_decode_layers calls per step (2: selecting layers, then "
+                         "the layers reusing their selection)")
     ap.add_argument("--separate", action="store_true",
                     help="time kvo_append_rows + kvo_select_topk + kvo_resolve_gather instead of kvo_decode_step")
     args = ap.parse_args()
 
     if args.workload == "miss_rate_sweep":
         sweep_main(args)
+        return
+    if args.workload == "cold_start":
+        cold_start_main(args)
         return
     if args.workload == W.PROBE.name:
         probe_main(args, int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")))
@@ -1117,12 +1302,15 @@ def main():
         sessions_main(args, int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")))
         return
     w = W.WORKLOADS[args.workload]
-    settle = int(w.extra.get("settle", 0))
+    if args.layers:                        # a smaller stack of the same layers (profiling captures)
+        w = w.scaled(layers=args.layers)
+    settle = int(w.extra.get("settle", 0)) if args.settle is None else args.settle
     args.warmup += settle                  # untimed steps: the workload's settle phase, then the warm-up
     if args.steps is None:
         args.steps = max(1, w.steps - args.warmup)
-    if args.warmup + args.steps > w.steps:
-        w = w.scaled(steps=args.warmup + args.steps)
+    extra = args.phase_steps if (not args.separate and w.queries == 1 and w.layers > 1) else 0
+    if args.warmup + args.steps + extra > w.steps:
+        w = w.scaled(steps=args.warmup + args.steps + extra)
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     config = {"workload": w.name, "layers": w.layers, "history": w.n0, "hot_rows": w.hot_rows, "k": w.k,
@@ -1131,7 +1319,9 @@ def main():
               "gather": args.gather if args.gather != "auto" else f"auto>={args.auto_miss_pct}%", "parallelism": f"replicas{world}",
               "calls": ("kvo_append_rows+kvo_select_topk_batch(%d rows)+kvo_resolve_gather_multi" % w.queries if w.queries > 1
                         else "kvo_append_rows+kvo_select_topk+kvo_resolve_gather" if args.separate
-                        else "kvo_decode_layers x2 (selecting layers, then reusing layers)" if w.layers > 1
+                        else ("kvo_decode_layers (every layer; reusing layers name their source's idx)"
+                              if args.layer_calls == 1 else
+                              "kvo_decode_layers x2 (selecting layers, then reusing layers)") if w.layers > 1
                         else "kvo_decode_step"),
               "l2": "flushed between steps (1 GiB memset, outside the step events)"}
     if settle:
@@ -1183,16 +1373,50 @@ def main():
     ab = algorithmic_bytes(w, nmean, g["delta"], nres, nsel)
     kern_avg = {kind: float(np.mean(v)) for kind, v in g["kern_ms"].items()}
     kern_tot = {kind: float(np.sum(v)) for kind, v in g["kern_ms"].items()}
-    dominant = max(kern_tot, key=kern_tot.get)
     step_bytes = (w.layers * (ab["resolve_hbm"] + ROW * w.appends_per_step)
                   + len(w.selecting_layers()) * ab["select_hbm"])
-    per_launch_bytes = {"resolve": ab["resolve_hbm"], "select": ab["select_hbm"], "append": 2 * ROW * w.appends_per_step,
-                        "step": ab["resolve_hbm"] + ab["select_hbm"] + ROW * w.appends_per_step,
-                        "layers": step_bytes / max(1, len(g["kern_ms"].get("layers", [])) / args.steps)}[dominant]
+    gpu_launches = g["launches"]
+    ph = g.get("phases")
+    kern_note = None
+    if ph and ph["calls"]:
+        kern_note = (f"kernel durations from {ph['steps']} steps after the timed region, with CUDA events between "
+                     "the launches of each kvo_decode_layers call (launches serialised on one stream); step "
+                     f"p50 there {1e3 * float(np.percentile(ph['step_ms'], 50)):.1f} us")
+        # kvo_decode_layers by its launches, from the pass after the timed
+        # region: the selections, the gathers (one launch over every layer of
+        # the call) and the finishes, with their own counters
+        pst = ph["steps"]
+        calls_per_step = ph["calls"] / pst
+        nmean_p = float(np.mean([w.n_at(s) for s in range(args.warmup + args.steps,
+                                                              args.warmup + args.steps + pst)]))
+        abp = algorithmic_bytes(w, nmean_p, ph["delta"], pst * w.layers, pst * len(w.selecting_layers()))
+        kern_tot = {"layers_select": ph["layers_select"], "layers_gather": ph["layers_gather"],
+                    "layers_finish": ph["layers_finish"]}
+        kern_avg = {"layers_select": ph["layers_select"] / pst,
+                    "layers_gather": ph["layers_gather"] / ph["calls"],
+                    "layers_finish": ph["layers_finish"] / ph["calls"], "layers": kern_avg.get("layers")}
+        gb = gather_bytes(w, abp)
+        per_launch = {"layers_select": len(w.selecting_layers()) * abp["select_hbm"],
+                      "layers_gather": w.layers * gb / calls_per_step,
+                      "layers_finish": w.layers * finish_bytes(w, abp) / calls_per_step}
+    else:
+        per_launch = {"resolve": ab["resolve_hbm"], "select": ab["select_hbm"],
+                      "append": 2 * ROW * w.appends_per_step,
+                      "step": ab["resolve_hbm"] + ab["select_hbm"] + ROW * w.appends_per_step,
+                      "layers": step_bytes / max(1, len(g["kern_ms"].get("layers", [])) / args.steps)}
+    dominant = max((kd for kd in kern_tot), key=kern_tot.get)
+    per_launch_bytes = per_launch[dominant]
     achieved = per_launch_bytes / (kern_avg[dominant] * 1e-3) / 1e9
     traffic = dram_traffic(w.name, dominant)
-    t_resolve = kern_avg.get("resolve", kern_avg.get("step", 1e9))
-    host_gbs = ab["resolve_host"] / (t_resolve * 1e-3) / 1e9
+    # miss traffic over the host link: the resolving launches' host bytes over
+    # their time (per resolve launch, per gather launch of the batched layers)
+    if ph and ph["calls"]:
+        host_gbs = w.layers * abp["resolve_host"] / (kern_tot["layers_gather"] / ph["steps"] * 1e-3) / 1e9
+    elif "layers" in kern_tot:
+        host_gbs = w.layers * ab["resolve_host"] / (kern_tot["layers"] / args.steps * 1e-3) / 1e9
+    else:
+        t_resolve = kern_avg.get("resolve", kern_avg.get("step", 1e9))
+        host_gbs = ab["resolve_host"] / (t_resolve * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "rows/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(1e3 * g["total_s"] / args.steps, 4),
@@ -1205,15 +1429,28 @@ def main():
                      "algorithmic_bytes_per_launch": round(per_launch_bytes)},
         "host_link": {"achieved_miss_gbs": round(host_gbs, 2), "peak_gbs": link["peak_gbs"],
                       "frac": round(host_gbs / link["peak_gbs"], 4) if link["peak_gbs"] else None,
-                      "probe": link, "miss_bytes_per_launch": round(ab["resolve_host"])},
-        "kernels_us": {k: round(1e3 * v, 3) for k, v in kern_avg.items()},
+                      "probe": link, "miss_bytes_per_launch": round(ab["resolve_host"]),
+                      # the whole timed step: every layer's miss bytes over the step time
+                      "step_miss_gbs": round(w.layers * ab["resolve_host"] * args.steps / g["total_s"] / 1e9, 2),
+                      "step_frac": round(w.layers * ab["resolve_host"] * args.steps / g["total_s"] / 1e9
+                                         / link["peak_gbs"], 4) if link["peak_gbs"] else None},
+        "kernels_us": {k: round(1e3 * v, 3) for k, v in kern_avg.items() if v is not None},
+        "kernels_note": kern_note,
         "per_step": {"hits": round(ab["hits"], 1), "misses": round(ab["misses"], 1),
                      "fills": round(ab["fills"], 1),
                      "step_us_p50": round(1e3 * float(np.percentile(g["step_ms"], 50)), 2),
                      "step_us_p99": round(1e3 * float(np.percentile(g["step_ms"], 99)), 2),
-                     "step_us_max": round(1e3 * float(np.max(g["step_ms"])), 2)},
-        "gpu_launches": g["launches"], "clocks": g["clocks"],
+                     "step_us_max": round(1e3 * float(np.max(g["step_ms"])), 2),
+                     # the untimed steps before the timed region: the workload's
+                     # settle phase, then the warm-up (the cold start)
+                     "untimed_steps": len(g["settle_ms"]),
+                     "untimed_first_us": [round(1e3 * x, 1) for x in g["settle_ms"][:4]],
+                     "untimed_us_p50": round(1e3 * float(np.percentile(g["settle_ms"], 50)), 2)
+                     if g["settle_ms"] else None,
+                     "untimed_us_max": round(1e3 * float(np.max(g["settle_ms"])), 2) if g["settle_ms"] else None},
+        "gpu_launches": gpu_launches, "clocks": g["clocks"],
         "wall_s": round(g["wall"], 3), "device_status": g["status"],
+        "api_host_us_per_step": round(g["api_host_us"], 1),
     }
     if cpu is not None:
         line["cpu_baseline"] = {"value": round(cpu["rows_per_s"], 1), "unit": "rows/s", "cores": cpu["cores"],

@@ -20,7 +20,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libkvo.so")
-SOURCES = ["kvo_api.cu", "kvo_topk.cu", "kvo_resolve.cu", "kvo_step.cu", "kvo_pool.cu"]
+SOURCES = ["kvo_api.cu", "kvo_topk.cu", "kvo_resolve.cu", "kvo_step.cu", "kvo_layers.cu", "kvo_pool.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-I", INCLUDE]
 

@@ -31,6 +31,7 @@ struct kvo_ctx {
   int32_t* evlog = nullptr;              // device [layers][1 + 3*KVO_MAX_ROUND] when recording
   uint32_t* status = nullptr;            // device status word
   bool resolved = false;                 // a resolve has been enqueued (the policy is fixed from then on)
+  bool unusable = false;                 // a bulk copy may still land in freed shared memory: no more launches
   uint32_t ring_rows = 0;                // recent ring rows per layer (0: appends go straight to RAM)
   std::vector<int64_t> ram_len;          // per layer: rows the host history (RAM) holds
   struct {                               // kvo_decode_step_host's device staging
@@ -41,6 +42,12 @@ struct kvo_ctx {
     uint8_t* rows = nullptr;             // rows_cap new rows (grows)
     int64_t rows_cap = 0;
   } stage;
+  kvo::LayerStatic* statics = nullptr;   // device [layers]: what the batched decode step reads per layer
+  bool statics_dirty = true;             // the views changed since the last upload
+  int64_t launches = 0;                  // kernels kvo_decode_layers has launched
+  bool phase_timing = false;             // kvo_decode_layers records events around its launches
+  std::vector<cudaEvent_t> phase_ev;     // 4 per recorded call, reused
+  size_t phase_calls = 0;                // calls recorded since the last kvo_layers_phase_times
 };
 
 namespace {
@@ -69,6 +76,8 @@ void free_ctx(kvo_ctx* c) {
   cudaFree(c->stage.rows);
   cudaFree(c->evlog);
   cudaFree(c->status);
+  cudaFree(c->statics);
+  for (cudaEvent_t e : c->phase_ev) cudaEventDestroy(e);
   delete c;
 }
 
@@ -83,6 +92,62 @@ bool is_device_pointer(const void* p) {
     return false;
   }
   return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+}
+
+// The driver's cuMemGetAddressRange (base and size of the allocation that
+// holds a device address), reached through the runtime.
+using GetRangeFn = int (*)(unsigned long long*, size_t*, unsigned long long);
+GetRangeFn address_range_fn() {
+  static const GetRangeFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+      cudaGetLastError();
+      return static_cast<GetRangeFn>(nullptr);
+    }
+    return reinterpret_cast<GetRangeFn>(f);
+  }();
+  return fn;
+}
+
+// The device allocations that one call's argument checks have found: a
+// buffer inside one of them needs no further driver query (the layers of a
+// batched call usually take their rows from one tensor).
+struct DeviceRanges {
+  std::vector<std::pair<uintptr_t, uintptr_t>> r;   // [lo, hi)
+  // Whether [p, p + bytes) is device memory.
+  bool check(const void* p, size_t bytes) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    for (const auto& x : r)
+      if (a >= x.first && a + bytes <= x.second) return true;
+    if (!is_device_pointer(p)) return false;
+    unsigned long long base = 0;
+    size_t size = 0;
+    const GetRangeFn fn = address_range_fn();
+    if (fn && fn(&base, &size, (unsigned long long)a) == 0) {
+      if (a + bytes > base + size) return false;     // the buffer runs past its allocation
+      r.emplace_back((uintptr_t)base, (uintptr_t)(base + size));
+    }
+    return true;
+  }
+};
+
+// Uploads the per-layer table the batched decode step reads, when the views
+// changed (the work in flight that reads the old table is waited for first).
+cudaError_t upload_statics(kvo_ctx* c) {
+  if (!c->statics_dirty) return cudaSuccess;
+  std::vector<kvo::LayerStatic> h(c->layers);
+  for (int32_t l = 0; l < c->layers; ++l) {
+    const kvo::LayerView& v = c->views[l];
+    h[l] = kvo::LayerStatic{v.pos2slot, v.slot2pos, v.last_use, v.hot, v.hist, v.counters, v.stats,
+                            c->evlog ? c->evlog + kEvlogStride * l : nullptr, v.ring, v.recent,
+                            v.hot_rows, v.history_cap, v.ring_cap, v.ring_rows};
+  }
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(c->statics, h.data(), h.size() * sizeof(h[0]), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) c->statics_dirty = false;
+  return e;
 }
 
 // Copies device rows into the mapped host history and publishes the new
@@ -108,12 +173,13 @@ __global__ void ring_append_kernel(const uint4* __restrict__ src, uint4* __restr
   if (blockIdx.x == 0 && threadIdx.x == 0) counters[1] = new_len;
 }
 
-// Reads pinned host memory with 16-byte zero-copy loads; XOR-folds into sink.
-__global__ void probe_kernel(const uint4* __restrict__ src, uint64_t nvec, uint4* sink) {
+// Reads pinned host memory with 16-byte zero-copy loads, one piece every
+// `step` pieces; XOR-folds into sink.
+__global__ void probe_kernel(const uint4* __restrict__ src, uint64_t nvec, uint64_t step, uint4* sink) {
   const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
   uint4 acc = make_uint4(0, 0, 0, 0);
-  for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
-    const uint4 v = src[i];
+  for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i * step < nvec; i += stride) {
+    const uint4 v = src[i * step];
     acc.x ^= v.x;
     acc.y ^= v.y;
     acc.z ^= v.z;
@@ -154,11 +220,11 @@ cudaError_t launch_ring_append(const void* src_dev, uint8_t* ring, uint32_t r, u
   return cudaGetLastError();
 }
 
-cudaError_t launch_probe(const void* src, uint64_t bytes, void* sink, cudaStream_t stream) {
+cudaError_t launch_probe(const void* src, uint64_t bytes, void* sink, cudaStream_t stream, uint64_t stride) {
   int sms = 0, dev = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  probe_kernel<<<sms * 4, 512, 0, stream>>>(static_cast<const uint4*>(src), bytes / 16,
+  probe_kernel<<<sms * 4, 512, 0, stream>>>(static_cast<const uint4*>(src), bytes / 16, stride / 16,
                                             static_cast<uint4*>(sink));
   return cudaGetLastError();
 }
@@ -194,6 +260,29 @@ cudaError_t ring_after_append(kvo_ctx* ctx, int32_t layer, cudaStream_t s) {
   if (!ctx->ring_rows) return cudaSuccess;
   const int64_t pending = ctx->length[layer] - ctx->ram_len[layer];
   return ring_copyback(ctx, layer, ctx->ram_len[layer] + pending / KVO_COPYBACK_BATCH * KVO_COPYBACK_BATCH, s);
+}
+
+// The rows RAM holds once r device rows are appended to the layer: every
+// appended row without the ring; with it, the rows before the ring's pending
+// ones plus every whole batch of KVO_COPYBACK_BATCH pending rows (a batch is
+// copied back as soon as it is complete).
+int64_t ram_after_append(const kvo_ctx* ctx, int32_t layer, int64_t r) {
+  const int64_t len = ctx->length[layer] + r;
+  if (!ctx->ring_rows) return len;
+  const int64_t ram = ctx->ram_len[layer];
+  return ram + (len - ram) / KVO_COPYBACK_BATCH * KVO_COPYBACK_BATCH;
+}
+
+// A launch that appends r device rows and resolves in the same step sees the
+// append's copyback already done: the ring rows it moves to RAM that were
+// appended by earlier calls are copied here, before the launch; the launch
+// itself writes its own rows below the new RAM length to the host history
+// rather than to the ring.  Returns the new RAM length (the launch's
+// ram_len); the caller stores it once the launch is enqueued.
+cudaError_t copyback_before_step(kvo_ctx* ctx, int32_t layer, int64_t r, cudaStream_t s, int64_t* ram) {
+  *ram = ram_after_append(ctx, layer, r);
+  if (!ctx->ring_rows) return cudaSuccess;
+  return ring_copyback(ctx, layer, std::min(*ram, ctx->length[layer]), s);
 }
 
 }  // namespace
@@ -238,6 +327,7 @@ kvo_status kvo_create(int32_t layers, int64_t history_cap, int32_t hot_rows, int
   bool good = ok(cudaMalloc(&c->counters, sizeof(uint32_t) * 8 * layers)) &&
               ok(cudaMalloc(&c->stats, sizeof(unsigned long long) * 8 * layers)) &&
               ok(cudaMalloc(&c->status, sizeof(uint32_t))) &&
+              ok(cudaMalloc(&c->statics, sizeof(kvo::LayerStatic) * layers)) &&
               ok(cudaMemset(c->counters, 0, sizeof(uint32_t) * 8 * layers)) &&
               ok(cudaMemset(c->stats, 0, sizeof(unsigned long long) * 8 * layers)) &&
               ok(cudaMemset(c->status, 0, sizeof(uint32_t)));
@@ -298,6 +388,7 @@ kvo_status kvo_destroy(kvo_ctx* ctx) {
 }
 
 kvo_status kvo_append_rows(kvo_ctx* ctx, int32_t layer, const void* rows, int64_t r, void* stream) {
+  if (ctx && ctx->unusable) return KVO_ECUDA;
   if (!ctx || layer < 0 || layer >= ctx->layers || r < 0) return KVO_EINVAL;
   if (r == 0) return KVO_OK;
   if (!rows || !aligned16(rows) || ctx->length[layer] + r > ctx->history_cap) return KVO_EINVAL;
@@ -334,6 +425,7 @@ kvo_status kvo_append_rows(kvo_ctx* ctx, int32_t layer, const void* rows, int64_
 
 kvo_status kvo_select_topk(kvo_ctx* ctx, const float* scores, int64_t n, int32_t k, int32_t* idx,
                            void* stream) {
+  if (ctx && ctx->unusable) return KVO_ECUDA;
   if (!ctx || !scores || !idx || k < 1 || k > KVO_MAX_K || n < k || n > INT32_MAX) return KVO_EINVAL;
   if (!aligned4(scores) || !aligned4(idx)) return KVO_EINVAL;
   const cudaError_t e = kvo::launch_topk(scores, (uint32_t)n, (uint32_t)k, idx, ctx->max_cluster,
@@ -352,6 +444,7 @@ kvo_status kvo_set_recent_ring(kvo_ctx* ctx, int32_t rows) {
     v.ring_rows = 0;
   }
   ctx->ring_rows = 0;
+  ctx->statics_dirty = true;
   if (!rows) return KVO_OK;
   for (kvo::LayerView& v : ctx->views) {
     if (!ok(cudaMalloc(&v.recent, (size_t)rows * KVO_ROW_BYTES))) {
@@ -370,9 +463,40 @@ kvo_status kvo_set_recent_ring(kvo_ctx* ctx, int32_t rows) {
 }
 
 kvo_status kvo_flush_ring(kvo_ctx* ctx, int32_t layer, void* stream) {
+  if (ctx && ctx->unusable) return KVO_ECUDA;
   if (!ctx || layer < 0 || layer >= ctx->layers) return KVO_EINVAL;
   return ok(ring_copyback(ctx, layer, ctx->length[layer], static_cast<cudaStream_t>(stream))) ? KVO_OK
                                                                                                 : KVO_ECUDA;
+}
+
+kvo_status kvo_set_phase_timing(kvo_ctx* ctx, int32_t on) {
+  if (!ctx) return KVO_EINVAL;
+  ctx->phase_timing = on != 0;
+  ctx->phase_calls = 0;
+  return KVO_OK;
+}
+
+kvo_status kvo_layers_launch_count(kvo_ctx* ctx, int64_t* out) {
+  if (!ctx || !out) return KVO_EINVAL;
+  *out = ctx->launches;
+  return KVO_OK;
+}
+
+kvo_status kvo_layers_phase_times(kvo_ctx* ctx, double* ms, int64_t* calls) {
+  if (!ctx || !ms || !calls) return KVO_EINVAL;
+  ms[0] = ms[1] = ms[2] = 0.0;
+  for (size_t c = 0; c < ctx->phase_calls; ++c) {
+    cudaEvent_t* ev = ctx->phase_ev.data() + 4 * c;
+    if (!ok(cudaEventSynchronize(ev[3]))) return KVO_ECUDA;
+    for (int i = 0; i < 3; ++i) {
+      float t = 0.f;
+      if (!ok(cudaEventElapsedTime(&t, ev[i], ev[i + 1]))) return KVO_ECUDA;
+      ms[i] += t;
+    }
+  }
+  *calls = (int64_t)ctx->phase_calls;
+  ctx->phase_calls = 0;
+  return KVO_OK;
 }
 
 kvo_status kvo_ram_length(kvo_ctx* ctx, int32_t layer, int64_t* out) {
@@ -407,6 +531,15 @@ kvo_status kvo_set_policy(kvo_ctx* ctx, int32_t policy) {
   return KVO_OK;
 }
 
+kvo_status kvo_debug_raise_status(kvo_ctx* ctx, uint32_t bits) {
+  if (!ctx || bits > 15u) return KVO_EINVAL;
+  uint32_t st = 0;
+  if (!ok(cudaDeviceSynchronize()) || !ok(cudaMemcpy(&st, ctx->status, sizeof st, cudaMemcpyDeviceToHost)))
+    return KVO_ECUDA;
+  st |= bits;
+  return ok(cudaMemcpy(ctx->status, &st, sizeof st, cudaMemcpyHostToDevice)) ? KVO_OK : KVO_ECUDA;
+}
+
 kvo_status kvo_debug_layer_counters(kvo_ctx* ctx, int32_t layer, uint32_t* out) {
   if (!ctx || !out || layer < 0 || layer >= ctx->layers) return KVO_EINVAL;
   if (!ok(cudaDeviceSynchronize())) return KVO_ECUDA;
@@ -416,6 +549,7 @@ kvo_status kvo_debug_layer_counters(kvo_ctx* ctx, int32_t layer, uint32_t* out) 
 
 kvo_status kvo_select_topk_batch(kvo_ctx* ctx, const float* scores, int64_t n, int64_t ld, int32_t nq, int32_t k,
                                  int32_t* idx, void* stream) {
+  if (ctx && ctx->unusable) return KVO_ECUDA;
   if (!ctx || !scores || !idx || nq < 1 || nq > 65535 || k < 1 || k > KVO_MAX_K || n < k || n > INT32_MAX ||
       ld < n || !aligned4(scores) || !aligned4(idx))
     return KVO_EINVAL;
@@ -426,6 +560,7 @@ kvo_status kvo_select_topk_batch(kvo_ctx* ctx, const float* scores, int64_t n, i
 
 kvo_status kvo_resolve_gather(kvo_ctx* ctx, int32_t layer, const int32_t* idx, int32_t k,
                               void* out_rows, uint16_t* out_bf16, void* stream) {
+  if (ctx && ctx->unusable) return KVO_ECUDA;
   if (!ctx || layer < 0 || layer >= ctx->layers || !idx || !aligned4(idx) || k < 1 || k > KVO_MAX_K ||
       k > ctx->hot_rows || (!out_rows && !out_bf16))
     return KVO_EINVAL;
@@ -442,6 +577,7 @@ kvo_status kvo_resolve_gather(kvo_ctx* ctx, int32_t layer, const int32_t* idx, i
 
 kvo_status kvo_resolve_gather_multi(kvo_ctx* ctx, int32_t layer, const int32_t* idx, int32_t nq, int32_t k,
                                     void* out_rows, uint16_t* out_bf16, void* stream) {
+  if (ctx && ctx->unusable) return KVO_ECUDA;
   if (!ctx || layer < 0 || layer >= ctx->layers || !idx || !aligned4(idx) || nq < 1 || k < 1 || k > KVO_MAX_K ||
       (int64_t)nq * k > KVO_MAX_ROUND || (int64_t)nq * k > ctx->hot_rows || (!out_rows && !out_bf16))
     return KVO_EINVAL;
@@ -458,40 +594,66 @@ kvo_status kvo_resolve_gather_multi(kvo_ctx* ctx, int32_t layer, const int32_t* 
 }
 
 kvo_status kvo_decode_layers(kvo_ctx* ctx, const kvo_layer_task* tasks, int32_t ntasks, int32_t k, void* stream) {
+  if (ctx && ctx->unusable) return KVO_ECUDA;
   if (!ctx || !tasks || ntasks < 0 || ntasks > ctx->layers || k < 1 || k > KVO_MAX_K || k > ctx->hot_rows)
     return KVO_EINVAL;
   if (ntasks == 0) return KVO_OK;
-  std::vector<kvo::StepTask> st(ntasks);
-  std::vector<bool> seen(ctx->layers, false);
+  static thread_local std::vector<kvo::StepTask> st;
+  static thread_local std::vector<uint32_t> lay;
+  static thread_local std::vector<uint8_t> seen;
+  static thread_local DeviceRanges dev;
+  st.resize(ntasks);
+  lay.resize(ntasks);
+  seen.assign(ctx->layers, 0);
+  dev.r.clear();
   for (int32_t i = 0; i < ntasks; ++i) {
     const kvo_layer_task& t = tasks[i];
     if (t.layer < 0 || t.layer >= ctx->layers || seen[t.layer] || t.r < 0 || !t.idx || !aligned4(t.idx) ||
         (t.scores && !aligned4(t.scores)) || (!t.out_rows && !t.out_bf16) || (t.out_rows && !aligned16(t.out_rows)) ||
         (t.out_bf16 && !aligned16(t.out_bf16)))
       return KVO_EINVAL;
-    seen[t.layer] = true;
-    if (t.r > 0 && (!t.new_rows || !aligned16(t.new_rows) || !is_device_pointer(t.new_rows))) return KVO_EINVAL;
+    seen[t.layer] = 1;
+    lay[i] = (uint32_t)t.layer;
+    if (t.r > 0 && (!t.new_rows || !aligned16(t.new_rows) || !dev.check(t.new_rows, (size_t)t.r * KVO_ROW_BYTES)))
+      return KVO_EINVAL;
     if (ctx->ring_rows && t.r > (int64_t)ctx->ring_rows - KVO_COPYBACK_BATCH) return KVO_EINVAL;
     const int64_t start = ctx->length[t.layer];
     if (start + t.r > ctx->history_cap) return KVO_EINVAL;
     if (t.scores && (t.n < k || t.n > start + t.r)) return KVO_EINVAL;
     kvo::LayerView v = ctx->views[t.layer];
     v.evlog = ctx->evlog ? ctx->evlog + kEvlogStride * t.layer : nullptr;
-    v.ram_len = (uint32_t)ctx->ram_len[t.layer];
     st[i] = kvo::StepTask{v, t.r ? t.new_rows : nullptr, (uint32_t)t.r, (uint32_t)start, t.scores,
                           (uint32_t)(t.scores ? t.n : 0), t.idx, static_cast<uint8_t*>(t.out_rows), t.out_bf16};
   }
+  cudaEvent_t* ev = nullptr;
+  if (ctx->phase_timing) {
+    const size_t need = 4 * (ctx->phase_calls + 1);
+    while (ctx->phase_ev.size() < need) {
+      cudaEvent_t e = nullptr;
+      if (!ok(cudaEventCreate(&e))) return KVO_ECUDA;
+      ctx->phase_ev.push_back(e);
+    }
+    ev = ctx->phase_ev.data() + 4 * ctx->phase_calls;
+  }
+  if (!ok(upload_statics(ctx))) return KVO_ECUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const cudaError_t e =
-      kvo::launch_decode_layers(st.data(), (uint32_t)ntasks, (uint32_t)k, ctx->status, ctx->max_cluster, s);
-  if (e == cudaErrorInvalidValue) return KVO_EINVAL;
+  static thread_local std::vector<int64_t> ram;
+  ram.resize(ntasks);
+  for (int32_t i = 0; i < ntasks; ++i) {
+    if (!ok(copyback_before_step(ctx, tasks[i].layer, tasks[i].r, s, &ram[i]))) return KVO_ECUDA;
+    st[i].L.ram_len = (uint32_t)ram[i];
+  }
+  uint32_t launched = 0;
+  const cudaError_t e = kvo::launch_layers(st.data(), lay.data(), (uint32_t)ntasks, (uint32_t)k, ctx->statics,
+                                           ctx->status, ctx->max_cluster, s, ev, &launched);
   if (!ok(e)) return KVO_ECUDA;
+  ctx->launches += launched;
+  if (ev) ++ctx->phase_calls;
   ctx->resolved = true;
   for (int32_t i = 0; i < ntasks; ++i) {
     const int32_t l = tasks[i].layer;
     ctx->length[l] += tasks[i].r;
-    if (!ctx->ring_rows) ctx->ram_len[l] = ctx->length[l];
-    else if (!ok(ring_after_append(ctx, l, s))) return KVO_ECUDA;
+    ctx->ram_len[l] = ram[i];
   }
   return KVO_OK;
 }
@@ -517,20 +679,23 @@ static kvo_status decode_step_enqueue(kvo_ctx* ctx, int32_t layer, const void* n
   const int64_t start = ctx->length[layer];
   kvo::LayerView v = ctx->views[layer];
   v.evlog = ctx->evlog ? ctx->evlog + kEvlogStride * layer : nullptr;
-  v.ram_len = (uint32_t)ctx->ram_len[layer];
+  int64_t ram = 0;
+  if (!ok(copyback_before_step(ctx, layer, r, stream, &ram))) return KVO_ECUDA;
+  v.ram_len = (uint32_t)ram;
   const cudaError_t e = kvo::launch_decode_step(v, r ? new_rows : nullptr, (uint32_t)r, (uint32_t)start, scores,
                                                 (uint32_t)n, (uint32_t)k, idx, static_cast<uint8_t*>(out_rows),
                                                 out_bf16, ctx->status, ctx->max_cluster, stream, out_host);
   if (!ok(e)) return KVO_ECUDA;
   ctx->resolved = true;
   ctx->length[layer] = start + r;
-  if (!ctx->ring_rows) ctx->ram_len[layer] = start + r;
-  return ok(ring_after_append(ctx, layer, stream)) ? KVO_OK : KVO_ECUDA;
+  ctx->ram_len[layer] = ram;
+  return KVO_OK;
 }
 
 kvo_status kvo_decode_step(kvo_ctx* ctx, int32_t layer, const void* new_rows, int64_t r,
                            const float* scores, int64_t n, int32_t k, int32_t* idx,
                            void* out_rows, uint16_t* out_bf16, void* stream) {
+  if (ctx && ctx->unusable) return KVO_ECUDA;
   if (!decode_step_args_ok(ctx, layer, new_rows, r, scores, n, k, idx, out_rows, out_bf16)) return KVO_EINVAL;
   if ((out_rows && !aligned16(out_rows)) || (out_bf16 && !aligned16(out_bf16))) return KVO_EINVAL;
   if (r > 0 && (!aligned16(new_rows) || !is_device_pointer(new_rows))) return KVO_EINVAL;
@@ -552,6 +717,7 @@ static void* mapped_host(const void* p) {
 kvo_status kvo_decode_step_host(kvo_ctx* ctx, int32_t layer, const void* new_rows, int64_t r,
                                 const float* scores, int64_t n, int32_t k, int32_t* idx,
                                 void* out_rows, uint16_t* out_bf16, void* stream) {
+  if (ctx && ctx->unusable) return KVO_ECUDA;
   if (!decode_step_args_ok(ctx, layer, new_rows, r, scores, n, k, idx, out_rows, out_bf16)) return KVO_EINVAL;
   if (is_device_pointer(scores) || is_device_pointer(idx) || (r > 0 && is_device_pointer(new_rows)) ||
       (out_rows && is_device_pointer(out_rows)) || (out_bf16 && is_device_pointer(out_bf16)))
@@ -625,6 +791,7 @@ kvo_status kvo_sync(kvo_ctx* ctx, void* stream) {
   if (!ok(cudaMemcpy(&st, ctx->status, sizeof st, cudaMemcpyDeviceToHost))) return KVO_ECUDA;
   if (st == 0) return KVO_OK;
   if (!ok(cudaMemset(ctx->status, 0, sizeof st))) return KVO_ECUDA;
+  if (st & kvo::kFlagInflight) ctx->unusable = true;
   if (st & kvo::kFlagTimeout) return KVO_ETIMEDOUT;
   if (st & kvo::kFlagRange) return KVO_ERANGE;
   return KVO_ECUDA;
@@ -684,6 +851,7 @@ kvo_status kvo_debug_record_evictions(kvo_ctx* ctx, int32_t on) {
     cudaFree(ctx->evlog);
     ctx->evlog = nullptr;
   }
+  ctx->statics_dirty = true;
   return KVO_OK;
 }
 
@@ -707,14 +875,27 @@ kvo_status kvo_debug_evictions(kvo_ctx* ctx, int32_t layer, int32_t* triples, in
 }
 
 kvo_status kvo_probe_host_read(const void* src, int64_t bytes, void* sink, void* stream) {
-  if (!src || !sink || bytes <= 0 || (bytes & 15) || !aligned16(src) || !aligned16(sink)) return KVO_EINVAL;
+  return kvo_probe_host_touch(src, bytes, 16, sink, stream);
+}
+
+kvo_status kvo_probe_host_touch(const void* src, int64_t bytes, int64_t stride, void* sink, void* stream) {
+  if (!src || !sink || bytes <= 0 || (bytes & 15) || stride < 16 || (stride & 15) || !aligned16(src) ||
+      !aligned16(sink))
+    return KVO_EINVAL;
   void* dev = nullptr;
   if (!ok(cudaHostGetDevicePointer(&dev, const_cast<void*>(src), 0))) {
     cudaGetLastError();
     return KVO_EINVAL;
   }
-  return ok(kvo::launch_probe(dev, (uint64_t)bytes, sink, static_cast<cudaStream_t>(stream))) ? KVO_OK
-                                                                                             : KVO_ECUDA;
+  return ok(kvo::launch_probe(dev, (uint64_t)bytes, sink, static_cast<cudaStream_t>(stream), (uint64_t)stride))
+             ? KVO_OK
+             : KVO_ECUDA;
+}
+
+kvo_status kvo_debug_history_host(kvo_ctx* ctx, int32_t layer, void** out) {
+  if (!ctx || !out || layer < 0 || layer >= ctx->layers) return KVO_EINVAL;
+  *out = ctx->hist_host[layer];
+  return KVO_OK;
 }
 
 }  // extern "C"

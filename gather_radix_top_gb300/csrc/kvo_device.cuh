@@ -17,6 +17,8 @@ constexpr uint32_t kMaxCluster = 16;
 constexpr uint32_t kFlagRange = 1u;
 constexpr uint32_t kFlagInternal = 2u;  // an internal consistency check failed
 constexpr uint32_t kFlagTimeout = 4u;   // a bounded device-side wait gave up
+constexpr uint32_t kFlagInflight = 8u;  // and its second wait too: a bulk copy may still be in flight into the
+                                        // shared memory of a CTA that has exited
 
 // ---------------------------------------------------------------- cluster
 __device__ __forceinline__ uint32_t cluster_rank() {

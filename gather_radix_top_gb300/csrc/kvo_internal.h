@@ -29,7 +29,8 @@ struct LayerView {
   uint32_t policy;                // KVO_POLICY_LRU or KVO_POLICY_CIRCULAR
   uint8_t* recent;                // NULL, or the recent ring: [ring_rows * 656] in HBM
   uint32_t ring_rows;             // 0, or a power of two: position p waits in slot p mod ring_rows
-  uint32_t ram_len;               // per launch: positions below it are in the host history
+  uint32_t ram_len;               // per launch: positions below it are in the host history (for a
+                                  // launch that appends, the length after its append's copyback)
   uint32_t gather_mode;           // KVO_GATHER_LOADS, KVO_GATHER_STAGED or KVO_GATHER_AUTO
   uint32_t auto_miss_pct;         // KVO_GATHER_AUTO: staged when a CTA's misses are at least this share
 };
@@ -58,8 +59,32 @@ struct StepTask {
   uint16_t* out_bf16;
   uint32_t out_host;              // out_rows is mapped host memory (plain stores, never read back)
 };
-cudaError_t launch_decode_layers(const StepTask* tasks, uint32_t ntasks, uint32_t k, uint32_t* status,
-                                 int max_cluster, cudaStream_t stream);
+// One layer's fixed device pointers and sizes, as the batched decode step
+// reads them from device memory (one entry per layer of a context).
+struct LayerStatic {
+  int32_t* pos2slot;
+  int32_t* slot2pos;
+  uint32_t* last_use;
+  uint8_t* hot;
+  const uint8_t* hist;          // device address of the mapped host history
+  uint32_t* counters;
+  unsigned long long* stats;
+  int32_t* evlog;               // NULL unless evictions are recorded
+  uint64_t* ring;               // LRU queue, two buffers of ring_cap entries
+  uint8_t* recent;              // recent ring rows, or NULL
+  uint32_t hot_rows, history_cap, ring_cap, ring_rows;
+};
+
+// One decode step of many layers in three launches over all of them (select,
+// gather, finish); tasks without scores read their idx after the selections.
+// layers[i]: task i's layer (its entry of `statics`, a device array).  ev:
+// NULL, or four events recorded before the selections, before the gathers,
+// before the finishes and after them (without events, each launch may be
+// scheduled before the previous one ends and waits for it on the GPU).
+// *launched grows by the number of kernels launched.
+cudaError_t launch_layers(const StepTask* tasks, const uint32_t* layers, uint32_t ntasks, uint32_t k,
+                          const LayerStatic* statics, uint32_t* status, int max_cluster, cudaStream_t stream,
+                          cudaEvent_t* ev, uint32_t* launched);
 cudaError_t launch_decode_step(const LayerView& L, const void* new_rows, uint32_t r, uint32_t old_len,
                                const float* scores, uint32_t n, uint32_t k, int32_t* idx, uint8_t* out_rows,
                                uint16_t* out_bf16, uint32_t* status, int max_cluster, cudaStream_t stream,
@@ -68,7 +93,7 @@ cudaError_t launch_append(const void* src_dev, uint8_t* hist_dev_dst, uint64_t b
                           uint32_t* counters, uint32_t new_len, cudaStream_t stream);
 cudaError_t launch_ring_append(const void* src_dev, uint8_t* ring, uint32_t r, uint32_t start, uint32_t ring_mask,
                                uint32_t* counters, uint32_t new_len, cudaStream_t stream);
-cudaError_t launch_probe(const void* src, uint64_t bytes, void* sink, cudaStream_t stream);
+cudaError_t launch_probe(const void* src, uint64_t bytes, void* sink, cudaStream_t stream, uint64_t stride = 16);
 
 // Largest cluster size (16 non-portable, else 8, 4, 2) that can run with the
 // given kernel's resources; 0 if none.

@@ -1,0 +1,806 @@
+// One decode step of many layers (kvo_decode_layers) in three launches, each
+// over every layer of the call at once:
+//   A select:  the top-K of every layer that brings scores (one cluster per
+//              selecting layer, the body of kvo_select_topk);
+//   B gather:  every selected entry of every layer: lookup, classify (hit:
+//              stamp; miss: first-occurrence claim), and the row copied to
+//              the output, hits from the HBM hot slot, misses from host
+//              memory (or the recent ring, or this call's new rows), with
+//              the bf16 dequant; the whole GPU moves rows, so the step runs
+//              at the rate of HBM and of the host link rather than at the
+//              latency of one cluster per layer;
+//   C finish:  one CTA per layer: rank the unique misses, walk the LRU queue
+//              (or the circular hand) for their victims, update the maps,
+//              fill the victim slots from the rows B wrote, append the new
+//              rows to the host history or the recent ring, and append the
+//              used slots to the LRU queue.
+//
+// "From 1M Total to 15+ x 1M Contexts: GLM-5.3 KV Cache Offloading":
+//   "Decision three: let the GPU manage the hot cache directly" - hits read
+//   the HBM slot, misses read the registered host copy, the gather emits a
+//   compact selection, and the CPU stays out of the per-selection loop;
+//   "GPU cache management has hazards too" - a slot filled in this round is
+//   a hit source only in the next round (fills happen in C, after every row
+//   of B is out), duplicate misses read host memory, and slots used by the
+//   round are pinned (B stamps every hit slot with the step before C picks
+//   victims among the slots not stamped);
+//   "Separate historical capacity from the current working set" - later
+//   layers reuse a selection: a layer without scores resolves its idx as it
+//   stands after A, so it may name the idx of a selecting layer of the same
+//   call.
+//
+// Results equal those of the single-layer calls in the order append, select,
+// resolve (the same LRU queue, the same first-occurrence dedupe, the same
+// (last_use, slot) victim order).  Nothing but the layers' own tables and the
+// caller's outputs carries state from one launch to the next: B leaves its
+// claims in pos2slot and its stamps in last_use, and C reads them there.
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+
+#include "kvo_internal.h"
+#include "kvo_resolve_body.cuh"
+#include "kvo_topk_body.cuh"
+
+namespace kvo {
+
+namespace {
+
+using resolve_detail::dequant_row;
+using resolve_detail::kRowVec;
+
+// One layer of the call: what changes from call to call.
+struct LayerCall {
+  const float* scores;          // NULL: idx is resolved as it stands after A
+  int32_t* idx;
+  uint8_t* out_rows;
+  uint16_t* out_bf16;
+  const uint8_t* fresh;         // this call's new rows (device), or NULL
+  uint32_t layer;
+  uint32_t n;                   // scores
+  uint32_t ram_len;             // rows in the host history after this call's append and copyback
+  uint32_t len;                 // history length after this call's append
+  uint32_t fresh_from;          // position of the first new row (the old length)
+  uint32_t r;                   // new rows
+  uint32_t to_ram;              // the first to_ram new rows go to the host history, the rest to the ring
+};
+
+constexpr uint32_t kBatchTasks = 128;                    // layers per launch (9 KB of parameters)
+// shared memory of a selecting CTA for resident keys: 50,279 of them fit one CTA
+constexpr uint32_t kSelectMaxSmem = 220u * 1024u;
+struct LayerBatch {
+  const LayerStatic* statics;   // device array, one entry per layer of the context
+  uint32_t k;
+  uint32_t chunks;              // B: CTAs per layer
+  uint32_t cand_bytes;          // A (filtered route): shared memory for candidates
+  uint32_t ntasks;
+  LayerCall t[kBatchTasks];
+};
+
+// Programmatic dependent launch: a launch that waits for the previous one on
+// the stream may be scheduled before it ends, and waits here (in hardware)
+// until the previous grid has completed and its memory is visible; the
+// previous grid lets it be scheduled once every CTA has signalled.
+__device__ __forceinline__ void wait_previous_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_next_grid() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ------------------------------------------------------------ A: select
+template <bool kResident>
+__global__ void __launch_bounds__(kThreads, 1) layers_select_kernel(const __grid_constant__ LayerBatch b) {
+  extern __shared__ __align__(16) uint8_t dyn_smem[];
+  __shared__ RadixSmem rsm;
+  const LayerCall& T = b.t[blockIdx.x / cluster_size()];
+  allow_next_grid();                                     // the gathers may be scheduled; they wait for this grid
+  int32_t* idx = T.idx;
+  const int32_t* pos2slot = b.statics[T.layer].pos2slot;
+  topk_detail::topk_body<kResident>(T.scores, T.n, b.k, dyn_smem, b.cand_bytes, &rsm,
+                                    [&](uint32_t pos, uint32_t out) {
+                                      idx[out] = (int32_t)pos;
+                                      prefetch_l2(&pos2slot[pos]);   // B looks it up next
+                                    });
+}
+
+// ------------------------------------------------------------ B: gather
+constexpr uint32_t kGatherThreads = 256;
+constexpr uint32_t kGatherWarps = kGatherThreads / 32;
+constexpr uint32_t kGatherEntries = 64;                  // entries per CTA
+constexpr uint32_t kGatherInFlight = 4;                  // rows a warp loads before it stores
+static_assert(kGatherEntries <= kGatherThreads, "one thread per entry classifies");
+
+// The row of a missing position: this call's new rows from their device
+// copy; rows still waiting in the recent ring from the ring; else the host
+// history.  *host: the row crosses the host link.
+__device__ __forceinline__ const uint4* miss_source(const LayerStatic& S, const LayerCall& T, uint32_t p,
+                                                   bool* host) {
+  *host = false;
+  if (T.fresh && p >= T.fresh_from) return reinterpret_cast<const uint4*>(T.fresh) + (size_t)(p - T.fresh_from) * kRowVec;
+  if (S.ring_rows && p >= T.ram_len)
+    return reinterpret_cast<const uint4*>(S.recent) + (size_t)(p & (S.ring_rows - 1u)) * kRowVec;
+  *host = true;
+  return reinterpret_cast<const uint4*>(S.hist) + (size_t)p * kRowVec;
+}
+
+__global__ void __launch_bounds__(kGatherThreads) layers_gather_kernel(const __grid_constant__ LayerBatch b,
+                                                                       uint32_t* status) {
+  __shared__ const uint4* src[kGatherEntries];           // NULL: an invalid entry (zero row)
+  __shared__ uint32_t cnt[4];                            // hits, misses, RAM reads, invalid
+  const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const LayerCall& T = b.t[blockIdx.x / b.chunks];
+  const LayerStatic S = b.statics[T.layer];
+  const uint32_t k = b.k;
+  const uint32_t j0 = (blockIdx.x % b.chunks) * kGatherEntries;
+  const uint32_t nj = j0 < k ? min(kGatherEntries, k - j0) : 0u;
+  if (tid < 4) cnt[tid] = 0;
+  wait_previous_grid();                                  // the selections are complete
+  __syncthreads();
+
+  // classify: one thread per entry
+  uint32_t hit = 0, miss = 0, ram = 0, inv = 0;
+  if (tid < nj) {
+    const uint32_t j = j0 + tid;
+    const int32_t p = T.idx[j];
+    const uint4* s = nullptr;
+    if (p < 0 || (uint32_t)p >= T.len) {
+      inv = 1;
+    } else {
+      int32_t sl = __ldcg(&S.pos2slot[p]);
+      if (sl >= (int32_t)S.hot_rows) {
+        atomicOr(status, kFlagInternal);                 // cannot happen; keep every index in bounds
+        sl = -1;
+      }
+      if (sl >= 0) {
+        S.last_use[sl] = S.counters[0] + 1u;             // pinned for this step
+        s = reinterpret_cast<const uint4*>(S.hot) + (size_t)sl * kRowVec;
+        hit = 1;
+      } else {
+        atomicMin(&S.pos2slot[p], (int32_t)j - (int32_t)k - 1);   // the smallest j claims the position
+        bool host;
+        s = miss_source(S, T, (uint32_t)p, &host);
+        miss = 1;
+        // a RAM read as append-then-resolve defines it: below the RAM length
+        // (this call's own rows there are served from their device copy,
+        // which holds the same bytes)
+        ram = !(S.ring_rows && (uint32_t)p >= T.ram_len);
+      }
+    }
+    src[tid] = s;
+  }
+  if (warp * 32 < nj) {                                  // warps holding entries: their counts
+    const uint32_t h = __reduce_add_sync(0xffffffffu, hit), m = __reduce_add_sync(0xffffffffu, miss);
+    const uint32_t rr = __reduce_add_sync(0xffffffffu, ram), iv = __reduce_add_sync(0xffffffffu, inv);
+    if (lane == 0) {
+      if (h) atomicAdd(&cnt[0], h);
+      if (m) atomicAdd(&cnt[1], m);
+      if (rr) atomicAdd(&cnt[2], rr);
+      if (iv) atomicAdd(&cnt[3], iv);
+    }
+  }
+  __syncthreads();
+
+  // rows: each warp keeps kGatherInFlight rows in flight
+  for (uint32_t e0 = warp; e0 < nj; e0 += kGatherWarps * kGatherInFlight) {
+    uint4 va[kGatherInFlight], vb[kGatherInFlight];
+#pragma unroll
+    for (uint32_t u = 0; u < kGatherInFlight; ++u) {
+      const uint32_t e = e0 + u * kGatherWarps;
+      va[u] = make_uint4(0, 0, 0, 0);
+      vb[u] = make_uint4(0, 0, 0, 0);
+      const uint4* s = e < nj ? src[e] : nullptr;
+      if (s) {
+        va[u] = s[lane];
+        if (lane < kRowVec - 32) vb[u] = s[32 + lane];
+      }
+    }
+#pragma unroll
+    for (uint32_t u = 0; u < kGatherInFlight; ++u) {
+      const uint32_t e = e0 + u * kGatherWarps;
+      if (e >= nj) break;
+      const uint32_t j = j0 + e;
+      if (T.out_rows) {
+        uint4* d = reinterpret_cast<uint4*>(T.out_rows) + (size_t)j * kRowVec;
+        d[lane] = va[u];
+        if (lane < kRowVec - 32) d[32 + lane] = vb[u];
+      }
+      if (T.out_bf16) dequant_row(va[u], vb[u], lane, reinterpret_cast<uint4*>(T.out_bf16 + (size_t)j * KVO_DEQUANT_VALUES));
+    }
+  }
+  if (tid == 0) {
+    unsigned long long* st = S.stats;
+    if (cnt[0]) atomicAdd(st + 1, (unsigned long long)cnt[0]);
+    if (cnt[1]) atomicAdd(st + 2, (unsigned long long)cnt[1]);
+    if (cnt[2]) atomicAdd(st + 6, (unsigned long long)cnt[2] * KVO_ROW_BYTES);
+    if (cnt[3]) {
+      atomicAdd(st + 5, (unsigned long long)cnt[3]);
+      atomicOr(status, kFlagRange);
+    }
+  }
+  allow_next_grid();                                     // the finishes may be scheduled; they wait for this grid
+}
+
+// ------------------------------------------------------------ C: finish
+constexpr uint32_t kFinishPer = 4;                        // queue entries a thread examines per round
+constexpr uint32_t kFinishEntries = KVO_MAX_K / kThreads;  // selection entries per thread
+constexpr uint32_t kCompactPer = 16;                      // queue entries a thread keeps in flight when compacting
+constexpr uint32_t kNoEntry = 0xffffffffu;
+constexpr uint32_t kFillInFlight = 8;                     // fill pieces a thread loads before it stores
+
+// Copies the current entries of [head, tail) of queue buffer `buf`, in
+// order, to the front of the other buffer; returns how many (the number of
+// slots).  One CTA.
+__device__ uint32_t compact_queue_cta(const LayerStatic& T, uint32_t head, uint32_t tail, uint32_t buf,
+                                      uint32_t* scratch) {
+  const uint32_t Q = T.ring_cap, qmask = Q - 1u;
+  const uint64_t* in = T.ring + (size_t)buf * Q;
+  uint64_t* out = T.ring + (size_t)(buf ^ 1u) * Q;
+  const uint32_t span = tail - head;
+  uint32_t kept = 0;
+  for (uint32_t base = 0; base < span; base += kCompactPer * kThreads) {
+    uint64_t e[kCompactPer];
+    uint32_t lu[kCompactPer];
+#pragma unroll
+    for (uint32_t q = 0; q < kCompactPer; ++q) {
+      const uint32_t o = base + kCompactPer * threadIdx.x + q;
+      e[q] = o < span ? __ldcg(&in[(head + o) & qmask]) : ~0ull;
+    }
+#pragma unroll
+    for (uint32_t q = 0; q < kCompactPer; ++q) {
+      const uint32_t sl = (uint32_t)e[q];
+      lu[q] = e[q] != ~0ull && sl < T.hot_rows ? __ldcg(&T.last_use[sl]) : 0u;
+    }
+    uint32_t mine = 0, keep = 0;
+#pragma unroll
+    for (uint32_t q = 0; q < kCompactPer; ++q) {
+      const bool cur = e[q] != ~0ull && (uint32_t)e[q] < T.hot_rows && lu[q] == (uint32_t)(e[q] >> 32);
+      keep |= (uint32_t)cur << q;
+      mine += cur;
+    }
+    uint32_t tot;
+    uint32_t pos = kept + block_excl_sum(mine, scratch, &tot);
+#pragma unroll
+    for (uint32_t q = 0; q < kCompactPer; ++q)
+      if ((keep >> q) & 1u) {
+        if (pos < Q) out[pos] = e[q];
+        ++pos;
+      }
+    kept += tot;
+  }
+  return kept;
+}
+
+// Shared memory of the finish launch (4-byte words): per unique miss u its
+// entry, victim slot and position, then the bitmap of the slots used in the
+// step (hits, then victims).
+__host__ __device__ inline size_t finish_smem_bytes(uint32_t k, uint32_t H) {
+  return (3u * (size_t)k + (H + 31u) / 32u) * 4u;
+}
+
+// One cluster of F CTAs per layer (F = 1 for many layers).  CTA 0 picks the
+// victims and keeps the maps and the LRU queue; then every CTA of the
+// cluster fills its share of the victim slots.  The loads that do not depend
+// on one another are issued together (the positions and the queue window,
+// then their claims and stamps), so that the chain of dependent global
+// accesses stays short after an L2 flush.
+template <bool kLru>
+__global__ void __launch_bounds__(kThreads, 1) layers_finish_kernel(const __grid_constant__ LayerBatch b,
+                                                                    uint32_t* status) {
+  extern __shared__ __align__(16) uint32_t fsm[];
+  __shared__ uint32_t scratch[2 * kWarps + 2];
+  __shared__ uint32_t head_hit, last_vic, nevict, nvic_s;
+  const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t F = cluster_size(), f = cluster_rank();
+  const LayerCall& T = b.t[blockIdx.x / F];
+  const LayerStatic S = b.statics[T.layer];
+  const uint32_t k = b.k, H = S.hot_rows;
+  uint32_t* mlist = fsm;                                 // [k]: entry of unique miss u
+  uint32_t* vslot = fsm + k;                             // [k]: victim slot of unique miss u
+  int32_t* mpos = reinterpret_cast<int32_t*>(fsm + 2 * k);   // [k]: position of unique miss u
+  uint32_t* used = fsm + 3 * k;                          // [ceil(H/32)]: slots used in this step
+  const uint32_t hwords = (H + 31u) / 32u;
+  wait_previous_grid();                                  // every gather of the call is complete
+
+  if (f == 0) {
+    const uint32_t t = __ldcg(&S.counters[0]) + 1u;
+    uint32_t head = __ldcg(&S.counters[2]), tail = __ldcg(&S.counters[3]), buf = __ldcg(&S.counters[4]) & 1u;
+    const uint32_t hand = __ldcg(&S.counters[5]);
+    const uint32_t Q = S.ring_cap, qmask = Q - 1u;
+    if (tid == 0) {
+      head_hit = kNoEntry;
+      nevict = 0;
+    }
+    // The queue gets at most k entries in this call: make room first.
+    if (kLru && tail - head > Q - k) {
+      tail = compact_queue_cta(S, head, tail, buf, scratch);
+      if (tid == 0 && tail != H) atomicOr(status, kFlagInternal);
+      head = 0;
+      buf ^= 1u;
+      __syncthreads();
+    }
+    const uint64_t* ring_in = S.ring + (size_t)buf * Q;
+    uint64_t* ring_out = S.ring + (size_t)buf * Q;
+    const uint32_t span = tail - head;
+    const uint32_t limit = kLru ? span : H;
+
+    // 1. positions of this thread's entries and the first queue window,
+    //    issued together
+    for (uint32_t w = tid; w < hwords; w += kThreads) used[w] = 0;
+    int32_t pj[kFinishEntries];
+#pragma unroll
+    for (uint32_t q = 0; q < kFinishEntries; ++q) {
+      const uint32_t j = q * kThreads + tid;
+      pj[q] = j < k ? __ldcg(&T.idx[j]) : -1;
+    }
+    uint64_t e[kFinishPer];
+#pragma unroll
+    for (uint32_t q = 0; q < kFinishPer; ++q) {
+      const uint32_t o = kFinishPer * tid + q;
+      if (kLru) e[q] = o < span ? __ldcg(&ring_in[(head + o) & qmask]) : ~0ull;
+      else e[q] = o < H ? (uint64_t)(hand + o < H ? hand + o : hand + o - H) : ~0ull;
+    }
+
+    // 2. their claims and stamps: an entry is a unique miss when its claim
+    //    won, a hit when it holds a slot (the slots the gathers stamped, the
+    //    first members of this step's used slots); a queue entry is a victim
+    //    candidate while it is current and its slot was not stamped
+    int32_t claim[kFinishEntries];
+#pragma unroll
+    for (uint32_t q = 0; q < kFinishEntries; ++q)
+      claim[q] = pj[q] >= 0 && (uint32_t)pj[q] < T.len ? __ldcg(&S.pos2slot[pj[q]]) : -1;
+    __syncthreads();                                     // the used bitmap is zero
+#pragma unroll
+    for (uint32_t q = 0; q < kFinishEntries; ++q)
+      if (claim[q] >= 0 && (uint32_t)claim[q] < H) atomicOr(&used[(uint32_t)claim[q] >> 5], 1u << (claim[q] & 31));
+    uint32_t lu[kFinishPer];
+#pragma unroll
+    for (uint32_t q = 0; q < kFinishPer; ++q) {
+      const uint32_t sl = (uint32_t)e[q];
+      lu[q] = e[q] != ~0ull && sl < H ? __ldcg(&S.last_use[sl]) : t;
+    }
+    uint32_t M = 0;
+#pragma unroll
+    for (uint32_t q = 0; q < kFinishEntries; ++q) {
+      if (q * kThreads >= k) break;                      // uniform over the CTA
+      const uint32_t j = q * kThreads + tid;
+      const bool fl = j < k && pj[q] >= 0 && (uint32_t)pj[q] < T.len && claim[q] == (int32_t)j - (int32_t)k - 1;
+      uint32_t tile;
+      const uint32_t rank = block_flag_scan(fl, scratch, &tile);
+      if (fl) {
+        mlist[M + rank] = j;
+        mpos[M + rank] = pj[q];
+      }
+      M += tile;
+    }
+
+    // 3. victims: the first M current, unstamped entries of the queue from
+    //    its head, or the first M unstamped slots from the circular hand
+    uint32_t found = 0, off = 0;
+    for (bool first_round = true; found < M && off < limit; first_round = false) {   // uniform over the CTA
+      if (!first_round) {
+#pragma unroll
+        for (uint32_t q = 0; q < kFinishPer; ++q) {
+          const uint32_t o = off + kFinishPer * tid + q;
+          if (kLru) e[q] = o < span ? __ldcg(&ring_in[(head + o) & qmask]) : ~0ull;
+          else e[q] = o < H ? (uint64_t)(hand + o < H ? hand + o : hand + o - H) : ~0ull;
+        }
+#pragma unroll
+        for (uint32_t q = 0; q < kFinishPer; ++q) {
+          const uint32_t sl = (uint32_t)e[q];
+          lu[q] = e[q] != ~0ull && sl < H ? __ldcg(&S.last_use[sl]) : t;
+        }
+      }
+      uint32_t ncur = 0;
+#pragma unroll
+      for (uint32_t q = 0; q < kFinishPer; ++q) {
+        const bool cur = e[q] != ~0ull && (uint32_t)e[q] < H &&
+                         (kLru ? lu[q] == (uint32_t)(e[q] >> 32) : lu[q] != t);
+        if (cur) ++ncur;
+        else e[q] = ~0ull;
+      }
+      uint32_t tot;
+      uint32_t u = found + block_excl_sum(ncur, scratch, &tot);
+#pragma unroll
+      for (uint32_t q = 0; q < kFinishPer; ++q) {
+        if (e[q] == ~0ull) continue;
+        if (u < M) {
+          vslot[u] = (uint32_t)e[q];
+          if (u == M - 1) last_vic = (uint32_t)e[q];
+        } else if (u == M) {
+          head_hit = off + kFinishPer * tid + q;         // the first current entry that stays
+        }
+        ++u;
+      }
+      found += tot;
+      off += kFinishPer * kThreads;
+    }
+    __syncthreads();
+    if (found < M && tid == 0) atomicOr(status, kFlagInternal);   // cannot happen: M <= unpinned slots
+    const uint32_t nvic = found < M ? found : M;
+
+    // 4. map updates, one thread per unique miss; the victims join the used
+    //    slots
+    for (uint32_t u = tid; u < nvic; u += kThreads) {
+      const uint32_t v = vslot[u];
+      const int32_t p = mpos[u];
+      if (v >= H || p < 0 || (uint32_t)p >= S.history_cap) {
+        atomicOr(status, kFlagInternal);                 // cannot happen; never write out of bounds
+        continue;
+      }
+      const int32_t old = __ldcg(&S.slot2pos[v]);
+      if (old >= 0) {
+        S.pos2slot[old] = -1;
+        atomicAdd(&nevict, 1u);
+      }
+      S.pos2slot[p] = (int32_t)v;
+      S.slot2pos[v] = p;
+      S.last_use[v] = t;
+      atomicOr(&used[v >> 5], 1u << (v & 31));
+      if (S.evlog) {
+        S.evlog[1 + 3 * u] = (int32_t)v;
+        S.evlog[2 + 3 * u] = old;
+        S.evlog[3 + 3 * u] = p;
+      }
+    }
+
+    // 5. the new rows, to the host history below the RAM length, else to the
+    //    recent ring
+    for (uint32_t i = warp; i < T.r; i += kWarps) {
+      uint4* dst = i >= T.to_ram ? reinterpret_cast<uint4*>(S.recent) +
+                                       (size_t)((T.fresh_from + i) & (S.ring_rows - 1u)) * kRowVec
+                                 : reinterpret_cast<uint4*>(const_cast<uint8_t*>(S.hist)) +
+                                       (size_t)(T.fresh_from + i) * kRowVec;
+      const uint4* src = reinterpret_cast<const uint4*>(T.fresh) + (size_t)i * kRowVec;
+      dst[lane] = src[lane];
+      if (lane < kRowVec - 32) dst[32 + lane] = src[32 + lane];
+    }
+    __syncthreads();                                     // the used bitmap is complete
+
+    // 6. LRU queue: every slot used in this step, in slot order, stamped t,
+    //    at the tail
+    uint32_t appended = 0;
+    if (kLru) {
+      const uint64_t stamp = (uint64_t)t << 32;
+      for (uint32_t w0 = 0; w0 < hwords; w0 += kThreads) {
+        const uint32_t w = w0 + tid;
+        uint32_t bits = w < hwords ? used[w] : 0u;
+        uint32_t tot;
+        uint32_t pos = tail + appended + block_excl_sum(__popc(bits), scratch, &tot);
+        while (bits) {
+          const uint32_t bit = __ffs(bits) - 1;
+          bits &= bits - 1;
+          ring_out[pos & qmask] = stamp | (uint64_t)(32 * w + bit);
+          ++pos;
+        }
+        appended += tot;
+      }
+    }
+
+    // 7. counters and stats
+    if (tid == 0) {
+      S.counters[0] = t;
+      S.counters[1] = T.len;
+      if (kLru) {
+        S.counters[2] = nvic > 0 ? head + (head_hit != kNoEntry ? head_hit : min(off, span)) : head;
+        S.counters[3] = tail + appended;
+        S.counters[4] = buf;
+      } else if (nvic > 0) {
+        S.counters[5] = last_vic + 1u == H ? 0u : last_vic + 1u;
+      }
+      unsigned long long* st = S.stats;
+      atomicAdd(st + 0, 1ull);
+      if (M) atomicAdd(st + 3, (unsigned long long)M);
+      if (nevict) atomicAdd(st + 4, (unsigned long long)nevict);
+      atomicAdd(st + 7, (unsigned long long)k);
+      if (S.evlog) S.evlog[0] = (int32_t)nvic;
+      nvic_s = nvic;
+    }
+  }
+
+  // 8. fills: each victim slot receives its row, from the output the gathers
+  // wrote (or from the row's source when only bf16 rows were asked for); the
+  // CTAs of the cluster share the rows, each taking the victim list from
+  // CTA 0 over distributed shared memory first
+  if (F > 1) {
+    cluster_sync();                                      // CTA 0's lists are complete
+    if (f != 0) {
+      const uint32_t n = dsmem_ld_u32(dsmem_addr(&nvic_s, 0));
+      for (uint32_t i = tid; i < n; i += kThreads) {
+        mlist[i] = dsmem_ld_u32(dsmem_addr(&mlist[i], 0));
+        vslot[i] = dsmem_ld_u32(dsmem_addr(&vslot[i], 0));
+        mpos[i] = (int32_t)dsmem_ld_u32(dsmem_addr(&mpos[i], 0));
+      }
+      if (tid == 0) nvic_s = n;
+    }
+  }
+  __syncthreads();
+  const uint32_t nvic = nvic_s;
+  const uint32_t pieces = nvic * kRowVec;
+  const uint32_t share = (pieces + F - 1) / F;
+  const uint32_t plo = min(pieces, f * share), phi = min(pieces, plo + share);
+  for (uint32_t base = plo; base < phi; base += kFillInFlight * kThreads) {
+    uint4 x[kFillInFlight];
+    uint32_t dst[kFillInFlight];                          // piece index in the hot cache, or kNoEntry
+#pragma unroll
+    for (uint32_t q = 0; q < kFillInFlight; ++q) {
+      const uint32_t i = base + q * kThreads + tid;
+      dst[q] = kNoEntry;
+      x[q] = make_uint4(0, 0, 0, 0);
+      if (i < phi) {
+        const uint32_t u = i / kRowVec, piece = i - u * kRowVec;
+        const uint32_t v = vslot[u];
+        if (v < H) {
+          const uint4* src;
+          if (T.out_rows) {
+            src = reinterpret_cast<const uint4*>(T.out_rows) + (size_t)mlist[u] * kRowVec;
+          } else {
+            bool host;
+            src = miss_source(S, T, (uint32_t)mpos[u], &host);
+          }
+          x[q] = __ldcg(src + piece);
+          dst[q] = v * kRowVec + piece;
+        }
+      }
+    }
+#pragma unroll
+    for (uint32_t q = 0; q < kFillInFlight; ++q)
+      if (dst[q] != kNoEntry) reinterpret_cast<uint4*>(S.hot)[dst[q]] = x[q];
+  }
+  if (F > 1) cluster_sync();                             // no CTA reads CTA 0's lists any more
+}
+
+// ------------------------------------------------------------ launch
+struct LayersConfig {
+  bool init = false;
+  int active[5] = {0, 0, 0, 0, 0};     // select clusters of 1, 2, 4, 8, 16 CTAs that fit at once (resident)
+  int active_stream[5] = {0, 0, 0, 0, 0};
+  int active_finish[4] = {0, 0, 0, 0};   // finish clusters of 1, 2, 4, 8 CTAs that fit at once
+  int force_select = 0;
+};
+LayersConfig g_layers[64];
+
+int active_clusters(const void* kern, int C, size_t smem) {
+  cudaLaunchConfig_t lc = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  lc.gridDim = dim3(C, 1, 1);
+  lc.blockDim = dim3(kThreads, 1, 1);
+  lc.dynamicSmemBytes = smem;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &lc) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+cudaError_t layers_init(LayersConfig** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  LayersConfig& cfg = g_layers[dev & 63];
+  if (!cfg.init) {
+    const void* sel[2] = {(const void*)layers_select_kernel<true>, (const void*)layers_select_kernel<false>};
+    for (const void* kern : sel) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSelectMaxSmem);
+      if (e != cudaSuccess) return e;
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+        cudaGetLastError();
+    }
+    for (const void* kern : {(const void*)layers_finish_kernel<true>, (const void*)layers_finish_kernel<false>}) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)finish_smem_bytes(KVO_MAX_K, KVO_MAX_HOT_ROWS));
+      if (e != cudaSuccess) return e;
+    }
+    for (int i = 0; i < 4; ++i)
+      cfg.active_finish[i] = active_clusters((const void*)layers_finish_kernel<true>, 1 << i,
+                                             finish_smem_bytes(KVO_MAX_K, KVO_MAX_HOT_ROWS));
+    for (int i = 0; i < 5; ++i) {
+      cfg.active[i] = active_clusters(sel[0], 1 << i, kSelectMaxSmem);
+      cfg.active_stream[i] = i ? active_clusters(sel[1], 1 << i, topk_detail::kTopkMaxDynSmem) : 0;
+    }
+    // KVO_SELECT_CLUSTER (1, 2, 4, 8 or 16): a tuning knob that fixes the
+    // selection's cluster size where it fits
+    if (const char* env = std::getenv("KVO_SELECT_CLUSTER")) {
+      const int m = std::atoi(env);
+      if (m == 1 || m == 2 || m == 4 || m == 8 || m == 16) cfg.force_select = m;
+    }
+    cfg.init = true;
+  }
+  *out = &cfg;
+  return cudaSuccess;
+}
+
+// CTAs per selecting cluster, at least min_cluster: the size with the fewest
+// waves of clusters, ties to the larger clusters (so the largest size whose
+// clusters all run in one wave, when there is one).
+uint32_t select_cluster(const int* active, uint32_t nsel, int max_cluster, int min_cluster = 1) {
+  int best = 0;
+  uint32_t best_waves = 0xffffffffu;
+  for (int i = 4; i >= 0; --i) {
+    const int C = 1 << i;
+    if (C > max_cluster || C < min_cluster || active[i] <= 0) continue;
+    const uint32_t waves = (nsel + (uint32_t)active[i] - 1) / (uint32_t)active[i];
+    if (waves < best_waves) {
+      best_waves = waves;
+      best = C;
+    }
+  }
+  return (uint32_t)best;
+}
+
+LayerCall make_call(const StepTask& s, uint32_t layer) {
+  LayerCall t;
+  std::memset(static_cast<void*>(&t), 0, sizeof t);
+  const LayerView& L = s.L;
+  t.scores = s.scores;
+  t.idx = s.idx;
+  t.out_rows = s.out_rows;
+  t.out_bf16 = s.out_bf16;
+  t.fresh = s.r ? static_cast<const uint8_t*>(s.new_rows) : nullptr;
+  t.layer = layer;
+  t.n = s.n;
+  t.ram_len = L.ram_len;
+  t.len = s.old_len + s.r;
+  t.fresh_from = s.old_len;
+  t.r = s.r;
+  t.to_ram = !L.ring_rows ? s.r : L.ram_len <= s.old_len ? 0u : (L.ram_len - s.old_len < s.r ? L.ram_len - s.old_len : s.r);
+  return t;
+}
+
+cudaError_t launch_config(const void* kern, dim3 grid, uint32_t threads, size_t smem, cudaStream_t stream,
+                          uint32_t cluster, bool after_previous, cudaLaunchConfig_t* lc, cudaLaunchAttribute* attr) {
+  (void)kern;
+  *lc = cudaLaunchConfig_t{};
+  lc->gridDim = grid;
+  lc->blockDim = dim3(threads, 1, 1);
+  lc->dynamicSmemBytes = smem;
+  lc->stream = stream;
+  uint32_t na = 0;
+  if (cluster > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = cluster;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  if (after_previous) {                                  // scheduled early, waits in griddepcontrol.wait
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  lc->attrs = attr;
+  lc->numAttrs = na;
+  return cudaSuccess;
+}
+
+}  // namespace
+
+namespace {
+
+// Launch parameters of one part of a call, built before its first launch.
+struct PartBuffers {
+  std::vector<LayerBatch> sel, res;
+  std::vector<uint32_t> sel_c;
+  std::vector<uint8_t> sel_resident;
+};
+
+// One part of a call on one stream: the selections of its selecting layers,
+// then the gathers, then the finishes of all its layers.  which[0..n): the
+// part's tasks.  after_select: recorded once the selections are enqueued
+// (NULL: none).  ev: the phase events (NULL: none).
+cudaError_t enqueue_part(LayersConfig* cfg, const StepTask* tasks, const uint32_t* layers, const uint32_t* which,
+                         uint32_t n, uint32_t k, const LayerStatic* statics, uint32_t* status, int max_cluster,
+                         cudaStream_t stream, cudaEvent_t* ev, cudaEvent_t after_select, PartBuffers& pb,
+                         uint32_t* launched) {
+  cudaError_t e;
+  pb.sel.clear();
+  pb.res.clear();
+  pb.sel_c.clear();
+  pb.sel_resident.clear();
+  for (uint32_t w = 0; w < n; ++w) {
+    const uint32_t i = which[w];
+    if (!tasks[i].scores) continue;
+    if (pb.sel.empty() || pb.sel.back().ntasks == kBatchTasks) {
+      pb.sel.emplace_back();
+      pb.sel.back().ntasks = 0;
+    }
+    LayerBatch& sb = pb.sel.back();
+    sb.t[sb.ntasks++] = make_call(tasks[i], layers[i]);
+  }
+  for (LayerBatch& sb : pb.sel) {
+    uint32_t nmax = 0;
+    for (uint32_t i = 0; i < sb.ntasks; ++i) nmax = sb.t[i].n > nmax ? sb.t[i].n : nmax;
+    // resident keys when every selecting layer's slice fits the CTA's
+    // shared memory (the smallest such cluster and up), else the filtered
+    // route
+    int cmin = 1;
+    while (cmin <= 16 && (uint64_t)topk_detail::topk_chunk(nmax, (uint32_t)cmin) * 4u > kSelectMaxSmem) cmin <<= 1;
+    if (cfg->force_select && cfg->force_select >= cmin) cmin = cfg->force_select;
+    uint32_t C = cmin <= 16 ? select_cluster(cfg->active, sb.ntasks, cfg->force_select ? cmin : max_cluster, cmin)
+                            : 0u;
+    const bool resident = C != 0;
+    if (!resident) C = select_cluster(cfg->active_stream, sb.ntasks, max_cluster, 2);
+    if (!C) return cudaErrorInvalidConfiguration;
+    sb.statics = statics;
+    sb.k = k;
+    sb.cand_bytes = resident ? (uint32_t)topk_detail::topk_chunk(nmax, C) * 4u : topk_detail::kTopkMaxDynSmem;
+    pb.sel_c.push_back(C);
+    pb.sel_resident.push_back(resident ? 1 : 0);
+  }
+  for (uint32_t first = 0; first < n; first += kBatchTasks) {
+    pb.res.emplace_back();
+    LayerBatch& rb = pb.res.back();
+    rb.ntasks = n - first < kBatchTasks ? n - first : kBatchTasks;
+    for (uint32_t i = 0; i < rb.ntasks; ++i) rb.t[i] = make_call(tasks[which[first + i]], layers[which[first + i]]);
+    rb.statics = statics;
+    rb.k = k;
+    rb.chunks = (k + kGatherEntries - 1) / kGatherEntries;
+  }
+
+  cudaLaunchConfig_t lc;
+  cudaLaunchAttribute attr[2];
+  bool after = false;                                    // a launch of this part precedes on the stream
+  if (ev && (e = cudaEventRecord(ev[0], stream)) != cudaSuccess) return e;
+  for (size_t i = 0; i < pb.sel.size(); ++i) {
+    const bool resident = pb.sel_resident[i] != 0;
+    launch_config(nullptr, dim3(pb.sel_c[i] * pb.sel[i].ntasks, 1, 1), kThreads,
+                  resident ? pb.sel[i].cand_bytes : topk_detail::kTopkMaxDynSmem, stream, pb.sel_c[i], false, &lc,
+                  attr);
+    e = resident ? cudaLaunchKernelEx(&lc, layers_select_kernel<true>, pb.sel[i])
+                 : cudaLaunchKernelEx(&lc, layers_select_kernel<false>, pb.sel[i]);
+    if (e != cudaSuccess) return e;
+    after = true;
+    ++*launched;
+  }
+  if (after_select && (e = cudaEventRecord(after_select, stream)) != cudaSuccess) return e;
+  if (ev && (e = cudaEventRecord(ev[1], stream)) != cudaSuccess) return e;
+  // (an event between two launches ends the early scheduling of the second)
+  const bool pdl = !ev && !after_select;
+  for (const LayerBatch& rb : pb.res) {
+    launch_config(nullptr, dim3(rb.ntasks * rb.chunks, 1, 1), kGatherThreads, 0, stream, 1, pdl && after, &lc, attr);
+    if ((e = cudaLaunchKernelEx(&lc, layers_gather_kernel, rb, status)) != cudaSuccess) return e;
+    after = true;
+    ++*launched;
+  }
+  if (ev && (e = cudaEventRecord(ev[2], stream)) != cudaSuccess) return e;
+  const size_t fsmem = finish_smem_bytes(k, tasks[which[0]].L.hot_rows);
+  for (const LayerBatch& rb : pb.res) {
+    // CTAs per layer for the fills: the largest cluster whose clusters all
+    // run at once (one CTA per layer for a deep stack)
+    uint32_t F = 1;
+    for (int i = 3; i >= 1; --i)
+      if (cfg->active_finish[i] >= (int)rb.ntasks) {
+        F = 1u << i;
+        break;
+      }
+    launch_config(nullptr, dim3(rb.ntasks * F, 1, 1), kThreads, fsmem, stream, F, !ev, &lc, attr);
+    e = tasks[which[0]].L.policy == KVO_POLICY_LRU
+            ? cudaLaunchKernelEx(&lc, layers_finish_kernel<true>, rb, status)
+            : cudaLaunchKernelEx(&lc, layers_finish_kernel<false>, rb, status);
+    if (e != cudaSuccess) return e;
+    ++*launched;
+  }
+  if (ev && (e = cudaEventRecord(ev[3], stream)) != cudaSuccess) return e;
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_layers(const StepTask* tasks, const uint32_t* layers, uint32_t ntasks, uint32_t k,
+                          const LayerStatic* statics, uint32_t* status, int max_cluster, cudaStream_t stream,
+                          cudaEvent_t* ev, uint32_t* launched) {
+  LayersConfig* cfg = nullptr;
+  cudaError_t e = layers_init(&cfg);
+  if (e != cudaSuccess) return e;
+  static thread_local PartBuffers pb;
+  static thread_local std::vector<uint32_t> all;
+  all.resize(ntasks);
+  for (uint32_t i = 0; i < ntasks; ++i) all[i] = i;
+  return enqueue_part(cfg, tasks, layers, all.data(), ntasks, k, statics, status, max_cluster, stream, ev, nullptr,
+                      pb, launched);
+}
+
+}  // namespace kvo

@@ -506,6 +506,7 @@ int2* g_noalloc_addr[64] = {};   // per device, looked up by the first call on i
 extern "C" kvo_status kvo_copy_blocks_noalloc(const void* src, void* dst, int64_t block_bytes,
                                               const int32_t* pairs, int64_t n, void* stream) {
   if (n < 0 || n > KVO_NOALLOC_MAX_PAIRS || block_bytes <= 0 || (block_bytes & 15) ||
+      block_bytes / 16 > (int64_t)UINT32_MAX ||   // the kernel counts a block's 16-byte pieces in 32 bits
       (n > 0 && (!src || !dst || !pairs || (reinterpret_cast<uintptr_t>(src) & 15u) ||
                  (reinterpret_cast<uintptr_t>(dst) & 15u))))
     return KVO_EINVAL;

@@ -122,6 +122,15 @@ __device__ __forceinline__ bool miss_from_host(const ResolveArgs& a, int32_t p) 
   return !(a.L.ring_rows && (uint32_t)p >= a.L.ram_len);
 }
 
+// A row appended by this launch whose position the host history (RAM)
+// already holds at this step: without a recent ring every appended row, with
+// one the rows whose copyback batch completes in this step.  Such a miss is
+// counted as a RAM read, as the append-then-resolve order defines it; the
+// launch serves it from the row's device copy, which holds the same bytes.
+__device__ __forceinline__ bool fresh_in_ram(const ResolveArgs& a, int32_t p) {
+  return a.fresh && (uint32_t)p >= a.fresh_from && !(a.L.ring_rows && (uint32_t)p >= a.L.ram_len);
+}
+
 struct SmemLayout {
   uint32_t pinbits, meta_slot, meta_pos, uniq, sel, vslot, mlist, window, fullpin, total;
 };
@@ -282,6 +291,7 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
   __shared__ uint32_t last_vic;                    // CTA 0: the last victim (circular policy)
   __shared__ uint32_t nevict_cta;
   __shared__ uint32_t cta_hits, cta_inv, cta_host;
+  __shared__ uint32_t cta_fresh_ram;               // misses on this launch's rows that RAM already holds
   __shared__ __align__(8) uint64_t wbar;           // CTA 0: completion of the window copy
   __shared__ __align__(8) uint64_t gbar;           // other CTAs: completion of the staged rows
 
@@ -340,6 +350,7 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
     nevict_cta = 0;
     ring_off = 0;
     head_hit = kNoRank;
+    cta_fresh_ram = 0;
   }
   // CTA 0 copies the head of the queue now (one or two bulk copies from a
   // 16-byte boundary: window[sh + o] is the entry o places after the head);
@@ -357,6 +368,7 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
     bulk_copy_g2s(window, ring_in + a0, first * 8u, &wbar);
     if (wcopy > first) bulk_copy_g2s(window + first, ring_in, (wcopy - first) * 8u, &wbar);
   }
+  __syncthreads();                                  // the counters above are zero before P1 adds into them
   // B0: every CTA of the cluster is running (and has zeroed what others add
   // into) before any DSMEM access; classification overlaps the barrier.
   cluster_arrive();
@@ -388,6 +400,7 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
         atomicMin(&L.pos2slot[p], (int32_t)j - (int32_t)k - 1);
         ++nmiss;
         nhost += miss_from_host(a, p);
+        if (fresh_in_ram(a, p)) atomicAdd(&cta_fresh_ram, 1u);
       }
     }
     meta_slot[jj] = slot;
@@ -734,7 +747,11 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
     if (lane < kRowVec - 32) dst[32 + lane] = y;
   }
   if (staged) bulk_wait_all();                      // the output slice and the fills have left shared memory
-  if (staged && !gather_ok) mbar_wait_bounded(&gbar, 0, kWindowPolls);   // nothing may land after the exit
+  // A copy that outlasted the wait is waited for once more (bounded); if it
+  // still has not landed, the status says so and the context refuses further
+  // launches: the copy's bytes could land in shared memory that another CTA
+  // owns after this one exits.
+  if (staged && !gather_ok && tid == 0 && !mbar_wait_bounded(&gbar, 0, kWindowPolls)) atomicOr(a.status, kFlagInflight);
 
   // ---------------------------------------------------------------- P5
   // The used slots of this CTA's range, in slot order, stamped t, at the
@@ -759,8 +776,8 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
     }
   }
   if (L.evlog && r == 0 && tid == 0) L.evlog[0] = (int32_t)M;
-  // a window copy that never completed must not land after this CTA exits
-  if (r == 0 && !win_ok) mbar_wait_bounded(&wbar, 0, kWindowPolls);
+  // a window copy that outlasted the wait: the same second, bounded wait
+  if (r == 0 && !win_ok && tid == 0 && !mbar_wait_bounded(&wbar, 0, kWindowPolls)) atomicOr(a.status, kFlagInflight);
 
   // ------------------------------------------------------------- stats
   __syncthreads();
@@ -769,7 +786,8 @@ __device__ __forceinline__ void resolve_body(const ResolveArgs& a, uint8_t* dyn_
     if (cta_hits) atomicAdd(st + 1, (unsigned long long)cta_hits);
     if (cta_miss) {
       atomicAdd(st + 2, (unsigned long long)cta_miss);
-      if (cta_host) atomicAdd(st + 6, (unsigned long long)cta_host * KVO_ROW_BYTES);
+      if (cta_host + cta_fresh_ram)
+        atomicAdd(st + 6, (unsigned long long)(cta_host + cta_fresh_ram) * KVO_ROW_BYTES);
     }
     if (nevict_cta) atomicAdd(st + 4, (unsigned long long)nevict_cta);
     if (cta_inv) {

@@ -1,7 +1,6 @@
 // Fused decode step of one layer (kvo_decode_step): append the new rows,
 // select the top-K positions and resolve + gather them, in one cluster
-// launch; and the same for many layers at once (kvo_decode_layers), one
-// cluster per layer in one launch.
+// launch.  (Many layers at once go through kvo_layers.cu.)
 //
 // "From 1M Total to 15+ x 1M Contexts: GLM-5.3 KV Cache Offloading",
 // "Decision three: let the GPU manage the hot cache directly": the CPU stays
@@ -9,9 +8,7 @@
 // back to back.  Fusing them also removes two kernel launches and the trip of
 // the selection through global memory: the top-K compaction hands each
 // selected position straight to the CTA that resolves it, over distributed
-// shared memory.  Section "Separate historical capacity from the current
-// working set": later layers reuse a selection and keep their own KV, so a
-// layer's task may also bring its selection instead of scores.
+// shared memory.
 //
 // The step's results are those of append, then select, then resolve: the
 // selection sees the new rows, and the resolve reads them from their device
@@ -37,9 +34,10 @@ struct StepArgs {
   uint32_t n;
   int32_t* idx;               // the selection, also returned to the caller
   const uint4* new_rows;      // r rows appended in this step (device memory)
-  uint4* hist_dst;            // device address of history row `old length` (no recent ring)
+  uint4* hist_dst;            // device address of history row `old length`
   uint32_t old_len;
   uint32_t r;
+  uint32_t to_ram;            // the first to_ram new rows go to the host history, the rest to the recent ring
   uint32_t topk_bytes;        // dynamic shared memory of the top-K phase (resident keys or candidates)
 };
 
@@ -63,15 +61,17 @@ __device__ __forceinline__ void decode_body(const StepArgs& s, uint8_t* dyn_smem
     });
     cluster_sync();                                // every selected position delivered
   }
-  // The append: one warp per new row, to the recent ring when there is one,
-  // else to the host history.  This call reads these rows from their device
-  // copy (the resolve's fresh rows), so they are written while CTAs 1..C-1
-  // wait for CTA 0's victims rather than by CTA 0 ahead of the top-K.
+  // The append: one warp per new row, to the host history when the row is
+  // below the step's RAM length (always without a recent ring; with one,
+  // the rows whose batch of the copyback completes in this step), else to
+  // the ring.  This call reads these rows from their device copy (the
+  // resolve's fresh rows), so they are written while CTAs 1..C-1 wait for
+  // CTA 0's victims rather than by CTA 0 ahead of the top-K.
   const LayerView& L = s.R.L;
   resolve_body<kLru>(s.R, rdyn, [&](uint32_t w, uint32_t nw) {
     for (uint32_t i = w; i < s.r; i += nw) {
-      uint4* dst = L.ring_rows ? reinterpret_cast<uint4*>(L.recent) + (size_t)((s.old_len + i) & (L.ring_rows - 1u)) * kVec
-                               : s.hist_dst + (size_t)i * kVec;
+      uint4* dst = i >= s.to_ram ? reinterpret_cast<uint4*>(L.recent) + (size_t)((s.old_len + i) & (L.ring_rows - 1u)) * kVec
+                                 : s.hist_dst + (size_t)i * kVec;
       dst[lane] = s.new_rows[(size_t)i * kVec + lane];
       if (lane < kVec - 32) dst[32 + lane] = s.new_rows[(size_t)i * kVec + 32 + lane];
     }
@@ -86,41 +86,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const StepArgs
   decode_body<kResident, kLru>(s, dyn_smem, &rsm);
 }
 
-// The tasks of one launch travel as its parameter (no staging buffer, no
-// upload): as many as fit the 32 KB parameter space.
-constexpr uint32_t kParamTasks = 30000u / sizeof(StepArgs);
-struct TaskBatch {
-  StepArgs t[kParamTasks];
-};
-
-// Cluster blockIdx.x / clusterDim.x runs task b.t[that index].
-template <bool kResident, bool kLru>
-__global__ void __launch_bounds__(kThreads, 1) decode_layers_kernel(const __grid_constant__ TaskBatch b) {
-  extern __shared__ __align__(16) uint8_t dyn_smem[];
-  __shared__ RadixSmem rsm;
-  decode_body<kResident, kLru>(b.t[blockIdx.x / cluster_size()], dyn_smem, &rsm);
-}
-
 struct StepConfig {
   bool init = false;
   int cluster = 0;
-  int active16 = 0;          // 16-CTA clusters of the batched kernel that fit at once
 };
 StepConfig g_step[64];
 
 constexpr size_t kStepMaxDynSmem = 187 * 1024;     // 227 KB less the static radix histograms
 
-cudaError_t step_init(int* cluster, int* active16 = nullptr) {
+cudaError_t step_init(int* cluster) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   StepConfig& cfg = g_step[dev & 63];
   if (!cfg.init) {
-    const void* kernels[8] = {
-        (const void*)decode_step_kernel<true, true>,   (const void*)decode_step_kernel<false, true>,
-        (const void*)decode_step_kernel<true, false>,  (const void*)decode_step_kernel<false, false>,
-        (const void*)decode_layers_kernel<true, true>, (const void*)decode_layers_kernel<false, true>,
-        (const void*)decode_layers_kernel<true, false>, (const void*)decode_layers_kernel<false, false>};
+    const void* kernels[4] = {(const void*)decode_step_kernel<true, true>, (const void*)decode_step_kernel<false, true>,
+                              (const void*)decode_step_kernel<true, false>, (const void*)decode_step_kernel<false, false>};
     int c1 = (int)kMaxCluster;
     for (const void* kern : kernels) {
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStepMaxDynSmem);
@@ -130,28 +111,9 @@ cudaError_t step_init(int* cluster, int* active16 = nullptr) {
     }
     cfg.cluster = c1;
     if (cfg.cluster == 0) return cudaErrorInvalidConfiguration;
-    if (cfg.cluster >= 16) {
-      cudaLaunchConfig_t lc = {};
-      cudaLaunchAttribute attr[1];
-      attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = 16;
-      attr[0].val.clusterDim.y = 1;
-      attr[0].val.clusterDim.z = 1;
-      lc.gridDim = dim3(16, 1, 1);
-      lc.blockDim = dim3(kThreads, 1, 1);
-      lc.dynamicSmemBytes = kStepMaxDynSmem;
-      lc.attrs = attr;
-      lc.numAttrs = 1;
-      if (cudaOccupancyMaxActiveClusters(&cfg.active16, (const void*)decode_layers_kernel<false, true>, &lc) !=
-          cudaSuccess) {
-        cudaGetLastError();
-        cfg.active16 = 0;
-      }
-    }
     cfg.init = true;
   }
   *cluster = cfg.cluster;
-  if (active16) *active16 = cfg.active16;
   return cudaSuccess;
 }
 
@@ -185,6 +147,10 @@ void build_step(const StepTask& t, uint32_t k, uint32_t* status, uint32_t C, Ste
   s->hist_dst = reinterpret_cast<uint4*>(const_cast<uint8_t*>(L.hist) + (size_t)t.old_len * KVO_ROW_BYTES);
   s->old_len = t.old_len;
   s->r = t.r;
+  // L.ram_len is the RAM length after this step's append and copyback
+  s->to_ram = !L.ring_rows ? t.r
+              : L.ram_len <= t.old_len ? 0u
+              : L.ram_len - t.old_len < t.r ? L.ram_len - t.old_len : t.r;
   // staged gather when the rows fit, else rows through registers
   a.stage_rows = L.gather_mode != KVO_GATHER_LOADS ? (a.kchunk < kStageMax ? a.kchunk : kStageMax) : 0u;
   a.stage_min_miss_pct = L.gather_mode == KVO_GATHER_STAGED ? 0u : L.auto_miss_pct;
@@ -201,30 +167,23 @@ void build_step(const StepTask& t, uint32_t k, uint32_t* status, uint32_t C, Ste
   s->topk_bytes = (uint32_t)topk_res;               // replaced by *stream_topk when keys are streamed
 }
 
-cudaError_t launch(uint32_t C, uint32_t nclusters, size_t smem, cudaStream_t stream, bool resident, bool lru,
-                   const StepArgs* one, const TaskBatch* many) {
+cudaError_t launch(uint32_t C, size_t smem, cudaStream_t stream, bool resident, bool lru, const StepArgs& one) {
   cudaLaunchConfig_t lc = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  lc.gridDim = dim3(C * nclusters, 1, 1);
+  lc.gridDim = dim3(C, 1, 1);
   lc.blockDim = dim3(kThreads, 1, 1);
   lc.dynamicSmemBytes = smem;
   lc.stream = stream;
   lc.attrs = attr;
   lc.numAttrs = 1;
-  if (one) {
-    if (resident) return lru ? cudaLaunchKernelEx(&lc, decode_step_kernel<true, true>, *one)
-                             : cudaLaunchKernelEx(&lc, decode_step_kernel<true, false>, *one);
-    return lru ? cudaLaunchKernelEx(&lc, decode_step_kernel<false, true>, *one)
-               : cudaLaunchKernelEx(&lc, decode_step_kernel<false, false>, *one);
-  }
-  if (resident) return lru ? cudaLaunchKernelEx(&lc, decode_layers_kernel<true, true>, *many)
-                           : cudaLaunchKernelEx(&lc, decode_layers_kernel<true, false>, *many);
-  return lru ? cudaLaunchKernelEx(&lc, decode_layers_kernel<false, true>, *many)
-             : cudaLaunchKernelEx(&lc, decode_layers_kernel<false, false>, *many);
+  if (resident) return lru ? cudaLaunchKernelEx(&lc, decode_step_kernel<true, true>, one)
+                           : cudaLaunchKernelEx(&lc, decode_step_kernel<true, false>, one);
+  return lru ? cudaLaunchKernelEx(&lc, decode_step_kernel<false, true>, one)
+             : cudaLaunchKernelEx(&lc, decode_step_kernel<false, false>, one);
 }
 
 }  // namespace
@@ -245,41 +204,7 @@ cudaError_t launch_decode_step(const LayerView& L, const void* new_rows, uint32_
   if (!need_stream) return cudaErrorInvalidValue;
   const bool resident = need_res != 0;
   if (!resident) s.topk_bytes = stream_topk;
-  return launch(C, 1, resident ? need_res : need_stream, stream, resident, L.policy == KVO_POLICY_LRU, &s, nullptr);
-}
-
-cudaError_t launch_decode_layers(const StepTask* tasks, uint32_t ntasks, uint32_t k, uint32_t* status,
-                                 int max_cluster, cudaStream_t stream) {
-  int cl = 0, active16 = 0;
-  cudaError_t e = step_init(&cl, &active16);
-  if (e != cudaSuccess) return e;
-  // 16-CTA clusters while the tasks fit one wave of them (a cluster stays
-  // inside one GPC: 7 at a time on a 152-SM GB300), else 8 (15 at a time:
-  // 0.60 vs 0.47 G rows/s on the 78-layer stack)
-  int want = cl < max_cluster ? cl : max_cluster;
-  if (want > 8 && (uint32_t)active16 < ntasks) want = 8;
-  const uint32_t C = (uint32_t)want;
-  static thread_local TaskBatch b;                  // 30 KB: kept off the stack
-  for (uint32_t first = 0; first < ntasks; first += kParamTasks) {
-    const uint32_t nb = ntasks - first < kParamTasks ? ntasks - first : kParamTasks;
-    size_t res_max = 0, stream_max = 0;
-    bool resident = true;
-    static thread_local uint32_t stream_topk[kParamTasks];
-    for (uint32_t i = 0; i < nb; ++i) {
-      size_t need_res = 0, need_stream = 0;
-      build_step(tasks[first + i], k, status, C, &b.t[i], &need_res, &need_stream, &stream_topk[i]);
-      if (!need_stream) return cudaErrorInvalidValue;
-      resident = resident && need_res != 0;
-      res_max = need_res > res_max ? need_res : res_max;
-      stream_max = need_stream > stream_max ? need_stream : stream_max;
-    }
-    if (!resident)
-      for (uint32_t i = 0; i < nb; ++i) b.t[i].topk_bytes = stream_topk[i];
-    e = launch(C, nb, resident ? res_max : stream_max, stream, resident, tasks[first].L.policy == KVO_POLICY_LRU,
-               nullptr, &b);
-    if (e != cudaSuccess) return e;
-  }
-  return cudaSuccess;
+  return launch(C, resident ? need_res : need_stream, stream, resident, L.policy == KVO_POLICY_LRU, s);
 }
 
 }  // namespace kvo

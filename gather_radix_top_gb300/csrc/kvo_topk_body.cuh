@@ -12,9 +12,10 @@
 // Resident route (a CTA's keys fit in shared memory):
 //   1. the keys are loaded into shared memory once;
 //   2. an MSB-first 8-bit radix select finds the cut; each pass builds a
-//      warp-aggregated per-CTA histogram and adds its nonzero bins into every
-//      CTA's cluster-wide histogram over distributed shared memory (one
-//      cluster barrier per pass);
+//      per-CTA histogram in shared memory, adds each nonzero bin into the
+//      one CTA that owns that bin over distributed shared memory, and after
+//      one cluster barrier every CTA reads all bins back from their owners
+//      and scans them, so that every CTA finds the same bucket;
 //   3. an ordered compaction writes the chosen positions in ascending order:
 //      per-CTA counts (taken from the radix histograms) are published over
 //      DSMEM, then each CTA walks its range four keys per thread, one block

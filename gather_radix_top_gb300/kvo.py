@@ -30,13 +30,14 @@ EXPORTED = [
     "kvo_select_topk_batch",
     "kvo_resolve_gather", "kvo_resolve_gather_multi", "kvo_decode_step", "kvo_decode_step_host", "kvo_decode_layers", "kvo_sync", "kvo_get_stats", "kvo_history_length",
     "kvo_debug_dump_layer", "kvo_debug_record_evictions", "kvo_debug_evictions", "kvo_set_policy",
-    "kvo_debug_layer_counters", "kvo_set_recent_ring", "kvo_flush_ring", "kvo_ram_length",
+    "kvo_debug_layer_counters", "kvo_debug_raise_status", "kvo_set_recent_ring", "kvo_flush_ring", "kvo_ram_length",
     "kvo_debug_read_history", "kvo_set_gather_mode",
     "kvo_probe_host_read",
     "kvo_tier_blocks", "kvo_pool_create", "kvo_pool_destroy", "kvo_pool_alloc", "kvo_pool_write",
     "kvo_pool_read", "kvo_pool_fill", "kvo_store_blocks", "kvo_pool_release", "kvo_restore_blocks",
     "kvo_pool_sync", "kvo_pool_block_table", "kvo_pool_get_stats", "kvo_pool_debug_fail_after",
-    "kvo_pool_debug_free_queue", "kvo_copy_blocks_noalloc",
+    "kvo_pool_debug_free_queue", "kvo_copy_blocks_noalloc", "kvo_set_phase_timing", "kvo_layers_phase_times",
+    "kvo_layers_launch_count", "kvo_probe_host_touch", "kvo_debug_history_host",
 ]
 
 
@@ -111,6 +112,7 @@ def lib() -> ctypes.CDLL:
         "kvo_ram_length": (ctypes.c_int, [_vp, _i32, ctypes.POINTER(_i64)]),
         "kvo_debug_read_history": (ctypes.c_int, [_vp, _i32, _i64, _i64, _vp]),
         "kvo_debug_layer_counters": (ctypes.c_int, [_vp, _i32, _vp]),
+        "kvo_debug_raise_status": (ctypes.c_int, [_vp, ctypes.c_uint32]),
         "kvo_tier_blocks": (_i64, [_i64, _i64]),
         "kvo_pool_create": (ctypes.c_int, [_i32, _i64, _i32, _i32, _i64, ctypes.POINTER(_vp)]),
         "kvo_pool_destroy": (ctypes.c_int, [_vp]),
@@ -127,6 +129,11 @@ def lib() -> ctypes.CDLL:
         "kvo_pool_debug_fail_after": (ctypes.c_int, [_vp, _i32, _i64]),
         "kvo_pool_debug_free_queue": (ctypes.c_int, [_vp, _i32, _vp, _i64, ctypes.POINTER(_i64)]),
         "kvo_copy_blocks_noalloc": (ctypes.c_int, [_vp, _vp, _i64, _vp, _i64, _vp]),
+        "kvo_set_phase_timing": (ctypes.c_int, [_vp, _i32]),
+        "kvo_layers_phase_times": (ctypes.c_int, [_vp, _vp, _vp]),
+        "kvo_layers_launch_count": (ctypes.c_int, [_vp, _vp]),
+        "kvo_probe_host_touch": (ctypes.c_int, [_vp, _i64, _i64, _vp, _vp]),
+        "kvo_debug_history_host": (ctypes.c_int, [_vp, _i32, _vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -414,6 +421,13 @@ def kvo_probe_host_read(src_pinned, sink, stream=None) -> None:
                                      _dev_ptr(sink), _stream_ptr(stream)), "kvo_probe_host_read")
 
 
+def kvo_probe_host_touch(addr: int, nbytes: int, stride: int, sink, stream=None) -> None:
+    """One 16-byte zero-copy load every `stride` bytes of pinned host memory
+    at `addr` (an address, e.g. Context.history_host); sink: 16-byte CUDA tensor."""
+    _check(lib().kvo_probe_host_touch(ctypes.c_void_p(addr), nbytes, stride, _dev_ptr(sink), _stream_ptr(stream)),
+           "kvo_probe_host_touch")
+
+
 class Context:
     """Owns one kvo context; methods forward to the kvo_* calls above."""
 
@@ -465,6 +479,28 @@ class Context:
     def decode_layers_prepared(self, arr, k, stream=None):
         kvo_decode_layers_prepared(self.handle, arr, k, stream)
 
+    def set_phase_timing(self, on=True):
+        _check(lib().kvo_set_phase_timing(self.handle, 1 if on else 0), "kvo_set_phase_timing")
+
+    def history_host(self, layer) -> int:
+        """Host address of the layer's pinned history (read-only use)."""
+        p = ctypes.c_void_p()
+        _check(lib().kvo_debug_history_host(self.handle, layer, ctypes.byref(p)), "kvo_debug_history_host")
+        return p.value
+
+    def layers_launch_count(self) -> int:
+        n = ctypes.c_int64()
+        _check(lib().kvo_layers_launch_count(self.handle, ctypes.byref(n)), "kvo_layers_launch_count")
+        return n.value
+
+    def layers_phase_times(self):
+        """(select, gather, finish) milliseconds summed over the recorded
+        kvo_decode_layers calls, and the number of calls."""
+        ms = (ctypes.c_double * 3)()
+        calls = ctypes.c_int64()
+        _check(lib().kvo_layers_phase_times(self.handle, ms, ctypes.byref(calls)), "kvo_layers_phase_times")
+        return (ms[0], ms[1], ms[2]), calls.value
+
     def sync(self, stream=None) -> int:
         return kvo_sync(self.handle, stream)
 
@@ -497,6 +533,9 @@ class Context:
 
     def counters(self, layer) -> dict:
         return kvo_debug_layer_counters(self.handle, layer)
+
+    def raise_status(self, bits):
+        _check(lib().kvo_debug_raise_status(self.handle, bits), "kvo_debug_raise_status")
 
     def record_evictions(self, on=True):
         kvo_debug_record_evictions(self.handle, on)
@@ -621,6 +660,18 @@ def kvo_copy_blocks_noalloc(src, dst, block_bytes: int, pairs, stream=None) -> N
             raise ValueError("expected a CUDA tensor or pinned host memory")
         return ctypes.c_void_p(t.data_ptr())
 
+    # the library cannot see the buffers' sizes: every block id must lie
+    # inside its tensor, or the kernel would address past it
+    if block_bytes <= 0:
+        raise ValueError("block_bytes must be positive")
+    nbytes = [t.numel() * t.element_size() for t in (src, dst)]
+    if any(b % block_bytes for b in nbytes):
+        raise ValueError("block_bytes must divide the byte size of src and dst")
+    if pr.shape[0]:
+        if int(pr.min()) < 0:
+            raise ValueError("block ids must be non-negative")
+        if int(pr[:, 0].max()) >= nbytes[0] // block_bytes or int(pr[:, 1].max()) >= nbytes[1] // block_bytes:
+            raise ValueError("a block id lies past the end of src or dst")
     _check(lib().kvo_copy_blocks_noalloc(ptr(src), ptr(dst), block_bytes, ctypes.c_void_p(pr.ctypes.data),
                                          pr.shape[0], _stream_ptr(stream)), "kvo_copy_blocks_noalloc")
 

@@ -56,7 +56,11 @@ typedef enum kvo_status {
   KVO_ECUDA = -3,      /* a CUDA runtime call failed */
   KVO_ERANGE = -4,     /* a kernel saw a selected position outside [0, length) */
   KVO_EBUSY = -5,      /* resource still referenced by in-flight work */
-  KVO_ETIMEDOUT = -6,  /* a bounded device-side wait gave up */
+  KVO_ETIMEDOUT = -6,  /* a bounded device-side wait gave up (reported by kvo_sync).  The waiting
+                        * CTA waits once more, again bounded; if that wait gives up too, a bulk
+                        * copy into its shared memory may still land after it exits, and the
+                        * context refuses every later launch (KVO_ECUDA): destroy it and create
+                        * a new one. */
   KVO_ECAPACITY = -7   /* not enough blocks; allocation rolled back */
 } kvo_status;
 
@@ -256,12 +260,14 @@ kvo_status kvo_resolve_gather_multi(kvo_ctx* ctx, int32_t layer, const int32_t* 
                                     void* out_rows, uint16_t* out_bf16, void* stream);
 
 /*
- * kvo_decode_layers - one decode step of several layers in one launch (one
- * thread-block cluster per task); each task is what kvo_decode_step does for
- * its layer, except that a task without scores resolves the selection its
- * idx already holds ([KVO] "Separate historical capacity from the current
- * working set": later layers reuse a layer's selection and keep their own
- * KV).  Per task:
+ * kvo_decode_layers - one decode step of several layers; each task is what
+ * kvo_decode_step does for its layer, except that a task without scores
+ * resolves a selection it is given ([KVO] "Separate historical capacity from
+ * the current working set": later layers reuse a layer's selection and keep
+ * their own KV).  Three launches, each over every task of the call: the
+ * top-K of the tasks with scores; then the lookup and the row gather of
+ * every task on the whole GPU; then, one CTA per task, the victims, the map
+ * updates, the fills, the appends and the LRU queue.  Per task:
  *   layer     a layer of the context; at most one task per layer per call.
  *   new_rows  device rows to append first (16-byte aligned), r of them, or
  *             NULL with r = 0.
@@ -270,10 +276,12 @@ kvo_status kvo_resolve_gather_multi(kvo_ctx* ctx, int32_t layer, const int32_t* 
  *             kvo_resolve_gather), and n is ignored.
  *   idx       device int32[k].
  *   out_rows / out_bf16  as in kvo_resolve_gather (at least one).
- * The tasks of one call run concurrently: a task must not read an idx that
- * another task of the same call writes (select in one call, reuse in the
- * next).  KVO_EINVAL on a bad task (nothing enqueued), misaligned scores or
- * idx (4 bytes) included.
+ * The selections of a call are made before any task resolves: a task
+ * without scores may name the idx of a task of the same call that has
+ * scores, and then resolves that task's new selection (one call per decode
+ * step for a whole stack).  Two tasks with scores must not share an idx.
+ * KVO_EINVAL on a bad task (nothing enqueued), misaligned scores or idx
+ * (4 bytes) included.
  */
 typedef struct kvo_layer_task {
   int32_t layer;
@@ -287,6 +295,23 @@ typedef struct kvo_layer_task {
   uint16_t* out_bf16;
 } kvo_layer_task;
 kvo_status kvo_decode_layers(kvo_ctx* ctx, const kvo_layer_task* tasks, int32_t ntasks, int32_t k, void* stream);
+
+/*
+ * Measurement of kvo_decode_layers by its phases.  kvo_set_phase_timing(ctx,
+ * 1) makes every later kvo_decode_layers call record CUDA events on its
+ * stream around its three launches (selections, gathers, finishes), and run
+ * them in order on that one stream (no overlap of the call's parts, no
+ * early scheduling of a launch before the previous one ends);
+ * kvo_layers_phase_times waits for the recorded calls, adds up the elapsed
+ * milliseconds of each phase into ms[0..2], returns the number of calls in
+ * *calls and starts a new count.  Off by default; switching it resets the
+ * count.  KVO_EINVAL for NULL arguments, KVO_ECUDA if an event call fails.
+ */
+kvo_status kvo_set_phase_timing(kvo_ctx* ctx, int32_t on);
+kvo_status kvo_layers_phase_times(kvo_ctx* ctx, double* ms, int64_t* calls);
+/* kvo_layers_launch_count - the number of kernels that kvo_decode_layers has
+ * launched on this context since it was created (host counter). */
+kvo_status kvo_layers_launch_count(kvo_ctx* ctx, int64_t* out);
 
 /*
  * kvo_decode_step - one decode step of one layer in a single launch: the
@@ -360,6 +385,15 @@ kvo_status kvo_debug_dump_layer(kvo_ctx* ctx, int32_t layer, int32_t* pos2slot,
 kvo_status kvo_debug_layer_counters(kvo_ctx* ctx, int32_t layer, uint32_t* out);
 
 /*
+ * kvo_debug_raise_status - test hook: ORs `bits` into the device status word
+ * (1 = an index out of range, 2 = an internal check, 4 = a bounded wait gave
+ * up, 8 = its second wait gave up too), as a kernel would, so that the
+ * handling in kvo_sync can be tested without making a wait run out.
+ * Synchronous.
+ */
+kvo_status kvo_debug_raise_status(kvo_ctx* ctx, uint32_t bits);
+
+/*
  * kvo_debug_record_evictions - when enabled (on != 0), every resolve call
  * records its fills as (slot, evicted position or -1, new position) triples,
  * in the order the misses took them.  kvo_debug_evictions copies the last
@@ -376,6 +410,16 @@ kvo_status kvo_debug_evictions(kvo_ctx* ctx, int32_t layer, int32_t* triples, in
  * device uint4 `sink`; used to measure the host link.  Stream-ordered.
  */
 kvo_status kvo_probe_host_read(const void* src, int64_t bytes, void* sink, void* stream);
+
+/* kvo_probe_host_touch - the same with one 16-byte load every `stride`
+ * bytes (a multiple of 16): touches every page of a buffer while moving few
+ * bytes.  Stream-ordered. */
+kvo_status kvo_probe_host_touch(const void* src, int64_t bytes, int64_t stride, void* sink, void* stream);
+
+/* kvo_debug_history_host - the host address of the layer's pinned history
+ * (history_cap * 656 bytes), for measurements of how the host memory behaves
+ * (reading it, or probing it from the GPU).  The caller must not write it. */
+kvo_status kvo_debug_history_host(kvo_ctx* ctx, int32_t layer, void** out);
 
 /* ------------------------------------------------------------------------
  * Session block store/restore.
@@ -530,8 +574,10 @@ kvo_status kvo_pool_debug_free_queue(kvo_pool* pool, int32_t which, int32_t* out
  *                aligned, holding at least (largest id + 1) blocks each;
  *                owned by the caller.  Source and destination blocks must
  *                not overlap.
- *   block_bytes  > 0, a multiple of 16.
- *   pairs        host array of 2n non-negative block ids.  It is copied with
+ *   block_bytes  > 0, a multiple of 16, at most 16 * (2^32 - 1).
+ *   pairs        host array of 2n non-negative block ids.  The library
+ *                cannot see the buffers' sizes: ids past their ends are
+ *                the caller's error (the Python binding checks them).  It is copied with
  *                cudaMemcpyAsync on `stream`: pageable memory may be reused
  *                when the call returns, pinned memory only once the stream
  *                has passed the call.

@@ -30,8 +30,8 @@ What the method computes (the plain definitions, in the pages' order):
     not referenced this step, taken one miss at a time in selection order.
   * Dequant: bf16 = round-to-nearest-even(float32(q) * float32(scale)).
 
-Readings of points the pages leave open are listed in the design doc of the
-repository; each function below states the one it uses.
+Where the pages leave a point open, the function that meets it states the
+reading it uses.
 """
 from __future__ import annotations
 
@@ -145,13 +145,17 @@ class LayerState:
         self.last_use = np.zeros(self.hot_rows, np.int64)
         self.step = 0
 
-    def append(self, new_rows: np.ndarray, from_device: bool = False, copyback: bool = True) -> None:
+    def append(self, new_rows: np.ndarray, from_device: bool = False) -> None:
         """Rows for history positions [length, length + r); length grows.
 
         Reading: append never touches the hot cache; an appended row becomes
-        a miss the first time it is selected.  With the ring, device rows
-        wait in it until COPYBACK_BATCH of them have gathered (then whole
-        batches move to RAM); host rows first flush the ring, then go to RAM.
+        a miss the first time it is selected.  With the ring, the pipeline
+        "New KV -> GPU recent ring -> batched copyback -> RAM history" runs
+        as one step: device rows enter the ring, and every whole batch of
+        COPYBACK_BATCH pending rows then moves to RAM before the append
+        returns (a batch is copied back as soon as it is complete).  Host rows
+        first flush the ring, then go to RAM.  Without the ring, every
+        appended row is in RAM at once.
         """
         new_rows = np.asarray(new_rows, np.uint8).reshape(-1, ROW_BYTES)
         r = new_rows.shape[0]
@@ -160,16 +164,10 @@ class LayerState:
         self.history[self.length:self.length + r] = new_rows
         self.length += r
         if self.ring_rows and from_device:
-            if copyback:
-                self.ring_copyback()
-        else:
-            self.ram_len = self.length
-
-    def ring_copyback(self) -> None:
-        """Whole batches of COPYBACK_BATCH pending ring rows move to RAM."""
-        if self.ring_rows:
             pending = self.length - self.ram_len
             self.ram_len += pending // COPYBACK_BATCH * COPYBACK_BATCH
+        else:
+            self.ram_len = self.length
 
     def flush_ring(self) -> None:
         """Every pending ring row to RAM (the export consistency boundary)."""

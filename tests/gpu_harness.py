@@ -76,8 +76,11 @@ class GpuLayerRun:
 
 
 class OracleLayerRun:
-    def __init__(self, w: W.Workload, layer: int, want_bf16=None, policy: str = "lru", ring: int = 0,
-                 fused: bool = False):
+    """One layer of a workload through the oracle: append, select, resolve.
+    Every GPU entry point (separate calls, the one-launch decode step, the
+    batched layers) is checked against this one sequence."""
+
+    def __init__(self, w: W.Workload, layer: int, want_bf16=None, policy: str = "lru", ring: int = 0):
         self.w, self.layer = w, layer
         self.st = O.LayerState(w.history_cap, w.hot_rows, policy=policy, ring_rows=ring)
         self.st.append(W.rows(w, layer, 0, w.n0))
@@ -85,15 +88,12 @@ class OracleLayerRun:
         self.bf = w.bf16 if want_bf16 is None else want_bf16
         self.prev = None
         self.last = None
-        # the fused decode step copies full ring batches back after its own
-        # resolve (its appended rows are read from its input rows)
-        self.fused = fused
 
     def step(self, step: int, idx_override=None):
         w = self.w
         for a in range(w.appends_per_step):
             pos = w.n0 + step * w.appends_per_step + a
-            self.st.append(self.extra[pos - w.n0:pos - w.n0 + 1], from_device=True, copyback=not self.fused)
+            self.st.append(self.extra[pos - w.n0:pos - w.n0 + 1], from_device=True)
         if idx_override is None:
             s = W.apply_carry(W.base_scores(w, self.layer, step), self.prev,
                               W.carry_draw(w, self.layer, step), w.carry_boost)
@@ -101,8 +101,6 @@ class OracleLayerRun:
         else:
             idx = idx_override
         self.last = O.resolve_gather(self.st, idx, want_bf16=self.bf)
-        if self.fused:
-            self.st.ring_copyback()
         self.prev = idx
         return idx
 

@@ -293,6 +293,30 @@ def test_argument_errors_change_nothing(kvo):
     ctx.close()
 
 
+def test_timed_out_copy_makes_the_context_refuse_launches(kvo):
+    """A bounded wait that gave up is reported once by kvo_sync; when its
+    second wait gave up too (a bulk copy may still land), the context
+    refuses every later launch.  The status bits are raised by the test hook,
+    as the kernel would raise them: no wait is made to run out."""
+    import torch
+    ctx = kvo.Context(1, 100, 16)
+    ctx.append_rows(0, np.zeros((50, O.ROW_BYTES), np.uint8))
+    idx = torch.arange(8, dtype=torch.int32, device="cuda")
+    out = torch.empty((8, O.ROW_BYTES), dtype=torch.uint8, device="cuda")
+    ctx.raise_status(4)                                  # a wait gave up, its second wait did not
+    assert ctx.sync() == kvo.KVO_ETIMEDOUT
+    assert ctx.sync() == 0                               # reported once
+    ctx.resolve_gather(0, idx, out)                      # still usable
+    assert ctx.sync() == 0
+    ctx.raise_status(4 | 8)                              # the second wait gave up too
+    assert ctx.sync() == kvo.KVO_ETIMEDOUT
+    with pytest.raises(kvo.KvoError):
+        ctx.resolve_gather(0, idx, out)
+    with pytest.raises(kvo.KvoError):
+        ctx.append_rows(0, np.zeros((1, O.ROW_BYTES), np.uint8))
+    ctx.close()
+
+
 # ------------------------------------------------ fused decode step
 @pytest.mark.parametrize("appends", [0, 2])
 def test_decode_step_tiny_full_parity(kvo, appends):
@@ -646,7 +670,7 @@ def test_recent_ring_parity(kvo, fused, appends):
     oracle's first ram_len rows; host_bytes counts only RAM reads."""
     w = W.TINY.scaled(appends_per_step=appends, steps=40)
     g = GpuLayerRun(w, 0, want_bf16=True, fused=fused, ring=128)
-    o = OracleLayerRun(w, 0, want_bf16=True, ring=128, fused=fused)
+    o = OracleLayerRun(w, 0, want_bf16=True, ring=128)
     g.ctx.record_evictions(True)
     host_reads = 0
     for step in range(w.steps):
@@ -702,16 +726,22 @@ def test_recent_ring_host_rows_flush_first(kvo):
 
 
 def test_recent_ring_50k_fused(kvo):
-    """The benchmark's fused path with a 1,024-row ring, 300 steps."""
+    """The benchmark's fused path with a 1,024-row ring, 300 steps: the same
+    oracle as the separate calls, RAM length and RAM reads included."""
     w = W.K50.scaled(steps=300)
     g = GpuLayerRun(w, 0, fused=True, ring=1024)
-    o = OracleLayerRun(w, 0, ring=1024, fused=True)
+    o = OracleLayerRun(w, 0, ring=1024)
+    host_reads = 0
     for step in range(w.steps):
         np.testing.assert_array_equal(g.step(step), o.step(step))
         assert g.ctx.ram_length(0) == o.st.ram_len
+        host_reads += o.last.host_reads
         if step % 50 == 0 or step == w.steps - 1:
             np.testing.assert_array_equal(g.rows(), o.last.rows)
+            assert g.ctx.stats(0)["host_bytes"] == host_reads * O.ROW_BYTES, step
     compare_state(g.ctx, 0, o.st)
+    ram = o.st.ram_len
+    np.testing.assert_array_equal(g.ctx.read_history(0, ram - 3000, 3000), o.st.history[ram - 3000:ram])
     g.ctx.close()
 
 
@@ -771,24 +801,31 @@ def test_staged_gather_random_selections(kvo, gather, seed, H, n, k, dup, bad):
 def test_staged_gather_50k_fused_with_ring(kvo, gather):
     w = W.K50.scaled(steps=200)
     g = GpuLayerRun(w, 0, fused=True, ring=1024, gather=gather)
-    o = OracleLayerRun(w, 0, ring=1024, fused=True)
+    o = OracleLayerRun(w, 0, ring=1024)
+    host_reads = 0
     for step in range(w.steps):
         np.testing.assert_array_equal(g.step(step), o.step(step))
+        assert g.ctx.ram_length(0) == o.st.ram_len
+        host_reads += o.last.host_reads
         if step % 25 == 0 or step == w.steps - 1:
             np.testing.assert_array_equal(g.rows(), o.last.rows)
+    assert g.ctx.stats(0)["host_bytes"] == host_reads * O.ROW_BYTES
     compare_state(g.ctx, 0, o.st)
     assert g.ctx.sync() == 0
     g.ctx.close()
 
 
 # ------------------------------------------------ batched layers (one launch)
-@pytest.mark.parametrize("policy,ring,gather", [(0, 0, None), (1, 128, (1, 0))])
-def test_decode_layers_stack_parity(kvo, policy, ring, gather):
-    """Eight layers, selection on layers 0 and 4 (one launch), reused by the
-    others (a second launch); appends every step.  Every layer equals its
-    own oracle: selections, rows, evictions, maps."""
+def _run_layers(kvo, w, steps, *, policy=0, ring=0, gather=None, full_check=lambda step: True, one_call=True):
+    """Drives a workload through kvo_decode_layers: per step one call with
+    every layer, a reusing layer naming its source layer's idx (the way the
+    benchmark does), or with one_call=False a call with the selecting layers
+    and then one with the reusing layers, each on its own copy of the
+    selection.  Every layer's selection is
+    compared every step; rows, bf16 rows and eviction order of every layer
+    on the steps `full_check` accepts; the maps and hot rows of every layer,
+    the RAM length and the RAM reads at the end."""
     import torch
-    w = W.STACK.scaled(layers=8, n0=6000, hot_rows=1024, k=256, steps=24, carry=150)
     L = w.layers
     ctx = kvo.Context(L, w.history_cap, w.hot_rows)
     if policy:
@@ -799,42 +836,93 @@ def test_decode_layers_stack_parity(kvo, policy, ring, gather):
         ctx.set_gather_mode(*gather)
     ctx.record_evictions(True)
     pol = "circular" if policy else "lru"
-    orc = [OracleLayerRun(w, l, policy=pol, ring=ring, fused=True) for l in range(L)]
-    new = [torch.from_numpy(W.rows(w, l, w.n0, w.history_cap - w.n0)).cuda() for l in range(L)]
+    orc = [OracleLayerRun(w, l, policy=pol, ring=ring) for l in range(L)]
+    a = w.appends_per_step
+    new = [torch.from_numpy(W.rows(w, l, w.n0, w.history_cap - w.n0)).cuda() if a else None for l in range(L)]
     for l in range(L):
         ctx.append_rows(l, W.rows(w, l, 0, w.n0))
     idx = [torch.empty(w.k, dtype=torch.int32, device="cuda") for _ in range(L)]
     out = [torch.empty((w.k, O.ROW_BYTES), dtype=torch.uint8, device="cuda") for _ in range(L)]
+    outb = [torch.empty((w.k, O.DEQUANT_VALUES), dtype=torch.int16, device="cuda") for _ in range(L)] if w.bf16 else None
     prev = {}
-    for step in range(w.steps):
+    host_reads = [0] * L
+    for step in range(steps):
         sel_tasks, reuse_tasks = [], []
         for l in range(L):
-            t = {"layer": l, "idx": idx[l], "out_rows": out[l], "new_rows": new[l][step:step + 1]}
+            t = {"layer": l, "idx": idx[w.source_layer(l) if one_call else l], "out_rows": out[l]}
+            if outb is not None:
+                t["out_bf16"] = outb[l]
+            if a:
+                t["new_rows"] = new[l][step * a:(step + 1) * a]
             if l in w.selecting_layers():
                 s = W.apply_carry(W.base_scores(w, l, step), prev.get(l), W.carry_draw(w, l, step), w.carry_boost)
                 t["scores"] = torch.from_numpy(s).cuda()
                 sel_tasks.append(t)
             else:
                 reuse_tasks.append(t)
-        ctx.decode_layers(sel_tasks, w.k)
-        for t in reuse_tasks:                           # the source layer's selection, copied in stream order
-            t["idx"].copy_(idx[w.source_layer(t["layer"])])
-        ctx.decode_layers(reuse_tasks, w.k)
+        if one_call:
+            ctx.decode_layers(sel_tasks + reuse_tasks, w.k)
+        else:
+            ctx.decode_layers(sel_tasks, w.k)
+            for t in reuse_tasks:                       # the source layer's selection, copied in stream order
+                t["idx"].copy_(idx[w.source_layer(t["layer"])])
+            if reuse_tasks:
+                ctx.decode_layers(reuse_tasks, w.k)
+        full = full_check(step)
         for l in range(L):
             src = w.source_layer(l)
             if l == src:
                 want = orc[l].step(step)
                 np.testing.assert_array_equal(idx[l].cpu().numpy(), want)
                 prev[l] = want
+            elif not one_call:
+                orc[l].step(step, idx_override=prev[src])
+                np.testing.assert_array_equal(idx[l].cpu().numpy(), prev[src])
             else:
                 orc[l].step(step, idx_override=prev[src])
-            np.testing.assert_array_equal(out[l].cpu().numpy(), orc[l].last.rows)
-            assert ctx.evictions(l) == orc[l].last.evictions, (step, l)
+            host_reads[l] += orc[l].last.host_reads
+            if full:
+                np.testing.assert_array_equal(out[l].cpu().numpy(), orc[l].last.rows)
+                if outb is not None:
+                    assert_bf16_equal(outb[l].cpu().numpy(), orc[l].last.bf16)
+                assert ctx.evictions(l) == orc[l].last.evictions, (step, l)
     for l in range(L):
         compare_state(ctx, l, orc[l].st)
         assert ctx.history_length(l) == orc[l].st.length
+        assert ctx.ram_length(l) == orc[l].st.ram_len
+        assert ctx.stats(l)["host_bytes"] == host_reads[l] * O.ROW_BYTES, l
     assert ctx.sync() == 0
     ctx.close()
+    return orc
+
+
+@pytest.mark.parametrize("one_call", [True, False])
+@pytest.mark.parametrize("policy,ring,gather", [(0, 0, None), (1, 128, (1, 0)), (0, 128, None)])
+def test_decode_layers_stack_parity(kvo, policy, ring, gather, one_call):
+    """Eight layers, selection on layers 0 and 4, reused by the others;
+    appends every step; in one call per step or in two.  Every layer equals
+    its own oracle: selections, rows, evictions, maps, RAM reads."""
+    w = W.STACK.scaled(layers=8, n0=6000, hot_rows=1024, k=256, steps=40, carry=150)
+    _run_layers(kvo, w, w.steps, policy=policy, ring=ring, gather=gather, one_call=one_call)
+
+
+def test_decode_layers_full_stack_parity(kvo):
+    """The 78-layer stack at full size, in the launch shapes the benchmark
+    times (20 selecting tasks, then 58 reusing ones; K = 2,048, 32,768 hot
+    rows per layer, 50,023-row histories), for 126 steps: the hot caches
+    fill up at step 121, so the last steps evict mapped positions.
+    Selections of every layer every step; rows, evictions and maps of every
+    layer every 16th step and on each of the last six."""
+    w = W.STACK.scaled(steps=126)
+    orc = _run_layers(kvo, w, w.steps, full_check=lambda step: step % 16 == 15 or step >= 120)
+    assert all(any(e[1] >= 0 for e in o.last.evictions) for o in orc)   # real LRU victims on every layer
+
+
+def test_decode_layers_1m_one_wave_parity(kvo):
+    """Eight layers of 1M positions in one launch with bf16 output (the
+    1M benchmark's shape): every output, both formats, every step."""
+    w = W.M1.scaled(steps=3)
+    _run_layers(kvo, w, w.steps)
 
 
 def test_decode_layers_argument_errors(kvo):

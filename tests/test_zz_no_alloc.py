@@ -62,13 +62,16 @@ def test_matches_store_and_restore(kvo):
 
     # call 1: pool -> pinned tier, with the store's pairs
     my_tier = torch.zeros((nb, bb), dtype=torch.uint8).pin_memory()
+    back = torch.full((nb, bb), 0x3C, dtype=torch.uint8, device=dev)
     p1 = np.array([(a, b) for key in first_pool for a, b in zip(first_pool[key], tier[key])], np.int32)
+    p2 = np.array([(a, b) for key in tier for a, b in zip(tier[key], second_pool[key])], np.int32)
+    torch.cuda.synchronize()
+    free_before = torch.cuda.mem_get_info()[0]
     kvo.kvo_copy_blocks_noalloc(mine, my_tier, bb, p1)
     # call 2, right after: tier -> a fresh pool, with the restore's pairs
-    back = torch.full((nb, bb), 0x3C, dtype=torch.uint8, device=dev)
-    p2 = np.array([(a, b) for key in tier for a, b in zip(tier[key], second_pool[key])], np.int32)
     kvo.kvo_copy_blocks_noalloc(my_tier, back, bb, p2)
     torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free_before            # the two calls took no device memory
 
     out = torch.empty((sw.tokens, ROW), dtype=torch.uint8, device=dev)
     for (s, layer), r in rows.items():
@@ -108,6 +111,15 @@ def test_limits(kvo):
     pr[:] = (-1, 0)
     assert L.kvo_copy_blocks_noalloc(ctypes.c_void_p(a.data_ptr()), ctypes.c_void_p(b.data_ptr()), 32, p, 1,
                                      None) == kvo.KVO_EINVAL          # negative block id
+    with pytest.raises(ValueError):
+        kvo.kvo_copy_blocks_noalloc(a, b, 32, np.array([[4, 0]], np.int32))    # past the end of src
+    with pytest.raises(ValueError):
+        kvo.kvo_copy_blocks_noalloc(a, b, 32, np.array([[0, 4]], np.int32))    # past the end of dst
+    with pytest.raises(ValueError):
+        kvo.kvo_copy_blocks_noalloc(a, b, 48, np.array([[0, 0]], np.int32))    # does not divide the buffers
+    pr[:] = (0, 0)
+    assert L.kvo_copy_blocks_noalloc(ctypes.c_void_p(a.data_ptr()), ctypes.c_void_p(b.data_ptr()), 16 << 32, p, 1,
+                                     None) == kvo.KVO_EINVAL          # block_bytes / 16 beyond 32 bits
     a.fill_(7)
     kvo.kvo_copy_blocks_noalloc(a, b, 32, np.array([[3, 0], [0, 2]], np.int32))
     torch.cuda.synchronize()

@@ -1104,56 +1104,106 @@ def probe_main(args, rank, world):
 SWEEP_PCTS = [0, 1, 5, 10, 25, 50, 75, 100]
 
 
+def sweep_rounds(m, rounds, warm, k, spread, seed):
+    """A full 32,768-row hot cache, then rounds that keep k - m positions of
+    the previous round (hits) and add m never-seen ones (misses): one run of
+    consecutive positions (spread 1), or one position every `spread` (runs
+    of length 1)."""
+    g = np.random.default_rng([seed, m, spread])
+    idxs, prev = [], None
+    base = warm * k
+    for s in range(warm + rounds):
+        if s < warm:
+            cur = np.arange(s * k, (s + 1) * k)
+        else:
+            keep = g.choice(prev, size=k - m, replace=False) if m < k else np.zeros(0, np.int64)
+            new = base + spread * np.arange(m)
+            base += spread * max(m, 1)
+            cur = np.sort(np.concatenate([keep, new]))
+        idxs.append(cur.astype(np.int32))
+        prev = cur
+    return np.stack(idxs), base
+
+
 def sweep_main(args):
-    """Resolve time per 2,048-row call against the miss rate, for both
-    gather modes (register loads and TMA-staged), on a full 32,768-row hot
-    cache: every round keeps k - m positions of the previous round (hits)
-    and adds m never-seen ones (misses, read from host memory)."""
+    """Against the miss rate, on a full 32,768-row hot cache with 2,048-row
+    calls: (1) the single-layer resolve's two gather modes (register loads,
+    TMA-staged); (2) kvo_decode_layers' two ways of fetching the misses from
+    the host history, zero-copy loads and batched copies (one
+    cudaMemcpyAsync per run of consecutive positions), with the misses in one
+    run per call and with every miss its own run."""
     import torch
     from gather_radix_top_gb300 import build, kvo
     build.build()
     rounds = args.steps or 64
-    rows = []
+    warm = 16
+    k, H = 2048, 32_768
+    flush = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
+    nmax = max(sweep_rounds(k * p // 100, args.warmup + rounds, warm, k, sp, 11)[1]
+               for p in SWEEP_PCTS for sp in (1, 8))
+    all_rows = W.rows(W.PROBE.scaled(name="miss_rate_sweep", n0=nmax), 0, 0, nmax)   # a row depends on its position only
+
+    def history(n):
+        return all_rows[:n]
+
+    def timed(ctx, call, idxs):
+        ms = []
+        for s in range(idxs.shape[0]):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            call(idxs[s])
+            b.record()
+            if s >= warm + args.warmup:
+                ms.append((a, b))
+        torch.cuda.synchronize()
+        assert ctx.sync() == 0
+        # CUDA event stamps tick in ~2 us steps here: the mean of many calls is the estimate
+        return round(float(np.mean([x.elapsed_time(y) * 1e3 for x, y in ms])), 2)
+
+    gather_rows, fetch_rows = [], []
     for pct in SWEEP_PCTS:
-        m = 2048 * pct // 100
-        w = W.PROBE.scaled(name="miss_rate_sweep", n0=32_768 + max(m, 1) * (rounds + args.warmup + 1),
-                           extra={"warm_rounds": 16, "fresh": m})
-        steps = 16 + args.warmup + rounds
-        idxs = torch.from_numpy(probe_rounds(w, steps)).cuda()
-        hist = W.rows(w, 0, 0, w.n0)
-        res = {"miss_pct": pct, "misses_per_call": m}
-        for mode, code in (("loads", kvo.GATHER_LOADS), ("staged", kvo.GATHER_STAGED)):
-            ctx = kvo.Context(1, w.n0, w.hot_rows)
-            ctx.set_gather_mode(code, 0)
-            ctx.append_rows(0, hist)
-            out = torch.empty((w.k, ROW), dtype=torch.uint8, device="cuda")
-            flush = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
-            ms = []
-            for s in range(steps):
-                flush.zero_()
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record()
-                ctx.resolve_gather(0, idxs[s], out)
-                b.record()
-                if s >= 16 + args.warmup:
-                    ms.append((a, b))
-            torch.cuda.synchronize()
-            t = [x.elapsed_time(y) * 1e3 for x, y in ms]
-            assert ctx.sync() == 0
-            # CUDA event stamps tick in ~2 us steps here: the mean of many calls is the estimate
-            res[mode + "_us_mean"] = round(float(np.mean(t)), 2)
-            ctx.close()
-            del flush
-        res["faster"] = "staged" if res["staged_us_mean"] < res["loads_us_mean"] else "loads"
-        rows.append(res)
-    staged_up_to = max([r["miss_pct"] for r in rows if r["faster"] == "staged"], default=None)
-    best = min(min(r["loads_us_mean"], r["staged_us_mean"]) for r in rows)
-    line = {"metric": METRIC, "value": round(2048 / (best * 1e-6), 1), "unit": "rows/s", "n_gpus": 1,
+        m = k * pct // 100
+        for spread in (1, 8):
+            idx_np, n = sweep_rounds(m, args.warmup + rounds, warm, k, spread, 11)
+            idxs = torch.from_numpy(idx_np).cuda()
+            hist = history(n)
+            out = torch.empty((k, ROW), dtype=torch.uint8, device="cuda")
+            res = {"miss_pct": pct, "misses_per_call": m, "runs_per_call": (1 if spread == 1 else m) if m else 0}
+            if spread == 1:                            # (1) gather modes of the single-layer resolve
+                gres = {"miss_pct": pct}
+                for mode, code in (("loads", kvo.GATHER_LOADS), ("staged", kvo.GATHER_STAGED)):
+                    ctx = kvo.Context(1, n, H)
+                    ctx.set_gather_mode(code, 0)
+                    ctx.append_rows(0, hist)
+                    gres[mode + "_us_mean"] = timed(ctx, lambda i: ctx.resolve_gather(0, i, out), idxs)
+                    ctx.close()
+                gres["faster"] = "staged" if gres["staged_us_mean"] < gres["loads_us_mean"] else "loads"
+                gather_rows.append(gres)
+            for mode, code in (("zerocopy", kvo.MISS_ZEROCOPY), ("batched", kvo.MISS_BATCHED)):   # (2)
+                ctx = kvo.Context(1, n, H)
+                ctx.set_miss_fetch(code)
+                ctx.append_rows(0, hist)
+                holder = {}
+
+                def call(i, ctx=ctx, holder=holder):
+                    holder["arr"] = kvo.make_layer_tasks([{"layer": 0, "idx": i, "out_rows": out}])
+                    ctx.decode_layers_prepared(holder["arr"], k)
+                res[mode + "_us_mean"] = timed(ctx, call, idxs)
+                ctx.close()
+            res["faster"] = "batched" if res["batched_us_mean"] < res["zerocopy_us_mean"] else "zerocopy"
+            fetch_rows.append(res)
+    staged_up_to = max([r["miss_pct"] for r in gather_rows if r["faster"] == "staged"], default=None)
+    batched_wins = [(r["miss_pct"], r["runs_per_call"]) for r in fetch_rows if r["faster"] == "batched"]
+    best = min(min(r["loads_us_mean"], r["staged_us_mean"]) for r in gather_rows)
+    line = {"metric": METRIC, "value": round(k / (best * 1e-6), 1), "unit": "rows/s", "n_gpus": 1,
             "steps": rounds, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "u8", "data": "synthetic",
-            "config": {"workload": "miss_rate_sweep", "hot_rows": 32_768, "k": 2048,
-                       "calls": "kvo_resolve_gather", "l2": "flushed between calls"},
-            "sweep": rows, "staged_faster_up_to_miss_pct": staged_up_to}
+            "config": {"workload": "miss_rate_sweep", "hot_rows": H, "k": k,
+                       "calls": "kvo_resolve_gather (gather modes); kvo_decode_layers (miss fetch modes)",
+                       "l2": "flushed between calls"},
+            "gather_modes": gather_rows, "staged_faster_up_to_miss_pct": staged_up_to,
+            "miss_fetch": fetch_rows, "batched_faster_at": batched_wins}
     print(json.dumps(line))
 
 

@@ -43,8 +43,22 @@ struct kvo_ctx {
     int64_t rows_cap = 0;
   } stage;
   kvo::LayerStatic* statics = nullptr;   // device [layers]: what the batched decode step reads per layer
+  uint32_t* first_hist = nullptr;        // device [layers][2048]: the batched step's filtering histograms (zero
+                                         // between calls: each selection zeroes its own after use)
   bool statics_dirty = true;             // the views changed since the last upload
   int64_t launches = 0;                  // kernels kvo_decode_layers has launched
+  // kvo_set_miss_fetch: how kvo_decode_layers fetches the misses of the host
+  // history (zero-copy loads, batched copies, or chosen by the miss rate)
+  int32_t miss_mode = KVO_MISS_ZEROCOPY;
+  int32_t miss_auto_pct = 100;
+  kvo::LayersDefer defer = {};           // the batched-copy buffers (made on first use)
+  int32_t defer_k = 0;                   // staging rows per layer
+  std::vector<const uint8_t*> hist_ptrs; // host address of each layer's history
+  unsigned long long* stats_snap = nullptr;   // pinned [layers][8]: the last stats snapshot (AUTO)
+  cudaEvent_t snap_ev = nullptr;         // the snapshot has landed
+  bool snap_pending = false;
+  double snap_hits = -1.0, snap_misses = 0.0;  // totals of the last snapshot read
+  double miss_rate = 0.0;                // the last measured miss share of kvo_decode_layers
   bool phase_timing = false;             // kvo_decode_layers records events around its launches
   std::vector<cudaEvent_t> phase_ev;     // 4 per recorded call, reused
   size_t phase_calls = 0;                // calls recorded since the last kvo_layers_phase_times
@@ -77,6 +91,16 @@ void free_ctx(kvo_ctx* c) {
   cudaFree(c->evlog);
   cudaFree(c->status);
   cudaFree(c->statics);
+  cudaFree(c->first_hist);
+  cudaFreeHost(const_cast<int2*>(c->defer.dlist_host));
+  cudaFree(c->defer.dcount_dev);
+  cudaFreeHost(c->defer.dcount_host);
+  cudaFreeHost(c->defer.plist_host);
+  cudaFreeHost(c->defer.pcount_host);
+  cudaFree(c->defer.staging);
+  if (c->defer.listed) cudaEventDestroy(c->defer.listed);
+  cudaFreeHost(c->stats_snap);
+  if (c->snap_ev) cudaEventDestroy(c->snap_ev);
   for (cudaEvent_t e : c->phase_ev) cudaEventDestroy(e);
   delete c;
 }
@@ -132,6 +156,80 @@ struct DeviceRanges {
     return true;
   }
 };
+
+// The batched-copy buffers, made on first use (staging grows with k).
+cudaError_t ensure_defer(kvo_ctx* c, int32_t k) {
+  kvo::LayersDefer& d = c->defer;
+  cudaError_t e = cudaSuccess;
+  const size_t L = (size_t)c->layers;
+  if (!d.dlist_host) {
+    void* p = nullptr;
+    if ((e = cudaHostAlloc(&p, L * KVO_MAX_K * sizeof(int2), cudaHostAllocMapped)) != cudaSuccess) return e;
+    d.dlist_host = static_cast<const int2*>(p);
+    if ((e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&d.dlist_dev), p, 0)) != cudaSuccess) return e;
+    if ((e = cudaMalloc(&d.dcount_dev, L * sizeof(uint32_t))) != cudaSuccess) return e;
+    if ((e = cudaMemset(d.dcount_dev, 0, L * sizeof(uint32_t))) != cudaSuccess) return e;
+    if ((e = cudaHostAlloc(reinterpret_cast<void**>(&d.dcount_host), L * sizeof(uint32_t), 0)) != cudaSuccess)
+      return e;
+    if ((e = cudaHostAlloc(reinterpret_cast<void**>(&d.plist_host), L * KVO_MAX_K * sizeof(int2),
+                           cudaHostAllocMapped)) != cudaSuccess)
+      return e;
+    if ((e = cudaHostGetDevicePointer(const_cast<void**>(reinterpret_cast<const void**>(&d.plist_dev)), d.plist_host,
+                                      0)) != cudaSuccess)
+      return e;
+    if ((e = cudaHostAlloc(reinterpret_cast<void**>(&d.pcount_host), L * sizeof(uint32_t), cudaHostAllocMapped)) !=
+        cudaSuccess)
+      return e;
+    if ((e = cudaHostGetDevicePointer(const_cast<void**>(reinterpret_cast<const void**>(&d.pcount_dev)),
+                                      d.pcount_host, 0)) != cudaSuccess)
+      return e;
+    if ((e = cudaEventCreateWithFlags(&d.listed, cudaEventDisableTiming)) != cudaSuccess) return e;
+    c->hist_ptrs.assign(c->hist_host.begin(), c->hist_host.end());
+    d.hist_host = c->hist_ptrs.data();
+  }
+  if (c->defer_k < k) {
+    cudaFree(d.staging);
+    d.staging = nullptr;
+    c->defer_k = 0;
+    if ((e = cudaMalloc(&d.staging, L * (size_t)k * KVO_ROW_BYTES)) != cudaSuccess) return e;
+    c->defer_k = k;
+  }
+  return cudaSuccess;
+}
+
+// AUTO: the miss share of the recent kvo_decode_layers calls, from stats
+// snapshots copied asynchronously after a call and read at a later call once
+// they have landed (no wait).
+cudaError_t measure_miss_rate(kvo_ctx* c, cudaStream_t s) {
+  cudaError_t e;
+  if (!c->stats_snap) {
+    if ((e = cudaHostAlloc(reinterpret_cast<void**>(&c->stats_snap), sizeof(unsigned long long) * 8 * c->layers, 0)) !=
+        cudaSuccess)
+      return e;
+    if ((e = cudaEventCreateWithFlags(&c->snap_ev, cudaEventDisableTiming)) != cudaSuccess) return e;
+  }
+  if (c->snap_pending && cudaEventQuery(c->snap_ev) == cudaSuccess) {
+    double hits = 0, misses = 0;
+    for (int32_t l = 0; l < c->layers; ++l) {
+      hits += (double)c->stats_snap[8 * l + 1];
+      misses += (double)c->stats_snap[8 * l + 2];
+    }
+    if (c->snap_hits >= 0.0 && hits + misses > c->snap_hits + c->snap_misses)
+      c->miss_rate = (misses - c->snap_misses) / (hits + misses - c->snap_hits - c->snap_misses);
+    c->snap_hits = hits;
+    c->snap_misses = misses;
+    c->snap_pending = false;
+  }
+  cudaGetLastError();                                    // a query that is not ready is not an error
+  if (!c->snap_pending) {
+    if ((e = cudaMemcpyAsync(c->stats_snap, c->stats, sizeof(unsigned long long) * 8 * c->layers,
+                             cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+      return e;
+    if ((e = cudaEventRecord(c->snap_ev, s)) != cudaSuccess) return e;
+    c->snap_pending = true;
+  }
+  return cudaSuccess;
+}
 
 // Uploads the per-layer table the batched decode step reads, when the views
 // changed (the work in flight that reads the old table is waited for first).
@@ -328,6 +426,8 @@ kvo_status kvo_create(int32_t layers, int64_t history_cap, int32_t hot_rows, int
               ok(cudaMalloc(&c->stats, sizeof(unsigned long long) * 8 * layers)) &&
               ok(cudaMalloc(&c->status, sizeof(uint32_t))) &&
               ok(cudaMalloc(&c->statics, sizeof(kvo::LayerStatic) * layers)) &&
+              ok(cudaMalloc(&c->first_hist, sizeof(uint32_t) * 2048 * layers)) &&
+              ok(cudaMemset(c->first_hist, 0, sizeof(uint32_t) * 2048 * layers)) &&
               ok(cudaMemset(c->counters, 0, sizeof(uint32_t) * 8 * layers)) &&
               ok(cudaMemset(c->stats, 0, sizeof(unsigned long long) * 8 * layers)) &&
               ok(cudaMemset(c->status, 0, sizeof(uint32_t)));
@@ -524,6 +624,14 @@ kvo_status kvo_set_gather_mode(kvo_ctx* ctx, int32_t mode, int32_t auto_miss_pct
   return KVO_OK;
 }
 
+kvo_status kvo_set_miss_fetch(kvo_ctx* ctx, int32_t mode, int32_t auto_miss_pct) {
+  if (!ctx || mode < KVO_MISS_ZEROCOPY || mode > KVO_MISS_AUTO || auto_miss_pct < 0 || auto_miss_pct > 100)
+    return KVO_EINVAL;
+  ctx->miss_mode = mode;
+  ctx->miss_auto_pct = auto_miss_pct;
+  return KVO_OK;
+}
+
 kvo_status kvo_set_policy(kvo_ctx* ctx, int32_t policy) {
   if (!ctx || (policy != KVO_POLICY_LRU && policy != KVO_POLICY_CIRCULAR)) return KVO_EINVAL;
   if (ctx->resolved) return KVO_EBUSY;
@@ -636,6 +744,9 @@ kvo_status kvo_decode_layers(kvo_ctx* ctx, const kvo_layer_task* tasks, int32_t 
     ev = ctx->phase_ev.data() + 4 * ctx->phase_calls;
   }
   if (!ok(upload_statics(ctx))) return KVO_ECUDA;
+  const bool batched = ctx->miss_mode == KVO_MISS_BATCHED ||
+                       (ctx->miss_mode == KVO_MISS_AUTO && 100.0 * ctx->miss_rate >= ctx->miss_auto_pct);
+  if (batched && !ok(ensure_defer(ctx, k))) return KVO_ENOMEM;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   static thread_local std::vector<int64_t> ram;
   ram.resize(ntasks);
@@ -645,9 +756,11 @@ kvo_status kvo_decode_layers(kvo_ctx* ctx, const kvo_layer_task* tasks, int32_t 
   }
   uint32_t launched = 0;
   const cudaError_t e = kvo::launch_layers(st.data(), lay.data(), (uint32_t)ntasks, (uint32_t)k, ctx->statics,
-                                           ctx->status, ctx->max_cluster, s, ev, &launched);
+                                           ctx->status, ctx->max_cluster, s, ev, ctx->first_hist,
+                                           batched ? &ctx->defer : nullptr, &launched);
   if (!ok(e)) return KVO_ECUDA;
   ctx->launches += launched;
+  if (ctx->miss_mode == KVO_MISS_AUTO && !ok(measure_miss_rate(ctx, s))) return KVO_ECUDA;
   if (ev) ++ctx->phase_calls;
   ctx->resolved = true;
   for (int32_t i = 0; i < ntasks; ++i) {

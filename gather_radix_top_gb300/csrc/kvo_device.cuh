@@ -375,7 +375,7 @@ __device__ RadixCut cluster_radix_select(Key4 key4, uint32_t count, uint32_t wan
       hist_add_warp4(sm->hist, bins, vm);
     }
     __syncthreads();
-    const uint32_t per_owner = kBins / nrank;
+    const uint32_t per_owner = (kBins + nrank - 1) / nrank;   // bins per owning CTA (the last may own fewer)
     for (uint32_t b = tid; b <= dmask; b += kThreads) {
       const uint32_t v = sm->hist[b];
       if (v) dsmem_red_add_u32(dsmem_addr(&tot[b], b / per_owner), v);

@@ -34,9 +34,11 @@
 // (last_use, slot) victim order).  Nothing but the layers' own tables and the
 // caller's outputs carries state from one launch to the next: B leaves its
 // claims in pos2slot and its stamps in last_use, and C reads them there.
+#include <algorithm>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <vector>
 
 #include "kvo_internal.h"
 #include "kvo_resolve_body.cuh"
@@ -63,6 +65,7 @@ struct LayerCall {
   uint32_t fresh_from;          // position of the first new row (the old length)
   uint32_t r;                   // new rows
   uint32_t to_ram;              // the first to_ram new rows go to the host history, the rest to the ring
+  uint32_t* first_hist;         // filtered selections: the histogram of the scores' top key bits, or NULL
 };
 
 constexpr uint32_t kBatchTasks = 128;                    // layers per launch (9 KB of parameters)
@@ -74,6 +77,17 @@ struct LayerBatch {
   uint32_t chunks;              // B: CTAs per layer
   uint32_t cand_bytes;          // A (filtered route): shared memory for candidates
   uint32_t ntasks;
+  // Misses fetched by batched copies (deferred is non-zero): the gathers
+  // leave out the rows of the host history and list them instead, (entry,
+  // position) at dlist[layer * KVO_MAX_K + i], counted in dcount[layer]; the
+  // host copies the rows into staging (layer * k rows per layer) and lists
+  // (entry, staging row) at plist, counted in pcount, for the placement.
+  uint32_t deferred;
+  int2* dlist;                  // device address of mapped host memory
+  uint32_t* dcount;             // device memory, zero between calls
+  const int2* plist;            // device address of mapped host memory
+  const uint32_t* pcount;       // device address of mapped host memory
+  const uint8_t* staging;       // device memory
   LayerCall t[kBatchTasks];
 };
 
@@ -84,6 +98,46 @@ struct LayerBatch {
 __device__ __forceinline__ void wait_previous_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void allow_next_grid() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// ------------------------------------------------------- A0: histogram
+// For selections on the filtered route (histories whose keys do not fit the
+// cluster's shared memory): the histogram of the top kFirstBits key bits of
+// every score, built by the whole GPU (each CTA a slice of one layer's
+// scores) rather than by the selecting cluster alone.  The selection finds
+// its bucket from it, and its CTA 0 zeroes it for the next call.
+constexpr uint32_t kHistThreads = 256;
+constexpr uint32_t kHistSlice = 16384;                   // scores per CTA
+constexpr uint32_t kHistCopies = 4;                      // shared histograms, one per warp mod 4
+
+__global__ void __launch_bounds__(kHistThreads) layers_hist_kernel(const __grid_constant__ LayerBatch b) {
+  __shared__ uint32_t h[kHistCopies][topk_detail::kFirstBins];
+  const LayerCall& T = b.t[blockIdx.x / b.chunks];
+  const uint32_t lo = (blockIdx.x % b.chunks) * kHistSlice;
+  const uint32_t hi = min(T.n, lo + kHistSlice);
+  for (uint32_t i = threadIdx.x; i < kHistCopies * topk_detail::kFirstBins; i += kHistThreads) (&h[0][0])[i] = 0;
+  __syncthreads();
+  uint32_t* mine = h[(threadIdx.x >> 5) % kHistCopies];
+  const bool vec = (reinterpret_cast<uintptr_t>(T.scores + lo) & 15u) == 0;
+  for (uint32_t i0 = lo + 4 * threadIdx.x; i0 < hi; i0 += 4 * kHistThreads) {
+    float f[4];
+    if (vec && i0 + 3 < hi) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(T.scores + i0));
+      f[0] = v.x, f[1] = v.y, f[2] = v.z, f[3] = v.w;
+    } else {
+      for (uint32_t e = 0; e < 4; ++e) f[e] = i0 + e < hi ? __ldg(T.scores + i0 + e) : 0.f;
+    }
+#pragma unroll
+    for (uint32_t e = 0; e < 4; ++e)
+      if (i0 + e < hi) atomicAdd(&mine[score_key(f[e]) >> topk_detail::kLowBits], 1u);
+  }
+  __syncthreads();
+  for (uint32_t bin = threadIdx.x; bin < topk_detail::kFirstBins; bin += kHistThreads) {
+    uint32_t v = 0;
+#pragma unroll
+    for (uint32_t c = 0; c < kHistCopies; ++c) v += h[c][bin];
+    if (v) atomicAdd(&T.first_hist[bin], v);
+  }
+}
+
 // ------------------------------------------------------------ A: select
 template <bool kResident>
 __global__ void __launch_bounds__(kThreads, 1) layers_select_kernel(const __grid_constant__ LayerBatch b) {
@@ -93,11 +147,17 @@ __global__ void __launch_bounds__(kThreads, 1) layers_select_kernel(const __grid
   allow_next_grid();                                     // the gathers may be scheduled; they wait for this grid
   int32_t* idx = T.idx;
   const int32_t* pos2slot = b.statics[T.layer].pos2slot;
-  topk_detail::topk_body<kResident>(T.scores, T.n, b.k, dyn_smem, b.cand_bytes, &rsm,
-                                    [&](uint32_t pos, uint32_t out) {
-                                      idx[out] = (int32_t)pos;
-                                      prefetch_l2(&pos2slot[pos]);   // B looks it up next
-                                    });
+  topk_detail::topk_body<kResident>(
+      T.scores, T.n, b.k, dyn_smem, b.cand_bytes, &rsm,
+      [&](uint32_t pos, uint32_t out) {
+        idx[out] = (int32_t)pos;
+        prefetch_l2(&pos2slot[pos]);                     // B looks it up next
+      },
+      T.first_hist);
+  // every CTA of the cluster has read the histogram (cluster barriers came
+  // after its reads): zero it for the next call
+  if (T.first_hist && cluster_rank() == 0)
+    for (uint32_t bin = threadIdx.x; bin < topk_detail::kFirstBins; bin += kThreads) T.first_hist[bin] = 0;
 }
 
 // ------------------------------------------------------------ B: gather
@@ -123,6 +183,7 @@ __device__ __forceinline__ const uint4* miss_source(const LayerStatic& S, const 
 __global__ void __launch_bounds__(kGatherThreads) layers_gather_kernel(const __grid_constant__ LayerBatch b,
                                                                        uint32_t* status) {
   __shared__ const uint4* src[kGatherEntries];           // NULL: an invalid entry (zero row)
+  __shared__ uint8_t later[kGatherEntries];              // the row comes by a batched copy (placed later)
   __shared__ uint32_t cnt[4];                            // hits, misses, RAM reads, invalid
   const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const LayerCall& T = b.t[blockIdx.x / b.chunks];
@@ -140,6 +201,7 @@ __global__ void __launch_bounds__(kGatherThreads) layers_gather_kernel(const __g
     const uint32_t j = j0 + tid;
     const int32_t p = T.idx[j];
     const uint4* s = nullptr;
+    uint8_t defer = 0;
     if (p < 0 || (uint32_t)p >= T.len) {
       inv = 1;
     } else {
@@ -157,6 +219,11 @@ __global__ void __launch_bounds__(kGatherThreads) layers_gather_kernel(const __g
         bool host;
         s = miss_source(S, T, (uint32_t)p, &host);
         miss = 1;
+        if (host && b.deferred) {                        // listed for the host's batched copies
+          const uint32_t i = atomicAdd(&b.dcount[T.layer], 1u);
+          b.dlist[(size_t)T.layer * KVO_MAX_K + i] = make_int2((int32_t)j, p);
+          defer = 1;
+        }
         // a RAM read as append-then-resolve defines it: below the RAM length
         // (this call's own rows there are served from their device copy,
         // which holds the same bytes)
@@ -164,6 +231,7 @@ __global__ void __launch_bounds__(kGatherThreads) layers_gather_kernel(const __g
       }
     }
     src[tid] = s;
+    later[tid] = defer;
   }
   if (warp * 32 < nj) {                                  // warps holding entries: their counts
     const uint32_t h = __reduce_add_sync(0xffffffffu, hit), m = __reduce_add_sync(0xffffffffu, miss);
@@ -185,7 +253,7 @@ __global__ void __launch_bounds__(kGatherThreads) layers_gather_kernel(const __g
       const uint32_t e = e0 + u * kGatherWarps;
       va[u] = make_uint4(0, 0, 0, 0);
       vb[u] = make_uint4(0, 0, 0, 0);
-      const uint4* s = e < nj ? src[e] : nullptr;
+      const uint4* s = e < nj && !later[e] ? src[e] : nullptr;
       if (s) {
         va[u] = s[lane];
         if (lane < kRowVec - 32) vb[u] = s[32 + lane];
@@ -195,6 +263,7 @@ __global__ void __launch_bounds__(kGatherThreads) layers_gather_kernel(const __g
     for (uint32_t u = 0; u < kGatherInFlight; ++u) {
       const uint32_t e = e0 + u * kGatherWarps;
       if (e >= nj) break;
+      if (later[e]) continue;
       const uint32_t j = j0 + e;
       if (T.out_rows) {
         uint4* d = reinterpret_cast<uint4*>(T.out_rows) + (size_t)j * kRowVec;
@@ -215,6 +284,47 @@ __global__ void __launch_bounds__(kGatherThreads) layers_gather_kernel(const __g
     }
   }
   allow_next_grid();                                     // the finishes may be scheduled; they wait for this grid
+}
+
+// --------------------------------------------------- B2: batched placement
+// The rows the host copied into staging, to their entries of the output
+// (and their bf16 rows): one warp per row, kGatherInFlight rows in flight.
+__global__ void __launch_bounds__(kGatherThreads) layers_place_kernel(const __grid_constant__ LayerBatch b) {
+  const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const LayerCall& T = b.t[blockIdx.x / b.chunks];
+  wait_previous_grid();
+  const uint32_t m = b.pcount[T.layer];
+  const uint32_t e0 = (blockIdx.x % b.chunks) * kGatherEntries;
+  const int2* pl = b.plist + (size_t)T.layer * KVO_MAX_K;
+  const uint4* stage = reinterpret_cast<const uint4*>(b.staging) + (size_t)T.layer * b.k * kRowVec;
+  for (uint32_t i0 = e0 + warp; i0 < min(m, e0 + kGatherEntries); i0 += kGatherWarps * kGatherInFlight) {
+    uint4 va[kGatherInFlight], vb[kGatherInFlight];
+    int2 pe[kGatherInFlight];
+#pragma unroll
+    for (uint32_t u = 0; u < kGatherInFlight; ++u) {
+      const uint32_t i = i0 + u * kGatherWarps;
+      pe[u] = i < min(m, e0 + kGatherEntries) ? pl[i] : make_int2(-1, -1);
+      va[u] = make_uint4(0, 0, 0, 0);
+      vb[u] = make_uint4(0, 0, 0, 0);
+      if (pe[u].x >= 0 && (uint32_t)pe[u].x < b.k && (uint32_t)pe[u].y < b.k) {
+        const uint4* s = stage + (size_t)pe[u].y * kRowVec;
+        va[u] = s[lane];
+        if (lane < kRowVec - 32) vb[u] = s[32 + lane];
+      }
+    }
+#pragma unroll
+    for (uint32_t u = 0; u < kGatherInFlight; ++u) {
+      if (pe[u].x < 0 || (uint32_t)pe[u].x >= b.k || (uint32_t)pe[u].y >= b.k) continue;
+      const uint32_t j = (uint32_t)pe[u].x;
+      if (T.out_rows) {
+        uint4* d = reinterpret_cast<uint4*>(T.out_rows) + (size_t)j * kRowVec;
+        d[lane] = va[u];
+        if (lane < kRowVec - 32) d[32 + lane] = vb[u];
+      }
+      if (T.out_bf16) dequant_row(va[u], vb[u], lane, reinterpret_cast<uint4*>(T.out_bf16 + (size_t)j * KVO_DEQUANT_VALUES));
+    }
+  }
+  allow_next_grid();
 }
 
 // ------------------------------------------------------------ C: finish
@@ -491,6 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1) layers_finish_kernel(const __grid
       atomicAdd(st + 7, (unsigned long long)k);
       if (S.evlog) S.evlog[0] = (int32_t)nvic;
       nvic_s = nvic;
+      if (b.deferred) b.dcount[T.layer] = 0;             // the host has read this call's list
     }
   }
 
@@ -500,21 +611,23 @@ __global__ void __launch_bounds__(kThreads, 1) layers_finish_kernel(const __grid
   // CTA 0 over distributed shared memory first
   if (F > 1) {
     cluster_sync();                                      // CTA 0's lists are complete
-    if (f != 0) {
-      const uint32_t n = dsmem_ld_u32(dsmem_addr(&nvic_s, 0));
-      for (uint32_t i = tid; i < n; i += kThreads) {
-        mlist[i] = dsmem_ld_u32(dsmem_addr(&mlist[i], 0));
-        vslot[i] = dsmem_ld_u32(dsmem_addr(&vslot[i], 0));
-        mpos[i] = (int32_t)dsmem_ld_u32(dsmem_addr(&mpos[i], 0));
-      }
-      if (tid == 0) nvic_s = n;
-    }
+    if (f != 0 && tid == 0) nvic_s = dsmem_ld_u32(dsmem_addr(&nvic_s, 0));
   }
   __syncthreads();
   const uint32_t nvic = nvic_s;
   const uint32_t pieces = nvic * kRowVec;
   const uint32_t share = (pieces + F - 1) / F;
   const uint32_t plo = min(pieces, f * share), phi = min(pieces, plo + share);
+  if (F > 1 && f != 0 && plo < phi) {
+    // only the list entries of this CTA's rows, from CTA 0
+    const uint32_t u0 = plo / kRowVec, u1 = (phi - 1) / kRowVec + 1;
+    for (uint32_t u = u0 + tid; u < u1; u += kThreads) {
+      mlist[u] = dsmem_ld_u32(dsmem_addr(&mlist[u], 0));
+      vslot[u] = dsmem_ld_u32(dsmem_addr(&vslot[u], 0));
+      mpos[u] = (int32_t)dsmem_ld_u32(dsmem_addr(&mpos[u], 0));
+    }
+    __syncthreads();
+  }
   for (uint32_t base = plo; base < phi; base += kFillInFlight * kThreads) {
     uint4 x[kFillInFlight];
     uint32_t dst[kFillInFlight];                          // piece index in the hot cache, or kNoEntry
@@ -694,7 +807,7 @@ struct PartBuffers {
 cudaError_t enqueue_part(LayersConfig* cfg, const StepTask* tasks, const uint32_t* layers, const uint32_t* which,
                          uint32_t n, uint32_t k, const LayerStatic* statics, uint32_t* status, int max_cluster,
                          cudaStream_t stream, cudaEvent_t* ev, cudaEvent_t after_select, PartBuffers& pb,
-                         uint32_t* launched) {
+                         uint32_t* hist, const LayersDefer* defer, uint32_t* launched) {
   cudaError_t e;
   pb.sel.clear();
   pb.res.clear();
@@ -727,6 +840,10 @@ cudaError_t enqueue_part(LayersConfig* cfg, const StepTask* tasks, const uint32_
     sb.statics = statics;
     sb.k = k;
     sb.cand_bytes = resident ? (uint32_t)topk_detail::topk_chunk(nmax, C) * 4u : topk_detail::kTopkMaxDynSmem;
+    // the filtered route takes its first histogram from the whole-GPU pass
+    for (uint32_t i = 0; i < sb.ntasks; ++i)
+      sb.t[i].first_hist = !resident && hist ? hist + (size_t)sb.t[i].layer * topk_detail::kFirstBins : nullptr;
+    sb.chunks = (nmax + kHistSlice - 1) / kHistSlice;
     pb.sel_c.push_back(C);
     pb.sel_resident.push_back(resident ? 1 : 0);
   }
@@ -738,6 +855,14 @@ cudaError_t enqueue_part(LayersConfig* cfg, const StepTask* tasks, const uint32_
     rb.statics = statics;
     rb.k = k;
     rb.chunks = (k + kGatherEntries - 1) / kGatherEntries;
+    rb.deferred = defer ? 1u : 0u;
+    if (defer) {
+      rb.dlist = defer->dlist_dev;
+      rb.dcount = defer->dcount_dev;
+      rb.plist = defer->plist_dev;
+      rb.pcount = defer->pcount_dev;
+      rb.staging = defer->staging;
+    }
   }
 
   cudaLaunchConfig_t lc;
@@ -746,6 +871,11 @@ cudaError_t enqueue_part(LayersConfig* cfg, const StepTask* tasks, const uint32_
   if (ev && (e = cudaEventRecord(ev[0], stream)) != cudaSuccess) return e;
   for (size_t i = 0; i < pb.sel.size(); ++i) {
     const bool resident = pb.sel_resident[i] != 0;
+    if (!resident && hist) {
+      layers_hist_kernel<<<pb.sel[i].ntasks * pb.sel[i].chunks, kHistThreads, 0, stream>>>(pb.sel[i]);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+      ++*launched;
+    }
     launch_config(nullptr, dim3(pb.sel_c[i] * pb.sel[i].ntasks, 1, 1), kThreads,
                   resident ? pb.sel[i].cand_bytes : topk_detail::kTopkMaxDynSmem, stream, pb.sel_c[i], false, &lc,
                   attr);
@@ -764,6 +894,51 @@ cudaError_t enqueue_part(LayersConfig* cfg, const StepTask* tasks, const uint32_
     if ((e = cudaLaunchKernelEx(&lc, layers_gather_kernel, rb, status)) != cudaSuccess) return e;
     after = true;
     ++*launched;
+  }
+  if (defer) {
+    // The batched-copy fetch: wait for the lists, copy every run of
+    // consecutive missing positions with one cudaMemcpyAsync into staging
+    // (rows in position order), then place the rows.
+    uint32_t nl = 0;                                     // the counters up to the part's highest layer
+    for (uint32_t w = 0; w < n; ++w) nl = layers[which[w]] + 1 > nl ? layers[which[w]] + 1 : nl;
+    if ((e = cudaMemcpyAsync(defer->dcount_host, defer->dcount_dev, sizeof(uint32_t) * nl, cudaMemcpyDeviceToHost,
+                             stream)) != cudaSuccess)
+      return e;
+    if ((e = cudaEventRecord(defer->listed, stream)) != cudaSuccess) return e;
+    if ((e = cudaEventSynchronize(defer->listed)) != cudaSuccess) return e;
+    static thread_local std::vector<int2> ent;
+    static thread_local std::vector<int32_t> uniq;
+    for (uint32_t w = 0; w < n; ++w) {
+      const uint32_t l = layers[which[w]];
+      const uint32_t m = defer->dcount_host[l] < k ? defer->dcount_host[l] : k;
+      const int2* dl = defer->dlist_host + (size_t)l * KVO_MAX_K;
+      ent.assign(dl, dl + m);
+      uniq.resize(m);
+      for (uint32_t i = 0; i < m; ++i) uniq[i] = ent[i].y;
+      std::sort(uniq.begin(), uniq.end());
+      uniq.erase(std::unique(uniq.begin(), uniq.end()), uniq.end());
+      uint8_t* stage = defer->staging + (size_t)l * k * KVO_ROW_BYTES;
+      const uint8_t* hist_h = defer->hist_host[l];
+      for (size_t a = 0; a < uniq.size();) {              // one copy per run of consecutive positions
+        size_t z = a + 1;
+        while (z < uniq.size() && uniq[z] == uniq[z - 1] + 1) ++z;
+        if ((e = cudaMemcpyAsync(stage + a * KVO_ROW_BYTES, hist_h + (size_t)uniq[a] * KVO_ROW_BYTES,
+                                 (z - a) * KVO_ROW_BYTES, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+          return e;
+        a = z;
+      }
+      int2* pl = defer->plist_host + (size_t)l * KVO_MAX_K;
+      for (uint32_t i = 0; i < m; ++i) {
+        const int32_t srow = (int32_t)(std::lower_bound(uniq.begin(), uniq.end(), ent[i].y) - uniq.begin());
+        pl[i] = make_int2(ent[i].x, srow);
+      }
+      defer->pcount_host[l] = m;
+    }
+    for (const LayerBatch& rb : pb.res) {
+      launch_config(nullptr, dim3(rb.ntasks * rb.chunks, 1, 1), kGatherThreads, 0, stream, 1, false, &lc, attr);
+      if ((e = cudaLaunchKernelEx(&lc, layers_place_kernel, rb)) != cudaSuccess) return e;
+      ++*launched;
+    }
   }
   if (ev && (e = cudaEventRecord(ev[2], stream)) != cudaSuccess) return e;
   const size_t fsmem = finish_smem_bytes(k, tasks[which[0]].L.hot_rows);
@@ -791,7 +966,7 @@ cudaError_t enqueue_part(LayersConfig* cfg, const StepTask* tasks, const uint32_
 
 cudaError_t launch_layers(const StepTask* tasks, const uint32_t* layers, uint32_t ntasks, uint32_t k,
                           const LayerStatic* statics, uint32_t* status, int max_cluster, cudaStream_t stream,
-                          cudaEvent_t* ev, uint32_t* launched) {
+                          cudaEvent_t* ev, uint32_t* hist, const LayersDefer* defer, uint32_t* launched) {
   LayersConfig* cfg = nullptr;
   cudaError_t e = layers_init(&cfg);
   if (e != cudaSuccess) return e;
@@ -800,7 +975,7 @@ cudaError_t launch_layers(const StepTask* tasks, const uint32_t* layers, uint32_
   all.resize(ntasks);
   for (uint32_t i = 0; i < ntasks; ++i) all[i] = i;
   return enqueue_part(cfg, tasks, layers, all.data(), ntasks, k, statics, status, max_cluster, stream, ev, nullptr,
-                      pb, launched);
+                      pb, hist, defer, launched);
 }
 
 }  // namespace kvo

@@ -284,7 +284,9 @@ __device__ __forceinline__ uint32_t filter_keys(LoadF4 loadf4, uint32_t count, u
   return base;
 }
 
-// Selects the k largest of n scores with the whole cluster.  dyn_smem holds
+// Selects the k largest of n scores with the whole cluster.  first_hist:
+// NULL, or (filtered route) the counts of the top kFirstBits key bits of all
+// n scores, made beforehand.  dyn_smem holds
 // topk_chunk(n, C) keys when kResident, else `cand_bytes` of room for the
 // filtered route's candidates (0: stream every pass).  emit(pos, out) is
 // called once for every chosen position with its rank `out` in ascending
@@ -293,7 +295,8 @@ __device__ __forceinline__ uint32_t filter_keys(LoadF4 loadf4, uint32_t count, u
 // then fence with a cluster barrier.
 template <bool kResident, typename Emit>
 __device__ __forceinline__ void topk_body(const float* __restrict__ scores, uint32_t n, uint32_t k,
-                                          uint8_t* dyn_smem, uint32_t cand_bytes, RadixSmem* rsm, Emit emit) {
+                                          uint8_t* dyn_smem, uint32_t cand_bytes, RadixSmem* rsm, Emit emit,
+                                          const uint32_t* first_hist = nullptr) {
   __shared__ uint32_t scratch[2][2 * kWarps + 2];
   __shared__ uint32_t table[kMaxCluster][4];
   __shared__ uint32_t cutw[4];
@@ -350,7 +353,16 @@ __device__ __forceinline__ void topk_body(const float* __restrict__ scores, uint
     select_and_emit(load4, cnt, k, 32, rsm, scratch, table, emit_at);
     return;
   }
-  first_digit_cut(load4, cnt, k, keys, keys + kHistCopies * kFirstBins, &scratch[0][0], cutw);
+  if (first_hist) {
+    // the filtering pass's histogram was built beforehand over the whole
+    // history (device memory, kFirstBins counts): only the cut is found here
+    uint32_t* tot = keys + kHistCopies * kFirstBins;
+    for (uint32_t b = tid; b < kFirstBins; b += kThreads) tot[b] = __ldcg(&first_hist[b]);
+    __syncthreads();
+    find_cut<kFirstBins / kThreads>(tot, k, &scratch[0][0], cutw);
+  } else {
+    first_digit_cut(load4, cnt, k, keys, keys + kHistCopies * kFirstBins, &scratch[0][0], cutw);
+  }
   const uint32_t bucket = cutw[0];
   const uint32_t total = cutw[1] + cutw[2];        // keys in or above the bucket, cluster-wide
   if (total <= cap) {

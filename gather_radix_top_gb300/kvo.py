@@ -19,6 +19,7 @@ MAX_ROUND = 8192
 POLICY_LRU, POLICY_CIRCULAR = 0, 1
 COPYBACK_BATCH = 64
 GATHER_LOADS, GATHER_STAGED, GATHER_AUTO = 0, 1, 2
+MISS_ZEROCOPY, MISS_BATCHED, MISS_AUTO = 0, 1, 2
 MAX_HOT_ROWS = 131072
 NOALLOC_MAX_PAIRS = 65536
 
@@ -37,7 +38,7 @@ EXPORTED = [
     "kvo_pool_read", "kvo_pool_fill", "kvo_store_blocks", "kvo_pool_release", "kvo_restore_blocks",
     "kvo_pool_sync", "kvo_pool_block_table", "kvo_pool_get_stats", "kvo_pool_debug_fail_after",
     "kvo_pool_debug_free_queue", "kvo_copy_blocks_noalloc", "kvo_set_phase_timing", "kvo_layers_phase_times",
-    "kvo_layers_launch_count", "kvo_probe_host_touch", "kvo_debug_history_host",
+    "kvo_layers_launch_count", "kvo_probe_host_touch", "kvo_debug_history_host", "kvo_set_miss_fetch",
 ]
 
 
@@ -134,6 +135,7 @@ def lib() -> ctypes.CDLL:
         "kvo_layers_launch_count": (ctypes.c_int, [_vp, _vp]),
         "kvo_probe_host_touch": (ctypes.c_int, [_vp, _i64, _i64, _vp, _vp]),
         "kvo_debug_history_host": (ctypes.c_int, [_vp, _i32, _vp]),
+        "kvo_set_miss_fetch": (ctypes.c_int, [_vp, _i32, _i32]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -518,6 +520,9 @@ class Context:
 
     def set_gather_mode(self, mode, auto_miss_pct=0):
         kvo_set_gather_mode(self.handle, mode, auto_miss_pct)
+
+    def set_miss_fetch(self, mode, auto_miss_pct=100):
+        _check(lib().kvo_set_miss_fetch(self.handle, mode, auto_miss_pct), "kvo_set_miss_fetch")
 
     def set_recent_ring(self, rows):
         kvo_set_recent_ring(self.handle, rows)

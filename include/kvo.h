@@ -169,6 +169,31 @@ kvo_status kvo_debug_read_history(kvo_ctx* ctx, int32_t layer, int64_t start, in
 kvo_status kvo_set_gather_mode(kvo_ctx* ctx, int32_t mode, int32_t auto_miss_pct);
 
 /*
+ * kvo_set_miss_fetch - how kvo_decode_layers fetches the misses whose rows
+ * are in the host history ([KVO] "Decision two": per-row transfers cost more
+ * than their bytes, batching them paid; "Decision three": misses read the
+ * registered host memory directly).
+ *   KVO_MISS_ZEROCOPY  the gathers read the rows over the host link with
+ *                      16-byte loads, in the same launch (default);
+ *   KVO_MISS_BATCHED   the gathers list the missing positions; the call waits
+ *                      for the list on the host, copies every run of
+ *                      consecutive positions with one cudaMemcpyAsync into
+ *                      device staging, and a placement launch writes the rows
+ *                      out (the call returns only after the gathers ran);
+ *   KVO_MISS_AUTO      batched while the last measured miss share of the
+ *                      calls is at least auto_miss_pct percent, else
+ *                      zero-copy (the share comes from statistics copied back
+ *                      asynchronously after each call; it lags by a call or
+ *                      two).
+ * Results are identical in every mode.  KVO_EINVAL for another mode or a
+ * percentage outside 0..100.  Other entry points always use zero-copy loads.
+ */
+#define KVO_MISS_ZEROCOPY 0
+#define KVO_MISS_BATCHED 1
+#define KVO_MISS_AUTO 2
+kvo_status kvo_set_miss_fetch(kvo_ctx* ctx, int32_t mode, int32_t auto_miss_pct);
+
+/*
  * Replacement policies ([KVO] "GPU cache management has hazards too").  In
  * both, the slots used by a round (its hits, and the slots it fills) are
  * pinned, and the round's distinct missing positions, in first-occurrence

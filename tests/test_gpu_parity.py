@@ -816,7 +816,8 @@ def test_staged_gather_50k_fused_with_ring(kvo, gather):
 
 
 # ------------------------------------------------ batched layers (one launch)
-def _run_layers(kvo, w, steps, *, policy=0, ring=0, gather=None, full_check=lambda step: True, one_call=True):
+def _run_layers(kvo, w, steps, *, policy=0, ring=0, gather=None, full_check=lambda step: True, one_call=True,
+                miss=None):
     """Drives a workload through kvo_decode_layers: per step one call with
     every layer, a reusing layer naming its source layer's idx (the way the
     benchmark does), or with one_call=False a call with the selecting layers
@@ -834,6 +835,8 @@ def _run_layers(kvo, w, steps, *, policy=0, ring=0, gather=None, full_check=lamb
         ctx.set_recent_ring(ring)
     if gather:
         ctx.set_gather_mode(*gather)
+    if miss:
+        ctx.set_miss_fetch(*miss)
     ctx.record_evictions(True)
     pol = "circular" if policy else "lru"
     orc = [OracleLayerRun(w, l, policy=pol, ring=ring) for l in range(L)]
@@ -904,6 +907,24 @@ def test_decode_layers_stack_parity(kvo, policy, ring, gather, one_call):
     its own oracle: selections, rows, evictions, maps, RAM reads."""
     w = W.STACK.scaled(layers=8, n0=6000, hot_rows=1024, k=256, steps=40, carry=150)
     _run_layers(kvo, w, w.steps, policy=policy, ring=ring, gather=gather, one_call=one_call)
+
+
+@pytest.mark.parametrize("miss", [(1, 100), (2, 0), (2, 30)])
+@pytest.mark.parametrize("policy,ring", [(0, 0), (1, 128), (0, 128)])
+def test_decode_layers_batched_miss_fetch(kvo, miss, policy, ring):
+    """The misses of the host history fetched by batched copies (always, or
+    chosen by the measured miss share): the same oracle as zero-copy loads,
+    rows, bf16 rows, evictions, maps and RAM reads included (the recent ring
+    and this step's rows still come from device memory)."""
+    w = W.STACK.scaled(layers=8, n0=6000, hot_rows=1024, k=256, steps=40, carry=150, bf16=True)
+    _run_layers(kvo, w, w.steps, policy=policy, ring=ring, miss=miss)
+
+
+def test_decode_layers_batched_miss_fetch_1m(kvo):
+    """Batched copies on 8 layers of 1M positions with bf16 output: about
+    2,000 scattered missing rows per layer and step, one copy each."""
+    w = W.M1.scaled(steps=2)
+    _run_layers(kvo, w, w.steps, miss=(1, 100))
 
 
 def test_decode_layers_full_stack_parity(kvo):

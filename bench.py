@@ -218,19 +218,28 @@ class GpuWorkload:
             self.new_rows_host = torch.from_numpy(new).pin_memory() if host_inputs else None
             self.new_rows = None if host_inputs else torch.from_numpy(new).to(dev)
         nmax = w.n_at(steps - 1)
-        self.scores = {}
-        self.draws = {}
-        for l in self.sel:
-            base = np.zeros((steps, nmax), np.float32)
+        self.nmax = nmax
+        # every selecting layer's scores in one array [steps, selecting layers,
+        # nmax] (layer j's are a view), so that the carry boost of a step is a
+        # few whole-array ops rather than a few per layer
+        nsel = len(self.sel)
+        base = np.zeros((steps, nsel, nmax), np.float32)
+        for j, l in enumerate(self.sel):
             for s in range(steps):
                 n = w.n_at(s)
-                base[s, :n] = W.base_scores(w, layer_base + l, s, n)
-            t = torch.from_numpy(base)
-            self.scores[l] = t.pin_memory() if host_inputs else t.to(dev)
-            if w.carry:
-                d = np.stack([W.carry_draw(w, layer_base + l, s) if s else np.zeros(w.carry, np.int64)
-                              for s in range(steps)])
-                self.draws[l] = torch.from_numpy(d).to(dev)
+                base[s, j, :n] = W.base_scores(w, layer_base + l, s, n)
+        t = torch.from_numpy(base)
+        self.scores_all = t.pin_memory() if host_inputs else t.to(dev)
+        self.scores = {l: self.scores_all[:, j] for j, l in enumerate(self.sel)}
+        self.draws = {}
+        if w.carry:
+            d = np.stack([np.stack([W.carry_draw(w, layer_base + l, s) if s else np.zeros(w.carry, np.int64)
+                                    for s in range(steps)]) for l in self.sel], axis=1)
+            self.draws_all = torch.from_numpy(d).to(dev)           # [steps, nsel, carry]
+            self.draws = {l: self.draws_all[:, j] for j, l in enumerate(self.sel)}
+            self.row_off = (torch.arange(nsel, dtype=torch.int64, device=dev) * nmax).unsqueeze(1)
+            self.boost = torch.full((w.carry,), w.carry_boost, dtype=torch.float32, device=dev)
+            self.boost_all = torch.full((nsel * w.carry,), w.carry_boost, dtype=torch.float32, device=dev)
         # query rows 1.. of an MTP round: row 0 plus float32 noise, added in float64
         self.nq = w.queries
         self.noise = {}
@@ -246,8 +255,9 @@ class GpuWorkload:
                             for l in self.sel} if self.nq > 1 and host_inputs else None
         self.qrows = {l: torch.empty((self.nq, nmax), dtype=torch.float32, device=dev) for l in self.sel}
         self.stage = {l: torch.empty(nmax, dtype=torch.float32, device=dev) for l in self.sel}
-        self.idx = {l: [torch.zeros((self.nq, w.k), dtype=torch.int32, device=dev) for _ in range(2)]
-                    for l in self.sel}
+        self.idx_all = torch.zeros((2, nsel, self.nq, w.k), dtype=torch.int32, device=dev)
+        self.idx = {l: [self.idx_all[0, j], self.idx_all[1, j]] for j, l in enumerate(self.sel)}
+        self.prepared = {}                    # step -> task arrays (device addresses only)
         kq = self.nq * w.k
         self.out_rows = torch.empty((kq, ROW), dtype=torch.uint8, device=dev)
         # batched layers run concurrently: one output buffer per layer
@@ -261,6 +271,9 @@ class GpuWorkload:
         self.idx_hist = torch.zeros((steps, w.k), dtype=torch.int32, device=dev)
         self.launches = 0
         self.api_host_s = 0.0                 # host time spent inside the kvo_decode_layers calls
+        self.stream = torch.cuda.current_stream()
+        self.stream_ptr = ctypes.c_void_p(self.stream.cuda_stream)
+        self.check = kvo._check
         self.fused = fused
         # host-input runs stage each step's new rows on the device (H2D inside the step)
         self.new_stage = (torch.empty((w.layers, max(a, 1), ROW), dtype=torch.uint8, device=dev)
@@ -278,8 +291,20 @@ class GpuWorkload:
         if w.carry and s > 0:
             prev = self.idx[l][(s - 1) & 1][0]
             pos = prev.index_select(0, self.draws[l][s]).long()
-            sc.index_add_(0, pos, torch.full((w.carry,), w.carry_boost, dtype=torch.float32, device="cuda"))
+            sc.index_add_(0, pos, self.boost)
         return sc
+
+    def all_scores(self, s):
+        """Every selecting layer's scores of step s on the device, the carry
+        boost applied to all of them at once (device inputs; not timed): the
+        same one float32 add per boosted position as scores_for."""
+        w = self.w
+        n = w.n_at(s)
+        if w.carry and s > 0:
+            prev = self.idx_all[(s - 1) & 1, :, 0]                   # [nsel, k]
+            pos = prev.gather(1, self.draws_all[s]).long() + self.row_off
+            self.scores_all[s].view(-1).index_add_(0, pos.view(-1), self.boost_all)
+        return {l: self.scores[l][s, :n] for l in self.sel}
 
     def query_rows(self, l, s, row0):
         """Rows 1.. of an MTP round (row 0 + noise in float64, cast once)."""
@@ -316,25 +341,49 @@ class GpuWorkload:
         return (self.kvo.make_layer_tasks(groups[True]),
                 self.kvo.make_layer_tasks(groups[False]) if groups[False] else None)
 
+    def prepare_all(self):
+        """The task arrays of every step, built before the first (device
+        inputs: the addresses they hold do not change), so that the host's
+        work per step is the boost, the call and the events, and the GPU's
+        queue stays ahead of it."""
+        if self.batched and not self.host_inputs and self.nq == 1:
+            for s in range(self.steps):
+                n = self.w.n_at(s)
+                self.prepared[s] = self.prepare_layers(s, {l: self.scores[l][s, :n] for l in self.sel})
+
     def step(self, s, ev=None, kev=None):
         """One decode step over all layers.  ev: (start, end) events; kev: dict
         kind -> list of (start, end) event pairs appended per launch."""
         torch, w, ctx = self.torch, self.w, self.ctx
-        sc = {l: self.scores_for(l, s) for l in self.sel}
+        if self.batched and not self.host_inputs and self.nq == 1:
+            sc = self.all_scores(s)
+        else:
+            sc = {l: self.scores_for(l, s) for l in self.sel}
         qr = {l: self.query_rows(l, s, sc[l]) for l in self.sel} if self.nq > 1 and not self.host_inputs else None
+
+        # per-launch event pairs, made before the step's first event so that
+        # the host work between the step's events is the calls themselves
+        nrec = 2 if self.batched else 2 + 3 * w.layers
+        spare = [torch.cuda.Event(enable_timing=True) for _ in range(2 * nrec)] if kev is not None else []
 
         def rec(kind, fn):
             if kev is None:
                 fn()
             else:
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a, b = spare.pop(), spare.pop()
                 a.record()
                 fn()
                 b.record()
                 kev.setdefault(kind, []).append((a, b))
             self.launches += 1
 
-        prepared = self.prepare_layers(s, sc) if self.batched else None   # host work, before the events
+        prepared = None
+        if self.batched:                    # host work, before the events; device inputs: once per step
+            prepared = self.prepared.get(s) if not self.host_inputs else None
+            if prepared is None:
+                prepared = self.prepare_layers(s, sc)
+                if not self.host_inputs:
+                    self.prepared[s] = prepared
         if ev:
             ev[0].record()
         if self.nq > 1 and self.host_inputs:                # the rows' noise is a step input too
@@ -348,10 +397,15 @@ class GpuWorkload:
             if a and self.host_inputs:
                 for l in range(w.layers):
                     self.new_stage[l, :a].copy_(self.new_rows_host[l, s * a:(s + 1) * a], non_blocking=True)
+            # the C function itself, its arguments made beforehand: the host
+            # work between the step's events is the call
+            fn = self.kvo.lib().kvo_decode_layers
+            calls = [(ctx.handle, arr, len(arr), w.k, self.stream_ptr) for arr in (sel_arr, reuse_arr)
+                     if arr is not None]
             h0 = time.perf_counter()
-            rec("layers", lambda: ctx.decode_layers_prepared(sel_arr, w.k))
-            if reuse_arr is not None:
-                rec("layers", lambda: ctx.decode_layers_prepared(reuse_arr, w.k))
+            for args in calls:
+                self.check(fn(*args), "kvo_decode_layers")
+                self.launches += 1
             self.api_host_s += time.perf_counter() - h0
             if self.host_inputs:
                 self.out_host.copy_(self.out_layers[w.layers - 1], non_blocking=True)
@@ -432,6 +486,7 @@ def run_gpu_arm(args, w, rank, world):
     wl = GpuWorkload(w, layer_base=rank * w.layers, steps=steps + phase_steps, fused=not args.separate,
                      policy=args.policy, ring=args.ring, gather=args.gather, auto_miss_pct=args.auto_miss_pct,
                      layer_calls=args.layer_calls)
+    wl.prepare_all()
     flush = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
     dist = world > 1
     if dist:
@@ -459,7 +514,7 @@ def run_gpu_arm(args, w, rank, world):
     clocks.start()
     t0 = time.perf_counter()
     launches0 = wl.launches
-    klaunch0 = wl.ctx.layers_launch_count() if wl.batched else 0
+    klaunch0, khost0 = wl.ctx.layers_counters() if wl.batched else (0, 0.0)
     wl.api_host_s = 0.0
     for s in range(args.warmup, steps):
         flush.zero_()                      # L2 flush between timed steps (not timed)
@@ -471,9 +526,12 @@ def run_gpu_arm(args, w, rank, world):
     wall = time.perf_counter() - t0
     clk = clocks.stop()
     launches = wl.launches - launches0
-    if wl.batched:                         # the kernels kvo_decode_layers launched in the timed steps
-        launches = wl.ctx.layers_launch_count() - klaunch0
     api_host_us = 1e6 * wl.api_host_s / max(1, steps - args.warmup)
+    lib_host_us = None
+    if wl.batched:                         # the kernels kvo_decode_layers launched in the timed steps
+        klaunch1, khost1 = wl.ctx.layers_counters()
+        launches = klaunch1 - klaunch0
+        lib_host_us = 1e6 * (khost1 - khost0) / max(1, steps - args.warmup)
     st1 = {l: wl.ctx.stats(l) for l in range(w.layers)}
     status = wl.ctx.sync()
     phases = None
@@ -508,7 +566,7 @@ def run_gpu_arm(args, w, rank, world):
     torch.cuda.empty_cache()
     return {"total_s": total_s, "step_ms": step_ms, "kern_ms": kern, "delta": delta, "wall": wall,
             "clocks": clk, "launches": launches, "status": status, "idx_hist": idx_hist, "settle_ms": settle_ms,
-            "phases": phases, "api_host_us": api_host_us}
+            "phases": phases, "api_host_us": api_host_us, "lib_host_us": lib_host_us}
 
 
 def run_e2e_host_step(args, w, steps):
@@ -1421,8 +1479,11 @@ def main():
     nres = args.steps * w.layers                          # layer resolves in the timed steps
     nsel = args.steps * len(w.selecting_layers())
     ab = algorithmic_bytes(w, nmean, g["delta"], nres, nsel)
-    kern_avg = {kind: float(np.mean(v)) for kind, v in g["kern_ms"].items()}
-    kern_tot = {kind: float(np.sum(v)) for kind, v in g["kern_ms"].items()}
+    kern_ms = dict(g["kern_ms"])
+    if not kern_ms:                        # batched layers without a phase pass: the whole call
+        kern_ms["layers"] = g["step_ms"]
+    kern_avg = {kind: float(np.mean(v)) for kind, v in kern_ms.items()}
+    kern_tot = {kind: float(np.sum(v)) for kind, v in kern_ms.items()}
     step_bytes = (w.layers * (ab["resolve_hbm"] + ROW * w.appends_per_step)
                   + len(w.selecting_layers()) * ab["select_hbm"])
     gpu_launches = g["launches"]
@@ -1453,7 +1514,7 @@ def main():
         per_launch = {"resolve": ab["resolve_hbm"], "select": ab["select_hbm"],
                       "append": 2 * ROW * w.appends_per_step,
                       "step": ab["resolve_hbm"] + ab["select_hbm"] + ROW * w.appends_per_step,
-                      "layers": step_bytes / max(1, len(g["kern_ms"].get("layers", [])) / args.steps)}
+                      "layers": step_bytes / max(1, len(kern_ms.get("layers", [])) / args.steps)}
     dominant = max((kd for kd in kern_tot), key=kern_tot.get)
     per_launch_bytes = per_launch[dominant]
     achieved = per_launch_bytes / (kern_avg[dominant] * 1e-3) / 1e9
@@ -1501,6 +1562,7 @@ def main():
         "gpu_launches": gpu_launches, "clocks": g["clocks"],
         "wall_s": round(g["wall"], 3), "device_status": g["status"],
         "api_host_us_per_step": round(g["api_host_us"], 1),
+        "lib_host_us_per_step": round(g["lib_host_us"], 1) if g.get("lib_host_us") is not None else None,
     }
     if cpu is not None:
         line["cpu_baseline"] = {"value": round(cpu["rows_per_s"], 1), "unit": "rows/s", "cores": cpu["cores"],

@@ -9,6 +9,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <algorithm>
+#include <chrono>
 #include <cstring>
 #include <new>
 #include <vector>
@@ -47,6 +48,8 @@ struct kvo_ctx {
                                          // between calls: each selection zeroes its own after use)
   bool statics_dirty = true;             // the views changed since the last upload
   int64_t launches = 0;                  // kernels kvo_decode_layers has launched
+  double host_seconds = 0.0;             // host time spent inside kvo_decode_layers
+  void* touch_sink = nullptr;            // kvo_touch_history's 16-byte sink
   // kvo_set_miss_fetch: how kvo_decode_layers fetches the misses of the host
   // history (zero-copy loads, batched copies, or chosen by the miss rate)
   int32_t miss_mode = KVO_MISS_ZEROCOPY;
@@ -92,6 +95,7 @@ void free_ctx(kvo_ctx* c) {
   cudaFree(c->status);
   cudaFree(c->statics);
   cudaFree(c->first_hist);
+  cudaFree(c->touch_sink);
   cudaFreeHost(const_cast<int2*>(c->defer.dlist_host));
   cudaFree(c->defer.dcount_dev);
   cudaFreeHost(c->defer.dcount_host);
@@ -576,9 +580,10 @@ kvo_status kvo_set_phase_timing(kvo_ctx* ctx, int32_t on) {
   return KVO_OK;
 }
 
-kvo_status kvo_layers_launch_count(kvo_ctx* ctx, int64_t* out) {
-  if (!ctx || !out) return KVO_EINVAL;
-  *out = ctx->launches;
+kvo_status kvo_layers_counters(kvo_ctx* ctx, int64_t* launches, double* host_seconds) {
+  if (!ctx || !launches || !host_seconds) return KVO_EINVAL;
+  *launches = ctx->launches;
+  *host_seconds = ctx->host_seconds;
   return KVO_OK;
 }
 
@@ -701,7 +706,18 @@ kvo_status kvo_resolve_gather_multi(kvo_ctx* ctx, int32_t layer, const int32_t* 
   return ok(e) ? KVO_OK : KVO_ECUDA;
 }
 
+static kvo_status decode_layers_impl(kvo_ctx* ctx, const kvo_layer_task* tasks, int32_t ntasks, int32_t k,
+                                     void* stream);
+
 kvo_status kvo_decode_layers(kvo_ctx* ctx, const kvo_layer_task* tasks, int32_t ntasks, int32_t k, void* stream) {
+  const auto t0 = std::chrono::steady_clock::now();
+  const kvo_status rc = decode_layers_impl(ctx, tasks, ntasks, k, stream);
+  if (ctx) ctx->host_seconds += std::chrono::duration<double>(std::chrono::steady_clock::now() - t0).count();
+  return rc;
+}
+
+static kvo_status decode_layers_impl(kvo_ctx* ctx, const kvo_layer_task* tasks, int32_t ntasks, int32_t k,
+                                     void* stream) {
   if (ctx && ctx->unusable) return KVO_ECUDA;
   if (!ctx || !tasks || ntasks < 0 || ntasks > ctx->layers || k < 1 || k > KVO_MAX_K || k > ctx->hot_rows)
     return KVO_EINVAL;
@@ -1003,6 +1019,19 @@ kvo_status kvo_probe_host_touch(const void* src, int64_t bytes, int64_t stride, 
   return ok(kvo::launch_probe(dev, (uint64_t)bytes, sink, static_cast<cudaStream_t>(stream), (uint64_t)stride))
              ? KVO_OK
              : KVO_ECUDA;
+}
+
+kvo_status kvo_touch_history(kvo_ctx* ctx, int32_t layer, void* stream) {
+  if (!ctx || layer < -1 || layer >= ctx->layers) return KVO_EINVAL;
+  if (ctx->unusable) return KVO_ECUDA;
+  if (!ctx->touch_sink && !ok(cudaMalloc(&ctx->touch_sink, 16))) return KVO_ENOMEM;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (int32_t l = layer < 0 ? 0 : layer; l < (layer < 0 ? ctx->layers : layer + 1); ++l) {
+    const int64_t bytes = ctx->length[l] * KVO_ROW_BYTES;
+    if (bytes <= 0) continue;
+    if (!ok(kvo::launch_probe(ctx->views[l].hist, (uint64_t)bytes, ctx->touch_sink, s, 4096))) return KVO_ECUDA;
+  }
+  return KVO_OK;
 }
 
 kvo_status kvo_debug_history_host(kvo_ctx* ctx, int32_t layer, void** out) {

@@ -105,7 +105,8 @@ __device__ __forceinline__ void allow_next_grid() { asm volatile("griddepcontrol
 // scores) rather than by the selecting cluster alone.  The selection finds
 // its bucket from it, and its CTA 0 zeroes it for the next call.
 constexpr uint32_t kHistThreads = 256;
-constexpr uint32_t kHistSlice = 16384;                   // scores per CTA
+constexpr uint32_t kHistPer = 4;                         // float4 groups a thread loads at once
+constexpr uint32_t kHistSlice = 4 * kHistPer * kHistThreads;   // scores per CTA (4,096)
 constexpr uint32_t kHistCopies = 4;                      // shared histograms, one per warp mod 4
 
 __global__ void __launch_bounds__(kHistThreads) layers_hist_kernel(const __grid_constant__ LayerBatch b) {
@@ -117,17 +118,23 @@ __global__ void __launch_bounds__(kHistThreads) layers_hist_kernel(const __grid_
   __syncthreads();
   uint32_t* mine = h[(threadIdx.x >> 5) % kHistCopies];
   const bool vec = (reinterpret_cast<uintptr_t>(T.scores + lo) & 15u) == 0;
-  for (uint32_t i0 = lo + 4 * threadIdx.x; i0 < hi; i0 += 4 * kHistThreads) {
-    float f[4];
+  float f[kHistPer][4];                                  // every load of the thread in flight at once
+#pragma unroll
+  for (uint32_t q = 0; q < kHistPer; ++q) {
+    const uint32_t i0 = lo + 4 * (q * kHistThreads + threadIdx.x);
     if (vec && i0 + 3 < hi) {
       const float4 v = __ldg(reinterpret_cast<const float4*>(T.scores + i0));
-      f[0] = v.x, f[1] = v.y, f[2] = v.z, f[3] = v.w;
+      f[q][0] = v.x, f[q][1] = v.y, f[q][2] = v.z, f[q][3] = v.w;
     } else {
-      for (uint32_t e = 0; e < 4; ++e) f[e] = i0 + e < hi ? __ldg(T.scores + i0 + e) : 0.f;
+      for (uint32_t e = 0; e < 4; ++e) f[q][e] = i0 + e < hi ? __ldg(T.scores + i0 + e) : 0.f;
     }
+  }
+#pragma unroll
+  for (uint32_t q = 0; q < kHistPer; ++q) {
+    const uint32_t i0 = lo + 4 * (q * kHistThreads + threadIdx.x);
 #pragma unroll
     for (uint32_t e = 0; e < 4; ++e)
-      if (i0 + e < hi) atomicAdd(&mine[score_key(f[e]) >> topk_detail::kLowBits], 1u);
+      if (i0 + e < hi) atomicAdd(&mine[score_key(f[q][e]) >> topk_detail::kLowBits], 1u);
   }
   __syncthreads();
   for (uint32_t bin = threadIdx.x; bin < topk_detail::kFirstBins; bin += kHistThreads) {
@@ -136,6 +143,7 @@ __global__ void __launch_bounds__(kHistThreads) layers_hist_kernel(const __grid_
     for (uint32_t c = 0; c < kHistCopies; ++c) v += h[c][bin];
     if (v) atomicAdd(&T.first_hist[bin], v);
   }
+  allow_next_grid();                                     // the selections may be scheduled; they wait for this grid
 }
 
 // ------------------------------------------------------------ A: select
@@ -144,6 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1) layers_select_kernel(const __grid
   extern __shared__ __align__(16) uint8_t dyn_smem[];
   __shared__ RadixSmem rsm;
   const LayerCall& T = b.t[blockIdx.x / cluster_size()];
+  wait_previous_grid();                                  // the histograms are complete (after a histogram launch)
   allow_next_grid();                                     // the gathers may be scheduled; they wait for this grid
   int32_t* idx = T.idx;
   const int32_t* pos2slot = b.statics[T.layer].pos2slot;
@@ -245,7 +254,10 @@ __global__ void __launch_bounds__(kGatherThreads) layers_gather_kernel(const __g
   }
   __syncthreads();
 
-  // rows: each warp keeps kGatherInFlight rows in flight
+  // rows: each warp keeps kGatherInFlight rows in flight in registers.
+  // (Staging every piece in shared memory with 16-byte asynchronous copies,
+  // all in flight at once, was slower: 90 vs 70 us for the 78-layer stack's
+  // gathers, 106 vs 65 us at 1M.)
   for (uint32_t e0 = warp; e0 < nj; e0 += kGatherWarps * kGatherInFlight) {
     uint4 va[kGatherInFlight], vb[kGatherInFlight];
 #pragma unroll
@@ -384,12 +396,13 @@ __host__ __device__ inline size_t finish_smem_bytes(uint32_t k, uint32_t H) {
   return (3u * (size_t)k + (H + 31u) / 32u) * 4u;
 }
 
-// One cluster of F CTAs per layer (F = 1 for many layers).  CTA 0 picks the
-// victims and keeps the maps and the LRU queue; then every CTA of the
-// cluster fills its share of the victim slots.  The loads that do not depend
-// on one another are issued together (the positions and the queue window,
-// then their claims and stamps), so that the chain of dependent global
-// accesses stays short after an L2 flush.
+// One cluster of F CTAs per layer (F = 1 for a deep stack, up to 8 when
+// few layers leave SMs free).  CTA 0 picks the victims and keeps the maps
+// and the LRU queue; then every CTA of the cluster fills its share of the
+// victim slots.  The loads that do not depend on one
+// another are issued together (the positions and the queue window, then
+// their claims and stamps), so that the chain of dependent global accesses
+// stays short after an L2 flush.
 template <bool kLru>
 __global__ void __launch_bounds__(kThreads, 1) layers_finish_kernel(const __grid_constant__ LayerBatch b,
                                                                     uint32_t* status) {
@@ -664,8 +677,8 @@ struct LayersConfig {
   bool init = false;
   int active[5] = {0, 0, 0, 0, 0};     // select clusters of 1, 2, 4, 8, 16 CTAs that fit at once (resident)
   int active_stream[5] = {0, 0, 0, 0, 0};
-  int active_finish[4] = {0, 0, 0, 0};   // finish clusters of 1, 2, 4, 8 CTAs that fit at once
   int force_select = 0;
+  int active_finish[4] = {0, 0, 0, 0};   // finish clusters of 1, 2, 4, 8 CTAs that fit at once
 };
 LayersConfig g_layers[64];
 
@@ -793,9 +806,30 @@ cudaError_t launch_config(const void* kern, dim3 grid, uint32_t threads, size_t 
 
 namespace {
 
+// Launch parameters, reused from call to call: clear() keeps the storage, so
+// a call does not zero 10 KB per batch; push() hands out the next one.
+struct BatchList {
+  std::vector<LayerBatch> store;
+  size_t n = 0;
+  void clear() { n = 0; }
+  bool empty() const { return n == 0; }
+  size_t size() const { return n; }
+  LayerBatch& back() { return store[n - 1]; }
+  LayerBatch& operator[](size_t i) { return store[i]; }
+  LayerBatch& push() {
+    if (n == store.size()) store.emplace_back();
+    LayerBatch& b = store[n++];
+    b.ntasks = 0;
+    b.deferred = 0;
+    return b;
+  }
+  LayerBatch* begin() { return store.data(); }
+  LayerBatch* end() { return store.data() + n; }
+};
+
 // Launch parameters of one part of a call, built before its first launch.
 struct PartBuffers {
-  std::vector<LayerBatch> sel, res;
+  BatchList sel, res;
   std::vector<uint32_t> sel_c;
   std::vector<uint8_t> sel_resident;
 };
@@ -816,10 +850,7 @@ cudaError_t enqueue_part(LayersConfig* cfg, const StepTask* tasks, const uint32_
   for (uint32_t w = 0; w < n; ++w) {
     const uint32_t i = which[w];
     if (!tasks[i].scores) continue;
-    if (pb.sel.empty() || pb.sel.back().ntasks == kBatchTasks) {
-      pb.sel.emplace_back();
-      pb.sel.back().ntasks = 0;
-    }
+    if (pb.sel.empty() || pb.sel.back().ntasks == kBatchTasks) pb.sel.push();
     LayerBatch& sb = pb.sel.back();
     sb.t[sb.ntasks++] = make_call(tasks[i], layers[i]);
   }
@@ -829,13 +860,20 @@ cudaError_t enqueue_part(LayersConfig* cfg, const StepTask* tasks, const uint32_
     // resident keys when every selecting layer's slice fits the CTA's
     // shared memory (the smallest such cluster and up), else the filtered
     // route
+    // With the whole-GPU histogram every selection takes the filtered route
+    // (the keys in and above the cut bucket, a few thousand, rather than all
+    // of them: 50K positions, 4-CTA clusters: ~19 us per selection on the
+    // resident route); without it, resident keys where they fit.
     int cmin = 1;
     while (cmin <= 16 && (uint64_t)topk_detail::topk_chunk(nmax, (uint32_t)cmin) * 4u > kSelectMaxSmem) cmin <<= 1;
     if (cfg->force_select && cfg->force_select >= cmin) cmin = cfg->force_select;
-    uint32_t C = cmin <= 16 ? select_cluster(cfg->active, sb.ntasks, cfg->force_select ? cmin : max_cluster, cmin)
-                            : 0u;
+    uint32_t C = !hist && cmin <= 16
+                     ? select_cluster(cfg->active, sb.ntasks, cfg->force_select ? cmin : max_cluster, cmin)
+                     : 0u;
     const bool resident = C != 0;
-    if (!resident) C = select_cluster(cfg->active_stream, sb.ntasks, max_cluster, 2);
+    if (!resident)
+      C = select_cluster(cfg->active_stream, sb.ntasks, cfg->force_select ? cfg->force_select : max_cluster,
+                         cfg->force_select ? cfg->force_select : 2);
     if (!C) return cudaErrorInvalidConfiguration;
     sb.statics = statics;
     sb.k = k;
@@ -848,8 +886,7 @@ cudaError_t enqueue_part(LayersConfig* cfg, const StepTask* tasks, const uint32_
     pb.sel_resident.push_back(resident ? 1 : 0);
   }
   for (uint32_t first = 0; first < n; first += kBatchTasks) {
-    pb.res.emplace_back();
-    LayerBatch& rb = pb.res.back();
+    LayerBatch& rb = pb.res.push();
     rb.ntasks = n - first < kBatchTasks ? n - first : kBatchTasks;
     for (uint32_t i = 0; i < rb.ntasks; ++i) rb.t[i] = make_call(tasks[which[first + i]], layers[which[first + i]]);
     rb.statics = statics;
@@ -871,14 +908,16 @@ cudaError_t enqueue_part(LayersConfig* cfg, const StepTask* tasks, const uint32_
   if (ev && (e = cudaEventRecord(ev[0], stream)) != cudaSuccess) return e;
   for (size_t i = 0; i < pb.sel.size(); ++i) {
     const bool resident = pb.sel_resident[i] != 0;
+    bool hist_before = false;
     if (!resident && hist) {
       layers_hist_kernel<<<pb.sel[i].ntasks * pb.sel[i].chunks, kHistThreads, 0, stream>>>(pb.sel[i]);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
       ++*launched;
+      hist_before = true;
     }
     launch_config(nullptr, dim3(pb.sel_c[i] * pb.sel[i].ntasks, 1, 1), kThreads,
-                  resident ? pb.sel[i].cand_bytes : topk_detail::kTopkMaxDynSmem, stream, pb.sel_c[i], false, &lc,
-                  attr);
+                  resident ? pb.sel[i].cand_bytes : topk_detail::kTopkMaxDynSmem, stream, pb.sel_c[i],
+                  hist_before && !ev, &lc, attr);
     e = resident ? cudaLaunchKernelEx(&lc, layers_select_kernel<true>, pb.sel[i])
                  : cudaLaunchKernelEx(&lc, layers_select_kernel<false>, pb.sel[i]);
     if (e != cudaSuccess) return e;
@@ -944,7 +983,8 @@ cudaError_t enqueue_part(LayersConfig* cfg, const StepTask* tasks, const uint32_
   const size_t fsmem = finish_smem_bytes(k, tasks[which[0]].L.hot_rows);
   for (const LayerBatch& rb : pb.res) {
     // CTAs per layer for the fills: the largest cluster whose clusters all
-    // run at once (one CTA per layer for a deep stack)
+    // run at once (one CTA per layer for a deep stack; 8 layers of 1M
+    // positions and ~2,000 fills each: 8-CTA clusters, 47 -> 25 us)
     uint32_t F = 1;
     for (int i = 3; i >= 1; --i)
       if (cfg->active_finish[i] >= (int)rb.ntasks) {

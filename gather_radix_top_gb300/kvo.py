@@ -38,7 +38,8 @@ EXPORTED = [
     "kvo_pool_read", "kvo_pool_fill", "kvo_store_blocks", "kvo_pool_release", "kvo_restore_blocks",
     "kvo_pool_sync", "kvo_pool_block_table", "kvo_pool_get_stats", "kvo_pool_debug_fail_after",
     "kvo_pool_debug_free_queue", "kvo_copy_blocks_noalloc", "kvo_set_phase_timing", "kvo_layers_phase_times",
-    "kvo_layers_launch_count", "kvo_probe_host_touch", "kvo_debug_history_host", "kvo_set_miss_fetch",
+    "kvo_layers_counters", "kvo_probe_host_touch", "kvo_debug_history_host", "kvo_set_miss_fetch",
+    "kvo_touch_history",
 ]
 
 
@@ -132,10 +133,11 @@ def lib() -> ctypes.CDLL:
         "kvo_copy_blocks_noalloc": (ctypes.c_int, [_vp, _vp, _i64, _vp, _i64, _vp]),
         "kvo_set_phase_timing": (ctypes.c_int, [_vp, _i32]),
         "kvo_layers_phase_times": (ctypes.c_int, [_vp, _vp, _vp]),
-        "kvo_layers_launch_count": (ctypes.c_int, [_vp, _vp]),
+        "kvo_layers_counters": (ctypes.c_int, [_vp, _vp, _vp]),
         "kvo_probe_host_touch": (ctypes.c_int, [_vp, _i64, _i64, _vp, _vp]),
         "kvo_debug_history_host": (ctypes.c_int, [_vp, _i32, _vp]),
         "kvo_set_miss_fetch": (ctypes.c_int, [_vp, _i32, _i32]),
+        "kvo_touch_history": (ctypes.c_int, [_vp, _i32, _vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -183,8 +185,8 @@ def _dev_ptr(t, dtype_name: str | None = None):
 
 
 def _stream_ptr(stream):
-    import torch
     if stream is None:
+        import torch
         stream = torch.cuda.current_stream()
     return ctypes.c_void_p(stream.cuda_stream)
 
@@ -484,16 +486,20 @@ class Context:
     def set_phase_timing(self, on=True):
         _check(lib().kvo_set_phase_timing(self.handle, 1 if on else 0), "kvo_set_phase_timing")
 
+    def touch_history(self, layer=-1, stream=None):
+        _check(lib().kvo_touch_history(self.handle, layer, _stream_ptr(stream)), "kvo_touch_history")
+
     def history_host(self, layer) -> int:
         """Host address of the layer's pinned history (read-only use)."""
         p = ctypes.c_void_p()
         _check(lib().kvo_debug_history_host(self.handle, layer, ctypes.byref(p)), "kvo_debug_history_host")
         return p.value
 
-    def layers_launch_count(self) -> int:
-        n = ctypes.c_int64()
-        _check(lib().kvo_layers_launch_count(self.handle, ctypes.byref(n)), "kvo_layers_launch_count")
-        return n.value
+    def layers_counters(self):
+        """(kernels launched by kvo_decode_layers, host seconds spent in its calls)."""
+        n, t = ctypes.c_int64(), ctypes.c_double()
+        _check(lib().kvo_layers_counters(self.handle, ctypes.byref(n), ctypes.byref(t)), "kvo_layers_counters")
+        return n.value, t.value
 
     def layers_phase_times(self):
         """(select, gather, finish) milliseconds summed over the recorded

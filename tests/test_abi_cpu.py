@@ -50,6 +50,14 @@ def test_bad_arguments_rejected_without_a_device(kvo):
     assert L.kvo_append_rows(None, 0, None, 1, None) == kvo.KVO_EINVAL
     assert L.kvo_destroy(None) == kvo.KVO_EINVAL
     assert L.kvo_set_policy(None, 0) == kvo.KVO_EINVAL
+    assert L.kvo_decode_layers(None, None, 1, 16, None) == kvo.KVO_EINVAL
+    assert L.kvo_set_miss_fetch(None, 0, 0) == kvo.KVO_EINVAL
+    assert L.kvo_set_phase_timing(None, 1) == kvo.KVO_EINVAL
+    assert L.kvo_layers_phase_times(None, None, None) == kvo.KVO_EINVAL
+    assert L.kvo_layers_counters(None, None, None) == kvo.KVO_EINVAL
+    assert L.kvo_touch_history(None, -1, None) == kvo.KVO_EINVAL
+    assert L.kvo_debug_raise_status(None, 4) == kvo.KVO_EINVAL
+    assert L.kvo_probe_host_touch(None, 16, 16, None, None) == kvo.KVO_EINVAL
     assert kvo.status_string(kvo.KVO_ERANGE) == "selected position outside the history"
 
 

@@ -317,6 +317,30 @@ def test_timed_out_copy_makes_the_context_refuse_launches(kvo):
     ctx.close()
 
 
+def test_touch_history_changes_nothing(kvo):
+    """kvo_touch_history reads one piece per 4 KiB of every layer's history
+    and changes no state: the maps before and after are equal, and the next
+    step still equals the oracle's."""
+    w = W.TINY.scaled(steps=3)
+    ctx = kvo.Context(2, w.history_cap, w.hot_rows)
+    g = GpuLayerRun(w, 0, ctx=ctx, ctx_layer=0)
+    o = OracleLayerRun(w, 0)
+    for step in range(2):
+        np.testing.assert_array_equal(g.step(step), o.step(step))
+    before = ctx.dump_layer(0)
+    ctx.touch_history()                                  # every layer (layer 1 is empty)
+    ctx.touch_history(0)
+    assert ctx.sync() == 0
+    after = ctx.dump_layer(0)
+    for key in ("pos2slot", "slot2pos", "last_use", "hot"):
+        np.testing.assert_array_equal(before[key], after[key])
+    np.testing.assert_array_equal(g.step(2), o.step(2))
+    np.testing.assert_array_equal(g.rows(), o.last.rows)
+    with pytest.raises(kvo.KvoError):
+        ctx.touch_history(2)
+    ctx.close()
+
+
 # ------------------------------------------------ fused decode step
 @pytest.mark.parametrize("appends", [0, 2])
 def test_decode_step_tiny_full_parity(kvo, appends):

@@ -139,24 +139,24 @@ def algorithmic_bytes(w: W.Workload, n_avg: float, stats_delta: dict, resolve_la
 
 def gather_bytes(w: W.Workload, ab: dict) -> float:
     """HBM bytes of one layer in the gather launch of kvo_decode_layers: its
-    positions and their pos2slot entries (4k + 4k), the hit slots' stamps and
-    rows (4 + 656 per hit), the output (R_out per entry) and this step's new
-    rows read from their device copy; misses cross the host link instead."""
+    entry codes and positions (4k + 4k), the hit rows (656 per hit), the
+    output (R_out per entry) and the fills (656 written to each victim slot
+    from the same registers); misses cross the host link instead."""
     k = w.k * w.queries
     r_out = ROW + (2 * 576 if w.bf16 else 0)
-    return 8 * k + (4 + ROW) * ab["hits"] + r_out * k
+    return 8 * k + ROW * ab["hits"] + r_out * k + ROW * ab["fills"]
 
 
-def finish_bytes(w: W.Workload, ab: dict) -> float:
-    """HBM bytes of one layer in the finish launch: the positions and their
-    claims again (8k), the LRU queue window and its slots' last_use (12 per
-    entry; up to 4,096), the map updates (16 per fill), the fills (656 read
-    from the output, 656 written to the slot), the scan of last_use for the
-    used slots (4 per slot) and their queue entries (8 per used slot), and
-    the new rows' copy to the host history (656 read per row)."""
+def resolve_bytes(w: W.Workload, ab: dict) -> float:
+    """HBM bytes of one layer in the resolve launch: the positions and their
+    pos2slot entries (8k), the hit stamps (4 per hit), the misses' claims
+    and their re-read (8 per miss), the LRU queue window and its slots'
+    last_use (12 per entry; up to 4,096), the map updates (16 per fill), the
+    entry codes (4k), the used slots' queue entries (8 per used slot), and
+    the new rows read from their device copy (656 per row)."""
     k = w.k * w.queries
     window = min(4096, 8 * w.hot_rows)
-    return (8 * k + 12 * window + (16 + 2 * ROW) * ab["fills"] + 4 * w.hot_rows
+    return (12 * k + 4 * ab["hits"] + 8 * ab["misses"] + 12 * window + 16 * ab["fills"]
             + 8 * (ab["hits"] + ab["fills"]) + ROW * w.appends_per_step)
 
 
@@ -549,11 +549,11 @@ def run_gpu_arm(args, w, rank, world):
             wl.step(s, ev)
             pev.append(ev)
         torch.cuda.synchronize()
-        (t_sel, t_gat, t_fin), calls = wl.ctx.layers_phase_times()
+        (t_sel, t_res, t_gat), calls = wl.ctx.layers_phase_times()
         wl.ctx.set_phase_timing(False)
         pst1 = {l: wl.ctx.stats(l) for l in range(w.layers)}
-        phases = {"calls": calls, "steps": phase_steps, "layers_select": t_sel, "layers_gather": t_gat,
-                  "layers_finish": t_fin, "step_ms": [a.elapsed_time(b) for a, b in pev],
+        phases = {"calls": calls, "steps": phase_steps, "layers_select": t_sel, "layers_resolve": t_res,
+                  "layers_gather": t_gat, "step_ms": [a.elapsed_time(b) for a, b in pev],
                   "delta": {f: sum(pst1[l][f] - pst0[l][f] for l in range(w.layers)) for f in pst0[0]}}
     step_ms = [a.elapsed_time(b) for a, b in evs]
     total_s = sum(step_ms) * 1e-3
@@ -1494,22 +1494,22 @@ def main():
                      "the launches of each kvo_decode_layers call (launches serialised on one stream); step "
                      f"p50 there {1e3 * float(np.percentile(ph['step_ms'], 50)):.1f} us")
         # kvo_decode_layers by its launches, from the pass after the timed
-        # region: the selections, the gathers (one launch over every layer of
-        # the call) and the finishes, with their own counters
+        # region: the selections, the resolves and the gathers (one launch
+        # over every layer of the call), with their own counters
         pst = ph["steps"]
         calls_per_step = ph["calls"] / pst
         nmean_p = float(np.mean([w.n_at(s) for s in range(args.warmup + args.steps,
                                                               args.warmup + args.steps + pst)]))
         abp = algorithmic_bytes(w, nmean_p, ph["delta"], pst * w.layers, pst * len(w.selecting_layers()))
-        kern_tot = {"layers_select": ph["layers_select"], "layers_gather": ph["layers_gather"],
-                    "layers_finish": ph["layers_finish"]}
+        kern_tot = {"layers_select": ph["layers_select"], "layers_resolve": ph["layers_resolve"],
+                    "layers_gather": ph["layers_gather"]}
         kern_avg = {"layers_select": ph["layers_select"] / pst,
-                    "layers_gather": ph["layers_gather"] / ph["calls"],
-                    "layers_finish": ph["layers_finish"] / ph["calls"], "layers": kern_avg.get("layers")}
+                    "layers_resolve": ph["layers_resolve"] / ph["calls"],
+                    "layers_gather": ph["layers_gather"] / ph["calls"], "layers": kern_avg.get("layers")}
         gb = gather_bytes(w, abp)
         per_launch = {"layers_select": len(w.selecting_layers()) * abp["select_hbm"],
-                      "layers_gather": w.layers * gb / calls_per_step,
-                      "layers_finish": w.layers * finish_bytes(w, abp) / calls_per_step}
+                      "layers_resolve": w.layers * resolve_bytes(w, abp) / calls_per_step,
+                      "layers_gather": w.layers * gb / calls_per_step}
     else:
         per_launch = {"resolve": ab["resolve_hbm"], "select": ab["select_hbm"],
                       "append": 2 * ROW * w.appends_per_step,

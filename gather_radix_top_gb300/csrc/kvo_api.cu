@@ -46,6 +46,7 @@ struct kvo_ctx {
   kvo::LayerStatic* statics = nullptr;   // device [layers]: what the batched decode step reads per layer
   uint32_t* first_hist = nullptr;        // device [layers][2048]: the batched step's filtering histograms (zero
                                          // between calls: each selection zeroes its own after use)
+  uint32_t* ent = nullptr;               // device [layers][KVO_MAX_K]: the batched step's entry codes
   bool statics_dirty = true;             // the views changed since the last upload
   int64_t launches = 0;                  // kernels kvo_decode_layers has launched
   double host_seconds = 0.0;             // host time spent inside kvo_decode_layers
@@ -95,6 +96,7 @@ void free_ctx(kvo_ctx* c) {
   cudaFree(c->status);
   cudaFree(c->statics);
   cudaFree(c->first_hist);
+  cudaFree(c->ent);
   cudaFree(c->touch_sink);
   cudaFreeHost(const_cast<int2*>(c->defer.dlist_host));
   cudaFree(c->defer.dcount_dev);
@@ -432,6 +434,7 @@ kvo_status kvo_create(int32_t layers, int64_t history_cap, int32_t hot_rows, int
               ok(cudaMalloc(&c->statics, sizeof(kvo::LayerStatic) * layers)) &&
               ok(cudaMalloc(&c->first_hist, sizeof(uint32_t) * 2048 * layers)) &&
               ok(cudaMemset(c->first_hist, 0, sizeof(uint32_t) * 2048 * layers)) &&
+              ok(cudaMalloc(&c->ent, sizeof(uint32_t) * KVO_MAX_K * layers)) &&
               ok(cudaMemset(c->counters, 0, sizeof(uint32_t) * 8 * layers)) &&
               ok(cudaMemset(c->stats, 0, sizeof(unsigned long long) * 8 * layers)) &&
               ok(cudaMemset(c->status, 0, sizeof(uint32_t)));
@@ -772,7 +775,7 @@ static kvo_status decode_layers_impl(kvo_ctx* ctx, const kvo_layer_task* tasks, 
   }
   uint32_t launched = 0;
   const cudaError_t e = kvo::launch_layers(st.data(), lay.data(), (uint32_t)ntasks, (uint32_t)k, ctx->statics,
-                                           ctx->status, ctx->max_cluster, s, ev, ctx->first_hist,
+                                           ctx->status, ctx->max_cluster, s, ev, ctx->first_hist, ctx->ent,
                                            batched ? &ctx->defer : nullptr, &launched);
   if (!ok(e)) return KVO_ECUDA;
   ctx->launches += launched;

@@ -80,9 +80,9 @@ struct LayerStatic {
 // memory; a device counter per layer; the staging rows; the per-layer host
 // history.
 struct LayersDefer {
-  int2* dlist_dev;              // [layers][KVO_MAX_K] (entry, position), written by the gathers
+  int2* dlist_dev;              // [layers][KVO_MAX_K] (entry, position), written by the resolves
   const int2* dlist_host;
-  uint32_t* dcount_dev;         // [layers], zero between calls
+  uint32_t* dcount_dev;         // [layers], the length of each layer's list
   uint32_t* dcount_host;        // [layers], pinned, copied from dcount_dev
   int2* plist_host;             // [layers][KVO_MAX_K] (entry, staging row), written by the host
   const int2* plist_dev;
@@ -93,20 +93,23 @@ struct LayersDefer {
   const uint8_t* const* hist_host;   // [layers]: host address of each layer's history
 };
 
-// One decode step of many layers in three launches over all of them (select,
-// gather, finish); tasks without scores read their idx after the selections.
-// layers[i]: task i's layer (its entry of `statics`, a device array).  ev:
-// NULL, or four events recorded before the selections, before the gathers,
-// before the finishes and after them (without events, each launch may be
-// scheduled before the previous one ends and waits for it on the GPU).
-// hist: device [layers][2048] counts, zero between calls (the filtered
-// selections' histograms), or NULL.  defer: NULL for zero-copy loads of the
-// misses, else the batched-copy fetch (the host waits for the gathers, then
-// copies the missing rows with one cudaMemcpyAsync per run of consecutive
+// One decode step of many layers in three launches over all of them
+// (select, resolve, gather); tasks without scores read their idx after the
+// selections.  layers[i]: task i's layer (its entry of `statics`, a device
+// array).  ev: NULL, or four events recorded before the selections, before
+// the resolves, before the gathers and after them (without events, each
+// launch may be scheduled before the previous one ends and waits for it on
+// the GPU).  hist: device [layers][2048] counts, zero between calls (the
+// filtered selections' histograms), or NULL.  ent: device
+// [layers][KVO_MAX_K] words, the entry codes the resolves hand to the
+// gathers.  defer: NULL for zero-copy loads of the misses, else the
+// batched-copy fetch (the host waits for the resolves' lists, then copies
+// the missing rows with one cudaMemcpyAsync per run of consecutive
 // positions).  *launched grows by the number of kernels launched.
 cudaError_t launch_layers(const StepTask* tasks, const uint32_t* layers, uint32_t ntasks, uint32_t k,
                           const LayerStatic* statics, uint32_t* status, int max_cluster, cudaStream_t stream,
-                          cudaEvent_t* ev, uint32_t* hist, const LayersDefer* defer, uint32_t* launched);
+                          cudaEvent_t* ev, uint32_t* hist, uint32_t* ent, const LayersDefer* defer,
+                          uint32_t* launched);
 cudaError_t launch_decode_step(const LayerView& L, const void* new_rows, uint32_t r, uint32_t old_len,
                                const float* scores, uint32_t n, uint32_t k, int32_t* idx, uint8_t* out_rows,
                                uint16_t* out_bf16, uint32_t* status, int max_cluster, cudaStream_t stream,

@@ -1,29 +1,31 @@
 // One decode step of many layers (kvo_decode_layers) in three launches, each
 // over every layer of the call at once:
 //   A select:  the top-K of every layer that brings scores (one cluster per
-//              selecting layer, the body of kvo_select_topk);
-//   B gather:  every selected entry of every layer: lookup, classify (hit:
-//              stamp; miss: first-occurrence claim), and the row copied to
-//              the output, hits from the HBM hot slot, misses from host
-//              memory (or the recent ring, or this call's new rows), with
-//              the bf16 dequant; the whole GPU moves rows, so the step runs
-//              at the rate of HBM and of the host link rather than at the
-//              latency of one cluster per layer;
-//   C finish:  one CTA per layer: rank the unique misses, walk the LRU queue
-//              (or the circular hand) for their victims, update the maps,
-//              fill the victim slots from the rows B wrote, append the new
-//              rows to the host history or the recent ring, and append the
-//              used slots to the LRU queue.
+//              selecting layer, the body of kvo_select_topk; histories too
+//              long for a cluster's shared memory take their first key digit
+//              from a whole-GPU histogram launch before it);
+//   B resolve: one CTA per layer: look every selected position up (hit:
+//              stamp its slot; miss: first-occurrence claim), rank the
+//              unique misses, walk the LRU queue (or the circular hand) for
+//              their victims, update the maps, append the new rows to the
+//              host history or the recent ring, append the used slots to the
+//              LRU queue, and leave one code per entry for C;
+//   C gather:  every selected entry of every layer on the whole GPU: the row
+//              to the output with the bf16 dequant, hits from the HBM slot,
+//              misses from host memory (or the recent ring, or this call's
+//              new rows) and, for a position's first occurrence, into its
+//              victim slot from the same registers; the step runs at the rate
+//              of HBM and of the host link rather than at the latency of one
+//              cluster per layer.
 //
 // "From 1M Total to 15+ x 1M Contexts: GLM-5.3 KV Cache Offloading":
 //   "Decision three: let the GPU manage the hot cache directly" - hits read
 //   the HBM slot, misses read the registered host copy, the gather emits a
 //   compact selection, and the CPU stays out of the per-selection loop;
-//   "GPU cache management has hazards too" - a slot filled in this round is
-//   a hit source only in the next round (fills happen in C, after every row
-//   of B is out), duplicate misses read host memory, and slots used by the
-//   round are pinned (B stamps every hit slot with the step before C picks
-//   victims among the slots not stamped);
+//   "GPU cache management has hazards too" - the victims are slots the step
+//   does not use (B stamps every hit slot before it picks them), so no row C
+//   writes into the cache is one C reads in the same step; duplicate misses
+//   read host memory;
 //   "Separate historical capacity from the current working set" - later
 //   layers reuse a selection: a layer without scores resolves its idx as it
 //   stands after A, so it may name the idx of a selecting layer of the same
@@ -31,9 +33,9 @@
 //
 // Results equal those of the single-layer calls in the order append, select,
 // resolve (the same LRU queue, the same first-occurrence dedupe, the same
-// (last_use, slot) victim order).  Nothing but the layers' own tables and the
-// caller's outputs carries state from one launch to the next: B leaves its
-// claims in pos2slot and its stamps in last_use, and C reads them there.
+// (last_use, slot) victim order).  Nothing but the layers' own tables, the
+// entry codes and the caller's outputs carries state from one launch to the
+// next.
 #include <algorithm>
 #include <cstdint>
 #include <cstdlib>
@@ -66,6 +68,7 @@ struct LayerCall {
   uint32_t r;                   // new rows
   uint32_t to_ram;              // the first to_ram new rows go to the host history, the rest to the ring
   uint32_t* first_hist;         // filtered selections: the histogram of the scores' top key bits, or NULL
+  uint32_t* ent;                // [k] entry codes, written by B and read by C
 };
 
 constexpr uint32_t kBatchTasks = 128;                    // layers per launch (9 KB of parameters)
@@ -169,12 +172,21 @@ __global__ void __launch_bounds__(kThreads, 1) layers_select_kernel(const __grid
     for (uint32_t bin = threadIdx.x; bin < topk_detail::kFirstBins; bin += kThreads) T.first_hist[bin] = 0;
 }
 
-// ------------------------------------------------------------ B: gather
-constexpr uint32_t kGatherThreads = 256;
-constexpr uint32_t kGatherWarps = kGatherThreads / 32;
-constexpr uint32_t kGatherEntries = 64;                  // entries per CTA
-constexpr uint32_t kGatherInFlight = 4;                  // rows a warp loads before it stores
-static_assert(kGatherEntries <= kGatherThreads, "one thread per entry classifies");
+// ------------------------------------------------------------ B: resolve
+// Entry codes: B writes one per selected entry of a layer (ent[j]), C reads
+// them.  A hit holds its slot; a miss is flagged, and when it is the first
+// occurrence of its position it also holds the victim slot its row goes to.
+constexpr uint32_t kEntInvalid = 0xffffffffu;            // position out of range: a zero row
+constexpr uint32_t kEntMiss = 1u << 31;                  // the row comes from its source
+constexpr uint32_t kEntFill = 1u << 30;                  // ... and is written to the slot in the low bits too
+constexpr uint32_t kEntLater = 1u << 29;                 // ... by a batched copy (placed after the copies)
+constexpr uint32_t kEntSlot = (1u << 24) - 1u;
+static_assert(KVO_MAX_HOT_ROWS <= kEntSlot, "a slot fits the entry code");
+
+constexpr uint32_t kFinishPer = 4;                        // queue entries a thread examines per round
+constexpr uint32_t kFinishEntries = KVO_MAX_K / kThreads;  // selection entries per thread
+constexpr uint32_t kCompactPer = 16;                      // queue entries a thread keeps in flight when compacting
+constexpr uint32_t kNoEntry = 0xffffffffu;
 
 // The row of a missing position: this call's new rows from their device
 // copy; rows still waiting in the recent ring from the ring; else the host
@@ -188,163 +200,6 @@ __device__ __forceinline__ const uint4* miss_source(const LayerStatic& S, const 
   *host = true;
   return reinterpret_cast<const uint4*>(S.hist) + (size_t)p * kRowVec;
 }
-
-__global__ void __launch_bounds__(kGatherThreads) layers_gather_kernel(const __grid_constant__ LayerBatch b,
-                                                                       uint32_t* status) {
-  __shared__ const uint4* src[kGatherEntries];           // NULL: an invalid entry (zero row)
-  __shared__ uint8_t later[kGatherEntries];              // the row comes by a batched copy (placed later)
-  __shared__ uint32_t cnt[4];                            // hits, misses, RAM reads, invalid
-  const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const LayerCall& T = b.t[blockIdx.x / b.chunks];
-  const LayerStatic S = b.statics[T.layer];
-  const uint32_t k = b.k;
-  const uint32_t j0 = (blockIdx.x % b.chunks) * kGatherEntries;
-  const uint32_t nj = j0 < k ? min(kGatherEntries, k - j0) : 0u;
-  if (tid < 4) cnt[tid] = 0;
-  wait_previous_grid();                                  // the selections are complete
-  __syncthreads();
-
-  // classify: one thread per entry
-  uint32_t hit = 0, miss = 0, ram = 0, inv = 0;
-  if (tid < nj) {
-    const uint32_t j = j0 + tid;
-    const int32_t p = T.idx[j];
-    const uint4* s = nullptr;
-    uint8_t defer = 0;
-    if (p < 0 || (uint32_t)p >= T.len) {
-      inv = 1;
-    } else {
-      int32_t sl = __ldcg(&S.pos2slot[p]);
-      if (sl >= (int32_t)S.hot_rows) {
-        atomicOr(status, kFlagInternal);                 // cannot happen; keep every index in bounds
-        sl = -1;
-      }
-      if (sl >= 0) {
-        S.last_use[sl] = S.counters[0] + 1u;             // pinned for this step
-        s = reinterpret_cast<const uint4*>(S.hot) + (size_t)sl * kRowVec;
-        hit = 1;
-      } else {
-        atomicMin(&S.pos2slot[p], (int32_t)j - (int32_t)k - 1);   // the smallest j claims the position
-        bool host;
-        s = miss_source(S, T, (uint32_t)p, &host);
-        miss = 1;
-        if (host && b.deferred) {                        // listed for the host's batched copies
-          const uint32_t i = atomicAdd(&b.dcount[T.layer], 1u);
-          b.dlist[(size_t)T.layer * KVO_MAX_K + i] = make_int2((int32_t)j, p);
-          defer = 1;
-        }
-        // a RAM read as append-then-resolve defines it: below the RAM length
-        // (this call's own rows there are served from their device copy,
-        // which holds the same bytes)
-        ram = !(S.ring_rows && (uint32_t)p >= T.ram_len);
-      }
-    }
-    src[tid] = s;
-    later[tid] = defer;
-  }
-  if (warp * 32 < nj) {                                  // warps holding entries: their counts
-    const uint32_t h = __reduce_add_sync(0xffffffffu, hit), m = __reduce_add_sync(0xffffffffu, miss);
-    const uint32_t rr = __reduce_add_sync(0xffffffffu, ram), iv = __reduce_add_sync(0xffffffffu, inv);
-    if (lane == 0) {
-      if (h) atomicAdd(&cnt[0], h);
-      if (m) atomicAdd(&cnt[1], m);
-      if (rr) atomicAdd(&cnt[2], rr);
-      if (iv) atomicAdd(&cnt[3], iv);
-    }
-  }
-  __syncthreads();
-
-  // rows: each warp keeps kGatherInFlight rows in flight in registers.
-  // (Staging every piece in shared memory with 16-byte asynchronous copies,
-  // all in flight at once, was slower: 90 vs 70 us for the 78-layer stack's
-  // gathers, 106 vs 65 us at 1M.)
-  for (uint32_t e0 = warp; e0 < nj; e0 += kGatherWarps * kGatherInFlight) {
-    uint4 va[kGatherInFlight], vb[kGatherInFlight];
-#pragma unroll
-    for (uint32_t u = 0; u < kGatherInFlight; ++u) {
-      const uint32_t e = e0 + u * kGatherWarps;
-      va[u] = make_uint4(0, 0, 0, 0);
-      vb[u] = make_uint4(0, 0, 0, 0);
-      const uint4* s = e < nj && !later[e] ? src[e] : nullptr;
-      if (s) {
-        va[u] = s[lane];
-        if (lane < kRowVec - 32) vb[u] = s[32 + lane];
-      }
-    }
-#pragma unroll
-    for (uint32_t u = 0; u < kGatherInFlight; ++u) {
-      const uint32_t e = e0 + u * kGatherWarps;
-      if (e >= nj) break;
-      if (later[e]) continue;
-      const uint32_t j = j0 + e;
-      if (T.out_rows) {
-        uint4* d = reinterpret_cast<uint4*>(T.out_rows) + (size_t)j * kRowVec;
-        d[lane] = va[u];
-        if (lane < kRowVec - 32) d[32 + lane] = vb[u];
-      }
-      if (T.out_bf16) dequant_row(va[u], vb[u], lane, reinterpret_cast<uint4*>(T.out_bf16 + (size_t)j * KVO_DEQUANT_VALUES));
-    }
-  }
-  if (tid == 0) {
-    unsigned long long* st = S.stats;
-    if (cnt[0]) atomicAdd(st + 1, (unsigned long long)cnt[0]);
-    if (cnt[1]) atomicAdd(st + 2, (unsigned long long)cnt[1]);
-    if (cnt[2]) atomicAdd(st + 6, (unsigned long long)cnt[2] * KVO_ROW_BYTES);
-    if (cnt[3]) {
-      atomicAdd(st + 5, (unsigned long long)cnt[3]);
-      atomicOr(status, kFlagRange);
-    }
-  }
-  allow_next_grid();                                     // the finishes may be scheduled; they wait for this grid
-}
-
-// --------------------------------------------------- B2: batched placement
-// The rows the host copied into staging, to their entries of the output
-// (and their bf16 rows): one warp per row, kGatherInFlight rows in flight.
-__global__ void __launch_bounds__(kGatherThreads) layers_place_kernel(const __grid_constant__ LayerBatch b) {
-  const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const LayerCall& T = b.t[blockIdx.x / b.chunks];
-  wait_previous_grid();
-  const uint32_t m = b.pcount[T.layer];
-  const uint32_t e0 = (blockIdx.x % b.chunks) * kGatherEntries;
-  const int2* pl = b.plist + (size_t)T.layer * KVO_MAX_K;
-  const uint4* stage = reinterpret_cast<const uint4*>(b.staging) + (size_t)T.layer * b.k * kRowVec;
-  for (uint32_t i0 = e0 + warp; i0 < min(m, e0 + kGatherEntries); i0 += kGatherWarps * kGatherInFlight) {
-    uint4 va[kGatherInFlight], vb[kGatherInFlight];
-    int2 pe[kGatherInFlight];
-#pragma unroll
-    for (uint32_t u = 0; u < kGatherInFlight; ++u) {
-      const uint32_t i = i0 + u * kGatherWarps;
-      pe[u] = i < min(m, e0 + kGatherEntries) ? pl[i] : make_int2(-1, -1);
-      va[u] = make_uint4(0, 0, 0, 0);
-      vb[u] = make_uint4(0, 0, 0, 0);
-      if (pe[u].x >= 0 && (uint32_t)pe[u].x < b.k && (uint32_t)pe[u].y < b.k) {
-        const uint4* s = stage + (size_t)pe[u].y * kRowVec;
-        va[u] = s[lane];
-        if (lane < kRowVec - 32) vb[u] = s[32 + lane];
-      }
-    }
-#pragma unroll
-    for (uint32_t u = 0; u < kGatherInFlight; ++u) {
-      if (pe[u].x < 0 || (uint32_t)pe[u].x >= b.k || (uint32_t)pe[u].y >= b.k) continue;
-      const uint32_t j = (uint32_t)pe[u].x;
-      if (T.out_rows) {
-        uint4* d = reinterpret_cast<uint4*>(T.out_rows) + (size_t)j * kRowVec;
-        d[lane] = va[u];
-        if (lane < kRowVec - 32) d[32 + lane] = vb[u];
-      }
-      if (T.out_bf16) dequant_row(va[u], vb[u], lane, reinterpret_cast<uint4*>(T.out_bf16 + (size_t)j * KVO_DEQUANT_VALUES));
-    }
-  }
-  allow_next_grid();
-}
-
-// ------------------------------------------------------------ C: finish
-constexpr uint32_t kFinishPer = 4;                        // queue entries a thread examines per round
-constexpr uint32_t kFinishEntries = KVO_MAX_K / kThreads;  // selection entries per thread
-constexpr uint32_t kCompactPer = 16;                      // queue entries a thread keeps in flight when compacting
-constexpr uint32_t kNoEntry = 0xffffffffu;
-constexpr uint32_t kFillInFlight = 8;                     // fill pieces a thread loads before it stores
 
 // Copies the current entries of [head, tail) of queue buffer `buf`, in
 // order, to the front of the other buffer; returns how many (the number of
@@ -389,287 +244,469 @@ __device__ uint32_t compact_queue_cta(const LayerStatic& T, uint32_t head, uint3
   return kept;
 }
 
-// Shared memory of the finish launch (4-byte words): per unique miss u its
-// entry, victim slot and position, then the bitmap of the slots used in the
-// step (hits, then victims).
-__host__ __device__ inline size_t finish_smem_bytes(uint32_t k, uint32_t H) {
-  return (3u * (size_t)k + (H + 31u) / 32u) * 4u;
+// Shared memory of the resolve launch (4-byte words): per unique miss u its
+// entry, victim slot and position; every entry's code; then the bitmap of
+// the slots used in the step (hits, then victims).
+__host__ __device__ inline size_t resolve_smem_bytes(uint32_t k, uint32_t H) {
+  return (4u * (size_t)k + (H + 31u) / 32u) * 4u;
 }
 
-// One cluster of F CTAs per layer (F = 1 for a deep stack, up to 8 when
-// few layers leave SMs free).  CTA 0 picks the victims and keeps the maps
-// and the LRU queue; then every CTA of the cluster fills its share of the
-// victim slots.  The loads that do not depend on one
-// another are issued together (the positions and the queue window, then
-// their claims and stamps), so that the chain of dependent global accesses
-// stays short after an L2 flush.
+// One CTA per layer.  The loads that do not depend on one another are
+// issued together (the positions and the first queue window, then the
+// positions' slots and the window's stamps), so that the chain of dependent
+// global accesses stays short after an L2 flush.
 template <bool kLru>
-__global__ void __launch_bounds__(kThreads, 1) layers_finish_kernel(const __grid_constant__ LayerBatch b,
-                                                                    uint32_t* status) {
+__global__ void __launch_bounds__(kThreads, 1) layers_resolve_kernel(const __grid_constant__ LayerBatch b,
+                                                                     uint32_t* status) {
   extern __shared__ __align__(16) uint32_t fsm[];
   __shared__ uint32_t scratch[2 * kWarps + 2];
-  __shared__ uint32_t head_hit, last_vic, nevict, nvic_s;
-  const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const uint32_t F = cluster_size(), f = cluster_rank();
-  const LayerCall& T = b.t[blockIdx.x / F];
+  __shared__ uint32_t head_hit, last_vic, nevict, cnt[4];
+  const uint32_t tid = threadIdx.x, lane = tid & 31;
+  const LayerCall& T = b.t[blockIdx.x];
   const LayerStatic S = b.statics[T.layer];
   const uint32_t k = b.k, H = S.hot_rows;
   uint32_t* mlist = fsm;                                 // [k]: entry of unique miss u
   uint32_t* vslot = fsm + k;                             // [k]: victim slot of unique miss u
   int32_t* mpos = reinterpret_cast<int32_t*>(fsm + 2 * k);   // [k]: position of unique miss u
-  uint32_t* used = fsm + 3 * k;                          // [ceil(H/32)]: slots used in this step
+  uint32_t* code = fsm + 3 * k;                          // [k]: entry codes
+  uint32_t* used = fsm + 4 * k;                          // [ceil(H/32)]: slots used in this step
   const uint32_t hwords = (H + 31u) / 32u;
-  wait_previous_grid();                                  // every gather of the call is complete
+  wait_previous_grid();                                  // the selections are complete
+  allow_next_grid();                                     // the gathers may be scheduled; they wait for this grid
 
-  if (f == 0) {
-    const uint32_t t = __ldcg(&S.counters[0]) + 1u;
-    uint32_t head = __ldcg(&S.counters[2]), tail = __ldcg(&S.counters[3]), buf = __ldcg(&S.counters[4]) & 1u;
-    const uint32_t hand = __ldcg(&S.counters[5]);
-    const uint32_t Q = S.ring_cap, qmask = Q - 1u;
-    if (tid == 0) {
-      head_hit = kNoEntry;
-      nevict = 0;
-    }
-    // The queue gets at most k entries in this call: make room first.
-    if (kLru && tail - head > Q - k) {
-      tail = compact_queue_cta(S, head, tail, buf, scratch);
-      if (tid == 0 && tail != H) atomicOr(status, kFlagInternal);
-      head = 0;
-      buf ^= 1u;
-      __syncthreads();
-    }
-    const uint64_t* ring_in = S.ring + (size_t)buf * Q;
-    uint64_t* ring_out = S.ring + (size_t)buf * Q;
-    const uint32_t span = tail - head;
-    const uint32_t limit = kLru ? span : H;
-
-    // 1. positions of this thread's entries and the first queue window,
-    //    issued together
-    for (uint32_t w = tid; w < hwords; w += kThreads) used[w] = 0;
-    int32_t pj[kFinishEntries];
-#pragma unroll
-    for (uint32_t q = 0; q < kFinishEntries; ++q) {
-      const uint32_t j = q * kThreads + tid;
-      pj[q] = j < k ? __ldcg(&T.idx[j]) : -1;
-    }
-    uint64_t e[kFinishPer];
-#pragma unroll
-    for (uint32_t q = 0; q < kFinishPer; ++q) {
-      const uint32_t o = kFinishPer * tid + q;
-      if (kLru) e[q] = o < span ? __ldcg(&ring_in[(head + o) & qmask]) : ~0ull;
-      else e[q] = o < H ? (uint64_t)(hand + o < H ? hand + o : hand + o - H) : ~0ull;
-    }
-
-    // 2. their claims and stamps: an entry is a unique miss when its claim
-    //    won, a hit when it holds a slot (the slots the gathers stamped, the
-    //    first members of this step's used slots); a queue entry is a victim
-    //    candidate while it is current and its slot was not stamped
-    int32_t claim[kFinishEntries];
-#pragma unroll
-    for (uint32_t q = 0; q < kFinishEntries; ++q)
-      claim[q] = pj[q] >= 0 && (uint32_t)pj[q] < T.len ? __ldcg(&S.pos2slot[pj[q]]) : -1;
-    __syncthreads();                                     // the used bitmap is zero
-#pragma unroll
-    for (uint32_t q = 0; q < kFinishEntries; ++q)
-      if (claim[q] >= 0 && (uint32_t)claim[q] < H) atomicOr(&used[(uint32_t)claim[q] >> 5], 1u << (claim[q] & 31));
-    uint32_t lu[kFinishPer];
-#pragma unroll
-    for (uint32_t q = 0; q < kFinishPer; ++q) {
-      const uint32_t sl = (uint32_t)e[q];
-      lu[q] = e[q] != ~0ull && sl < H ? __ldcg(&S.last_use[sl]) : t;
-    }
-    uint32_t M = 0;
-#pragma unroll
-    for (uint32_t q = 0; q < kFinishEntries; ++q) {
-      if (q * kThreads >= k) break;                      // uniform over the CTA
-      const uint32_t j = q * kThreads + tid;
-      const bool fl = j < k && pj[q] >= 0 && (uint32_t)pj[q] < T.len && claim[q] == (int32_t)j - (int32_t)k - 1;
-      uint32_t tile;
-      const uint32_t rank = block_flag_scan(fl, scratch, &tile);
-      if (fl) {
-        mlist[M + rank] = j;
-        mpos[M + rank] = pj[q];
-      }
-      M += tile;
-    }
-
-    // 3. victims: the first M current, unstamped entries of the queue from
-    //    its head, or the first M unstamped slots from the circular hand
-    uint32_t found = 0, off = 0;
-    for (bool first_round = true; found < M && off < limit; first_round = false) {   // uniform over the CTA
-      if (!first_round) {
-#pragma unroll
-        for (uint32_t q = 0; q < kFinishPer; ++q) {
-          const uint32_t o = off + kFinishPer * tid + q;
-          if (kLru) e[q] = o < span ? __ldcg(&ring_in[(head + o) & qmask]) : ~0ull;
-          else e[q] = o < H ? (uint64_t)(hand + o < H ? hand + o : hand + o - H) : ~0ull;
-        }
-#pragma unroll
-        for (uint32_t q = 0; q < kFinishPer; ++q) {
-          const uint32_t sl = (uint32_t)e[q];
-          lu[q] = e[q] != ~0ull && sl < H ? __ldcg(&S.last_use[sl]) : t;
-        }
-      }
-      uint32_t ncur = 0;
-#pragma unroll
-      for (uint32_t q = 0; q < kFinishPer; ++q) {
-        const bool cur = e[q] != ~0ull && (uint32_t)e[q] < H &&
-                         (kLru ? lu[q] == (uint32_t)(e[q] >> 32) : lu[q] != t);
-        if (cur) ++ncur;
-        else e[q] = ~0ull;
-      }
-      uint32_t tot;
-      uint32_t u = found + block_excl_sum(ncur, scratch, &tot);
-#pragma unroll
-      for (uint32_t q = 0; q < kFinishPer; ++q) {
-        if (e[q] == ~0ull) continue;
-        if (u < M) {
-          vslot[u] = (uint32_t)e[q];
-          if (u == M - 1) last_vic = (uint32_t)e[q];
-        } else if (u == M) {
-          head_hit = off + kFinishPer * tid + q;         // the first current entry that stays
-        }
-        ++u;
-      }
-      found += tot;
-      off += kFinishPer * kThreads;
-    }
+  const uint32_t t = __ldcg(&S.counters[0]) + 1u;
+  uint32_t head = __ldcg(&S.counters[2]), tail = __ldcg(&S.counters[3]), buf = __ldcg(&S.counters[4]) & 1u;
+  const uint32_t hand = __ldcg(&S.counters[5]);
+  const uint32_t Q = S.ring_cap, qmask = Q - 1u;
+  if (tid == 0) {
+    head_hit = kNoEntry;
+    nevict = 0;
+  }
+  if (tid < 4) cnt[tid] = 0;
+  // The queue gets at most k entries in this call: make room first.
+  if (kLru && tail - head > Q - k) {
+    tail = compact_queue_cta(S, head, tail, buf, scratch);
+    if (tid == 0 && tail != H) atomicOr(status, kFlagInternal);
+    head = 0;
+    buf ^= 1u;
     __syncthreads();
-    if (found < M && tid == 0) atomicOr(status, kFlagInternal);   // cannot happen: M <= unpinned slots
-    const uint32_t nvic = found < M ? found : M;
+  }
+  const uint64_t* ring_in = S.ring + (size_t)buf * Q;
+  uint64_t* ring_out = S.ring + (size_t)buf * Q;
+  const uint32_t span = tail - head;
+  const uint32_t limit = kLru ? span : H;
 
-    // 4. map updates, one thread per unique miss; the victims join the used
-    //    slots
-    for (uint32_t u = tid; u < nvic; u += kThreads) {
-      const uint32_t v = vslot[u];
-      const int32_t p = mpos[u];
-      if (v >= H || p < 0 || (uint32_t)p >= S.history_cap) {
-        atomicOr(status, kFlagInternal);                 // cannot happen; never write out of bounds
-        continue;
-      }
-      const int32_t old = __ldcg(&S.slot2pos[v]);
-      if (old >= 0) {
-        S.pos2slot[old] = -1;
-        atomicAdd(&nevict, 1u);
-      }
-      S.pos2slot[p] = (int32_t)v;
-      S.slot2pos[v] = p;
-      S.last_use[v] = t;
-      atomicOr(&used[v >> 5], 1u << (v & 31));
-      if (S.evlog) {
-        S.evlog[1 + 3 * u] = (int32_t)v;
-        S.evlog[2 + 3 * u] = old;
-        S.evlog[3 + 3 * u] = p;
-      }
-    }
-
-    // 5. the new rows, to the host history below the RAM length, else to the
-    //    recent ring
-    for (uint32_t i = warp; i < T.r; i += kWarps) {
-      uint4* dst = i >= T.to_ram ? reinterpret_cast<uint4*>(S.recent) +
-                                       (size_t)((T.fresh_from + i) & (S.ring_rows - 1u)) * kRowVec
-                                 : reinterpret_cast<uint4*>(const_cast<uint8_t*>(S.hist)) +
-                                       (size_t)(T.fresh_from + i) * kRowVec;
-      const uint4* src = reinterpret_cast<const uint4*>(T.fresh) + (size_t)i * kRowVec;
-      dst[lane] = src[lane];
-      if (lane < kRowVec - 32) dst[32 + lane] = src[32 + lane];
-    }
-    __syncthreads();                                     // the used bitmap is complete
-
-    // 6. LRU queue: every slot used in this step, in slot order, stamped t,
-    //    at the tail
-    uint32_t appended = 0;
-    if (kLru) {
-      const uint64_t stamp = (uint64_t)t << 32;
-      for (uint32_t w0 = 0; w0 < hwords; w0 += kThreads) {
-        const uint32_t w = w0 + tid;
-        uint32_t bits = w < hwords ? used[w] : 0u;
-        uint32_t tot;
-        uint32_t pos = tail + appended + block_excl_sum(__popc(bits), scratch, &tot);
-        while (bits) {
-          const uint32_t bit = __ffs(bits) - 1;
-          bits &= bits - 1;
-          ring_out[pos & qmask] = stamp | (uint64_t)(32 * w + bit);
-          ++pos;
-        }
-        appended += tot;
-      }
-    }
-
-    // 7. counters and stats
-    if (tid == 0) {
-      S.counters[0] = t;
-      S.counters[1] = T.len;
-      if (kLru) {
-        S.counters[2] = nvic > 0 ? head + (head_hit != kNoEntry ? head_hit : min(off, span)) : head;
-        S.counters[3] = tail + appended;
-        S.counters[4] = buf;
-      } else if (nvic > 0) {
-        S.counters[5] = last_vic + 1u == H ? 0u : last_vic + 1u;
-      }
-      unsigned long long* st = S.stats;
-      atomicAdd(st + 0, 1ull);
-      if (M) atomicAdd(st + 3, (unsigned long long)M);
-      if (nevict) atomicAdd(st + 4, (unsigned long long)nevict);
-      atomicAdd(st + 7, (unsigned long long)k);
-      if (S.evlog) S.evlog[0] = (int32_t)nvic;
-      nvic_s = nvic;
-      if (b.deferred) b.dcount[T.layer] = 0;             // the host has read this call's list
-    }
+  // 1. positions of this thread's entries and the first queue window,
+  //    issued together
+  for (uint32_t w = tid; w < hwords; w += kThreads) used[w] = 0;
+  int32_t pj[kFinishEntries];
+#pragma unroll
+  for (uint32_t q = 0; q < kFinishEntries; ++q) {
+    const uint32_t j = q * kThreads + tid;
+    pj[q] = j < k ? __ldcg(&T.idx[j]) : -1;
+  }
+  uint64_t e[kFinishPer];
+#pragma unroll
+  for (uint32_t q = 0; q < kFinishPer; ++q) {
+    const uint32_t o = kFinishPer * tid + q;
+    if (kLru) e[q] = o < span ? __ldcg(&ring_in[(head + o) & qmask]) : ~0ull;
+    else e[q] = o < H ? (uint64_t)(hand + o < H ? hand + o : hand + o - H) : ~0ull;
   }
 
-  // 8. fills: each victim slot receives its row, from the output the gathers
-  // wrote (or from the row's source when only bf16 rows were asked for); the
-  // CTAs of the cluster share the rows, each taking the victim list from
-  // CTA 0 over distributed shared memory first
-  if (F > 1) {
-    cluster_sync();                                      // CTA 0's lists are complete
-    if (f != 0 && tid == 0) nvic_s = dsmem_ld_u32(dsmem_addr(&nvic_s, 0));
+  // 2. the positions' slots and the window's stamps (read before this
+  //    step's hits are stamped: a window entry whose slot is hit is left out
+  //    by the used bitmap below, as the stamp would leave it out)
+  int32_t sl[kFinishEntries];
+#pragma unroll
+  for (uint32_t q = 0; q < kFinishEntries; ++q)
+    sl[q] = pj[q] >= 0 && (uint32_t)pj[q] < T.len ? __ldcg(&S.pos2slot[pj[q]]) : -1;
+  uint32_t lu[kFinishPer];
+#pragma unroll
+  for (uint32_t q = 0; q < kFinishPer; ++q) {
+    const uint32_t s = (uint32_t)e[q];
+    lu[q] = kLru && e[q] != ~0ull && s < H ? __ldcg(&S.last_use[s]) : 0u;
+  }
+  __syncthreads();                                       // the used bitmap is zero
+
+  // 3. classify: a hit stamps its slot with the step and joins the used
+  //    slots; a miss claims its position (the smallest entry wins: the
+  //    first occurrence fills the slot, later ones read the source too)
+  uint32_t nhit = 0, nmiss = 0, nram = 0, ninv = 0;
+#pragma unroll
+  for (uint32_t q = 0; q < kFinishEntries; ++q) {
+    const uint32_t j = q * kThreads + tid;
+    if (j >= k) continue;
+    const int32_t p = pj[q];
+    if (p < 0 || (uint32_t)p >= T.len) {
+      code[j] = kEntInvalid;
+      ++ninv;
+      continue;
+    }
+    int32_t s = sl[q];
+    if (s >= (int32_t)H) {
+      atomicOr(status, kFlagInternal);                   // cannot happen; keep every index in bounds
+      s = -1;
+      sl[q] = -1;
+    }
+    if (s >= 0) {
+      S.last_use[s] = t;                                 // pinned for this step
+      atomicOr(&used[(uint32_t)s >> 5], 1u << (s & 31));
+      code[j] = (uint32_t)s;
+      ++nhit;
+    } else {
+      atomicMin(&S.pos2slot[p], (int32_t)j - (int32_t)k - 1);
+      bool host;
+      (void)miss_source(S, T, (uint32_t)p, &host);
+      code[j] = kEntMiss | (host && b.deferred ? kEntLater : 0u);
+      ++nmiss;
+      // a RAM read as append-then-resolve defines it: below the RAM length
+      // (this call's own rows there are served from their device copy,
+      // which holds the same bytes)
+      nram += !(S.ring_rows && (uint32_t)p >= T.ram_len);
+    }
+  }
+  {
+    const uint32_t h = __reduce_add_sync(0xffffffffu, nhit), m = __reduce_add_sync(0xffffffffu, nmiss);
+    const uint32_t rr = __reduce_add_sync(0xffffffffu, nram), iv = __reduce_add_sync(0xffffffffu, ninv);
+    if (lane == 0) {
+      if (h) atomicAdd(&cnt[0], h);
+      if (m) atomicAdd(&cnt[1], m);
+      if (rr) atomicAdd(&cnt[2], rr);
+      if (iv) atomicAdd(&cnt[3], iv);
+    }
+  }
+  __syncthreads();                                       // the claims are in place; used holds every hit
+
+  // 4. unique misses: the entries whose claim won, in entry order
+  int32_t claim[kFinishEntries];
+#pragma unroll
+  for (uint32_t q = 0; q < kFinishEntries; ++q) {
+    const uint32_t j = q * kThreads + tid;
+    claim[q] = j < k && pj[q] >= 0 && (uint32_t)pj[q] < T.len && sl[q] < 0 ? __ldcg(&S.pos2slot[pj[q]]) : 0;
+  }
+  uint32_t M = 0;
+#pragma unroll
+  for (uint32_t q = 0; q < kFinishEntries; ++q) {
+    if (q * kThreads >= k) break;                        // uniform over the CTA
+    const uint32_t j = q * kThreads + tid;
+    const bool fl = j < k && pj[q] >= 0 && (uint32_t)pj[q] < T.len && sl[q] < 0 &&
+                    claim[q] == (int32_t)j - (int32_t)k - 1;
+    uint32_t tile;
+    const uint32_t rank = block_flag_scan(fl, scratch, &tile);
+    if (fl) {
+      mlist[M + rank] = j;
+      mpos[M + rank] = pj[q];
+    }
+    M += tile;
+  }
+
+  // 5. victims: the first M current entries of the queue from its head
+  //    whose slot this step does not use, or the first M such slots from
+  //    the circular hand
+  uint32_t found = 0, off = 0;
+  for (bool first_round = true; found < M && off < limit; first_round = false) {   // uniform over the CTA
+    if (!first_round) {
+#pragma unroll
+      for (uint32_t q = 0; q < kFinishPer; ++q) {
+        const uint32_t o = off + kFinishPer * tid + q;
+        if (kLru) e[q] = o < span ? __ldcg(&ring_in[(head + o) & qmask]) : ~0ull;
+        else e[q] = o < H ? (uint64_t)(hand + o < H ? hand + o : hand + o - H) : ~0ull;
+      }
+#pragma unroll
+      for (uint32_t q = 0; q < kFinishPer; ++q) {
+        const uint32_t s = (uint32_t)e[q];
+        lu[q] = kLru && e[q] != ~0ull && s < H ? __ldcg(&S.last_use[s]) : 0u;
+      }
+    }
+    uint32_t ncur = 0;
+#pragma unroll
+    for (uint32_t q = 0; q < kFinishPer; ++q) {
+      const uint32_t s = (uint32_t)e[q];
+      const bool cur = e[q] != ~0ull && s < H && (!kLru || lu[q] == (uint32_t)(e[q] >> 32)) &&
+                       !((used[s >> 5] >> (s & 31)) & 1u);
+      if (cur) ++ncur;
+      else e[q] = ~0ull;
+    }
+    uint32_t tot;
+    uint32_t u = found + block_excl_sum(ncur, scratch, &tot);
+#pragma unroll
+    for (uint32_t q = 0; q < kFinishPer; ++q) {
+      if (e[q] == ~0ull) continue;
+      if (u < M) {
+        vslot[u] = (uint32_t)e[q];
+        if (u == M - 1) last_vic = (uint32_t)e[q];
+      } else if (u == M) {
+        head_hit = off + kFinishPer * tid + q;           // the first current entry that stays
+      }
+      ++u;
+    }
+    found += tot;
+    off += kFinishPer * kThreads;
   }
   __syncthreads();
-  const uint32_t nvic = nvic_s;
-  const uint32_t pieces = nvic * kRowVec;
-  const uint32_t share = (pieces + F - 1) / F;
-  const uint32_t plo = min(pieces, f * share), phi = min(pieces, plo + share);
-  if (F > 1 && f != 0 && plo < phi) {
-    // only the list entries of this CTA's rows, from CTA 0
-    const uint32_t u0 = plo / kRowVec, u1 = (phi - 1) / kRowVec + 1;
-    for (uint32_t u = u0 + tid; u < u1; u += kThreads) {
-      mlist[u] = dsmem_ld_u32(dsmem_addr(&mlist[u], 0));
-      vslot[u] = dsmem_ld_u32(dsmem_addr(&vslot[u], 0));
-      mpos[u] = (int32_t)dsmem_ld_u32(dsmem_addr(&mpos[u], 0));
+  if (found < M && tid == 0) atomicOr(status, kFlagInternal);   // cannot happen: M <= unpinned slots
+  const uint32_t nvic = found < M ? found : M;
+
+  // 6. map updates, one thread per unique miss; the victims join the used
+  //    slots, and the miss's entry code names its slot
+  for (uint32_t u = tid; u < nvic; u += kThreads) {
+    const uint32_t v = vslot[u];
+    const int32_t p = mpos[u];
+    if (v >= H || p < 0 || (uint32_t)p >= S.history_cap) {
+      atomicOr(status, kFlagInternal);                   // cannot happen; never write out of bounds
+      continue;
     }
-    __syncthreads();
+    const int32_t old = __ldcg(&S.slot2pos[v]);
+    if (old >= 0) {
+      S.pos2slot[old] = -1;
+      atomicAdd(&nevict, 1u);
+    }
+    S.pos2slot[p] = (int32_t)v;
+    S.slot2pos[v] = p;
+    S.last_use[v] = t;
+    atomicOr(&used[v >> 5], 1u << (v & 31));
+    code[mlist[u]] |= kEntFill | v;
+    if (S.evlog) {
+      S.evlog[1 + 3 * u] = (int32_t)v;
+      S.evlog[2 + 3 * u] = old;
+      S.evlog[3 + 3 * u] = p;
+    }
   }
-  for (uint32_t base = plo; base < phi; base += kFillInFlight * kThreads) {
-    uint4 x[kFillInFlight];
-    uint32_t dst[kFillInFlight];                          // piece index in the hot cache, or kNoEntry
+
+  // 7. the new rows, to the host history below the RAM length, else to the
+  //    recent ring
+  const uint32_t warp = tid >> 5;
+  for (uint32_t i = warp; i < T.r; i += kWarps) {
+    uint4* dst = i >= T.to_ram ? reinterpret_cast<uint4*>(S.recent) +
+                                     (size_t)((T.fresh_from + i) & (S.ring_rows - 1u)) * kRowVec
+                               : reinterpret_cast<uint4*>(const_cast<uint8_t*>(S.hist)) +
+                                     (size_t)(T.fresh_from + i) * kRowVec;
+    const uint4* src = reinterpret_cast<const uint4*>(T.fresh) + (size_t)i * kRowVec;
+    dst[lane] = src[lane];
+    if (lane < kRowVec - 32) dst[32 + lane] = src[32 + lane];
+  }
+  __syncthreads();                                       // the used bitmap and the codes are complete
+
+  // 8. the codes for the gathers, and (batched copies) the list of the
+  //    entries whose rows the host copies, in entry order
+  for (uint32_t j = tid; j < k; j += kThreads) T.ent[j] = code[j];
+  if (b.deferred) {
+    uint32_t nl = 0;
+    for (uint32_t j0 = 0; j0 < k; j0 += kThreads) {      // uniform over the CTA
+      const uint32_t j = j0 + tid;
+      const bool fl = j < k && code[j] != kEntInvalid && (code[j] & kEntLater);
+      uint32_t tile;
+      const uint32_t rank = block_flag_scan(fl, scratch, &tile);
+      if (fl) b.dlist[(size_t)T.layer * KVO_MAX_K + nl + rank] = make_int2((int32_t)j, __ldcg(&T.idx[j]));
+      nl += tile;
+    }
+    if (tid == 0) b.dcount[T.layer] = nl;
+  }
+
+  // 9. LRU queue: every slot used in this step, in slot order, stamped t,
+  //    at the tail
+  uint32_t appended = 0;
+  if (kLru) {
+    const uint64_t stamp = (uint64_t)t << 32;
+    for (uint32_t w0 = 0; w0 < hwords; w0 += kThreads) {
+      const uint32_t w = w0 + tid;
+      uint32_t bits = w < hwords ? used[w] : 0u;
+      uint32_t tot;
+      uint32_t pos = tail + appended + block_excl_sum(__popc(bits), scratch, &tot);
+      while (bits) {
+        const uint32_t bit = __ffs(bits) - 1;
+        bits &= bits - 1;
+        ring_out[pos & qmask] = stamp | (uint64_t)(32 * w + bit);
+        ++pos;
+      }
+      appended += tot;
+    }
+  }
+
+  // 10. counters and stats
+  if (tid == 0) {
+    S.counters[0] = t;
+    S.counters[1] = T.len;
+    if (kLru) {
+      S.counters[2] = nvic > 0 ? head + (head_hit != kNoEntry ? head_hit : min(off, span)) : head;
+      S.counters[3] = tail + appended;
+      S.counters[4] = buf;
+    } else if (nvic > 0) {
+      S.counters[5] = last_vic + 1u == H ? 0u : last_vic + 1u;
+    }
+    unsigned long long* st = S.stats;
+    atomicAdd(st + 0, 1ull);
+    if (cnt[0]) atomicAdd(st + 1, (unsigned long long)cnt[0]);
+    if (cnt[1]) atomicAdd(st + 2, (unsigned long long)cnt[1]);
+    if (M) atomicAdd(st + 3, (unsigned long long)M);
+    if (nevict) atomicAdd(st + 4, (unsigned long long)nevict);
+    if (cnt[3]) {
+      atomicAdd(st + 5, (unsigned long long)cnt[3]);
+      atomicOr(status, kFlagRange);
+    }
+    if (cnt[2]) atomicAdd(st + 6, (unsigned long long)cnt[2] * KVO_ROW_BYTES);
+    atomicAdd(st + 7, (unsigned long long)k);
+    if (S.evlog) S.evlog[0] = (int32_t)nvic;
+  }
+}
+
+// ------------------------------------------------------------ C: gather
+constexpr uint32_t kGatherThreads = 256;
+constexpr uint32_t kGatherWarps = kGatherThreads / 32;
+constexpr uint32_t kGatherEntries = 64;                  // entries per CTA
+constexpr uint32_t kGatherInFlight = 4;                  // rows a warp loads before it stores
+static_assert(kGatherEntries <= kGatherThreads, "one thread per entry reads its code");
+
+// The row of entry j by its code: a hit's slot, a miss's source, or NULL
+// (a zero row).  *fill: the slot a first-occurrence miss also fills, or
+// NULL.  Codes and positions are checked again (never an access out of
+// bounds, whatever the tables hold).
+__device__ __forceinline__ const uint4* entry_source(const LayerStatic& S, const LayerCall& T, uint32_t c, int32_t p,
+                                                     uint4** fill, uint32_t* status) {
+  *fill = nullptr;
+  if (c == kEntInvalid) return nullptr;
+  const uint32_t s = c & kEntSlot;
+  if (!(c & kEntMiss)) {
+    if (s >= S.hot_rows) {
+      atomicOr(status, kFlagInternal);
+      return nullptr;
+    }
+    return reinterpret_cast<const uint4*>(S.hot) + (size_t)s * kRowVec;
+  }
+  if (p < 0 || (uint32_t)p >= T.len) {
+    atomicOr(status, kFlagInternal);
+    return nullptr;
+  }
+  if (c & kEntFill) {
+    if (s < S.hot_rows) *fill = reinterpret_cast<uint4*>(S.hot) + (size_t)s * kRowVec;
+    else atomicOr(status, kFlagInternal);
+  }
+  bool host;
+  return miss_source(S, T, (uint32_t)p, &host);
+}
+
+// Every selected entry of every layer: the row to the output (and its bf16
+// dequant), hits from the HBM slot, misses from their source and, for the
+// first occurrence of a position, into the victim slot B chose as well.  No
+// slot this launch writes is read by it: victims are slots the step does
+// not use.
+__global__ void __launch_bounds__(kGatherThreads) layers_gather_kernel(const __grid_constant__ LayerBatch b,
+                                                                       uint32_t* status) {
+  __shared__ const uint4* src[kGatherEntries];           // NULL: a zero row
+  __shared__ uint4* fill[kGatherEntries];                // the victim slot's row, or NULL
+  __shared__ uint8_t later[kGatherEntries];              // the row comes by a batched copy (placed later)
+  const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const LayerCall& T = b.t[blockIdx.x / b.chunks];
+  const LayerStatic S = b.statics[T.layer];
+  const uint32_t k = b.k;
+  const uint32_t j0 = (blockIdx.x % b.chunks) * kGatherEntries;
+  const uint32_t nj = j0 < k ? min(kGatherEntries, k - j0) : 0u;
+  wait_previous_grid();                                  // the resolves are complete
+
+  if (tid < nj) {
+    const uint32_t j = j0 + tid;
+    const uint32_t c = __ldcg(&T.ent[j]);
+    const int32_t p = __ldcg(&T.idx[j]);
+    uint4* f;
+    const uint4* s = entry_source(S, T, c, p, &f, status);
+    const bool l = c != kEntInvalid && (c & kEntLater);
+    src[tid] = l ? nullptr : s;
+    fill[tid] = l ? nullptr : f;
+    later[tid] = l;
+  }
+  __syncthreads();
+
+  // rows: each warp keeps kGatherInFlight rows in flight in registers.
+  // (Staging every piece in shared memory with 16-byte asynchronous copies,
+  // all in flight at once, was slower: 90 vs 70 us for the 78-layer stack's
+  // gathers, 106 vs 65 us at 1M.)
+  for (uint32_t e0 = warp; e0 < nj; e0 += kGatherWarps * kGatherInFlight) {
+    uint4 va[kGatherInFlight], vb[kGatherInFlight];
 #pragma unroll
-    for (uint32_t q = 0; q < kFillInFlight; ++q) {
-      const uint32_t i = base + q * kThreads + tid;
-      dst[q] = kNoEntry;
-      x[q] = make_uint4(0, 0, 0, 0);
-      if (i < phi) {
-        const uint32_t u = i / kRowVec, piece = i - u * kRowVec;
-        const uint32_t v = vslot[u];
-        if (v < H) {
-          const uint4* src;
-          if (T.out_rows) {
-            src = reinterpret_cast<const uint4*>(T.out_rows) + (size_t)mlist[u] * kRowVec;
-          } else {
-            bool host;
-            src = miss_source(S, T, (uint32_t)mpos[u], &host);
-          }
-          x[q] = __ldcg(src + piece);
-          dst[q] = v * kRowVec + piece;
-        }
+    for (uint32_t u = 0; u < kGatherInFlight; ++u) {
+      const uint32_t e = e0 + u * kGatherWarps;
+      va[u] = make_uint4(0, 0, 0, 0);
+      vb[u] = make_uint4(0, 0, 0, 0);
+      const uint4* s = e < nj ? src[e] : nullptr;
+      if (s) {
+        va[u] = s[lane];
+        if (lane < kRowVec - 32) vb[u] = s[32 + lane];
       }
     }
 #pragma unroll
-    for (uint32_t q = 0; q < kFillInFlight; ++q)
-      if (dst[q] != kNoEntry) reinterpret_cast<uint4*>(S.hot)[dst[q]] = x[q];
+    for (uint32_t u = 0; u < kGatherInFlight; ++u) {
+      const uint32_t e = e0 + u * kGatherWarps;
+      if (e >= nj) break;
+      if (later[e]) continue;
+      const uint32_t j = j0 + e;
+      if (T.out_rows) {
+        uint4* d = reinterpret_cast<uint4*>(T.out_rows) + (size_t)j * kRowVec;
+        d[lane] = va[u];
+        if (lane < kRowVec - 32) d[32 + lane] = vb[u];
+      }
+      if (uint4* f = fill[e]) {
+        f[lane] = va[u];
+        if (lane < kRowVec - 32) f[32 + lane] = vb[u];
+      }
+      if (T.out_bf16) dequant_row(va[u], vb[u], lane, reinterpret_cast<uint4*>(T.out_bf16 + (size_t)j * KVO_DEQUANT_VALUES));
+    }
   }
-  if (F > 1) cluster_sync();                             // no CTA reads CTA 0's lists any more
+  allow_next_grid();
+}
+
+// --------------------------------------------------- C2: batched placement
+// The rows the host copied into staging, to their entries of the output
+// (and their bf16 rows) and, for first occurrences, to their victim slots:
+// one warp per row, kGatherInFlight rows in flight.
+__global__ void __launch_bounds__(kGatherThreads) layers_place_kernel(const __grid_constant__ LayerBatch b,
+                                                                      uint32_t* status) {
+  const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const LayerCall& T = b.t[blockIdx.x / b.chunks];
+  const uint32_t H = b.statics[T.layer].hot_rows;
+  uint8_t* hot = b.statics[T.layer].hot;
+  wait_previous_grid();
+  const uint32_t m = b.pcount[T.layer];
+  const uint32_t e0 = (blockIdx.x % b.chunks) * kGatherEntries;
+  const int2* pl = b.plist + (size_t)T.layer * KVO_MAX_K;
+  const uint4* stage = reinterpret_cast<const uint4*>(b.staging) + (size_t)T.layer * b.k * kRowVec;
+  for (uint32_t i0 = e0 + warp; i0 < min(m, e0 + kGatherEntries); i0 += kGatherWarps * kGatherInFlight) {
+    uint4 va[kGatherInFlight], vb[kGatherInFlight];
+    int2 pe[kGatherInFlight];
+#pragma unroll
+    for (uint32_t u = 0; u < kGatherInFlight; ++u) {
+      const uint32_t i = i0 + u * kGatherWarps;
+      pe[u] = i < min(m, e0 + kGatherEntries) ? pl[i] : make_int2(-1, -1);
+      va[u] = make_uint4(0, 0, 0, 0);
+      vb[u] = make_uint4(0, 0, 0, 0);
+      if (pe[u].x >= 0 && (uint32_t)pe[u].x < b.k && (uint32_t)pe[u].y < b.k) {
+        const uint4* s = stage + (size_t)pe[u].y * kRowVec;
+        va[u] = s[lane];
+        if (lane < kRowVec - 32) vb[u] = s[32 + lane];
+      }
+    }
+#pragma unroll
+    for (uint32_t u = 0; u < kGatherInFlight; ++u) {
+      if (pe[u].x < 0 || (uint32_t)pe[u].x >= b.k || (uint32_t)pe[u].y >= b.k) continue;
+      const uint32_t j = (uint32_t)pe[u].x;
+      if (T.out_rows) {
+        uint4* d = reinterpret_cast<uint4*>(T.out_rows) + (size_t)j * kRowVec;
+        d[lane] = va[u];
+        if (lane < kRowVec - 32) d[32 + lane] = vb[u];
+      }
+      const uint32_t c = __ldcg(&T.ent[j]);
+      if (c != kEntInvalid && (c & kEntMiss) && (c & kEntFill)) {
+        if ((c & kEntSlot) < H) {
+          uint4* f = reinterpret_cast<uint4*>(hot) + (size_t)(c & kEntSlot) * kRowVec;
+          f[lane] = va[u];
+          if (lane < kRowVec - 32) f[32 + lane] = vb[u];
+        } else if (lane == 0) {
+          atomicOr(status, kFlagInternal);
+        }
+      }
+      if (T.out_bf16) dequant_row(va[u], vb[u], lane, reinterpret_cast<uint4*>(T.out_bf16 + (size_t)j * KVO_DEQUANT_VALUES));
+    }
+  }
+  allow_next_grid();
 }
 
 // ------------------------------------------------------------ launch
@@ -678,7 +715,6 @@ struct LayersConfig {
   int active[5] = {0, 0, 0, 0, 0};     // select clusters of 1, 2, 4, 8, 16 CTAs that fit at once (resident)
   int active_stream[5] = {0, 0, 0, 0, 0};
   int force_select = 0;
-  int active_finish[4] = {0, 0, 0, 0};   // finish clusters of 1, 2, 4, 8 CTAs that fit at once
 };
 LayersConfig g_layers[64];
 
@@ -715,14 +751,11 @@ cudaError_t layers_init(LayersConfig** out) {
       if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
         cudaGetLastError();
     }
-    for (const void* kern : {(const void*)layers_finish_kernel<true>, (const void*)layers_finish_kernel<false>}) {
+    for (const void* kern : {(const void*)layers_resolve_kernel<true>, (const void*)layers_resolve_kernel<false>}) {
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)finish_smem_bytes(KVO_MAX_K, KVO_MAX_HOT_ROWS));
+                               (int)resolve_smem_bytes(KVO_MAX_K, KVO_MAX_HOT_ROWS));
       if (e != cudaSuccess) return e;
     }
-    for (int i = 0; i < 4; ++i)
-      cfg.active_finish[i] = active_clusters((const void*)layers_finish_kernel<true>, 1 << i,
-                                             finish_smem_bytes(KVO_MAX_K, KVO_MAX_HOT_ROWS));
     for (int i = 0; i < 5; ++i) {
       cfg.active[i] = active_clusters(sel[0], 1 << i, kSelectMaxSmem);
       cfg.active_stream[i] = i ? active_clusters(sel[1], 1 << i, topk_detail::kTopkMaxDynSmem) : 0;
@@ -835,13 +868,13 @@ struct PartBuffers {
 };
 
 // One part of a call on one stream: the selections of its selecting layers,
-// then the gathers, then the finishes of all its layers.  which[0..n): the
+// then the resolves, then the gathers of all its layers.  which[0..n): the
 // part's tasks.  after_select: recorded once the selections are enqueued
 // (NULL: none).  ev: the phase events (NULL: none).
 cudaError_t enqueue_part(LayersConfig* cfg, const StepTask* tasks, const uint32_t* layers, const uint32_t* which,
                          uint32_t n, uint32_t k, const LayerStatic* statics, uint32_t* status, int max_cluster,
                          cudaStream_t stream, cudaEvent_t* ev, cudaEvent_t after_select, PartBuffers& pb,
-                         uint32_t* hist, const LayersDefer* defer, uint32_t* launched) {
+                         uint32_t* hist, uint32_t* ent, const LayersDefer* defer, uint32_t* launched) {
   cudaError_t e;
   pb.sel.clear();
   pb.res.clear();
@@ -888,7 +921,10 @@ cudaError_t enqueue_part(LayersConfig* cfg, const StepTask* tasks, const uint32_
   for (uint32_t first = 0; first < n; first += kBatchTasks) {
     LayerBatch& rb = pb.res.push();
     rb.ntasks = n - first < kBatchTasks ? n - first : kBatchTasks;
-    for (uint32_t i = 0; i < rb.ntasks; ++i) rb.t[i] = make_call(tasks[which[first + i]], layers[which[first + i]]);
+    for (uint32_t i = 0; i < rb.ntasks; ++i) {
+      rb.t[i] = make_call(tasks[which[first + i]], layers[which[first + i]]);
+      rb.t[i].ent = ent + (size_t)rb.t[i].layer * KVO_MAX_K;
+    }
     rb.statics = statics;
     rb.k = k;
     rb.chunks = (k + kGatherEntries - 1) / kGatherEntries;
@@ -928,22 +964,36 @@ cudaError_t enqueue_part(LayersConfig* cfg, const StepTask* tasks, const uint32_
   if (ev && (e = cudaEventRecord(ev[1], stream)) != cudaSuccess) return e;
   // (an event between two launches ends the early scheduling of the second)
   const bool pdl = !ev && !after_select;
+  const size_t rsmem = resolve_smem_bytes(k, tasks[which[0]].L.hot_rows);
   for (const LayerBatch& rb : pb.res) {
-    launch_config(nullptr, dim3(rb.ntasks * rb.chunks, 1, 1), kGatherThreads, 0, stream, 1, pdl && after, &lc, attr);
-    if ((e = cudaLaunchKernelEx(&lc, layers_gather_kernel, rb, status)) != cudaSuccess) return e;
+    launch_config(nullptr, dim3(rb.ntasks, 1, 1), kThreads, rsmem, stream, 1, pdl && after, &lc, attr);
+    e = tasks[which[0]].L.policy == KVO_POLICY_LRU
+            ? cudaLaunchKernelEx(&lc, layers_resolve_kernel<true>, rb, status)
+            : cudaLaunchKernelEx(&lc, layers_resolve_kernel<false>, rb, status);
+    if (e != cudaSuccess) return e;
     after = true;
     ++*launched;
   }
+  if (ev && (e = cudaEventRecord(ev[2], stream)) != cudaSuccess) return e;
+  uint32_t nl = 0;                                       // the batched-copy counters up to the part's highest layer
   if (defer) {
-    // The batched-copy fetch: wait for the lists, copy every run of
-    // consecutive missing positions with one cudaMemcpyAsync into staging
-    // (rows in position order), then place the rows.
-    uint32_t nl = 0;                                     // the counters up to the part's highest layer
     for (uint32_t w = 0; w < n; ++w) nl = layers[which[w]] + 1 > nl ? layers[which[w]] + 1 : nl;
     if ((e = cudaMemcpyAsync(defer->dcount_host, defer->dcount_dev, sizeof(uint32_t) * nl, cudaMemcpyDeviceToHost,
                              stream)) != cudaSuccess)
       return e;
     if ((e = cudaEventRecord(defer->listed, stream)) != cudaSuccess) return e;
+  }
+  for (const LayerBatch& rb : pb.res) {
+    launch_config(nullptr, dim3(rb.ntasks * rb.chunks, 1, 1), kGatherThreads, 0, stream, 1, pdl && !defer, &lc,
+                  attr);
+    if ((e = cudaLaunchKernelEx(&lc, layers_gather_kernel, rb, status)) != cudaSuccess) return e;
+    ++*launched;
+  }
+  if (defer) {
+    // The batched-copy fetch: wait for the lists (the gathers of the other
+    // rows run meanwhile), copy every run of consecutive missing positions
+    // with one cudaMemcpyAsync into staging (rows in position order), then
+    // place the rows.
     if ((e = cudaEventSynchronize(defer->listed)) != cudaSuccess) return e;
     static thread_local std::vector<int2> ent;
     static thread_local std::vector<int32_t> uniq;
@@ -975,28 +1025,9 @@ cudaError_t enqueue_part(LayersConfig* cfg, const StepTask* tasks, const uint32_
     }
     for (const LayerBatch& rb : pb.res) {
       launch_config(nullptr, dim3(rb.ntasks * rb.chunks, 1, 1), kGatherThreads, 0, stream, 1, false, &lc, attr);
-      if ((e = cudaLaunchKernelEx(&lc, layers_place_kernel, rb)) != cudaSuccess) return e;
+      if ((e = cudaLaunchKernelEx(&lc, layers_place_kernel, rb, status)) != cudaSuccess) return e;
       ++*launched;
     }
-  }
-  if (ev && (e = cudaEventRecord(ev[2], stream)) != cudaSuccess) return e;
-  const size_t fsmem = finish_smem_bytes(k, tasks[which[0]].L.hot_rows);
-  for (const LayerBatch& rb : pb.res) {
-    // CTAs per layer for the fills: the largest cluster whose clusters all
-    // run at once (one CTA per layer for a deep stack; 8 layers of 1M
-    // positions and ~2,000 fills each: 8-CTA clusters, 47 -> 25 us)
-    uint32_t F = 1;
-    for (int i = 3; i >= 1; --i)
-      if (cfg->active_finish[i] >= (int)rb.ntasks) {
-        F = 1u << i;
-        break;
-      }
-    launch_config(nullptr, dim3(rb.ntasks * F, 1, 1), kThreads, fsmem, stream, F, !ev, &lc, attr);
-    e = tasks[which[0]].L.policy == KVO_POLICY_LRU
-            ? cudaLaunchKernelEx(&lc, layers_finish_kernel<true>, rb, status)
-            : cudaLaunchKernelEx(&lc, layers_finish_kernel<false>, rb, status);
-    if (e != cudaSuccess) return e;
-    ++*launched;
   }
   if (ev && (e = cudaEventRecord(ev[3], stream)) != cudaSuccess) return e;
   return cudaSuccess;
@@ -1006,7 +1037,8 @@ cudaError_t enqueue_part(LayersConfig* cfg, const StepTask* tasks, const uint32_
 
 cudaError_t launch_layers(const StepTask* tasks, const uint32_t* layers, uint32_t ntasks, uint32_t k,
                           const LayerStatic* statics, uint32_t* status, int max_cluster, cudaStream_t stream,
-                          cudaEvent_t* ev, uint32_t* hist, const LayersDefer* defer, uint32_t* launched) {
+                          cudaEvent_t* ev, uint32_t* hist, uint32_t* ent, const LayersDefer* defer,
+                          uint32_t* launched) {
   LayersConfig* cfg = nullptr;
   cudaError_t e = layers_init(&cfg);
   if (e != cudaSuccess) return e;
@@ -1015,7 +1047,7 @@ cudaError_t launch_layers(const StepTask* tasks, const uint32_t* layers, uint32_
   all.resize(ntasks);
   for (uint32_t i = 0; i < ntasks; ++i) all[i] = i;
   return enqueue_part(cfg, tasks, layers, all.data(), ntasks, k, statics, status, max_cluster, stream, ev, nullptr,
-                      pb, hist, defer, launched);
+                      pb, hist, ent, defer, launched);
 }
 
 }  // namespace kvo

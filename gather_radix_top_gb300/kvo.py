@@ -502,7 +502,7 @@ class Context:
         return n.value, t.value
 
     def layers_phase_times(self):
-        """(select, gather, finish) milliseconds summed over the recorded
+        """(select, resolve, gather) milliseconds summed over the recorded
         kvo_decode_layers calls, and the number of calls."""
         ms = (ctypes.c_double * 3)()
         calls = ctypes.c_int64()

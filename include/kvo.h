@@ -324,7 +324,7 @@ kvo_status kvo_decode_layers(kvo_ctx* ctx, const kvo_layer_task* tasks, int32_t 
 /*
  * Measurement of kvo_decode_layers by its phases.  kvo_set_phase_timing(ctx,
  * 1) makes every later kvo_decode_layers call record CUDA events on its
- * stream around its three launches (selections, gathers, finishes), and run
+ * stream around its three launches (selections, resolves, gathers), and run
  * them in order on that one stream (no overlap of the call's parts, no
  * early scheduling of a launch before the previous one ends);
  * kvo_layers_phase_times waits for the recorded calls, adds up the elapsed

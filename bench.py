@@ -223,7 +223,8 @@ class GpuWorkload:
         # nmax] (layer j's are a view), so that the carry boost of a step is a
         # few whole-array ops rather than a few per layer
         nsel = len(self.sel)
-        base = np.zeros((steps, nsel, nmax), np.float32)
+        stride = (nmax + 3) // 4 * 4                   # each layer's scores start 16-byte aligned
+        base = np.zeros((steps, nsel, stride), np.float32)
         for j, l in enumerate(self.sel):
             for s in range(steps):
                 n = w.n_at(s)
@@ -237,7 +238,7 @@ class GpuWorkload:
                                     for s in range(steps)]) for l in self.sel], axis=1)
             self.draws_all = torch.from_numpy(d).to(dev)           # [steps, nsel, carry]
             self.draws = {l: self.draws_all[:, j] for j, l in enumerate(self.sel)}
-            self.row_off = (torch.arange(nsel, dtype=torch.int64, device=dev) * nmax).unsqueeze(1)
+            self.row_off = (torch.arange(nsel, dtype=torch.int64, device=dev) * stride).unsqueeze(1)
             self.boost = torch.full((w.carry,), w.carry_boost, dtype=torch.float32, device=dev)
             self.boost_all = torch.full((nsel * w.carry,), w.carry_boost, dtype=torch.float32, device=dev)
         # query rows 1.. of an MTP round: row 0 plus float32 noise, added in float64

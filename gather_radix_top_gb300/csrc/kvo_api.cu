@@ -47,6 +47,7 @@ struct kvo_ctx {
   uint32_t* first_hist = nullptr;        // device [layers][2048]: the batched step's filtering histograms (zero
                                          // between calls: each selection zeroes its own after use)
   uint32_t* ent = nullptr;               // device [layers][KVO_MAX_K]: the batched step's entry codes
+  kvo::LayersFilter filt{};              // the batched step's filter lists (one allocation, grown on demand)
   bool statics_dirty = true;             // the views changed since the last upload
   int64_t launches = 0;                  // kernels kvo_decode_layers has launched
   double host_seconds = 0.0;             // host time spent inside kvo_decode_layers
@@ -97,6 +98,7 @@ void free_ctx(kvo_ctx* c) {
   cudaFree(c->statics);
   cudaFree(c->first_hist);
   cudaFree(c->ent);
+  cudaFree(c->filt.count);
   cudaFree(c->touch_sink);
   cudaFreeHost(const_cast<int2*>(c->defer.dlist_host));
   cudaFree(c->defer.dcount_dev);
@@ -162,6 +164,25 @@ struct DeviceRanges {
     return true;
   }
 };
+
+// Room for the filter lists of `slices` slices of 4,096 scores (grown by a
+// quarter beyond the need; the old lists are freed once the device is idle).
+cudaError_t ensure_filter(kvo_ctx* c, size_t slices) {
+  kvo::LayersFilter& f = c->filt;
+  if (slices <= f.slices) return cudaSuccess;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return e;
+  cudaFree(f.count);
+  f = kvo::LayersFilter{};
+  const size_t want = slices + slices / 4;
+  void* p = nullptr;
+  if ((e = cudaMalloc(&p, want * (sizeof(uint32_t) + 2 * sizeof(uint32_t) * 4096))) != cudaSuccess) return e;
+  f.count = static_cast<uint32_t*>(p);
+  f.key = f.count + want;
+  f.pos = f.key + want * 4096;
+  f.slices = want;
+  return cudaSuccess;
+}
 
 // The batched-copy buffers, made on first use (staging grows with k).
 cudaError_t ensure_defer(kvo_ctx* c, int32_t k) {
@@ -432,8 +453,8 @@ kvo_status kvo_create(int32_t layers, int64_t history_cap, int32_t hot_rows, int
               ok(cudaMalloc(&c->stats, sizeof(unsigned long long) * 8 * layers)) &&
               ok(cudaMalloc(&c->status, sizeof(uint32_t))) &&
               ok(cudaMalloc(&c->statics, sizeof(kvo::LayerStatic) * layers)) &&
-              ok(cudaMalloc(&c->first_hist, sizeof(uint32_t) * 2048 * layers)) &&
-              ok(cudaMemset(c->first_hist, 0, sizeof(uint32_t) * 2048 * layers)) &&
+              ok(cudaMalloc(&c->first_hist, sizeof(uint32_t) * kvo::kLayersHistWords * layers)) &&
+              ok(cudaMemset(c->first_hist, 0, sizeof(uint32_t) * kvo::kLayersHistWords * layers)) &&
               ok(cudaMalloc(&c->ent, sizeof(uint32_t) * KVO_MAX_K * layers)) &&
               ok(cudaMemset(c->counters, 0, sizeof(uint32_t) * 8 * layers)) &&
               ok(cudaMemset(c->stats, 0, sizeof(unsigned long long) * 8 * layers)) &&
@@ -766,6 +787,10 @@ static kvo_status decode_layers_impl(kvo_ctx* ctx, const kvo_layer_task* tasks, 
   const bool batched = ctx->miss_mode == KVO_MISS_BATCHED ||
                        (ctx->miss_mode == KVO_MISS_AUTO && 100.0 * ctx->miss_rate >= ctx->miss_auto_pct);
   if (batched && !ok(ensure_defer(ctx, k))) return KVO_ENOMEM;
+  size_t slices = 0;                                     // the selections' filter lists
+  for (int32_t i = 0; i < ntasks; ++i)
+    if (tasks[i].scores) slices += (size_t)(tasks[i].n + 4095) / 4096;
+  if (!ok(ensure_filter(ctx, slices))) return KVO_ENOMEM;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   static thread_local std::vector<int64_t> ram;
   ram.resize(ntasks);
@@ -775,7 +800,8 @@ static kvo_status decode_layers_impl(kvo_ctx* ctx, const kvo_layer_task* tasks, 
   }
   uint32_t launched = 0;
   const cudaError_t e = kvo::launch_layers(st.data(), lay.data(), (uint32_t)ntasks, (uint32_t)k, ctx->statics,
-                                           ctx->status, ctx->max_cluster, s, ev, ctx->first_hist, ctx->ent,
+                                           ctx->status, ctx->max_cluster, s, ev, ctx->first_hist, &ctx->filt,
+                                           ctx->ent,
                                            batched ? &ctx->defer : nullptr, &launched);
   if (!ok(e)) return KVO_ECUDA;
   ctx->launches += launched;

@@ -93,14 +93,30 @@ struct LayersDefer {
   const uint8_t* const* hist_host;   // [layers]: host address of each layer's history
 };
 
+// Words per layer of the batched step's histogram buffer: 2,048 bins, then
+// the arrival count and the cut of the whole-GPU histogram launch.
+constexpr uint32_t kLayersHistWords = 2048 + 16;
+
+// The whole-GPU filter's lists (device): per slice of 4,096 scores its
+// candidates' count, and room for 4,096 keys and positions.
+struct LayersFilter {
+  uint32_t* count;              // [slices]
+  uint32_t* key;                // [slices * 4096]
+  uint32_t* pos;                // [slices * 4096]
+  size_t slices;
+};
+
 // One decode step of many layers in three launches over all of them
 // (select, resolve, gather); tasks without scores read their idx after the
 // selections.  layers[i]: task i's layer (its entry of `statics`, a device
 // array).  ev: NULL, or four events recorded before the selections, before
 // the resolves, before the gathers and after them (without events, each
 // launch may be scheduled before the previous one ends and waits for it on
-// the GPU).  hist: device [layers][2048] counts, zero between calls (the
-// filtered selections' histograms), or NULL.  ent: device
+// the GPU).  hist: device [layers][kLayersHistWords] words, zero between
+// calls (the filtered selections' histograms), or NULL.  filt: NULL, or room
+// for the filter's lists of every selecting task (ceil(n / 4096) slices
+// each; without it, or without room, a filtered selection filters inside its
+// cluster).  ent: device
 // [layers][KVO_MAX_K] words, the entry codes the resolves hand to the
 // gathers.  defer: NULL for zero-copy loads of the misses, else the
 // batched-copy fetch (the host waits for the resolves' lists, then copies
@@ -108,8 +124,8 @@ struct LayersDefer {
 // positions).  *launched grows by the number of kernels launched.
 cudaError_t launch_layers(const StepTask* tasks, const uint32_t* layers, uint32_t ntasks, uint32_t k,
                           const LayerStatic* statics, uint32_t* status, int max_cluster, cudaStream_t stream,
-                          cudaEvent_t* ev, uint32_t* hist, uint32_t* ent, const LayersDefer* defer,
-                          uint32_t* launched);
+                          cudaEvent_t* ev, uint32_t* hist, const LayersFilter* filt, uint32_t* ent,
+                          const LayersDefer* defer, uint32_t* launched);
 cudaError_t launch_decode_step(const LayerView& L, const void* new_rows, uint32_t r, uint32_t old_len,
                                const float* scores, uint32_t n, uint32_t k, int32_t* idx, uint8_t* out_rows,
                                uint16_t* out_bf16, uint32_t* status, int max_cluster, cudaStream_t stream,

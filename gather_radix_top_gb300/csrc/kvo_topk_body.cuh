@@ -30,7 +30,11 @@
 //   c. steps 2 and 3 run on those candidates only, on the key bits below
 //      the bucket's.
 // When the candidates would not fit (a crowded bucket: many equal or nearly
-// equal scores), step c streams the scores for every pass instead.
+// equal scores), step c streams the scores for every pass instead.  In the
+// batched decode step, steps a and b run on the whole GPU before the
+// selection (a histogram launch that also finds the bucket, then a filter
+// launch that lists the candidates of every 4,096-score slice in position
+// order); the cluster then reads its slices' lists instead of the scores.
 //
 // Ties at the cut go to the lowest positions because the compaction takes
 // equal keys in position order, and (b) keeps position order.
@@ -55,6 +59,20 @@ constexpr uint32_t kHistCopies = 4;                        // filtering histogra
 constexpr uint32_t kFilterMinBytes = (kHistCopies + 1) * kFirstBins * 4;   // the copies and the totals
 constexpr int kUnroll = 4;                                 // 4-key groups in flight per thread
 static_assert(kFirstBins % kThreads == 0, "whole bins per thread in the cut scan");
+
+// Scores per slice of the whole-GPU histogram and filter launches.
+constexpr uint32_t kSliceScores = 4096;
+
+// The whole-GPU filter's output for one selection: the cut (bucket, keys
+// above it, keys in it), and per slice of kSliceScores scores its count of
+// candidates and their keys and positions at slice * kSliceScores + i, in
+// position order.
+struct FilterPre {
+  const uint32_t* cut;
+  const uint32_t* count;
+  const uint32_t* key;
+  const uint32_t* pos;
+};
 
 __host__ __device__ __forceinline__ uint32_t topk_chunk(uint32_t n, uint32_t C) {
   return ((n + C - 1) / C + 3u) & ~3u;   // multiples of 4 positions: 16-byte aligned slices
@@ -284,6 +302,46 @@ __device__ __forceinline__ uint32_t filter_keys(LoadF4 loadf4, uint32_t count, u
   return base;
 }
 
+// The whole-GPU filter's candidates of this CTA's slices (CTA r of C takes
+// a contiguous run of slices, so that the cluster's order is position
+// order) into ckey / cpos; returns how many.  One block scan of the slice
+// counts per kThreads slices, then every thread copies entries, finding
+// each one's slice by binary search over the scanned counts.
+__device__ __forceinline__ uint32_t load_candidates(const FilterPre* pre, uint32_t n, uint32_t r, uint32_t C,
+                                                    uint32_t cap, uint32_t* ckey, uint32_t* cpos,
+                                                    uint32_t* scratch) {
+  __shared__ uint32_t off[kThreads];
+  const uint32_t tid = threadIdx.x;
+  const uint32_t S = (n + kSliceScores - 1) / kSliceScores;
+  const uint32_t per = (S + C - 1) / C;
+  const uint32_t s0 = min(S, r * per), s1 = min(S, s0 + per);
+  uint32_t m = 0;
+  for (uint32_t base = s0; base < s1; base += kThreads) {   // uniform over the CTA
+    const uint32_t sl = base + tid;
+    const uint32_t c = sl < s1 ? min(__ldcg(&pre->count[sl]), kSliceScores) : 0u;
+    uint32_t tot;
+    off[tid] = block_excl_sum(c, scratch, &tot);
+    __syncthreads();
+    const uint32_t nsl = min((uint32_t)kThreads, s1 - base);
+    for (uint32_t i = tid; i < tot; i += kThreads) {
+      uint32_t lo = 0, hi = nsl;                         // the last slice whose offset is at most i
+      while (hi - lo > 1) {
+        const uint32_t mid = (lo + hi) >> 1;
+        if (off[mid] <= i) lo = mid;
+        else hi = mid;
+      }
+      const size_t at = (size_t)(base + lo) * kSliceScores + (i - off[lo]);
+      if (m + i < cap) {                                 // always: the cut's count bounds the lists
+        ckey[m + i] = __ldcg(&pre->key[at]);
+        cpos[m + i] = __ldcg(&pre->pos[at]);
+      }
+    }
+    m += tot;
+    __syncthreads();                                     // off is rewritten next round
+  }
+  return min(m, cap);
+}
+
 // Selects the k largest of n scores with the whole cluster.  first_hist:
 // NULL, or (filtered route) the counts of the top kFirstBits key bits of all
 // n scores, made beforehand.  dyn_smem holds
@@ -296,7 +354,7 @@ __device__ __forceinline__ uint32_t filter_keys(LoadF4 loadf4, uint32_t count, u
 template <bool kResident, typename Emit>
 __device__ __forceinline__ void topk_body(const float* __restrict__ scores, uint32_t n, uint32_t k,
                                           uint8_t* dyn_smem, uint32_t cand_bytes, RadixSmem* rsm, Emit emit,
-                                          const uint32_t* first_hist = nullptr) {
+                                          const uint32_t* first_hist = nullptr, const FilterPre* pre = nullptr) {
   __shared__ uint32_t scratch[2][2 * kWarps + 2];
   __shared__ uint32_t table[kMaxCluster][4];
   __shared__ uint32_t cutw[4];
@@ -339,7 +397,7 @@ __device__ __forceinline__ void topk_body(const float* __restrict__ scores, uint
   const uint32_t cap = kResident ? 0u : topk_candidates(cand_bytes);
   if (kResident) {
     for (uint32_t g = tid; g < (cnt + 3) / 4; g += kThreads) reinterpret_cast<uint4*>(keys)[g] = load4(g);
-  } else if (cap) {
+  } else if (cap && !pre) {
     for (uint32_t b = tid; b < (kHistCopies + 1) * kFirstBins; b += kThreads) keys[b] = 0;   // the filtering histograms
   }
   cluster_sync();                                  // histograms zeroed everywhere, keys in place
@@ -351,6 +409,22 @@ __device__ __forceinline__ void topk_body(const float* __restrict__ scores, uint
   }
   if (!cap) {
     select_and_emit(load4, cnt, k, 32, rsm, scratch, table, emit_at);
+    return;
+  }
+  if (pre) {
+    // the bucket and the candidates were found beforehand on the whole GPU
+    const uint32_t bucket = __ldcg(&pre->cut[0]);
+    const uint32_t total = __ldcg(&pre->cut[1]) + __ldcg(&pre->cut[2]);
+    if (total <= cap) {
+      uint32_t* ckey = keys;
+      uint32_t* cpos = keys + cap;
+      const uint32_t m = load_candidates(pre, n, r, C, cap, ckey, cpos, &scratch[0][0]);
+      select_and_emit([&](uint32_t g) { return narrow4(reinterpret_cast<const uint4*>(ckey)[g], bucket); }, m, k,
+                      kNarrowBits, rsm, scratch, table, [&](uint32_t i, uint32_t out) { emit(cpos[i], out); });
+    } else {
+      select_and_emit([&](uint32_t g) { return narrow4(load4(g), bucket); }, cnt, k, kNarrowBits, rsm, scratch,
+                      table, emit_at);
+    }
     return;
   }
   if (first_hist) {

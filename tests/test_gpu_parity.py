@@ -970,6 +970,46 @@ def test_decode_layers_1m_one_wave_parity(kvo):
     _run_layers(kvo, w, w.steps)
 
 
+def _selection_kinds(n_scale):
+    k = 2048
+    crowded = W.random_scores(31, 40_000 * n_scale, "normal")
+    crowded[5_000 * n_scale:35_000 * n_scale] = np.float32(1.0)
+    return [crowded, W.random_scores(32, 33_001 * n_scale, "special"), W.random_scores(33, 20_000 * n_scale, "coarse"),
+            W.random_scores(34, 45_000 * n_scale, "recent"), W.random_scores(35, 12_289 * n_scale, "negzero"),
+            W.random_scores(36, k, "normal")]
+
+
+@pytest.mark.parametrize("n_scale", [1, 16])
+def test_decode_layers_selection_score_kinds(kvo, n_scale):
+    """One kvo_decode_layers call whose selecting layers hold different
+    history lengths and score shapes: a crowded cut bucket (equal scores on
+    three quarters of the positions: more keys in and above it than a
+    selecting CTA can list, so the selection streams the scores), specials
+    (NaN, +-0, +-inf, denormals), a coarse grid, raised recent positions,
+    all-negative scores with -0, and k = n.  The lengths differ, so the
+    histogram (and filter) launches have CTAs past some layers' scores.  At
+    16x the lengths (up to 720,000 scores) the selecting CTAs would stream
+    more than 32,768 scores each, so the whole-GPU filter lists the
+    candidates.  Every selection equals the oracle's, twice in a row."""
+    import torch
+    k = 2048
+    cases = _selection_kinds(n_scale)
+    L = len(cases)
+    ctx = kvo.Context(L, max(sc.size for sc in cases), 4096)
+    for l, sc in enumerate(cases):
+        ctx.append_rows(l, np.zeros((sc.size, O.ROW_BYTES), np.uint8))
+    idx = [torch.empty(k, dtype=torch.int32, device="cuda") for _ in range(L)]
+    out = [torch.empty((k, O.ROW_BYTES), dtype=torch.uint8, device="cuda") for _ in range(L)]
+    dev = [torch.from_numpy(sc).cuda() for sc in cases]
+    want = [O.select_topk(sc, k) for sc in cases]
+    for rep in range(2):                                # the second call finds the histograms zeroed
+        ctx.decode_layers([{"layer": l, "idx": idx[l], "out_rows": out[l], "scores": dev[l]} for l in range(L)], k)
+        for l in range(L):
+            np.testing.assert_array_equal(idx[l].cpu().numpy(), want[l], err_msg=f"layer {l}")
+    assert ctx.sync() == 0
+    ctx.close()
+
+
 def test_decode_layers_argument_errors(kvo):
     import torch
     ctx = kvo.Context(2, 1000, 64)

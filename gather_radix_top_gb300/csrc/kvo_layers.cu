@@ -404,9 +404,11 @@ __global__ void __launch_bounds__(kThreads, 1) layers_resolve_kernel(const __gri
   uint32_t* code = fsm + 3 * k;                          // [k]: entry codes
   uint32_t* used = fsm + 4 * k;                          // [ceil(H/32)]: slots used in this step
   const uint32_t hwords = (H + 31u) / 32u;
-  wait_previous_grid();                                  // the selections are complete
-  allow_next_grid();                                     // the gathers may be scheduled; they wait for this grid
-
+  // Before the selections end: the layer's counters, the queue (compacted
+  // if need be) and its first window with the window's stamps, none of
+  // which this call's earlier launches touch.  (This launch is scheduled
+  // once every CTA of the previous one runs, which is after the previous
+  // call has ended.)
   const uint32_t t = __ldcg(&S.counters[0]) + 1u;
   uint32_t head = __ldcg(&S.counters[2]), tail = __ldcg(&S.counters[3]), buf = __ldcg(&S.counters[4]) & 1u;
   const uint32_t hand = __ldcg(&S.counters[5]);
@@ -429,15 +431,10 @@ __global__ void __launch_bounds__(kThreads, 1) layers_resolve_kernel(const __gri
   const uint32_t span = tail - head;
   const uint32_t limit = kLru ? span : H;
 
-  // 1. positions of this thread's entries and the first queue window,
-  //    issued together
+  // 1. the first queue window and its slots' stamps (read before this
+  //    step's hits are stamped: a window entry whose slot is hit is left out
+  //    by the used bitmap below, as the stamp would leave it out)
   for (uint32_t w = tid; w < hwords; w += kThreads) used[w] = 0;
-  int32_t pj[kFinishEntries];
-#pragma unroll
-  for (uint32_t q = 0; q < kFinishEntries; ++q) {
-    const uint32_t j = q * kThreads + tid;
-    pj[q] = j < k ? __ldcg(&T.idx[j]) : -1;
-  }
   uint64_t e[kFinishPer];
 #pragma unroll
   for (uint32_t q = 0; q < kFinishPer; ++q) {
@@ -445,21 +442,31 @@ __global__ void __launch_bounds__(kThreads, 1) layers_resolve_kernel(const __gri
     if (kLru) e[q] = o < span ? __ldcg(&ring_in[(head + o) & qmask]) : ~0ull;
     else e[q] = o < H ? (uint64_t)(hand + o < H ? hand + o : hand + o - H) : ~0ull;
   }
-
-  // 2. the positions' slots and the window's stamps (read before this
-  //    step's hits are stamped: a window entry whose slot is hit is left out
-  //    by the used bitmap below, as the stamp would leave it out)
-  int32_t sl[kFinishEntries];
-#pragma unroll
-  for (uint32_t q = 0; q < kFinishEntries; ++q)
-    sl[q] = pj[q] >= 0 && (uint32_t)pj[q] < T.len ? __ldcg(&S.pos2slot[pj[q]]) : -1;
   uint32_t lu[kFinishPer];
 #pragma unroll
   for (uint32_t q = 0; q < kFinishPer; ++q) {
     const uint32_t s = (uint32_t)e[q];
     lu[q] = kLru && e[q] != ~0ull && s < H ? __ldcg(&S.last_use[s]) : 0u;
   }
-  __syncthreads();                                       // the used bitmap is zero
+  wait_previous_grid();                                  // the selections are complete
+  allow_next_grid();                                     // the gathers may be scheduled; they wait for this grid
+
+  // 2. positions of this thread's entries (and whether the whole selection
+  //    increases: then every position is distinct and no claims are
+  //    needed), then their slots
+  int32_t pj[kFinishEntries];
+  bool inc = true;
+#pragma unroll
+  for (uint32_t q = 0; q < kFinishEntries; ++q) {
+    const uint32_t j = q * kThreads + tid;
+    pj[q] = j < k ? __ldcg(&T.idx[j]) : -1;
+    if (j + 1 < k) inc = inc && pj[q] < __ldcg(&T.idx[j + 1]);
+  }
+  int32_t sl[kFinishEntries];
+#pragma unroll
+  for (uint32_t q = 0; q < kFinishEntries; ++q)
+    sl[q] = pj[q] >= 0 && (uint32_t)pj[q] < T.len ? __ldcg(&S.pos2slot[pj[q]]) : -1;
+  const bool increasing = __syncthreads_and(inc);       // and the used bitmap is zero
 
   // 3. classify: a hit stamps its slot with the step and joins the used
   //    slots; a miss claims its position (the smallest entry wins: the
@@ -487,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1) layers_resolve_kernel(const __gri
       code[j] = (uint32_t)s;
       ++nhit;
     } else {
-      atomicMin(&S.pos2slot[p], (int32_t)j - (int32_t)k - 1);
+      if (!increasing) atomicMin(&S.pos2slot[p], (int32_t)j - (int32_t)k - 1);
       bool host;
       (void)miss_source(S, T, (uint32_t)p, &host);
       code[j] = kEntMiss | (host && b.deferred ? kEntLater : 0u);
@@ -510,12 +517,15 @@ __global__ void __launch_bounds__(kThreads, 1) layers_resolve_kernel(const __gri
   }
   __syncthreads();                                       // the claims are in place; used holds every hit
 
-  // 4. unique misses: the entries whose claim won, in entry order
+  // 4. unique misses: the entries whose claim won (every miss of an
+  //    increasing selection), in entry order
   int32_t claim[kFinishEntries];
 #pragma unroll
   for (uint32_t q = 0; q < kFinishEntries; ++q) {
     const uint32_t j = q * kThreads + tid;
-    claim[q] = j < k && pj[q] >= 0 && (uint32_t)pj[q] < T.len && sl[q] < 0 ? __ldcg(&S.pos2slot[pj[q]]) : 0;
+    claim[q] = !increasing && j < k && pj[q] >= 0 && (uint32_t)pj[q] < T.len && sl[q] < 0
+                   ? __ldcg(&S.pos2slot[pj[q]])
+                   : (int32_t)j - (int32_t)k - 1;
   }
   uint32_t M = 0;
 #pragma unroll

@@ -970,6 +970,52 @@ def test_decode_layers_1m_one_wave_parity(kvo):
     _run_layers(kvo, w, w.steps)
 
 
+@pytest.mark.parametrize("seed,H,n,k,dup,bad", [(1, 16, 40, 16, 0.3, 2), (3, 1024, 5000, 256, 0.2, 5),
+                                               (5, 4096, 70_000, 2048, 0.4, 3), (7, 4096, 70_000, 2048, 0.0, 0)])
+def test_decode_layers_random_idx(kvo, seed, H, n, k, dup, bad):
+    """kvo_decode_layers with resolve-only tasks on three layers whose idx is
+    in any order, with duplicates (the first occurrence claims the slot,
+    later ones read the source) and out-of-range entries (zero rows,
+    counted), and one layer whose idx increases (no claims needed); bf16
+    rows on odd steps.  Rows, evictions, maps and status equal the oracle's
+    on every step."""
+    import torch
+    L = 4
+    g = np.random.default_rng(seed)
+    hist = [g.integers(0, 256, size=(n, O.ROW_BYTES), dtype=np.uint8) for _ in range(L)]
+    ctx = kvo.Context(L, n, H)
+    ctx.record_evictions(True)
+    st = []
+    for l in range(L):
+        ctx.append_rows(l, hist[l])
+        st.append(O.LayerState(n, H))
+        st[l].append(hist[l])
+    out = [torch.empty((k, O.ROW_BYTES), dtype=torch.uint8, device="cuda") for _ in range(L)]
+    outb = [torch.empty((k, O.DEQUANT_VALUES), dtype=torch.int16, device="cuda") for _ in range(L)]
+    for step in range(10):
+        span = n if step % 3 else min(n, 2 * H)
+        idx = [W.random_idx(seed * 100 + 10 * step + l, span, k, dup, bad if step % 2 else 0) for l in range(L - 1)]
+        idx.append(np.sort(np.random.default_rng(seed + step).choice(span, size=k, replace=False)).astype(np.int32))
+        dev = [torch.from_numpy(i).cuda() for i in idx]
+        tasks = [{"layer": l, "idx": dev[l], "out_rows": out[l]} for l in range(L)]
+        if step % 2:
+            for l in range(L):
+                tasks[l]["out_bf16"] = outb[l]
+        ctx.decode_layers(tasks, k)
+        invalid = False
+        for l in range(L):
+            res = O.resolve_gather(st[l], idx[l], want_bf16=bool(step % 2))
+            np.testing.assert_array_equal(out[l].cpu().numpy(), res.rows, err_msg=f"step {step} layer {l}")
+            if step % 2:
+                assert_bf16_equal(outb[l].cpu().numpy(), res.bf16)
+            assert ctx.evictions(l) == res.evictions, (step, l)
+            invalid = invalid or bool(res.invalid)
+        assert ctx.sync() == (kvo.KVO_ERANGE if invalid else 0)
+    for l in range(L):
+        compare_state(ctx, l, st[l])
+    ctx.close()
+
+
 def _selection_kinds(n_scale):
     k = 2048
     crowded = W.random_scores(31, 40_000 * n_scale, "normal")

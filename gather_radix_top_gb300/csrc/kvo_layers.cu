@@ -70,7 +70,7 @@ struct LayerCall {
   uint32_t* first_hist;         // filtered selections: the histogram of the scores' top key bits (then the
                                 //   arrival count and the cut), or NULL
   uint32_t* cand_count;         // filtered selections: per slice of the scores, its candidates' count, key
-  uint32_t* cand_key;           //   and position (the whole-GPU filter's lists), or NULL
+  uint32_t* cand_key;           //   and position (the histogram launch's lists), or NULL
   uint32_t* cand_pos;
   uint32_t* ent;                // [k] entry codes, written by B and read by C
 };
@@ -109,35 +109,42 @@ __device__ __forceinline__ void allow_next_grid() { asm volatile("griddepcontrol
 // For selections on the filtered route (histories whose keys do not fit the
 // cluster's shared memory): the histogram of the top kFirstBits key bits of
 // every score, built by the whole GPU (each CTA a slice of one layer's
-// scores) rather than by the selecting cluster alone.  The selection (or
-// the filter launch) finds the cut bucket from it; the selection's CTA 0
-// zeroes it for the next call.
+// scores) rather than by the selecting cluster alone.  The selection finds
+// its bucket from it, and its CTA 0 zeroes it for the next call.
+//
+// In the same pass each CTA lists its slice's candidates for the layer's
+// selection: every key in or above the bucket one below the bucket the
+// layer's previous selection cut in (kept in the histogram buffer), with
+// its position, in position order.  The selection uses the lists when its
+// own bucket is at or above that one (then the lists hold every key it
+// needs) and they fit its shared memory; otherwise it filters the scores
+// itself.  The lists cost one compare and a block scan per slice, and save
+// the selection its own pass over the scores.
 constexpr uint32_t kHistThreads = 256;
-constexpr uint32_t kHistPer = 4;                         // float4 groups a thread loads at once
-constexpr uint32_t kHistSlice = 4 * kHistPer * kHistThreads;   // scores per CTA (4,096)
+constexpr uint32_t kHistSlice = 16 * kHistThreads;      // scores per CTA (4,096): four float4 per thread
 constexpr uint32_t kHistCopies = 4;                      // shared histograms, one per warp mod 4
-static_assert(kHistSlice == topk_detail::kSliceScores, "the filter's slices are the histogram's");
-// Words per layer of the histogram buffer: the bins, then the cut (bucket,
-// keys above it, keys in it) that the filter launch publishes.
-constexpr uint32_t kHistCut = topk_detail::kFirstBins;
-// A selecting CTA that would stream more scores than this filters on the
-// whole GPU first (8 layers of 1M scores, 8-CTA clusters: the cluster's own
-// filtering pass took 22 us of a 32 us selection).
-constexpr uint32_t kGpuFilterMin = 32768;
+static_assert(kHistSlice == topk_detail::kSliceScores, "the lists' slices are the histogram's");
+// Word of the histogram buffer (after the bins) holding the bucket from
+// which the next call lists candidates (0: list none).
+constexpr uint32_t kHistSpec = topk_detail::kFirstBins;
 
 __global__ void __launch_bounds__(kHistThreads) layers_hist_kernel(const __grid_constant__ LayerBatch b) {
   __shared__ uint32_t h[kHistCopies][topk_detail::kFirstBins];
+  __shared__ unsigned long long wsum[kHistThreads / 32];
+  const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const LayerCall& T = b.t[blockIdx.x / b.chunks];
-  const uint32_t lo = (blockIdx.x % b.chunks) * kHistSlice;
+  const uint32_t slice = blockIdx.x % b.chunks;
+  const uint32_t lo = slice * kHistSlice;
   const uint32_t hi = min(T.n, lo + kHistSlice);
-  for (uint32_t i = threadIdx.x; i < kHistCopies * topk_detail::kFirstBins; i += kHistThreads) (&h[0][0])[i] = 0;
-  __syncthreads();
-  uint32_t* mine = h[(threadIdx.x >> 5) % kHistCopies];
+  const uint32_t spec = T.cand_count ? __ldcg(&T.first_hist[kHistSpec]) : 0u;
+  for (uint32_t i = tid; i < kHistCopies * topk_detail::kFirstBins; i += kHistThreads) (&h[0][0])[i] = 0;
+  // group q of this thread: scores lo + 4 (q kHistThreads + tid) .. + 3
+  // (coalesced), every load in flight at once
   const bool vec = (reinterpret_cast<uintptr_t>(T.scores + lo) & 15u) == 0;
-  float f[kHistPer][4];                                  // every load of the thread in flight at once
+  float f[4][4];
 #pragma unroll
-  for (uint32_t q = 0; q < kHistPer; ++q) {
-    const uint32_t i0 = lo + 4 * (q * kHistThreads + threadIdx.x);
+  for (uint32_t q = 0; q < 4; ++q) {
+    const uint32_t i0 = lo + 4 * (q * kHistThreads + tid);
     if (vec && i0 + 3 < hi) {
       const float4 v = __ldg(reinterpret_cast<const float4*>(T.scores + i0));
       f[q][0] = v.x, f[q][1] = v.y, f[q][2] = v.z, f[q][3] = v.w;
@@ -145,139 +152,71 @@ __global__ void __launch_bounds__(kHistThreads) layers_hist_kernel(const __grid_
       for (uint32_t e = 0; e < 4; ++e) f[q][e] = i0 + e < hi ? __ldg(T.scores + i0 + e) : 0.f;
     }
   }
+  __syncthreads();                                       // the shared histograms are zero
+  uint32_t* mine = h[warp % kHistCopies];
 #pragma unroll
-  for (uint32_t q = 0; q < kHistPer; ++q) {
-    const uint32_t i0 = lo + 4 * (q * kHistThreads + threadIdx.x);
+  for (uint32_t q = 0; q < 4; ++q) {
+    const uint32_t i0 = lo + 4 * (q * kHistThreads + tid);
 #pragma unroll
     for (uint32_t e = 0; e < 4; ++e)
       if (i0 + e < hi) atomicAdd(&mine[score_key(f[q][e]) >> topk_detail::kLowBits], 1u);
   }
+  if (spec && lo < hi) {                                 // uniform over the CTA
+    // the slice's candidates in position order (group row q, then thread,
+    // then element): one float compare each, as in the selection's own
+    // filtering pass, and one block scan of the four rows' counts packed
+    // in 16-bit fields (at most 1,024 per row)
+    const float t = topk_detail::key_floor_float(spec << topk_detail::kLowBits);
+    uint32_t keep[4];
+    unsigned long long c = 0;
+#pragma unroll
+    for (uint32_t q = 0; q < 4; ++q) {
+      const uint32_t i0 = lo + 4 * (q * kHistThreads + tid);
+      keep[q] = 0;
+#pragma unroll
+      for (uint32_t e = 0; e < 4; ++e) keep[q] |= (uint32_t)(i0 + e < hi && f[q][e] >= t) << e;
+      c |= (unsigned long long)__popc(keep[q]) << (16 * q);
+    }
+    unsigned long long incl = c;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const unsigned long long o = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= (uint32_t)d) incl += o;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    unsigned long long before = 0, all_c = 0;
+#pragma unroll
+    for (uint32_t w = 0; w < kHistThreads / 32; ++w) {
+      before += w < warp ? wsum[w] : 0ull;
+      all_c += wsum[w];
+    }
+    const unsigned long long mine_off = before + incl - c;   // per row: entries before this thread's
+    const size_t base = (size_t)slice * kHistSlice;
+    uint32_t row_base = 0;                               // entries of the rows before q
+#pragma unroll
+    for (uint32_t q = 0; q < 4; ++q) {
+      uint32_t o = row_base + (uint32_t)((mine_off >> (16 * q)) & 0xffffu);
+      const uint32_t i0 = lo + 4 * (q * kHistThreads + tid);
+#pragma unroll
+      for (uint32_t e = 0; e < 4; ++e)
+        if ((keep[q] >> e) & 1u) {
+          T.cand_key[base + o] = score_key(f[q][e]);
+          T.cand_pos[base + o] = i0 + e;
+          ++o;
+        }
+      row_base += (uint32_t)((all_c >> (16 * q)) & 0xffffu);
+    }
+    if (tid == 0) T.cand_count[slice] = row_base;
+  }
   __syncthreads();
-  for (uint32_t bin = threadIdx.x; bin < topk_detail::kFirstBins; bin += kHistThreads) {
+  for (uint32_t bin = tid; bin < topk_detail::kFirstBins; bin += kHistThreads) {
     uint32_t v = 0;
 #pragma unroll
     for (uint32_t c = 0; c < kHistCopies; ++c) v += h[c][bin];
     if (v) atomicAdd(&T.first_hist[bin], v);
   }
-  allow_next_grid();                                     // the next launch may be scheduled; it waits for this grid
-}
-
-// The bucket holding the want-th largest key of the complete histogram h
-// (kHistThreads threads, 8 bins each, from the top), into cut[0..2] (shared
-// memory) as in the selection's own cut scan.  Ends with a block barrier.
-__device__ __forceinline__ void hist_cut(const uint32_t* h, uint32_t want, uint32_t* cut) {
-  constexpr uint32_t kPer = topk_detail::kFirstBins / kHistThreads;
-  __shared__ uint32_t wsum[kHistThreads / 32];
-  const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  uint32_t c[kPer], sum = 0;
-  const uint4* h4 = reinterpret_cast<const uint4*>(h + topk_detail::kFirstBins - kPer * (tid + 1));
-  const uint4 x = __ldcg(h4), y = __ldcg(h4 + 1);       // bins top - 8 tid - 7 .. top - 8 tid
-  const uint32_t v[8] = {y.w, y.z, y.y, y.x, x.w, x.z, x.y, x.x};
-#pragma unroll
-  for (uint32_t e = 0; e < kPer; ++e) {
-    c[e] = v[e];
-    sum += c[e];
-  }
-  uint32_t incl = sum;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const uint32_t o = __shfl_up_sync(0xffffffffu, incl, d);
-    if (lane >= (uint32_t)d) incl += o;
-  }
-  if (lane == 31) wsum[warp] = incl;
-  __syncthreads();
-  uint32_t before = 0;
-#pragma unroll
-  for (uint32_t w = 0; w < kHistThreads / 32; ++w) before += w < warp ? wsum[w] : 0u;
-  const uint32_t excl = before + incl - sum;
-  if (excl < want && want <= excl + sum) {
-    uint32_t above = excl;
-#pragma unroll
-    for (uint32_t e = 0; e < kPer; ++e) {
-      if (above + c[e] >= want) {
-        cut[0] = topk_detail::kFirstBins - 1 - kPer * tid - e;
-        cut[1] = above;
-        cut[2] = c[e];
-        break;
-      }
-      above += c[e];
-    }
-  }
-  if (tid == kHistThreads - 1 && excl + sum < want) {   // fewer keys than want (refused by the API): all of them
-    cut[0] = 0;
-    cut[1] = 0;
-    cut[2] = excl + sum;
-  }
-  __syncthreads();
-}
-
-// ------------------------------------------------------- A1: filter
-// For selections whose CTAs would stream many scores: the candidates of
-// every slice of the scores, the keys in or above the cut's bucket (one
-// float compare against the bucket's lowest float), with their positions,
-// in position order (thread t takes the slice's scores 16t .. 16t + 15).
-// Each CTA finds the cut from the histogram while its scores are in flight;
-// the first CTA of a layer publishes it for the selection.  Nothing is
-// listed when the cut's count exceeds what a selecting CTA can hold (the
-// selection then streams the scores).
-__global__ void __launch_bounds__(kHistThreads) layers_filter_kernel(const __grid_constant__ LayerBatch b) {
-  __shared__ uint32_t wsum[kHistThreads / 32];
-  __shared__ uint32_t cut[3];
-  const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const LayerCall& T = b.t[blockIdx.x / b.chunks];
-  const uint32_t slice = blockIdx.x % b.chunks;
-  const uint32_t lo = slice * kHistSlice;
-  wait_previous_grid();                                  // the histograms are complete
   allow_next_grid();                                     // the selections may be scheduled; they wait for this grid
-  if (lo >= T.n || !T.cand_count) return;                // uniform over the CTA
-  const uint32_t hi = min(T.n, lo + kHistSlice);
-  const uint32_t i0 = lo + 16 * tid;
-  const bool vec = (reinterpret_cast<uintptr_t>(T.scores + lo) & 15u) == 0;
-  float f[16];
-#pragma unroll
-  for (uint32_t q = 0; q < 4; ++q) {
-    const uint32_t i = i0 + 4 * q;
-    if (vec && i + 3 < hi) {
-      const float4 v = __ldg(reinterpret_cast<const float4*>(T.scores + i));
-      f[4 * q] = v.x, f[4 * q + 1] = v.y, f[4 * q + 2] = v.z, f[4 * q + 3] = v.w;
-    } else {
-      for (uint32_t e = 0; e < 4; ++e) f[4 * q + e] = i + e < hi ? __ldg(T.scores + i + e) : 0.f;
-    }
-  }
-  hist_cut(T.first_hist, b.k, cut);
-  const uint32_t bucket = cut[0], total = cut[1] + cut[2];
-  if (slice == 0 && tid < 3) T.first_hist[kHistCut + tid] = cut[tid];
-  if (total > topk_detail::topk_candidates(b.cand_bytes)) return;   // uniform over the CTA
-  const float t = topk_detail::key_floor_float(bucket << topk_detail::kLowBits);
-  const bool all = bucket == 0;                          // every key, NaN included
-  uint32_t keep = 0;
-#pragma unroll
-  for (uint32_t e = 0; e < 16; ++e) keep |= (uint32_t)(i0 + e < hi && (all || f[e] >= t)) << e;
-  const uint32_t c = __popc(keep);
-  uint32_t incl = c;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const uint32_t o = __shfl_up_sync(0xffffffffu, incl, d);
-    if (lane >= (uint32_t)d) incl += o;
-  }
-  if (lane == 31) wsum[warp] = incl;
-  __syncthreads();
-  uint32_t before = 0, all_c = 0;
-#pragma unroll
-  for (uint32_t w = 0; w < kHistThreads / 32; ++w) {
-    before += w < warp ? wsum[w] : 0u;
-    all_c += wsum[w];
-  }
-  uint32_t o = before + incl - c;
-  const size_t base = (size_t)slice * kHistSlice;
-#pragma unroll
-  for (uint32_t e = 0; e < 16; ++e)
-    if ((keep >> e) & 1u) {
-      T.cand_key[base + o] = score_key(f[e]);
-      T.cand_pos[base + o] = i0 + e;
-      ++o;
-    }
-  if (tid == 0) T.cand_count[slice] = all_c;
 }
 
 // ------------------------------------------------------------ A: select
@@ -286,23 +225,27 @@ __global__ void __launch_bounds__(kThreads, 1) layers_select_kernel(const __grid
   extern __shared__ __align__(16) uint8_t dyn_smem[];
   __shared__ RadixSmem rsm;
   const LayerCall& T = b.t[blockIdx.x / cluster_size()];
-  wait_previous_grid();                                  // the histograms (and the filter's lists) are complete
+  wait_previous_grid();                                  // the histograms and the lists are complete
   allow_next_grid();                                     // the gathers may be scheduled; they wait for this grid
   int32_t* idx = T.idx;
   const int32_t* pos2slot = b.statics[T.layer].pos2slot;
-  const topk_detail::FilterPre pre{T.first_hist + kHistCut, T.cand_count, T.cand_key, T.cand_pos};
+  __shared__ uint32_t next_spec;
+  const uint32_t spec = T.first_hist && T.cand_count ? __ldcg(&T.first_hist[kHistSpec]) : 0u;
+  const topk_detail::FilterPre pre{spec, T.cand_count, T.cand_key, T.cand_pos};
   topk_detail::topk_body<kResident>(
       T.scores, T.n, b.k, dyn_smem, b.cand_bytes, &rsm,
       [&](uint32_t pos, uint32_t out) {
         idx[out] = (int32_t)pos;
         prefetch_l2(&pos2slot[pos]);                     // B looks it up next
       },
-      T.first_hist, T.cand_count ? &pre : nullptr);
-  // every CTA of the cluster and every filter CTA has read the histogram
-  // (cluster barriers came after the cluster's reads; the filter launch has
-  // ended): zero it for the next call
-  if (T.first_hist && cluster_rank() == 0)
+      T.first_hist, T.cand_count ? &pre : nullptr, &next_spec);
+  // every CTA of the cluster has read the histogram and the listing bucket
+  // (cluster barriers came after its reads): zero the histogram for the
+  // next call, and set the bucket it lists from
+  if (T.first_hist && cluster_rank() == 0) {
     for (uint32_t bin = threadIdx.x; bin < topk_detail::kFirstBins; bin += kThreads) T.first_hist[bin] = 0;
+    if (threadIdx.x == 0) T.first_hist[kHistSpec] = T.cand_count ? next_spec : 0u;
+  }
 }
 
 // ------------------------------------------------------------ B: resolve
@@ -1011,7 +954,6 @@ struct PartBuffers {
   BatchList sel, res;
   std::vector<uint32_t> sel_c;
   std::vector<uint8_t> sel_resident;
-  std::vector<uint8_t> sel_filter;      // some task of the batch has filter lists: launch the filter
 };
 
 // One part of a call on one stream: the selections of its selecting layers,
@@ -1028,7 +970,6 @@ cudaError_t enqueue_part(LayersConfig* cfg, const StepTask* tasks, const uint32_
   pb.res.clear();
   pb.sel_c.clear();
   pb.sel_resident.clear();
-  pb.sel_filter.clear();
   for (uint32_t w = 0; w < n; ++w) {
     const uint32_t i = which[w];
     if (!tasks[i].scores) continue;
@@ -1061,24 +1002,19 @@ cudaError_t enqueue_part(LayersConfig* cfg, const StepTask* tasks, const uint32_
     sb.statics = statics;
     sb.k = k;
     sb.cand_bytes = resident ? (uint32_t)topk_detail::topk_chunk(nmax, C) * 4u : topk_detail::kTopkMaxDynSmem;
-    // the filtered route takes its first histogram from the whole-GPU
-    // launch, and its candidates from the whole-GPU filter when each CTA
-    // would otherwise stream more than kGpuFilterMin scores
-    const bool gpu_filter = !resident && topk_detail::topk_chunk(nmax, C) > kGpuFilterMin;
-    bool listed = false;
+    // the filtered route takes its first histogram, and the candidate
+    // lists, from the whole-GPU histogram launch
     for (uint32_t i = 0; i < sb.ntasks; ++i) {
       LayerCall& c = sb.t[i];
       c.first_hist = !resident && hist ? hist + (size_t)c.layer * kLayersHistWords : nullptr;
       const size_t ns = (c.n + kHistSlice - 1) / kHistSlice;
-      if (c.first_hist && filt && gpu_filter && slices + ns <= filt->slices) {
+      if (c.first_hist && filt && slices + ns <= filt->slices) {
         c.cand_count = filt->count + slices;
         c.cand_key = filt->key + slices * kHistSlice;
         c.cand_pos = filt->pos + slices * kHistSlice;
         slices += ns;
-        listed = true;
       }
     }
-    pb.sel_filter.push_back(listed ? 1 : 0);
     sb.chunks = (nmax + kHistSlice - 1) / kHistSlice;
     pb.sel_c.push_back(C);
     pb.sel_resident.push_back(resident ? 1 : 0);
@@ -1114,12 +1050,6 @@ cudaError_t enqueue_part(LayersConfig* cfg, const StepTask* tasks, const uint32_
       layers_hist_kernel<<<pb.sel[i].ntasks * pb.sel[i].chunks, kHistThreads, 0, stream>>>(pb.sel[i]);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
       ++*launched;
-      if (pb.sel_filter[i]) {
-        launch_config(nullptr, dim3(pb.sel[i].ntasks * pb.sel[i].chunks, 1, 1), kHistThreads, 0, stream, 1, !ev,
-                      &lc, attr);
-        if ((e = cudaLaunchKernelEx(&lc, layers_filter_kernel, pb.sel[i])) != cudaSuccess) return e;
-        ++*launched;
-      }
       hist_before = true;
     }
     launch_config(nullptr, dim3(pb.sel_c[i] * pb.sel[i].ntasks, 1, 1), kThreads,

@@ -31,10 +31,12 @@
 //      the bucket's.
 // When the candidates would not fit (a crowded bucket: many equal or nearly
 // equal scores), step c streams the scores for every pass instead.  In the
-// batched decode step, steps a and b run on the whole GPU before the
-// selection (a histogram launch that also finds the bucket, then a filter
-// launch that lists the candidates of every 4,096-score slice in position
-// order); the cluster then reads its slices' lists instead of the scores.
+// batched decode step, step a's histogram is built on the whole GPU before
+// the selection, and the same launch lists, per 4,096-score slice in
+// position order, the keys in or above a bucket chosen from the layer's
+// previous selection; when this selection's bucket is at or above that one,
+// the cluster reads its slices' lists instead of step b's pass over the
+// scores.
 //
 // Ties at the cut go to the lowest positions because the compaction takes
 // equal keys in position order, and (b) keeps position order.
@@ -63,12 +65,12 @@ static_assert(kFirstBins % kThreads == 0, "whole bins per thread in the cut scan
 // Scores per slice of the whole-GPU histogram and filter launches.
 constexpr uint32_t kSliceScores = 4096;
 
-// The whole-GPU filter's output for one selection: the cut (bucket, keys
-// above it, keys in it), and per slice of kSliceScores scores its count of
-// candidates and their keys and positions at slice * kSliceScores + i, in
-// position order.
+// Candidate lists made before the selection (the batched step's histogram
+// launch): every key in or above bucket `spec` (0: none listed), per slice
+// of kSliceScores scores its count and the keys and positions at
+// slice * kSliceScores + i, in position order.
 struct FilterPre {
-  const uint32_t* cut;
+  uint32_t spec;
   const uint32_t* count;
   const uint32_t* key;
   const uint32_t* pos;
@@ -302,7 +304,7 @@ __device__ __forceinline__ uint32_t filter_keys(LoadF4 loadf4, uint32_t count, u
   return base;
 }
 
-// The whole-GPU filter's candidates of this CTA's slices (CTA r of C takes
+// The listed candidates of this CTA's slices (CTA r of C takes
 // a contiguous run of slices, so that the cluster's order is position
 // order) into ckey / cpos; returns how many.  One block scan of the slice
 // counts per kThreads slices, then every thread copies entries, finding
@@ -354,7 +356,8 @@ __device__ __forceinline__ uint32_t load_candidates(const FilterPre* pre, uint32
 template <bool kResident, typename Emit>
 __device__ __forceinline__ void topk_body(const float* __restrict__ scores, uint32_t n, uint32_t k,
                                           uint8_t* dyn_smem, uint32_t cand_bytes, RadixSmem* rsm, Emit emit,
-                                          const uint32_t* first_hist = nullptr, const FilterPre* pre = nullptr) {
+                                          const uint32_t* first_hist = nullptr, const FilterPre* pre = nullptr,
+                                          uint32_t* cut_out = nullptr) {
   __shared__ uint32_t scratch[2][2 * kWarps + 2];
   __shared__ uint32_t table[kMaxCluster][4];
   __shared__ uint32_t cutw[4];
@@ -411,22 +414,6 @@ __device__ __forceinline__ void topk_body(const float* __restrict__ scores, uint
     select_and_emit(load4, cnt, k, 32, rsm, scratch, table, emit_at);
     return;
   }
-  if (pre) {
-    // the bucket and the candidates were found beforehand on the whole GPU
-    const uint32_t bucket = __ldcg(&pre->cut[0]);
-    const uint32_t total = __ldcg(&pre->cut[1]) + __ldcg(&pre->cut[2]);
-    if (total <= cap) {
-      uint32_t* ckey = keys;
-      uint32_t* cpos = keys + cap;
-      const uint32_t m = load_candidates(pre, n, r, C, cap, ckey, cpos, &scratch[0][0]);
-      select_and_emit([&](uint32_t g) { return narrow4(reinterpret_cast<const uint4*>(ckey)[g], bucket); }, m, k,
-                      kNarrowBits, rsm, scratch, table, [&](uint32_t i, uint32_t out) { emit(cpos[i], out); });
-    } else {
-      select_and_emit([&](uint32_t g) { return narrow4(load4(g), bucket); }, cnt, k, kNarrowBits, rsm, scratch,
-                      table, emit_at);
-    }
-    return;
-  }
   if (first_hist) {
     // the filtering pass's histogram was built beforehand over the whole
     // history (device memory, kFirstBins counts): only the cut is found here
@@ -434,6 +421,30 @@ __device__ __forceinline__ void topk_body(const float* __restrict__ scores, uint
     for (uint32_t b = tid; b < kFirstBins; b += kThreads) tot[b] = __ldcg(&first_hist[b]);
     __syncthreads();
     find_cut<kFirstBins / kThreads>(tot, k, &scratch[0][0], cutw);
+    const uint32_t bucket = cutw[0];
+    // keys from the bucket below the cut: the next call lists from there
+    // while that leaves half the room free (a margin for the cut moving
+    // down), else from the cut's own bucket
+    const uint32_t below = bucket > 0 ? tot[bucket - 1] : 0u;
+    uint32_t mine = 0;
+    if (pre && pre->spec)
+      for (uint32_t b = tid; b < kFirstBins; b += kThreads) mine += b >= pre->spec ? tot[b] : 0u;
+    uint32_t listed;
+    block_excl_sum(mine, &scratch[1][0], &listed);       // after it no thread reads tot
+    if (cut_out && tid == 0)
+      *cut_out = bucket > 1 && cutw[1] + cutw[2] + below <= cap / 2 ? bucket - 1 : bucket;
+    if (pre && pre->spec) {
+      // the lists hold every key in or above bucket spec: enough when the
+      // cut is at or above it, and usable when they fit
+      if (bucket >= pre->spec && listed <= cap) {        // uniform over the cluster
+        uint32_t* ckey = keys;
+        uint32_t* cpos = keys + cap;
+        const uint32_t m = load_candidates(pre, n, r, C, cap, ckey, cpos, &scratch[0][0]);
+        select_and_emit([&](uint32_t g) { return narrow4(reinterpret_cast<const uint4*>(ckey)[g], bucket); }, m,
+                        k, kNarrowBits, rsm, scratch, table, [&](uint32_t i, uint32_t out) { emit(cpos[i], out); });
+        return;
+      }
+    }
   } else {
     first_digit_cut(load4, cnt, k, keys, keys + kHistCopies * kFirstBins, &scratch[0][0], cutw);
   }

@@ -1033,10 +1033,11 @@ def test_decode_layers_selection_score_kinds(kvo, n_scale):
     selecting CTA can list, so the selection streams the scores), specials
     (NaN, +-0, +-inf, denormals), a coarse grid, raised recent positions,
     all-negative scores with -0, and k = n.  The lengths differ, so the
-    histogram (and filter) launches have CTAs past some layers' scores.  At
-    16x the lengths (up to 720,000 scores) the selecting CTAs would stream
-    more than 32,768 scores each, so the whole-GPU filter lists the
-    candidates.  Every selection equals the oracle's, twice in a row."""
+    histogram launch has CTAs past some layers' scores; 16x the lengths
+    reach 720,000 scores.  Four calls in a row take every way through the
+    candidate lists the histogram launch makes from the previous call's cut
+    (none yet; used; a cut below them; a cut far above them).  Every
+    selection equals the oracle's."""
     import torch
     k = 2048
     cases = _selection_kinds(n_scale)
@@ -1047,11 +1048,18 @@ def test_decode_layers_selection_score_kinds(kvo, n_scale):
     idx = [torch.empty(k, dtype=torch.int32, device="cuda") for _ in range(L)]
     out = [torch.empty((k, O.ROW_BYTES), dtype=torch.uint8, device="cuda") for _ in range(L)]
     dev = [torch.from_numpy(sc).cuda() for sc in cases]
+    lower = [(sc - np.float32(4.0)).astype(np.float32) for sc in cases]
+    dev_lower = [torch.from_numpy(sc).cuda() for sc in lower]
     want = [O.select_topk(sc, k) for sc in cases]
-    for rep in range(2):                                # the second call finds the histograms zeroed
-        ctx.decode_layers([{"layer": l, "idx": idx[l], "out_rows": out[l], "scores": dev[l]} for l in range(L)], k)
+    want_lower = [O.select_topk(sc, k) for sc in lower]
+    # the second call lists candidates from one bucket below the first's cut
+    # and uses them; the third (every score 4 lower) cuts below the listing
+    # bucket and filters the scores itself; the fourth lists from far below
+    # its cut (more candidates than fit, or many extra ones)
+    for rep, (d, wnt) in enumerate([(dev, want), (dev, want), (dev_lower, want_lower), (dev, want)]):
+        ctx.decode_layers([{"layer": l, "idx": idx[l], "out_rows": out[l], "scores": d[l]} for l in range(L)], k)
         for l in range(L):
-            np.testing.assert_array_equal(idx[l].cpu().numpy(), want[l], err_msg=f"layer {l}")
+            np.testing.assert_array_equal(idx[l].cpu().numpy(), wnt[l], err_msg=f"call {rep} layer {l}")
     assert ctx.sync() == 0
     ctx.close()
 

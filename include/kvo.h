@@ -175,11 +175,12 @@ kvo_status kvo_set_gather_mode(kvo_ctx* ctx, int32_t mode, int32_t auto_miss_pct
  * registered host memory directly).
  *   KVO_MISS_ZEROCOPY  the gathers read the rows over the host link with
  *                      16-byte loads, in the same launch (default);
- *   KVO_MISS_BATCHED   the gathers list the missing positions; the call waits
- *                      for the list on the host, copies every run of
+ *   KVO_MISS_BATCHED   the resolves list the missing positions; the call
+ *                      waits for the list on the host, copies every run of
  *                      consecutive positions with one cudaMemcpyAsync into
  *                      device staging, and a placement launch writes the rows
- *                      out (the call returns only after the gathers ran);
+ *                      out and fills their victim slots (the call returns
+ *                      only after the resolves ran);
  *   KVO_MISS_AUTO      batched while the last measured miss share of the
  *                      calls is at least auto_miss_pct percent, else
  *                      zero-copy (the share comes from statistics copied back
@@ -290,9 +291,11 @@ kvo_status kvo_resolve_gather_multi(kvo_ctx* ctx, int32_t layer, const int32_t* 
  * resolves a selection it is given ([KVO] "Separate historical capacity from
  * the current working set": later layers reuse a layer's selection and keep
  * their own KV).  Three launches, each over every task of the call: the
- * top-K of the tasks with scores; then the lookup and the row gather of
- * every task on the whole GPU; then, one CTA per task, the victims, the map
- * updates, the fills, the appends and the LRU queue.  Per task:
+ * top-K of the tasks with scores (after a whole-GPU histogram launch for
+ * histories too long for one cluster's shared memory); then, one CTA per
+ * task, the lookup, the victims, the map updates, the appends and the LRU
+ * queue; then the row gather of every task on the whole GPU, which also
+ * fills the victim slots.  Per task:
  *   layer     a layer of the context; at most one task per layer per call.
  *   new_rows  device rows to append first (16-byte aligned), r of them, or
  *             NULL with r = 0.

@@ -1016,6 +1016,51 @@ def test_decode_layers_random_idx(kvo, seed, H, n, k, dup, bad):
     ctx.close()
 
 
+def test_decode_layers_more_tasks_than_one_launch_holds(kvo):
+    """140 layers in one kvo_decode_layers call: more than the 128 tasks one
+    launch takes, so every phase runs as two launches (130 selecting layers:
+    two histogram and two selection launches; 140 tasks: two resolve and two
+    gather launches).  The last 10 layers reuse the selections of layers
+    0-9, made in the other launch.  Selections, rows, evictions and maps
+    equal the oracle's over three steps."""
+    import torch
+    L, n, H, k = 140, 3000, 256, 64
+    ctx = kvo.Context(L, n + 8, H)
+    ctx.record_evictions(True)
+    g = np.random.default_rng(140)
+    st = []
+    for l in range(L):
+        hist = g.integers(0, 256, size=(n, O.ROW_BYTES), dtype=np.uint8)
+        ctx.append_rows(l, hist)
+        st.append(O.LayerState(n + 8, H))
+        st[-1].append(hist)
+    sel = list(range(130))                              # layers 130..139 reuse layers 0..9
+    src = {l: l if l < 130 else l - 130 for l in range(L)}
+    idx = {l: torch.empty(k, dtype=torch.int32, device="cuda") for l in sel}
+    out = [torch.empty((k, O.ROW_BYTES), dtype=torch.uint8, device="cuda") for _ in range(L)]
+    for step in range(3):
+        scores = {l: g.standard_normal(n, dtype=np.float32) for l in sel}
+        dev = {l: torch.from_numpy(scores[l]).cuda() for l in sel}
+        tasks = []
+        for l in range(L):
+            t = {"layer": l, "idx": idx[src[l]], "out_rows": out[l]}
+            if l in idx:
+                t["scores"] = dev[l]
+            tasks.append(t)
+        ctx.decode_layers(tasks, k)
+        want = {l: O.select_topk(scores[l], k) for l in sel}
+        for l in sel:
+            np.testing.assert_array_equal(idx[l].cpu().numpy(), want[l], err_msg=f"step {step} layer {l}")
+        for l in range(L):
+            res = O.resolve_gather(st[l], want[src[l]])
+            np.testing.assert_array_equal(out[l].cpu().numpy(), res.rows, err_msg=f"step {step} layer {l}")
+            assert ctx.evictions(l) == res.evictions, (step, l)
+    assert ctx.sync() == 0
+    for l in range(L):
+        compare_state(ctx, l, st[l])
+    ctx.close()
+
+
 def _selection_kinds(n_scale):
     k = 2048
     crowded = W.random_scores(31, 40_000 * n_scale, "normal")

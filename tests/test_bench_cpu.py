@@ -1,5 +1,6 @@
 """bench.py's contract on the CPU: the reference arm's JSON line, the silent
-non-zero ranks, and the host-side carry boost the e2e runs use."""
+non-zero ranks, the host-side carry boost the e2e runs use, and the batched
+step's byte models behind the roofline."""
 import json
 import os
 import pathlib
@@ -99,3 +100,21 @@ def test_max_over_ranks_two_gloo_ranks():
         p.join(timeout=60)
         assert p.exitcode == 0
     assert got == {0: 13.5, 1: 13.5}
+
+
+def test_batched_step_byte_models():
+    """The roofline's algorithmic bytes for the batched step, counted by hand
+    for one layer of the stack: the gather reads codes and positions (8 B
+    per entry) and the hit rows, and writes every output row and every fill;
+    the resolve touches the tables named in its docstring."""
+    sys.path.insert(0, str(ROOT))
+    import bench
+    w = W.STACK
+    ab = {"hits": 1800.0, "misses": 248.0, "fills": 248.0}
+    k = 2048
+    assert bench.gather_bytes(w, ab) == 8 * k + 656 * 1800 + 656 * k + 656 * 248
+    window = min(4096, 8 * w.hot_rows)
+    want = 12 * k + 4 * 1800 + 8 * 248 + 12 * window + 16 * 248 + 8 * (1800 + 248) + 656 * 1
+    assert bench.resolve_bytes(w, ab) == want
+    wb = W.M1                                           # bf16 rows too: 2 x 576 B more per entry
+    assert bench.gather_bytes(wb, ab) == 8 * k + 656 * 1800 + (656 + 1152) * k + 656 * 248

@@ -308,6 +308,10 @@ kvo_status kvo_resolve_gather_multi(kvo_ctx* ctx, int32_t layer, const int32_t* 
  * without scores may name the idx of a task of the same call that has
  * scores, and then resolves that task's new selection (one call per decode
  * step for a whole stack).  Two tasks with scores must not share an idx.
+ * Memory: the context keeps the candidate lists of the selections, about 8
+ * bytes per score of the call's tasks with scores, in device memory; a call
+ * that needs more than it holds grows them (a device-wide synchronisation,
+ * once), and KVO_ENOMEM if that allocation fails.
  * KVO_EINVAL on a bad task (nothing enqueued), misaligned scores or idx
  * (4 bytes) included.
  */
